@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark: paged GQA decode attention on the 24-layer, 14 q / 2 KV head model shape.
+
+One step = one decode token for 32 sequences at context 2048 through all 24
+layers: per layer kv_append (the new token's K/V into the paged cache) and
+paged_decode_attention (split-context decode + combine).  Inputs are seeded
+synthetic data (N(0,1) fp16) resident in HBM; the K/V pools (768 MiB per
+step) are larger than L2, so every step streams its cache from HBM.
+
+value       KV-cache bytes read per step / device time per step (GB/s), all ranks
+e2e         the same metric through the C ABI with host buffers: per step the
+            host->device copy of q, k_new, v_new, slots, block table and
+            context lengths and the device->host copy of the outputs are timed
+roofline    the decode call (decode kernel + split combine) alone: algorithmic
+            bytes per launch / CUDA-event launch time, against MEASURED_PEAKS
+cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
+
+--impl reference times the fp64 CPU oracle on the same workload instead.
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling), no
+collective on the data path; the timing barrier and max-over-ranks use
+torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attention: KV-cache GB/s (% HBM peak) and decode tokens/s"
+WORKLOAD = ("decode step of a 24-layer model: 32 sequences x context 2048 (incl. the new token), 14 q / 2 KV "
+            "heads, head_dim 64, fp16, block size 16, block tables permuted over a pool of 32 x 2048 tokens; "
+            "per layer kv_append + paged_decode_attention")
+L, B, CTX, HQ, HKV, D = 24, 32, 2048, 14, 2, 64
+
+
+def kv_bytes_per_step(ctx_total: int, layers: int) -> int:
+    """Algorithmic KV-cache bytes read per step: every context token's K and V rows, every layer."""
+    return ctx_total * HKV * D * 2 * 2 * layers
+
+
+def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
+    """Algorithmic bytes of one paged_decode_attention call (one layer): K/V rows, q, out (fp16), table."""
+    return kv_bytes_per_step(ctx_total, 1) + B * HQ * D * 2 * 2 + nblocks_total * 4 + B * 4
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.uuid = gpu_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        return self.summary()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        pw = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_median": float(np.median(pw)) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier_max(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle as it stands
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, seqs: int, layers, nthreads=None):
+    """Time the oracle's decode on `seqs` sequences of the given layers; returns (seconds, kv bytes)."""
+    import oracle
+    from oracle import paging
+    sub_table = wl.block_table[:seqs]
+    sub_ctx = wl.ctx[:seqs]
+    secs, nbytes = 0.0, 0
+    for layer in layers:
+        kc, vc = paging.fill_layer(wl, layer)
+        oracle.append(kc, vc, wl.k_new[layer], wl.v_new[layer], paging.step_slots(wl.block_table, wl.ctx, wl.bs))
+        t0 = time.perf_counter()
+        oracle.decode(wl.q[layer][:seqs], kc, vc, sub_table, sub_ctx, wl.scale, nthreads=nthreads)
+        secs += time.perf_counter() - t0
+        nbytes += int(sub_ctx.astype(np.int64).sum()) * HKV * D * 2 * 2
+    return secs, nbytes
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+    wl = workloads.config2(L=1)
+    seqs = 8
+    cores = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle_sample(wl, seqs, [0])
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        s, n = oracle_sample(wl, seqs, [0])
+        secs += s
+        nbytes += n
+    gbs = nbytes / secs / 1e9
+    sample = f"{seqs} of the 32 sequences of one layer per step (context 2048, 14 q / 2 KV heads)"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    import paged_kv_cache_27_gb300 as kvc
+    from paged_kv_cache_27_gb300.harness import DecodeSession, _dev
+    import workloads
+
+    wl = workloads.config2()
+    sess = DecodeSession(wl, device=device, out_dtype=torch.float16, blocks_per_split=args.blocks_per_split).fill()
+    ctx_total = int(wl.ctx.astype(np.int64).sum())
+    nblocks_total = int(sum(-(-int(c) // 16) for c in wl.ctx))
+    step_bytes = kv_bytes_per_step(ctx_total, L)
+    combine = 1 if sess.nsplit > 1 else 0
+    launches_per_step = L * (2 + combine)
+
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        sess.step()  # eager warm-up: one-time attribute setup, plan caching
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sess.step()
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph, stream=stream):
+        for layer in range(L):
+            sess.decode(layer)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+
+    if args.profile_only:
+        # a short fixed run for the ncu launch list
+        for _ in range(args.warmup + args.steps):
+            graph.replay()
+        torch.cuda.synchronize()
+        return 0
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid).start()
+    cur = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(cur)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    # keep the same load running briefly if the timed region was too short for clock samples
+    soak_until = time.time() + max(0.0, 1.5 - ms_step * args.steps / 1e3)
+    while time.time() < soak_until:
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms_step = barrier_max(ms_step, world, device)
+
+    # the decode call alone (roofline): all 24 layers back to back, so every launch streams from HBM
+    reps = max(5, min(200, args.steps))
+    for _ in range(3):
+        dgraph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(cur)
+    for _ in range(reps):
+        dgraph.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    us_decode = e0.elapsed_time(e1) * 1e3 / (reps * L)
+
+    # end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_q, h_kn, h_vn = pin(wl.q), pin(wl.k_new), pin(wl.v_new)
+    h_slots, h_table, h_ctx = pin(sess.step_slots_host), pin(wl.block_table), pin(wl.ctx)
+    h_out = torch.empty(sess.out.shape, dtype=torch.float16).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(sess.q), torch.empty_like(sess.k_new), torch.empty_like(sess.v_new)
+    d_slots, d_table, d_ctx = (torch.empty_like(x) for x in (sess.step_slots, sess.block_table, sess.context_lens))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_table, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d_, h_ in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots), (d_table, h_table),
+                       (d_ctx, h_ctx)):
+            d_.copy_(h_, non_blocking=True)
+        for layer in range(L):
+            kvc.kv_append(sess.h, layer, d_kn[layer], d_vn[layer], d_slots)
+            kvc.paged_decode_attention(d_q[layer], sess.k_pool[layer], sess.v_pool[layer], d_table, d_ctx,
+                                       wl.scale, sess.out[layer], sess.workspace, sess.max_ctx,
+                                       args.blocks_per_split)
+        h_out.copy_(sess.out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    ms_e2e = (time.perf_counter() - w0) * 1e3 / e2e_steps
+    ms_e2e = barrier_max(ms_e2e, world, device)
+
+    # CPU baseline (rank 0, N = 1 only): the oracle on a bounded sample of the same workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        secs, nbytes, layers = 0.0, 0, 0
+        while layers < L and secs < 10.0:
+            s, n = oracle_sample(wl, B, [layers])
+            secs += s
+            nbytes += n
+            layers += 1
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.default_threads(), "kind": "oracle",
+               "sample": f"{layers} of 24 layers, all 32 sequences, decode only (fp64, {secs:.1f} s)"}
+
+    peak, peak_kind = load_peaks()
+    gbs = step_bytes * world / (ms_step * 1e-3) / 1e9
+    call_bytes = decode_call_bytes(ctx_total, nblocks_total)
+    achieved = call_bytes / (us_decode * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": L, "batch_per_gpu": B, "context": CTX, "q_heads": HQ,
+                   "kv_heads": HKV, "head_dim": D, "block_size": 16, "num_splits": sess.nsplit,
+                   "blocks_per_split": sess.bps, "l2": "inputs larger than L2: 768 MiB of K/V per step",
+                   "launch": "CUDA graph of the 24-layer step"},
+        "tokens_per_s": B * world / (ms_step * 1e-3),
+        "pct_hbm_peak": gbs / world / peak * 100.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "paged_decode_attention call (decode kernel + split combine), one layer",
+                     "bytes_per_launch": call_bytes, "us_per_launch": us_decode},
+        "cpu_baseline": cpu,
+        "e2e": {"value": step_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--blocks-per-split", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

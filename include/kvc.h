@@ -1,0 +1,217 @@
+/*
+ * kvc.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library.
+ *
+ * What the library computes (sources are web pages, cited by title and section):
+ *  - "La caché de claves y valores: cuánto cuesta cada token" (gustavoai.dev),
+ *    section "Las claves y los valores de una posición no cambian": a decode
+ *    token appends its k_t, v_t to the end of each head's cache and its query
+ *    row then attends, unmasked, over every cached row including its own:
+ *        o_t = softmax(q_t K^T * scale) V.
+ *  - "Tornar a inferência barata: KV cache, batching e quantização"
+ *    (neuralialabs.com), PagedAttention paragraph: the cache is stored in
+ *    fixed-size blocks with one block table per sequence, logically
+ *    contiguous and physically scattered; sequences with a common prefix can
+ *    share the blocks that hold it.  Grouped-query attention paragraph: each
+ *    KV head is shared by a group of query heads.
+ *  - "Aufmerksamkeit" feed (chatgpz.de), PagedAttention article, SECTION 2
+ *    (PagePool, PagedRequest: FIFO free list, refcounts, a page claimed at each
+ *    page boundary) and SECTION 3 (copy-on-write prefix sharing); xformers
+ *    article parts 4-5 (packed varlen batches with block-diagonal (causal)
+ *    masks; BMGHK grouped-query layout); FlashAttention article, "Was ist der
+ *    mathematische Aspekt von Softmax?" (per-block max and exp-sum, rescaled
+ *    by e^(m_block - m_global) when merged).
+ *
+ * Conventions
+ *  - Every function returns kvc_status; nothing throws across the ABI.  On
+ *    failure kvc_last_error_string() (thread-local) holds a message.
+ *  - Device buffers are allocated by the caller and passed as raw device
+ *    pointers; the library never allocates device memory.  The library owns
+ *    only the host metadata behind a kvc_handle (free list, refcounts).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Device work is asynchronous on it; argument errors are
+ *    returned synchronously before anything is launched.
+ *  - Element type: fp16 (IEEE binary16) for q, k, v and the caches; outputs
+ *    fp16 or fp32 (kvc_dtype).  Arithmetic accumulates in fp32.
+ *  - Cache layout (this library's choice; results do not depend on it): all
+ *    layers in one allocation per K and V, element
+ *        pool[layer][block][kv_head][offset][dim]
+ *    i.e. [L][NB][Hkv][bs][D], so one (block, KV head) tile of bs*D fp16 is
+ *    contiguous.  slot = block * bs + offset.
+ *  - Query head h reads KV head h / (Hq / Hkv) (contiguous groups).
+ *  - Kernels never spin without bound and never trap: device-side problems
+ *    (an out-of-range id, a bad context length, an expired wait) set bits in a
+ *    sticky device error word (kvc_device_error_flags) and the affected rows
+ *    are skipped or zero-filled.  Checked mode validates device-side index
+ *    arrays on the host first and returns the error synchronously.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_INVALID = 1,     /* bad argument, or a block that is not live */
+    KVC_ERR_OOM = 2,         /* the block pool has no free block ("OOM -- no free pages") */
+    KVC_ERR_CAPACITY = 3,    /* a position/context beyond the block table or the pool */
+    KVC_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+    KVC_ERR_UNSUPPORTED = 5  /* a shape this build does not compile (head_dim, block_size, group) */
+} kvc_status;
+
+typedef enum { KVC_F16 = 0, KVC_F32 = 1 } kvc_dtype;
+
+/* device error word bits (kvc_device_error_flags) */
+#define KVC_DEVERR_BLOCK_ID 0x1u   /* a block-table entry outside [0, num_blocks) */
+#define KVC_DEVERR_CONTEXT 0x2u    /* a context length < 1 or beyond the table / max_context_len */
+#define KVC_DEVERR_SLOT 0x4u       /* an append slot >= num_blocks * block_size */
+#define KVC_DEVERR_TIMEOUT 0x8u    /* a bounded wait on a copy expired (the work was skipped) */
+#define KVC_DEVERR_SEQLENS 0x10u   /* cu_seqlens not non-decreasing / beyond total_tokens */
+
+typedef struct {
+    int num_layers;   /* L */
+    int num_blocks;   /* NB, physical blocks per layer */
+    int block_size;   /* bs, tokens per block (16) */
+    int num_kv_heads; /* Hkv */
+    int head_dim;     /* D (64 or 128) */
+    int dtype;        /* kvc_dtype of the cache: KVC_F16 */
+} kvc_config;
+
+typedef struct kvc_cache* kvc_handle;
+
+/* ---- diagnostics ---------------------------------------------------- */
+const char* kvc_last_error_string(void);
+int kvc_version(void);
+/* Checked mode (process-wide, default off): device index arrays passed to
+ * kv_append / paged_decode_attention / prefill_attention are copied to the
+ * host (synchronising `stream`) and validated before launch. */
+kvc_status kvc_set_checked_mode(int on);
+/* Read (and optionally clear) the sticky device error word of the current
+ * device.  Synchronous. */
+kvc_status kvc_device_error_flags(uint32_t* flags, int clear);
+
+/* ---- cache geometry and the block pool (host) ------------------------
+ * Bytes of ONE pool (K or V) for all layers: L*NB*Hkv*bs*D*2.  The K+V total
+ * per token is 2*L*Hkv*D*2 bytes (the neuralialabs page's formula). */
+kvc_status kv_cache_pool_bytes(const kvc_config* cfg, size_t* bytes);
+
+/* Create a cache over caller-allocated pools (each kv_cache_pool_bytes
+ * bytes, 16-byte aligned).  k_pool/v_pool may both be NULL: a host-only
+ * cache whose block pool works but whose device operations return
+ * KVC_ERR_INVALID.  The free list starts as 0, 1, ..., NB-1. */
+kvc_status kv_cache_create(const kvc_config* cfg, void* k_pool, void* v_pool, kvc_handle* out);
+kvc_status kv_cache_destroy(kvc_handle h);
+/* Device pointers to one layer's K and V slices ([NB][Hkv][bs][D]). */
+kvc_status kv_cache_layer(kvc_handle h, int layer, void** k_layer, void** v_layer);
+
+/* PagePool semantics (chatgpz.de PagedAttention article, SECTION 2-3):
+ * alloc pops the head of the FIFO free list (refcount 1; empty -> KVC_ERR_OOM);
+ * share increments a live block's refcount; release decrements it and at zero
+ * appends the block to the tail of the free list.  Sharing or releasing a
+ * block that is not live is KVC_ERR_INVALID. */
+kvc_status kv_block_alloc(kvc_handle h, int32_t* block);
+kvc_status kv_block_share(kvc_handle h, int32_t block);
+kvc_status kv_block_release(kvc_handle h, int32_t block);
+kvc_status kv_block_refcount(kvc_handle h, int32_t block, int32_t* refcount);
+kvc_status kv_block_num_free(kvc_handle h, int32_t* num_free);
+/* (NB - free) / NB * 100 */
+kvc_status kv_cache_utilisation(kvc_handle h, double* percent);
+
+/* Copy-on-write of one block: if its refcount is > 1, allocate a new block,
+ * queue a device copy of the whole block (all layers, K and V) on `stream`,
+ * release the old reference and return the new id; otherwise *new_block =
+ * block and nothing is copied. */
+kvc_status kv_block_cow(kvc_handle h, int32_t block, int32_t* new_block, void* stream);
+/* Device copy of whole blocks src[i] -> dst[i] (host arrays of n ids), all
+ * layers, K and V, on `stream`.  Bit copy. */
+kvc_status kv_copy_blocks(kvc_handle h, const int32_t* src, const int32_t* dst, int n, void* stream);
+
+/* ---- slot arithmetic (host) -----------------------------------------
+ * Slots of positions first_pos[b] .. first_pos[b]+count[b]-1 of every
+ * sequence b, packed in order into slots (host, sum(count) entries):
+ *     slot = block_table[b][pos / bs] * bs + pos % bs.
+ * block_table is a host [B][max_blocks] array.  A position past the table
+ * or on a negative entry is KVC_ERR_CAPACITY. */
+kvc_status kv_slot_mapping(const int32_t* block_table, int max_blocks, int B, const int32_t* first_pos,
+                           const int32_t* count, int block_size, int64_t* slots);
+
+/* One decode step's block management for B sequences (host; the
+ * PagedRequest rule plus copy-on-write): for each sequence b in order, the
+ * new token goes to position positions[b]; if that position starts a new
+ * block (positions[b] == num_blocks[b] * bs) a block is allocated and
+ * appended to the table; otherwise, if its block has refcount > 1, a new
+ * block is allocated, the pair (old, new) is recorded in copy_src/copy_dst
+ * (capacity B), the old reference is released and the table entry replaced.
+ * slot_mapping[b] receives the token's slot.  The caller then runs
+ * kv_copy_blocks(copy_src, copy_dst, *n_copies) BEFORE kv_append.
+ * block_table ([B][max_blocks]) and num_blocks ([B]) are host arrays updated
+ * in place.  All-or-nothing: on KVC_ERR_OOM / KVC_ERR_CAPACITY nothing is
+ * changed. */
+kvc_status kv_step_prepare(kvc_handle h, int32_t* block_table, int max_blocks, int32_t* num_blocks,
+                           const int32_t* positions, int B, int64_t* slot_mapping, int32_t* copy_src,
+                           int32_t* copy_dst, int* n_copies);
+
+/* ---- device operations ----------------------------------------------
+ * kv_append ("La caché de claves y valores", step 2 of a decode token):
+ * k_cache[layer][slot] = k_new[t], v_cache[layer][slot] = v_new[t] for every
+ * token t < n and KV head, where slot = slot_mapping[t].  k_new/v_new are
+ * device [n][Hkv][D] fp16; slot_mapping is device int64 [n]; a negative slot
+ * is skipped; a slot >= NB*bs sets KVC_DEVERR_SLOT and is skipped.  Bit copy. */
+kvc_status kv_append(kvc_handle h, int layer, const void* k_new, const void* v_new,
+                     const int64_t* slot_mapping, int n, void* stream);
+
+/* Split plan of paged_decode_attention for these sizes on the current
+ * device: the number of context splits, the blocks per split and the
+ * workspace bytes it needs.  blocks_per_split = 0 picks automatically. */
+kvc_status paged_decode_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                             int blocks_per_split, int* num_splits, int* blocks_per_split_out,
+                             size_t* workspace_bytes);
+/* Zero-fill a workspace before its first use (cudaMemsetAsync).  Every
+ * decode call leaves its counters at zero again. */
+kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Paged GQA decode attention for one token per sequence:
+ *   out[b][h] = softmax(q[b][h] . K_b^T * scale) V_b
+ * over the context_lens[b] tokens of sequence b (the appended token
+ * included), K_b/V_b gathered through block_table[b] from KV head
+ * h / (Hq / Hkv).
+ *   q            device fp16 [B][Hq][D]
+ *   k_cache      device fp16 [num_blocks][Hkv][bs][D] (one layer), v_cache same
+ *   block_table  device int32 [B][max_blocks]
+ *   context_lens device int32 [B], 1 <= ctx <= min(max_blocks*bs, max_context_len)
+ *   out          device [B][Hq][D], out_dtype KVC_F16 or KVC_F32
+ *   workspace    device, >= paged_decode_plan(...)'s bytes, zero-filled once
+ * The context of each sequence is cut into splits of blocks_per_split blocks;
+ * each (sequence, KV head, split) is one CTA that keeps the running max and
+ * exp-sum per query head; the last split to finish merges the partials with
+ * the rescaling rule of the FlashAttention article.
+ * Preconditions: Hq % Hkv == 0, Hq/Hkv <= 8, head_dim in {64, 128},
+ * block_size == 16; 16-byte aligned pointers. */
+kvc_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                  const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                  int B, int Hq, int Hkv, int head_dim, int block_size,
+                                  int max_context_len, float scale, void* out, int out_dtype,
+                                  void* workspace, size_t workspace_bytes, int blocks_per_split,
+                                  void* stream);
+
+/* Varlen packed prefill (xformers article parts 4-5): for every segment s
+ * (rows cu_seqlens[s] .. cu_seqlens[s+1]-1) and query head h,
+ *   out = softmax(Q K^T * scale + mask) V,
+ * K/V of KV head h / (Hq/Hkv) from the same segment only; mask allows j <= i
+ * when causal, everything in the segment otherwise.
+ *   q device fp16 [total_tokens][Hq][D]; k, v device fp16 [total_tokens][Hkv][D]
+ *   cu_seqlens device int32 [nseq+1], cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[nseq] = total_tokens; max_seqlen >= every segment length.
+ *   out device [total_tokens][Hq][D], out_dtype KVC_F16 or KVC_F32. */
+kvc_status prefill_attention(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                             int nseq, int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim,
+                             float scale, int causal, void* out, int out_dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

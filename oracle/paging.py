@@ -78,12 +78,12 @@ def serving_mix(mix, nthreads=None):
          FIFO allocation walks a seeded random physical order;
       2. per group in order: allocate the prefix pages; each member in order
          shares the first ceil(min(prefix_len, ctx-1) / bs) of them; the
-         prompt's own reference is then released (pages nobody needs return
-         to the pool); members in order then allocate private pages until
-         their table covers ctx-1 tokens;
-      3. the history is written: prefix tokens into the shared pages, each
-         member's suffix into its private pages;
-      4. the decode step, members in order: position p = ctx-1; if p falls on
+         prefix tokens that at least one member holds are written into the
+         shared pages; the prompt's own reference is then released (pages
+         nobody needs return to the pool); members in order then allocate
+         private pages until their table covers ctx-1 tokens and their
+         suffix tokens are written there;
+      3. the decode step, members in order: position p = ctx-1; if p falls on
          a new page, allocate it; else if its page has refcount > 1, take a
          copy-on-write private copy (the whole page is copied, then the old
          reference is released); the token's K/V are then appended at p and
@@ -107,12 +107,12 @@ def serving_mix(mix, nthreads=None):
             for pid in prefix_pages[:need]:
                 pool.share(pid)
             tables[b] = list(prefix_pages[:need])
+        # prefix tokens some member holds go into the shared pages, then the prompt's reference is dropped
+        n_pre = max(min(mix.prefix_len, int(mix.ctx[b]) - 1) for b in members)
+        slots = np.array([prefix_pages[p // bs] * bs + p % bs for p in range(n_pre)], dtype=np.int64)
+        _append(kc, vc, mix.prefix_k[g, :n_pre], mix.prefix_v[g, :n_pre], slots)
         for pid in prefix_pages:
             pool.release(pid)
-        # prefix tokens into the shared pages
-        pos = np.arange(mix.prefix_len)
-        slots = np.array([prefix_pages[p // bs] * bs + p % bs for p in pos], dtype=np.int64)
-        _append(kc, vc, mix.prefix_k[g], mix.prefix_v[g], slots)
         for b in members:
             while len(tables[b]) * bs < int(mix.ctx[b]) - 1:
                 tables[b].append(pool.allocate())

@@ -1,0 +1,119 @@
+// Append (slot-mapped scatter of new K/V rows into the paged cache) and
+// whole-block copy (the device half of copy-on-write).
+//
+// Append is step 2 of a decode token in "La caché de claves y valores"
+// (gustavoai.dev, section "Las claves y los valores de una posición no
+// cambian"): k_t, v_t go to the end of each head's cache before attention.
+// The slot of a token is block_table[pos / bs] * bs + pos % bs (PagedAttention
+// article, chatgpz.de, SECTION 2); here the caller passes the slots.
+// Copy-on-write (same article, SECTION 3): a sequence about to write into a
+// shared block first gets a private copy of the whole block.
+//
+// Both kernels are pure bandwidth: 16-byte vector loads/stores, consecutive
+// threads on consecutive 16-byte chunks of a row.
+#include <atomic>
+
+#include "../../include/kvc.h"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+__device__ unsigned g_error_word;
+
+cudaError_t device_error_word(unsigned** ptr) {
+    static std::atomic<unsigned*> cache[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) {
+        unsigned* p = cache[dev].load(std::memory_order_acquire);
+        if (p) {
+            *ptr = p;
+            return cudaSuccess;
+        }
+    }
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_error_word);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) cache[dev].store(static_cast<unsigned*>(addr), std::memory_order_release);
+    *ptr = static_cast<unsigned*>(addr);
+    return cudaSuccess;
+}
+
+// One thread per 16-byte chunk of a (token, KV head) row; rows of D fp16.
+__global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict__ k_new,
+                                                         const uint4* __restrict__ v_new,
+                                                         const int64_t* __restrict__ slots, int n,
+                                                         uint4* __restrict__ k_layer, uint4* __restrict__ v_layer,
+                                                         int num_blocks, int Hkv, int chunks_per_row,
+                                                         unsigned* err) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t total = static_cast<int64_t>(n) * Hkv * chunks_per_row;
+    if (idx >= total) return;
+    const int c = static_cast<int>(idx % chunks_per_row);
+    const int64_t row = idx / chunks_per_row;  // t * Hkv + h
+    const int h = static_cast<int>(row % Hkv);
+    const int64_t t = row / Hkv;
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= static_cast<int64_t>(num_blocks) * kBlockSize) {
+        if (c == 0) atomicOr(err, KVC_DEVERR_SLOT);
+        return;
+    }
+    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+    const int64_t dst = ((blk * Hkv + h) * kBlockSize + off) * chunks_per_row + c;
+    k_layer[dst] = k_new[idx];
+    v_layer[dst] = v_new[idx];
+}
+
+cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_t* slots, int n, __half* k_layer,
+                          __half* v_layer, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int cpr = D / 8;
+    const int64_t total = static_cast<int64_t>(n) * Hkv * cpr;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new), slots, n,
+        reinterpret_cast<uint4*>(k_layer), reinterpret_cast<uint4*>(v_layer), num_blocks, Hkv, cpr, err);
+    return cudaGetLastError();
+}
+
+constexpr int kMaxCopyPairs = 128;
+struct CopyPairs {
+    int32_t src[kMaxCopyPairs];
+    int32_t dst[kMaxCopyPairs];
+};
+
+// grid (pair, layer, K|V); each CTA copies one block of one layer of one pool.
+__global__ void __launch_bounds__(256) kv_copy_blocks_kernel(const CopyPairs pairs, uint4* __restrict__ k_pool,
+                                                              uint4* __restrict__ v_pool, int64_t layer_u4,
+                                                              int64_t block_u4) {
+    uint4* pool = blockIdx.z ? v_pool : k_pool;
+    const int64_t base = static_cast<int64_t>(blockIdx.y) * layer_u4;
+    const uint4* s = pool + base + static_cast<int64_t>(pairs.src[blockIdx.x]) * block_u4;
+    uint4* d = pool + base + static_cast<int64_t>(pairs.dst[blockIdx.x]) * block_u4;
+    for (int64_t c = threadIdx.x; c < block_u4; c += blockDim.x) d[c] = s[c];
+}
+
+cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __half* k_pool, __half* v_pool,
+                               int L, int num_blocks, int64_t block_elems, cudaStream_t stream) {
+    const int64_t block_u4 = block_elems / 8;
+    const int64_t layer_u4 = block_u4 * num_blocks;
+    for (int i0 = 0; i0 < n; i0 += kMaxCopyPairs) {
+        const int m = (n - i0 < kMaxCopyPairs) ? n - i0 : kMaxCopyPairs;
+        CopyPairs p;
+        for (int i = 0; i < m; ++i) {
+            p.src[i] = src[i0 + i];
+            p.dst[i] = dst[i0 + i];
+        }
+        dim3 grid(m, L, 2);
+        kv_copy_blocks_kernel<<<grid, 256, 0, stream>>>(p, reinterpret_cast<uint4*>(k_pool),
+                                                        reinterpret_cast<uint4*>(v_pool), layer_u4, block_u4);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kvc

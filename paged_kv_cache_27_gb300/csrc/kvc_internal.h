@@ -1,0 +1,67 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvc {
+
+constexpr int kBlockSize = 16;  // tokens per block (the page size used throughout the pages)
+
+// Device address of the sticky error word of the current device.
+cudaError_t device_error_word(unsigned** ptr);
+
+// ---- append / block copy (append.cu) ---------------------------------------
+cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_t* slots, int n, __half* k_layer,
+                          __half* v_layer, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream);
+// copies whole blocks src[i] -> dst[i] for every layer (pools [L][NB][block_elems])
+cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __half* k_pool, __half* v_pool,
+                               int L, int num_blocks, int64_t block_elems, cudaStream_t stream);
+
+// ---- decode (decode.cu) ------------------------------------------------------
+struct DecodePlan {
+    int num_splits;        // grid.x: splits of the longest context
+    int blocks_per_split;  // blocks of 16 tokens per split
+    size_t workspace_bytes;
+};
+cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_context_len, int blocks_per_split,
+                        DecodePlan* plan);
+struct DecodeArgs {
+    const __half* q;
+    const __half* k_cache;
+    const __half* v_cache;
+    int num_blocks;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* context_lens;
+    int B, Hq, Hkv, D;
+    int max_context_len;
+    float scale;
+    void* out;
+    int out_f32;
+    void* workspace;
+    size_t workspace_bytes;
+    int blocks_per_split;  // 0 = automatic
+    unsigned* err;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// ---- prefill (prefill.cu) ----------------------------------------------------
+struct PrefillArgs {
+    const __half* q;
+    const __half* k;
+    const __half* v;
+    const int32_t* cu_seqlens;
+    int nseq, total_tokens, max_seqlen;
+    int Hq, Hkv, D;
+    float scale;
+    int causal;
+    void* out;
+    int out_f32;
+    unsigned* err;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace kvc

@@ -1,0 +1,190 @@
+"""Drives the library through its public API on the synthetic workloads.
+
+Used by the benchmark and the GPU tests: it allocates pools and buffers with
+PyTorch, fills caches through ``kv_append``, runs decode steps, the
+serving-mix allocation protocol on the library's own block pool, and the
+prefill-then-decode flow.  Every step calls the C ABI; nothing here computes
+attention or slots itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (KvcConfig, kv_append, kv_block_alloc, kv_block_release, kv_block_share, kv_cache_create,
+               kv_cache_destroy, kv_copy_blocks, kv_slot_mapping, kv_step_prepare, paged_decode_attention,
+               paged_decode_plan, paged_decode_workspace_init, prefill_attention)
+
+F16_NAN = 0x7E00  # a quiet-NaN bit pattern used to poison cache slots nobody owns
+
+
+def _dev(a, device, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+def poisoned_pool(shape, device) -> torch.Tensor:
+    """fp16 pool filled with NaN bits: any read of a slot outside a context would show up."""
+    return torch.full(shape, F16_NAN, dtype=torch.int16, device=device).view(torch.float16)
+
+
+class DecodeSession:
+    """A paged cache holding a DecodeWorkload's history, ready for decode steps on every layer."""
+
+    def __init__(self, wl, device="cuda", out_dtype=torch.float32, blocks_per_split=0, poison=True):
+        self.wl = wl
+        self.device = device
+        cfg = KvcConfig(num_layers=wl.L, num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_dim=wl.D, block_size=wl.bs)
+        self.cfg = cfg
+        alloc = poisoned_pool if poison else (lambda s, d: torch.zeros(s, dtype=torch.float16, device=d))
+        self.k_pool = alloc(cfg.pool_shape, device)
+        self.v_pool = alloc(cfg.pool_shape, device)
+        self.h = kv_cache_create(cfg, self.k_pool, self.v_pool)
+        B = wl.B
+        self.max_ctx = int(wl.ctx.max())
+        self.block_table = _dev(wl.block_table, device)
+        self.context_lens = _dev(wl.ctx, device)
+        ones = np.ones(B, np.int32)
+        self.hist_slots = _dev(kv_slot_mapping(wl.block_table, np.zeros(B, np.int32), wl.ctx - 1, wl.bs), device)
+        self.step_slots_host = kv_slot_mapping(wl.block_table, wl.ctx - 1, ones, wl.bs)
+        self.step_slots = _dev(self.step_slots_host, device)
+        self.q = _dev(wl.q, device)
+        self.k_new = _dev(wl.k_new, device)
+        self.v_new = _dev(wl.v_new, device)
+        self.out = torch.empty((wl.L, B, wl.Hq, wl.D), dtype=out_dtype, device=device)
+        self.blocks_per_split = blocks_per_split
+        self.nsplit, self.bps, ws = paged_decode_plan(B, wl.Hq, wl.Hkv, wl.D, self.max_ctx, blocks_per_split)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        paged_decode_workspace_init(self.workspace)
+
+    def fill(self):
+        """Write every sequence's history (positions 0 .. ctx-2) into the cache, layer by layer."""
+        for layer in range(self.wl.L):
+            kh = _dev(self.wl.k_hist[layer], self.device)
+            vh = _dev(self.wl.v_hist[layer], self.device)
+            kv_append(self.h, layer, kh, vh, self.hist_slots)
+        return self
+
+    def append(self, layer, stream=None):
+        kv_append(self.h, layer, self.k_new[layer], self.v_new[layer], self.step_slots, stream=stream)
+
+    def decode(self, layer, stream=None):
+        paged_decode_attention(self.q[layer], self.k_pool[layer], self.v_pool[layer], self.block_table,
+                               self.context_lens, self.wl.scale, self.out[layer], self.workspace, self.max_ctx,
+                               self.blocks_per_split, stream=stream)
+
+    def step(self, stream=None):
+        """One decode step: for every layer, append the new token's K/V, then attend."""
+        for layer in range(self.wl.L):
+            self.append(layer, stream)
+            self.decode(layer, stream)
+
+    def close(self):
+        if self.h:
+            kv_cache_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def serving_mix(mix, device="cuda", out_dtype=torch.float32, poison=True):
+    """The serving-mix protocol on the library's block pool (see the design doc for the protocol).
+
+    Returns a dict: block tables before/after the step, copy pairs, slots, pools and the output."""
+    bs = mix.bs
+    cfg = KvcConfig(num_layers=1, num_blocks=mix.NB, num_kv_heads=mix.Hkv, head_dim=mix.D, block_size=bs)
+    alloc = poisoned_pool if poison else (lambda s, d: torch.zeros(s, dtype=torch.float16, device=d))
+    k_pool, v_pool = alloc(cfg.pool_shape, device), alloc(cfg.pool_shape, device)
+    h = kv_cache_create(cfg, k_pool, v_pool)
+    try:
+        for _ in range(mix.NB):
+            kv_block_alloc(h)
+        for pid in mix.free_order:
+            kv_block_release(h, int(pid))
+        B, G = mix.B, mix.group
+        npre = -(-mix.prefix_len // bs)
+        tables = [[] for _ in range(B)]
+        for g in range(-(-B // G)):
+            members = range(g * G, min(B, (g + 1) * G))
+            prefix_pages = [kv_block_alloc(h) for _ in range(npre)]
+            for b in members:
+                need = -(-min(mix.prefix_len, int(mix.ctx[b]) - 1) // bs)
+                for pid in prefix_pages[:need]:
+                    kv_block_share(h, pid)
+                tables[b] = list(prefix_pages[:need])
+            n_pre = max(min(mix.prefix_len, int(mix.ctx[b]) - 1) for b in members)
+            slots = kv_slot_mapping(np.array([prefix_pages], np.int32), [0], [n_pre], bs)
+            kv_append(h, 0, _dev(mix.prefix_k[g, :n_pre], device), _dev(mix.prefix_v[g, :n_pre], device),
+                      _dev(slots, device))
+            for pid in prefix_pages:
+                kv_block_release(h, pid)
+            for b in members:
+                while len(tables[b]) * bs < int(mix.ctx[b]) - 1:
+                    tables[b].append(kv_block_alloc(h))
+                n_suf = int(mix.suffix_off[b + 1] - mix.suffix_off[b])
+                if n_suf:
+                    row = np.array([tables[b]], np.int32)
+                    slots = kv_slot_mapping(row, [mix.prefix_len], [n_suf], bs)
+                    sl = slice(int(mix.suffix_off[b]), int(mix.suffix_off[b + 1]))
+                    kv_append(h, 0, _dev(mix.suffix_k[sl], device), _dev(mix.suffix_v[sl], device),
+                              _dev(slots, device))
+        tables_before = [list(t) for t in tables]
+        mb = max(-(-int(c) // bs) for c in mix.ctx)
+        table = np.full((B, mb), -1, np.int32)
+        nblk = np.zeros(B, np.int32)
+        for b in range(B):
+            table[b, :len(tables[b])] = tables[b]
+            nblk[b] = len(tables[b])
+        slots, copies = kv_step_prepare(h, table, nblk, mix.ctx - 1)
+        kv_copy_blocks(h, copies[:, 0], copies[:, 1])
+        kv_append(h, 0, _dev(mix.k_new, device), _dev(mix.v_new, device), _dev(slots, device))
+        q = _dev(mix.q, device)
+        out = torch.empty((B, mix.Hq, mix.D), dtype=out_dtype, device=device)
+        max_ctx = int(mix.ctx.max())
+        _, _, ws = paged_decode_plan(B, mix.Hq, mix.Hkv, mix.D, max_ctx)
+        workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        paged_decode_workspace_init(workspace)
+        paged_decode_attention(q, k_pool[0], v_pool[0], _dev(table, device), _dev(mix.ctx, device), mix.scale, out,
+                               workspace, max_ctx)
+        torch.cuda.synchronize()
+        return {"tables_before": tables_before, "block_table": table, "copies": copies, "slots": slots,
+                "k_cache": k_pool[0], "v_cache": v_pool[0], "out": out, "handle": None}
+    finally:
+        kv_cache_destroy(h)
+
+
+def prefill_then_decode(wl, causal=True, device="cuda", out_dtype=torch.float32, poison=True):
+    """Prefill a packed batch, write all its K/V into a paged cache, then one decode token per sequence."""
+    q, k, v = _dev(wl.q, device), _dev(wl.k, device), _dev(wl.v, device)
+    cu = _dev(wl.cu_seqlens, device)
+    T = q.shape[0]
+    out = torch.empty((T, wl.Hq, wl.D), dtype=out_dtype, device=device)
+    prefill_attention(q, k, v, cu, max(wl.seqlens), wl.scale, causal, out)
+    n = len(wl.seqlens)
+    cfg = KvcConfig(num_layers=1, num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_dim=wl.D, block_size=wl.bs)
+    alloc = poisoned_pool if poison else (lambda s, d: torch.zeros(s, dtype=torch.float16, device=d))
+    k_pool, v_pool = alloc(cfg.pool_shape, device), alloc(cfg.pool_shape, device)
+    h = kv_cache_create(cfg, k_pool, v_pool)
+    try:
+        seqlens = np.array(wl.seqlens, np.int32)
+        slots = kv_slot_mapping(wl.block_table, np.zeros(n, np.int32), seqlens, wl.bs)
+        kv_append(h, 0, k, v, _dev(slots, device))
+        step = kv_slot_mapping(wl.block_table, seqlens, np.ones(n, np.int32), wl.bs)
+        kv_append(h, 0, _dev(wl.k_dec, device), _dev(wl.v_dec, device), _dev(step, device))
+        ctx = seqlens + 1
+        dec = torch.empty((n, wl.Hq, wl.D), dtype=out_dtype, device=device)
+        _, _, ws = paged_decode_plan(n, wl.Hq, wl.Hkv, wl.D, int(ctx.max()))
+        workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        paged_decode_workspace_init(workspace)
+        paged_decode_attention(_dev(wl.q_dec, device), k_pool[0], v_pool[0], _dev(wl.block_table, device),
+                               _dev(ctx, device), wl.scale, dec, workspace, int(ctx.max()))
+        torch.cuda.synchronize()
+        return {"prefill_out": out, "decode_out": dec, "k_cache": k_pool[0], "v_cache": v_pool[0]}
+    finally:
+        kv_cache_destroy(h)

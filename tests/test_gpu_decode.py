@@ -1,0 +1,110 @@
+"""GPU parity of kv_append + paged_decode_attention against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import paging as opaging
+import workloads
+from parity import check_attention, check_cache_bits, owned_slots
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import paged_kv_cache_27_gb300 as m
+    return m
+
+
+def run_session(kvc, wl, out_dtype=torch.float32, bps=0):
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    s = DecodeSession(wl, out_dtype=out_dtype, blocks_per_split=bps).fill()
+    s.step()
+    torch.cuda.synchronize()
+    return s
+
+
+def check_workload(kvc, wl, out_dtype=torch.float32, bps=0, layers=None, cache_bits=True):
+    s = run_session(kvc, wl, out_dtype, bps)
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    errs = []
+    for layer in (range(wl.L) if layers is None else layers):
+        ref, kc, vc = opaging.decode_step(wl, layer)
+        errs.append(check_attention(s.out[layer], ref, f"{wl.name} layer {layer}"))
+        if cache_bits:
+            slots = owned_slots(wl.block_table, wl.ctx, wl.bs)
+            check_cache_bits(s.k_pool[layer], kc, slots)
+            check_cache_bits(s.v_pool[layer], vc, slots)
+    s.close()
+    return max(errs)
+
+
+def test_config1_single_sequence(kvc):
+    wl = workloads.config1()
+    for dt in (torch.float32, torch.float16):
+        check_workload(kvc, wl, dt)
+    # the cached row equals the last row of the full 256 x 256 causal recompute
+    s = run_session(kvc, wl)
+    K = np.concatenate([wl.k_hist[0], wl.k_new[0]])[:, 0].astype(np.float64)
+    V = np.concatenate([wl.v_hist[0], wl.v_new[0]])[:, 0].astype(np.float64)
+    Q = np.zeros_like(K)
+    Q[-1] = wl.q[0, 0, 0].astype(np.float64)
+    full = oracle.causal_attention(Q, K, V, wl.scale)
+    check_attention(s.out[0, 0], full[-1:], "config 1 vs 256x256 causal")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,ctx", [
+    (1, 1, 1, 64, [1]),
+    (3, 4, 4, 64, [1, 2, 3]),
+    (5, 14, 2, 64, [16, 17, 31, 32, 33]),
+    (4, 8, 1, 64, [255, 256, 257, 1000]),
+    (6, 7, 7, 128, [5, 64, 65, 200, 511, 700]),
+    (2, 16, 2, 128, [300, 1500]),
+    (9, 14, 2, 64, [4096, 1, 77, 2048, 3000, 16, 15, 999, 1024]),
+])
+def test_small_sweep(kvc, B, Hq, Hkv, D, ctx):
+    wl = workloads.small_decode(B * 100 + D, B=B, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, L=2)
+    for dt in (torch.float32, torch.float16):
+        check_workload(kvc, wl, dt)
+
+
+@pytest.mark.parametrize("bps", [1, 2, 3, 4, 7, 8, 64])
+def test_forced_split_sizes(kvc, bps):
+    wl = workloads.small_decode(77, B=4, Hq=14, Hkv=2, D=64, ctx=[1, 300, 1025, 2048], peak_frac=0.01)
+    check_workload(kvc, wl, torch.float32, bps=bps)
+
+
+def test_config2_full(kvc):
+    """24 layers x 32 sequences x context 2048, 14 q / 2 KV heads: every layer against the oracle."""
+    wl = workloads.config2()
+    err = check_workload(kvc, wl, torch.float32, layers=range(wl.L), cache_bits=True)
+    assert err < 2e-3
+
+
+def test_config2_fp16_out_sampled_layers(kvc):
+    wl = workloads.config2()
+    check_workload(kvc, wl, torch.float16, layers=[0, 11, 23], cache_bits=False)
+
+
+@pytest.mark.parametrize("B", [1, 4, 16])
+@pytest.mark.parametrize("ctx", [4096, 16384, 65536, 131072])
+def test_config4_long_context(kvc, B, ctx):
+    wl = workloads.config4(B, ctx)
+    check_workload(kvc, wl, torch.float32, cache_bits=(B * ctx <= 4 * 65536))
+
+
+def test_results_invariant_to_physical_placement(kvc):
+    """Same logical data under two block permutations gives bit-identical outputs."""
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    wl = workloads.small_decode(9, B=3, Hq=14, Hkv=2, D=64, ctx=[100, 1000, 2000])
+    outs = []
+    for seed in (1, 2):
+        perm = np.random.default_rng(seed).permutation(wl.NB).astype(np.int32)
+        wl2 = type(wl)(**{**wl.__dict__, "block_table": np.where(wl.block_table >= 0, perm[wl.block_table], -1)})
+        s = DecodeSession(wl2).fill()
+        s.step()
+        torch.cuda.synchronize()
+        outs.append(s.out.clone())
+        s.close()
+    assert torch.equal(outs[0], outs[1])

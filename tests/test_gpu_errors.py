@@ -1,0 +1,96 @@
+"""Error behaviour on the GPU: checked mode, device error flags, bad arguments (no fault, no hang).
+
+Every bad index here is caught by a bounds check on the host or inside the
+kernel before any memory access; nothing in this file faults the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def kvc():
+    import paged_kv_cache_27_gb300 as m
+    m.kvc_device_error_flags(clear=True)
+    yield m
+    m.kvc_set_checked_mode(False)
+    m.kvc_device_error_flags(clear=True)
+
+
+def session(wl):
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    return DecodeSession(wl).fill()
+
+
+def test_checked_mode_rejects_bad_tables_and_contexts(kvc):
+    wl = workloads.small_decode(1, B=2, Hq=4, Hkv=2, D=64, ctx=[20, 40])
+    s = session(wl)
+    kvc.kvc_set_checked_mode(True)
+    s.step()  # valid inputs pass
+    bad = s.block_table.clone()
+    bad[1, 1] = wl.NB + 5
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], bad, s.context_lens, wl.scale, s.out[0],
+                                   s.workspace, s.max_ctx)
+    assert e.value.name == "KVC_ERR_INVALID"
+    ctx0 = s.context_lens.clone()
+    ctx0[0] = 0
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, ctx0, wl.scale, s.out[0],
+                                   s.workspace, s.max_ctx)
+    assert e.value.name == "KVC_ERR_CAPACITY"
+    slots = torch.tensor([wl.NB * 16, 0], dtype=torch.int64, device="cuda")
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kv_append(s.h, 0, s.k_new[0], s.v_new[0], slots)
+    assert e.value.name == "KVC_ERR_CAPACITY"
+    s.close()
+
+
+def test_unchecked_bad_inputs_set_device_flags_without_faulting(kvc):
+    wl = workloads.small_decode(2, B=3, Hq=4, Hkv=2, D=64, ctx=[20, 40, 60])
+    s = session(wl)
+    bad = s.block_table.clone()
+    bad[1, 1] = -7  # in-kernel range check skips the block
+    ctx = s.context_lens.clone()
+    ctx[2] = 0  # in-kernel check writes zeros for this sequence
+    out = torch.full_like(s.out[0], 5.0)
+    kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], bad, ctx, wl.scale, out, s.workspace, s.max_ctx)
+    torch.cuda.synchronize()
+    f = kvc.kvc_device_error_flags(clear=True)
+    assert f & kvc.DEVERR["BLOCK_ID"] and f & kvc.DEVERR["CONTEXT"]
+    assert torch.isfinite(out).all()
+    assert (out[2] == 0).all()
+    # a slot past the pool is skipped by the append kernel and flagged
+    before = s.k_pool.clone()
+    slots = torch.tensor([wl.NB * 16 + 3, -1, -1], dtype=torch.int64, device="cuda")
+    kvc.kv_append(s.h, 0, s.k_new[0], s.v_new[0], slots)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["SLOT"]
+    assert torch.equal(before.view(torch.int16), s.k_pool.view(torch.int16))
+    s.close()
+
+
+def test_argument_errors(kvc):
+    wl = workloads.small_decode(3, B=2, Hq=4, Hkv=2, D=64, ctx=[20, 40])
+    s = session(wl)
+    small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    ns, bps, need = kvc.paged_decode_plan(2, 4, 2, 64, 40, blocks_per_split=1)
+    assert ns == 3 and need > 16
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
+                                   s.out[0], small_ws, s.max_ctx, blocks_per_split=1)
+    assert e.value.name == "KVC_ERR_INVALID"
+    q9 = torch.zeros((2, 18, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_attention(q9, s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
+                                   torch.empty_like(q9, dtype=torch.float32), s.workspace, s.max_ctx)
+    assert e.value.name == "KVC_ERR_UNSUPPORTED"  # group of 9 query heads per KV head
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
+                                   s.out[0], s.workspace, 10 ** 6)
+    assert e.value.name == "KVC_ERR_CAPACITY"
+    s.close()

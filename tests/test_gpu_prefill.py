@@ -1,0 +1,63 @@
+"""Varlen causal prefill into the paged cache, then a decode step, vs the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import check_attention, check_cache_bits, owned_slots
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_flow(wl, causal):
+    out = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
+    n = len(wl.seqlens)
+    kc = np.zeros((wl.NB, wl.Hkv, wl.bs, wl.D), np.float16)
+    vc = np.zeros_like(kc)
+    slots = []
+    for s in range(n):
+        for p in range(wl.seqlens[s]):
+            slots.append(int(wl.block_table[s][p // wl.bs]) * wl.bs + p % wl.bs)
+    oracle.append(kc, vc, wl.k, wl.v, np.array(slots, np.int64))
+    step = [int(wl.block_table[s][wl.seqlens[s] // wl.bs]) * wl.bs + wl.seqlens[s] % wl.bs for s in range(n)]
+    oracle.append(kc, vc, wl.k_dec, wl.v_dec, np.array(step, np.int64))
+    ctx = np.array(wl.seqlens, np.int32) + 1
+    dec = oracle.decode(wl.q_dec, kc, vc, wl.block_table, ctx, wl.scale)
+    return out, dec, kc, vc, ctx
+
+
+@pytest.mark.parametrize("make", [workloads.config5_varlen, workloads.config5_gqa])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_config5(make, causal, out_dtype):
+    from paged_kv_cache_27_gb300 import harness, kvc_device_error_flags
+    wl = make()
+    got = harness.prefill_then_decode(wl, causal=causal, out_dtype=out_dtype)
+    assert kvc_device_error_flags(clear=True) == 0
+    out, dec, kc, vc, ctx = oracle_flow(wl, causal)
+    check_attention(got["prefill_out"], out, f"{wl.name} prefill causal={causal}")
+    check_attention(got["decode_out"], dec, f"{wl.name} decode")
+    slots = owned_slots(wl.block_table, ctx, wl.bs)
+    check_cache_bits(got["k_cache"], kc, slots)
+    check_cache_bits(got["v_cache"], vc, slots)
+
+
+@pytest.mark.parametrize("seqlens,Hq,Hkv,D", [
+    ((1,), 2, 1, 64),
+    ((63, 64, 65, 1, 130), 4, 2, 64),
+    ((200, 3, 129), 8, 8, 128),
+    ((333,), 14, 2, 64),
+])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_ragged(seqlens, Hq, Hkv, D, causal):
+    import paged_kv_cache_27_gb300 as kvc
+    wl = workloads._prefill("ragged", [99, sum(seqlens), D], seqlens, Hq, Hkv, D)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
+    cu = torch.from_numpy(wl.cu_seqlens).cuda()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    kvc.prefill_attention(q, k, v, cu, max(seqlens), wl.scale, causal, out)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
+    check_attention(out, ref, f"prefill {seqlens}")

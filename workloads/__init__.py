@@ -29,6 +29,8 @@ Workload shapes follow the five configurations this library is measured on:
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import Optional
 
@@ -92,6 +94,9 @@ def _placement(rng, ctx, bs, NB=None, max_blocks=None):
 
 
 def _decode(name, seed, L, B, Hq, Hkv, D, ctx, bs=16, NB=None, peak_frac=0.0, peak_factor=3.0):
+    """Placement and peaked positions come from ``default_rng(seed)``; layer l's values from
+    ``default_rng([*seed, 1000 + l])`` (drawn in parallel threads: numpy releases the GIL)."""
+    seed = list(np.atleast_1d(seed).tolist())
     rng = np.random.default_rng(seed)
     ctx = np.asarray(ctx, dtype=np.int32)
     NB, mb, table = _placement(rng, ctx, bs, NB)
@@ -99,27 +104,40 @@ def _decode(name, seed, L, B, Hq, Hkv, D, ctx, bs=16, NB=None, peak_frac=0.0, pe
     hist_off = np.zeros(B + 1, dtype=np.int64)
     hist_off[1:] = np.cumsum(hist)
     rows = int(hist_off[-1])
-    k32 = rng.standard_normal(size=(L, rows, Hkv, D), dtype=np.float32)
-    v_hist = normal_f16(rng, (L, rows, Hkv, D))
-    q = normal_f16(rng, (L, B, Hq, D))
-    kn32 = rng.standard_normal(size=(L, B, Hkv, D), dtype=np.float32)
-    v_new = normal_f16(rng, (L, B, Hkv, D))
     peaks = []
     if peak_frac > 0:
-        # keys x3 on round(frac * ctx) seeded positions of each sequence
+        # keys x3 on round(frac * ctx) seeded positions of each sequence (all KV heads, all dims)
         for b in range(B):
             n = int(round(peak_frac * int(ctx[b])))
-            pos = np.sort(rng.permutation(int(ctx[b]))[:n])
-            peaks.append(pos)
+            peaks.append(np.sort(rng.permutation(int(ctx[b]))[:n]))
+    k_hist = np.empty((L, rows, Hkv, D), np.float16)
+    v_hist = np.empty((L, rows, Hkv, D), np.float16)
+    q = np.empty((L, B, Hq, D), np.float16)
+    k_new = np.empty((L, B, Hkv, D), np.float16)
+    v_new = np.empty((L, B, Hkv, D), np.float16)
+
+    def layer(l):
+        r = np.random.default_rng(seed + [1000 + l])
+        k32 = r.standard_normal(size=(rows, Hkv, D), dtype=np.float32)
+        v_hist[l] = normal_f16(r, (rows, Hkv, D))
+        q[l] = normal_f16(r, (B, Hq, D))
+        kn32 = r.standard_normal(size=(B, Hkv, D), dtype=np.float32)
+        v_new[l] = normal_f16(r, (B, Hkv, D))
+        for b, pos in enumerate(peaks):
             cached = pos[pos < ctx[b] - 1]
-            k32[:, hist_off[b] + cached] *= peak_factor
+            k32[hist_off[b] + cached] *= peak_factor
             if (pos == ctx[b] - 1).any():
-                kn32[:, b] *= peak_factor
+                kn32[b] *= peak_factor
+        k_hist[l] = k32
+        k_new[l] = kn32
+
+    with ThreadPoolExecutor(max_workers=min(L, os.cpu_count() or 1)) as ex:
+        list(ex.map(layer, range(L)))
     return DecodeWorkload(
         name=name, L=L, B=B, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, max_blocks=mb,
         scale=1.0 / float(np.sqrt(D)), ctx=ctx, block_table=table, hist_off=hist_off,
-        k_hist=k32.astype(np.float16), v_hist=v_hist, q=q, k_new=kn32.astype(np.float16),
-        v_new=v_new, extra={"peaks": peaks, "seed": seed})
+        k_hist=k_hist, v_hist=v_hist, q=q, k_new=k_new, v_new=v_new,
+        extra={"peaks": peaks, "seed": seed})
 
 
 def config1() -> DecodeWorkload:
