@@ -2,8 +2,10 @@
 """Benchmark: paged GQA decode attention on the 24-layer, 14 q / 2 KV head model shape.
 
 One step = one decode token for 32 sequences at context 2048 through all 24
-layers: per layer kv_append (the new token's K/V into the paged cache) and
-paged_decode_attention (split-context decode + combine).  Inputs are seeded
+layers: per layer the new token's K/V go into the paged cache and the token
+attends over its context (paged_decode_append_attention: append, split-context
+decode and split merge in one kernel; --unfused times kv_append +
+paged_decode_attention instead).  Inputs are seeded
 synthetic data (N(0,1) fp16) resident in HBM; the K/V pools (768 MiB per
 step) are larger than L2, so every step streams its cache from HBM.
 
@@ -11,8 +13,9 @@ value       KV-cache bytes read per step / device time per step (GB/s), all rank
 e2e         the same metric through the C ABI with host buffers: per step the
             host->device copy of q, k_new, v_new, slots, block table and
             context lengths and the device->host copy of the outputs are timed
-roofline    the decode call (decode kernel + split combine) alone: algorithmic
-            bytes per launch / CUDA-event launch time, against MEASURED_PEAKS
+roofline    the decode call (append + decode + split merge, one kernel) alone:
+            algorithmic bytes per launch / CUDA-event launch time, against the
+            measured HBM copy bandwidth
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
 
 --impl reference times the fp64 CPU oracle on the same workload instead.
@@ -38,7 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged GQA decode attention: KV-cache GB/s (% HBM peak) and decode tokens/s"
 WORKLOAD = ("decode step of a 24-layer model: 32 sequences x context 2048 (incl. the new token), 14 q / 2 KV "
             "heads, head_dim 64, fp16, block size 16, block tables permuted over a pool of 32 x 2048 tokens; "
-            "per layer kv_append + paged_decode_attention")
+            "per layer the new token's K/V appended to the paged cache, then paged GQA decode attention")
 L, B, CTX, HQ, HKV, D = 24, 32, 2048, 14, 2, 64
 
 
@@ -204,21 +207,15 @@ def run_ours(args):
     ctx_total = int(wl.ctx.astype(np.int64).sum())
     nblocks_total = int(sum(-(-int(c) // 16) for c in wl.ctx))
     step_bytes = kv_bytes_per_step(ctx_total, L)
-    combine = 1 if sess.nsplit > 1 else 0
-    launches_per_step = L * (2 + combine)
+    fused = not args.unfused
+    kvc.kvc_set_launch_overlap(not args.no_overlap)
+    # combine kernel only when the splits exceed the last-CTA merge limit (32)
+    combine = 1 if sess.nsplit > 32 else 0
+    launches_per_step = L * ((1 if fused else 2) + combine)
 
     stream = torch.cuda.Stream(device)
-    with torch.cuda.stream(stream):
-        sess.step()  # eager warm-up: one-time attribute setup, plan caching
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        sess.step()
-    dgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(dgraph, stream=stream):
-        for layer in range(L):
-            sess.decode(layer)
-    torch.cuda.synchronize()
+    graph = sess.capture(fused=fused, stream=stream)
+    dgraph = sess.capture(fused=fused, decode_only=True, stream=stream)
     assert kvc.kvc_device_error_flags(clear=True) == 0
 
     if args.profile_only:
@@ -286,10 +283,15 @@ def run_ours(args):
                        (d_ctx, h_ctx)):
             d_.copy_(h_, non_blocking=True)
         for layer in range(L):
-            kvc.kv_append(sess.h, layer, d_kn[layer], d_vn[layer], d_slots)
-            kvc.paged_decode_attention(d_q[layer], sess.k_pool[layer], sess.v_pool[layer], d_table, d_ctx,
-                                       wl.scale, sess.out[layer], sess.workspace, sess.max_ctx,
-                                       args.blocks_per_split)
+            if fused:
+                kvc.paged_decode_append_attention(d_q[layer], d_kn[layer], d_vn[layer], sess.k_pool[layer],
+                                                  sess.v_pool[layer], d_table, d_ctx, wl.scale, sess.out[layer],
+                                                  sess.workspace, sess.max_ctx, args.blocks_per_split)
+            else:
+                kvc.kv_append(sess.h, layer, d_kn[layer], d_vn[layer], d_slots)
+                kvc.paged_decode_attention(d_q[layer], sess.k_pool[layer], sess.v_pool[layer], d_table, d_ctx,
+                                           wl.scale, sess.out[layer], sess.workspace, sess.max_ctx,
+                                           args.blocks_per_split)
         h_out.copy_(sess.out, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 50))
@@ -308,17 +310,18 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         secs, nbytes, layers = 0.0, 0, 0
-        while layers < L and secs < 10.0:
-            s, n = oracle_sample(wl, B, [layers])
+        while secs < 10.0 and layers < 20 * L:
+            s, n = oracle_sample(wl, B, [layers % L])
             secs += s
             nbytes += n
             layers += 1
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.default_threads(), "kind": "oracle",
-               "sample": f"{layers} of 24 layers, all 32 sequences, decode only (fp64, {secs:.1f} s)"}
+               "sample": f"{layers} layer decodes of the 24-layer step (all 32 sequences, cycling layers), fp64, "
+                         f"{secs:.1f} s of oracle time"}
 
     peak, peak_kind = load_peaks()
     gbs = step_bytes * world / (ms_step * 1e-3) / 1e9
-    call_bytes = decode_call_bytes(ctx_total, nblocks_total)
+    call_bytes = decode_call_bytes(ctx_total, nblocks_total) + (B * HKV * D * 2 * 2 * 2 if fused else 0)
     achieved = call_bytes / (us_decode * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -327,12 +330,15 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "layers": L, "batch_per_gpu": B, "context": CTX, "q_heads": HQ,
                    "kv_heads": HKV, "head_dim": D, "block_size": 16, "num_splits": sess.nsplit,
                    "blocks_per_split": sess.bps, "l2": "inputs larger than L2: 768 MiB of K/V per step",
-                   "launch": "CUDA graph of the 24-layer step"},
+                   "launch": "CUDA graph of the 24-layer step" + ("" if args.no_overlap else
+                                                                             ", programmatic dependent launch"),
+                   "append": "fused into the decode kernel" if fused else "separate kv_append kernel"},
         "tokens_per_s": B * world / (ms_step * 1e-3),
         "pct_hbm_peak": gbs / world / peak * 100.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "paged_decode_attention call (decode kernel + split combine), one layer",
+                     "kernel": ("paged_decode_append_attention" if fused else "paged_decode_attention")
+                               + " call, one layer (split merge inside the kernel)",
                      "bytes_per_launch": call_bytes, "us_per_launch": us_decode},
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
@@ -356,6 +362,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--blocks-per-split", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="separate kv_append + paged_decode_attention calls")
+    ap.add_argument("--no-overlap", action="store_true", help="no programmatic dependent launch")
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -171,7 +171,10 @@ kvc_status paged_decode_plan(int B, int Hq, int Hkv, int head_dim, int block_siz
                              int blocks_per_split, int* num_splits, int* blocks_per_split_out,
                              size_t* workspace_bytes);
 /* Zero-fill a workspace before its first use (cudaMemsetAsync).  Every
- * decode call leaves its counters at zero again. */
+ * decode call leaves its split counters at zero again, so a workspace can be
+ * reused by later calls with the same B and Hkv (any context length); zero it
+ * again before reusing it for another B or Hkv.  Calls that share a workspace
+ * must not overlap in time (same stream, or ordered by events). */
 kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* Paged GQA decode attention for one token per sequence:
@@ -197,6 +200,28 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
                                   int max_context_len, float scale, void* out, int out_dtype,
                                   void* workspace, size_t workspace_bytes, int blocks_per_split,
                                   void* stream);
+
+/* The same step with the append fused in (steps 2 and 3 of a decode token
+ * on the gustavoai.dev page in one kernel): for every sequence b the new
+ * token's rows k_new[b], v_new[b] (device fp16 [B][Hkv][D]) are written to
+ * position context_lens[b]-1 of the cache, i.e. slot
+ * block_table[b][(ctx-1)/bs]*bs + (ctx-1)%bs, and take part in the attention
+ * of that same call.  Bit-identical cache contents to kv_append with those
+ * slots followed by paged_decode_attention. */
+kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                         void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                                         const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim,
+                                         int block_size, int max_context_len, float scale, void* out, int out_dtype,
+                                         void* workspace, size_t workspace_bytes, int blocks_per_split, void* stream);
+
+/* Launch overlap (process-wide, default off).  When on, decode kernels are
+ * launched as programmatic dependents of the kernel before them on the
+ * stream: they read block tables, context lengths and the cached K/V
+ * history before that kernel has finished, and q, k_new, v_new, the
+ * workspace and out only after.  Contract: the kernel launched immediately
+ * before a decode call must not write its block table, context lengths or
+ * the cache rows the call reads (other than through this call's append). */
+kvc_status kvc_set_launch_overlap(int on);
 
 /* Varlen packed prefill (xformers article parts 4-5): for every segment s
  * (rows cu_seqlens[s] .. cu_seqlens[s+1]-1) and query head h,

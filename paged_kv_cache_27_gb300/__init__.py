@@ -28,6 +28,7 @@ __all__ = [
     "kv_block_release", "kv_block_refcount", "kv_block_num_free", "kv_cache_utilisation",
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
+    "paged_decode_append_attention", "kvc_set_launch_overlap",
     "prefill_attention", "DEVERR",
 ]
 
@@ -102,6 +103,9 @@ def _load():
         "paged_decode_plan": (I, [I, I, I, I, I, I, I, PI, PI, PSZ]),
         "paged_decode_workspace_init": (I, [P, SZ, P]),
         "paged_decode_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ, I, P]),
+        "paged_decode_append_attention": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
+                                              P, SZ, I, P]),
+        "kvc_set_launch_overlap": (I, [I]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
     }
     for name, (res, args) in sig.items():
@@ -157,6 +161,11 @@ def kvc_version() -> int:
 
 def kvc_set_checked_mode(on: bool) -> None:
     _check(_lib.kvc_set_checked_mode(int(bool(on))), "kvc_set_checked_mode")
+
+
+def kvc_set_launch_overlap(on: bool) -> None:
+    """Launch decode kernels as programmatic dependents of the previous kernel (see include/kvc.h)."""
+    _check(_lib.kvc_set_launch_overlap(int(bool(on))), "kvc_set_launch_overlap")
 
 
 def kvc_device_error_flags(clear: bool = False) -> int:
@@ -332,6 +341,33 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs,
         int(max_context_len), float(scale), _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split),
         _stream(stream, q)), "paged_decode_attention")
+
+
+def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                                  v_cache: torch.Tensor, block_table: torch.Tensor, context_lens: torch.Tensor,
+                                  scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor],
+                                  max_context_len: int, blocks_per_split: int = 0, stream=None) -> None:
+    """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel)."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B][Hkv][D]")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table / context_lens do not match B")
+    od = KVC_F16 if out.dtype == torch.float16 else KVC_F32 if out.dtype == torch.float32 else None
+    if od is None:
+        raise TypeError("out must be float16 or float32")
+    ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.paged_decode_append_attention(
+        _dptr(q, torch.float16, "q"), _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
+        _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"), NB,
+        _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
+        _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),
+        "paged_decode_append_attention")
 
 
 def paged_decode_attention_raw(q_ptr: int, k_ptr: int, v_ptr: int, num_blocks: int, table_ptr: int, max_blocks: int,

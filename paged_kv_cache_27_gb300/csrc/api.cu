@@ -359,11 +359,44 @@ kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stre
     return KVC_OK;
 }
 
+kvc_status kvc_set_launch_overlap(int on) {
+    kvc::set_launch_overlap(on);
+    return KVC_OK;
+}
+
+static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                                const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim, int block_size,
+                                int max_context_len, float scale, void* out, int out_dtype, void* workspace,
+                                size_t workspace_bytes, int blocks_per_split, void* stream);
+
 kvc_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
                                   const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
                                   int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
                                   int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
                                   void* stream) {
+    return decode_common(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B,
+                         Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype, workspace,
+                         workspace_bytes, blocks_per_split, stream);
+}
+
+kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                         void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                                         const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim,
+                                         int block_size, int max_context_len, float scale, void* out, int out_dtype,
+                                         void* workspace, size_t workspace_bytes, int blocks_per_split, void* stream) {
+    if (B > 0 && (!k_new || !v_new)) return fail(KVC_ERR_INVALID, "null k_new/v_new");
+    if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVC_ERR_INVALID, "k_new/v_new must be 16-byte aligned");
+    return decode_common(q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B, Hq,
+                         Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype, workspace,
+                         workspace_bytes, blocks_per_split, stream);
+}
+
+static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                                const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim, int block_size,
+                                int max_context_len, float scale, void* out, int out_dtype, void* workspace,
+                                size_t workspace_bytes, int blocks_per_split, void* stream) {
     kvc_status s = check_decode_shape(B, Hq, Hkv, head_dim, block_size, max_context_len);
     if (s != KVC_OK) return s;
     if (B == 0) return KVC_OK;
@@ -394,6 +427,8 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
     }
     kvc::DecodeArgs a;
     a.q = static_cast<const __half*>(q);
+    a.k_new = static_cast<const __half*>(k_new);
+    a.v_new = static_cast<const __half*>(v_new);
     a.k_cache = static_cast<const __half*>(k_cache);
     a.v_cache = static_cast<const __half*>(v_cache);
     a.num_blocks = num_blocks;
@@ -419,7 +454,7 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
     e = kvc::device_error_word(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     e = kvc::launch_decode(a, as_stream(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attention launch");
+    if (e != cudaSuccess) return cuda_fail(e, k_new ? "paged_decode_append_attention launch" : "paged_decode_attention launch");
     return KVC_OK;
 }
 

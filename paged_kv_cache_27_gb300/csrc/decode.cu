@@ -8,24 +8,33 @@
 // included).  K_b, V_b are found through the sequence's block table
 // (PagedAttention, chatgpz.de SECTION 2 and neuralialabs.com); query head h
 // reads KV head h / G, G = Hq / Hkv (xformers article part 5, BMGHK).
+// With k_new/v_new the kernel also performs the step's append: the new
+// token's K/V go to position ctx-1 of the cache (step 2 of a decode token on
+// the gustavoai.dev page) and enter the attention directly.
 //
 // Design (GB300):
-//  * one CTA per (context split, KV head, sequence); the G <= 8 query heads of
-//    a KV head are the rows of one m16n8k16 tile, so every K/V tile fetched
-//    from HBM is used by the whole group;
-//  * each warp owns a private ring of kStages stages; one lane issues the two
-//    TMA tile loads (K and V, 16 tokens x D fp16 each, 128-byte swizzled so the
-//    ldmatrix reads below are bank-conflict free) and the warp waits on the
-//    stage's mbarrier (bounded wait, error flag on expiry);
+//  * one CTA per (context split, KV head, sequence); the grid is sized from
+//    the measured occupancy so that all CTAs are resident at once;
+//  * the G <= 8 query heads of a KV head are the rows of one m16n8k16 tile, so
+//    every K/V tile fetched from HBM serves the whole group;
+//  * each warp owns a ring of kStages stages; lane 0 issues the K and V tile
+//    loads (16 tokens x D fp16 each) with 2-D TMA and the 128-byte swizzle so
+//    that the ldmatrix reads are bank-conflict free; the warp waits on the
+//    stage's mbarrier (bounded wait, error flag on expiry) and refills it;
+//  * the split's block-table entries are fetched in one coalesced load (one
+//    entry per lane) and passed by shuffles;
 //  * S = Q K^T and O += P V on the tensor cores (mma.sync, fp16 in, fp32
-//    accumulate); P is split into an fp16 high part and an fp16 residual so the
-//    P V product keeps ~fp32 accuracy;
-//  * online softmax in fp32, base 2 (scale * log2 e folded into the scores),
-//    row max by quad shuffles;
-//  * warps of a CTA merge through shared memory, splits of a sequence through
-//    a workspace and a small combine kernel, both with the rescaling rule of
-//    the FlashAttention article ("Was ist der mathematische Aspekt von
-//    Softmax?"): partial (m, l, acc) are rescaled by 2^(m - M), M the global max.
+//    accumulate); P is split into an fp16 high part and an fp16 residual so
+//    the P V product keeps ~fp32 accuracy; online softmax in fp32, base 2;
+//  * warps of a CTA merge through shared memory; splits of a sequence merge
+//    in the last CTA to finish (atomic ticket, no waiting) or, for many
+//    splits, in a separate combine kernel; both use the rule of the
+//    FlashAttention article ("Was ist der mathematische Aspekt von Softmax?"):
+//    partial (m, l, acc) are rescaled by 2^(m - M), M the global maximum;
+//  * with launch overlap on, the kernel is launched as a programmatic
+//    dependent of the previous kernel: it fetches block tables, context lengths
+//    and cached K/V before waiting for that kernel, and reads q, k_new, v_new
+//    (and writes anything) only after.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -38,32 +47,43 @@
 
 namespace kvc {
 
-constexpr int kWarps = 4;   // warps per CTA
-constexpr int kStages = 4;  // ring stages per warp
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxWarpBlocks = 32;    // blocks per warp per split (one table entry per lane)
+constexpr int kMaxInlineSplits = 32;  // splits merged by the last CTA; more go to the combine kernel
+
+std::atomic<int> g_launch_overlap{0};
 
 template <int D>
-struct DecodeGeom {
+struct DecodeCfg {
+    static constexpr int kWarps = 4;
+    static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr int kTileBytes = kBlockSize * D * 2;  // one 16 x D fp16 tile
     static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
     static constexpr int kWarpRingBytes = kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kSmemBytes = kRingBytes + kBarBytes + 1024;  // + alignment slack
-    static constexpr int kMergeStride = D + 4;                        // floats per merged row
-    static_assert(8 * 2 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "merge area must fit a warp ring");
+    static constexpr int kMiscBytes = 16 + 8 * kMaxInlineSplits * 4;  // ticket flag + combine weights
+    static constexpr int kSmemBytes = kRingBytes + kBarBytes + kMiscBytes + 1024;  // + alignment slack
+    static constexpr int kMergeStride = D + 4;                                      // floats per merged row
+    static constexpr int kMaxBps = kWarps * kMaxWarpBlocks;
+    static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "merge area must fit a warp ring");
 };
 
 struct DecodeKernelParams {
     const __half* q;
+    const __half* k_new;  // null: no append
+    const __half* v_new;
+    __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
+    __half* v_cache;
     const int32_t* block_table;
     const int32_t* context_lens;
     void* out;
     float* part_ml;   // [B][Hq][nsplit][2] (m, l) in base-2 units
     float* part_acc;  // [B][Hq][nsplit][D]
+    int* tickets;     // [B][Hkv], zero between calls
     unsigned* err;
-    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx, bps, nsplit, out_f32;
+    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx, bps, nsplit, out_f32, inline_combine;
     float scale_log2;
 };
 
@@ -73,22 +93,28 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(((chunk >> 3) << 11) + (row << 7) + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <int D>
-__device__ __forceinline__ void store_out(const DecodeKernelParams& p, int64_t idx, float v) {
-    if (p.out_f32)
-        static_cast<float*>(p.out)[idx] = v;
+__device__ __forceinline__ void store_out(void* out, int out_f32, int64_t idx, float v) {
+    if (out_f32)
+        static_cast<float*>(out)[idx] = v;
     else
-        static_cast<__half*>(p.out)[idx] = __float2half_rn(v);
+        static_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+__device__ __forceinline__ int split_count(int ctx, int bps) {
+    return ((ctx + kBlockSize - 1) / kBlockSize + bps - 1) / bps;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                                   const __grid_constant__ CUtensorMap tmV,
-                                                                   const DecodeKernelParams p) {
-    using Geo = DecodeGeom<D>;
+__global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecodeKernelParams p) {
+    using C = DecodeCfg<D>;
+    constexpr int NW = C::kWarps, ST = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kRingBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+    int* s_flag = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes);
+    float* s_w = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + 16);  // [8][kMaxInlineSplits]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -96,10 +122,11 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
 
     const int ctx = p.context_lens[b];
     if (ctx < 1 || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
+        grid_dependency_wait();
         if (split == 0) {
             if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
             for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
-                store_out<D>(p, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
+                store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
         }
         return;
     }
@@ -108,44 +135,49 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
     if (split >= nsplit) return;
     const int j0 = split * p.bps;
     const int nb_split = min(j0 + p.bps, nblk) - j0;
-    const int nb_w = warp < nb_split ? (nb_split - warp + kWarps - 1) / kWarps : 0;
+    const int nb_w = warp < nb_split ? (nb_split - warp + NW - 1) / NW : 0;  // <= kMaxWarpBlocks
+
+    // this warp's block-table entries, one per lane
+    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+    const int my_blk = lane < nb_w ? table[j0 + warp + lane * NW] : -1;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kWarps * kStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NW * ST; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
     __syncthreads();
 
-    uint64_t* wbars = bars + warp * kStages;
-    uint8_t* wring = smem + warp * Geo::kWarpRingBytes;
-    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+    uint64_t* wbars = bars + warp * ST;
+    uint8_t* wring = smem + warp * C::kWarpRingBytes;
+    const uint64_t policy = l2_policy_evict_first();
 
-    // lane 0: issue the K and V tiles of this warp's i-th block into stage i % kStages
-    auto issue = [&](int i) {
-        const int jj = j0 + warp + i * kWarps;
-        const int phys = table[jj];
-        uint64_t* bar = &wbars[i % kStages];
+    // lane 0: the K and V tiles of this warp's i-th block into stage i % ST
+    auto issue = [&](int i, int phys) {
+        uint64_t* bar = &wbars[i % ST];
         if (phys < 0 || phys >= p.num_blocks) {
             atomicOr(p.err, KVC_DEVERR_BLOCK_ID);
             mbar_arrive(bar);  // complete the phase without data; the block is skipped
             return;
         }
-        const uint64_t policy = l2_policy_evict_first();
-        uint8_t* st = wring + (i % kStages) * Geo::kStageBytes;
-        mbar_arrive_expect_tx(bar, Geo::kStageBytes);
+        uint8_t* st = wring + (i % ST) * C::kStageBytes;
+        mbar_arrive_expect_tx(bar, C::kStageBytes);
         const int y = (phys * p.Hkv + kvh) * kBlockSize;
 #pragma unroll
         for (int x = 0; x < D; x += 64) {
             tma_load_2d(st + (x / 64) * 2048, &tmK, bar, x, y, policy);
-            tma_load_2d(st + Geo::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
+            tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
         }
     };
-    if (lane == 0) {
-        const int n0 = min(nb_w, kStages);
-        for (int i = 0; i < n0; ++i) issue(i);
+#pragma unroll
+    for (int i = 0; i < ST; ++i) {
+        const int phys = __shfl_sync(0xffffffffu, my_blk, i);
+        if (lane == 0 && i < nb_w) issue(i, phys);
     }
+
+    // ---- everything below may read what the previous kernel wrote ----
+    grid_dependency_wait();
 
     // query fragments (A operand, rows = the G heads of this KV head; rows >= G are zero)
     uint32_t qa[D / 16][2];
@@ -159,6 +191,27 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
         }
     }
 
+    // fused append: the warp holding the block of position ctx-1 writes the new row to the cache
+    // and patches it into its shared-memory tile before use
+    int app_iter = -1;
+    const int app_row = (ctx - 1) % kBlockSize;
+    uint4 app_val = make_uint4(0, 0, 0, 0);
+    if (p.k_new != nullptr && split == nsplit - 1 && ((nblk - 1 - j0) % NW) == warp) {
+        app_iter = (nblk - 1 - j0) / NW;
+        const int phys = __shfl_sync(0xffffffffu, my_blk, app_iter);
+        const int c = lane & 15;
+        const bool is_v = lane >= 16;
+        if (c < D / 8) {
+            const __half* src = (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.Hkv + kvh) * D + c * 8;
+            app_val = *reinterpret_cast<const uint4*>(src);
+            if (phys >= 0 && phys < p.num_blocks) {
+                __half* dst = (is_v ? p.v_cache : p.k_cache) +
+                              ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D + c * 8;
+                *reinterpret_cast<uint4*>(dst) = app_val;
+            }
+        }
+    }
+
     float o[D / 8][4];
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
@@ -168,18 +221,28 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
     int i = 0;
     bool timed_out = false;
     for (; i < nb_w; ++i) {
-        const int stage = i % kStages;
-        const uint32_t parity = (i / kStages) & 1;
-        const int jj = j0 + warp + i * kWarps;
-        const int phys = table[jj];
+        const int stage = i % ST;
+        const uint32_t parity = (i / ST) & 1;
+        const int jj = j0 + warp + i * NW;
+        const int phys = __shfl_sync(0xffffffffu, my_blk, i);
         const bool ok = mbar_wait_bounded(&wbars[stage], parity, kWaitLimitNs);
         if (__any_sync(0xffffffffu, !ok)) {
             timed_out = true;
             break;
         }
         if (phys >= 0 && phys < p.num_blocks) {
-            const uint32_t kbase = smem_u32(wring + stage * Geo::kStageBytes);
-            const uint32_t vbase = kbase + Geo::kTileBytes;
+            const uint32_t kbase = smem_u32(wring + stage * C::kStageBytes);
+            const uint32_t vbase = kbase + C::kTileBytes;
+            if (i == app_iter) {
+                const int c = lane & 15;
+                if (c < D / 8) {
+                    const uint32_t a = (lane >= 16 ? vbase : kbase) + swz(app_row, c);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(app_val.x), "r"(app_val.y),
+                                 "r"(app_val.z), "r"(app_val.w)
+                                 : "memory");
+                }
+                __syncwarp();
+            }
             // ---- S = Q K^T for the 16 tokens of this block (two n-tiles of 8) ----
             float sc[2][4];
 #pragma unroll
@@ -249,15 +312,19 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
             }
         }
         __syncwarp();
-        if (lane == 0 && i + kStages < nb_w) issue(i + kStages);
+        const int nxt = __shfl_sync(0xffffffffu, my_blk, (i + ST) & 31);
+        if (lane == 0 && i + ST < nb_w) issue(i + ST, nxt);
     }
+    // the next kernel may start its prologue while this one finishes
+    grid_dependents_launch();
     if (timed_out) {
         if (lane == 0) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
         // let copies still in flight land before the shared memory is reused
-        for (int k = i; k < min(nb_w, i + kStages); ++k)
-            mbar_wait_bounded(&wbars[k % kStages], (k / kStages) & 1, kWaitLimitNs / 8);
+        for (int k = i; k < min(nb_w, i + ST); ++k) mbar_wait_bounded(&wbars[k % ST], (k / ST) & 1, kWaitLimitNs / 8);
         m_run = -INFINITY;
         l_run = 0.f;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = 0.f;
     }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
@@ -272,7 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
     float* wo = wm + 16;
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd)
-        *reinterpret_cast<float2*>(wo + g * Geo::kMergeStride + nd * 8 + 2 * t4) = make_float2(o[nd][0], o[nd][1]);
+        *reinterpret_cast<float2*>(wo + g * C::kMergeStride + nd * 8 + 2 * t4) = make_float2(o[nd][0], o[nd][1]);
     __syncthreads();
 
     const bool direct = nsplit == 1;
@@ -280,18 +347,20 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
         const int gg = e / D, d = e % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * Geo::kWarpRingBytes)[gg]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes)[gg]);
         float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float* r = reinterpret_cast<const float*>(smem + w * Geo::kWarpRingBytes);
-            const float wgt = ex2(r[gg] - M);  // an empty warp has m = -inf -> weight 0
-            L += r[8 + gg] * wgt;
-            O += r[16 + gg * Geo::kMergeStride + d] * wgt;
+            for (int w = 0; w < NW; ++w) {
+                const float* r = reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes);
+                const float wgt = ex2(r[gg] - M);  // an empty warp has m = -inf -> weight 0
+                L += r[8 + gg] * wgt;
+                O += r[16 + gg * C::kMergeStride + d] * wgt;
+            }
         }
         const int h = kvh * p.G + gg;
         if (direct) {
-            store_out<D>(p, (static_cast<int64_t>(b) * p.Hq + h) * D + d, L > 0.f ? O / L : 0.f);
+            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, L > 0.f ? O / L : 0.f);
         } else {
             const int64_t row = (static_cast<int64_t>(b) * p.Hq + h) * p.nsplit + split;
             if (d == 0) {
@@ -301,10 +370,62 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const __grid_
             p.part_acc[row * D + d] = O;
         }
     }
+    if (direct || !p.inline_combine) return;
+
+    // ---- the last split of this (sequence, KV head) to finish merges all of them ----
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int t = atomicAdd(&p.tickets[b * p.Hkv + kvh], 1);
+        *s_flag = (t == nsplit - 1);
+    }
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+    // per head: global max M and the weights 2^(m_s - M) / L
+    {
+        const int gg = threadIdx.x >> 4, sub = threadIdx.x & 15;  // 16 threads per head, 8 heads
+        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nsplit;
+        float M = -INFINITY;
+        if (gg < p.G)
+            for (int s = sub; s < nsplit; s += 16) M = fmaxf(M, __ldcg(p.part_ml + (row0 + s) * 2));
+#pragma unroll
+        for (int off = 8; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        if (gg < p.G)
+            for (int s = sub; s < nsplit; s += 16) {
+                const float m = __ldcg(p.part_ml + (row0 + s) * 2), l = __ldcg(p.part_ml + (row0 + s) * 2 + 1);
+                const float w = m == -INFINITY ? 0.f : ex2(m - M);
+                s_w[gg * kMaxInlineSplits + s] = w;
+                L += l * w;
+            }
+#pragma unroll
+        for (int off = 8; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        __syncwarp();
+        if (gg < p.G)
+            for (int s = sub; s < nsplit; s += 16) s_w[gg * kMaxInlineSplits + s] *= (L > 0.f ? 1.f / L : 0.f);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.G * (D / 2); e += blockDim.x) {
+        const int gg = e / (D / 2), d = (e % (D / 2)) * 2;
+        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nsplit;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int s = 0; s < nsplit; ++s) {
+            const float w = s_w[gg * kMaxInlineSplits + s];
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_acc + (row0 + s) * D + d));
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+        }
+        const int64_t idx = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d;
+        store_out(p.out, p.out_f32, idx, acc.x);
+        store_out(p.out, p.out_f32, idx + 1, acc.y);
+    }
+    if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0;  // ready for the next call
 }
 
-// Merge the split partials of every (sequence, query head): 8 groups of 32
-// lanes walk the splits with a running (M, L, acc), then the groups merge.
+// Merge the split partials of every (sequence, query head) when there are too
+// many splits for the last-CTA merge: 8 groups of 32 lanes walk the splits
+// with a running (M, L, acc), then the groups merge.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* __restrict__ part_ml,
                                                                     const float* __restrict__ part_acc,
@@ -313,11 +434,12 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
                                                                     int max_blocks, int max_ctx, int out_f32) {
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
+    grid_dependency_wait();
     const int h = blockIdx.x, b = blockIdx.y;
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctx = context_lens[b];
     if (ctx < 1 || ctx > max_blocks * kBlockSize || ctx > max_ctx) return;
-    const int nsplit = ((ctx + kBlockSize - 1) / kBlockSize + bps - 1) / bps;
+    const int nsplit = split_count(ctx, bps);
     if (nsplit <= 1) return;
     const int64_t row0 = (static_cast<int64_t>(b) * Hq + h) * nsplit_grid;
     float M = -INFINITY, L = 0.f, O[V];
@@ -326,7 +448,8 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
     for (int s = grp; s < nsplit; s += 8) {
         const float m = part_ml[(row0 + s) * 2], l = part_ml[(row0 + s) * 2 + 1];
         const float Mn = fmaxf(M, m);
-        const float a = ex2(M - Mn), w = ex2(m - Mn);
+        const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
+        const float w = m == -INFINITY ? 0.f : ex2(m - Mn);
         L = L * a + l * w;
 #pragma unroll
         for (int v = 0; v < V; ++v) O[v] = O[v] * a + part_acc[(row0 + s) * D + lane * V + v] * w;
@@ -345,16 +468,11 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
         for (int k = 0; k < 8; ++k) Mx = fmaxf(Mx, sM[k]);
         float Lt = 0.f, Ot = 0.f;
         for (int k = 0; k < 8; ++k) {
-            const float w = ex2(sM[k] - Mx);  // groups that saw no split have M = -inf
+            const float w = sM[k] == -INFINITY ? 0.f : ex2(sM[k] - Mx);  // groups that saw no split
             Lt += sL[k] * w;
             Ot += sO[k][d] * w;
         }
-        const float r = Lt > 0.f ? Ot / Lt : 0.f;
-        const int64_t idx = (static_cast<int64_t>(b) * Hq + h) * D + d;
-        if (out_f32)
-            static_cast<float*>(out)[idx] = r;
-        else
-            static_cast<__half*>(out)[idx] = __float2half_rn(r);
+        store_out(out, out_f32, (static_cast<int64_t>(b) * Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
     }
 }
 
@@ -372,24 +490,54 @@ static int sm_count() {
     return n;
 }
 
+// one-time kernel attributes and the resident CTAs per SM of the decode kernel
+template <int D>
+static cudaError_t decode_setup(int* ctas_per_sm) {
+    using C = DecodeCfg<D>;
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    static int occ = 0;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (err == cudaSuccess)
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kWarps * 32,
+                                                                C::kSmemBytes);
+        if (err == cudaSuccess && occ < 1) err = cudaErrorInvalidConfiguration;
+    });
+    if (ctas_per_sm) *ctas_per_sm = occ;
+    return err;
+}
+
+// workspace layout: [tickets: B*Hkv int32, padded to 256 B][m, l: B*Hq*nsplit*2 fp32][acc: B*Hq*nsplit*D fp32].
+// The tickets sit first so that calls with the same B and Hkv but another split
+// count (a longer context) find them where the previous call left them (zero).
+static size_t ticket_bytes(int B, int Hkv) { return (static_cast<size_t>(B) * Hkv * 4 + 255) / 256 * 256; }
+
 cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_ctx, int bps_req, DecodePlan* plan) {
     const int nblk = (max_ctx + kBlockSize - 1) / kBlockSize;
+    const int NW = 4;
+    const int max_bps = NW * kMaxWarpBlocks;
     int bps = bps_req;
     if (bps <= 0) {
         const int sms = sm_count();
         if (sms <= 0) return cudaErrorNoDevice;
-        // aim for about two waves of 3 resident CTAs per SM, at least one block per warp
+        int occ = 0;
+        cudaError_t e = D == 64 ? decode_setup<64>(&occ) : decode_setup<128>(&occ);
+        if (e != cudaSuccess) return e;
+        // one wave: every CTA resident at once; at least one block per warp
         const int64_t work = static_cast<int64_t>(B) * Hkv * nblk;
-        const int64_t target = static_cast<int64_t>(sms) * 6;
-        int64_t want = (work + target - 1) / target;
-        want = std::max<int64_t>(want, kWarps);
-        want = (want + kWarps - 1) / kWarps * kWarps;
-        bps = static_cast<int>(std::min<int64_t>(want, nblk));
+        const int64_t slots = static_cast<int64_t>(sms) * occ;
+        int64_t want = (work + slots - 1) / slots;
+        want = std::max<int64_t>(want, NW);
+        want = (want + NW - 1) / NW * NW;
+        bps = static_cast<int>(std::min<int64_t>(std::min<int64_t>(want, max_bps), std::max(nblk, 1)));
     }
+    if (bps > max_bps) bps = max_bps;
     const int nsplit = (nblk + bps - 1) / bps;
     plan->blocks_per_split = bps;
     plan->num_splits = nsplit;
-    plan->workspace_bytes = nsplit > 1 ? static_cast<size_t>(B) * Hq * nsplit * (2 + D) * sizeof(float) : 0;
+    plan->workspace_bytes =
+        nsplit > 1 ? ticket_bytes(B, Hkv) + static_cast<size_t>(B) * Hq * nsplit * (2 + D) * sizeof(float) : 0;
     return cudaSuccess;
 }
 
@@ -399,12 +547,12 @@ static EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
-        void* p = nullptr;
+        void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
 }
@@ -424,32 +572,49 @@ static cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <typename Kern, typename... Args>
+static cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D>
 static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
-    using Geo = DecodeGeom<D>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Geo::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    using C = DecodeCfg<D>;
+    cudaError_t e = decode_setup<D>(nullptr);
+    if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
     CUtensorMap tmK, tmV;
-    cudaError_t e = make_tile_map(&tmK, a.k_cache, D, rows);
+    e = make_tile_map(&tmK, a.k_cache, D, rows);
     if (e != cudaSuccess) return e;
     e = make_tile_map(&tmV, a.v_cache, D, rows);
     if (e != cudaSuccess) return e;
 
     DecodeKernelParams p;
     p.q = a.q;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_cache = const_cast<__half*>(a.k_cache);
+    p.v_cache = const_cast<__half*>(a.v_cache);
     p.block_table = a.block_table;
     p.context_lens = a.context_lens;
     p.out = a.out;
-    p.part_ml = static_cast<float*>(a.workspace);
-    p.part_acc = plan.num_splits > 1
-                     ? static_cast<float*>(a.workspace) + static_cast<size_t>(a.B) * a.Hq * plan.num_splits * 2
-                     : nullptr;
+    const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;
+    p.tickets = plan.num_splits > 1 ? static_cast<int*>(a.workspace) : nullptr;
+    p.part_ml = plan.num_splits > 1
+                    ? reinterpret_cast<float*>(static_cast<char*>(a.workspace) + ticket_bytes(a.B, a.Hkv))
+                    : nullptr;
+    p.part_acc = plan.num_splits > 1 ? p.part_ml + nrow * 2 : nullptr;
     p.err = a.err;
     p.max_blocks = a.max_blocks;
     p.num_blocks = a.num_blocks;
@@ -461,18 +626,18 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.bps = plan.blocks_per_split;
     p.nsplit = plan.num_splits;
     p.out_f32 = a.out_f32;
+    p.inline_combine = plan.num_splits <= kMaxInlineSplits ? 1 : 0;
     p.scale_log2 = a.scale * kLog2e;
 
+    const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
-    paged_decode_kernel<D><<<grid, kWarps * 32, Geo::kSmemBytes, stream>>>(tmK, tmV, p);
-    e = cudaGetLastError();
+    e = launch(paged_decode_kernel<D>, grid, dim3(C::kWarps * 32), C::kSmemBytes, stream, pdl, tmK, tmV, p);
     if (e != cudaSuccess) return e;
-    if (plan.num_splits > 1) {
+    if (plan.num_splits > 1 && !p.inline_combine) {
         dim3 cgrid(a.Hq, a.B);
-        paged_decode_combine_kernel<D><<<cgrid, 256, 0, stream>>>(p.part_ml, p.part_acc, a.context_lens, a.out,
-                                                                  a.Hq, plan.num_splits, plan.blocks_per_split,
-                                                                  a.max_blocks, a.max_context_len, a.out_f32);
-        e = cudaGetLastError();
+        e = launch(paged_decode_combine_kernel<D>, cgrid, dim3(256), 0, stream, true,
+                   static_cast<const float*>(p.part_ml), static_cast<const float*>(p.part_acc), a.context_lens,
+                   a.out, a.Hq, plan.num_splits, plan.blocks_per_split, a.max_blocks, a.max_context_len, a.out_f32);
     }
     return e;
 }
@@ -488,5 +653,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
         default: return cudaErrorInvalidValue;
     }
 }
+
+void set_launch_overlap(int on) { g_launch_overlap.store(on ? 1 : 0); }
+int launch_overlap() { return g_launch_overlap.load(); }
 
 }  // namespace kvc

@@ -30,6 +30,8 @@ cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_context_len, int 
                         DecodePlan* plan);
 struct DecodeArgs {
     const __half* q;
+    const __half* k_new;  // null: attention only; else the step's new K/V rows [B][Hkv][D]
+    const __half* v_new;
     const __half* k_cache;
     const __half* v_cache;
     int num_blocks;
@@ -47,6 +49,9 @@ struct DecodeArgs {
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// process-wide: launch decode kernels as programmatic dependents of the previous kernel
+void set_launch_overlap(int on);
+int launch_overlap();
 
 // ---- prefill (prefill.cu) ----------------------------------------------------
 struct PrefillArgs {

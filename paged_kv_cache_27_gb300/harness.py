@@ -12,8 +12,8 @@ import numpy as np
 import torch
 
 from . import (KvcConfig, kv_append, kv_block_alloc, kv_block_release, kv_block_share, kv_cache_create,
-               kv_cache_destroy, kv_copy_blocks, kv_slot_mapping, kv_step_prepare, paged_decode_attention,
-               paged_decode_plan, paged_decode_workspace_init, prefill_attention)
+               kv_cache_destroy, kv_copy_blocks, kv_slot_mapping, kv_step_prepare, paged_decode_append_attention,
+               paged_decode_attention, paged_decode_plan, paged_decode_workspace_init, prefill_attention)
 
 F16_NAN = 0x7E00  # a quiet-NaN bit pattern used to poison cache slots nobody owns
 
@@ -75,11 +75,41 @@ class DecodeSession:
                                self.context_lens, self.wl.scale, self.out[layer], self.workspace, self.max_ctx,
                                self.blocks_per_split, stream=stream)
 
-    def step(self, stream=None):
-        """One decode step: for every layer, append the new token's K/V, then attend."""
+    def decode_append(self, layer, stream=None):
+        paged_decode_append_attention(self.q[layer], self.k_new[layer], self.v_new[layer], self.k_pool[layer],
+                                      self.v_pool[layer], self.block_table, self.context_lens, self.wl.scale,
+                                      self.out[layer], self.workspace, self.max_ctx, self.blocks_per_split,
+                                      stream=stream)
+
+    def step(self, stream=None, fused=False):
+        """One decode step: for every layer, append the new token's K/V, then attend.
+
+        fused=False: kv_append then paged_decode_attention; fused=True: paged_decode_append_attention."""
         for layer in range(self.wl.L):
-            self.append(layer, stream)
-            self.decode(layer, stream)
+            if fused:
+                self.decode_append(layer, stream)
+            else:
+                self.append(layer, stream)
+                self.decode(layer, stream)
+
+    def capture(self, fused=True, decode_only=False, stream=None):
+        """CUDA graph of one step (or of the 24 decode calls alone); eager warm-up first."""
+        stream = stream or torch.cuda.Stream(self.device)
+        with torch.cuda.stream(stream):
+            self._graph_body(fused, decode_only)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self._graph_body(fused, decode_only)
+        torch.cuda.synchronize(self.device)
+        return graph
+
+    def _graph_body(self, fused, decode_only):
+        if decode_only:
+            for layer in range(self.wl.L):
+                self.decode_append(layer) if fused else self.decode(layer)
+        else:
+            self.step(fused=fused)
 
     def close(self):
         if self.h:

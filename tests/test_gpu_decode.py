@@ -17,16 +17,28 @@ def kvc():
     return m
 
 
-def run_session(kvc, wl, out_dtype=torch.float32, bps=0):
+def run_session(kvc, wl, out_dtype=torch.float32, bps=0, fused=False, graph=False, overlap=False):
+    """One decode step: eager, or replayed from a CUDA graph (with launch overlap) as the benchmark runs it."""
     from paged_kv_cache_27_gb300.harness import DecodeSession
     s = DecodeSession(wl, out_dtype=out_dtype, blocks_per_split=bps).fill()
-    s.step()
-    torch.cuda.synchronize()
+    kvc.kvc_set_launch_overlap(overlap)
+    try:
+        if graph:
+            g = s.capture(fused=fused)
+            s.out.fill_(float("nan"))
+            g.replay()
+            g.replay()
+        else:
+            s.step(fused=fused)
+        torch.cuda.synchronize()
+    finally:
+        kvc.kvc_set_launch_overlap(False)
     return s
 
 
-def check_workload(kvc, wl, out_dtype=torch.float32, bps=0, layers=None, cache_bits=True):
-    s = run_session(kvc, wl, out_dtype, bps)
+def check_workload(kvc, wl, out_dtype=torch.float32, bps=0, layers=None, cache_bits=True, fused=False, graph=False,
+                   overlap=False):
+    s = run_session(kvc, wl, out_dtype, bps, fused, graph, overlap)
     assert kvc.kvc_device_error_flags(clear=True) == 0
     errs = []
     for layer in (range(wl.L) if layers is None else layers):
@@ -63,35 +75,59 @@ def test_config1_single_sequence(kvc):
     (2, 16, 2, 128, [300, 1500]),
     (9, 14, 2, 64, [4096, 1, 77, 2048, 3000, 16, 15, 999, 1024]),
 ])
-def test_small_sweep(kvc, B, Hq, Hkv, D, ctx):
+@pytest.mark.parametrize("fused", [False, True])
+def test_small_sweep(kvc, B, Hq, Hkv, D, ctx, fused):
     wl = workloads.small_decode(B * 100 + D, B=B, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, L=2)
     for dt in (torch.float32, torch.float16):
-        check_workload(kvc, wl, dt)
+        check_workload(kvc, wl, dt, fused=fused)
 
 
-@pytest.mark.parametrize("bps", [1, 2, 3, 4, 7, 8, 64])
-def test_forced_split_sizes(kvc, bps):
+@pytest.mark.parametrize("bps", [1, 2, 3, 4, 7, 8, 64, 128])
+@pytest.mark.parametrize("fused", [False, True])
+def test_forced_split_sizes(kvc, bps, fused):
+    """1 block per split (129 splits: combine kernel) up to 128 (a single split): both merge paths."""
     wl = workloads.small_decode(77, B=4, Hq=14, Hkv=2, D=64, ctx=[1, 300, 1025, 2048], peak_frac=0.01)
-    check_workload(kvc, wl, torch.float32, bps=bps)
+    check_workload(kvc, wl, torch.float32, bps=bps, fused=fused)
 
 
-def test_config2_full(kvc):
-    """24 layers x 32 sequences x context 2048, 14 q / 2 KV heads: every layer against the oracle."""
+def test_config2_full_as_benchmarked(kvc):
+    """24 layers x 32 sequences x context 2048, 14 q / 2 KV heads, in the benchmark's launch configuration
+    (fused append + decode, CUDA graph, launch overlap): every layer and the whole cache against the oracle."""
     wl = workloads.config2()
-    err = check_workload(kvc, wl, torch.float32, layers=range(wl.L), cache_bits=True)
+    err = check_workload(kvc, wl, torch.float16, layers=range(wl.L), cache_bits=True, fused=True, graph=True,
+                         overlap=True)
     assert err < 2e-3
 
 
-def test_config2_fp16_out_sampled_layers(kvc):
+def test_config2_fp32_out_unfused_sampled_layers(kvc):
     wl = workloads.config2()
-    check_workload(kvc, wl, torch.float16, layers=[0, 11, 23], cache_bits=False)
+    check_workload(kvc, wl, torch.float32, layers=[0, 11, 23], cache_bits=False)
 
 
 @pytest.mark.parametrize("B", [1, 4, 16])
 @pytest.mark.parametrize("ctx", [4096, 16384, 65536, 131072])
 def test_config4_long_context(kvc, B, ctx):
     wl = workloads.config4(B, ctx)
-    check_workload(kvc, wl, torch.float32, cache_bits=(B * ctx <= 4 * 65536))
+    check_workload(kvc, wl, torch.float32, cache_bits=(B * ctx <= 4 * 65536), fused=True, graph=True, overlap=True)
+
+
+def test_workspace_reuse_across_context_lengths(kvc):
+    """Growing contexts change the split count; one workspace serves every step (counters stay at zero)."""
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    base = workloads.small_decode(21, B=6, Hq=14, Hkv=2, D=64, ctx=[3000, 2000, 1000, 500, 4000, 64])
+    s = DecodeSession(base).fill()
+    ws = s.workspace
+    for ctx_scale in (0.25, 0.5, 1.0, 0.1, 1.0):
+        wl = workloads.small_decode(21, B=6, Hq=14, Hkv=2, D=64,
+                                    ctx=[max(1, int(c * ctx_scale)) for c in base.ctx])
+        s2 = DecodeSession(wl).fill()
+        s2.workspace = ws  # shared workspace, same B and Hkv
+        s2.step(fused=True)
+        torch.cuda.synchronize()
+        ref, _, _ = opaging.decode_step(wl, 0)
+        check_attention(s2.out[0], ref, f"ctx scale {ctx_scale}")
+        s2.close()
+    s.close()
 
 
 def test_results_invariant_to_physical_placement(kvc):
