@@ -165,16 +165,16 @@ kvc_status kv_append(kvc_handle h, int layer, const void* k_new, const void* v_n
                      const int64_t* slot_mapping, int n, void* stream);
 
 /* Split plan of paged_decode_attention for these sizes on the current
- * device: the number of context splits, the blocks per split and the
- * workspace bytes it needs.  blocks_per_split = 0 picks automatically. */
+ * device: the number of context splits (CTAs along the context, a whole
+ * number of thread-block clusters of up to 8), the blocks per split and the
+ * workspace bytes it needs (zero unless the longest context needs more than
+ * one cluster).  blocks_per_split = 0 picks automatically. */
 kvc_status paged_decode_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                              int blocks_per_split, int* num_splits, int* blocks_per_split_out,
                              size_t* workspace_bytes);
-/* Zero-fill a workspace before its first use (cudaMemsetAsync).  Every
- * decode call leaves its split counters at zero again, so a workspace can be
- * reused by later calls with the same B and Hkv (any context length); zero it
- * again before reusing it for another B or Hkv.  Calls that share a workspace
- * must not overlap in time (same stream, or ordered by events). */
+/* Zero-fill a workspace (cudaMemsetAsync).  Optional: the decode kernels
+ * write every workspace word they read.  Calls that share a workspace must not
+ * overlap in time (same stream, or ordered by events). */
 kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /* Paged GQA decode attention for one token per sequence:
@@ -187,11 +187,12 @@ kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stre
  *   block_table  device int32 [B][max_blocks]
  *   context_lens device int32 [B], 1 <= ctx <= min(max_blocks*bs, max_context_len)
  *   out          device [B][Hq][D], out_dtype KVC_F16 or KVC_F32
- *   workspace    device, >= paged_decode_plan(...)'s bytes, zero-filled once
+ *   workspace    device, >= paged_decode_plan(...)'s bytes (may be NULL when that is 0)
  * The context of each sequence is cut into splits of blocks_per_split blocks;
  * each (sequence, KV head, split) is one CTA that keeps the running max and
- * exp-sum per query head; the last split to finish merges the partials with
- * the rescaling rule of the FlashAttention article.
+ * exp-sum per query head; the splits merge with the rescaling rule of the
+ * FlashAttention article, on chip within a thread-block cluster and, for
+ * contexts longer than one cluster covers, through the workspace.
  * Preconditions: Hq % Hkv == 0, Hq/Hkv <= 8, head_dim in {64, 128},
  * block_size == 16; 16-byte aligned pointers. */
 kvc_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
@@ -222,6 +223,14 @@ kvc_status paged_decode_append_attention(const void* q, const void* k_new, const
  * before a decode call must not write its block table, context lengths or
  * the cache rows the call reads (other than through this call's append). */
 kvc_status kvc_set_launch_overlap(int on);
+
+/* Per-CTA timeline of decode launches (builds with -DKVC_TRACE=1 only;
+ * otherwise KVC_ERR_UNSUPPORTED).  Each 48-byte record holds five global-timer
+ * stamps in ns (CTA start, K/V copies issued, dependency wait passed, main
+ * loop done, exit), then uint32 launch number, SM id, blockIdx.x and
+ * (blockIdx.y << 16 | blockIdx.z).  Copies up to `capacity` records into host
+ * memory; `clear` resets the device buffer.  Synchronous. */
+kvc_status kvc_trace_read(void* records, int capacity, int* count, int clear);
 
 /* Varlen packed prefill (xformers article parts 4-5): for every segment s
  * (rows cu_seqlens[s] .. cu_seqlens[s+1]-1) and query head h,

@@ -28,7 +28,7 @@ __all__ = [
     "kv_block_release", "kv_block_refcount", "kv_block_num_free", "kv_cache_utilisation",
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
-    "paged_decode_append_attention", "kvc_set_launch_overlap",
+    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
     "prefill_attention", "DEVERR",
 ]
 
@@ -106,6 +106,7 @@ def _load():
         "paged_decode_append_attention": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
                                               P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
+        "kvc_trace_read": (I, [P, I, PI, I]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
     }
     for name, (res, args) in sig.items():
@@ -166,6 +167,17 @@ def kvc_set_checked_mode(on: bool) -> None:
 def kvc_set_launch_overlap(on: bool) -> None:
     """Launch decode kernels as programmatic dependents of the previous kernel (see include/kvc.h)."""
     _check(_lib.kvc_set_launch_overlap(int(bool(on))), "kvc_set_launch_overlap")
+
+
+TRACE_DTYPE = np.dtype([("t", "<u8", (5,)), ("seq", "<u4"), ("smid", "<u4"), ("x", "<u4"), ("yz", "<u4")])
+
+
+def kvc_trace_read(capacity: int = 1 << 16, clear: bool = True) -> np.ndarray:
+    """Decode-kernel timeline records (library built with -DKVC_TRACE=1)."""
+    buf = np.zeros(capacity, dtype=TRACE_DTYPE)
+    n = ctypes.c_int(0)
+    _check(_lib.kvc_trace_read(_np_ptr(buf), capacity, ctypes.byref(n), int(bool(clear))), "kvc_trace_read")
+    return buf[:n.value]
 
 
 def kvc_device_error_flags(clear: bool = False) -> int:

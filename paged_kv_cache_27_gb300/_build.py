@@ -33,12 +33,18 @@ def _cuda_lib_dir(nv: str) -> str:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile libkvc.so; KVC_NVCC_FLAGS (environment) adds nvcc flags, e.g. -D tuning knobs."""
+    extra_flags = list(extra_flags) + os.environ.get("KVC_NVCC_FLAGS", "").split()
     os.makedirs(OUT_DIR, exist_ok=True)
+    stamp = LIB + ".flags"
+    flags_id = " ".join(extra_flags)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(HERE), "include", "kvc.h"))
-    if not force and os.path.exists(LIB):
+    if not force and os.path.exists(LIB) and os.path.exists(stamp):
         newest = max(os.path.getmtime(d) for d in deps)
-        if os.path.getmtime(LIB) >= newest:
+        with open(stamp) as f:
+            same_flags = f.read() == flags_id
+        if same_flags and os.path.getmtime(LIB) >= newest:
             return LIB
     nv = nvcc()
     objdir = os.path.join(OUT_DIR, "obj")
@@ -63,6 +69,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(flags_id)
     return LIB
 
 

@@ -359,6 +359,14 @@ kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stre
     return KVC_OK;
 }
 
+kvc_status kvc_trace_read(void* records, int capacity, int* count, int clear) {
+    if (!count || capacity < 0 || (capacity > 0 && !records)) return fail(KVC_ERR_INVALID, "bad arguments");
+    cudaError_t e = kvc::trace_read(records, capacity, count, clear);
+    if (e == cudaErrorNotSupported) return fail(KVC_ERR_UNSUPPORTED, "library built without -DKVC_TRACE=1");
+    if (e != cudaSuccess) return cuda_fail(e, "trace read");
+    return KVC_OK;
+}
+
 kvc_status kvc_set_launch_overlap(int on) {
     kvc::set_launch_overlap(on);
     return KVC_OK;

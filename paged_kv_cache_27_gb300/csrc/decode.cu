@@ -13,28 +13,30 @@
 // the gustavoai.dev page) and enter the attention directly.
 //
 // Design (GB300):
-//  * one CTA per (context split, KV head, sequence); the grid is sized from
-//    the measured occupancy so that all CTAs are resident at once;
+//  * one CTA per (context split, KV head, sequence), the grid sized from the
+//    measured occupancy so that every CTA is resident at once; the splits of
+//    one (sequence, KV head) form a thread-block cluster (up to 8 CTAs);
 //  * the G <= 8 query heads of a KV head are the rows of one m16n8k16 tile, so
 //    every K/V tile fetched from HBM serves the whole group;
-//  * each warp owns a ring of kStages stages; lane 0 issues the K and V tile
-//    loads (16 tokens x D fp16 each) with 2-D TMA and the 128-byte swizzle so
-//    that the ldmatrix reads are bank-conflict free; the warp waits on the
-//    stage's mbarrier (bounded wait, error flag on expiry) and refills it;
-//  * the split's block-table entries are fetched in one coalesced load (one
-//    entry per lane) and passed by shuffles;
+//  * each warp owns a ring of stages; lane 0 issues the K and V tile loads
+//    (16 tokens x D fp16 each) with 2-D TMA and the 128-byte swizzle so that
+//    the ldmatrix reads are bank-conflict free; the warp waits on the stage's
+//    mbarrier (bounded wait, error flag on expiry) and refills it;
+//  * the block-table entries are fetched in one coalesced load (one entry per
+//    lane) together with the context length, and passed by shuffles;
 //  * S = Q K^T and O += P V on the tensor cores (mma.sync, fp16 in, fp32
 //    accumulate); P is split into an fp16 high part and an fp16 residual so
 //    the P V product keeps ~fp32 accuracy; online softmax in fp32, base 2;
-//  * warps of a CTA merge through shared memory; splits of a sequence merge
-//    in the last CTA to finish (atomic ticket, no waiting) or, for many
-//    splits, in a separate combine kernel; both use the rule of the
-//    FlashAttention article ("Was ist der mathematische Aspekt von Softmax?"):
-//    partial (m, l, acc) are rescaled by 2^(m - M), M the global maximum;
-//  * with launch overlap on, the kernel is launched as a programmatic
-//    dependent of the previous kernel: it fetches block tables, context lengths
-//    and cached K/V before waiting for that kernel, and reads q, k_new, v_new
-//    (and writes anything) only after.
+//  * merging follows the FlashAttention article ("Was ist der mathematische
+//    Aspekt von Softmax?"): partial (m, l, acc) are rescaled by 2^(m - M), M
+//    the global maximum.  Warps merge through shared memory, the CTAs of a
+//    cluster through distributed shared memory (no global round trip); only
+//    contexts longer than a cluster's reach write per-cluster partials, which
+//    a small combine kernel merges;
+//  * with launch overlap on, the kernel is a programmatic dependent of the
+//    previous kernel: it fetches block tables, context lengths and cached K/V
+//    before waiting for that kernel, and reads q, k_new, v_new (and writes
+//    anything) only after.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -47,27 +49,48 @@
 
 namespace kvc {
 
+// Tuning knobs (compile-time; the defaults are the measured best on GB300).
+#ifndef KVC_DEC_WARPS64
+#define KVC_DEC_WARPS64 8
+#endif
+#ifndef KVC_DEC_STAGES64
+#define KVC_DEC_STAGES64 2
+#endif
+#ifndef KVC_DEC_WARPS128
+#define KVC_DEC_WARPS128 4
+#endif
+#ifndef KVC_DEC_STAGES128
+#define KVC_DEC_STAGES128 2
+#endif
+#ifndef KVC_DEC_MAX_CLUSTER
+#define KVC_DEC_MAX_CLUSTER 8
+#endif
+#ifndef KVC_DEC_EARLY_TRIGGER  // let the next kernel launch as soon as every CTA of this one has started
+#define KVC_DEC_EARLY_TRIGGER 1
+#endif
+
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxWarpBlocks = 32;    // blocks per warp per split (one table entry per lane)
-constexpr int kMaxInlineSplits = 32;  // splits merged by the last CTA; more go to the combine kernel
+constexpr int kMaxWarpBlocks = 32;  // blocks per warp per split (one table entry per lane)
+constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
 
 std::atomic<int> g_launch_overlap{0};
 
 template <int D>
 struct DecodeCfg {
-    static constexpr int kWarps = 4;
-    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
+    static constexpr int kStages = D == 64 ? KVC_DEC_STAGES64 : KVC_DEC_STAGES128;
+    static constexpr int kThreads = kWarps * 32;
     static constexpr int kTileBytes = kBlockSize * D * 2;  // one 16 x D fp16 tile
     static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
     static constexpr int kWarpRingBytes = kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kMiscBytes = 16 + 8 * kMaxInlineSplits * 4;  // ticket flag + combine weights
-    static constexpr int kSmemBytes = kRingBytes + kBarBytes + kMiscBytes + 1024;  // + alignment slack
-    static constexpr int kMergeStride = D + 4;                                      // floats per merged row
+    static constexpr int kStateBytes = 8 * (D + 2) * 4;  // the CTA's merged (m, l, acc) for 8 rows
+    static constexpr int kSmemBytes = kRingBytes + kBarBytes + kStateBytes + 1024;  // + alignment slack
+    static constexpr int kMergeStride = D + 4;                                       // floats per parked row
     static constexpr int kMaxBps = kWarps * kMaxWarpBlocks;
-    static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "merge area must fit a warp ring");
+    static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
 };
 
 struct DecodeKernelParams {
@@ -79,13 +102,55 @@ struct DecodeKernelParams {
     const int32_t* block_table;
     const int32_t* context_lens;
     void* out;
-    float* part_ml;   // [B][Hq][nsplit][2] (m, l) in base-2 units
-    float* part_acc;  // [B][Hq][nsplit][D]
-    int* tickets;     // [B][Hkv], zero between calls
+    float* part_ml;   // [B][Hq][nparts][2] (m, l) in base-2 units, one part per cluster
+    float* part_acc;  // [B][Hq][nparts][D]
     unsigned* err;
-    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx, bps, nsplit, out_f32, inline_combine;
+    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx, bps, csize, nparts, out_f32;
     float scale_log2;
+    unsigned trace_seq;  // launch counter, used by the optional trace only
 };
+
+// ---- optional per-CTA timeline trace (build with -DKVC_TRACE=1) -----------------------------
+// Each CTA records the global timer at: start, TMA issued, dependency wait passed, main loop done,
+// exit; plus its SM and coordinates.  kvc_trace_read() copies the records out.
+#ifndef KVC_TRACE
+#define KVC_TRACE 0
+#endif
+#if KVC_TRACE
+struct TraceRec {
+    unsigned long long t[5];
+    unsigned seq, smid, x, yz;
+};
+constexpr int kTraceCap = 1 << 16;
+__device__ TraceRec g_trace[kTraceCap];
+__device__ unsigned g_trace_n;
+#define KVC_TRACE_MARK(i) \
+    if (threadIdx.x == 0) tr_t[i] = global_timer_ns()
+#define KVC_TRACE_END()                                                    \
+    do {                                                                   \
+        if (threadIdx.x == 0) {                                            \
+            tr_t[4] = global_timer_ns();                                   \
+            const unsigned k = atomicAdd(&g_trace_n, 1u);                  \
+            if (k < kTraceCap) {                                           \
+                TraceRec& r = g_trace[k];                                  \
+                for (int q_ = 0; q_ < 5; ++q_) r.t[q_] = tr_t[q_];         \
+                unsigned sm_;                                              \
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));           \
+                r.seq = p.trace_seq;                                       \
+                r.smid = sm_;                                              \
+                r.x = blockIdx.x;                                          \
+                r.yz = (blockIdx.y << 16) | blockIdx.z;                    \
+            }                                                              \
+        }                                                                  \
+    } while (0)
+#else
+#define KVC_TRACE_MARK(i) \
+    do {                  \
+    } while (0)
+#define KVC_TRACE_END() \
+    do {                \
+    } while (0)
+#endif
 
 // byte offset of 16-byte chunk `chunk` (8 fp16 columns) of row `row` inside a
 // tile loaded as boxes of 16 rows x 64 columns with the 128-byte swizzle.
@@ -100,12 +165,29 @@ __device__ __forceinline__ void store_out(void* out, int out_f32, int64_t idx, f
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
-__device__ __forceinline__ int split_count(int ctx, int bps) {
-    return ((ctx + kBlockSize - 1) / kBlockSize + bps - 1) / bps;
+// ---- thread-block cluster helpers ------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 template <int D>
-__global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
+__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeKernelParams p) {
     using C = DecodeCfg<D>;
@@ -113,14 +195,30 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
-    int* s_flag = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes);
-    float* s_w = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + 16);  // [8][kMaxInlineSplits]
+    // the CTA's merged state: m[8], l[8], acc[8][D]
+    float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
+    float* s_l = s_m + 8;
+    float* s_acc = s_m + 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+#if KVC_TRACE
+    unsigned long long tr_t[5] = {0, 0, 0, 0, 0};
+#endif
+#if KVC_DEC_EARLY_TRIGGER
+    grid_dependents_launch();
+#endif
+    KVC_TRACE_MARK(0);
 
+    // The block-table entries this lane would own if the split were full are fetched together with the
+    // context length (one round trip instead of two); indices stay inside the table row.
+    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+    const int j0 = split * p.bps;
+    const int jl = j0 + warp + lane * NW;
+    const int spec_blk = (warp + lane * NW < p.bps && jl < p.max_blocks) ? table[jl] : -1;
     const int ctx = p.context_lens[b];
+    // every CTA of a cluster sees the same (b, kvh): these exits are uniform over the cluster
     if (ctx < 1 || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
         grid_dependency_wait();
         if (split == 0) {
@@ -132,14 +230,14 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
     }
     const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
     const int nsplit = (nblk + p.bps - 1) / p.bps;
-    if (split >= nsplit) return;
-    const int j0 = split * p.bps;
-    const int nb_split = min(j0 + p.bps, nblk) - j0;
+    const int cs = p.csize;
+    const int cidx = split / cs;                       // this CTA's cluster along the context
+    const int nclus = (nsplit + cs - 1) / cs;          // clusters this sequence needs
+    if (cidx >= nclus) return;                         // the whole cluster is past the context
+    const bool active = split < nsplit;                // an inactive CTA only joins the cluster merge
+    const int nb_split = active ? min(j0 + p.bps, nblk) - j0 : 0;
     const int nb_w = warp < nb_split ? (nb_split - warp + NW - 1) / NW : 0;  // <= kMaxWarpBlocks
-
-    // this warp's block-table entries, one per lane
-    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-    const int my_blk = lane < nb_w ? table[j0 + warp + lane * NW] : -1;
+    const int my_blk = lane < nb_w ? spec_blk : -1;  // this warp's block-table entries, one per lane
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NW * ST; ++i) mbar_init(&bars[i], 1);
@@ -175,9 +273,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
         const int phys = __shfl_sync(0xffffffffu, my_blk, i);
         if (lane == 0 && i < nb_w) issue(i, phys);
     }
+    KVC_TRACE_MARK(1);
 
     // ---- everything below may read what the previous kernel wrote ----
     grid_dependency_wait();
+    KVC_TRACE_MARK(2);
 
     // query fragments (A operand, rows = the G heads of this KV head; rows >= G are zero)
     uint32_t qa[D / 16][2];
@@ -315,8 +415,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
         const int nxt = __shfl_sync(0xffffffffu, my_blk, (i + ST) & 31);
         if (lane == 0 && i + ST < nb_w) issue(i + ST, nxt);
     }
-    // the next kernel may start its prologue while this one finishes
-    grid_dependents_launch();
+#if !KVC_DEC_EARLY_TRIGGER
+    grid_dependents_launch();  // the next kernel may start its prologue while this one finishes
+#endif
+    KVC_TRACE_MARK(3);
     if (timed_out) {
         if (lane == 0) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
         // let copies still in flight land before the shared memory is reused
@@ -342,7 +444,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
         *reinterpret_cast<float2*>(wo + g * C::kMergeStride + nd * 8 + 2 * t4) = make_float2(o[nd][0], o[nd][1]);
     __syncthreads();
 
-    const bool direct = nsplit == 1;
+    const bool direct = nclus == 1 && cs == 1;  // a single CTA holds the whole context
     for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
         const int gg = e / D, d = e % D;
         float M = -INFINITY;
@@ -358,11 +460,55 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
                 O += r[16 + gg * C::kMergeStride + d] * wgt;
             }
         }
-        const int h = kvh * p.G + gg;
         if (direct) {
+            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d,
+                      L > 0.f ? O / L : 0.f);
+        } else {
+            if (d == 0) {
+                s_m[gg] = M;
+                s_l[gg] = L;
+            }
+            s_acc[gg * D + d] = O;
+        }
+    }
+    if (direct) {
+        KVC_TRACE_END();
+        return;
+    }
+
+    // ---- merge the CTAs of this cluster through distributed shared memory ----
+    if (cs > 1)
+        cluster_sync_all();  // every CTA's state is in its shared memory
+    else
+        __syncthreads();
+    const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int nthreads = cs * C::kThreads;
+    for (int e = rank * C::kThreads + threadIdx.x; e < p.G * D; e += nthreads) {
+        const int gg = e / D, d = e % D;
+        float mc[kMaxCluster], lc[kMaxCluster];
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+            if (c < cs) {
+                mc[c] = ld_cluster_f32(map_to_rank(s_m + gg, c));
+                lc[c] = ld_cluster_f32(map_to_rank(s_l + gg, c));
+                M = fmaxf(M, mc[c]);
+            }
+        }
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) {
+            if (c < cs && lc[c] > 0.f) {  // an inactive or empty CTA contributes nothing
+                const float w = ex2(mc[c] - M);
+                L += lc[c] * w;
+                O += ld_cluster_f32(map_to_rank(s_acc + gg * D + d, c)) * w;
+            }
+        }
+        const int h = kvh * p.G + gg;
+        if (nclus == 1) {
             store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, L > 0.f ? O / L : 0.f);
         } else {
-            const int64_t row = (static_cast<int64_t>(b) * p.Hq + h) * p.nsplit + split;
+            const int64_t row = (static_cast<int64_t>(b) * p.Hq + h) * p.nparts + cidx;
             if (d == 0) {
                 p.part_ml[row * 2 + 0] = M;
                 p.part_ml[row * 2 + 1] = L;
@@ -370,68 +516,20 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kWarps * 32)
             p.part_acc[row * D + d] = O;
         }
     }
-    if (direct || !p.inline_combine) return;
-
-    // ---- the last split of this (sequence, KV head) to finish merges all of them ----
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int t = atomicAdd(&p.tickets[b * p.Hkv + kvh], 1);
-        *s_flag = (t == nsplit - 1);
-    }
-    __syncthreads();
-    if (!*s_flag) return;
-    __threadfence();
-    // per head: global max M and the weights 2^(m_s - M) / L
-    {
-        const int gg = threadIdx.x >> 4, sub = threadIdx.x & 15;  // 16 threads per head, 8 heads
-        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nsplit;
-        float M = -INFINITY;
-        if (gg < p.G)
-            for (int s = sub; s < nsplit; s += 16) M = fmaxf(M, __ldcg(p.part_ml + (row0 + s) * 2));
-#pragma unroll
-        for (int off = 8; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        if (gg < p.G)
-            for (int s = sub; s < nsplit; s += 16) {
-                const float m = __ldcg(p.part_ml + (row0 + s) * 2), l = __ldcg(p.part_ml + (row0 + s) * 2 + 1);
-                const float w = m == -INFINITY ? 0.f : ex2(m - M);
-                s_w[gg * kMaxInlineSplits + s] = w;
-                L += l * w;
-            }
-#pragma unroll
-        for (int off = 8; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        __syncwarp();
-        if (gg < p.G)
-            for (int s = sub; s < nsplit; s += 16) s_w[gg * kMaxInlineSplits + s] *= (L > 0.f ? 1.f / L : 0.f);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < p.G * (D / 2); e += blockDim.x) {
-        const int gg = e / (D / 2), d = (e % (D / 2)) * 2;
-        const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nsplit;
-        float2 acc = make_float2(0.f, 0.f);
-        for (int s = 0; s < nsplit; ++s) {
-            const float w = s_w[gg * kMaxInlineSplits + s];
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_acc + (row0 + s) * D + d));
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-        }
-        const int64_t idx = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d;
-        store_out(p.out, p.out_f32, idx, acc.x);
-        store_out(p.out, p.out_f32, idx + 1, acc.y);
-    }
-    if (threadIdx.x == 0) p.tickets[b * p.Hkv + kvh] = 0;  // ready for the next call
+    if (cs > 1) cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+    KVC_TRACE_END();
 }
 
-// Merge the split partials of every (sequence, query head) when there are too
-// many splits for the last-CTA merge: 8 groups of 32 lanes walk the splits
-// with a running (M, L, acc), then the groups merge.
+// Merge the per-cluster partials of every (sequence, query head) for contexts
+// longer than one cluster covers: 8 groups of 32 lanes walk the parts with a
+// running (M, L, acc), then the groups merge.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* __restrict__ part_ml,
                                                                     const float* __restrict__ part_acc,
                                                                     const int32_t* __restrict__ context_lens,
-                                                                    void* out, int Hq, int nsplit_grid, int bps,
-                                                                    int max_blocks, int max_ctx, int out_f32) {
+                                                                    void* out, int Hq, int nparts_grid, int bps,
+                                                                    int csize, int max_blocks, int max_ctx,
+                                                                    int out_f32) {
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
     grid_dependency_wait();
@@ -439,17 +537,19 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctx = context_lens[b];
     if (ctx < 1 || ctx > max_blocks * kBlockSize || ctx > max_ctx) return;
-    const int nsplit = split_count(ctx, bps);
-    if (nsplit <= 1) return;
-    const int64_t row0 = (static_cast<int64_t>(b) * Hq + h) * nsplit_grid;
+    const int nsplit = ((ctx + kBlockSize - 1) / kBlockSize + bps - 1) / bps;
+    const int nparts = (nsplit + csize - 1) / csize;
+    if (nparts <= 1) return;  // the cluster wrote the output itself
+    const int64_t row0 = (static_cast<int64_t>(b) * Hq + h) * nparts_grid;
     float M = -INFINITY, L = 0.f, O[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) O[v] = 0.f;
-    for (int s = grp; s < nsplit; s += 8) {
+    for (int s = grp; s < nparts; s += 8) {
         const float m = part_ml[(row0 + s) * 2], l = part_ml[(row0 + s) * 2 + 1];
+        if (!(l > 0.f)) continue;
         const float Mn = fmaxf(M, m);
         const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
-        const float w = m == -INFINITY ? 0.f : ex2(m - Mn);
+        const float w = ex2(m - Mn);
         L = L * a + l * w;
 #pragma unroll
         for (int v = 0; v < V; ++v) O[v] = O[v] * a + part_acc[(row0 + s) * D + lane * V + v] * w;
@@ -468,7 +568,8 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
         for (int k = 0; k < 8; ++k) Mx = fmaxf(Mx, sM[k]);
         float Lt = 0.f, Ot = 0.f;
         for (int k = 0; k < 8; ++k) {
-            const float w = sM[k] == -INFINITY ? 0.f : ex2(sM[k] - Mx);  // groups that saw no split
+            if (!(sL[k] > 0.f)) continue;  // groups that saw no part
+            const float w = ex2(sM[k] - Mx);
             Lt += sL[k] * w;
             Ot += sO[k][d] * w;
         }
@@ -499,8 +600,10 @@ static cudaError_t decode_setup(int* ctas_per_sm) {
     static int occ = 0;
     std::call_once(once, [] {
         err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (err == cudaSuccess && kMaxCluster > 8)
+            err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (err == cudaSuccess)
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kWarps * 32,
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kThreads,
                                                                 C::kSmemBytes);
         if (err == cudaSuccess && occ < 1) err = cudaErrorInvalidConfiguration;
     });
@@ -508,37 +611,43 @@ static cudaError_t decode_setup(int* ctas_per_sm) {
     return err;
 }
 
-// workspace layout: [tickets: B*Hkv int32, padded to 256 B][m, l: B*Hq*nsplit*2 fp32][acc: B*Hq*nsplit*D fp32].
-// The tickets sit first so that calls with the same B and Hkv but another split
-// count (a longer context) find them where the previous call left them (zero).
-static size_t ticket_bytes(int B, int Hkv) { return (static_cast<size_t>(B) * Hkv * 4 + 255) / 256 * 256; }
-
-cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_ctx, int bps_req, DecodePlan* plan) {
-    const int nblk = (max_ctx + kBlockSize - 1) / kBlockSize;
-    const int NW = 4;
-    const int max_bps = NW * kMaxWarpBlocks;
+template <int D>
+static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bps_req, DecodePlan* plan) {
+    using C = DecodeCfg<D>;
+    const int nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
     int bps = bps_req;
     if (bps <= 0) {
         const int sms = sm_count();
         if (sms <= 0) return cudaErrorNoDevice;
         int occ = 0;
-        cudaError_t e = D == 64 ? decode_setup<64>(&occ) : decode_setup<128>(&occ);
+        cudaError_t e = decode_setup<D>(&occ);
         if (e != cudaSuccess) return e;
         // one wave: every CTA resident at once; at least one block per warp
         const int64_t work = static_cast<int64_t>(B) * Hkv * nblk;
         const int64_t slots = static_cast<int64_t>(sms) * occ;
         int64_t want = (work + slots - 1) / slots;
-        want = std::max<int64_t>(want, NW);
-        want = (want + NW - 1) / NW * NW;
-        bps = static_cast<int>(std::min<int64_t>(std::min<int64_t>(want, max_bps), std::max(nblk, 1)));
+        want = std::max<int64_t>(want, C::kWarps);
+        want = (want + C::kWarps - 1) / C::kWarps * C::kWarps;
+        bps = static_cast<int>(std::min<int64_t>(std::min<int64_t>(want, C::kMaxBps), nblk));
     }
-    if (bps > max_bps) bps = max_bps;
+    if (bps > C::kMaxBps) bps = C::kMaxBps;
     const int nsplit = (nblk + bps - 1) / bps;
+    const int cs = std::min(nsplit, kMaxCluster);
+    const int nparts = (nsplit + cs - 1) / cs;
     plan->blocks_per_split = bps;
-    plan->num_splits = nsplit;
-    plan->workspace_bytes =
-        nsplit > 1 ? ticket_bytes(B, Hkv) + static_cast<size_t>(B) * Hq * nsplit * (2 + D) * sizeof(float) : 0;
+    plan->cluster = cs;
+    plan->num_splits = nparts * cs;  // grid.x, a whole number of clusters
+    plan->num_parts = nparts;
+    plan->workspace_bytes = nparts > 1 ? static_cast<size_t>(B) * Hq * nparts * (2 + D) * sizeof(float) : 0;
     return cudaSuccess;
+}
+
+cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_ctx, int bps_req, DecodePlan* plan) {
+    switch (D) {
+        case 64: return plan_d<64>(B, Hq, Hkv, max_ctx, bps_req, plan);
+        case 128: return plan_d<128>(B, Hq, Hkv, max_ctx, bps_req, plan);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
@@ -574,17 +683,28 @@ static cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int6
 
 template <typename Kern, typename... Args>
 static cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
-                          Args... args) {
+                          unsigned cluster_x, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
@@ -609,12 +729,9 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.block_table = a.block_table;
     p.context_lens = a.context_lens;
     p.out = a.out;
-    const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;
-    p.tickets = plan.num_splits > 1 ? static_cast<int*>(a.workspace) : nullptr;
-    p.part_ml = plan.num_splits > 1
-                    ? reinterpret_cast<float*>(static_cast<char*>(a.workspace) + ticket_bytes(a.B, a.Hkv))
-                    : nullptr;
-    p.part_acc = plan.num_splits > 1 ? p.part_ml + nrow * 2 : nullptr;
+    const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
+    p.part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    p.part_acc = plan.num_parts > 1 ? p.part_ml + nrow * 2 : nullptr;
     p.err = a.err;
     p.max_blocks = a.max_blocks;
     p.num_blocks = a.num_blocks;
@@ -624,20 +741,24 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.G = a.Hq / a.Hkv;
     p.max_ctx = a.max_context_len;
     p.bps = plan.blocks_per_split;
-    p.nsplit = plan.num_splits;
+    p.csize = plan.cluster;
+    p.nparts = plan.num_parts;
     p.out_f32 = a.out_f32;
-    p.inline_combine = plan.num_splits <= kMaxInlineSplits ? 1 : 0;
     p.scale_log2 = a.scale * kLog2e;
+    static std::atomic<unsigned> launch_seq{0};
+    p.trace_seq = launch_seq.fetch_add(1);
 
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
-    e = launch(paged_decode_kernel<D>, grid, dim3(C::kWarps * 32), C::kSmemBytes, stream, pdl, tmK, tmV, p);
+    e = launch(paged_decode_kernel<D>, grid, dim3(C::kThreads), C::kSmemBytes, stream, pdl,
+               static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
-    if (plan.num_splits > 1 && !p.inline_combine) {
+    if (plan.num_parts > 1) {
         dim3 cgrid(a.Hq, a.B);
-        e = launch(paged_decode_combine_kernel<D>, cgrid, dim3(256), 0, stream, true,
+        e = launch(paged_decode_combine_kernel<D>, cgrid, dim3(256), 0, stream, true, 1u,
                    static_cast<const float*>(p.part_ml), static_cast<const float*>(p.part_acc), a.context_lens,
-                   a.out, a.Hq, plan.num_splits, plan.blocks_per_split, a.max_blocks, a.max_context_len, a.out_f32);
+                   a.out, a.Hq, plan.num_parts, plan.blocks_per_split, plan.cluster, a.max_blocks,
+                   a.max_context_len, a.out_f32);
     }
     return e;
 }
@@ -652,6 +773,29 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
         case 128: return launch_decode_d<128>(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t trace_read(void* host, int cap, int* n, int clear) {
+#if KVC_TRACE
+    unsigned cnt = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&cnt, g_trace_n, sizeof(cnt));
+    if (e != cudaSuccess) return e;
+    const int m = static_cast<int>(std::min<unsigned>(std::min<unsigned>(cnt, kTraceCap), static_cast<unsigned>(cap)));
+    if (m > 0) e = cudaMemcpyFromSymbol(host, g_trace, sizeof(TraceRec) * m);
+    if (e != cudaSuccess) return e;
+    *n = m;
+    if (clear) {
+        const unsigned z = 0;
+        e = cudaMemcpyToSymbol(g_trace_n, &z, sizeof(z));
+    }
+    return e;
+#else
+    (void)host;
+    (void)cap;
+    (void)clear;
+    *n = 0;
+    return cudaErrorNotSupported;
+#endif
 }
 
 void set_launch_overlap(int on) { g_launch_overlap.store(on ? 1 : 0); }

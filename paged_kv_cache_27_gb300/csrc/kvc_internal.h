@@ -22,8 +22,10 @@ cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __
 
 // ---- decode (decode.cu) ------------------------------------------------------
 struct DecodePlan {
-    int num_splits;        // grid.x: splits of the longest context
+    int num_splits;        // grid.x: splits of the longest context, rounded up to whole clusters
     int blocks_per_split;  // blocks of 16 tokens per split
+    int cluster;           // CTAs per thread-block cluster (the splits merged on chip)
+    int num_parts;         // clusters along the longest context; > 1 needs the workspace + combine kernel
     size_t workspace_bytes;
 };
 cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_context_len, int blocks_per_split,
@@ -51,6 +53,9 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // process-wide: launch decode kernels as programmatic dependents of the previous kernel
 void set_launch_overlap(int on);
+// copies up to `cap` trace records (48 bytes each) of the decode kernel; cudaErrorNotSupported
+// unless the library was built with -DKVC_TRACE=1
+cudaError_t trace_read(void* host, int cap, int* n, int clear);
 int launch_overlap();
 
 // ---- prefill (prefill.cu) ----------------------------------------------------

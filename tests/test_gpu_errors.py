@@ -75,11 +75,11 @@ def test_unchecked_bad_inputs_set_device_flags_without_faulting(kvc):
 
 
 def test_argument_errors(kvc):
-    wl = workloads.small_decode(3, B=2, Hq=4, Hkv=2, D=64, ctx=[20, 40])
+    wl = workloads.small_decode(3, B=2, Hq=4, Hkv=2, D=64, ctx=[20, 300])
     s = session(wl)
     small_ws = torch.empty(16, dtype=torch.uint8, device="cuda")
-    ns, bps, need = kvc.paged_decode_plan(2, 4, 2, 64, 40, blocks_per_split=1)
-    assert ns == 3 and need > 16
+    ns, bps, need = kvc.paged_decode_plan(2, 4, 2, 64, 300, blocks_per_split=1)
+    assert ns == 24 and bps == 1 and need > 16  # 19 splits -> 3 clusters of 8 -> partials in the workspace
     with pytest.raises(kvc.KvcError) as e:
         kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
                                    s.out[0], small_ws, s.max_ctx, blocks_per_split=1)
