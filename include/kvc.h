@@ -208,12 +208,18 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
  * position context_lens[b]-1 of the cache, i.e. slot
  * block_table[b][(ctx-1)/bs]*bs + (ctx-1)%bs, and take part in the attention
  * of that same call.  Bit-identical cache contents to kv_append with those
- * slots followed by paged_decode_attention. */
+ * slots followed by paged_decode_attention.
+ * k_next/v_next (both NULL, or both set): the pools of the layer the caller
+ * runs next ([num_blocks][Hkv][bs][D], same block tables).  The blocks this
+ * call reads are also requested from them into L2 (a prefetch hint, no
+ * effect on any result), so that the next layer's call finds its K/V in L2
+ * while HBM streams without a gap between layers. */
 kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
-                                         void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
-                                         const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim,
-                                         int block_size, int max_context_len, float scale, void* out, int out_dtype,
-                                         void* workspace, size_t workspace_bytes, int blocks_per_split, void* stream);
+                                         void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                         const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                         int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                         float scale, void* out, int out_dtype, void* workspace,
+                                         size_t workspace_bytes, int blocks_per_split, void* stream);
 
 /* Launch overlap (process-wide, default off).  When on, decode kernels are
  * launched as programmatic dependents of the kernel before them on the
@@ -225,10 +231,11 @@ kvc_status paged_decode_append_attention(const void* q, const void* k_new, const
 kvc_status kvc_set_launch_overlap(int on);
 
 /* Per-CTA timeline of decode launches (builds with -DKVC_TRACE=1 only;
- * otherwise KVC_ERR_UNSUPPORTED).  Each 48-byte record holds five global-timer
- * stamps in ns (CTA start, K/V copies issued, dependency wait passed, main
- * loop done, exit), then uint32 launch number, SM id, blockIdx.x and
- * (blockIdx.y << 16 | blockIdx.z).  Copies up to `capacity` records into host
+ * otherwise KVC_ERR_UNSUPPORTED).  Each 80-byte record holds eight global-timer
+ * stamps in ns (CTA start, first K/V copies issued, dependency wait passed,
+ * warp 0's main loop done, all warps done, CTA merge done, cluster merge
+ * reached (rank 0: every CTA of the cluster arrived), exit; 0 = not reached),
+ * then uint32 launch number, SM id, blockIdx.x and (blockIdx.y << 16 | blockIdx.z).  Copies up to `capacity` records into host
  * memory; `clear` resets the device buffer.  Synchronous. */
 kvc_status kvc_trace_read(void* records, int capacity, int* count, int clear);
 

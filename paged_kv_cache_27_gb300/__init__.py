@@ -103,8 +103,8 @@ def _load():
         "paged_decode_plan": (I, [I, I, I, I, I, I, I, PI, PI, PSZ]),
         "paged_decode_workspace_init": (I, [P, SZ, P]),
         "paged_decode_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ, I, P]),
-        "paged_decode_append_attention": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
-                                              P, SZ, I, P]),
+        "paged_decode_append_attention": (I, [P, P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
+                                              I, P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
         "kvc_trace_read": (I, [P, I, PI, I]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
@@ -169,7 +169,7 @@ def kvc_set_launch_overlap(on: bool) -> None:
     _check(_lib.kvc_set_launch_overlap(int(bool(on))), "kvc_set_launch_overlap")
 
 
-TRACE_DTYPE = np.dtype([("t", "<u8", (5,)), ("seq", "<u4"), ("smid", "<u4"), ("x", "<u4"), ("yz", "<u4")])
+TRACE_DTYPE = np.dtype([("t", "<u8", (8,)), ("seq", "<u4"), ("smid", "<u4"), ("x", "<u4"), ("yz", "<u4")])
 
 
 def kvc_trace_read(capacity: int = 1 << 16, clear: bool = True) -> np.ndarray:
@@ -358,8 +358,15 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
 def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                                   v_cache: torch.Tensor, block_table: torch.Tensor, context_lens: torch.Tensor,
                                   scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor],
-                                  max_context_len: int, blocks_per_split: int = 0, stream=None) -> None:
-    """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel)."""
+                                  max_context_len: int, blocks_per_split: int = 0, stream=None,
+                                  k_next: Optional[torch.Tensor] = None, v_next: Optional[torch.Tensor] = None) -> None:
+    """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel).
+
+    k_next/v_next: the next layer's pools (same shape as k_cache); this call's blocks of them are prefetched to L2."""
+    if (k_next is None) != (v_next is None):
+        raise ValueError("k_next and v_next: both or neither")
+    if k_next is not None and (k_next.shape != k_cache.shape or v_next.shape != k_cache.shape):
+        raise ValueError("k_next/v_next must have k_cache's shape")
     B, Hq, D = q.shape
     NB, Hkv, bs, Dk = k_cache.shape
     if Dk != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
@@ -375,7 +382,8 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_lib.paged_decode_append_attention(
         _dptr(q, torch.float16, "q"), _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
-        _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"), NB,
+        _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"),
+        _dptr(k_next, torch.float16, "k_next"), _dptr(v_next, torch.float16, "v_next"), NB,
         _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
         _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
         _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),

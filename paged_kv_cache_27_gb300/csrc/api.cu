@@ -373,38 +373,43 @@ kvc_status kvc_set_launch_overlap(int on) {
 }
 
 static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
-                                const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim, int block_size,
-                                int max_context_len, float scale, void* out, int out_dtype, void* workspace,
-                                size_t workspace_bytes, int blocks_per_split, void* stream);
+                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
+                                int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
+                                int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
+                                void* stream);
 
 kvc_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
                                   const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
                                   int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
                                   int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
                                   void* stream) {
-    return decode_common(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B,
-                         Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype, workspace,
-                         workspace_bytes, blocks_per_split, stream);
+    return decode_common(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table, max_blocks,
+                         context_lens, B, Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype,
+                         workspace, workspace_bytes, blocks_per_split, stream);
 }
 
 kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
-                                         void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
-                                         const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim,
-                                         int block_size, int max_context_len, float scale, void* out, int out_dtype,
-                                         void* workspace, size_t workspace_bytes, int blocks_per_split, void* stream) {
+                                         void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                         const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                         int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                         float scale, void* out, int out_dtype, void* workspace,
+                                         size_t workspace_bytes, int blocks_per_split, void* stream) {
     if (B > 0 && (!k_new || !v_new)) return fail(KVC_ERR_INVALID, "null k_new/v_new");
     if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVC_ERR_INVALID, "k_new/v_new must be 16-byte aligned");
-    return decode_common(q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B, Hq,
-                         Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype, workspace,
-                         workspace_bytes, blocks_per_split, stream);
+    if ((k_next == nullptr) != (v_next == nullptr)) return fail(KVC_ERR_INVALID, "k_next and v_next: both or neither");
+    if (!aligned16(k_next) || !aligned16(v_next)) return fail(KVC_ERR_INVALID, "k_next/v_next must be 16-byte aligned");
+    return decode_common(q, k_new, v_new, k_cache, v_cache, k_next, v_next, num_blocks, block_table, max_blocks,
+                         context_lens, B, Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype,
+                         workspace, workspace_bytes, blocks_per_split, stream);
 }
 
 static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
-                                const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim, int block_size,
-                                int max_context_len, float scale, void* out, int out_dtype, void* workspace,
-                                size_t workspace_bytes, int blocks_per_split, void* stream) {
+                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
+                                int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
+                                int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
+                                void* stream) {
     kvc_status s = check_decode_shape(B, Hq, Hkv, head_dim, block_size, max_context_len);
     if (s != KVC_OK) return s;
     if (B == 0) return KVC_OK;
@@ -437,6 +442,8 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
     a.q = static_cast<const __half*>(q);
     a.k_new = static_cast<const __half*>(k_new);
     a.v_new = static_cast<const __half*>(v_new);
+    a.k_next = static_cast<const __half*>(k_next);
+    a.v_next = static_cast<const __half*>(v_next);
     a.k_cache = static_cast<const __half*>(k_cache);
     a.v_cache = static_cast<const __half*>(v_cache);
     a.num_blocks = num_blocks;

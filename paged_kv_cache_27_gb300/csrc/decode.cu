@@ -13,18 +13,24 @@
 // the gustavoai.dev page) and enter the attention directly.
 //
 // Design (GB300):
-//  * one CTA per (context split, KV head, sequence), the grid sized from the
-//    measured occupancy so that every CTA is resident at once; the splits of
-//    one (sequence, KV head) form a thread-block cluster (up to 8 CTAs);
-//  * the G <= 8 query heads of a KV head are the rows of one m16n8k16 tile, so
-//    every K/V tile fetched from HBM serves the whole group;
+//  * a thread-block cluster of up to 8 CTAs per (range of the context, KV
+//    head, sequence), the grid sized from the measured occupancy so that every
+//    CTA is resident at once; a cluster usually covers a whole context;
+//  * inside a cluster, after a static first round, every warp takes the next
+//    block of the cluster's range from a counter in distributed shared memory
+//    (atom.shared::cluster), so that all warps of the cluster finish together;
+//  * the G <= 8 query heads of a KV head are the 8 columns of the m16n8k16
+//    tiles (S^T = K Q^T with the 16 tokens of a block as rows, then
+//    O^T += V^T P^T with 16 head dims as rows, P^T transposed in registers by
+//    movmatrix), so every K/V tile fetched from HBM serves the whole group and
+//    no tensor-core row is padding;
 //  * each warp owns a ring of stages; lane 0 issues the K and V tile loads
 //    (16 tokens x D fp16 each) with 2-D TMA and the 128-byte swizzle so that
 //    the ldmatrix reads are bank-conflict free; the warp waits on the stage's
 //    mbarrier (bounded wait, error flag on expiry) and refills it;
-//  * the block-table entries are fetched in one coalesced load (one entry per
-//    lane) together with the context length, and passed by shuffles;
-//  * S = Q K^T and O += P V on the tensor cores (mma.sync, fp16 in, fp32
+//  * the cluster's slice of the block table is copied to shared memory in one
+//    coalesced pass, in parallel with the context-length load;
+//  * the products run on the tensor cores (mma.sync, fp16 in, fp32
 //    accumulate); P is split into an fp16 high part and an fp16 residual so
 //    the P V product keeps ~fp32 accuracy; online softmax in fp32, base 2;
 //  * merging follows the FlashAttention article ("Was ist der mathematische
@@ -68,11 +74,20 @@ namespace kvc {
 #ifndef KVC_DEC_EARLY_TRIGGER  // let the next kernel launch as soon as every CTA of this one has started
 #define KVC_DEC_EARLY_TRIGGER 1
 #endif
+#ifndef KVC_DEC_MIN_CTAS  // resident CTAs per SM the register allocation must allow
+#define KVC_DEC_MIN_CTAS 1
+#endif
+#ifndef KVC_DEC_PREFETCH_AT  // when the next layer's blocks are requested into L2: 0 at start, 1 after the main loop
+#define KVC_DEC_PREFETCH_AT 1
+#endif
+#ifndef KVC_DEC_STEAL  // 1: warps take blocks from a cluster-wide counter; 0: fixed round-robin over the cluster's warps
+#define KVC_DEC_STEAL 1
+#endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxWarpBlocks = 32;  // blocks per warp per split (one table entry per lane)
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
+constexpr int kMaxClusterBlocks = 512;  // blocks one cluster covers at most (its table slice is in shared memory)
 
 std::atomic<int> g_launch_overlap{0};
 
@@ -86,10 +101,12 @@ struct DecodeCfg {
     static constexpr int kWarpRingBytes = kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kStateBytes = 8 * (D + 2) * 4;  // the CTA's merged (m, l, acc) for 8 rows
-    static constexpr int kSmemBytes = kRingBytes + kBarBytes + kStateBytes + 1024;  // + alignment slack
-    static constexpr int kMergeStride = D + 4;                                       // floats per parked row
-    static constexpr int kMaxBps = kWarps * kMaxWarpBlocks;
+    static constexpr int kStateBytes = (8 * (D + 2) + 16 * 8) * 4;  // merged (m, l, acc) of 8 heads + merge weights
+    static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice + block counter
+    static constexpr int kInboxBytes = kMaxCluster * kStateBytes;    // cluster rank 0: every CTA's merged state
+    static constexpr int kSmemBytes =
+        kRingBytes + kBarBytes + kStateBytes + kTableBytes + kInboxBytes + 1024;  // + alignment slack
+    static constexpr int kMergeStride = D + 4;  // floats per parked row
     static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
 };
 
@@ -99,41 +116,49 @@ struct DecodeKernelParams {
     const __half* v_new;
     __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
     __half* v_cache;
+    const __half* k_next;  // optional: the next layer's pools, whose blocks of this CTA are prefetched to L2
+    const __half* v_next;
     const int32_t* block_table;
     const int32_t* context_lens;
     void* out;
     float* part_ml;   // [B][Hq][nparts][2] (m, l) in base-2 units, one part per cluster
     float* part_acc;  // [B][Hq][nparts][D]
     unsigned* err;
-    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx, bps, csize, nparts, out_f32;
+    int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx;
+    int bpc;     // blocks per cluster: a cluster covers context blocks [c * bpc, (c + 1) * bpc)
+    int csize;   // CTAs per cluster
+    int nparts;  // clusters along the longest context (partials per (sequence, head) when > 1)
+    int out_f32;
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
 };
 
 // ---- optional per-CTA timeline trace (build with -DKVC_TRACE=1) -----------------------------
-// Each CTA records the global timer at: start, TMA issued, dependency wait passed, main loop done,
+// Each CTA records the global timer at: start, first copies issued, dependency wait passed, warp 0's
+// main loop done, all warps done, CTA merge done, cluster merge passed (rank 0: all CTAs arrived),
 // exit; plus its SM and coordinates.  kvc_trace_read() copies the records out.
 #ifndef KVC_TRACE
 #define KVC_TRACE 0
 #endif
 #if KVC_TRACE
+constexpr int kTraceStamps = 8;
 struct TraceRec {
-    unsigned long long t[5];
+    unsigned long long t[kTraceStamps];
     unsigned seq, smid, x, yz;
 };
 constexpr int kTraceCap = 1 << 16;
 __device__ TraceRec g_trace[kTraceCap];
 __device__ unsigned g_trace_n;
 #define KVC_TRACE_MARK(i) \
-    if (threadIdx.x == 0) tr_t[i] = global_timer_ns()
+    if (threadIdx.x == 0) s_trace_t[i] = global_timer_ns()
 #define KVC_TRACE_END()                                                    \
     do {                                                                   \
         if (threadIdx.x == 0) {                                            \
-            tr_t[4] = global_timer_ns();                                   \
+            s_trace_t[kTraceStamps - 1] = global_timer_ns();               \
             const unsigned k = atomicAdd(&g_trace_n, 1u);                  \
             if (k < kTraceCap) {                                           \
                 TraceRec& r = g_trace[k];                                  \
-                for (int q_ = 0; q_ < 5; ++q_) r.t[q_] = tr_t[q_];         \
+                for (int q_ = 0; q_ < kTraceStamps; ++q_) r.t[q_] = s_trace_t[q_]; \
                 unsigned sm_;                                              \
                 asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));           \
                 r.seq = p.trace_seq;                                       \
@@ -166,9 +191,6 @@ __device__ __forceinline__ void store_out(void* out, int out_f32, int64_t idx, f
 }
 
 // ---- thread-block cluster helpers ------------------------------------------------------------
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -180,14 +202,9 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 template <int D>
-__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeKernelParams p) {
     using C = DecodeCfg<D>;
@@ -199,29 +216,49 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
     float* s_l = s_m + 8;
     float* s_acc = s_m + 16;
+    float* s_wgt = s_acc + 8 * D;  // [16 sources][8 heads] merge weights
+    int* s_table = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
+    int* s_counter = s_table + kMaxClusterBlocks;  // next block to hand out (used in cluster rank 0)
+    // rank 0's inbox: slot c holds CTA c's merged state laid out like s_m/s_l/s_acc
+    float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes + C::kTableBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int cs = p.csize;
+    const int cidx = blockIdx.x / cs;                                    // this CTA's cluster along the context
+    const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;   // == blockIdx.x % cs
 #if KVC_TRACE
-    unsigned long long tr_t[5] = {0, 0, 0, 0, 0};
+    __shared__ unsigned long long s_trace_t[8];
+    if (threadIdx.x == 0)
+        for (int q_ = 0; q_ < 8; ++q_) s_trace_t[q_] = 0;
 #endif
 #if KVC_DEC_EARLY_TRIGGER
     grid_dependents_launch();
 #endif
     KVC_TRACE_MARK(0);
 
-    // The block-table entries this lane would own if the split were full are fetched together with the
-    // context length (one round trip instead of two); indices stay inside the table row.
+    // One round trip before the first copies: each warp's lane 0 fetches the table entries of its
+    // static first round and the context length together; the cluster's whole slice of the table
+    // (entries [cb0, cb0 + bpc), clipped to the row) goes to shared memory meanwhile, for the refills.
     const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-    const int j0 = split * p.bps;
-    const int jl = j0 + warp + lane * NW;
-    const int spec_blk = (warp + lane * NW < p.bps && jl < p.max_blocks) ? table[jl] : -1;
+    const int cb0 = cidx * p.bpc;
+    const int nwarps_cl = cs * NW;
+    const int gw = rank * NW + warp;  // warp index within the cluster
+    const int row_end = min(cb0 + p.bpc, p.max_blocks);
+    int first_phys[ST];
+#pragma unroll
+    for (int s = 0; s < ST; ++s) {
+        const int j = cb0 + gw + s * nwarps_cl;
+        first_phys[s] = (lane == 0 && j < row_end) ? table[j] : -1;
+    }
+    const int nload = max(0, row_end - cb0);
+    for (int t = threadIdx.x; t < nload; t += C::kThreads) s_table[t] = table[cb0 + t];
     const int ctx = p.context_lens[b];
     // every CTA of a cluster sees the same (b, kvh): these exits are uniform over the cluster
     if (ctx < 1 || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
         grid_dependency_wait();
-        if (split == 0) {
+        if (blockIdx.x == 0) {
             if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
             for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
                 store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
@@ -229,37 +266,23 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         return;
     }
     const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
-    const int nsplit = (nblk + p.bps - 1) / p.bps;
-    const int cs = p.csize;
-    const int cidx = split / cs;                       // this CTA's cluster along the context
-    const int nclus = (nsplit + cs - 1) / cs;          // clusters this sequence needs
-    if (cidx >= nclus) return;                         // the whole cluster is past the context
-    const bool active = split < nsplit;                // an inactive CTA only joins the cluster merge
-    const int nb_split = active ? min(j0 + p.bps, nblk) - j0 : 0;
-    const int nb_w = warp < nb_split ? (nb_split - warp + NW - 1) / NW : 0;  // <= kMaxWarpBlocks
-    const int my_blk = lane < nb_w ? spec_blk : -1;  // this warp's block-table entries, one per lane
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NW * ST; ++i) mbar_init(&bars[i], 1);
-        fence_barrier_init();
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
-    }
-    __syncthreads();
+    const int nclus = (nblk + p.bpc - 1) / p.bpc;  // clusters this sequence needs
+    if (cidx >= nclus) return;                     // the whole cluster is past the context
+    const int cb1 = min(cb0 + p.bpc, nblk);        // this cluster covers blocks [cb0, cb1)
 
     uint64_t* wbars = bars + warp * ST;
     uint8_t* wring = smem + warp * C::kWarpRingBytes;
     const uint64_t policy = l2_policy_evict_first();
 
-    // lane 0: the K and V tiles of this warp's i-th block into stage i % ST
-    auto issue = [&](int i, int phys) {
-        uint64_t* bar = &wbars[i % ST];
+    // lane 0: the K and V tiles of physical block phys into stage s
+    auto issue = [&](int s, int phys) {
+        uint64_t* bar = &wbars[s];
         if (phys < 0 || phys >= p.num_blocks) {
             atomicOr(p.err, KVC_DEVERR_BLOCK_ID);
             mbar_arrive(bar);  // complete the phase without data; the block is skipped
             return;
         }
-        uint8_t* st = wring + (i % ST) * C::kStageBytes;
+        uint8_t* st = wring + s * C::kStageBytes;
         mbar_arrive_expect_tx(bar, C::kStageBytes);
         const int y = (phys * p.Hkv + kvh) * kBlockSize;
 #pragma unroll
@@ -268,12 +291,32 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
         }
     };
+    // each warp owns its barriers: lane 0 initialises them and issues the static first round
+    // (stage s gets block cb0 + gw + s * warps-in-the-cluster) without waiting for the rest of the CTA
+    int blk[ST];
 #pragma unroll
-    for (int i = 0; i < ST; ++i) {
-        const int phys = __shfl_sync(0xffffffffu, my_blk, i);
-        if (lane == 0 && i < nb_w) issue(i, phys);
+    for (int s = 0; s < ST; ++s) {
+        const int j = cb0 + gw + s * nwarps_cl;
+        blk[s] = j < cb1 ? j : -1;
     }
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
+        fence_barrier_init();
+        if (warp == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            if (rank == 0) *s_counter = cb0 + ST * nwarps_cl;  // blocks handed out after the first round
+        }
+#pragma unroll
+        for (int s = 0; s < ST; ++s)
+            if (blk[s] >= 0) issue(s, first_phys[s]);
+    }
+    __syncwarp();
     KVC_TRACE_MARK(1);
+
+    __syncthreads();  // the table slice (and, in rank 0, the counter) is in shared memory
+    // the counter is visible cluster-wide once every CTA has passed the matching wait below
+    if (cs > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
     // ---- everything below may read what the previous kernel wrote ----
     grid_dependency_wait();
@@ -290,130 +333,159 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
             qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t4) : 0u;
         }
     }
-
-    // fused append: the warp holding the block of position ctx-1 writes the new row to the cache
-    // and patches it into its shared-memory tile before use
-    int app_iter = -1;
+    // fused append: any warp of the last cluster may get the block of position ctx-1; each holds the
+    // new row (lanes 0-15: K chunks, 16-31: V chunks) to write it to the cache and patch its tile
+    const int app_blk = p.k_new != nullptr && cidx == nclus - 1 ? nblk - 1 : -1;
     const int app_row = (ctx - 1) % kBlockSize;
     uint4 app_val = make_uint4(0, 0, 0, 0);
-    if (p.k_new != nullptr && split == nsplit - 1 && ((nblk - 1 - j0) % NW) == warp) {
-        app_iter = (nblk - 1 - j0) / NW;
-        const int phys = __shfl_sync(0xffffffffu, my_blk, app_iter);
-        const int c = lane & 15;
-        const bool is_v = lane >= 16;
-        if (c < D / 8) {
-            const __half* src = (is_v ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.Hkv + kvh) * D + c * 8;
-            app_val = *reinterpret_cast<const uint4*>(src);
-            if (phys >= 0 && phys < p.num_blocks) {
-                __half* dst = (is_v ? p.v_cache : p.k_cache) +
-                              ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D + c * 8;
-                *reinterpret_cast<uint4*>(dst) = app_val;
-            }
-        }
+    if (app_blk >= 0 && (lane & 15) < D / 8) {
+        const __half* src = (lane >= 16 ? p.v_new : p.k_new) + (static_cast<int64_t>(b) * p.Hkv + kvh) * D +
+                            (lane & 15) * 8;
+        app_val = *reinterpret_cast<const uint4*>(src);
     }
 
-    float o[D / 8][4];
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    const float sl2 = p.scale_log2;
+    // the counter lives in rank 0's shared memory
+    uint32_t counter_addr = 0;
+    if (cs > 1) {
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        counter_addr = map_to_rank(s_counter, 0);
+    }
+#if KVC_DEC_STEAL
+    auto grab = [&]() -> int {  // lane 0 only
+        if (cs > 1) {
+            int v;
+            asm volatile("atom.shared::cluster.add.u32 %0, [%1], 1;" : "=r"(v) : "r"(counter_addr) : "memory");
+            return v;
+        }
+        return atomicAdd(s_counter, 1);
+    };
+    int next_j = (lane == 0) ? grab() : 0;  // the block the next refill will load
+#else
+    int next_j = cb0 + gw + ST * nwarps_cl;  // fixed round-robin: this warp's blocks are gw mod (warps)
+    auto grab = [&]() -> int { return next_j + nwarps_cl; };
+#endif
 
-    int i = 0;
+    // O^T accumulators: o[mt] = dims mt*16 + g (+8) x heads 2*t4, 2*t4+1; running max / sum per head pair
+    float o[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const float sl2 = p.scale_log2;
+    uint32_t phase = 0;  // bit s: parity of stage s's next completion
     bool timed_out = false;
-    for (; i < nb_w; ++i) {
-        const int stage = i % ST;
-        const uint32_t parity = (i / ST) & 1;
-        const int jj = j0 + warp + i * NW;
-        const int phys = __shfl_sync(0xffffffffu, my_blk, i);
-        const bool ok = mbar_wait_bounded(&wbars[stage], parity, kWaitLimitNs);
-        if (__any_sync(0xffffffffu, !ok)) {
-            timed_out = true;
-            break;
-        }
-        if (phys >= 0 && phys < p.num_blocks) {
-            const uint32_t kbase = smem_u32(wring + stage * C::kStageBytes);
-            const uint32_t vbase = kbase + C::kTileBytes;
-            if (i == app_iter) {
-                const int c = lane & 15;
-                if (c < D / 8) {
-                    const uint32_t a = (lane >= 16 ? vbase : kbase) + swz(app_row, c);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(app_val.x), "r"(app_val.y),
-                                 "r"(app_val.z), "r"(app_val.w)
-                                 : "memory");
+
+#pragma unroll 1
+    for (int i = 0;; ++i) {
+        const int s = i % ST;
+        int jj = -1;
+#pragma unroll
+        for (int k = 0; k < ST; ++k)
+            if (k == s) jj = blk[k];  // register select, no local memory
+        if (jj < 0) break;            // grabs only grow: the first empty stage ends the warp's work
+        {
+            const bool ok = mbar_wait_bounded(&wbars[s], (phase >> s) & 1u, kWaitLimitNs);
+            phase ^= 1u << s;
+            if (__any_sync(0xffffffffu, !ok)) {
+                timed_out = true;
+                break;
+            }
+            const int phys = s_table[jj - cb0];
+            if (phys >= 0 && phys < p.num_blocks) {
+                const uint32_t kbase = smem_u32(wring + s * C::kStageBytes);
+                const uint32_t vbase = kbase + C::kTileBytes;
+                if (jj == app_blk) {
+                    const int c = lane & 15;
+                    if (c < D / 8) {
+                        const uint32_t a = (lane >= 16 ? vbase : kbase) + swz(app_row, c);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(app_val.x),
+                                     "r"(app_val.y), "r"(app_val.z), "r"(app_val.w)
+                                     : "memory");
+                        __half* dst = (lane >= 16 ? p.v_cache : p.k_cache) +
+                                      ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D + c * 8;
+                        *reinterpret_cast<uint4*>(dst) = app_val;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-            }
-            // ---- S = Q K^T for the 16 tokens of this block (two n-tiles of 8) ----
-            float sc[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-                for (int kc = 0; kc < D / 32; ++kc) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + swz(nt * 8 + (lane & 7), kc * 4 + (lane >> 3)), b0, b1, b2, b3);
-                    mma_f16_16816(sc[nt], qa[2 * kc][0], 0u, qa[2 * kc][1], 0u, b0, b1);
-                    mma_f16_16816(sc[nt], qa[2 * kc + 1][0], 0u, qa[2 * kc + 1][1], 0u, b2, b3);
-                }
-            }
-            // ---- online softmax (row g; columns 2*t4, 2*t4+1 of each n-tile) ----
-            const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
-            float x[2][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = nt * 8 + 2 * t4 + e;
-                    x[nt][e] = tok < rem ? sc[nt][e] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, x[nt][e]);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = ex2(m_run - m_new);
-            m_run = m_new;
-            uint32_t phi[2], plo[2];
-            float ps = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float p0 = ex2(x[nt][0] - m_new), p1 = ex2(x[nt][1] - m_new);
-                ps += p0 + p1;
-                phi[nt] = pack_half2(p0, p1);
-                const float2 h = unpack_half2(phi[nt]);
-                plo[nt] = pack_half2(p0 - h.x, p1 - h.y);
-            }
-            l_run = l_run * alpha + ps;
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                o[nd][0] *= alpha;
-                o[nd][1] *= alpha;
-            }
-            // rows of V past the context may hold any bits (even NaN): zero them in registers
-            uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
-            if (rem < kBlockSize) {
-                keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
-                keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
-            }
-            // ---- O += P V (P = hi + lo) ----
-#pragma unroll
-            for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots ----
                 const int mi = lane >> 3;
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vbase + swz((mi & 1) * 8 + (lane & 7), nd2 * 2 + (mi >> 1)), v0, v1, v2, v3);
-                v0 &= keep0;
-                v2 &= keep0;
-                v1 &= keep1;
-                v3 &= keep1;
-                mma_f16_16816(o[2 * nd2], phi[0], 0u, phi[1], 0u, v0, v1);
-                mma_f16_16816(o[2 * nd2], plo[0], 0u, plo[1], 0u, v0, v1);
-                mma_f16_16816(o[2 * nd2 + 1], phi[0], 0u, phi[1], 0u, v2, v3);
-                mma_f16_16816(o[2 * nd2 + 1], plo[0], 0u, plo[1], 0u, v2, v3);
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                    mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
+                }
+                // ---- online softmax per head (column): this lane holds tokens g, g+8 of heads 2*t4, 2*t4+1 ----
+                const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
+                float x[4];
+                x[0] = g < rem ? sc[0] * sl2 : -INFINITY;
+                x[1] = g < rem ? sc[1] * sl2 : -INFINITY;
+                x[2] = g + 8 < rem ? sc[2] * sl2 : -INFINITY;
+                x[3] = g + 8 < rem ? sc[3] * sl2 : -INFINITY;
+                float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
+                m_run[0] = mn0;
+                m_run[1] = mn1;
+                const float p0 = ex2(x[0] - mn0), p1 = ex2(x[1] - mn1), p2 = ex2(x[2] - mn0), p3 = ex2(x[3] - mn1);
+                l_run[0] = l_run[0] * al0 + p0 + p2;
+                l_run[1] = l_run[1] * al1 + p1 + p3;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+                // P^T as the B operand (k = tokens, n = heads): transpose the two 8x8 halves in registers;
+                // P = hi + lo, both fp16, so the P V product keeps ~fp32 accuracy
+                const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
+                const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
+                const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+                const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
+                const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+                // rows of V past the context may hold any bits (even NaN): zero them in registers
+                uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+                if (rem < kBlockSize) {
+                    keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
+                    keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
+                }
+                // ---- O^T += V^T P^T, one m-tile per 16 dims ----
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                    a0 &= keep0;
+                    a1 &= keep0;
+                    a2 &= keep1;
+                    a3 &= keep1;
+                    mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+                    mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+                }
             }
+            __syncwarp();
+            // refill this stage with the next block of the cluster's range, if any is left
+#if KVC_DEC_STEAL
+            const int nj = __shfl_sync(0xffffffffu, next_j, 0);
+#else
+            const int nj = next_j;
+            next_j = grab();
+#endif
+            if (nj < cb1 && lane == 0) {
+                issue(s, s_table[nj - cb0]);
+#if KVC_DEC_STEAL
+                next_j = grab();
+#endif
+            }
+#pragma unroll
+            for (int k = 0; k < ST; ++k)
+                if (k == s) blk[k] = nj < cb1 ? nj : -1;
         }
-        __syncwarp();
-        const int nxt = __shfl_sync(0xffffffffu, my_blk, (i + ST) & 31);
-        if (lane == 0 && i + ST < nb_w) issue(i + ST, nxt);
     }
 #if !KVC_DEC_EARLY_TRIGGER
     grid_dependents_launch();  // the next kernel may start its prologue while this one finishes
@@ -422,101 +494,146 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     if (timed_out) {
         if (lane == 0) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
         // let copies still in flight land before the shared memory is reused
-        for (int k = i; k < min(nb_w, i + ST); ++k) mbar_wait_bounded(&wbars[k % ST], (k / ST) & 1, kWaitLimitNs / 8);
-        m_run = -INFINITY;
-        l_run = 0.f;
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = 0.f;
+        for (int s = 0; s < ST; ++s)
+            if (blk[s] >= 0) mbar_wait_bounded(&wbars[s], (phase >> s) & 1u, kWaitLimitNs / 8);
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {  // per-lane partial sums over the lanes of a head pair
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
+    }
 
     // ---- merge the warps of this CTA (each warp parks its state in its own ring) ----
     __syncwarp();
-    float* wm = reinterpret_cast<float*>(wring);  // [8] m, [8] l, then [8][D+4] acc
-    if (t4 == 0) {
-        wm[g] = m_run;
-        wm[8 + g] = l_run;
+    float* wm = reinterpret_cast<float*>(wring);  // [8] m, [8] l, then [8 heads][D+4] acc
+    if (g == 0) {
+        wm[2 * t4] = m_run[0];
+        wm[2 * t4 + 1] = m_run[1];
+        wm[8 + 2 * t4] = l_run[0];
+        wm[8 + 2 * t4 + 1] = l_run[1];
     }
     float* wo = wm + 16;
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-        *reinterpret_cast<float2*>(wo + g * C::kMergeStride + nd * 8 + 2 * t4) = make_float2(o[nd][0], o[nd][1]);
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int d = mt * 16 + g;
+        wo[(2 * t4) * C::kMergeStride + d] = o[mt][0];
+        wo[(2 * t4 + 1) * C::kMergeStride + d] = o[mt][1];
+        wo[(2 * t4) * C::kMergeStride + d + 8] = o[mt][2];
+        wo[(2 * t4 + 1) * C::kMergeStride + d + 8] = o[mt][3];
+    }
     __syncthreads();
+    KVC_TRACE_MARK(4);
 
     const bool direct = nclus == 1 && cs == 1;  // a single CTA holds the whole context
-    for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
-        const int gg = e / D, d = e % D;
+    // pass 1, one thread per head: the CTA maximum and every warp's weight 2^(m_w - M) (times 1/L when
+    // this CTA's result is final)
+    if (threadIdx.x < p.G) {
+        const int gg = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes)[gg]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        float L = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float* r = reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes);
-                const float wgt = ex2(r[gg] - M);  // an empty warp has m = -inf -> weight 0
-                L += r[8 + gg] * wgt;
-                O += r[16 + gg * C::kMergeStride + d] * wgt;
-            }
+        for (int w = 0; w < NW; ++w) {
+            const float* r = reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes);
+            const float wgt = M == -INFINITY ? 0.f : ex2(r[gg] - M);  // an empty warp has m = -inf: weight 0
+            s_wgt[w * 8 + gg] = wgt;
+            L += r[8 + gg] * wgt;
         }
         if (direct) {
-            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d,
-                      L > 0.f ? O / L : 0.f);
-        } else {
-            if (d == 0) {
-                s_m[gg] = M;
-                s_l[gg] = L;
-            }
-            s_acc[gg * D + d] = O;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s_wgt[w * 8 + gg] *= inv;
+        }
+        s_m[gg] = M;
+        s_l[gg] = L;
+        if (!direct && cs == 1) {  // one CTA per cluster: its state is the cluster's partial
+            const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx;
+            p.part_ml[row * 2 + 0] = M;
+            p.part_ml[row * 2 + 1] = L;
         }
     }
-    if (direct) {
+    __syncthreads();
+    // pass 2: acc = sum over warps of weight * acc_w
+    for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
+        const int gg = e / D, d = e % D;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            O += s_wgt[w * 8 + gg] *
+                 reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes)[16 + gg * C::kMergeStride + d];
+        if (direct)
+            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d, O);
+        else if (cs == 1)
+            p.part_acc[((static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx) * D + d] = O;
+        else
+            s_acc[gg * D + d] = O;
+    }
+    if (cs == 1) {
         KVC_TRACE_END();
         return;
     }
 
-    // ---- merge the CTAs of this cluster through distributed shared memory ----
-    if (cs > 1)
-        cluster_sync_all();  // every CTA's state is in its shared memory
-    else
-        __syncthreads();
-    const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;
-    const int nthreads = cs * C::kThreads;
-    for (int e = rank * C::kThreads + threadIdx.x; e < p.G * D; e += nthreads) {
-        const int gg = e / D, d = e % D;
-        float mc[kMaxCluster], lc[kMaxCluster];
+    // ---- merge the CTAs of this cluster in rank 0: every CTA pushes its state into rank 0's inbox
+    // (remote stores, no round trip), arrives on the cluster barrier and leaves; rank 0 waits for all
+    // arrivals, which makes the pushed states visible to it, and merges locally ----
+    __syncthreads();  // this CTA's s_m / s_l / s_acc are complete
+    KVC_TRACE_MARK(5);
+    {
+        const int stride = 16 + 8 * D;  // floats per inbox slot
+        const uint32_t slot = map_to_rank(s_inbox + rank * stride, 0);
+        // s_m, s_l, s_acc are contiguous: m[8], l[8], acc[8][D]; rows >= G are never read
+        for (int e = threadIdx.x; e < 16 + p.G * D; e += C::kThreads)
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(slot + 4u * e), "f"(s_m[e]) : "memory");
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (rank != 0) {
+        KVC_TRACE_MARK(6);
+        KVC_TRACE_END();
+        return;  // nothing of this CTA is read by others
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    KVC_TRACE_MARK(6);
+    const int stride = 16 + 8 * D;  // floats per inbox slot
+    // pass 1, one thread per head: cluster maximum and every CTA's weight (times 1/L when final)
+    if (threadIdx.x < p.G) {
+        const int gg = threadIdx.x;
         float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) {
-            if (c < cs) {
-                mc[c] = ld_cluster_f32(map_to_rank(s_m + gg, c));
-                lc[c] = ld_cluster_f32(map_to_rank(s_l + gg, c));
-                M = fmaxf(M, mc[c]);
-            }
+        for (int c = 0; c < cs; ++c)
+            if (s_inbox[c * stride + 8 + gg] > 0.f) M = fmaxf(M, s_inbox[c * stride + gg]);
+        float L = 0.f;
+        for (int c = 0; c < cs; ++c) {
+            const float l = s_inbox[c * stride + 8 + gg];
+            const float w = l > 0.f ? ex2(s_inbox[c * stride + gg] - M) : 0.f;  // a CTA without blocks: 0
+            s_wgt[c * 8 + gg] = w;
+            L += l * w;
         }
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) {
-            if (c < cs && lc[c] > 0.f) {  // an inactive or empty CTA contributes nothing
-                const float w = ex2(mc[c] - M);
-                L += lc[c] * w;
-                O += ld_cluster_f32(map_to_rank(s_acc + gg * D + d, c)) * w;
-            }
-        }
-        const int h = kvh * p.G + gg;
         if (nclus == 1) {
-            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, L > 0.f ? O / L : 0.f);
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            for (int c = 0; c < cs; ++c) s_wgt[c * 8 + gg] *= inv;
         } else {
-            const int64_t row = (static_cast<int64_t>(b) * p.Hq + h) * p.nparts + cidx;
-            if (d == 0) {
-                p.part_ml[row * 2 + 0] = M;
-                p.part_ml[row * 2 + 1] = L;
-            }
-            p.part_acc[row * D + d] = O;
+            const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx;
+            p.part_ml[row * 2 + 0] = M;
+            p.part_ml[row * 2 + 1] = L;
         }
     }
-    if (cs > 1) cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+    __syncthreads();
+    // pass 2: acc = sum over the cluster's CTAs of weight * acc_c
+    for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
+        const int gg = e / D, d = e % D;
+        float O = 0.f;
+        for (int c = 0; c < cs; ++c) O += s_wgt[c * 8 + gg] * s_inbox[c * stride + 16 + gg * D + d];
+        const int64_t h = kvh * p.G + gg;
+        if (nclus == 1)
+            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, O);
+        else
+            p.part_acc[((static_cast<int64_t>(b) * p.Hq + h) * p.nparts + cidx) * D + d] = O;
+    }
     KVC_TRACE_END();
 }
 
@@ -527,9 +644,8 @@ template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* __restrict__ part_ml,
                                                                     const float* __restrict__ part_acc,
                                                                     const int32_t* __restrict__ context_lens,
-                                                                    void* out, int Hq, int nparts_grid, int bps,
-                                                                    int csize, int max_blocks, int max_ctx,
-                                                                    int out_f32) {
+                                                                    void* out, int Hq, int nparts_grid, int bpc,
+                                                                    int max_blocks, int max_ctx, int out_f32) {
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
     grid_dependency_wait();
@@ -537,8 +653,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctx = context_lens[b];
     if (ctx < 1 || ctx > max_blocks * kBlockSize || ctx > max_ctx) return;
-    const int nsplit = ((ctx + kBlockSize - 1) / kBlockSize + bps - 1) / bps;
-    const int nparts = (nsplit + csize - 1) / csize;
+    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize + bpc - 1) / bpc;
     if (nparts <= 1) return;  // the cluster wrote the output itself
     const int64_t row0 = (static_cast<int64_t>(b) * Hq + h) * nparts_grid;
     float M = -INFINITY, L = 0.f, O[V];
@@ -612,40 +727,43 @@ static cudaError_t decode_setup(int* ctas_per_sm) {
 }
 
 template <int D>
-static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bps_req, DecodePlan* plan) {
+static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, DecodePlan* plan) {
     using C = DecodeCfg<D>;
     const int nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
-    int bps = bps_req;
-    if (bps <= 0) {
+    int cs, bpc;
+    if (bpc_req > 0) {
+        bpc = std::min(bpc_req, kMaxClusterBlocks);
+        cs = std::max(1, std::min(kMaxCluster, (bpc + C::kWarps - 1) / C::kWarps));
+    } else {
         const int sms = sm_count();
         if (sms <= 0) return cudaErrorNoDevice;
         int occ = 0;
         cudaError_t e = decode_setup<D>(&occ);
         if (e != cudaSuccess) return e;
-        // one wave: every CTA resident at once; at least one block per warp
-        const int64_t work = static_cast<int64_t>(B) * Hkv * nblk;
-        const int64_t slots = static_cast<int64_t>(sms) * occ;
-        int64_t want = (work + slots - 1) / slots;
-        want = std::max<int64_t>(want, C::kWarps);
-        want = (want + C::kWarps - 1) / C::kWarps * C::kWarps;
-        bps = static_cast<int>(std::min<int64_t>(std::min<int64_t>(want, C::kMaxBps), nblk));
+        // one wave: the CTAs of all (sequence, KV head) pairs resident at once, at least one block per warp
+        const int64_t segs = static_cast<int64_t>(B) * Hkv;
+        const int64_t per_seg = std::max<int64_t>(1, static_cast<int64_t>(sms) * occ / std::max<int64_t>(segs, 1));
+        cs = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>({kMaxCluster, per_seg, (nblk + C::kWarps - 1) / C::kWarps})));
+        int64_t ncl = std::max<int64_t>(
+            1, std::min<int64_t>(per_seg / cs, (nblk + static_cast<int64_t>(cs) * C::kWarps - 1) /
+                                                   (static_cast<int64_t>(cs) * C::kWarps)));
+        ncl = std::max<int64_t>(ncl, (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks);
+        bpc = static_cast<int>((nblk + ncl - 1) / ncl);
     }
-    if (bps > C::kMaxBps) bps = C::kMaxBps;
-    const int nsplit = (nblk + bps - 1) / bps;
-    const int cs = std::min(nsplit, kMaxCluster);
-    const int nparts = (nsplit + cs - 1) / cs;
-    plan->blocks_per_split = bps;
+    const int nparts = (nblk + bpc - 1) / bpc;
+    plan->blocks_per_split = bpc;
     plan->cluster = cs;
-    plan->num_splits = nparts * cs;  // grid.x, a whole number of clusters
     plan->num_parts = nparts;
+    plan->num_splits = nparts * cs;  // grid.x: whole clusters
     plan->workspace_bytes = nparts > 1 ? static_cast<size_t>(B) * Hq * nparts * (2 + D) * sizeof(float) : 0;
     return cudaSuccess;
 }
 
-cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_ctx, int bps_req, DecodePlan* plan) {
+cudaError_t decode_plan(int B, int Hq, int Hkv, int D, int max_ctx, int bpc_req, DecodePlan* plan) {
     switch (D) {
-        case 64: return plan_d<64>(B, Hq, Hkv, max_ctx, bps_req, plan);
-        case 128: return plan_d<128>(B, Hq, Hkv, max_ctx, bps_req, plan);
+        case 64: return plan_d<64>(B, Hq, Hkv, max_ctx, bpc_req, plan);
+        case 128: return plan_d<128>(B, Hq, Hkv, max_ctx, bpc_req, plan);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -726,6 +844,8 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.v_new = a.v_new;
     p.k_cache = const_cast<__half*>(a.k_cache);
     p.v_cache = const_cast<__half*>(a.v_cache);
+    p.k_next = a.k_next;
+    p.v_next = a.v_next;
     p.block_table = a.block_table;
     p.context_lens = a.context_lens;
     p.out = a.out;
@@ -740,7 +860,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.Hkv = a.Hkv;
     p.G = a.Hq / a.Hkv;
     p.max_ctx = a.max_context_len;
-    p.bps = plan.blocks_per_split;
+    p.bpc = plan.blocks_per_split;
     p.csize = plan.cluster;
     p.nparts = plan.num_parts;
     p.out_f32 = a.out_f32;
@@ -757,8 +877,8 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
         dim3 cgrid(a.Hq, a.B);
         e = launch(paged_decode_combine_kernel<D>, cgrid, dim3(256), 0, stream, true, 1u,
                    static_cast<const float*>(p.part_ml), static_cast<const float*>(p.part_acc), a.context_lens,
-                   a.out, a.Hq, plan.num_parts, plan.blocks_per_split, plan.cluster, a.max_blocks,
-                   a.max_context_len, a.out_f32);
+                   a.out, a.Hq, plan.num_parts, plan.blocks_per_split, a.max_blocks, a.max_context_len,
+                   a.out_f32);
     }
     return e;
 }

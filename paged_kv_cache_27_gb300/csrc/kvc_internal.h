@@ -22,9 +22,9 @@ cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __
 
 // ---- decode (decode.cu) ------------------------------------------------------
 struct DecodePlan {
-    int num_splits;        // grid.x: splits of the longest context, rounded up to whole clusters
-    int blocks_per_split;  // blocks of 16 tokens per split
-    int cluster;           // CTAs per thread-block cluster (the splits merged on chip)
+    int num_splits;        // grid.x = num_parts * cluster
+    int blocks_per_split;  // blocks of 16 tokens one cluster covers
+    int cluster;           // CTAs per thread-block cluster (they share the cluster's blocks)
     int num_parts;         // clusters along the longest context; > 1 needs the workspace + combine kernel
     size_t workspace_bytes;
 };
@@ -36,6 +36,8 @@ struct DecodeArgs {
     const __half* v_new;
     const __half* k_cache;
     const __half* v_cache;
+    const __half* k_next;  // null, or the next layer's pools: this call's blocks of them are prefetched to L2
+    const __half* v_next;
     int num_blocks;
     const int32_t* block_table;
     int max_blocks;
@@ -47,13 +49,13 @@ struct DecodeArgs {
     int out_f32;
     void* workspace;
     size_t workspace_bytes;
-    int blocks_per_split;  // 0 = automatic
+    int blocks_per_split;  // blocks per cluster, 0 = automatic
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // process-wide: launch decode kernels as programmatic dependents of the previous kernel
 void set_launch_overlap(int on);
-// copies up to `cap` trace records (48 bytes each) of the decode kernel; cudaErrorNotSupported
+// copies up to `cap` trace records (80 bytes each) of the decode kernel; cudaErrorNotSupported
 // unless the library was built with -DKVC_TRACE=1
 cudaError_t trace_read(void* host, int cap, int* n, int clear);
 int launch_overlap();
