@@ -239,6 +239,31 @@ kvc_status kvc_set_launch_overlap(int on);
  * memory; `clear` resets the device buffer.  Synchronous. */
 kvc_status kvc_trace_read(void* records, int capacity, int* count, int clear);
 
+/* Allocation-free decode.  The pages have no counterpart: this is an
+ * interface choice of this library.  Same arguments, preconditions and
+ * results as paged_decode_attention, but with no workspace argument: when the
+ * longest context needs split scratch, it goes to a fixed 16 MiB array that
+ * the library declares in device memory (every GPU that loads the library
+ * holds those 16 MiB until the process exits).  It serves callers that must
+ * not allocate device memory while they run: allocator or memory-pool code
+ * that would re-enter itself, plug-ins that are handed only their input and
+ * output buffers, and serving loops that forbid cudaMalloc after start-up.
+ * The call itself allocates nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array: calls that can overlap on
+ *    the GPU (other streams, concurrent graphs) race on it.  Nothing in it
+ *    needs to start at zero: every word a call reads, the same call writes first.
+ *  - Sizes whose scratch exceeds 16 MiB (see paged_decode_plan) return
+ *    KVC_ERR_CAPACITY without launching anything.
+ *  - Checked mode does not apply to this call. */
+kvc_status paged_decode_attention_static_workspace(const void* q, const void* k_cache, const void* v_cache,
+                                                   int num_blocks, const int32_t* block_table, int max_blocks,
+                                                   const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim,
+                                                   int block_size, int max_context_len, float scale, void* out,
+                                                   int out_dtype, int blocks_per_split, void* stream);
+
 /* Varlen packed prefill (xformers article parts 4-5): for every segment s
  * (rows cu_seqlens[s] .. cu_seqlens[s+1]-1) and query head h,
  *   out = softmax(Q K^T * scale + mask) V,

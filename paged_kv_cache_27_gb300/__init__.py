@@ -29,6 +29,7 @@ __all__ = [
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
     "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
+    "paged_decode_attention_static_workspace",
     "prefill_attention", "DEVERR",
 ]
 
@@ -106,6 +107,8 @@ def _load():
         "paged_decode_append_attention": (I, [P, P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
                                               I, P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
+        "paged_decode_attention_static_workspace": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
+                                                        I, P]),
         "kvc_trace_read": (I, [P, I, PI, I]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
     }
@@ -388,6 +391,32 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
         _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
         _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),
         "paged_decode_append_attention")
+
+
+def paged_decode_attention_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                            block_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                            out: torch.Tensor, max_context_len: int, blocks_per_split: int = 0,
+                                            stream=None) -> None:
+    """paged_decode_attention without a workspace argument: split scratch comes from the library's fixed
+    16 MiB device array, so the call allocates nothing (for callers that must not allocate device memory).
+
+    The first call on a device looks up that array's address; make it before any stream capture. Calls that
+    overlap on the GPU share the array and race on it."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table / context_lens do not match B")
+    od = KVC_F16 if out.dtype == torch.float16 else KVC_F32 if out.dtype == torch.float32 else None
+    if od is None:
+        raise TypeError("out must be float16 or float32")
+    _check(_lib.paged_decode_attention_static_workspace(
+        _dptr(q, torch.float16, "q"), _dptr(k_cache, torch.float16, "k_cache"),
+        _dptr(v_cache, torch.float16, "v_cache"), NB, _dptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs,
+        int(max_context_len), float(scale), _dptr(out, None, "out"), od, int(blocks_per_split), _stream(stream, q)),
+        "paged_decode_attention_static_workspace")
 
 
 def paged_decode_attention_raw(q_ptr: int, k_ptr: int, v_ptr: int, num_blocks: int, table_ptr: int, max_blocks: int,

@@ -72,6 +72,11 @@ kvc_status copy_to_host(std::vector<T>& dst, const T* src, size_t n, cudaStream_
 
 }  // namespace
 
+int kvc::set_last_error(int status, const char* msg) {
+    g_last_error = msg;
+    return status;
+}
+
 extern "C" {
 
 const char* kvc_last_error_string(void) { return g_last_error.c_str(); }

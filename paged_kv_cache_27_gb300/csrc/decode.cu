@@ -921,4 +921,90 @@ cudaError_t trace_read(void* host, int cap, int* n, int clear) {
 void set_launch_overlap(int on) { g_launch_overlap.store(on ? 1 : 0); }
 int launch_overlap() { return g_launch_overlap.load(); }
 
+// ---------------------------------------------------------------------------
+// Allocation-free decode: the split partials live in a fixed array that the
+// library holds in device memory instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB on every device that loads the library
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+// Device address of g_static_workspace on the current device, looked up once per device (host code
+// cannot use the symbol itself: on the host it only names a stand-in, not device memory).
+static cudaError_t static_workspace_address(void** out) {
+    static std::atomic<void*> cache[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    void* p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_static_workspace);
+        if (e != cudaSuccess) return e;
+        cache[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
 }  // namespace kvc
+
+extern "C" kvc_status paged_decode_attention_static_workspace(
+    const void* q, const void* k_cache, const void* v_cache, int num_blocks, const int32_t* block_table,
+    int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv, int head_dim, int block_size,
+    int max_context_len, float scale, void* out, int out_dtype, int blocks_per_split, void* stream) {
+    using kvc::set_last_error;
+    auto fail = [](kvc_status s, const char* m) { return static_cast<kvc_status>(set_last_error(s, m)); };
+    auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (B < 0 || Hq < 1 || Hkv < 1 || max_context_len < 1 || num_blocks < 1 || max_blocks < 1 || blocks_per_split < 0)
+        return fail(KVC_ERR_INVALID, "bad sizes");
+    if (Hq % Hkv) return fail(KVC_ERR_INVALID, "Hq must be a multiple of Hkv");
+    if (Hq / Hkv > 8) return fail(KVC_ERR_UNSUPPORTED, "group size > 8 not supported");
+    if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (block_size != kvc::kBlockSize) return fail(KVC_ERR_UNSUPPORTED, "block_size must be 16");
+    if (B > 65535 || Hkv > 65535) return fail(KVC_ERR_UNSUPPORTED, "B and Hkv must be <= 65535");
+    if (static_cast<int64_t>(num_blocks) * Hkv * block_size >= (int64_t(1) << 31))
+        return fail(KVC_ERR_UNSUPPORTED, "num_blocks * Hkv * block_size must be < 2^31");
+    if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks) * block_size)
+        return fail(KVC_ERR_CAPACITY, "max_context_len beyond max_blocks * block_size");
+    if (out_dtype != KVC_F16 && out_dtype != KVC_F32) return fail(KVC_ERR_INVALID, "bad out_dtype");
+    if (B == 0) return KVC_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out) return fail(KVC_ERR_INVALID, "null pointer");
+    if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(out))
+        return fail(KVC_ERR_INVALID, "q, caches and out must be 16-byte aligned");
+    kvc::DecodePlan plan;
+    cudaError_t e = kvc::decode_plan(B, Hq, Hkv, head_dim, max_context_len, blocks_per_split, &plan);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, cudaGetErrorString(e));
+    if (plan.workspace_bytes > kvc::kStaticWorkspaceBytes)
+        return fail(KVC_ERR_CAPACITY,
+                    "these sizes need more split scratch than the 16 MiB static workspace holds "
+                    "(use paged_decode_attention with a caller workspace, or fewer splits)");
+    kvc::DecodeArgs a;
+    a.q = static_cast<const __half*>(q);
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+    a.k_cache = static_cast<const __half*>(k_cache);
+    a.v_cache = static_cast<const __half*>(v_cache);
+    a.k_next = nullptr;
+    a.v_next = nullptr;
+    a.num_blocks = num_blocks;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.context_lens = context_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = head_dim;
+    a.max_context_len = max_context_len;
+    a.scale = scale;
+    a.out = out;
+    a.out_f32 = out_dtype == KVC_F32;
+    a.blocks_per_split = blocks_per_split;
+    a.workspace_bytes = kvc::kStaticWorkspaceBytes;
+    e = kvc::static_workspace_address(&a.workspace);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, cudaGetErrorString(e));
+    e = kvc::device_error_word(&a.err);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, cudaGetErrorString(e));
+    e = kvc::launch_decode(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, cudaGetErrorString(e));
+    return KVC_OK;
+}

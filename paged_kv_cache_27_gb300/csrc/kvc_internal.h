@@ -60,6 +60,9 @@ void set_launch_overlap(int on);
 cudaError_t trace_read(void* host, int cap, int* n, int clear);
 int launch_overlap();
 
+// Records `msg` as the calling thread's last error (kvc_last_error_string) and returns `status`.
+int set_last_error(int status, const char* msg);
+
 // ---- prefill (prefill.cu) ----------------------------------------------------
 struct PrefillArgs {
     const __half* q;
