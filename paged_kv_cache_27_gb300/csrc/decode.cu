@@ -77,17 +77,20 @@ namespace kvc {
 #ifndef KVC_DEC_MIN_CTAS  // resident CTAs per SM the register allocation must allow
 #define KVC_DEC_MIN_CTAS 1
 #endif
+#ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
+#define KVC_DEC_PLAN_CTAS 2
+#endif
 #ifndef KVC_DEC_PREFETCH_AT  // when the next layer's blocks are requested into L2: 0 at start, 1 after the main loop
 #define KVC_DEC_PREFETCH_AT 1
 #endif
 #ifndef KVC_DEC_STEAL  // 1: warps take blocks from a cluster-wide counter; 0: fixed round-robin over the cluster's warps
-#define KVC_DEC_STEAL 1
+#define KVC_DEC_STEAL 0
 #endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
-constexpr int kMaxClusterBlocks = 512;  // blocks one cluster covers at most (its table slice is in shared memory)
+constexpr int kMaxClusterBlocks = 256;  // blocks one cluster covers at most (its table slice is in shared memory)
 
 std::atomic<int> g_launch_overlap{0};
 
@@ -103,9 +106,9 @@ struct DecodeCfg {
     static constexpr int kBarBytes = kWarps * kStages * 8;
     static constexpr int kStateBytes = (8 * (D + 2) + 16 * 8) * 4;  // merged (m, l, acc) of 8 heads + merge weights
     static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice + block counter
-    static constexpr int kInboxBytes = kMaxCluster * kStateBytes;    // cluster rank 0: every CTA's merged state
-    static constexpr int kSmemBytes =
-        kRingBytes + kBarBytes + kStateBytes + kTableBytes + kInboxBytes + 1024;  // + alignment slack
+    // + the inbox of cluster rank 0 (one slot per other CTA of the cluster, sized at launch) + alignment slack
+    static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + kTableBytes + 1024;
+    static int smem_bytes(int cluster, int G) { return kBaseSmemBytes + (cluster - 1) * (16 + G * D) * 4; }
     static constexpr int kMergeStride = D + 4;  // floats per parked row
     static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
 };
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     float* s_wgt = s_acc + 8 * D;  // [16 sources][8 heads] merge weights
     int* s_table = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
     int* s_counter = s_table + kMaxClusterBlocks;  // next block to hand out (used in cluster rank 0)
-    // rank 0's inbox: slot c holds CTA c's merged state laid out like s_m/s_l/s_acc
+    // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like s_m / s_l / s_acc[0..G)
     float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes + C::kTableBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -584,11 +587,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // arrivals, which makes the pushed states visible to it, and merges locally ----
     __syncthreads();  // this CTA's s_m / s_l / s_acc are complete
     KVC_TRACE_MARK(5);
-    {
-        const int stride = 16 + 8 * D;  // floats per inbox slot
-        const uint32_t slot = map_to_rank(s_inbox + rank * stride, 0);
-        // s_m, s_l, s_acc are contiguous: m[8], l[8], acc[8][D]; rows >= G are never read
-        for (int e = threadIdx.x; e < 16 + p.G * D; e += C::kThreads)
+    const int stride = 16 + p.G * D;  // floats per inbox slot: m[8], l[8], acc[G][D]
+    if (rank != 0) {
+        const uint32_t slot = map_to_rank(s_inbox + (rank - 1) * stride, 0);
+        // s_m, s_l, s_acc are contiguous: m[8], l[8], acc[8][D]; the first `stride` floats are the state
+        for (int e = threadIdx.x; e < stride; e += C::kThreads)
             asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(slot + 4u * e), "f"(s_m[e]) : "memory");
     }
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -599,17 +602,18 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     KVC_TRACE_MARK(6);
-    const int stride = 16 + 8 * D;  // floats per inbox slot
+    // source c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c
+    auto src = [&](int c) -> const float* { return c == 0 ? s_m : s_inbox + (c - 1) * stride; };
     // pass 1, one thread per head: cluster maximum and every CTA's weight (times 1/L when final)
     if (threadIdx.x < p.G) {
         const int gg = threadIdx.x;
         float M = -INFINITY;
         for (int c = 0; c < cs; ++c)
-            if (s_inbox[c * stride + 8 + gg] > 0.f) M = fmaxf(M, s_inbox[c * stride + gg]);
+            if (src(c)[8 + gg] > 0.f) M = fmaxf(M, src(c)[gg]);
         float L = 0.f;
         for (int c = 0; c < cs; ++c) {
-            const float l = s_inbox[c * stride + 8 + gg];
-            const float w = l > 0.f ? ex2(s_inbox[c * stride + gg] - M) : 0.f;  // a CTA without blocks: 0
+            const float l = src(c)[8 + gg];
+            const float w = l > 0.f ? ex2(src(c)[gg] - M) : 0.f;  // a CTA without blocks: 0
             s_wgt[c * 8 + gg] = w;
             L += l * w;
         }
@@ -627,7 +631,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
         const int gg = e / D, d = e % D;
         float O = 0.f;
-        for (int c = 0; c < cs; ++c) O += s_wgt[c * 8 + gg] * s_inbox[c * stride + 16 + gg * D + d];
+        for (int c = 0; c < cs; ++c) O += s_wgt[c * 8 + gg] * src(c)[16 + gg * D + d];
         const int64_t h = kvh * p.G + gg;
         if (nclus == 1)
             store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, O);
@@ -706,30 +710,54 @@ static int sm_count() {
     return n;
 }
 
-// one-time kernel attributes and the resident CTAs per SM of the decode kernel
+// one-time kernel attributes (largest shared-memory size this kernel can be launched with)
 template <int D>
-static cudaError_t decode_setup(int* ctas_per_sm) {
+static cudaError_t decode_setup() {
     using C = DecodeCfg<D>;
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
-    static int occ = 0;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::smem_bytes(kMaxCluster, 8));
         if (err == cudaSuccess && kMaxCluster > 8)
             err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (err == cudaSuccess)
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kThreads,
-                                                                C::kSmemBytes);
-        if (err == cudaSuccess && occ < 1) err = cudaErrorInvalidConfiguration;
     });
-    if (ctas_per_sm) *ctas_per_sm = occ;
     return err;
+}
+
+// resident CTAs per SM of the decode kernel with `smem` bytes of dynamic shared memory (cached)
+template <int D>
+static cudaError_t decode_occupancy(int smem, int* ctas) {
+    using C = DecodeCfg<D>;
+    static std::mutex mu;
+    static int cached_smem[64] = {0}, cached_occ[64] = {0};
+    cudaError_t e = decode_setup<D>();
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < 64; ++i)
+        if (cached_smem[i] == smem) {
+            *ctas = cached_occ[i];
+            return cudaSuccess;
+        }
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    for (int i = 0; i < 64; ++i)
+        if (cached_smem[i] == 0) {
+            cached_smem[i] = smem;
+            cached_occ[i] = occ;
+            break;
+        }
+    *ctas = occ;
+    return cudaSuccess;
 }
 
 template <int D>
 static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, DecodePlan* plan) {
     using C = DecodeCfg<D>;
     const int nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
+    const int G = std::max(1, Hq / std::max(Hkv, 1));
     int cs, bpc;
     if (bpc_req > 0) {
         bpc = std::min(bpc_req, kMaxClusterBlocks);
@@ -737,19 +765,28 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
     } else {
         const int sms = sm_count();
         if (sms <= 0) return cudaErrorNoDevice;
+        // one wave of KVC_DEC_PLAN_CTAS CTAs per SM for all (sequence, KV head) pairs, at least one block per
+        // warp; recomputed once if the chosen cluster's inbox lowers the occupancy below that
         int occ = 0;
-        cudaError_t e = decode_setup<D>(&occ);
+        cudaError_t e = decode_occupancy<D>(C::smem_bytes(1, G), &occ);
         if (e != cudaSuccess) return e;
-        // one wave: the CTAs of all (sequence, KV head) pairs resident at once, at least one block per warp
-        const int64_t segs = static_cast<int64_t>(B) * Hkv;
-        const int64_t per_seg = std::max<int64_t>(1, static_cast<int64_t>(sms) * occ / std::max<int64_t>(segs, 1));
-        cs = static_cast<int>(std::max<int64_t>(
-            1, std::min<int64_t>({kMaxCluster, per_seg, (nblk + C::kWarps - 1) / C::kWarps})));
-        int64_t ncl = std::max<int64_t>(
-            1, std::min<int64_t>(per_seg / cs, (nblk + static_cast<int64_t>(cs) * C::kWarps - 1) /
-                                                   (static_cast<int64_t>(cs) * C::kWarps)));
-        ncl = std::max<int64_t>(ncl, (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks);
-        bpc = static_cast<int>((nblk + ncl - 1) / ncl);
+        const int64_t segs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
+        for (int pass = 0; pass < 2; ++pass) {
+            const int64_t slots = static_cast<int64_t>(sms) * std::min(occ, KVC_DEC_PLAN_CTAS);
+            const int64_t per_seg = std::max<int64_t>(1, slots / segs);
+            cs = static_cast<int>(std::max<int64_t>(
+                1, std::min<int64_t>({kMaxCluster, per_seg, (nblk + C::kWarps - 1) / C::kWarps})));
+            int64_t ncl = std::max<int64_t>(
+                1, std::min<int64_t>(per_seg / cs, (nblk + static_cast<int64_t>(cs) * C::kWarps - 1) /
+                                                       (static_cast<int64_t>(cs) * C::kWarps)));
+            ncl = std::max<int64_t>(ncl, (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks);
+            bpc = static_cast<int>((nblk + ncl - 1) / ncl);
+            int occ2 = 0;
+            e = decode_occupancy<D>(C::smem_bytes(cs, G), &occ2);
+            if (e != cudaSuccess) return e;
+            if (occ2 >= std::min(occ, KVC_DEC_PLAN_CTAS)) break;
+            occ = occ2;
+        }
     }
     const int nparts = (nblk + bpc - 1) / bpc;
     plan->blocks_per_split = bpc;
@@ -829,7 +866,7 @@ static cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStr
 template <int D>
 static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     using C = DecodeCfg<D>;
-    cudaError_t e = decode_setup<D>(nullptr);
+    cudaError_t e = decode_setup<D>();
     if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
     CUtensorMap tmK, tmV;
@@ -870,7 +907,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
 
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
-    e = launch(paged_decode_kernel<D>, grid, dim3(C::kThreads), C::kSmemBytes, stream, pdl,
+    e = launch(paged_decode_kernel<D>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream, pdl,
                static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
