@@ -225,9 +225,15 @@ kvc_status paged_decode_append_attention(const void* q, const void* k_new, const
  * launched as programmatic dependents of the kernel before them on the
  * stream: they read block tables, context lengths and the cached K/V
  * history before that kernel has finished, and q, k_new, v_new, the
- * workspace and out only after.  Contract: the kernel launched immediately
- * before a decode call must not write its block table, context lengths or
- * the cache rows the call reads (other than through this call's append). */
+ * workspace and out only after.  A decode kernel releases its own
+ * dependents as soon as it starts, so in an unbroken run of decode calls on
+ * one stream (no other kernel, copy or event between them) a call may start
+ * before any earlier call of the run has finished.  Contract: no kernel of
+ * that run, nor the kernel launched just before the run, writes a call's
+ * block table, context lengths or the cache rows it reads (other than
+ * through that call's own append).  One call per layer, every layer a
+ * different cache, meets this; calls on the same layer need something
+ * between them (a copy, an event, another kernel). */
 kvc_status kvc_set_launch_overlap(int on);
 
 /* Per-CTA timeline of decode launches (builds with -DKVC_TRACE=1 only;

@@ -241,6 +241,14 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
 #endif
     KVC_TRACE_MARK(0);
 
+    // each warp owns its barriers; lane 0 initialises them before it has any load outstanding, so
+    // the release fence that publishes the initialisation has nothing to wait for
+    uint64_t* wbars = bars + warp * ST;
+    if (lane == 0) {
+        for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
+        fence_barrier_init();
+    }
+
     // One round trip before the first copies: each warp's lane 0 fetches the table entries of its
     // static first round and the context length together; the cluster's whole slice of the table
     // (entries [cb0, cb0 + bpc), clipped to the row) goes to shared memory meanwhile, for the refills.
@@ -273,7 +281,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     if (cidx >= nclus) return;                     // the whole cluster is past the context
     const int cb1 = min(cb0 + p.bpc, nblk);        // this cluster covers blocks [cb0, cb1)
 
-    uint64_t* wbars = bars + warp * ST;
     uint8_t* wring = smem + warp * C::kWarpRingBytes;
     const uint64_t policy = l2_policy_evict_first();
 
@@ -294,8 +301,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
             tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
         }
     };
-    // each warp owns its barriers: lane 0 initialises them and issues the static first round
-    // (stage s gets block cb0 + gw + s * warps-in-the-cluster) without waiting for the rest of the CTA
+    // lane 0 issues the warp's static first round (stage s gets block cb0 + gw + s * warps-in-the-
+    // cluster) without waiting for the rest of the CTA
     int blk[ST];
 #pragma unroll
     for (int s = 0; s < ST; ++s) {
@@ -303,8 +310,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         blk[s] = j < cb1 ? j : -1;
     }
     if (lane == 0) {
-        for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
-        fence_barrier_init();
         if (warp == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
@@ -318,8 +323,14 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     KVC_TRACE_MARK(1);
 
     __syncthreads();  // the table slice (and, in rank 0, the counter) is in shared memory
+#if KVC_DEC_STEAL
     // the counter is visible cluster-wide once every CTA has passed the matching wait below
     if (cs > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+#else
+    // announces that this CTA has started; the matching wait comes before the first remote store
+    // into rank 0's shared memory. Nothing is published here, so the arrive needs no fence.
+    if (cs > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+#endif
 
     // ---- everything below may read what the previous kernel wrote ----
     grid_dependency_wait();
@@ -347,13 +358,13 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         app_val = *reinterpret_cast<const uint4*>(src);
     }
 
+#if KVC_DEC_STEAL
     // the counter lives in rank 0's shared memory
     uint32_t counter_addr = 0;
     if (cs > 1) {
         asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
         counter_addr = map_to_rank(s_counter, 0);
     }
-#if KVC_DEC_STEAL
     auto grab = [&]() -> int {  // lane 0 only
         if (cs > 1) {
             int v;
@@ -588,6 +599,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     __syncthreads();  // this CTA's s_m / s_l / s_acc are complete
     KVC_TRACE_MARK(5);
     const int stride = 16 + p.G * D;  // floats per inbox slot: m[8], l[8], acc[G][D]
+#if !KVC_DEC_STEAL
+    // every CTA of the cluster has started (the prologue arrive), so rank 0's shared memory is live
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+#endif
     if (rank != 0) {
         const uint32_t slot = map_to_rank(s_inbox + (rank - 1) * stride, 0);
         // s_m, s_l, s_acc are contiguous: m[8], l[8], acc[8][D]; the first `stride` floats are the state
