@@ -55,6 +55,31 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
     return kv_bytes_per_step(ctx_total, 1) + B * HQ * D * 2 * 2 + nblocks_total * 4 + B * 4
 
 
+# DRAM traffic of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture of
+# `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
+DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/ptx.cuh",
+                  "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
+NCU_DECODE_TRAFFIC = {"sources_sha256": "37c0665d7716666d6663075fafeac69cfa270d821231616b77145aea1a066db9",
+                      "bytes_per_launch": 33681152 + 0}
+
+
+def decode_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """Bytes per launch from the ncu capture, or None once the decode sources have changed since."""
+    rec = NCU_DECODE_TRAFFIC
+    if rec["bytes_per_launch"] is None or rec["sources_sha256"] != decode_sources_sha256():
+        return None
+    return rec["bytes_per_launch"]
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -341,7 +366,7 @@ def run_ours(args):
         "tokens_per_s": B * world / (ms_step * 1e-3),
         "pct_hbm_peak": gbs / world / peak * 100.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": measured_traffic(), "peak_kind": peak_kind,
                      "kernel": ("paged_decode_append_attention" if fused else "paged_decode_attention")
                                + " call, one layer (split merge inside the kernel, on chip)",
                      "bytes_per_launch": call_bytes, "us_per_launch": us_decode},
