@@ -162,6 +162,12 @@ def barrier_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Units all ranks processed per second: every rank runs its own replica (weak scaling) and the step time
+    is the slowest rank's."""
+    return units_per_rank * world / (ms_per_step_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------
 # reference arm / CPU baseline: the fp64 oracle as it stands
 # ---------------------------------------------------------------------------
@@ -349,7 +355,7 @@ def run_ours(args):
                          f"{secs:.1f} s of oracle time"}
 
     peak, peak_kind = load_peaks()
-    gbs = step_bytes * world / (ms_step * 1e-3) / 1e9
+    gbs = whole_job_rate(step_bytes, world, ms_step) / 1e9
     call_bytes = decode_call_bytes(ctx_total, nblocks_total) + (B * HKV * D * 2 * 2 * 2 if fused else 0)
     achieved = call_bytes / (us_decode * 1e-6) / 1e9
     line = {
@@ -363,7 +369,7 @@ def run_ours(args):
                                                                              ", programmatic dependent launch"),
                    "append": "fused into the decode kernel" if fused else "separate kv_append kernel",
                    "next_layer_l2_prefetch": bool(fused and args.prefetch)},
-        "tokens_per_s": B * world / (ms_step * 1e-3),
+        "tokens_per_s": whole_job_rate(B, world, ms_step),
         "pct_hbm_peak": gbs / world / peak * 100.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": measured_traffic(), "peak_kind": peak_kind,
@@ -371,7 +377,7 @@ def run_ours(args):
                                + " call, one layer (split merge inside the kernel, on chip)",
                      "bytes_per_launch": call_bytes, "us_per_launch": us_decode},
         "cpu_baseline": cpu,
-        "e2e": {"value": step_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
+        "e2e": {"value": whole_job_rate(step_bytes, world, ms_e2e) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
