@@ -104,7 +104,7 @@ struct DecodeCfg {
     static constexpr int kWarpRingBytes = kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
-    static constexpr int kStateBytes = (8 * (D + 2) + 16 * 8) * 4;  // merged (m, l, acc) of 8 heads + merge weights
+    static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA
     static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice + block counter
     // + the inbox of cluster rank 0 (one slot per other CTA of the cluster, sized at launch) + alignment slack
     static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + kTableBytes + 1024;
@@ -205,6 +205,9 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
@@ -216,13 +219,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
     // the CTA's merged state: m[8], l[8], acc[8][D]
+    // this CTA's merged state when it is cluster rank 0: m[8], l[8], acc[G][D] (the layout of an inbox slot)
     float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
-    float* s_l = s_m + 8;
-    float* s_acc = s_m + 16;
-    float* s_wgt = s_acc + 8 * D;  // [16 sources][8 heads] merge weights
     int* s_table = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
     int* s_counter = s_table + kMaxClusterBlocks;  // next block to hand out (used in cluster rank 0)
-    // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like s_m / s_l / s_acc[0..G)
+    // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like the state at s_m
     float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes + C::kTableBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -544,71 +545,63 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     KVC_TRACE_MARK(4);
 
     const bool direct = nclus == 1 && cs == 1;  // a single CTA holds the whole context
-    // pass 1, one thread per head: the CTA maximum and every warp's weight 2^(m_w - M) (times 1/L when
-    // this CTA's result is final)
-    if (threadIdx.x < p.G) {
-        const int gg = threadIdx.x;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes)[gg]);
-        float L = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float* r = reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes);
-            const float wgt = M == -INFINITY ? 0.f : ex2(r[gg] - M);  // an empty warp has m = -inf: weight 0
-            s_wgt[w * 8 + gg] = wgt;
-            L += r[8 + gg] * wgt;
-        }
-        if (direct) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) s_wgt[w * 8 + gg] *= inv;
-        }
-        s_m[gg] = M;
-        s_l[gg] = L;
-        if (!direct && cs == 1) {  // one CTA per cluster: its state is the cluster's partial
-            const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx;
-            p.part_ml[row * 2 + 0] = M;
-            p.part_ml[row * 2 + 1] = L;
-        }
+    const int stride = 16 + p.G * D;  // floats per cluster merge slot: m[8], l[8], acc[G][D]
+    // in a cluster this CTA's merged state goes to its slot in rank 0: rank 0's own state at s_m, or
+    // inbox slot rank - 1 (same layout)
+    uint32_t slot = 0;
+    if (cs > 1) {
+#if !KVC_DEC_STEAL
+        // every CTA of the cluster has started (the prologue arrive), so rank 0's shared memory is live
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+#endif
+        slot = map_to_rank(rank == 0 ? s_m : s_inbox + (rank - 1) * stride, 0);
     }
-    __syncthreads();
-    // pass 2: acc = sum over warps of weight * acc_w
-    for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
-        const int gg = e / D, d = e % D;
-        float O = 0.f;
+    // every thread merges the warps of this CTA for its own outputs (head gg, dim d): it takes the CTA
+    // maximum M of its head and the warp weights 2^(m_w - M) itself, so no further barrier is needed
+    {
+        constexpr int kRingF = C::kWarpRingBytes / 4;
+        const float* wst = reinterpret_cast<const float*>(smem);  // warp w's parked state at w * kRingF
+        for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
+            const int gg = e / D, d = e % D;
+            float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-            O += s_wgt[w * 8 + gg] *
-                 reinterpret_cast<const float*>(smem + w * C::kWarpRingBytes)[16 + gg * C::kMergeStride + d];
-        if (direct)
-            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * D + d, O);
-        else if (cs == 1)
-            p.part_acc[((static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx) * D + d] = O;
-        else
-            s_acc[gg * D + d] = O;
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[w * kRingF + gg]);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float* r = wst + w * kRingF;
+                const float wgt = M == -INFINITY ? 0.f : ex2(r[gg] - M);  // an empty warp has m = -inf: weight 0
+                L += r[8 + gg] * wgt;
+                O += wgt * r[16 + gg * C::kMergeStride + d];
+            }
+            const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
+            if (direct) {
+                store_out(p.out, p.out_f32, h * D + d, L > 0.f ? O * (1.f / L) : 0.f);
+            } else if (cs == 1) {  // one CTA per cluster: its state is the cluster's partial
+                const int64_t row = h * p.nparts + cidx;
+                p.part_acc[row * D + d] = O;
+                if (d == 0) {
+                    p.part_ml[row * 2 + 0] = M;
+                    p.part_ml[row * 2 + 1] = L;
+                }
+            } else {
+                st_cluster_f32(slot + 4u * (16 + gg * D + d), O);
+                if (d == 0) {
+                    st_cluster_f32(slot + 4u * gg, M);
+                    st_cluster_f32(slot + 4u * (8 + gg), L);
+                }
+            }
+        }
     }
     if (cs == 1) {
         KVC_TRACE_END();
         return;
     }
-
-    // ---- merge the CTAs of this cluster in rank 0: every CTA pushes its state into rank 0's inbox
-    // (remote stores, no round trip), arrives on the cluster barrier and leaves; rank 0 waits for all
-    // arrivals, which makes the pushed states visible to it, and merges locally ----
-    __syncthreads();  // this CTA's s_m / s_l / s_acc are complete
     KVC_TRACE_MARK(5);
-    const int stride = 16 + p.G * D;  // floats per inbox slot: m[8], l[8], acc[G][D]
-#if !KVC_DEC_STEAL
-    // every CTA of the cluster has started (the prologue arrive), so rank 0's shared memory is live
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-#endif
-    if (rank != 0) {
-        const uint32_t slot = map_to_rank(s_inbox + (rank - 1) * stride, 0);
-        // s_m, s_l, s_acc are contiguous: m[8], l[8], acc[8][D]; the first `stride` floats are the state
-        for (int e = threadIdx.x; e < stride; e += C::kThreads)
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(slot + 4u * e), "f"(s_m[e]) : "memory");
-    }
+
+    // ---- merge the CTAs of this cluster in rank 0: every CTA has pushed its state into its slot (remote
+    // stores, no round trip); it arrives on the cluster barrier (release) and leaves. Rank 0 waits for all
+    // arrivals (acquire), which makes every slot visible to it, and merges locally ----
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (rank != 0) {
         KVC_TRACE_MARK(6);
@@ -617,41 +610,33 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     KVC_TRACE_MARK(6);
-    // source c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c
+    // slot c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c; a CTA without
+    // blocks has l = 0 and takes no part
     auto src = [&](int c) -> const float* { return c == 0 ? s_m : s_inbox + (c - 1) * stride; };
-    // pass 1, one thread per head: cluster maximum and every CTA's weight (times 1/L when final)
-    if (threadIdx.x < p.G) {
-        const int gg = threadIdx.x;
+    for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
+        const int gg = e / D, d = e % D;
         float M = -INFINITY;
         for (int c = 0; c < cs; ++c)
             if (src(c)[8 + gg] > 0.f) M = fmaxf(M, src(c)[gg]);
-        float L = 0.f;
+        float L = 0.f, O = 0.f;
         for (int c = 0; c < cs; ++c) {
-            const float l = src(c)[8 + gg];
-            const float w = l > 0.f ? ex2(src(c)[gg] - M) : 0.f;  // a CTA without blocks: 0
-            s_wgt[c * 8 + gg] = w;
+            const float* r = src(c);
+            const float l = r[8 + gg];
+            const float w = l > 0.f ? ex2(r[gg] - M) : 0.f;
             L += l * w;
+            O += w * r[16 + gg * D + d];
         }
+        const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
         if (nclus == 1) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (int c = 0; c < cs; ++c) s_wgt[c * 8 + gg] *= inv;
+            store_out(p.out, p.out_f32, h * D + d, L > 0.f ? O * (1.f / L) : 0.f);
         } else {
-            const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.nparts + cidx;
-            p.part_ml[row * 2 + 0] = M;
-            p.part_ml[row * 2 + 1] = L;
+            const int64_t row = h * p.nparts + cidx;
+            p.part_acc[row * D + d] = O;
+            if (d == 0) {
+                p.part_ml[row * 2 + 0] = M;
+                p.part_ml[row * 2 + 1] = L;
+            }
         }
-    }
-    __syncthreads();
-    // pass 2: acc = sum over the cluster's CTAs of weight * acc_c
-    for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
-        const int gg = e / D, d = e % D;
-        float O = 0.f;
-        for (int c = 0; c < cs; ++c) O += s_wgt[c * 8 + gg] * src(c)[16 + gg * D + d];
-        const int64_t h = kvh * p.G + gg;
-        if (nclus == 1)
-            store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, O);
-        else
-            p.part_acc[((static_cast<int64_t>(b) * p.Hq + h) * p.nparts + cidx) * D + d] = O;
     }
     KVC_TRACE_END();
 }
