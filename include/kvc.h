@@ -187,7 +187,8 @@ kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stre
  *   block_table  device int32 [B][max_blocks]
  *   context_lens device int32 [B], 1 <= ctx <= min(max_blocks*bs, max_context_len)
  *   out          device [B][Hq][D], out_dtype KVC_F16 or KVC_F32
- *   workspace    device, >= paged_decode_plan(...)'s bytes (may be NULL when that is 0)
+ *   workspace    device, 16-byte aligned, >= paged_decode_plan(...)'s bytes (may be NULL when
+ *                that is 0)
  * The context of each sequence is cut into splits of blocks_per_split blocks;
  * each (sequence, KV head, split) is one CTA that keeps the running max and
  * exp-sum per query head; the splits merge with the rescaling rule of the

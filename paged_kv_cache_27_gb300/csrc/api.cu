@@ -471,6 +471,7 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
     if (e != cudaSuccess) return cuda_fail(e, "decode plan");
     if (plan.workspace_bytes > workspace_bytes || (plan.workspace_bytes && !workspace))
         return fail(KVC_ERR_INVALID, "workspace too small: need %zu bytes", plan.workspace_bytes);
+    if (plan.workspace_bytes && !aligned16(workspace)) return fail(KVC_ERR_INVALID, "workspace must be 16-byte aligned");
     e = kvc::device_error_word(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     e = kvc::launch_decode(a, as_stream(stream));

@@ -192,6 +192,21 @@ __device__ __forceinline__ void store_out(void* out, int out_f32, int64_t idx, f
     else
         static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
+// four consecutive outputs starting at idx (a multiple of 4)
+__device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, float4 v) {
+    if (out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+    } else {
+        uint2 h;
+        h.x = pack_half2(v.x, v.y);
+        h.y = pack_half2(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) = h;
+    }
+}
+__device__ __forceinline__ float4 fma4(float w, float4 a, float4 acc) {
+    return make_float4(fmaf(w, a.x, acc.x), fmaf(w, a.y, acc.y), fmaf(w, a.z, acc.z), fmaf(w, a.w, acc.w));
+}
+__device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
 
 // ---- thread-block cluster helpers ------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -556,36 +571,40 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
 #endif
         slot = map_to_rank(rank == 0 ? s_m : s_inbox + (rank - 1) * stride, 0);
     }
-    // every thread merges the warps of this CTA for its own outputs (head gg, dim d): it takes the CTA
-    // maximum M of its head and the warp weights 2^(m_w - M) itself, so no further barrier is needed
+    // every thread merges the warps of this CTA for four consecutive outputs (head gg, dims d..d+3): it
+    // takes the CTA maximum M of its head and the warp weights 2^(m_w - M) itself, so no further barrier
+    // is needed
     {
         constexpr int kRingF = C::kWarpRingBytes / 4;
         const float* wst = reinterpret_cast<const float*>(smem);  // warp w's parked state at w * kRingF
-        for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
+        for (int e = 4 * threadIdx.x; e < p.G * D; e += 4 * C::kThreads) {
             const int gg = e / D, d = e % D;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[w * kRingF + gg]);
-            float L = 0.f, O = 0.f;
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
                 const float* r = wst + w * kRingF;
                 const float wgt = M == -INFINITY ? 0.f : ex2(r[gg] - M);  // an empty warp has m = -inf: weight 0
                 L += r[8 + gg] * wgt;
-                O += wgt * r[16 + gg * C::kMergeStride + d];
+                O = fma4(wgt, *reinterpret_cast<const float4*>(r + 16 + gg * C::kMergeStride + d), O);
             }
             const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
             if (direct) {
-                store_out(p.out, p.out_f32, h * D + d, L > 0.f ? O * (1.f / L) : 0.f);
+                store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
             } else if (cs == 1) {  // one CTA per cluster: its state is the cluster's partial
                 const int64_t row = h * p.nparts + cidx;
-                p.part_acc[row * D + d] = O;
+                *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
                 if (d == 0) {
                     p.part_ml[row * 2 + 0] = M;
                     p.part_ml[row * 2 + 1] = L;
                 }
             } else {
-                st_cluster_f32(slot + 4u * (16 + gg * D + d), O);
+                asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(slot + 4u * (16 + e)),
+                             "f"(O.x), "f"(O.y), "f"(O.z), "f"(O.w)
+                             : "memory");
                 if (d == 0) {
                     st_cluster_f32(slot + 4u * gg, M);
                     st_cluster_f32(slot + 4u * (8 + gg), L);
@@ -613,25 +632,26 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // slot c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c; a CTA without
     // blocks has l = 0 and takes no part
     auto src = [&](int c) -> const float* { return c == 0 ? s_m : s_inbox + (c - 1) * stride; };
-    for (int e = threadIdx.x; e < p.G * D; e += C::kThreads) {
+    for (int e = 4 * threadIdx.x; e < p.G * D; e += 4 * C::kThreads) {
         const int gg = e / D, d = e % D;
         float M = -INFINITY;
         for (int c = 0; c < cs; ++c)
             if (src(c)[8 + gg] > 0.f) M = fmaxf(M, src(c)[gg]);
-        float L = 0.f, O = 0.f;
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c = 0; c < cs; ++c) {
             const float* r = src(c);
             const float l = r[8 + gg];
             const float w = l > 0.f ? ex2(r[gg] - M) : 0.f;
             L += l * w;
-            O += w * r[16 + gg * D + d];
+            O = fma4(w, *reinterpret_cast<const float4*>(r + 16 + e), O);
         }
         const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
         if (nclus == 1) {
-            store_out(p.out, p.out_f32, h * D + d, L > 0.f ? O * (1.f / L) : 0.f);
+            store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
         } else {
             const int64_t row = h * p.nparts + cidx;
-            p.part_acc[row * D + d] = O;
+            *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
             if (d == 0) {
                 p.part_ml[row * 2 + 0] = M;
                 p.part_ml[row * 2 + 1] = L;
@@ -793,7 +813,9 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
     plan->cluster = cs;
     plan->num_parts = nparts;
     plan->num_splits = nparts * cs;  // grid.x: whole clusters
-    plan->workspace_bytes = nparts > 1 ? static_cast<size_t>(B) * Hq * nparts * (2 + D) * sizeof(float) : 0;
+    // (m, l) rows, padded to a multiple of 4 floats so that the acc rows after them are 16-byte aligned
+    const size_t nrow = static_cast<size_t>(B) * Hq * nparts;
+    plan->workspace_bytes = nparts > 1 ? (((nrow * 2 + 3) & ~static_cast<size_t>(3)) + nrow * D) * sizeof(float) : 0;
     return cudaSuccess;
 }
 
@@ -888,7 +910,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.out = a.out;
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
     p.part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    p.part_acc = plan.num_parts > 1 ? p.part_ml + nrow * 2 : nullptr;
+    p.part_acc = plan.num_parts > 1 ? p.part_ml + ((nrow * 2 + 3) & ~static_cast<size_t>(3)) : nullptr;
     p.err = a.err;
     p.max_blocks = a.max_blocks;
     p.num_blocks = a.num_blocks;
