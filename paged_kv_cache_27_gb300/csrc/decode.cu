@@ -74,6 +74,9 @@ namespace kvc {
 #ifndef KVC_DEC_EARLY_TRIGGER  // let the next kernel launch as soon as every CTA of this one has started
 #define KVC_DEC_EARLY_TRIGGER 1
 #endif
+#ifndef KVC_DEC_EARLY_REFILL  // 1: refill a stage once its K and V are in registers, before the softmax
+#define KVC_DEC_EARLY_REFILL 1
+#endif
 #ifndef KVC_DEC_MIN_CTAS  // resident CTAs per SM the register allocation must allow
 #define KVC_DEC_MIN_CTAS 1
 #endif
@@ -404,9 +407,30 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     uint32_t phase = 0;  // bit s: parity of stage s's next completion
     bool timed_out = false;
 
+    // refill stage s with the next block of the cluster's range, if any is left (after the warp has read it)
+    auto refill = [&](int s) {
+        __syncwarp();
+#if KVC_DEC_STEAL
+        const int nj = __shfl_sync(0xffffffffu, next_j, 0);
+#else
+        const int nj = next_j;
+        next_j = grab();
+#endif
+        if (nj < cb1 && lane == 0) {
+            issue(s, s_table[nj - cb0]);
+#if KVC_DEC_STEAL
+            next_j = grab();
+#endif
+        }
+#pragma unroll
+        for (int k = 0; k < ST; ++k)
+            if (k == s) blk[k] = nj < cb1 ? nj : -1;
+    };
+
 #pragma unroll 1
     for (int i = 0;; ++i) {
         const int s = i % ST;
+        bool refilled = false;
         int jj = -1;
 #pragma unroll
         for (int k = 0; k < ST; ++k)
@@ -445,8 +469,38 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                     ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                     mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
                 }
-                // ---- online softmax per head (column): this lane holds tokens g, g+8 of heads 2*t4, 2*t4+1 ----
                 const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
+                // rows of V past the context may hold any bits (even NaN): zero them in registers
+                uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+                if (rem < kBlockSize) {
+                    keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
+                    keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
+                }
+#if KVC_DEC_EARLY_REFILL
+                // V^T fragments now; the stage is then free and its refill goes out before the softmax
+                uint32_t va[D / 16][4];
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), va[mt][0], va[mt][1],
+                              va[mt][2], va[mt][3]);
+                    va[mt][0] &= keep0;
+                    va[mt][1] &= keep0;
+                    va[mt][2] &= keep1;
+                    va[mt][3] &= keep1;
+                }
+                {
+                    // the copy may overwrite the stage only once the warp's reads of it have returned: fold
+                    // the loaded registers (the K fragments were consumed by the S products above)
+                    uint32_t dep = 0;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
+                }
+                refill(s);
+                refilled = true;
+#endif
+                // ---- online softmax per head (column): this lane holds tokens g, g+8 of heads 2*t4, 2*t4+1 ----
                 float x[4];
                 x[0] = g < rem ? sc[0] * sl2 : -INFINITY;
                 x[1] = g < rem ? sc[1] * sl2 : -INFINITY;
@@ -479,42 +533,24 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                 const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
                 const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
                 const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
-                // rows of V past the context may hold any bits (even NaN): zero them in registers
-                uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
-                if (rem < kBlockSize) {
-                    keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
-                    keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
-                }
                 // ---- O^T += V^T P^T, one m-tile per 16 dims ----
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
+#if KVC_DEC_EARLY_REFILL
+                    const uint32_t a0 = va[mt][0], a1 = va[mt][1], a2 = va[mt][2], a3 = va[mt][3];
+#else
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
                     a0 &= keep0;
                     a1 &= keep0;
                     a2 &= keep1;
                     a3 &= keep1;
+#endif
                     mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
                     mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
                 }
             }
-            __syncwarp();
-            // refill this stage with the next block of the cluster's range, if any is left
-#if KVC_DEC_STEAL
-            const int nj = __shfl_sync(0xffffffffu, next_j, 0);
-#else
-            const int nj = next_j;
-            next_j = grab();
-#endif
-            if (nj < cb1 && lane == 0) {
-                issue(s, s_table[nj - cb0]);
-#if KVC_DEC_STEAL
-                next_j = grab();
-#endif
-            }
-#pragma unroll
-            for (int k = 0; k < ST; ++k)
-                if (k == s) blk[k] = nj < cb1 ? nj : -1;
+            if (!refilled) refill(s);
         }
     }
 #if !KVC_DEC_EARLY_TRIGGER
