@@ -59,8 +59,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/ptx.cuh",
                   "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "37c0665d7716666d6663075fafeac69cfa270d821231616b77145aea1a066db9",
-                      "bytes_per_launch": 33681152 + 0}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "ee27d4072fb6e6c9b7346824adae2e891da699b8cd9f0582ec0b150a93ed39b3",
+                      "bytes_per_launch": 33674624 + 0}
 
 
 def decode_sources_sha256() -> str:
