@@ -1,17 +1,27 @@
-// Varlen packed prefill attention for sm_103a.
+// Varlen packed prefill attention for sm_103a on the 5th-generation tensor cores.
 //
 // What it computes (xformers article of the "Aufmerksamkeit" feed,
 // chatgpz.de, parts 4 and 5): sequences of different lengths are packed
 // back to back without padding (cu_seqlens); each segment attends only to
 // itself (block-diagonal mask), causally (j <= i) or not; query head h reads
-// KV head h / (Hq / Hkv).  Per row: softmax(q K^T * scale) V.
+// KV head h / (Hq / Hkv).  Per row: softmax(q K^T * scale) V, with the
+// running-max / exp-sum rule of the FlashAttention article over key tiles.
 //
-// Design: one CTA per (64-row query tile of a segment, query head); 4 warps
-// of 16 query rows.  Q, K and V tiles of 64 tokens x 64 columns are fetched by
-// 3-D TMA (token, head, dim) with the 128-byte swizzle into a two-stage ring;
-// S = Q K^T and O += P V run on the tensor cores (mma.sync, fp16 in, fp32
-// accumulate, P split into fp16 high + residual); online softmax in fp32
-// base 2 (the FlashAttention article's running max / exp-sum rule).
+// Design: one CTA per (128-row query tile of a segment, query head), five
+// warps.  Lane 0 of warp 4 issues every TMA copy and every tcgen05.mma;
+// warps 0-3 own the 128 query rows (thread = row = TMEM lane) and run the
+// softmax.  Per 64-key tile j:
+//   S = Q K^T   tcgen05.mma M=128 x N=64, Q and K K-major in shared memory
+//               (128-byte swizzle, as TMA writes them), fp32 accumulator in TMEM
+//   softmax     the row threads read S from TMEM, mask (segment end, causal),
+//               keep the running max until it has grown by 2^8 (then rescale
+//               O in TMEM), and write P = hi + lo (two fp16 parts, so the
+//               product keeps ~fp32 accuracy) to shared memory, K-major
+//   O += P V    tcgen05.mma M=128 x N=64 per 64-dim chunk, V MN-major; O stays
+//               in TMEM across tiles
+// K and V have two-stage rings of their own; S(j+1) is issued as soon as the
+// row threads have read S(j), so the tensor cores work on it during softmax(j).
+// Every wait is bounded; a timeout sets an error bit and drains the CTA.
 #include <algorithm>
 #include <cmath>
 #include <cudaTypedefs.h>
@@ -20,23 +30,36 @@
 #include "../../include/kvc.h"
 #include "kvc_internal.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace kvc {
 
-constexpr int kPfRows = 64;   // query rows per CTA
-constexpr int kPfKeys = 64;   // keys per KV tile
-constexpr int kPfWarps = 4;
+constexpr int kPfRows = 128;  // query rows per CTA: the MMA's M, one TMEM lane each
+constexpr int kPfKeys = 64;   // keys per K/V tile: N of S, K of P V
+constexpr int kPfRowWarps = 4;
+constexpr int kPfThreads = (kPfRowWarps + 1) * 32;
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 constexpr float kPfLog2e = 1.4426950408889634f;
+constexpr float kPfRescaleLog2 = 8.f;  // P stays below 2^8, far inside fp16
 
 template <int D>
-struct PrefillGeom {
-    static constexpr int kHalf = 64 * 128;                // one 64-row x 64-col swizzled box: 8 KiB
-    static constexpr int kTileBytes = (D / 64) * kHalf;   // 64 rows x D
+struct PfGeom {
+    static constexpr int kChunks = D / 64;                    // 64-dim (128-byte) column chunks
+    static constexpr int kQChunk = kPfRows * 128;             // 16 KiB
+    static constexpr int kKVChunk = kPfKeys * 128;            // 8 KiB
+    static constexpr int kQBytes = kChunks * kQChunk;
+    static constexpr int kKVBytes = kChunks * kKVChunk;       // one K or V tile
+    static constexpr int kPBytes = kPfRows * kPfKeys * 2;     // 16 KiB
     static constexpr int kQOff = 0;
-    static constexpr int kKVOff = kTileBytes;             // 2 stages x (K, V)
-    static constexpr int kBarOff = kKVOff + 4 * kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 64 + 1024;
+    static constexpr int kKOff = kQOff + kQBytes;             // 2 stages
+    static constexpr int kVOff = kKOff + 2 * kKVBytes;        // 2 stages
+    static constexpr int kPhiOff = kVOff + 2 * kKVBytes;
+    static constexpr int kPloOff = kPhiOff + kPBytes;
+    static constexpr int kBarOff = kPloOff + kPBytes;
+    static constexpr int kSmemBytes = kBarOff + 128 + 1024;  // barriers, TMEM address, abort flag; alignment
+    static constexpr int kTmemS = 0;                          // S: columns [0, 64)
+    static constexpr int kTmemO = kPfKeys;                    // O: columns [64, 64 + D)
+    static constexpr uint32_t kTmemCols = kPfKeys + D <= 128 ? 128 : 256;
 };
 
 struct PrefillKernelParams {
@@ -47,9 +70,10 @@ struct PrefillKernelParams {
     float scale_log2;
 };
 
-// 64-row tile, 128-byte swizzle, boxes of 64 columns stacked at 8 KiB
-__device__ __forceinline__ uint32_t pswz(int row, int chunk) {
-    return static_cast<uint32_t>(((chunk >> 3) << 13) + (row << 7) + (((chunk & 7) ^ (row & 7)) << 4));
+// byte offset of 16-byte chunk c (0..7) of row `row` in a 1024-byte aligned tile of 128-byte rows, 128-byte
+// swizzle (the layout TMA writes and the MMA reads)
+__device__ __forceinline__ uint32_t sw128(int row, int c) {
+    return static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
@@ -61,18 +85,44 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Wait for a phase; gives up when another thread of the CTA has given up (abort flag) or after the limit,
+// in which case it raises the flag itself.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((i & 63u) == 63u && global_timer_ns() - t0 > kPfWaitNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kPfWarps * 32) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                                const __grid_constant__ CUtensorMap tmK,
-                                                                const __grid_constant__ CUtensorMap tmV,
-                                                                const PrefillKernelParams p) {
-    using Geo = PrefillGeom<D>;
+__global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                             const __grid_constant__ CUtensorMap tmK,
+                                                             const __grid_constant__ CUtensorMap tmV,
+                                                             const PrefillKernelParams p) {
+    using Geo = PfGeom<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kBarOff);  // [0] Q, [1..2] KV stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kBarOff);
+    uint64_t* q_full = bars + 0;
+    uint64_t* k_full = bars + 1;   // [2] K tile landed
+    uint64_t* v_full = bars + 3;   // [2] V tile landed
+    uint64_t* k_empty = bars + 5;  // [2] S products of the stage's tile done
+    uint64_t* v_empty = bars + 7;  // [2] P V products of the stage's tile done
+    uint64_t* s_full = bars + 9;   // S of the current tile in TMEM
+    uint64_t* s_free = bars + 10;  // the row warps have read S (4 arrivals)
+    uint64_t* p_full = bars + 11;  // P of the current tile in shared memory (4 arrivals)
+    uint64_t* o_full = bars + 12;  // P V of the current tile done
+    uint64_t* fin = bars + 13;     // every MMA issued so far done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 14);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 14) + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t4 = lane & 3;
     const int seg = blockIdx.x / p.tiles_per_seq, tile = blockIdx.x % p.tiles_per_seq;
     const int h = blockIdx.y, hk = h / p.G;
 
@@ -90,179 +140,275 @@ __global__ void __launch_bounds__(kPfWarps * 32) prefill_kernel(const __grid_con
     const int ntiles = (kv_len + kPfKeys - 1) / kPfKeys;
 
     uint8_t* qs = smem + Geo::kQOff;
-    auto kv_stage = [&](int st) { return smem + Geo::kKVOff + st * 2 * Geo::kTileBytes; };
+    uint8_t* phi = smem + Geo::kPhiOff;
+    uint8_t* plo = smem + Geo::kPloOff;
+    auto kst = [&](int st) { return smem + Geo::kKOff + st * Geo::kKVBytes; };
+    auto vst = [&](int st) { return smem + Geo::kVOff + st * Geo::kKVBytes; };
 
-    auto issue_kv = [&](int kt) {
-        uint64_t* bar = &bars[1 + (kt & 1)];
-        uint8_t* st = kv_stage(kt & 1);
-        mbar_arrive_expect_tx(bar, 2 * Geo::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < D; x += 64) {
-            tma_load_3d(st + (x / 64) * Geo::kHalf, &tmK, bar, x, hk, beg + kt * kPfKeys);
-            tma_load_3d(st + Geo::kTileBytes + (x / 64) * Geo::kHalf, &tmV, bar, x, hk, beg + kt * kPfKeys);
-        }
-    };
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
-        fence_barrier_init();
-        mbar_arrive_expect_tx(&bars[0], Geo::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < D; x += 64) tma_load_3d(qs + (x / 64) * Geo::kHalf, &tmQ, &bars[0], x, h, beg + r0);
-        issue_kv(0);
-        if (ntiles > 1) issue_kv(1);
-    }
-    __syncthreads();
-
-    const bool q_ok = __syncthreads_and(mbar_wait_bounded(&bars[0], 0, kPfWaitNs) ? 1 : 0) != 0;
-    // query fragments of this warp's 16 rows
-    uint32_t qa[D / 16][4];
-    if (q_ok) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            ldsm_x4(smem_u32(qs) + pswz(row, ks * 2 + (lane >> 4)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, kPfRowWarps);
+        mbar_init(p_full, kPfRowWarps);
+        mbar_init(o_full, 1);
+        mbar_init(fin, 1);
+        *s_abort = 0;
+        fence_barrier_init();
     }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, Geo::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t tS = tmem + Geo::kTmemS, tO = tmem + Geo::kTmemO;
 
-    float o[D / 8][4];
+    if (warp == kPfRowWarps) {
+        // ================= producer: TMA copies and tensor-core products (one thread) =================
+        if (lane == 0) {
+            auto load_k = [&](int t) {
+                uint64_t* bar = &k_full[t & 1];
+                mbar_arrive_expect_tx(bar, Geo::kKVBytes);
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    const int qi0 = r0 + warp * 16 + g;  // rows qi0 and qi0 + 8 of the segment
-
-    int fail_kt = q_ok ? -1 : 0;
-    for (int kt = 0; kt < ntiles && fail_kt < 0; ++kt) {
-        const bool good = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[1 + (kt & 1)], (kt >> 1) & 1, kPfWaitNs));
-        if (good) {
-            const uint32_t kbase = smem_u32(kv_stage(kt & 1));
-            const uint32_t vbase = kbase + Geo::kTileBytes;
-            float sc[kPfKeys / 8][4];
+                for (int c = 0; c < Geo::kChunks; ++c)
+                    tma_load_3d(kst(t & 1) + c * Geo::kKVChunk, &tmK, bar, c * 64, hk, beg + t * kPfKeys);
+            };
+            auto load_v = [&](int t) {
+                uint64_t* bar = &v_full[t & 1];
+                mbar_arrive_expect_tx(bar, Geo::kKVBytes);
 #pragma unroll
-            for (int nt = 0; nt < kPfKeys / 8; ++nt) {
-                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                for (int c = 0; c < Geo::kChunks; ++c)
+                    tma_load_3d(vst(t & 1) + c * Geo::kKVChunk, &tmV, bar, c * 64, hk, beg + t * kPfKeys);
+            };
+            prefetch_tensormap(&tmQ);
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            mbar_arrive_expect_tx(q_full, Geo::kQBytes);
 #pragma unroll
-                for (int kc = 0; kc < D / 32; ++kc) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + pswz(nt * 8 + (lane & 7), kc * 4 + (lane >> 3)), b0, b1, b2, b3);
-                    mma_f16_16816(sc[nt], qa[2 * kc][0], qa[2 * kc][1], qa[2 * kc][2], qa[2 * kc][3], b0, b1);
-                    mma_f16_16816(sc[nt], qa[2 * kc + 1][0], qa[2 * kc + 1][1], qa[2 * kc + 1][2],
-                                  qa[2 * kc + 1][3], b2, b3);
-                }
-            }
-            const int k0 = kt * kPfKeys;
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < kPfKeys / 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kj = k0 + nt * 8 + 2 * t4 + (e & 1);
-                    const int qi = qi0 + (e >> 1) * 8;
-                    const bool valid = kj < len && (!p.causal || kj <= qi);
-                    sc[nt][e] = valid ? sc[nt][e] * p.scale_log2 : -INFINITY;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], sc[nt][e]);
-                }
-            float alpha[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float m_new = fmaxf(m_run[r], mx[r]);
-                // a row may see no valid key in this tile yet (m stays -inf): keep it at zero weight
-                alpha[r] = m_new == -INFINITY ? 1.f : ex2(m_run[r] - m_new);
-                m_run[r] = m_new;
-            }
-            float ps[2] = {0.f, 0.f};
-#pragma unroll
-            for (int nt = 0; nt < kPfKeys / 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float mr = m_run[e >> 1];
-                    const float pv = mr == -INFINITY ? 0.f : ex2(sc[nt][e] - mr);
-                    sc[nt][e] = pv;
-                    ps[e >> 1] += pv;
-                }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + ps[r];
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                o[nd][0] *= alpha[0];
-                o[nd][1] *= alpha[0];
-                o[nd][2] *= alpha[1];
-                o[nd][3] *= alpha[1];
-            }
-            const int vrem = len - k0;  // keys of this tile inside the segment
-#pragma unroll
-            for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-                uint32_t ah[4], al[4];
+            for (int c = 0; c < Geo::kChunks; ++c)
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
+                    tma_load_3d(qs + c * Geo::kQChunk + half * 64 * 128, &tmQ, q_full, c * 64, h, beg + r0 + half * 64);
+            int k_issued = 0, v_issued = 0;  // tiles whose copies were issued
+            for (; k_issued < min(ntiles, 2); ++k_issued) load_k(k_issued);
+            for (; v_issued < min(ntiles, 2); ++v_issued) load_v(v_issued);
+            int k_done = 0, v_done = 0;  // tiles whose copies were waited for
+            bool q_done = false;
+
+            constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, 0, 0);
+            constexpr uint32_t idPV = umma_idesc_f16(kPfRows, 64, 0, 1);
+            const uint32_t q_addr = smem_u32(qs);
+            // S(j) = Q K(j)^T over D / 16 steps of 16 dims
+            auto mma_s = [&](int j) {
+                const uint32_t k_addr = smem_u32(kst(j & 1));
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const float p0 = sc[2 * kk + half][2 * r], p1 = sc[2 * kk + half][2 * r + 1];
-                        const uint32_t hi = pack_half2(p0, p1);
-                        const float2 hf = unpack_half2(hi);
-                        ah[half * 2 + r] = hi;
-                        al[half * 2 + r] = pack_half2(p0 - hf.x, p1 - hf.y);
-                    }
-                uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
-                const int tb = kk * 16;
-                if (vrem < tb + 16) {
-                    keep0 = (tb + 2 * t4 < vrem ? 0x0000ffffu : 0u) | (tb + 2 * t4 + 1 < vrem ? 0xffff0000u : 0u);
-                    keep1 = (tb + 8 + 2 * t4 < vrem ? 0x0000ffffu : 0u) | (tb + 9 + 2 * t4 < vrem ? 0xffff0000u : 0u);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int c = ks >> 2, kk = ks & 3;
+                    const uint64_t a = umma_smem_desc(q_addr + c * Geo::kQChunk + kk * 32, 16, 1024);
+                    const uint64_t b = umma_smem_desc(k_addr + c * Geo::kKVChunk + kk * 32, 16, 1024);
+                    umma_f16_ss(tS, a, b, idS, ks > 0);
                 }
+                umma_commit(s_full);
+                umma_commit(&k_empty[j & 1]);
+            };
+            // O += P(j) V(j): per 64-dim chunk, 4 steps of 16 keys, high and residual parts of P
+            auto mma_pv = [&](int j) {
+                const uint32_t v_addr = smem_u32(vst(j & 1));
 #pragma unroll
-                for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-                    const int mi = lane >> 3;
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_t(vbase + pswz(tb + (mi & 1) * 8 + (lane & 7), nd2 * 2 + (mi >> 1)), v0, v1, v2, v3);
-                    v0 &= keep0;
-                    v2 &= keep0;
-                    v1 &= keep1;
-                    v3 &= keep1;
-                    mma_f16_16816(o[2 * nd2], ah[0], ah[1], ah[2], ah[3], v0, v1);
-                    mma_f16_16816(o[2 * nd2], al[0], al[1], al[2], al[3], v0, v1);
-                    mma_f16_16816(o[2 * nd2 + 1], ah[0], ah[1], ah[2], ah[3], v2, v3);
-                    mma_f16_16816(o[2 * nd2 + 1], al[0], al[1], al[2], al[3], v2, v3);
+                for (int c = 0; c < Geo::kChunks; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+                        // V MN-major: 16 keys = two 8-row groups of 1024 bytes (one 64-dim atom wide)
+                        const uint64_t b = umma_smem_desc(v_addr + c * Geo::kKVChunk + kk * 2048, 1024, 1024);
+                        const uint64_t ah = umma_smem_desc(smem_u32(phi) + kk * 32, 16, 1024);
+                        const uint64_t al = umma_smem_desc(smem_u32(plo) + kk * 32, 16, 1024);
+                        umma_f16_ss(tO + c * 64, ah, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_f16_ss(tO + c * 64, al, b, idPV, 1u);
+                    }
+                umma_commit(o_full);
+                umma_commit(&v_empty[j & 1]);
+            };
+
+            bool ok = pf_wait(q_full, 0, s_abort);
+            q_done = ok;
+            ok = ok && pf_wait(&k_full[0], 0, s_abort);
+            if (ok) {
+                k_done = 1;
+                tc_fence_after();
+                mma_s(0);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                // the K stage of tile j is free once S(j) is done: refill it with tile j + 2
+                if (j + 2 < ntiles) {
+                    if (!(ok = pf_wait(&k_empty[j & 1], (j >> 1) & 1, s_abort))) break;
+                    load_k(j + 2);
+                    k_issued = j + 3;
+                }
+                // S(j + 1) once its K tile has landed and the row warps have read S(j)
+                if (j + 1 < ntiles) {
+                    if (!(ok = pf_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, s_abort))) break;
+                    k_done = j + 2;
+                    if (!(ok = pf_wait(s_free, j & 1, s_abort))) break;
+                    tc_fence_after();
+                    mma_s(j + 1);
+                }
+                // P(j) V(j) once P(j) is written and V(j) has landed
+                if (!(ok = pf_wait(&v_full[j & 1], (j >> 1) & 1, s_abort))) break;
+                v_done = j + 1;
+                if (!(ok = pf_wait(p_full, j & 1, s_abort))) break;
+                tc_fence_after();
+                mma_pv(j);
+                if (j + 2 < ntiles) {
+                    if (!(ok = pf_wait(&v_empty[j & 1], (j >> 1) & 1, s_abort))) break;
+                    load_v(j + 2);
+                    v_issued = j + 3;
+                }
+            }
+            // every product issued is complete before the tensor memory is released
+            umma_commit(fin);
+            mbar_wait_bounded(fin, 0, kPfWaitNs);
+            if (!ok) {
+                atomicOr(p.err, KVC_DEVERR_TIMEOUT);
+                // copies still in flight land before the shared memory is released
+                if (!q_done) mbar_wait_bounded(q_full, 0, kPfWaitNs / 8);
+                for (int t = k_done; t < k_issued; ++t) mbar_wait_bounded(&k_full[t & 1], (t >> 1) & 1, kPfWaitNs / 8);
+                for (int t = v_done; t < v_issued; ++t) mbar_wait_bounded(&v_full[t & 1], (t >> 1) & 1, kPfWaitNs / 8);
+            }
+        }
+    } else {
+        // ================= row warps: softmax and output; thread = query row = TMEM lane =================
+        const int row = threadIdx.x;
+        const int qi = r0 + row;  // row of the segment
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            ok = __all_sync(0xffffffffu, pf_wait(s_full, j & 1, s_abort));
+            if (!ok) break;
+            tc_fence_after();
+            float s[2][32];  // keys c = 32 * (c >> 5) + (c & 31)
+            tmem_ld32(tS + lane_base, s[0]);
+            tmem_ld32(tS + lane_base + 32, s[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+
+            const int k0 = j * kPfKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kPfKeys; ++c) {
+                const int kj = k0 + c;
+                const bool valid = kj < len && (!p.causal || kj <= qi);
+                float& x = s[c >> 5][c & 31];
+                x = valid ? x * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x);
+            }
+            // the running max moves only when it has grown by 2^8 (or from -inf): then l and O are rescaled
+            float alpha = 1.f;
+            if (mx > m_used + kPfRescaleLog2) {  // includes the first finite max (m_used = -inf)
+                alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mx);
+                m_used = mx;
+            }
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < kPfKeys; ++c) {
+                float& x = s[c >> 5][c & 31];
+                x = m_used == -INFINITY ? 0.f : ex2(x - m_used);
+                ls += x;
+            }
+            l = l * alpha + ls;
+            // P(j-1) V(j-1) must be done before O is rescaled and P is overwritten
+            if (j > 0) {
+                ok = __all_sync(0xffffffffu, pf_wait(o_full, (j - 1) & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        tmem_ld32(tO + lane_base + c, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tO + lane_base + c, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // the last tile of a segment: V rows past its end (the next segment's tokens) are zeroed, so
+            // that whatever they hold cannot reach this segment's output through a zero weight
+            const int vrem = len - k0;
+            if (vrem < kPfKeys && warp == 0) {
+                ok = __all_sync(0xffffffffu, pf_wait(&v_full[j & 1], (j >> 1) & 1, s_abort));
+                if (!ok) break;
+                uint8_t* vt = vst(j & 1);
+                for (int e = lane; e < (kPfKeys - vrem) * 8 * Geo::kChunks; e += 32) {
+                    const int r = vrem + e / (8 * Geo::kChunks), rest = e % (8 * Geo::kChunks);
+                    *reinterpret_cast<uint4*>(vt + (rest / 8) * Geo::kKVChunk + sw128(r, rest % 8)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // P = hi + lo in fp16, row `row`, 64 keys = 8 chunks of 16 bytes, 128-byte swizzle
+#pragma unroll
+            for (int cc = 0; cc < kPfKeys / 8; ++cc) {
+                uint32_t hv[4], lv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = cc * 8 + 2 * e;
+                    const float p0 = s[c >> 5][c & 31], p1 = s[(c + 1) >> 5][(c + 1) & 31];
+                    hv[e] = pack_half2(p0, p1);
+                    const float2 f = unpack_half2(hv[e]);
+                    lv[e] = pack_half2(p0 - f.x, p1 - f.y);
+                }
+                *reinterpret_cast<uint4*>(phi + sw128(row, cc)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4*>(plo + sw128(row, cc)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            }
+            fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, pf_wait(o_full, (ntiles - 1) & 1, s_abort));
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t base = (static_cast<int64_t>(beg + qi) * p.Hq + h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                float o[32];
+                tmem_ld32(tO + lane_base + c, o);
+                if (qi < len) {
+                    if (p.out_f32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base + c);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(p.out) + base + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_half2(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                                pack_half2(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                                pack_half2(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                                pack_half2(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                    }
                 }
             }
         }
-        // every warp is done with this stage before it is refilled
-        if (!__syncthreads_and(good ? 1 : 0)) {
-            fail_kt = kt;
-            break;
-        }
-        if (threadIdx.x == 0 && kt + 2 < ntiles) issue_kv(kt + 2);
     }
-    if (fail_kt >= 0) {
-        if (threadIdx.x == 0) {
-            atomicOr(p.err, KVC_DEVERR_TIMEOUT);
-            // let the copies still in flight land before the shared memory is released
-            if (!q_ok) mbar_wait_bounded(&bars[0], 0, kPfWaitNs / 8);
-            for (int kt = fail_kt; kt < min(ntiles, fail_kt + 2); ++kt)
-                mbar_wait_bounded(&bars[1 + (kt & 1)], (kt >> 1) & 1, kPfWaitNs / 8);
-        }
-        return;
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-        l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int qi = qi0 + r * 8;
-        if (qi >= len) continue;
-        const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
-        const int64_t base = (static_cast<int64_t>(beg + qi) * p.Hq + h) * D;
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-            const float a = o[nd][2 * r] * inv, c = o[nd][2 * r + 1] * inv;
-            const int d = nd * 8 + 2 * t4;
-            if (p.out_f32)
-                *reinterpret_cast<float2*>(static_cast<float*>(p.out) + base + d) = make_float2(a, c);
-            else
-                *reinterpret_cast<__half2*>(static_cast<__half*>(p.out) + base + d) = __floats2half2_rn(a, c);
-        }
+    // every TMEM access of the CTA is complete; the allocating warp frees it
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Geo::kTmemCols);
     }
 }
 
@@ -282,7 +428,7 @@ static EncodeTiledFnP encode_fn_p() {
     return fn;
 }
 
-// [T][H][D] fp16 viewed as (dim, head, token); boxes of 64 dims x 1 head x 64 tokens
+// [T][H][D] fp16 viewed as (dim, head, token); boxes of 64 dims x 1 head x 64 tokens, 128-byte swizzle
 static cudaError_t make_packed_map(CUtensorMap* map, const void* base, int D, int H, int T) {
     EncodeTiledFnP fn = encode_fn_p();
     if (!fn) return cudaErrorNotSupported;
@@ -298,7 +444,7 @@ static cudaError_t make_packed_map(CUtensorMap* map, const void* base, int D, in
 
 template <int D>
 static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
-    using Geo = PrefillGeom<D>;
+    using Geo = PfGeom<D>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -325,7 +471,7 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kPfLog2e;
     dim3 grid(a.nseq * p.tiles_per_seq, a.Hq);
-    prefill_kernel<D><<<grid, kPfWarps * 32, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D><<<grid, kPfThreads, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

@@ -61,3 +61,25 @@ def test_prefill_ragged(seqlens, Hq, Hkv, D, causal):
     assert kvc.kvc_device_error_flags(clear=True) == 0
     ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
     check_attention(out, ref, f"prefill {seqlens}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_long_peaked(D, causal):
+    """Long segments whose scores jump by far more than 2^8 between key tiles (keys scaled x6 every 97
+    positions, growing along the segment): the running max moves and O is rescaled in place many times."""
+    import paged_kv_cache_27_gb300 as kvc
+    seqlens = (1500, 517)
+    wl = workloads._prefill("peaked", [7, sum(seqlens), D], seqlens, 4, 2, D)
+    k = wl.k.astype(np.float32)
+    pos = np.arange(k.shape[0])
+    boost = np.where(pos % 97 == 5, 2.0 + 4.0 * (pos / k.shape[0]), 1.0).astype(np.float32)
+    wl.k = (k * boost[:, None, None]).astype(np.float16)
+    q, kk, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
+    cu = torch.from_numpy(wl.cu_seqlens).cuda()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    kvc.prefill_attention(q, kk, v, cu, max(seqlens), wl.scale, causal, out)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
+    check_attention(out, ref, f"prefill peaked D={D} causal={causal}")
