@@ -390,6 +390,174 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# --suite: one JSON line per further configuration (parity is the tests' job; these only measure)
+# ---------------------------------------------------------------------------
+def _flush_l2(buf):
+    buf.add_(1)  # writes 256 MiB: nothing of the previous call stays in the 129 MB L2
+
+
+def _timed_calls(fn, reps, flush_buf, stream):
+    """Mean device time (us) of fn(), each call preceded by an L2 flush outside the timed span."""
+    import torch
+    total = 0.0
+    for r in range(reps + 3):
+        _flush_l2(flush_buf)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        if r >= 3:
+            total += e0.elapsed_time(e1) * 1e3
+    return total / reps
+
+
+def _decode_state(B, ctx, Hq, Hkv, D, device, seed):
+    """Seeded synthetic decode state made on the device (K/V N(0,1) fp16, permuted block tables)."""
+    import torch
+    bs = 16
+    nblk = -(-ctx // bs)
+    NB = B * nblk
+    gen = torch.Generator(device=device).manual_seed(seed)
+    k_pool = torch.empty((NB, Hkv, bs, D), dtype=torch.float16, device=device)
+    v_pool = torch.empty_like(k_pool)
+    step = max(1, (1 << 24) // (Hkv * bs * D))
+    for a in range(0, NB, step):
+        for pool in (k_pool, v_pool):
+            pool[a:a + step] = torch.randn(pool[a:a + step].shape, generator=gen, device=device).half()
+    rng = np.random.default_rng(seed)
+    table = torch.from_numpy(rng.permutation(NB).astype(np.int32).reshape(B, nblk)).to(device)
+    ctx_t = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    q = torch.randn((B, Hq, D), generator=gen, device=device).half()
+    kn = torch.randn((B, Hkv, D), generator=gen, device=device).half()
+    vn = torch.randn((B, Hkv, D), generator=gen, device=device).half()
+    return k_pool, v_pool, table, ctx_t, q, kn, vn
+
+
+def run_suite(args):
+    import torch
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peak, peak_kind = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops_peak = float(json.load(f)["bf16_tflops"])
+        tflops_kind = "measured (bf16 = fp16 tensor rate)"
+    except Exception:
+        tflops_peak, tflops_kind = 1900.0, "fallback"
+    stream = torch.cuda.current_stream(device)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=device)
+    emit = lambda d: print(json.dumps(dict(suite=True, **d)), flush=True)
+
+    if args.suite_part in ("all", "decode"):
+        run_suite_decode(device, stream, flush, emit, peak)
+    if args.suite_part in ("all", "prefill"):
+        run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind)
+    return 0
+
+
+def run_suite_decode(device, stream, flush, emit, peak):
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    import workloads
+    from paged_kv_cache_27_gb300 import harness
+
+    # config 1: one sequence at context 256 (L2-resident, latency-bound)
+    wl = workloads.config1()
+    sess = harness.DecodeSession(wl, device=device, out_dtype=torch.float32).fill()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(100):
+            sess.decode(0)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    emit({"config": "1: B=1, 1 q / 1 KV head, D=64, context 256", "us_per_decode": e0.elapsed_time(e1) * 1e3 / 1000,
+          "note": "100 back-to-back calls in a CUDA graph; latency-bound, the 64 KiB context sits in L2"})
+    sess.close()
+
+    # config 3: 200 sequences, groups of 8 share a 512-token prefix (refcounted blocks)
+    mix = workloads.config3()
+    res = harness.serving_mix(mix, device=device, poison=False)
+    table = torch.from_numpy(res["block_table"]).to(device)
+    ctx = torch.from_numpy(mix.ctx).to(device)
+    q = torch.from_numpy(mix.q).to(device)
+    kn, vn = torch.from_numpy(mix.k_new).to(device), torch.from_numpy(mix.v_new).to(device)
+    out = torch.empty((mix.B, mix.Hq, mix.D), dtype=torch.float16, device=device)
+    max_ctx = int(mix.ctx.max())
+    _, _, ws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
+    wsb = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+    step = lambda: kvc.paged_decode_append_attention(q, kn, vn, res["k_cache"], res["v_cache"], table, ctx,
+                                                      mix.scale, out, wsb, max_ctx)
+    us = _timed_calls(step, 20, flush, stream)
+    row = 2 * mix.Hkv * mix.D * 2  # K + V bytes per token
+    logical = int(mix.ctx.astype(np.int64).sum()) * row
+    used = set()
+    for b in range(mix.B):
+        used.update(res["block_table"][b, :-(-int(mix.ctx[b]) // 16)].tolist())
+    unique = len(used) * 16 * row
+    emit({"config": "3: B=200, 14 q / 2 KV heads, D=64, ctx ~ U{16..4096}, groups of 8 share a 512-token prefix",
+          "us_per_step": us, "tokens_per_s": mix.B / (us * 1e-6),
+          "logical_GBps": logical / (us * 1e-6) / 1e9, "unique_GBps": unique / (us * 1e-6) / 1e9,
+          "logical_bytes": logical, "unique_bytes": unique, "pct_hbm_peak_unique": unique / (us * 1e-6) / 1e9 / peak * 100,
+          "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
+                  "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
+
+    # config 4: long contexts, B in {1, 4, 16} x ctx in {4k, 16k, 64k, 128k}
+    for B in (1, 4, 16):
+        for c in (4096, 16384, 65536, 131072):
+            kp, vp, tb, ct, q4, kn4, vn4 = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
+            o4 = torch.empty((B, 14, 64), dtype=torch.float16, device=device)
+            ns, bps, ws = kvc.paged_decode_plan(B, 14, 2, 64, c)
+            w4 = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+            fn = lambda: kvc.paged_decode_append_attention(q4, kn4, vn4, kp, vp, tb, ct, 0.125, o4, w4, c)
+            us = _timed_calls(fn, 20, flush, stream)
+            nbytes = B * c * 2 * 2 * 64 * 2
+            emit({"config": f"4: B={B}, ctx={c}, 14 q / 2 KV heads, D=64", "us_per_call": us,
+                  "GBps": nbytes / (us * 1e-6) / 1e9, "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100,
+                  "splits": ns, "blocks_per_split": bps, "kv_bytes": nbytes})
+            del kp, vp
+
+
+
+def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+
+    # config 5 and larger prefill shapes: causal varlen prefill on the tensor cores
+    def prefill_case(name, seqlens, Hq, Hkv, D, causal=True):
+        T = sum(seqlens)
+        gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
+        qq = torch.randn((T, Hq, D), generator=gen, device=device).half()
+        kk = torch.randn((T, Hkv, D), generator=gen, device=device).half()
+        vv = torch.randn((T, Hkv, D), generator=gen, device=device).half()
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
+        oo = torch.empty((T, Hq, D), dtype=torch.float16, device=device)
+        fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo)
+        us = _timed_calls(fn, 20, flush, stream)
+        pairs = sum(s * (s + 1) // 2 for s in seqlens) if causal else sum(s * s for s in seqlens)
+        flops = 4 * D * Hq * pairs
+        tf = flops / (us * 1e-6) / 1e12
+        emit({"config": name, "us_per_call": us, "TFLOPs": tf, "pct_tensor_peak": tf / tflops_peak * 100,
+              "flops": flops, "peak_TFLOPs": tflops_peak, "peak_kind": tflops_kind,
+              "note": "algorithmic flops (masked half not counted); the kernel's tensor work is 1.5x that "
+                      "(P V runs for the fp16 high part and the residual of P)"})
+
+    prefill_case("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal", (37, 120, 8, 200), 8, 8, 64)
+    prefill_case("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2, 64)
+    prefill_case("supplementary (not a listed config): varlen x16, seqlens 592/1920/128/3200, 8/8, D=64, causal",
+                 (592, 1920, 128, 3200), 8, 8, 64)
+    prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",
+                 (4096,) * 4, 32, 8, 128)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,11 +571,16 @@ def main():
     ap.add_argument("--prefetch", action="store_true",
                     help="also request the next layer's blocks into L2 (measured: no gain on this workload)")
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
+    ap.add_argument("--suite", action="store_true",
+                    help="instead of the headline line: one JSON line per further configuration (1, 3, 4, 5)")
+    ap.add_argument("--suite-part", choices=["all", "decode", "prefill"], default="all")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.suite:
+        return run_suite(args)
     return run_ours(args)
 
 
