@@ -93,7 +93,7 @@ namespace kvc {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
-constexpr int kMaxClusterBlocks = 256;  // blocks one cluster covers at most (its table slice is in shared memory)
+constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
 
 std::atomic<int> g_launch_overlap{0};
 
