@@ -510,6 +510,22 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
                   "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
 
+    # head_dim 128 shapes: the 7B-class model (32 q / 8 KV heads) and the 32 x 32 x 128 MHA shape
+    for Hq, Hkv in ((32, 8), (32, 32)):
+        B, c, D = 32, 2048, 128
+        kp, vp, tb, ct, qd, knd, vnd = _decode_state(B, c, Hq, Hkv, D, device, seed=Hq * 100 + Hkv)
+        od = torch.empty((B, Hq, D), dtype=torch.float16, device=device)
+        ns, bps, ws = kvc.paged_decode_plan(B, Hq, Hkv, D, c)
+        wd = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+        fn = lambda: kvc.paged_decode_append_attention(qd, knd, vnd, kp, vp, tb, ct, 1.0 / np.sqrt(D), od, wd, c)
+        us = _timed_calls(fn, 20, flush, stream)
+        nbytes = B * c * Hkv * D * 2 * 2
+        emit({"config": f"head_dim 128: B={B}, ctx={c}, {Hq} q / {Hkv} KV heads, D={D} (one layer)",
+              "us_per_call": us, "GBps": nbytes / (us * 1e-6) / 1e9,
+              "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100, "splits": ns, "blocks_per_split": bps,
+              "kv_bytes": nbytes})
+        del kp, vp
+
     # config 4: long contexts, B in {1, 4, 16} x ctx in {4k, 16k, 64k, 128k}
     for B in (1, 4, 16):
         for c in (4096, 16384, 65536, 131072):
