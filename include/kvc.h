@@ -222,6 +222,51 @@ kvc_status paged_decode_append_attention(const void* q, const void* k_new, const
                                          float scale, void* out, int out_dtype, void* workspace,
                                          size_t workspace_bytes, int blocks_per_split, void* stream);
 
+/* Cascade (shared-prefix) decode.  Same result as paged_decode_attention on
+ * the same arguments; only the way it is computed differs.  Sequences form
+ * groups of consecutive indices that share the leading blocks of their block
+ * tables (a common prefix whose blocks the pool refcounts: the prefix
+ * sharing of the chatgpz.de PagedAttention article, SECTION 3, and the
+ * neuralialabs.com PagedAttention paragraph).  Each group's shared blocks are
+ * read once and attended by all of its members together; every sequence's
+ * remaining blocks are attended as in paged_decode_attention; the two
+ * partial states merge with the rescaling rule of the FlashAttention article.
+ *   group_start    device int32 [n_groups + 1]: group g is sequences
+ *                  group_start[g] .. group_start[g+1]-1; group_start[0] = 0,
+ *                  group_start[n_groups] = B, at most 8 sequences per group
+ *   shared_blocks  device int32 [B]: the number of leading blocks that every
+ *                  member of b's group has in common (the same value for all
+ *                  members; 0 = none), with 16 * shared_blocks[b] <
+ *                  context_lens[b] (each member keeps at least its newest
+ *                  token private)
+ *   max_shared_blocks  host upper bound of shared_blocks (sizes the launch)
+ *   workspace      device, 16-byte aligned, >= paged_decode_cascade_plan's bytes
+ * The members' rows must really begin with the same block ids: the call
+ * reads the shared blocks through the first member's row.  Checked mode
+ * verifies all of it on the host; unchecked, a bad group sets
+ * KVC_DEVERR_CONTEXT and its outputs are undefined.  Three kernel launches
+ * (prefix, suffix, merge) on `stream`. */
+/* Host helper for the cascade: forms the groups from host copies of the
+ * block table [B][max_blocks] and the context lengths [B].  Consecutive
+ * sequences whose rows begin with the same block id form a group (split into
+ * runs of at most max_group, 1..8); a group's shared block count is the
+ * number of leading entries all its members have in common, capped so that
+ * every member keeps at least its newest token outside it
+ * (16 * shared <= ctx - 1).  A sequence alone, or whose group shares nothing,
+ * gets shared 0.  Writes group_start [n_groups + 1] (capacity B + 1),
+ * *n_groups, shared_blocks [B] and *max_shared (all host memory). */
+kvc_status kv_cascade_groups(const int32_t* block_table, int B, int max_blocks, const int32_t* context_lens,
+                             int block_size, int max_group, int32_t* group_start, int* n_groups,
+                             int32_t* shared_blocks, int* max_shared);
+kvc_status paged_decode_cascade_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                     int n_groups, int max_shared_blocks, size_t* workspace_bytes);
+kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                          const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                          const int32_t* group_start, const int32_t* shared_blocks, int n_groups,
+                                          int max_shared_blocks, int B, int Hq, int Hkv, int head_dim,
+                                          int block_size, int max_context_len, float scale, void* out, int out_dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Launch overlap (process-wide, default off).  When on, decode kernels are
  * launched as programmatic dependents of the kernel before them on the
  * stream: they read block tables, context lengths and the cached K/V

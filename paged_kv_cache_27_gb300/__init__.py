@@ -29,7 +29,7 @@ __all__ = [
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
     "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
-    "paged_decode_attention_static_workspace",
+    "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "prefill_attention", "DEVERR",
 ]
 
@@ -110,6 +110,10 @@ def _load():
         "paged_decode_attention_static_workspace": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
                                                         I, P]),
         "kvc_trace_read": (I, [P, I, PI, I]),
+        "paged_decode_cascade_plan": (I, [I, I, I, I, I, I, I, I, PSZ]),
+        "kv_cascade_groups": (I, [P, I, I, P, I, I, P, PI, P, PI]),
+        "paged_decode_cascade_attention": (I, [P, P, P, I, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P,
+                                               I, P, SZ, P]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
     }
     for name, (res, args) in sig.items():
@@ -356,6 +360,67 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs,
         int(max_context_len), float(scale), _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split),
         _stream(stream, q)), "paged_decode_attention")
+
+
+def kv_cascade_groups(block_table: np.ndarray, context_lens, max_group: int = 8, block_size: int = 16):
+    """Groups for paged_decode_cascade_attention from a host block table [B][max_blocks] and context lengths:
+    returns (group_start int32 [n_groups + 1], shared_blocks int32 [B], max_shared)."""
+    table = _host(block_table, np.int32)
+    if table.ndim != 2:
+        raise ValueError("block_table must be [B][max_blocks]")
+    B, mb = table.shape
+    ctx = _host(context_lens, np.int32)
+    gs = np.zeros(B + 1, dtype=np.int32)
+    sh = np.zeros(max(B, 1), dtype=np.int32)
+    ng, mx = ctypes.c_int(), ctypes.c_int()
+    _check(_lib.kv_cascade_groups(_np_ptr(table), B, mb, _np_ptr(ctx), block_size, max_group, _np_ptr(gs),
+                                  ctypes.byref(ng), _np_ptr(sh), ctypes.byref(mx)), "kv_cascade_groups")
+    return gs[:ng.value + 1].copy(), sh[:B].copy(), mx.value
+
+
+def paged_decode_cascade_plan(B: int, Hq: int, Hkv: int, head_dim: int, max_context_len: int, n_groups: int,
+                              max_shared_blocks: int, block_size: int = 16) -> int:
+    """Workspace bytes of paged_decode_cascade_attention for these sizes."""
+    ws = ctypes.c_size_t()
+    _check(_lib.paged_decode_cascade_plan(B, Hq, Hkv, head_dim, block_size, max_context_len, n_groups,
+                                          max_shared_blocks, ctypes.byref(ws)), "paged_decode_cascade_plan")
+    return ws.value
+
+
+def paged_decode_cascade_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   block_table: torch.Tensor, context_lens: torch.Tensor, group_start: torch.Tensor,
+                                   shared_blocks: torch.Tensor, max_shared_blocks: int, scale: float,
+                                   out: torch.Tensor, workspace: torch.Tensor, max_context_len: int,
+                                   stream=None) -> None:
+    """paged_decode_attention's result, with each group's shared leading blocks read once for the group.
+
+    group_start int32 [n_groups + 1] (groups of consecutive sequences, at most 8 each); shared_blocks int32 [B]
+    (leading blocks every member of the sequence's group has in common); workspace: paged_decode_cascade_plan bytes.
+    """
+    B, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table / context_lens do not match B")
+    if shared_blocks.numel() != B or group_start.numel() < 2:
+        raise ValueError("shared_blocks must have B entries and group_start at least 2")
+    if out.dtype == torch.float16:
+        od = KVC_F16
+    elif out.dtype == torch.float32:
+        od = KVC_F32
+    else:
+        raise TypeError("out must be float16 or float32")
+    _check(_lib.paged_decode_cascade_attention(
+        _dptr(q, torch.float16, "q"), _dptr(k_cache, torch.float16, "k_cache"),
+        _dptr(v_cache, torch.float16, "v_cache"), NB, _dptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"),
+        _dptr(group_start, torch.int32, "group_start"), _dptr(shared_blocks, torch.int32, "shared_blocks"),
+        group_start.numel() - 1, int(max_shared_blocks), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
+        _dptr(out, None, "out"), od, _dptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream, q)), "paged_decode_cascade_attention")
 
 
 def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,

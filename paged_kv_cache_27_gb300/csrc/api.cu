@@ -409,12 +409,13 @@ kvc_status paged_decode_append_attention(const void* q, const void* k_new, const
                          workspace, workspace_bytes, blocks_per_split, stream);
 }
 
-static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
-                                const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
-                                int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
-                                int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
-                                void* stream) {
+// Every argument check of a decode call; in checked mode also the context lengths and the block-table
+// entries, on host copies that are returned through ctx / table (left empty otherwise).
+static kvc_status decode_validate(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                  const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B,
+                                  int Hq, int Hkv, int head_dim, int block_size, int max_context_len, void* out,
+                                  int out_dtype, int blocks_per_split, void* stream, std::vector<int32_t>& ctx,
+                                  std::vector<int32_t>& table) {
     kvc_status s = check_decode_shape(B, Hq, Hkv, head_dim, block_size, max_context_len);
     if (s != KVC_OK) return s;
     if (B == 0) return KVC_OK;
@@ -429,7 +430,6 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
     if (out_dtype != KVC_F16 && out_dtype != KVC_F32) return fail(KVC_ERR_INVALID, "bad out_dtype");
     if (blocks_per_split < 0) return fail(KVC_ERR_INVALID, "negative blocks_per_split");
     if (g_checked.load()) {
-        std::vector<int32_t> ctx, table;
         kvc_status st = copy_to_host(ctx, context_lens, static_cast<size_t>(B), as_stream(stream));
         if (st == KVC_OK) st = copy_to_host(table, block_table, static_cast<size_t>(B) * max_blocks, as_stream(stream));
         if (st != KVC_OK) return st;
@@ -443,6 +443,14 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
             }
         }
     }
+    return KVC_OK;
+}
+
+static kvc::DecodeArgs decode_args(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                   const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                   const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B,
+                                   int Hq, int Hkv, int head_dim, int max_context_len, float scale, void* out,
+                                   int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split) {
     kvc::DecodeArgs a;
     a.q = static_cast<const __half*>(q);
     a.k_new = static_cast<const __half*>(k_new);
@@ -466,16 +474,142 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     a.blocks_per_split = blocks_per_split;
+    a.err = nullptr;
+    return a;
+}
+
+static kvc_status check_workspace(size_t need, const void* workspace, size_t workspace_bytes) {
+    if (need > workspace_bytes || (need && !workspace))
+        return fail(KVC_ERR_INVALID, "workspace too small: need %zu bytes", need);
+    if (need && !aligned16(workspace)) return fail(KVC_ERR_INVALID, "workspace must be 16-byte aligned");
+    return KVC_OK;
+}
+
+static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
+                                int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
+                                int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
+                                void* stream) {
+    std::vector<int32_t> ctx, table;
+    kvc_status s = decode_validate(q, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B, Hq, Hkv,
+                                   head_dim, block_size, max_context_len, out, out_dtype, blocks_per_split, stream, ctx,
+                                   table);
+    if (s != KVC_OK || B == 0) return s;
+    kvc::DecodeArgs a = decode_args(q, k_new, v_new, k_cache, v_cache, k_next, v_next, num_blocks, block_table,
+                                    max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
+                                    out_dtype, workspace, workspace_bytes, blocks_per_split);
     kvc::DecodePlan plan;
     cudaError_t e = kvc::decode_plan(B, Hq, Hkv, head_dim, max_context_len, blocks_per_split, &plan);
     if (e != cudaSuccess) return cuda_fail(e, "decode plan");
-    if (plan.workspace_bytes > workspace_bytes || (plan.workspace_bytes && !workspace))
-        return fail(KVC_ERR_INVALID, "workspace too small: need %zu bytes", plan.workspace_bytes);
-    if (plan.workspace_bytes && !aligned16(workspace)) return fail(KVC_ERR_INVALID, "workspace must be 16-byte aligned");
+    s = check_workspace(plan.workspace_bytes, workspace, workspace_bytes);
+    if (s != KVC_OK) return s;
     e = kvc::device_error_word(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     e = kvc::launch_decode(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, k_new ? "paged_decode_append_attention launch" : "paged_decode_attention launch");
+    return KVC_OK;
+}
+
+kvc_status kv_cascade_groups(const int32_t* block_table, int B, int max_blocks, const int32_t* context_lens,
+                             int block_size, int max_group, int32_t* group_start, int* n_groups,
+                             int32_t* shared_blocks, int* max_shared) {
+    if (B < 0 || max_blocks < 1 || block_size < 1) return fail(KVC_ERR_INVALID, "bad sizes");
+    if (max_group < 1 || max_group > kvc::kMaxGroupSize)
+        return fail(KVC_ERR_INVALID, "max_group %d outside [1, %d]", max_group, kvc::kMaxGroupSize);
+    if (B > 0 && (!block_table || !context_lens || !group_start || !n_groups || !shared_blocks || !max_shared))
+        return fail(KVC_ERR_INVALID, "null pointer");
+    int ng = 0, mx = 0;
+    group_start[0] = 0;
+    for (int g0 = 0; g0 < B;) {
+        const int32_t* r0 = block_table + static_cast<size_t>(g0) * max_blocks;
+        int g1 = g0 + 1;  // members: consecutive rows that start with the same block, at most max_group
+        while (g1 < B && g1 - g0 < max_group && block_table[static_cast<size_t>(g1) * max_blocks] == r0[0]) ++g1;
+        int shared = 0;
+        if (g1 - g0 > 1) {
+            int cap = max_blocks;
+            for (int b = g0; b < g1; ++b) {
+                if (context_lens[b] < 1) return fail(KVC_ERR_INVALID, "sequence %d: context length %d", b, context_lens[b]);
+                cap = std::min(cap, (context_lens[b] - 1) / block_size);
+            }
+            while (shared < cap) {
+                bool same = true;
+                for (int b = g0 + 1; b < g1 && same; ++b)
+                    same = block_table[static_cast<size_t>(b) * max_blocks + shared] == r0[shared];
+                if (!same) break;
+                ++shared;
+            }
+        }
+        for (int b = g0; b < g1; ++b) shared_blocks[b] = shared;
+        mx = std::max(mx, shared);
+        group_start[++ng] = g1;
+        g0 = g1;
+    }
+    *n_groups = ng;
+    *max_shared = mx;
+    return KVC_OK;
+}
+
+kvc_status paged_decode_cascade_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                     int n_groups, int max_shared_blocks, size_t* workspace_bytes) {
+    kvc_status s = check_decode_shape(B, Hq, Hkv, head_dim, block_size, max_context_len);
+    if (s != KVC_OK) return s;
+    if (n_groups < 0 || max_shared_blocks < 0) return fail(KVC_ERR_INVALID, "bad group sizes");
+    kvc::CascadePlan plan;
+    cudaError_t e = kvc::cascade_plan(B, Hq, Hkv, head_dim, max_context_len, std::max(n_groups, 1),
+                                      max_shared_blocks, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "cascade plan");
+    if (workspace_bytes) *workspace_bytes = plan.workspace_bytes;
+    return KVC_OK;
+}
+
+kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                          const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                          const int32_t* group_start, const int32_t* shared_blocks, int n_groups,
+                                          int max_shared_blocks, int B, int Hq, int Hkv, int head_dim,
+                                          int block_size, int max_context_len, float scale, void* out, int out_dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+    std::vector<int32_t> ctx, table;
+    kvc_status s = decode_validate(q, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B, Hq, Hkv,
+                                   head_dim, block_size, max_context_len, out, out_dtype, 0, stream, ctx, table);
+    if (s != KVC_OK || B == 0) return s;
+    if (!group_start || !shared_blocks) return fail(KVC_ERR_INVALID, "null group_start / shared_blocks");
+    if (n_groups < 1 || n_groups > B) return fail(KVC_ERR_INVALID, "n_groups %d outside [1, B = %d]", n_groups, B);
+    if (max_shared_blocks < 0 || max_shared_blocks >= max_blocks)
+        return fail(KVC_ERR_INVALID, "max_shared_blocks %d outside [0, max_blocks)", max_shared_blocks);
+    if (g_checked.load()) {
+        std::vector<int32_t> gs, sh;
+        s = copy_to_host(gs, group_start, static_cast<size_t>(n_groups) + 1, as_stream(stream));
+        if (s == KVC_OK) s = copy_to_host(sh, shared_blocks, static_cast<size_t>(B), as_stream(stream));
+        if (s != KVC_OK) return s;
+        if (gs[0] != 0 || gs[n_groups] != B) return fail(KVC_ERR_INVALID, "group_start must run from 0 to B");
+        for (int g = 0; g < n_groups; ++g) {
+            const int g0 = gs[g], g1 = gs[g + 1];
+            if (g1 <= g0 || g1 - g0 > kvc::kMaxGroupSize)
+                return fail(KVC_ERR_INVALID, "group %d: %d members (1..%d)", g, g1 - g0, kvc::kMaxGroupSize);
+            for (int b = g0; b < g1; ++b) {
+                if (sh[b] != sh[g0]) return fail(KVC_ERR_INVALID, "group %d: members share different block counts", g);
+                if (sh[b] < 0 || sh[b] > max_shared_blocks || static_cast<int64_t>(sh[b]) * block_size >= ctx[b])
+                    return fail(KVC_ERR_INVALID, "sequence %d: %d shared blocks do not fit its context %d (or the bound %d)",
+                                b, sh[b], ctx[b], max_shared_blocks);
+                for (int j = 0; j < sh[b]; ++j)
+                    if (table[static_cast<size_t>(b) * max_blocks + j] != table[static_cast<size_t>(g0) * max_blocks + j])
+                        return fail(KVC_ERR_INVALID, "sequence %d: block %d is not the group's shared block", b, j);
+            }
+        }
+    }
+    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table,
+                                    max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
+                                    out_dtype, workspace, workspace_bytes, 0);
+    kvc::CascadePlan plan;
+    cudaError_t e = kvc::cascade_plan(B, Hq, Hkv, head_dim, max_context_len, n_groups, max_shared_blocks, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "cascade plan");
+    s = check_workspace(plan.workspace_bytes, workspace, workspace_bytes);
+    if (s != KVC_OK) return s;
+    e = kvc::device_error_word(&a.err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    e = kvc::launch_cascade(a, group_start, shared_blocks, n_groups, max_shared_blocks, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_cascade_attention launch");
     return KVC_OK;
 }
 

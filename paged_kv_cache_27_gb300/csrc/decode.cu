@@ -86,9 +86,6 @@ namespace kvc {
 #ifndef KVC_DEC_PREFETCH_AT  // when the next layer's blocks are requested into L2: 0 at start, 1 after the main loop
 #define KVC_DEC_PREFETCH_AT 1
 #endif
-#ifndef KVC_DEC_STEAL  // 1: warps take blocks from a cluster-wide counter; 0: fixed round-robin over the cluster's warps
-#define KVC_DEC_STEAL 0
-#endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -108,7 +105,7 @@ struct DecodeCfg {
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
     static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA
-    static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice + block counter
+    static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice (+ 16 bytes of alignment)
     // + the inbox of cluster rank 0 (one slot per other CTA of the cluster, sized at launch) + alignment slack
     static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + kTableBytes + 1024;
     static int smem_bytes(int cluster, int G) { return kBaseSmemBytes + (cluster - 1) * (16 + G * D) * 4; }
@@ -133,7 +130,11 @@ struct DecodeKernelParams {
     int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx;
     int bpc;     // blocks per cluster: a cluster covers context blocks [c * bpc, (c + 1) * bpc)
     int csize;   // CTAs per cluster
-    int nparts;  // clusters along the longest context (partials per (sequence, head) when > 1)
+    // partial state of cluster c of (sequence b, query head h) goes to row (b * Hq + h) * part_stride +
+    // part_base + c of part_ml / part_acc
+    int part_base, part_stride;
+    int force_partials;      // 1: every cluster writes its partial, even when it covers the whole range
+    const int32_t* blk_off;  // null, or per sequence: the leading blocks of its table row attended elsewhere
     int out_f32;
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
@@ -240,7 +241,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // this CTA's merged state when it is cluster rank 0: m[8], l[8], acc[G][D] (the layout of an inbox slot)
     float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
     int* s_table = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
-    int* s_counter = s_table + kMaxClusterBlocks;  // next block to hand out (used in cluster rank 0)
     // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like the state at s_m
     float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes + C::kTableBytes);
 
@@ -271,11 +271,16 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // One round trip before the first copies: each warp's lane 0 fetches the table entries of its
     // static first round and the context length together; the cluster's whole slice of the table
     // (entries [cb0, cb0 + bpc), clipped to the row) goes to shared memory meanwhile, for the refills.
-    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+    // the first blk_off[b] blocks of the row (a shared prefix attended elsewhere) are skipped: this call
+    // covers the rest of the context, in block coordinates relative to that offset
+    const int off_raw = p.blk_off != nullptr ? p.blk_off[b] : 0;
+    const bool off_ok = off_raw >= 0 && off_raw < p.max_blocks;
+    const int off = off_ok ? off_raw : 0;
+    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks + off;
     const int cb0 = cidx * p.bpc;
     const int nwarps_cl = cs * NW;
     const int gw = rank * NW + warp;  // warp index within the cluster
-    const int row_end = min(cb0 + p.bpc, p.max_blocks);
+    const int row_end = min(cb0 + p.bpc, p.max_blocks - off);
     int first_phys[ST];
 #pragma unroll
     for (int s = 0; s < ST; ++s) {
@@ -284,11 +289,13 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     }
     const int nload = max(0, row_end - cb0);
     for (int t = threadIdx.x; t < nload; t += C::kThreads) s_table[t] = table[cb0 + t];
-    const int ctx = p.context_lens[b];
+    const int ctx_full = p.context_lens[b];
+    const int ctx = ctx_full - off * kBlockSize;  // tokens this call covers (all of them without an offset)
     // every CTA of a cluster sees the same (b, kvh): these exits are uniform over the cluster
-    if (ctx < 1 || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
+    if (!off_ok || ctx_full < 1 || ctx_full > p.max_blocks * kBlockSize || ctx_full > p.max_ctx || ctx < 1) {
         grid_dependency_wait();
-        if (blockIdx.x == 0) {
+        // with forced partials the combine kernel checks the same and writes the zeros
+        if (blockIdx.x == 0 && !p.force_partials) {
             if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
             for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
                 store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
@@ -332,7 +339,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         if (warp == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
-            if (rank == 0) *s_counter = cb0 + ST * nwarps_cl;  // blocks handed out after the first round
         }
 #pragma unroll
         for (int s = 0; s < ST; ++s)
@@ -341,15 +347,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     __syncwarp();
     KVC_TRACE_MARK(1);
 
-    __syncthreads();  // the table slice (and, in rank 0, the counter) is in shared memory
-#if KVC_DEC_STEAL
-    // the counter is visible cluster-wide once every CTA has passed the matching wait below
-    if (cs > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-#else
+    __syncthreads();  // the table slice is in shared memory
     // announces that this CTA has started; the matching wait comes before the first remote store
     // into rank 0's shared memory. Nothing is published here, so the arrive needs no fence.
     if (cs > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-#endif
 
     // ---- everything below may read what the previous kernel wrote ----
     grid_dependency_wait();
@@ -377,26 +378,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         app_val = *reinterpret_cast<const uint4*>(src);
     }
 
-#if KVC_DEC_STEAL
-    // the counter lives in rank 0's shared memory
-    uint32_t counter_addr = 0;
-    if (cs > 1) {
-        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-        counter_addr = map_to_rank(s_counter, 0);
-    }
-    auto grab = [&]() -> int {  // lane 0 only
-        if (cs > 1) {
-            int v;
-            asm volatile("atom.shared::cluster.add.u32 %0, [%1], 1;" : "=r"(v) : "r"(counter_addr) : "memory");
-            return v;
-        }
-        return atomicAdd(s_counter, 1);
-    };
-    int next_j = (lane == 0) ? grab() : 0;  // the block the next refill will load
-#else
     int next_j = cb0 + gw + ST * nwarps_cl;  // fixed round-robin: this warp's blocks are gw mod (warps)
-    auto grab = [&]() -> int { return next_j + nwarps_cl; };
-#endif
 
     // O^T accumulators: o[mt] = dims mt*16 + g (+8) x heads 2*t4, 2*t4+1; running max / sum per head pair
     float o[D / 16][4];
@@ -410,18 +392,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // refill stage s with the next block of the cluster's range, if any is left (after the warp has read it)
     auto refill = [&](int s) {
         __syncwarp();
-#if KVC_DEC_STEAL
-        const int nj = __shfl_sync(0xffffffffu, next_j, 0);
-#else
         const int nj = next_j;
-        next_j = grab();
-#endif
-        if (nj < cb1 && lane == 0) {
-            issue(s, s_table[nj - cb0]);
-#if KVC_DEC_STEAL
-            next_j = grab();
-#endif
-        }
+        next_j += nwarps_cl;
+        if (nj < cb1 && lane == 0) issue(s, s_table[nj - cb0]);
 #pragma unroll
         for (int k = 0; k < ST; ++k)
             if (k == s) blk[k] = nj < cb1 ? nj : -1;
@@ -435,7 +408,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
 #pragma unroll
         for (int k = 0; k < ST; ++k)
             if (k == s) jj = blk[k];  // register select, no local memory
-        if (jj < 0) break;            // grabs only grow: the first empty stage ends the warp's work
+        if (jj < 0) break;            // blocks only grow: the first empty stage ends the warp's work
         {
             const bool ok = mbar_wait_bounded(&wbars[s], (phase >> s) & 1u, kWaitLimitNs);
             phase ^= 1u << s;
@@ -595,16 +568,15 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     __syncthreads();
     KVC_TRACE_MARK(4);
 
-    const bool direct = nclus == 1 && cs == 1;  // a single CTA holds the whole context
+    const bool final_here = nclus == 1 && !p.force_partials;  // this cluster's result is the output
+    const bool direct = final_here && cs == 1;                  // a single CTA holds the whole range
     const int stride = 16 + p.G * D;  // floats per cluster merge slot: m[8], l[8], acc[G][D]
     // in a cluster this CTA's merged state goes to its slot in rank 0: rank 0's own state at s_m, or
     // inbox slot rank - 1 (same layout)
     uint32_t slot = 0;
     if (cs > 1) {
-#if !KVC_DEC_STEAL
         // every CTA of the cluster has started (the prologue arrive), so rank 0's shared memory is live
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-#endif
         slot = map_to_rank(rank == 0 ? s_m : s_inbox + (rank - 1) * stride, 0);
     }
     // every thread merges the warps of this CTA for four consecutive outputs (head gg, dims d..d+3): it
@@ -631,7 +603,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
             if (direct) {
                 store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
             } else if (cs == 1) {  // one CTA per cluster: its state is the cluster's partial
-                const int64_t row = h * p.nparts + cidx;
+                const int64_t row = h * p.part_stride + p.part_base + cidx;
                 *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
                 if (d == 0) {
                     p.part_ml[row * 2 + 0] = M;
@@ -683,10 +655,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
             O = fma4(w, *reinterpret_cast<const float4*>(r + 16 + e), O);
         }
         const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
-        if (nclus == 1) {
+        if (final_here) {
             store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
         } else {
-            const int64_t row = h * p.nparts + cidx;
+            const int64_t row = h * p.part_stride + p.part_base + cidx;
             *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
             if (d == 0) {
                 p.part_ml[row * 2 + 0] = M;
@@ -697,37 +669,268 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     KVC_TRACE_END();
 }
 
-// Merge the per-cluster partials of every (sequence, query head) for contexts
-// longer than one cluster covers: 8 groups of 32 lanes walk the parts with a
-// running (M, L, acc), then the groups merge.
+// ---- cascade: the shared prefix of a group of sequences, read once per group ----------------------
+//
+// Sequences g0 .. g1-1 (a group of at most 8) begin their block-table rows with the same `nsh` blocks.
+// One CTA per (group, chunk of the shared blocks, KV head) streams those blocks once through a ring in
+// shared memory; warp w attends member g0 + w over every block of the chunk (the decode kernel's block
+// math: S^T = K Q^T, online softmax in base 2, O^T += V^T (P_hi + P_lo)^T) and writes its partial
+// state (m, l, acc) as prefix part `chunk` of (member, head). All prefix positions lie inside every
+// member's context (16 * nsh < ctx), so nothing is masked.
+constexpr int kPrefixStages = 4;
+
+struct PrefixKernelParams {
+    const __half* q;
+    const int32_t* block_table;
+    const int32_t* group_start;  // [n_groups + 1]
+    const int32_t* blk_off;      // per sequence: its group's shared blocks
+    float* part_ml;
+    float* part_acc;
+    unsigned* err;
+    int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride;
+    float scale_log2;
+};
+
 template <int D>
-__global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* __restrict__ part_ml,
-                                                                    const float* __restrict__ part_acc,
-                                                                    const int32_t* __restrict__ context_lens,
-                                                                    void* out, int Hq, int nparts_grid, int bpc,
-                                                                    int max_blocks, int max_ctx, int out_f32) {
+__global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                   const __grid_constant__ CUtensorMap tmV,
+                                                                   const PrefixKernelParams p) {
+    using C = DecodeCfg<D>;
+    constexpr int NW = 8, ST = kPrefixStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * C::kStageBytes);
+    uint64_t* empty = full + ST;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + ST);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int grp = blockIdx.x / p.nchunks, chunk = blockIdx.x % p.nchunks, kvh = blockIdx.y;
+#if KVC_DEC_EARLY_TRIGGER
+    grid_dependents_launch();
+#endif
+    const int g0 = p.group_start[grp], g1 = p.group_start[grp + 1];
+    const int nmem = g1 - g0;
+    if (nmem < 1) return;
+    const int nsh = p.blk_off[g0];
+    if (nmem > NW || nsh < 0 || nsh > p.max_blocks) {
+        if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+        return;
+    }
+    const int j0 = chunk * p.chunk, j1 = min(nsh, j0 + p.chunk);
+    if (j0 >= j1) return;  // the group's prefix is shorter
+    const int n = j1 - j0;
+    const int32_t* table = p.block_table + static_cast<int64_t>(g0) * p.max_blocks;  // the first member's row
+
+    auto issue = [&](int i) {  // thread 0: block j0 + i into stage i % ST
+        uint64_t* bar = &full[i % ST];
+        const int phys = table[j0 + i];
+        if (phys < 0 || phys >= p.num_blocks) {
+            atomicOr(p.err, KVC_DEVERR_BLOCK_ID);
+            mbar_arrive(bar);  // completes the phase without data: the block is skipped
+            return;
+        }
+        uint8_t* st = smem + (i % ST) * C::kStageBytes;
+        mbar_arrive_expect_tx(bar, C::kStageBytes);
+        const int y = (phys * p.Hkv + kvh) * kBlockSize;
+        const uint64_t policy = l2_policy_evict_first();
+#pragma unroll
+        for (int x = 0; x < D; x += 64) {
+            tma_load_2d(st + (x / 64) * 2048, &tmK, bar, x, y, policy);
+            tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
+        }
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NW);
+        }
+        *s_abort = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        for (int i = 0; i < min(n, ST); ++i) issue(i);
+    }
+    __syncthreads();
+    grid_dependency_wait();  // q may come from the previous kernel
+
+    const bool member = warp < nmem;
+    const int b = g0 + (member ? warp : 0);
+    uint32_t qa[D / 16][2];
+    {
+        const bool row_ok = member && g < p.G;
+        const __half* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (row_ok ? g : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t4) : 0u;
+            qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t4) : 0u;
+        }
+    }
+    float o[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const float sl2 = p.scale_log2;
+    const int mi = lane >> 3;
+    int issued = min(n, ST), i = 0;
+    bool ok = true;
+    // bounded wait that also gives up once another warp has
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t k = 0;; ++k) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (*s_abort) return false;
+            if ((k & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+                *s_abort = 1;
+                return false;
+            }
+        }
+    };
+#pragma unroll 1
+    for (; i < n; ++i) {
+        const int s = i % ST;
+        ok = __all_sync(0xffffffffu, wait(&full[s], (i / ST) & 1));
+        if (!ok) break;
+        if (member) {
+            const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
+            const uint32_t vbase = kbase + C::kTileBytes;
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
+            }
+            const float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+            }
+            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+            const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+            const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1), p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+            l_run[0] = l_run[0] * al0 + p0 + p2;
+            l_run[1] = l_run[1] * al1 + p1 + p3;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
+            const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
+            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+            const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
+            const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+                mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        // thread 0 refills the stage once every warp has read it
+        if (threadIdx.x == 0 && issued < n) {
+            if (!wait(&empty[s], (i / ST) & 1)) {
+                ok = false;
+            } else {
+                issue(issued);
+                ++issued;
+            }
+        }
+        if (!__all_sync(0xffffffffu, ok)) break;
+    }
+    if (!ok || *s_abort) {
+        // thread 0 lets copies still in flight land; the CTA's shared memory stays allocated until it exits
+        if (threadIdx.x == 0) {
+            atomicOr(p.err, KVC_DEVERR_TIMEOUT);
+            for (int k = i; k < issued; ++k) mbar_wait_bounded(&full[k % ST], (k / ST) & 1, kWaitLimitNs / 8);
+        }
+        return;
+    }
+    if (!member) return;
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], sh);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], sh);
+    }
+    // this warp's partial for heads 2*t4, 2*t4+1 (those < G): prefix part `chunk` of member b
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int gg = 2 * t4 + hh;
+        if (gg >= p.G) continue;
+        const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.part_stride + chunk;
+        if (g == 0) {
+            p.part_ml[row * 2 + 0] = m_run[hh];
+            p.part_ml[row * 2 + 1] = l_run[hh];
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            p.part_acc[row * D + mt * 16 + g] = o[mt][hh];
+            p.part_acc[row * D + mt * 16 + g + 8] = o[mt][2 + hh];
+        }
+    }
+}
+
+struct CombineParams {
+    const float* part_ml;
+    const float* part_acc;
+    const int32_t* context_lens;
+    const int32_t* blk_off;  // null, or per sequence: blocks of its row covered by the prefix parts
+    void* out;
+    unsigned* err;
+    int Hq, part_stride, part_base, bpc, max_blocks, max_ctx, out_f32;
+    int prefix_chunk;  // blocks per prefix part (cascade), 0 = no prefix parts
+    int cascade;       // 1: the decode kernel wrote only partials; this kernel writes every output row
+};
+
+// Merge the partial states of every (sequence, query head): the clusters along a context longer than
+// one cluster covers, and in a cascade also the parts of the shared prefix. 8 groups of 32 lanes walk
+// the parts with a running (M, L, acc), then the groups merge.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_combine_kernel(const CombineParams p) {
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
     grid_dependency_wait();
     const int h = blockIdx.x, b = blockIdx.y;
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ctx = context_lens[b];
-    if (ctx < 1 || ctx > max_blocks * kBlockSize || ctx > max_ctx) return;
-    const int nparts = ((ctx + kBlockSize - 1) / kBlockSize + bpc - 1) / bpc;
-    if (nparts <= 1) return;  // the cluster wrote the output itself
-    const int64_t row0 = (static_cast<int64_t>(b) * Hq + h) * nparts_grid;
+    const int ctx_full = p.context_lens[b];
+    const int off = p.blk_off != nullptr ? p.blk_off[b] : 0;
+    const int ctx = ctx_full - off * kBlockSize;  // tokens of the suffix parts
+    if (off < 0 || off >= p.max_blocks || ctx_full < 1 || ctx_full > p.max_blocks * kBlockSize ||
+        ctx_full > p.max_ctx || ctx < 1) {
+        if (p.cascade) {  // the decode kernel left this row to us
+            if (h == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+            if (threadIdx.x < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + threadIdx.x, 0.f);
+        }
+        return;
+    }
+    const int nsuf = ((ctx + kBlockSize - 1) / kBlockSize + p.bpc - 1) / p.bpc;
+    const int npre = off > 0 && p.prefix_chunk > 0 ? (off + p.prefix_chunk - 1) / p.prefix_chunk : 0;
+    if (!p.cascade && nsuf <= 1) return;  // the cluster wrote the output itself
+    const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h) * p.part_stride;
     float M = -INFINITY, L = 0.f, O[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) O[v] = 0.f;
-    for (int s = grp; s < nparts; s += 8) {
-        const float m = part_ml[(row0 + s) * 2], l = part_ml[(row0 + s) * 2 + 1];
+    for (int s = grp; s < npre + nsuf; s += 8) {
+        const int64_t row = row0 + (s < npre ? s : p.part_base + s - npre);
+        const float m = p.part_ml[row * 2], l = p.part_ml[row * 2 + 1];
         if (!(l > 0.f)) continue;
         const float Mn = fmaxf(M, m);
         const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
         const float w = ex2(m - Mn);
         L = L * a + l * w;
 #pragma unroll
-        for (int v = 0; v < V; ++v) O[v] = O[v] * a + part_acc[(row0 + s) * D + lane * V + v] * w;
+        for (int v = 0; v < V; ++v) O[v] = O[v] * a + p.part_acc[row * D + lane * V + v] * w;
         M = Mn;
     }
     if (lane == 0) {
@@ -748,7 +951,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const float* 
             Lt += sL[k] * w;
             Ot += sO[k][d] * w;
         }
-        store_out(out, out_f32, (static_cast<int64_t>(b) * Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
+        store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
     }
 }
 
@@ -764,6 +967,14 @@ static int sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 128) cached[dev].store(n);
     return n;
+}
+
+// partial rows in a workspace: (m, l) pairs padded to a multiple of 4 floats, then the acc rows (16-byte aligned)
+static size_t partials_bytes(size_t nrow, int D) {
+    return (((nrow * 2 + 3) & ~static_cast<size_t>(3)) + nrow * D) * sizeof(float);
+}
+static float* partials_acc(float* part_ml, size_t nrow) {
+    return part_ml + ((nrow * 2 + 3) & ~static_cast<size_t>(3));
 }
 
 // one-time kernel attributes (largest shared-memory size this kernel can be launched with)
@@ -849,9 +1060,7 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
     plan->cluster = cs;
     plan->num_parts = nparts;
     plan->num_splits = nparts * cs;  // grid.x: whole clusters
-    // (m, l) rows, padded to a multiple of 4 floats so that the acc rows after them are 16-byte aligned
-    const size_t nrow = static_cast<size_t>(B) * Hq * nparts;
-    plan->workspace_bytes = nparts > 1 ? (((nrow * 2 + 3) & ~static_cast<size_t>(3)) + nrow * D) * sizeof(float) : 0;
+    plan->workspace_bytes = nparts > 1 ? partials_bytes(static_cast<size_t>(B) * Hq * nparts, D) : 0;
     return cudaSuccess;
 }
 
@@ -921,6 +1130,43 @@ static cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// kernel parameters of a plain decode call (one part per cluster, final output where one cluster covers
+// the context); the cascade launch adjusts the partial layout and the block offset
+static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& plan, float* part_ml, float* part_acc) {
+    DecodeKernelParams p;
+    p.q = a.q;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_cache = const_cast<__half*>(a.k_cache);
+    p.v_cache = const_cast<__half*>(a.v_cache);
+    p.k_next = a.k_next;
+    p.v_next = a.v_next;
+    p.block_table = a.block_table;
+    p.context_lens = a.context_lens;
+    p.out = a.out;
+    p.part_ml = part_ml;
+    p.part_acc = part_acc;
+    p.err = a.err;
+    p.max_blocks = a.max_blocks;
+    p.num_blocks = a.num_blocks;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.max_ctx = a.max_context_len;
+    p.bpc = plan.blocks_per_split;
+    p.csize = plan.cluster;
+    p.part_base = 0;
+    p.part_stride = plan.num_parts;
+    p.force_partials = 0;
+    p.blk_off = nullptr;
+    p.out_f32 = a.out_f32;
+    p.scale_log2 = a.scale * kLog2e;
+    static std::atomic<unsigned> launch_seq{0};
+    p.trace_seq = launch_seq.fetch_add(1);
+    return p;
+}
+
 template <int D>
 static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     using C = DecodeCfg<D>;
@@ -933,47 +1179,32 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     e = make_tile_map(&tmV, a.v_cache, D, rows);
     if (e != cudaSuccess) return e;
 
-    DecodeKernelParams p;
-    p.q = a.q;
-    p.k_new = a.k_new;
-    p.v_new = a.v_new;
-    p.k_cache = const_cast<__half*>(a.k_cache);
-    p.v_cache = const_cast<__half*>(a.v_cache);
-    p.k_next = a.k_next;
-    p.v_next = a.v_next;
-    p.block_table = a.block_table;
-    p.context_lens = a.context_lens;
-    p.out = a.out;
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
-    p.part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    p.part_acc = plan.num_parts > 1 ? p.part_ml + ((nrow * 2 + 3) & ~static_cast<size_t>(3)) : nullptr;
-    p.err = a.err;
-    p.max_blocks = a.max_blocks;
-    p.num_blocks = a.num_blocks;
-    p.B = a.B;
-    p.Hq = a.Hq;
-    p.Hkv = a.Hkv;
-    p.G = a.Hq / a.Hkv;
-    p.max_ctx = a.max_context_len;
-    p.bpc = plan.blocks_per_split;
-    p.csize = plan.cluster;
-    p.nparts = plan.num_parts;
-    p.out_f32 = a.out_f32;
-    p.scale_log2 = a.scale * kLog2e;
-    static std::atomic<unsigned> launch_seq{0};
-    p.trace_seq = launch_seq.fetch_add(1);
-
+    float* part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
+    const DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
     e = launch(paged_decode_kernel<D>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream, pdl,
                static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
-        dim3 cgrid(a.Hq, a.B);
-        e = launch(paged_decode_combine_kernel<D>, cgrid, dim3(256), 0, stream, true, 1u,
-                   static_cast<const float*>(p.part_ml), static_cast<const float*>(p.part_acc), a.context_lens,
-                   a.out, a.Hq, plan.num_parts, plan.blocks_per_split, a.max_blocks, a.max_context_len,
-                   a.out_f32);
+        CombineParams c;
+        c.part_ml = p.part_ml;
+        c.part_acc = p.part_acc;
+        c.context_lens = a.context_lens;
+        c.blk_off = nullptr;
+        c.out = a.out;
+        c.err = a.err;
+        c.Hq = a.Hq;
+        c.part_stride = plan.num_parts;
+        c.part_base = 0;
+        c.bpc = plan.blocks_per_split;
+        c.max_blocks = a.max_blocks;
+        c.max_ctx = a.max_context_len;
+        c.out_f32 = a.out_f32;
+        c.prefix_chunk = 0;
+        c.cascade = 0;
+        e = launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
     }
     return e;
 }
@@ -986,6 +1217,108 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     switch (a.D) {
         case 64: return launch_decode_d<64>(a, plan, stream);
         case 128: return launch_decode_d<128>(a, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---- cascade ----------------------------------------------------------------------------------------
+cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_groups, int max_shared_blocks,
+                         CascadePlan* plan) {
+    cudaError_t e = decode_plan(B, Hq, Hkv, D, max_ctx, 0, &plan->suffix);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    // prefix CTAs: about two per SM over all (group, KV head) pairs, at least 4 blocks each
+    const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(n_groups) * Hkv);
+    const int64_t per_pair = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / pairs);
+    plan->chunk = static_cast<int>(std::max<int64_t>(4, (max_shared_blocks + per_pair - 1) / per_pair));
+    plan->nchunks = max_shared_blocks > 0 ? (max_shared_blocks + plan->chunk - 1) / plan->chunk : 0;
+    plan->part_stride = plan->nchunks + plan->suffix.num_parts;
+    plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * Hq * plan->part_stride, D);
+    return cudaSuccess;
+}
+
+template <int D>
+static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
+                                    int n_groups, const CascadePlan& cp, cudaStream_t stream) {
+    using C = DecodeCfg<D>;
+    cudaError_t e = decode_setup<D>();
+    if (e != cudaSuccess) return e;
+    const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
+    CUtensorMap tmK, tmV;
+    e = make_tile_map(&tmK, a.k_cache, D, rows);
+    if (e != cudaSuccess) return e;
+    e = make_tile_map(&tmV, a.v_cache, D, rows);
+    if (e != cudaSuccess) return e;
+    const size_t nrow = static_cast<size_t>(a.B) * a.Hq * cp.part_stride;
+    float* part_ml = static_cast<float*>(a.workspace);
+    float* part_acc = partials_acc(part_ml, nrow);
+    const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
+    const int G = a.Hq / a.Hkv;
+
+    // 1. the shared prefixes: prefix parts 0 .. nchunks-1
+    if (cp.nchunks > 0) {
+        PrefixKernelParams pp;
+        pp.q = a.q;
+        pp.block_table = a.block_table;
+        pp.group_start = group_start;
+        pp.blk_off = shared_blocks;
+        pp.part_ml = part_ml;
+        pp.part_acc = part_acc;
+        pp.err = a.err;
+        pp.max_blocks = a.max_blocks;
+        pp.num_blocks = a.num_blocks;
+        pp.Hq = a.Hq;
+        pp.Hkv = a.Hkv;
+        pp.G = G;
+        pp.chunk = cp.chunk;
+        pp.nchunks = cp.nchunks;
+        pp.part_stride = cp.part_stride;
+        pp.scale_log2 = a.scale * kLog2e;
+        const size_t smem = kPrefixStages * C::kStageBytes + 2 * kPrefixStages * 8 + 16 + 1024;
+        e = launch(paged_decode_prefix_kernel<D>, dim3(n_groups * cp.nchunks, a.Hkv), dim3(256), smem, stream, pdl,
+                   1u, tmK, tmV, pp);
+        if (e != cudaSuccess) return e;
+    }
+    // 2. every sequence past its shared blocks: suffix parts from nchunks on
+    DecodeKernelParams p = decode_params(a, cp.suffix, part_ml, part_acc);
+    p.blk_off = shared_blocks;
+    p.force_partials = 1;
+    p.part_base = cp.nchunks;
+    p.part_stride = cp.part_stride;
+    e = launch(paged_decode_kernel<D>, dim3(cp.suffix.num_splits, a.Hkv, a.B), dim3(C::kThreads),
+               C::smem_bytes(cp.suffix.cluster, G), stream, pdl, static_cast<unsigned>(cp.suffix.cluster), tmK, tmV,
+               p);
+    if (e != cudaSuccess) return e;
+    // 3. merge both into the output
+    CombineParams c;
+    c.part_ml = part_ml;
+    c.part_acc = part_acc;
+    c.context_lens = a.context_lens;
+    c.blk_off = shared_blocks;
+    c.out = a.out;
+    c.err = a.err;
+    c.Hq = a.Hq;
+    c.part_stride = cp.part_stride;
+    c.part_base = cp.nchunks;
+    c.bpc = cp.suffix.blocks_per_split;
+    c.max_blocks = a.max_blocks;
+    c.max_ctx = a.max_context_len;
+    c.out_f32 = a.out_f32;
+    c.prefix_chunk = cp.chunk;
+    c.cascade = 1;
+    return launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
+}
+
+cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
+                           int n_groups, int max_shared_blocks, cudaStream_t stream) {
+    CascadePlan cp;
+    cudaError_t e = cascade_plan(a.B, a.Hq, a.Hkv, a.D, a.max_context_len, n_groups, max_shared_blocks, &cp);
+    if (e != cudaSuccess) return e;
+    if (cp.workspace_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    switch (a.D) {
+        case 64: return launch_cascade_d<64>(a, group_start, shared_blocks, n_groups, cp, stream);
+        case 128: return launch_cascade_d<128>(a, group_start, shared_blocks, n_groups, cp, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -53,6 +53,23 @@ struct DecodeArgs {
     unsigned* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Cascade decode: groups of at most 8 consecutive sequences whose block-table rows begin with the same
+// shared blocks. The prefix kernel reads those blocks once per group; the decode kernel covers each
+// sequence's remaining blocks; the combine kernel merges both.
+constexpr int kMaxGroupSize = 8;
+struct CascadePlan {
+    DecodePlan suffix;  // the decode kernel over every sequence's blocks past its shared prefix
+    int chunk;          // shared blocks per prefix CTA
+    int nchunks;        // prefix parts per (sequence, head): chunks of the longest shared prefix
+    int part_stride;    // partial rows per (sequence, head): nchunks + suffix.num_parts
+    size_t workspace_bytes;
+};
+cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int n_groups, int max_shared_blocks,
+                         CascadePlan* plan);
+// group_start: device [n_groups + 1]; shared_blocks: device [B], the shared blocks of each sequence's group
+cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
+                           int n_groups, int max_shared_blocks, cudaStream_t stream);
 // process-wide: launch decode kernels as programmatic dependents of the previous kernel
 void set_launch_overlap(int on);
 // copies up to `cap` trace records (80 bytes each) of the decode kernel; cudaErrorNotSupported

@@ -273,3 +273,56 @@ def small_decode(seed, B, Hq, Hkv, D, ctx, L=1, bs=16, peak_frac=0.0) -> DecodeW
     """A small decode case for parity sweeps (ragged contexts allowed)."""
     return _decode(f"small_B{B}_{Hq}x{Hkv}_D{D}", [BASE_SEED, 1000 + seed], L=L, B=B, Hq=Hq,
                    Hkv=Hkv, D=D, ctx=list(ctx), bs=bs, peak_frac=peak_frac)
+
+
+@dataclass
+class CascadeWorkload:
+    """Groups of consecutive sequences whose block tables begin with the same blocks (one layer)."""
+
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    scale: float
+    NB: int
+    q: np.ndarray            # f16 [B][Hq][D]
+    k_pool: np.ndarray       # f16 [NB][Hkv][bs][D]
+    v_pool: np.ndarray
+    block_table: np.ndarray  # int32 [B][max_blocks], -1 past each context
+    ctx: np.ndarray          # int32 [B]
+    group_start: np.ndarray  # int32 [n_groups + 1]
+    shared_blocks: np.ndarray  # int32 [B]: the leading blocks of b's group
+
+
+def cascade_decode(seed, group_sizes, shared, extra, Hq=14, Hkv=2, D=64, bs=16) -> CascadeWorkload:
+    """Group g (group_sizes[g] consecutive sequences) shares shared[g] leading blocks; sequence b then owns
+    extra[b] >= 1 more tokens in private blocks. Physical blocks are a seeded permutation; every K/V row of the
+    pool, used or not, is N(0,1) fp16."""
+    rng = np.random.default_rng(seed)
+    B = int(sum(group_sizes))
+    assert len(extra) == B and len(shared) == len(group_sizes) and min(extra) >= 1
+    need = int(sum(shared)) + sum(_ceil_div(int(e), bs) for e in extra)
+    NB = need + 3
+    perm = iter(rng.permutation(NB).astype(np.int32).tolist())
+    rows, ctx, sh = [], [], []
+    b = 0
+    for g, n in enumerate(group_sizes):
+        common = [next(perm) for _ in range(int(shared[g]))]
+        for _ in range(n):
+            own = [next(perm) for _ in range(_ceil_div(int(extra[b]), bs))]
+            rows.append(common + own)
+            ctx.append(bs * int(shared[g]) + int(extra[b]))
+            sh.append(int(shared[g]))
+            b += 1
+    mb = max(len(r) for r in rows)
+    table = np.full((B, mb), -1, dtype=np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    gs = np.zeros(len(group_sizes) + 1, dtype=np.int32)
+    gs[1:] = np.cumsum(group_sizes)
+    return CascadeWorkload(
+        name=f"cascade_{seed}", Hq=Hq, Hkv=Hkv, D=D, bs=bs, scale=1.0 / float(np.sqrt(D)), NB=NB,
+        q=normal_f16(rng, (B, Hq, D)), k_pool=normal_f16(rng, (NB, Hkv, bs, D)),
+        v_pool=normal_f16(rng, (NB, Hkv, bs, D)), block_table=table, ctx=np.array(ctx, dtype=np.int32),
+        group_start=gs, shared_blocks=np.array(sh, dtype=np.int32))
