@@ -510,6 +510,50 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
                   "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
 
+    # config 3, attention only: the plain decode vs the cascade (each group's shared prefix read once)
+    _, _, pws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
+    pwsb = torch.zeros(max(pws, 16), dtype=torch.uint8, device=device)
+    plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, pwsb,
+                                               max_ctx)
+    us_plain = _timed_calls(plain, 20, flush, stream)
+    gs, sh, mxs = kvc.kv_cascade_groups(res["block_table"], mix.ctx)
+    gs_d, sh_d = torch.from_numpy(gs).to(device), torch.from_numpy(sh).to(device)
+    cws = kvc.paged_decode_cascade_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx, len(gs) - 1, mxs)
+    cwsb = torch.zeros(max(cws, 16), dtype=torch.uint8, device=device)
+    casc = lambda: kvc.paged_decode_cascade_attention(q, res["k_cache"], res["v_cache"], table, ctx, gs_d, sh_d, mxs,
+                                                      mix.scale, out, cwsb, max_ctx)
+    us_casc = _timed_calls(casc, 20, flush, stream)
+    shared_reads = int(sum(int(sh[b]) for b in range(mix.B)) - sum(int(sh[gs[g]]) for g in range(len(gs) - 1)))
+    emit({"config": "3, attention only: plain decode vs cascade (shared prefix blocks read once per group)",
+          "us_plain": us_plain, "us_cascade": us_casc, "speedup": us_plain / us_casc,
+          "groups": len(gs) - 1, "max_shared_blocks": mxs,
+          "block_reads_saved": shared_reads * mix.Hkv, "bytes_saved": shared_reads * 16 * row,
+          "logical_GBps_plain": logical / (us_plain * 1e-6) / 1e9,
+          "logical_GBps_cascade": logical / (us_casc * 1e-6) / 1e9})
+
+    # a long shared prefix (not a listed config): 8 groups x 8 sequences share 8192 tokens, 1..200 private
+    cw = workloads.cascade_decode(4242, [8] * 8, [512] * 8, list(np.random.default_rng(7).integers(1, 201, size=64)))
+    cq, ckp, cvp = (torch.from_numpy(x).to(device) for x in (cw.q, cw.k_pool, cw.v_pool))
+    ctb, cct = torch.from_numpy(cw.block_table).to(device), torch.from_numpy(cw.ctx).to(device)
+    cgs, csh = torch.from_numpy(cw.group_start).to(device), torch.from_numpy(cw.shared_blocks).to(device)
+    cout = torch.empty((64, cw.Hq, cw.D), dtype=torch.float16, device=device)
+    cmax = int(cw.ctx.max())
+    _, _, pws2 = kvc.paged_decode_plan(64, cw.Hq, cw.Hkv, cw.D, cmax)
+    pw2 = torch.zeros(max(pws2, 16), dtype=torch.uint8, device=device)
+    cws2 = kvc.paged_decode_cascade_plan(64, cw.Hq, cw.Hkv, cw.D, cmax, 8, 512)
+    cw2 = torch.zeros(max(cws2, 16), dtype=torch.uint8, device=device)
+    us_p = _timed_calls(lambda: kvc.paged_decode_attention(cq, ckp, cvp, ctb, cct, cw.scale, cout, pw2, cmax), 20,
+                        flush, stream)
+    us_c = _timed_calls(lambda: kvc.paged_decode_cascade_attention(cq, ckp, cvp, ctb, cct, cgs, csh, 512, cw.scale,
+                                                                   cout, cw2, cmax), 20, flush, stream)
+    lb = int(cw.ctx.astype(np.int64).sum()) * row
+    ub = (8 * 512 * 16 + int(sum(int(c) - 8192 for c in cw.ctx))) * row
+    emit({"config": "supplementary (not a listed config): 8 groups x 8 sequences sharing an 8192-token prefix, "
+                    "1..200 private tokens each, 14 q / 2 KV heads, D=64",
+          "us_plain": us_p, "us_cascade": us_c, "speedup": us_p / us_c, "logical_bytes": lb, "unique_bytes": ub,
+          "logical_GBps_plain": lb / (us_p * 1e-6) / 1e9, "unique_GBps_cascade": ub / (us_c * 1e-6) / 1e9})
+    del ckp, cvp
+
     # head_dim 128 shapes: the 7B-class model (32 q / 8 KV heads) and the 32 x 32 x 128 MHA shape
     for Hq, Hkv in ((32, 8), (32, 32)):
         B, c, D = 32, 2048, 128

@@ -133,8 +133,7 @@ struct DecodeKernelParams {
     // partial state of cluster c of (sequence b, query head h) goes to row (b * Hq + h) * part_stride +
     // part_base + c of part_ml / part_acc
     int part_base, part_stride;
-    int force_partials;      // 1: every cluster writes its partial, even when it covers the whole range
-    const int32_t* blk_off;  // null, or per sequence: the leading blocks of its table row attended elsewhere
+    const int32_t* blk_off;  // suffix pass: per sequence, the leading blocks of its table row attended elsewhere
     int out_f32;
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
@@ -228,7 +227,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-template <int D>
+// kSuffix: the cascade's suffix pass (per-sequence block offset, partial states only); the plain decode
+// is compiled without either
+template <int D, bool kSuffix>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeKernelParams p) {
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     // (entries [cb0, cb0 + bpc), clipped to the row) goes to shared memory meanwhile, for the refills.
     // the first blk_off[b] blocks of the row (a shared prefix attended elsewhere) are skipped: this call
     // covers the rest of the context, in block coordinates relative to that offset
-    const int off_raw = p.blk_off != nullptr ? p.blk_off[b] : 0;
+    const int off_raw = kSuffix ? p.blk_off[b] : 0;
     const bool off_ok = off_raw >= 0 && off_raw < p.max_blocks;
     const int off = off_ok ? off_raw : 0;
     const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.max_blocks + off;
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     if (!off_ok || ctx_full < 1 || ctx_full > p.max_blocks * kBlockSize || ctx_full > p.max_ctx || ctx < 1) {
         grid_dependency_wait();
         // with forced partials the combine kernel checks the same and writes the zeros
-        if (blockIdx.x == 0 && !p.force_partials) {
+        if (blockIdx.x == 0 && !kSuffix) {
             if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
             for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
                 store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     __syncthreads();
     KVC_TRACE_MARK(4);
 
-    const bool final_here = nclus == 1 && !p.force_partials;  // this cluster's result is the output
+    const bool final_here = nclus == 1 && !kSuffix;  // this cluster's result is the output
     const bool direct = final_here && cs == 1;                  // a single CTA holds the whole range
     const int stride = 16 + p.G * D;  // floats per cluster merge slot: m[8], l[8], acc[G][D]
     // in a cluster this CTA's merged state goes to its slot in rank 0: rank 0's own state at s_m, or
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
             if (direct) {
                 store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
             } else if (cs == 1) {  // one CTA per cluster: its state is the cluster's partial
-                const int64_t row = h * p.part_stride + p.part_base + cidx;
+                const int64_t row = h * p.part_stride + (kSuffix ? p.part_base : 0) + cidx;
                 *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
                 if (d == 0) {
                     p.part_ml[row * 2 + 0] = M;
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         if (final_here) {
             store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
         } else {
-            const int64_t row = h * p.part_stride + p.part_base + cidx;
+            const int64_t row = h * p.part_stride + (kSuffix ? p.part_base : 0) + cidx;
             *reinterpret_cast<float4*>(p.part_acc + row * D + d) = O;
             if (d == 0) {
                 p.part_ml[row * 2 + 0] = M;
@@ -677,7 +678,19 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
 // math: S^T = K Q^T, online softmax in base 2, O^T += V^T (P_hi + P_lo)^T) and writes its partial
 // state (m, l, acc) as prefix part `chunk` of (member, head). All prefix positions lie inside every
 // member's context (16 * nsh < ctx), so nothing is masked.
-constexpr int kPrefixStages = 4;
+#ifndef KVC_PREFIX_STAGES  // blocks in flight per prefix CTA
+#define KVC_PREFIX_STAGES 12
+#endif
+#ifndef KVC_PREFIX_CTAS  // prefix CTAs per SM the chunking aims for
+#define KVC_PREFIX_CTAS 4
+#endif
+constexpr int kPrefixStages = KVC_PREFIX_STAGES;
+
+// dynamic shared memory of the prefix kernel: the ring, its full/empty barriers, the abort flag, alignment
+template <int D>
+constexpr size_t prefix_smem_bytes() {
+    return kPrefixStages * DecodeCfg<D>::kStageBytes + 2 * kPrefixStages * 8 + 16 + 1024;
+}
 
 struct PrefixKernelParams {
     const __half* q;
@@ -984,10 +997,15 @@ static cudaError_t decode_setup() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::smem_bytes(kMaxCluster, 8));
-        if (err == cudaSuccess && kMaxCluster > 8)
-            err = cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        err = cudaFuncSetAttribute(paged_decode_prefix_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   prefix_smem_bytes<D>());
+        for (auto kern : {paged_decode_kernel<D, false>, paged_decode_kernel<D, true>}) {
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           C::smem_bytes(kMaxCluster, 8));
+            if (err == cudaSuccess && kMaxCluster > 8)
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
     });
     return err;
 }
@@ -1007,7 +1025,7 @@ static cudaError_t decode_occupancy(int smem, int* ctas) {
             return cudaSuccess;
         }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D>, C::kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, paged_decode_kernel<D, false>, C::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     for (int i = 0; i < 64; ++i)
@@ -1158,7 +1176,6 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.csize = plan.cluster;
     p.part_base = 0;
     p.part_stride = plan.num_parts;
-    p.force_partials = 0;
     p.blk_off = nullptr;
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kLog2e;
@@ -1184,7 +1201,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     const DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
-    e = launch(paged_decode_kernel<D>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream, pdl,
+    e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream, pdl,
                static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
@@ -1228,9 +1245,9 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_group
     if (e != cudaSuccess) return e;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
-    // prefix CTAs: about two per SM over all (group, KV head) pairs, at least 4 blocks each
+    // prefix CTAs: about KVC_PREFIX_CTAS per SM over all (group, KV head) pairs, at least 4 blocks each
     const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(n_groups) * Hkv);
-    const int64_t per_pair = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / pairs);
+    const int64_t per_pair = std::max<int64_t>(1, KVC_PREFIX_CTAS * static_cast<int64_t>(sms) / pairs);
     plan->chunk = static_cast<int>(std::max<int64_t>(4, (max_shared_blocks + per_pair - 1) / per_pair));
     plan->nchunks = max_shared_blocks > 0 ? (max_shared_blocks + plan->chunk - 1) / plan->chunk : 0;
     plan->part_stride = plan->nchunks + plan->suffix.num_parts;
@@ -1275,18 +1292,17 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
         pp.nchunks = cp.nchunks;
         pp.part_stride = cp.part_stride;
         pp.scale_log2 = a.scale * kLog2e;
-        const size_t smem = kPrefixStages * C::kStageBytes + 2 * kPrefixStages * 8 + 16 + 1024;
-        e = launch(paged_decode_prefix_kernel<D>, dim3(n_groups * cp.nchunks, a.Hkv), dim3(256), smem, stream, pdl,
+        e = launch(paged_decode_prefix_kernel<D>, dim3(n_groups * cp.nchunks, a.Hkv), dim3(256),
+                   prefix_smem_bytes<D>(), stream, pdl,
                    1u, tmK, tmV, pp);
         if (e != cudaSuccess) return e;
     }
     // 2. every sequence past its shared blocks: suffix parts from nchunks on
     DecodeKernelParams p = decode_params(a, cp.suffix, part_ml, part_acc);
     p.blk_off = shared_blocks;
-    p.force_partials = 1;
     p.part_base = cp.nchunks;
     p.part_stride = cp.part_stride;
-    e = launch(paged_decode_kernel<D>, dim3(cp.suffix.num_splits, a.Hkv, a.B), dim3(C::kThreads),
+    e = launch(paged_decode_kernel<D, true>, dim3(cp.suffix.num_splits, a.Hkv, a.B), dim3(C::kThreads),
                C::smem_bytes(cp.suffix.cluster, G), stream, pdl, static_cast<unsigned>(cp.suffix.cluster), tmK, tmV,
                p);
     if (e != cudaSuccess) return e;
