@@ -267,7 +267,29 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
                                           int block_size, int max_context_len, float scale, void* out, int out_dtype,
                                           void* workspace, size_t workspace_bytes, void* stream);
 
-/* Launch overlap (process-wide, default off).  When on, decode kernels are
+/* Multi-token decode (speculative verification): each sequence appends
+ * q_len (1..8) new tokens in one step and all of them attend at once,
+ * causally among themselves: token t sits at position ctx - q_len + t and
+ * attends to positions 0 .. ctx - q_len + t of its context (speculative
+ * decoding paragraph of "Tornar a inferência barata" (neuralialabs.com):
+ * verifying gamma proposed tokens is one forward pass over gamma positions).
+ *   q        device fp16 [B][q_len][Hq][D]
+ *   out      device [B][q_len][Hq][D], out_dtype KVC_F16 or KVC_F32
+ *   context_lens  device int32 [B], including the q_len new tokens
+ *                 (q_len <= ctx <= min(max_blocks * bs, max_context_len))
+ *   workspace     device, 16-byte aligned, >= paged_decode_multi_plan's bytes
+ * Other arguments as in paged_decode_attention; the new tokens' K/V must be
+ * in the cache already (kv_append with their slots).  Each chunk of a
+ * sequence's blocks is read once for all q_len tokens.  Two kernel launches. */
+kvc_status paged_decode_multi_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                   int q_len, size_t* workspace_bytes);
+kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                        const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                        int q_len, int B, int Hq, int Hkv, int head_dim, int block_size,
+                                        int max_context_len, float scale, void* out, int out_dtype, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* Launch overlap (process-wide, default off)./* Launch overlap (process-wide, default off).  When on, decode kernels are
  * launched as programmatic dependents of the kernel before them on the
  * stream: they read block tables, context lengths and the cached K/V
  * history before that kernel has finished, and q, k_new, v_new, the

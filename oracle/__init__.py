@@ -7,7 +7,8 @@ library (``paged_kv_cache_27_gb300``) and never imports it.
 Contents:
   * ``oracle.c`` (built into ``liboracle.so`` by :func:`build`): decode over a
     paged cache, full causal attention, varlen prefill, append scatter, and
-    the split-softmax partial/merge pair, all in fp64.
+    the split-softmax partial/merge pair, all in fp64; :func:`decode_multi`
+    (several new tokens per sequence) composes the decode.
   * :mod:`oracle.page_pool`: the block pool and per-request block table of
     the PagedAttention article, restated.
   * :mod:`oracle.paging`: slot arithmetic, cache filling and the serving-mix
@@ -118,6 +119,24 @@ def decode(q, k_cache, v_cache, block_table, context_lens, scale, nthreads=None)
                                nthreads or default_threads())
     if rc != 0:
         raise IndexError("oracle_decode: context length or block id out of range")
+    return out
+
+
+def decode_multi(q, k_cache, v_cache, block_table, context_lens, scale, nthreads=None):
+    """Multi-token decode, fp64: q [B][T][Hq][D] holds each sequence's T newest tokens (in the cache already,
+    context_lens including them); token t sits at position ctx - T + t and attends to positions 0 .. ctx - T + t
+    (verifying T drafted tokens in one pass over them: speculative-decoding paragraph of "Tornar a inferência
+    barata", neuralialabs.com).  Each token is the plain decode over its own prefix of the context.
+    Returns out [B][T][Hq][D] float64.  Pinned against full causal attention on gathered sequences."""
+    q = np.asarray(q)
+    B, T = q.shape[:2]
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    if np.any(ctx < T):
+        raise IndexError("decode_multi: a context is shorter than the new tokens")
+    out = np.empty(q.shape, dtype=np.float64)
+    for t in range(T):
+        out[:, t] = decode(np.ascontiguousarray(q[:, t]), k_cache, v_cache, block_table, ctx - T + 1 + t, scale,
+                           nthreads)
     return out
 
 

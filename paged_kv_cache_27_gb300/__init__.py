@@ -30,6 +30,7 @@ __all__ = [
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
     "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
+    "paged_decode_multi_plan", "paged_decode_multi_attention",
     "prefill_attention", "DEVERR",
 ]
 
@@ -112,6 +113,9 @@ def _load():
         "kvc_trace_read": (I, [P, I, PI, I]),
         "paged_decode_cascade_plan": (I, [I, I, I, I, I, I, I, I, PSZ]),
         "kv_cascade_groups": (I, [P, I, I, P, I, I, P, PI, P, PI]),
+        "paged_decode_multi_plan": (I, [I, I, I, I, I, I, I, PSZ]),
+        "paged_decode_multi_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ,
+                                             P]),
         "paged_decode_cascade_attention": (I, [P, P, P, I, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P,
                                                I, P, SZ, P]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
@@ -421,6 +425,43 @@ def paged_decode_cascade_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         group_start.numel() - 1, int(max_shared_blocks), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
         _dptr(out, None, "out"), od, _dptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream, q)), "paged_decode_cascade_attention")
+
+
+def paged_decode_multi_plan(B: int, Hq: int, Hkv: int, head_dim: int, max_context_len: int, q_len: int,
+                            block_size: int = 16) -> int:
+    """Workspace bytes of paged_decode_multi_attention for these sizes."""
+    ws = ctypes.c_size_t()
+    _check(_lib.paged_decode_multi_plan(B, Hq, Hkv, head_dim, block_size, max_context_len, q_len, ctypes.byref(ws)),
+           "paged_decode_multi_plan")
+    return ws.value
+
+
+def paged_decode_multi_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 block_table: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                 out: torch.Tensor, workspace: torch.Tensor, max_context_len: int,
+                                 stream=None) -> None:
+    """q [B][q_len][Hq][D] fp16: the q_len newest tokens of every sequence (already in the cache), causal among
+    themselves; out like q (fp16 or fp32); workspace: paged_decode_multi_plan bytes."""
+    B, T, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shapes do not match q")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table / context_lens do not match B")
+    if out.dtype == torch.float16:
+        od = KVC_F16
+    elif out.dtype == torch.float32:
+        od = KVC_F32
+    else:
+        raise TypeError("out must be float16 or float32")
+    _check(_lib.paged_decode_multi_attention(
+        _dptr(q, torch.float16, "q"), _dptr(k_cache, torch.float16, "k_cache"),
+        _dptr(v_cache, torch.float16, "v_cache"), NB, _dptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), T, B, Hq, Hkv, D, bs,
+        int(max_context_len), float(scale), _dptr(out, None, "out"), od, _dptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream, q)), "paged_decode_multi_attention")
 
 
 def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,

@@ -613,6 +613,49 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
     return KVC_OK;
 }
 
+kvc_status paged_decode_multi_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
+                                   int q_len, size_t* workspace_bytes) {
+    kvc_status s = check_decode_shape(B, Hq, Hkv, head_dim, block_size, max_context_len);
+    if (s != KVC_OK) return s;
+    if (q_len < 1 || q_len > kvc::kMaxQueryTokens)
+        return fail(KVC_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, kvc::kMaxQueryTokens);
+    kvc::MultiPlan plan;
+    cudaError_t e = kvc::multi_plan(B, Hq, Hkv, head_dim, max_context_len, q_len, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "multi-token plan");
+    if (workspace_bytes) *workspace_bytes = plan.workspace_bytes;
+    return KVC_OK;
+}
+
+kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                        const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                                        int q_len, int B, int Hq, int Hkv, int head_dim, int block_size,
+                                        int max_context_len, float scale, void* out, int out_dtype, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    if (q_len < 1 || q_len > kvc::kMaxQueryTokens)
+        return fail(KVC_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, kvc::kMaxQueryTokens);
+    std::vector<int32_t> ctx, table;
+    kvc_status s = decode_validate(q, k_cache, v_cache, num_blocks, block_table, max_blocks, context_lens, B, Hq, Hkv,
+                                   head_dim, block_size, max_context_len, out, out_dtype, 0, stream, ctx, table);
+    if (s != KVC_OK || B == 0) return s;
+    if (g_checked.load())
+        for (int b = 0; b < B; ++b)
+            if (ctx[b] < q_len)
+                return fail(KVC_ERR_CAPACITY, "sequence %d: context length %d below q_len %d", b, ctx[b], q_len);
+    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table,
+                                    max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
+                                    out_dtype, workspace, workspace_bytes, 0);
+    kvc::MultiPlan plan;
+    cudaError_t e = kvc::multi_plan(B, Hq, Hkv, head_dim, max_context_len, q_len, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "multi-token plan");
+    s = check_workspace(plan.workspace_bytes, workspace, workspace_bytes);
+    if (s != KVC_OK) return s;
+    e = kvc::device_error_word(&a.err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+    e = kvc::launch_multi(a, q_len, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_multi_attention launch");
+    return KVC_OK;
+}
+
 kvc_status prefill_attention(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int nseq,
                              int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim, float scale, int causal,
                              void* out, int out_dtype, void* stream) {

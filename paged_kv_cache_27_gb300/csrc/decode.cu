@@ -670,70 +670,90 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     KVC_TRACE_END();
 }
 
-// ---- cascade: the shared prefix of a group of sequences, read once per group ----------------------
+// ---- query groups that share their key blocks --------------------------------------------------------
 //
-// Sequences g0 .. g1-1 (a group of at most 8) begin their block-table rows with the same `nsh` blocks.
-// One CTA per (group, chunk of the shared blocks, KV head) streams those blocks once through a ring in
-// shared memory; warp w attends member g0 + w over every block of the chunk (the decode kernel's block
-// math: S^T = K Q^T, online softmax in base 2, O^T += V^T (P_hi + P_lo)^T) and writes its partial
-// state (m, l, acc) as prefix part `chunk` of (member, head). All prefix positions lie inside every
-// member's context (16 * nsh < ctx), so nothing is masked.
-#ifndef KVC_PREFIX_STAGES  // blocks in flight per prefix CTA
+// One CTA streams a range of K/V blocks once through a ring in shared memory (thread 0 issues the copies);
+// warp w attends its own query rows (the G heads of one query token) over every block of the range with the
+// decode kernel's block math (S^T = K Q^T, online softmax in base 2, O^T += V^T (P_hi + P_lo)^T) and
+// writes its partial state (m, l, acc) as part `chunk` of its rows; the combine kernel merges the parts.
+//  - cascade prefix (kMulti = false): the group is sequences g0 .. g1-1 (at most 8) whose block-table rows
+//    begin with the same `nsh` blocks; warp w is sequence g0 + w; the range is a chunk of those blocks, all
+//    of them inside every member's context, so nothing is masked.
+//  - multi-token decode (kMulti = true): the group is the q_len new tokens of one sequence; warp t
+//    is token t at position ctx - q_len + t, which sees keys 0 .. ctx - q_len + t (causal among the new
+//    tokens); the range is a chunk of the sequence's blocks.
+#ifndef KVC_PREFIX_STAGES  // blocks in flight per group CTA
 #define KVC_PREFIX_STAGES 12
 #endif
-#ifndef KVC_PREFIX_CTAS  // prefix CTAs per SM the chunking aims for
+#ifndef KVC_PREFIX_CTAS  // group CTAs per SM the chunking aims for
 #define KVC_PREFIX_CTAS 4
 #endif
-constexpr int kPrefixStages = KVC_PREFIX_STAGES;
+constexpr int kGroupStages = KVC_PREFIX_STAGES;
 
-// dynamic shared memory of the prefix kernel: the ring, its full/empty barriers, the abort flag, alignment
+// dynamic shared memory of the group kernel: the ring, its full/empty barriers, the abort flag, alignment
 template <int D>
-constexpr size_t prefix_smem_bytes() {
-    return kPrefixStages * DecodeCfg<D>::kStageBytes + 2 * kPrefixStages * 8 + 16 + 1024;
+constexpr size_t group_smem_bytes() {
+    return kGroupStages * DecodeCfg<D>::kStageBytes + 2 * kGroupStages * 8 + 16 + 1024;
 }
 
-struct PrefixKernelParams {
-    const __half* q;
+struct GroupKernelParams {
+    const __half* q;             // [B][Hq][D] (cascade) or [B][q_len][Hq][D] (multi-token)
     const int32_t* block_table;
-    const int32_t* group_start;  // [n_groups + 1]
-    const int32_t* blk_off;      // per sequence: its group's shared blocks
+    const int32_t* group_start;  // cascade: [n_groups + 1]
+    const int32_t* blk_off;      // cascade: per sequence, its group's shared blocks
+    const int32_t* context_lens; // multi-token: per sequence, including its q_len new tokens
     float* part_ml;
     float* part_acc;
     unsigned* err;
-    int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride;
+    int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride, q_len, max_ctx;
     float scale_log2;
 };
 
-template <int D>
-__global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                                   const __grid_constant__ CUtensorMap tmV,
-                                                                   const PrefixKernelParams p) {
+template <int D, bool kMulti>
+__global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                  const __grid_constant__ CUtensorMap tmV,
+                                                                  const GroupKernelParams p) {
     using C = DecodeCfg<D>;
-    constexpr int NW = 8, ST = kPrefixStages;
+    constexpr int ST = kGroupStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * C::kStageBytes);
     uint64_t* empty = full + ST;
     volatile int* s_abort = reinterpret_cast<volatile int*>(empty + ST);
 
+    const int NW = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int grp = blockIdx.x / p.nchunks, chunk = blockIdx.x % p.nchunks, kvh = blockIdx.y;
 #if KVC_DEC_EARLY_TRIGGER
     grid_dependents_launch();
 #endif
-    const int g0 = p.group_start[grp], g1 = p.group_start[grp + 1];
-    const int nmem = g1 - g0;
-    if (nmem < 1) return;
-    const int nsh = p.blk_off[g0];
-    if (nmem > NW || nsh < 0 || nsh > p.max_blocks) {
-        if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-        return;
+    // the group: its members (warps), the rows they attend through, and the block range [j0, j1)
+    int nmem, nblk, ctx = 0;
+    const int32_t* table;
+    if constexpr (kMulti) {
+        nmem = p.q_len;
+        ctx = p.context_lens[grp];
+        if (ctx < p.q_len || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
+            if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+            return;  // the combine kernel writes this sequence's zeros
+        }
+        nblk = (ctx + kBlockSize - 1) / kBlockSize;
+        table = p.block_table + static_cast<int64_t>(grp) * p.max_blocks;
+    } else {
+        const int g0 = p.group_start[grp];
+        nmem = p.group_start[grp + 1] - g0;
+        if (nmem < 1) return;
+        nblk = p.blk_off[g0];
+        if (nmem > NW || nblk < 0 || nblk > p.max_blocks) {
+            if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+            return;
+        }
+        table = p.block_table + static_cast<int64_t>(g0) * p.max_blocks;  // the first member's row
     }
-    const int j0 = chunk * p.chunk, j1 = min(nsh, j0 + p.chunk);
-    if (j0 >= j1) return;  // the group's prefix is shorter
+    const int j0 = chunk * p.chunk, j1 = min(nblk, j0 + p.chunk);
+    if (j0 >= j1) return;  // the range is shorter
     const int n = j1 - j0;
-    const int32_t* table = p.block_table + static_cast<int64_t>(g0) * p.max_blocks;  // the first member's row
 
     auto issue = [&](int i) {  // thread 0: block j0 + i into stage i % ST
         uint64_t* bar = &full[i % ST];
@@ -768,15 +788,18 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
     grid_dependency_wait();  // q may come from the previous kernel
 
     const bool member = warp < nmem;
-    const int b = g0 + (member ? warp : 0);
+    const int64_t qrow = kMulti ? static_cast<int64_t>(grp) * p.q_len + (member ? warp : 0)
+                                : static_cast<int64_t>(p.group_start[grp]) + (member ? warp : 0);
+    // multi-token: the last key position this warp's token sees
+    const int last_key = kMulti ? ctx - p.q_len + (member ? warp : 0) : 0;
     uint32_t qa[D / 16][2];
     {
         const bool row_ok = member && g < p.G;
-        const __half* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (row_ok ? g : 0)) * D;
+        const __half* qp = p.q + (qrow * p.Hq + kvh * p.G + (row_ok ? g : 0)) * D;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t4) : 0u;
-            qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t4) : 0u;
+            qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * t4) : 0u;
+            qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qp + ks * 16 + 8 + 2 * t4) : 0u;
         }
     }
     float o[D / 16][4];
@@ -808,6 +831,10 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
         if (member) {
             const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
             const uint32_t vbase = kbase + C::kTileBytes;
+            const int k0 = (j0 + i) * kBlockSize;  // first key position of the block
+            // keys this warp's token sees in the block, and rows of the block inside the context
+            const int vis = kMulti ? last_key - k0 + 1 : kBlockSize;
+            const int rem = kMulti ? ctx - k0 : kBlockSize;
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -815,7 +842,8 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
                 ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                 mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
             }
-            const float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
+            const float x0 = g < vis ? sc[0] * sl2 : -INFINITY, x1 = g < vis ? sc[1] * sl2 : -INFINITY;
+            const float x2 = g + 8 < vis ? sc[2] * sl2 : -INFINITY, x3 = g + 8 < vis ? sc[3] * sl2 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) {
@@ -823,10 +851,13 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
             }
             const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
+            // a block with no visible key (m stays -inf) leaves the state unchanged
+            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[0] - mn0);
+            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[1] - mn1);
             m_run[0] = mn0;
             m_run[1] = mn1;
-            const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1), p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+            const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0), p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
+            const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1), p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
             l_run[0] = l_run[0] * al0 + p0 + p2;
             l_run[1] = l_run[1] * al1 + p1 + p3;
 #pragma unroll
@@ -841,10 +872,20 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
             const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
             const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
             const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+            // rows of V past the context may hold any bits (even NaN): zero them in registers
+            uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+            if (rem < kBlockSize) {
+                keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
+                keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
+            }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                a0 &= keep0;
+                a1 &= keep0;
+                a2 &= keep1;
+                a3 &= keep1;
                 mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
                 mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
@@ -876,12 +917,12 @@ __global__ void __launch_bounds__(256) paged_decode_prefix_kernel(const __grid_c
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], sh);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], sh);
     }
-    // this warp's partial for heads 2*t4, 2*t4+1 (those < G): prefix part `chunk` of member b
+    // this warp's partial for heads 2*t4, 2*t4+1 (those < G): part `chunk` of its query rows
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int gg = 2 * t4 + hh;
         if (gg >= p.G) continue;
-        const int64_t row = (static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg) * p.part_stride + chunk;
+        const int64_t row = (qrow * p.Hq + kvh * p.G + gg) * p.part_stride + chunk;
         if (g == 0) {
             p.part_ml[row * 2 + 0] = m_run[hh];
             p.part_ml[row * 2 + 1] = l_run[hh];
@@ -903,7 +944,8 @@ struct CombineParams {
     unsigned* err;
     int Hq, part_stride, part_base, bpc, max_blocks, max_ctx, out_f32;
     int prefix_chunk;  // blocks per prefix part (cascade), 0 = no prefix parts
-    int cascade;       // 1: the decode kernel wrote only partials; this kernel writes every output row
+    int cascade;       // 1: only partials were written; this kernel writes every output row
+    int q_len;         // query rows per sequence (multi-token decode; 1 otherwise): row y is sequence y / q_len
 };
 
 // Merge the partial states of every (sequence, query head): the clusters along a context longer than
@@ -914,23 +956,23 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
     grid_dependency_wait();
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, y = blockIdx.y, b = y / p.q_len;  // y: the query row (a sequence's token)
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctx_full = p.context_lens[b];
     const int off = p.blk_off != nullptr ? p.blk_off[b] : 0;
     const int ctx = ctx_full - off * kBlockSize;  // tokens of the suffix parts
-    if (off < 0 || off >= p.max_blocks || ctx_full < 1 || ctx_full > p.max_blocks * kBlockSize ||
+    if (off < 0 || off >= p.max_blocks || ctx_full < p.q_len || ctx_full > p.max_blocks * kBlockSize ||
         ctx_full > p.max_ctx || ctx < 1) {
-        if (p.cascade) {  // the decode kernel left this row to us
+        if (p.cascade) {  // the attention kernels left this row to us
             if (h == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-            if (threadIdx.x < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + threadIdx.x, 0.f);
+            if (threadIdx.x < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + threadIdx.x, 0.f);
         }
         return;
     }
     const int nsuf = ((ctx + kBlockSize - 1) / kBlockSize + p.bpc - 1) / p.bpc;
     const int npre = off > 0 && p.prefix_chunk > 0 ? (off + p.prefix_chunk - 1) / p.prefix_chunk : 0;
     if (!p.cascade && nsuf <= 1) return;  // the cluster wrote the output itself
-    const int64_t row0 = (static_cast<int64_t>(b) * p.Hq + h) * p.part_stride;
+    const int64_t row0 = (static_cast<int64_t>(y) * p.Hq + h) * p.part_stride;
     float M = -INFINITY, L = 0.f, O[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) O[v] = 0.f;
@@ -964,7 +1006,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
             Lt += sL[k] * w;
             Ot += sO[k][d] * w;
         }
-        store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
+        store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
     }
 }
 
@@ -997,8 +1039,9 @@ static cudaError_t decode_setup() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(paged_decode_prefix_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   prefix_smem_bytes<D>());
+        for (auto kern : {paged_decode_group_kernel<D, false>, paged_decode_group_kernel<D, true>})
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, group_smem_bytes<D>());
         for (auto kern : {paged_decode_kernel<D, false>, paged_decode_kernel<D, true>}) {
             if (err == cudaSuccess)
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1221,6 +1264,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
         c.out_f32 = a.out_f32;
         c.prefix_chunk = 0;
         c.cascade = 0;
+        c.q_len = 1;
         e = launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
     }
     return e;
@@ -1275,7 +1319,7 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
 
     // 1. the shared prefixes: prefix parts 0 .. nchunks-1
     if (cp.nchunks > 0) {
-        PrefixKernelParams pp;
+        GroupKernelParams pp;
         pp.q = a.q;
         pp.block_table = a.block_table;
         pp.group_start = group_start;
@@ -1291,9 +1335,12 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
         pp.chunk = cp.chunk;
         pp.nchunks = cp.nchunks;
         pp.part_stride = cp.part_stride;
+        pp.context_lens = nullptr;
+        pp.q_len = 1;
+        pp.max_ctx = a.max_context_len;
         pp.scale_log2 = a.scale * kLog2e;
-        e = launch(paged_decode_prefix_kernel<D>, dim3(n_groups * cp.nchunks, a.Hkv), dim3(256),
-                   prefix_smem_bytes<D>(), stream, pdl,
+        e = launch(paged_decode_group_kernel<D, false>, dim3(n_groups * cp.nchunks, a.Hkv),
+                   dim3(32 * kMaxGroupSize), group_smem_bytes<D>(), stream, pdl,
                    1u, tmK, tmV, pp);
         if (e != cudaSuccess) return e;
     }
@@ -1323,6 +1370,7 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
     c.out_f32 = a.out_f32;
     c.prefix_chunk = cp.chunk;
     c.cascade = 1;
+    c.q_len = 1;
     return launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
 }
 
@@ -1335,6 +1383,89 @@ cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, cons
     switch (a.D) {
         case 64: return launch_cascade_d<64>(a, group_start, shared_blocks, n_groups, cp, stream);
         case 128: return launch_cascade_d<128>(a, group_start, shared_blocks, n_groups, cp, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---- multi-token decode ------------------------------------------------------------------------------
+cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, MultiPlan* plan) {
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    const int64_t nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
+    // about KVC_PREFIX_CTAS CTAs per SM over all (sequence, KV head) pairs, at least 4 blocks each
+    const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
+    const int64_t per_pair = std::max<int64_t>(1, KVC_PREFIX_CTAS * static_cast<int64_t>(sms) / pairs);
+    plan->chunk = static_cast<int>(std::max<int64_t>(4, (nblk + per_pair - 1) / per_pair));
+    plan->nchunks = static_cast<int>((nblk + plan->chunk - 1) / plan->chunk);
+    plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * q_len * Hq * plan->nchunks, D);
+    return cudaSuccess;
+}
+
+template <int D>
+static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPlan& mp, cudaStream_t stream) {
+    cudaError_t e = decode_setup<D>();
+    if (e != cudaSuccess) return e;
+    const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
+    CUtensorMap tmK, tmV;
+    e = make_tile_map(&tmK, a.k_cache, D, rows);
+    if (e != cudaSuccess) return e;
+    e = make_tile_map(&tmV, a.v_cache, D, rows);
+    if (e != cudaSuccess) return e;
+    const size_t nrow = static_cast<size_t>(a.B) * q_len * a.Hq * mp.nchunks;
+    float* part_ml = static_cast<float*>(a.workspace);
+    float* part_acc = partials_acc(part_ml, nrow);
+    const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
+    GroupKernelParams gp;
+    gp.q = a.q;
+    gp.block_table = a.block_table;
+    gp.group_start = nullptr;
+    gp.blk_off = nullptr;
+    gp.context_lens = a.context_lens;
+    gp.part_ml = part_ml;
+    gp.part_acc = part_acc;
+    gp.err = a.err;
+    gp.max_blocks = a.max_blocks;
+    gp.num_blocks = a.num_blocks;
+    gp.Hq = a.Hq;
+    gp.Hkv = a.Hkv;
+    gp.G = a.Hq / a.Hkv;
+    gp.chunk = mp.chunk;
+    gp.nchunks = mp.nchunks;
+    gp.part_stride = mp.nchunks;
+    gp.q_len = q_len;
+    gp.max_ctx = a.max_context_len;
+    gp.scale_log2 = a.scale * kLog2e;
+    e = launch(paged_decode_group_kernel<D, true>, dim3(a.B * mp.nchunks, a.Hkv), dim3(32 * q_len),
+               group_smem_bytes<D>(), stream, pdl, 1u, tmK, tmV, gp);
+    if (e != cudaSuccess) return e;
+    CombineParams c;
+    c.part_ml = part_ml;
+    c.part_acc = part_acc;
+    c.context_lens = a.context_lens;
+    c.blk_off = nullptr;
+    c.out = a.out;
+    c.err = a.err;
+    c.Hq = a.Hq;
+    c.part_stride = mp.nchunks;
+    c.part_base = 0;
+    c.bpc = mp.chunk;
+    c.max_blocks = a.max_blocks;
+    c.max_ctx = a.max_context_len;
+    c.out_f32 = a.out_f32;
+    c.prefix_chunk = 0;
+    c.cascade = 1;
+    c.q_len = q_len;
+    return launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B * q_len), dim3(256), 0, stream, true, 1u, c);
+}
+
+cudaError_t launch_multi(const DecodeArgs& a, int q_len, cudaStream_t stream) {
+    MultiPlan mp;
+    cudaError_t e = multi_plan(a.B, a.Hq, a.Hkv, a.D, a.max_context_len, q_len, &mp);
+    if (e != cudaSuccess) return e;
+    if (mp.workspace_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    switch (a.D) {
+        case 64: return launch_multi_d<64>(a, q_len, mp, stream);
+        case 128: return launch_multi_d<128>(a, q_len, mp, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -70,6 +70,18 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int
 // group_start: device [n_groups + 1]; shared_blocks: device [B], the shared blocks of each sequence's group
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);
+
+// Multi-token decode: q_len (1..8) new tokens per sequence, causal among them (token t at position
+// ctx - q_len + t); q and out are [B][q_len][Hq][D]. The group kernel streams each chunk of a sequence's
+// blocks once for all its tokens; the combine kernel merges the chunks.
+constexpr int kMaxQueryTokens = 8;
+struct MultiPlan {
+    int chunk;    // blocks per CTA
+    int nchunks;  // parts per (token, head): chunks of the longest context
+    size_t workspace_bytes;
+};
+cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_context_len, int q_len, MultiPlan* plan);
+cudaError_t launch_multi(const DecodeArgs& a, int q_len, cudaStream_t stream);
 // process-wide: launch decode kernels as programmatic dependents of the previous kernel
 void set_launch_overlap(int on);
 // copies up to `cap` trace records (80 bytes each) of the decode kernel; cudaErrorNotSupported

@@ -1,0 +1,97 @@
+"""Multi-token decode (several new tokens per sequence, causal among them) on the GPU vs the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def poisoned_pools(wl, dev="cuda"):
+    """The workload's pools on the device, every row past a sequence's context set to NaN."""
+    k = torch.from_numpy(wl.k_pool).to(dev)
+    v = torch.from_numpy(wl.v_pool).to(dev)
+    for b, c in enumerate(wl.ctx):
+        last, used = int(wl.block_table[b, (int(c) - 1) // wl.bs]), int(c) % wl.bs
+        if used:
+            k[last, :, used:] = float("nan")
+            v[last, :, used:] = float("nan")
+    return k, v
+
+
+def run_multi(wl, out_dtype=torch.float32, checked=False, ctx=None):
+    import paged_kv_cache_27_gb300 as kvc
+    dev = "cuda"
+    kp, vp = poisoned_pools(wl)
+    ctx_h = wl.ctx if ctx is None else ctx
+    q = torch.from_numpy(wl.q).to(dev)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(np.asarray(ctx_h, np.int32)).to(dev)
+    B = wl.q.shape[0]
+    max_ctx = int(np.max(wl.ctx))
+    ws = kvc.paged_decode_multi_plan(B, wl.Hq, wl.Hkv, wl.D, max_ctx, wl.T)
+    workspace = torch.full((max(ws, 16),), 0x7F, dtype=torch.uint8, device=dev)
+    out = torch.empty(wl.q.shape, dtype=out_dtype, device=dev)
+    kvc.kvc_set_checked_mode(checked)
+    try:
+        kvc.paged_decode_multi_attention(q, kp, vp, table, ctx_d, wl.scale, out, workspace, max_ctx)
+        torch.cuda.synchronize()
+    finally:
+        kvc.kvc_set_checked_mode(False)
+    return out, kp, vp, q, table, ctx_d, max_ctx
+
+
+CASES = [
+    # seed, contexts, T, Hq, Hkv, D
+    (1, [1], 1, 1, 1, 64),
+    (2, [2, 17, 300], 2, 14, 2, 64),
+    (3, [4, 16, 33, 1000], 4, 8, 1, 64),
+    (4, [8, 4096], 8, 8, 8, 128),
+    (5, [3, 15, 16, 17, 20000], 3, 14, 2, 64),
+    (6, [8, 9, 23, 24, 25, 31, 32, 33], 8, 14, 2, 64),
+    (7, [130, 5000], 5, 16, 2, 128),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_multi_token_matches_oracle(case, out_dtype):
+    import paged_kv_cache_27_gb300 as kvc
+    seed, ctx, T, Hq, Hkv, D = CASES[case]
+    wl = workloads.multi_token_decode(seed, ctx, T, Hq=Hq, Hkv=Hkv, D=D)
+    out = run_multi(wl, out_dtype, checked=(case % 2 == 1))[0]
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.decode_multi(wl.q, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+    check_attention(out.reshape(-1, Hq, D), ref.reshape(-1, Hq, D), f"multi-token case {case}")
+
+
+def test_single_token_agrees_with_decode():
+    import paged_kv_cache_27_gb300 as kvc
+    wl = workloads.multi_token_decode(11, [1, 16, 17, 700, 3000], 1)
+    out, kp, vp, q, table, ctx, max_ctx = run_multi(wl)
+    _, _, ws = kvc.paged_decode_plan(len(wl.ctx), wl.Hq, wl.Hkv, wl.D, max_ctx)
+    ref = torch.empty((len(wl.ctx), wl.Hq, wl.D), dtype=torch.float32, device="cuda")
+    kvc.paged_decode_attention(q[:, 0].contiguous(), kp, vp, table, ctx, wl.scale, ref,
+                               torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda"), max_ctx)
+    torch.cuda.synchronize()
+    assert (out[:, 0] - ref).abs().max().item() < 1e-5
+
+
+def test_multi_token_argument_errors():
+    import paged_kv_cache_27_gb300 as kvc
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_multi_plan(2, 14, 2, 64, 100, 9)
+    assert "KVC_ERR_UNSUPPORTED" in str(e.value)
+    wl = workloads.multi_token_decode(12, [5, 40], 4)
+    # checked mode: a context shorter than the new tokens
+    with pytest.raises(kvc.KvcError) as e:
+        run_multi(wl, checked=True, ctx=np.array([3, 40], np.int32))
+    assert "KVC_ERR_CAPACITY" in str(e.value)
+    # unchecked: the sequence is flagged and its rows are zero; the other is still right
+    out = run_multi(wl, ctx=np.array([3, 40], np.int32))[0]
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["CONTEXT"]
+    assert torch.all(out[0] == 0)
+    ref = oracle.decode_multi(wl.q[1:], wl.k_pool, wl.v_pool, wl.block_table[1:], wl.ctx[1:], wl.scale)
+    check_attention(out[1:].reshape(-1, wl.Hq, wl.D), ref.reshape(-1, wl.Hq, wl.D), "multi-token, other sequence")

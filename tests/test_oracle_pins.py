@@ -65,6 +65,35 @@ def test_decode_equals_last_row_of_full_causal(n):
             assert np.max(np.abs(o[0, 0] - full[t])) <= 1e-12
 
 
+@pytest.mark.parametrize("n,T", [(1, 1), (2, 2), (17, 2), (40, 4), (100, 8), (16, 8)])
+def test_decode_multi_equals_last_rows_of_full_causal(n, T):
+    """T new tokens verified at once: token t's output is row n - T + t of the n x n causal attention."""
+    D = 64
+    Q, K, V = f16(n, 1, D), f16(n, 1, D), f16(n, 1, D)
+    kc, vc, table = paged_single(K, V, perm_seed=n + 100 * T)
+    out = oracle.decode_multi(Q[None, n - T:n], kc, vc, table, np.array([n], np.int32), 0.125)
+    full = oracle.causal_attention(Q[:, 0].astype(np.float64), K[:, 0].astype(np.float64),
+                                   V[:, 0].astype(np.float64), 0.125)
+    for t in range(T):
+        assert np.max(np.abs(out[0, t, 0] - full[n - T + t])) <= 1e-12
+
+
+def test_decode_multi_gqa_vs_torch_sdpa():
+    """Several sequences, 8 query / 2 KV heads: torch float64 SDPA with the offset causal mask."""
+    Hq, Hkv, D, T = 8, 2, 64, 3
+    ctxs = [3, 20, 77]
+    for b, n in enumerate(ctxs):
+        Q, K, V = f16(T, Hq, D), f16(n, Hkv, D), f16(n, Hkv, D)
+        kc, vc, table = paged_single(K, V, perm_seed=b)
+        out = oracle.decode_multi(Q[None], kc, vc, table, np.array([n], np.int32), 1 / math.sqrt(D))
+        q = torch.from_numpy(Q.astype(np.float64)).permute(1, 0, 2)                 # [Hq][T][D]
+        k = torch.from_numpy(K.astype(np.float64)).permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+        v = torch.from_numpy(V.astype(np.float64)).permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+        mask = torch.arange(n)[None, :] <= (n - T + torch.arange(T))[:, None]     # [T][n]
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=1 / math.sqrt(D))
+        assert np.max(np.abs(out[0] - ref.permute(1, 0, 2).numpy())) <= 1e-12
+
+
 def test_full_causal_vs_torch_sdpa():
     n, D = 48, 64
     Q, K, V = (RNG.standard_normal((n, D)) for _ in range(3))

@@ -326,3 +326,41 @@ def cascade_decode(seed, group_sizes, shared, extra, Hq=14, Hkv=2, D=64, bs=16) 
         q=normal_f16(rng, (B, Hq, D)), k_pool=normal_f16(rng, (NB, Hkv, bs, D)),
         v_pool=normal_f16(rng, (NB, Hkv, bs, D)), block_table=table, ctx=np.array(ctx, dtype=np.int32),
         group_start=gs, shared_blocks=np.array(sh, dtype=np.int32))
+
+
+@dataclass
+class MultiTokenWorkload:
+    """Each sequence's T newest tokens (already in the cache) to be verified at once (one layer)."""
+
+    name: str
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    scale: float
+    NB: int
+    q: np.ndarray            # f16 [B][T][Hq][D]
+    k_pool: np.ndarray       # f16 [NB][Hkv][bs][D]
+    v_pool: np.ndarray
+    block_table: np.ndarray  # int32 [B][max_blocks], -1 past each context
+    ctx: np.ndarray          # int32 [B], including the T new tokens
+
+
+def multi_token_decode(seed, ctx, T, Hq=14, Hkv=2, D=64, bs=16) -> MultiTokenWorkload:
+    """Contexts ctx (each >= T) on seeded-permuted blocks; every K/V row of the pool N(0,1) fp16."""
+    rng = np.random.default_rng(seed)
+    ctx = np.array(ctx, dtype=np.int32)
+    assert np.all(ctx >= T)
+    nblk = [_ceil_div(int(c), bs) for c in ctx]
+    NB = sum(nblk) + 2
+    perm = rng.permutation(NB).astype(np.int32)
+    table = np.full((len(ctx), max(nblk)), -1, dtype=np.int32)
+    a = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[a:a + n]
+        a += n
+    return MultiTokenWorkload(
+        name=f"multi_{seed}_T{T}", T=T, Hq=Hq, Hkv=Hkv, D=D, bs=bs, scale=1.0 / float(np.sqrt(D)), NB=NB,
+        q=normal_f16(rng, (len(ctx), T, Hq, D)), k_pool=normal_f16(rng, (NB, Hkv, bs, D)),
+        v_pool=normal_f16(rng, (NB, Hkv, bs, D)), block_table=table, ctx=ctx)
