@@ -57,9 +57,9 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 
 # DRAM traffic of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture of
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
-DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/ptx.cuh",
-                  "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "ee27d4072fb6e6c9b7346824adae2e891da699b8cd9f0582ec0b150a93ed39b3",
+DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
+                  "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
+NCU_DECODE_TRAFFIC = {"sources_sha256": "883db2c17a074a6a85cb83e8418d9ab34a45fa9d12630a175d1025e718bbac9d",
                       "bytes_per_launch": 33674624 + 0}
 
 
@@ -553,6 +553,21 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "us_plain": us_p, "us_cascade": us_c, "speedup": us_p / us_c, "logical_bytes": lb, "unique_bytes": ub,
           "logical_GBps_plain": lb / (us_p * 1e-6) / 1e9, "unique_GBps_cascade": ub / (us_c * 1e-6) / 1e9})
     del ckp, cvp
+
+    # multi-token decode (speculative verification): T new tokens per sequence, B=32, context 2048
+    for T in (1, 2, 4, 8):
+        kp, vp, tb, ct, _, _, _ = _decode_state(32, 2048, 14, 2, 64, device, seed=77 + T)
+        qm = torch.randn((32, T, 14, 64), device=device).half()
+        om = torch.empty((32, T, 14, 64), dtype=torch.float16, device=device)
+        wsm = torch.zeros(max(kvc.paged_decode_multi_plan(32, 14, 2, 64, 2048, T), 16), dtype=torch.uint8,
+                          device=device)
+        us = _timed_calls(lambda: kvc.paged_decode_multi_attention(qm, kp, vp, tb, ct, 0.125, om, wsm, 2048), 20,
+                          flush, stream)
+        nbytes = 32 * 2048 * 2 * 2 * 64 * 2
+        emit({"config": f"multi-token decode: T={T} new tokens per sequence, B=32, ctx=2048, 14 q / 2 KV heads, D=64",
+              "us_per_call": us, "GBps": nbytes / (us * 1e-6) / 1e9,
+              "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100, "tokens_per_s": 32 * T / (us * 1e-6)})
+        del kp, vp
 
     # head_dim 128 shapes: the 7B-class model (32 q / 8 KV heads) and the 32 x 32 x 128 MHA shape
     for Hq, Hkv in ((32, 8), (32, 32)):

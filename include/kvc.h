@@ -289,7 +289,7 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
                                         int max_context_len, float scale, void* out, int out_dtype, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
-/* Launch overlap (process-wide, default off)./* Launch overlap (process-wide, default off).  When on, decode kernels are
+/* Launch overlap (process-wide, default off).  When on, decode kernels are
  * launched as programmatic dependents of the kernel before them on the
  * stream: they read block tables, context lengths and the cached K/V
  * history before that kernel has finished, and q, k_new, v_new, the

@@ -1,0 +1,177 @@
+// Pieces shared by the decode-side translation units (decode.cu: the decode and combine kernels;
+// group.cu: the kernel for query groups that share their key blocks): build knobs, the per-head-dim tile
+// configuration, the shared-memory swizzle of a K/V tile, output stores, and host launch helpers.
+#pragma once
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "../../include/kvc.h"
+#include "kvc_internal.h"
+#include "ptx.cuh"
+
+namespace kvc {
+
+// ---- build knobs (defaults are the measured best on GB300) ---------------------------------------
+#ifndef KVC_DEC_WARPS64
+#define KVC_DEC_WARPS64 8
+#endif
+#ifndef KVC_DEC_STAGES64
+#define KVC_DEC_STAGES64 2
+#endif
+#ifndef KVC_DEC_WARPS128
+#define KVC_DEC_WARPS128 4
+#endif
+#ifndef KVC_DEC_STAGES128
+#define KVC_DEC_STAGES128 2
+#endif
+#ifndef KVC_DEC_MAX_CLUSTER
+#define KVC_DEC_MAX_CLUSTER 8
+#endif
+#ifndef KVC_DEC_EARLY_TRIGGER  // let the next kernel launch as soon as every CTA of this one has started
+#define KVC_DEC_EARLY_TRIGGER 1
+#endif
+#ifndef KVC_DEC_EARLY_REFILL  // 1: refill a stage once its K and V are in registers, before the softmax
+#define KVC_DEC_EARLY_REFILL 1
+#endif
+#ifndef KVC_DEC_MIN_CTAS  // resident CTAs per SM the register allocation must allow
+#define KVC_DEC_MIN_CTAS 1
+#endif
+#ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
+#define KVC_DEC_PLAN_CTAS 2
+#endif
+#ifndef KVC_DEC_PREFETCH_AT  // when the next layer's blocks are requested into L2: 0 at start, 1 after the main loop
+#define KVC_DEC_PREFETCH_AT 1
+#endif
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
+constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
+
+template <int D>
+struct DecodeCfg {
+    static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
+    static constexpr int kStages = D == 64 ? KVC_DEC_STAGES64 : KVC_DEC_STAGES128;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kTileBytes = kBlockSize * D * 2;  // one 16 x D fp16 tile
+    static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
+    static constexpr int kWarpRingBytes = kStages * kStageBytes;
+    static constexpr int kRingBytes = kWarps * kWarpRingBytes;
+    static constexpr int kBarBytes = kWarps * kStages * 8;
+    static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA
+    static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice (+ 16 bytes of alignment)
+    // + the inbox of cluster rank 0 (one slot per other CTA of the cluster, sized at launch) + alignment slack
+    static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + kTableBytes + 1024;
+    static int smem_bytes(int cluster, int G) { return kBaseSmemBytes + (cluster - 1) * (16 + G * D) * 4; }
+    static constexpr int kMergeStride = D + 4;  // floats per parked row
+    static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
+};
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return static_cast<uint32_t>(((chunk >> 3) << 11) + (row << 7) + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void store_out(void* out, int out_f32, int64_t idx, float v) {
+    if (out_f32)
+        static_cast<float*>(out)[idx] = v;
+    else
+        static_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+// four consecutive outputs starting at idx (a multiple of 4)
+__device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, float4 v) {
+    if (out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+    } else {
+        uint2 h;
+        h.x = pack_half2(v.x, v.y);
+        h.y = pack_half2(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) = h;
+    }
+}
+__device__ __forceinline__ float4 fma4(float w, float4 a, float4 acc) {
+    return make_float4(fmaf(w, a.x, acc.x), fmaf(w, a.y, acc.y), fmaf(w, a.z, acc.z), fmaf(w, a.w, acc.w));
+}
+__device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
+
+// ---- host helpers ------------------------------------------------------------------------------------
+inline int sm_count() {
+    static std::atomic<int> cached[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 128 && cached[dev].load()) return cached[dev].load();
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 128) cached[dev].store(n);
+    return n;
+}
+
+// partial rows in a workspace: (m, l) pairs padded to a multiple of 4 floats, then the acc rows (16-byte aligned)
+inline size_t partials_bytes(size_t nrow, int D) {
+    return (((nrow * 2 + 3) & ~static_cast<size_t>(3)) + nrow * D) * sizeof(float);
+}
+inline float* partials_acc(float* part_ml, size_t nrow) {
+    return part_ml + ((nrow * 2 + 3) & ~static_cast<size_t>(3));
+}
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D view of one layer's pool: rows of D fp16 (a (block, KV head, offset) row each),
+// boxes of 16 rows x 64 columns, 128-byte swizzle.
+inline cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename Kern, typename... Args>
+inline cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace kvc

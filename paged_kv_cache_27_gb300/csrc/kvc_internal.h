@@ -54,6 +54,25 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Partial states of query rows (m, l, acc) merged into the output by the combine kernel (decode.cu).
+struct CombineParams {
+    const float* part_ml;
+    const float* part_acc;
+    const int32_t* context_lens;
+    const int32_t* blk_off;  // null, or per sequence: blocks of its row covered by the prefix parts
+    void* out;
+    unsigned* err;
+    int Hq, part_stride, part_base, bpc, max_blocks, max_ctx, out_f32;
+    int prefix_chunk;  // blocks per prefix part (cascade), 0 = no prefix parts
+    int cascade;       // 1: only partials were written; this kernel writes every output row
+    int q_len;         // query rows per sequence (multi-token decode; 1 otherwise): row y is sequence y / q_len
+};
+// grid (Hq, rows): one CTA per (query head, query row)
+cudaError_t launch_combine(const CombineParams& c, int D, int rows, cudaStream_t stream);
+// the decode kernel over every sequence past its first blk_off[b] blocks, partial states only (cascade suffix)
+cudaError_t launch_decode_suffix(const DecodeArgs& a, const DecodePlan& plan, const int32_t* blk_off, int part_base,
+                                 int part_stride, float* part_ml, float* part_acc, cudaStream_t stream);
+
 // Cascade decode: groups of at most 8 consecutive sequences whose block-table rows begin with the same
 // shared blocks. The prefix kernel reads those blocks once per group; the decode kernel covers each
 // sequence's remaining blocks; the combine kernel merges both.
