@@ -25,12 +25,15 @@ namespace kvc {
 #ifndef KVC_PREFIX_CTAS  // group CTAs per SM the chunking aims for
 #define KVC_PREFIX_CTAS 4
 #endif
-constexpr int kGroupStages = KVC_PREFIX_STAGES;
+constexpr int kGroupStages = KVC_PREFIX_STAGES;  // the deepest ring; a launch may use fewer stages
+constexpr int kGroupMaxChunk = 4096;              // blocks per CTA at most (their ids are in shared memory)
+constexpr int kGroupMaxSmem = 200 * 1024;         // the dynamic shared memory a group launch may use
 
-// dynamic shared memory of the group kernel: the ring, its full/empty barriers, the abort flag, alignment
+// dynamic shared memory of the group kernel with a ring of `stages` blocks and chunks of `chunk` blocks: the
+// ring, its full/empty barriers, the abort flag, the chunk's block ids, alignment
 template <int D>
-constexpr size_t group_smem_bytes() {
-    return kGroupStages * DecodeCfg<D>::kStageBytes + 2 * kGroupStages * 8 + 16 + 1024;
+constexpr size_t group_smem_bytes(int stages, int chunk) {
+    return stages * DecodeCfg<D>::kStageBytes + 2 * stages * 8 + 16 + 4 * static_cast<size_t>(chunk) + 1024;
 }
 
 struct GroupKernelParams {
@@ -43,6 +46,7 @@ struct GroupKernelParams {
     float* part_acc;
     unsigned* err;
     int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride, q_len, max_ctx;
+    int stages;  // ring depth of this launch, 1 .. kGroupStages
     float scale_log2;
 };
 
@@ -51,12 +55,13 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const GroupKernelParams p) {
     using C = DecodeCfg<D>;
-    constexpr int ST = kGroupStages;
+    const int ST = p.stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * C::kStageBytes);
     uint64_t* empty = full + ST;
     volatile int* s_abort = reinterpret_cast<volatile int*>(empty + ST);
+    int* s_ids = reinterpret_cast<int*>(empty + ST) + 4;  // the chunk's physical block ids
 
     const int NW = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
 
     auto issue = [&](int i) {  // thread 0: block j0 + i into stage i % ST
         uint64_t* bar = &full[i % ST];
-        const int phys = table[j0 + i];
+        const int phys = s_ids[i];
         if (phys < 0 || phys >= p.num_blocks) {
             atomicOr(p.err, KVC_DEVERR_BLOCK_ID);
             mbar_arrive(bar);  // completes the phase without data: the block is skipped
@@ -110,6 +115,8 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
             tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
         }
     };
+    // the chunk's block ids, all at once (one round trip instead of one per copy)
+    for (int k = threadIdx.x; k < n; k += blockDim.x) s_ids[k] = table[j0 + k];
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(&full[s], 1);
@@ -119,9 +126,10 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
         fence_barrier_init();
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
-        for (int i = 0; i < min(n, ST); ++i) issue(i);
     }
     __syncthreads();
+    if (threadIdx.x == 0)
+        for (int i = 0; i < min(n, ST); ++i) issue(i);
     grid_dependency_wait();  // q may come from the previous kernel
 
     const bool member = warp < nmem;
@@ -280,7 +288,7 @@ static cudaError_t group_setup() {
     std::call_once(once, [] {
         for (auto kern : {paged_decode_group_kernel<D, false>, paged_decode_group_kernel<D, true>})
             if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, group_smem_bytes<D>());
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupMaxSmem);
     });
     return err;
 }
@@ -295,7 +303,8 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_group
     // prefix CTAs: about KVC_PREFIX_CTAS per SM over all (group, KV head) pairs, at least 4 blocks each
     const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(n_groups) * Hkv);
     const int64_t per_pair = std::max<int64_t>(1, KVC_PREFIX_CTAS * static_cast<int64_t>(sms) / pairs);
-    plan->chunk = static_cast<int>(std::max<int64_t>(4, (max_shared_blocks + per_pair - 1) / per_pair));
+    plan->chunk = static_cast<int>(
+        std::min<int64_t>(kGroupMaxChunk, std::max<int64_t>(4, (max_shared_blocks + per_pair - 1) / per_pair)));
     plan->nchunks = max_shared_blocks > 0 ? (max_shared_blocks + plan->chunk - 1) / plan->chunk : 0;
     plan->part_stride = plan->nchunks + plan->suffix.num_parts;
     plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * Hq * plan->part_stride, D);
@@ -342,8 +351,9 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
         pp.q_len = 1;
         pp.max_ctx = a.max_context_len;
         pp.scale_log2 = a.scale * kLog2e;
+        pp.stages = kGroupStages;
         e = launch(paged_decode_group_kernel<D, false>, dim3(n_groups * cp.nchunks, a.Hkv),
-                   dim3(32 * kMaxGroupSize), group_smem_bytes<D>(), stream, pdl,
+                   dim3(32 * kMaxGroupSize), group_smem_bytes<D>(kGroupStages, cp.chunk), stream, pdl,
                    1u, tmK, tmV, pp);
         if (e != cudaSuccess) return e;
     }
@@ -389,12 +399,21 @@ cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, Mu
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
     const int64_t nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
-    // about KVC_PREFIX_CTAS CTAs per SM over all (sequence, KV head) pairs, at least 4 blocks each
+    // about KVC_PREFIX_CTAS CTAs per SM over all (sequence, KV head) pairs, at least 4 blocks each (measured
+    // better than sizing by warps: smaller chunks add per-CTA start-up and parts to merge); the ring holds a
+    // whole chunk up to kGroupStages blocks
     const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
     const int64_t per_pair = std::max<int64_t>(1, KVC_PREFIX_CTAS * static_cast<int64_t>(sms) / pairs);
-    plan->chunk = static_cast<int>(std::max<int64_t>(4, (nblk + per_pair - 1) / per_pair));
+    plan->chunk = static_cast<int>(std::min<int64_t>(kGroupMaxChunk, std::max<int64_t>(4, (nblk + per_pair - 1) / per_pair)));
     plan->nchunks = static_cast<int>((nblk + plan->chunk - 1) / plan->chunk);
+    plan->stages = std::min(plan->chunk, kGroupStages);
     plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * q_len * Hq * plan->nchunks, D);
+    if (q_len == 1) {  // a single new token is the plain decode
+        DecodePlan dp;
+        cudaError_t e = decode_plan(B, Hq, Hkv, D, max_ctx, 0, &dp);
+        if (e != cudaSuccess) return e;
+        plan->workspace_bytes = dp.workspace_bytes;
+    }
     return cudaSuccess;
 }
 
@@ -432,8 +451,9 @@ static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPla
     gp.q_len = q_len;
     gp.max_ctx = a.max_context_len;
     gp.scale_log2 = a.scale * kLog2e;
+    gp.stages = mp.stages;
     e = launch(paged_decode_group_kernel<D, true>, dim3(a.B * mp.nchunks, a.Hkv), dim3(32 * q_len),
-               group_smem_bytes<D>(), stream, pdl, 1u, tmK, tmV, gp);
+               group_smem_bytes<D>(mp.stages, mp.chunk), stream, pdl, 1u, tmK, tmV, gp);
     if (e != cudaSuccess) return e;
     CombineParams c;
     c.part_ml = part_ml;
@@ -460,6 +480,7 @@ cudaError_t launch_multi(const DecodeArgs& a, int q_len, cudaStream_t stream) {
     cudaError_t e = multi_plan(a.B, a.Hq, a.Hkv, a.D, a.max_context_len, q_len, &mp);
     if (e != cudaSuccess) return e;
     if (mp.workspace_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    if (q_len == 1) return launch_decode(a, stream);  // q [B][1][Hq][D] is the plain decode's q
     switch (a.D) {
         case 64: return launch_multi_d<64>(a, q_len, mp, stream);
         case 128: return launch_multi_d<128>(a, q_len, mp, stream);

@@ -97,6 +97,7 @@ constexpr int kMaxQueryTokens = 8;
 struct MultiPlan {
     int chunk;    // blocks per CTA
     int nchunks;  // parts per (token, head): chunks of the longest context
+    int stages;   // ring depth
     size_t workspace_bytes;
 };
 cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_context_len, int q_len, MultiPlan* plan);
