@@ -8,7 +8,8 @@ Contents:
   * ``oracle.c`` (built into ``liboracle.so`` by :func:`build`): decode over a
     paged cache, full causal attention, varlen prefill, append scatter, and
     the split-softmax partial/merge pair, all in fp64; :func:`decode_multi`
-    (several new tokens per sequence) composes the decode.
+    (several new tokens per sequence) composes the decode; the fp8 e4m3
+    codec, the per-row quantizer and the decode over an fp8 cache.
   * :mod:`oracle.page_pool`: the block pool and per-request block table of
     the PagedAttention article, restated.
   * :mod:`oracle.paging`: slot arithmetic, cache filling and the serving-mix
@@ -69,6 +70,14 @@ def _load():
             lib.oracle_partial.argtypes = [P, P, P, I, I, I, D, P, P, P]
             lib.oracle_merge.restype = None
             lib.oracle_merge.argtypes = [P, P, P, I, I, P]
+            lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_quantize_fp8.restype = None
+            lib.oracle_quantize_fp8.argtypes = [P, ctypes.c_int64, I, P, P]
+            lib.oracle_decode_fp8.restype = I
+            lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, I, D, P, I]
             _lib = lib
     return _lib
 
@@ -137,6 +146,54 @@ def decode_multi(q, k_cache, v_cache, block_table, context_lens, scale, nthreads
     for t in range(T):
         out[:, t] = decode(np.ascontiguousarray(q[:, t]), k_cache, v_cache, block_table, ctx - T + 1 + t, scale,
                            nthreads)
+    return out
+
+
+# ---- fp8 e4m3 cache (an extension; the pages fix no quantized KV format) ------------------------------
+def e4m3_to_float64(codes) -> np.ndarray:
+    """Value of every e4m3 code (1 sign, 4 exponent bits bias 7, 3 fraction bits; 0x7F / 0xFF are NaN)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_to_double(c) for c in range(256)], dtype=np.float64)
+    return table[codes]
+
+
+def e4m3_from_float32(x) -> np.ndarray:
+    """Nearest e4m3 code of each binary32 value, ties to even, saturating at +-448."""
+    x = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_from_float(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def quantize_fp8(x):
+    """Rows of D fp16 values (last axis) -> (codes uint8 like x, scales float32 x.shape[:-1]): scale = absmax /
+    448 in binary32 (1 for an all-zero row), code = e4m3(x / scale) with the quotient in binary32."""
+    x = _bits(np.asarray(x))
+    D = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    _load().oracle_quantize_fp8(_ptr(x), rows, D, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def decode_fp8(q, k_codes, v_codes, k_scales, v_scales, block_table, context_lens, scale, nthreads=None):
+    """Decode over an fp8 cache: codes [NB][Hkv][bs][D] uint8, scales [NB][Hkv][bs] float32; every cached value
+    is code value x scale (exact in fp64); otherwise :func:`decode`.  Returns out [B][Hq][D] float64."""
+    q = _bits(q)
+    kq, vq = _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    ks, vs = _c(k_scales, np.float32), _c(v_scales, np.float32)
+    NB, Hkv, bs, D = kq.shape
+    B, Hq, Dq = q.shape
+    assert Dq == D and vq.shape == kq.shape and ks.shape == (NB, Hkv, bs) and vs.shape == ks.shape
+    table = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    rc = _load().oracle_decode_fp8(_ptr(q), _ptr(kq), _ptr(vq), _ptr(ks), _ptr(vs), _ptr(table), table.shape[1],
+                                   _ptr(ctx), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(out),
+                                   nthreads or default_threads())
+    if rc != 0:
+        raise IndexError("oracle_decode_fp8: context length or block id out of range")
     return out
 
 

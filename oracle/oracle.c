@@ -64,6 +64,61 @@ void oracle_half_array_to_double(const uint16_t* src, double* dst, int64_t n) {
     for (int64_t i = 0; i < n; ++i) dst[i] = oracle_half_to_double(src[i]);
 }
 
+/* ---- fp8 e4m3 (the quantized-cache extension; the pages fix no KV format) ----
+ * 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; exponent field 0 holds the
+ * subnormals m * 2^-9 (m = 0..7); no infinities; exponent 15 with fraction 7 is NaN,
+ * so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1, expo = (c >> 3) & 0xf, frac = c & 7;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -9);
+    } else if (expo == 15 && frac == 7) {
+        v = NAN;
+    } else {
+        v = ldexp((double)(8 + frac), expo - 10);
+    }
+    return sign ? -v : v;
+}
+
+/* Round to the nearest e4m3 value, ties to the even fraction, magnitudes past 448 saturating to 448. */
+uint8_t oracle_e4m3_from_float(float x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {                 /* subnormal range: steps of 2^-9 */
+        double m = nearbyint(ldexp(a, 9));    /* default rounding: to nearest, ties to even */
+        return sign | (uint8_t)m;             /* m == 8 is 2^-6, the first normal: code 0x08 */
+    }
+    int e2;
+    frexp(a, &e2);                            /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;                           /* unbiased exponent, -6 .. 8 */
+    double m = nearbyint(ldexp(a, 3 - E));    /* 8 .. 16 */
+    if (m == 16.0) {
+        m = 8.0;
+        E += 1;
+    }
+    int code = ((E + 7) << 3) | ((int)m - 8);
+    if (code > 0x7e) code = 0x7e;
+    return sign | (uint8_t)code;
+}
+
+/* Quantize rows of D binary16 values: scale = absmax / 448 in binary32 (1 for an all-zero row),
+ * code_i = e4m3(x_i / scale) with the quotient in binary32.  codes [rows][D], scales [rows]. */
+void oracle_quantize_fp8(const uint16_t* x, int64_t rows, int D, uint8_t* codes, float* scales) {
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < D; ++c) {
+            float v = (float)fabs(oracle_half_to_double(x[r * D + c]));
+            if (v > amax) amax = v;
+        }
+        float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[r] = s;
+        for (int c = 0; c < D; ++c) codes[r * D + c] = oracle_e4m3_from_float((float)oracle_half_to_double(x[r * D + c]) / s);
+    }
+}
+
 /* ---- a tiny static thread pool: run fn(i, ctx) for i in [0, n) ---- */
 typedef void (*task_fn)(int64_t, void*);
 typedef struct {
@@ -134,6 +189,8 @@ static void attend_row(const double* q, const double* K, const double* V, int64_
  * ====================================================================== */
 typedef struct {
     const uint16_t *q, *k, *v;
+    const uint8_t *kq, *vq;       /* fp8 cache instead of k, v when not NULL */
+    const float *ks, *vs;         /* its per-row scales [NB][Hkv][bs] */
     const int32_t *table, *ctx;
     int max_blocks, B, Hq, Hkv, D, bs, NB;
     double scale;
@@ -165,8 +222,13 @@ static void decode_task(int64_t idx, void* p) {
         }
         int64_t row = (((int64_t)phys * J->Hkv + hk) * J->bs + j % J->bs) * D;
         for (int c = 0; c < D; ++c) {
-            K[j * D + c] = oracle_half_to_double(J->k[row + c]);
-            V[j * D + c] = oracle_half_to_double(J->v[row + c]);
+            if (J->kq) { /* dequantized: code value times the row's scale, exact in fp64 */
+                K[j * D + c] = oracle_e4m3_to_double(J->kq[row + c]) * (double)J->ks[row / D];
+                V[j * D + c] = oracle_e4m3_to_double(J->vq[row + c]) * (double)J->vs[row / D];
+            } else {
+                K[j * D + c] = oracle_half_to_double(J->k[row + c]);
+                V[j * D + c] = oracle_half_to_double(J->v[row + c]);
+            }
         }
     }
     for (int c = 0; c < D; ++c) qd[c] = oracle_half_to_double(J->q[((int64_t)b * J->Hq + h) * D + c]);
@@ -180,8 +242,20 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
                   const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B,
                   int Hq, int Hkv, int D, int bs, int NB, double scale, double* out, int nthreads) {
     if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || D > 512 || bs <= 0) return -1;
-    decode_job J = {q, k_cache, v_cache, block_table, context_lens, max_blocks, B, Hq, Hkv, D, bs, NB,
-                    scale, out, 0};
+    decode_job J = {q, k_cache, v_cache, NULL, NULL, NULL, NULL, block_table, context_lens, max_blocks, B, Hq,
+                    Hkv, D, bs, NB, scale, out, 0};
+    parallel_for((int64_t)B * Hq, nthreads, decode_task, &J);
+    return J.bad ? -1 : 0;
+}
+
+/* Decode over an fp8 e4m3 cache with per-row scales (k_codes/v_codes [NB][Hkv][bs][D], scales [NB][Hkv][bs]):
+ * every cached value is code value * scale; the rest is oracle_decode. */
+int oracle_decode_fp8(const uint16_t* q, const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
+                      const float* v_scales, const int32_t* block_table, int max_blocks, const int32_t* context_lens,
+                      int B, int Hq, int Hkv, int D, int bs, int NB, double scale, double* out, int nthreads) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || D > 512 || bs <= 0) return -1;
+    decode_job J = {q, NULL, NULL, k_codes, v_codes, k_scales, v_scales, block_table, context_lens, max_blocks, B,
+                    Hq, Hkv, D, bs, NB, scale, out, 0};
     parallel_for((int64_t)B * Hq, nthreads, decode_task, &J);
     return J.bad ? -1 : 0;
 }
