@@ -234,8 +234,7 @@ def run_ours(args):
     import workloads
 
     wl = workloads.config2()
-    sess = DecodeSession(wl, device=device, out_dtype=torch.float16, blocks_per_split=args.blocks_per_split,
-                         prefetch_next=args.prefetch).fill()
+    sess = DecodeSession(wl, device=device, out_dtype=torch.float16, blocks_per_split=args.blocks_per_split).fill()
     ctx_total = int(wl.ctx.astype(np.int64).sum())
     nblocks_total = int(sum(-(-int(c) // 16) for c in wl.ctx))
     step_bytes = kv_bytes_per_step(ctx_total, L)
@@ -316,12 +315,9 @@ def run_ours(args):
             d_.copy_(h_, non_blocking=True)
         for layer in range(L):
             if fused:
-                nxt = (layer + 1) % L
                 kvc.paged_decode_append_attention(d_q[layer], d_kn[layer], d_vn[layer], sess.k_pool[layer],
                                                   sess.v_pool[layer], d_table, d_ctx, wl.scale, sess.out[layer],
-                                                  sess.workspace, sess.max_ctx, args.blocks_per_split,
-                                                  k_next=sess.k_pool[nxt] if args.prefetch else None,
-                                                  v_next=sess.v_pool[nxt] if args.prefetch else None)
+                                                  sess.workspace, sess.max_ctx, args.blocks_per_split)
             else:
                 kvc.kv_append(sess.h, layer, d_kn[layer], d_vn[layer], d_slots)
                 kvc.paged_decode_attention(d_q[layer], sess.k_pool[layer], sess.v_pool[layer], d_table, d_ctx,
@@ -367,8 +363,7 @@ def run_ours(args):
                    "blocks_per_split": sess.bps, "l2": "inputs larger than L2: 768 MiB of K/V per step",
                    "launch": "CUDA graph of the 24-layer step" + ("" if args.no_overlap else
                                                                              ", programmatic dependent launch"),
-                   "append": "fused into the decode kernel" if fused else "separate kv_append kernel",
-                   "next_layer_l2_prefetch": bool(fused and args.prefetch)},
+                   "append": "fused into the decode kernel" if fused else "separate kv_append kernel"},
         "tokens_per_s": whole_job_rate(B, world, ms_step),
         "pct_hbm_peak": gbs / world / peak * 100.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -643,8 +638,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="separate kv_append + paged_decode_attention calls")
     ap.add_argument("--no-overlap", action="store_true", help="no programmatic dependent launch")
-    ap.add_argument("--prefetch", action="store_true",
-                    help="also request the next layer's blocks into L2 (measured: no gain on this workload)")
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
     ap.add_argument("--suite", action="store_true",
                     help="instead of the headline line: one JSON line per further configuration (1, 3, 4, 5)")

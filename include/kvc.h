@@ -210,11 +210,10 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
  * block_table[b][(ctx-1)/bs]*bs + (ctx-1)%bs, and take part in the attention
  * of that same call.  Bit-identical cache contents to kv_append with those
  * slots followed by paged_decode_attention.
- * k_next/v_next (both NULL, or both set): the pools of the layer the caller
- * runs next ([num_blocks][Hkv][bs][D], same block tables).  The blocks this
- * call reads are also requested from them into L2 (a prefetch hint, no
- * effect on any result), so that the next layer's call finds its K/V in L2
- * while HBM streams without a gap between layers. */
+ * k_next/v_next (both NULL, or both set, 16-byte aligned): the pools of the
+ * layer the caller runs next.  Accepted for a prefetch of the next layer's
+ * blocks into L2; that prefetch measured no gain on GB300 and is not issued,
+ * so the arguments have no effect. */
 kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
                                          void* v_cache, const void* k_next, const void* v_next, int num_blocks,
                                          const int32_t* block_table, int max_blocks, const int32_t* context_lens,

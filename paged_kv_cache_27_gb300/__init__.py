@@ -471,7 +471,8 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
                                   k_next: Optional[torch.Tensor] = None, v_next: Optional[torch.Tensor] = None) -> None:
     """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel).
 
-    k_next/v_next: the next layer's pools (same shape as k_cache); this call's blocks of them are prefetched to L2."""
+    k_next/v_next: the next layer's pools (same shape as k_cache); accepted and unused (the L2 prefetch they were
+    for measured no gain)."""
     if (k_next is None) != (v_next is None):
         raise ValueError("k_next and v_next: both or neither")
     if k_next is not None and (k_next.shape != k_cache.shape or v_next.shape != k_cache.shape):

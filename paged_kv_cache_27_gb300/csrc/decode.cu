@@ -53,7 +53,7 @@ struct DecodeKernelParams {
     const __half* v_new;
     __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
     __half* v_cache;
-    const __half* k_next;  // optional: the next layer's pools, whose blocks of this CTA are prefetched to L2
+    const __half* k_next;  // the next layer's pools (accepted, unused: the L2 prefetch measured no gain)
     const __half* v_next;
     const int32_t* block_table;
     const int32_t* context_lens;

@@ -42,23 +42,27 @@ namespace kvc {
 #ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
 #define KVC_DEC_PLAN_CTAS 2
 #endif
-#ifndef KVC_DEC_PREFETCH_AT  // when the next layer's blocks are requested into L2: 0 at start, 1 after the main loop
-#define KVC_DEC_PREFETCH_AT 1
-#endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
 constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
 
-template <int D>
+// Tile configuration per head dim. With kFp8 the cache holds e4m3 codes and a float scale per (token, KV
+// head) row: a stage is the block's K codes, V codes, K scales and V scales, and every warp also owns a
+// scratch pair of fp16 tiles (the codes converted, in the 128-byte swizzle the fp16 stages have).
+template <int D, bool kFp8 = false>
 struct DecodeCfg {
     static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
     static constexpr int kStages = D == 64 ? KVC_DEC_STAGES64 : KVC_DEC_STAGES128;
     static constexpr int kThreads = kWarps * 32;
-    static constexpr int kTileBytes = kBlockSize * D * 2;  // one 16 x D fp16 tile
-    static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
-    static constexpr int kWarpRingBytes = kStages * kStageBytes;
+    static constexpr int kTileBytes = kBlockSize * D * 2;    // one 16 x D fp16 tile
+    static constexpr int kCodeTileBytes = kBlockSize * D;    // one 16 x D e4m3 tile
+    static constexpr int kScaleBytes = kBlockSize * 4;       // 16 float scales
+    static constexpr int kStageBytes = kFp8 ? 2 * kCodeTileBytes + 2 * kScaleBytes  // K, V codes; K, V scales
+                                            : 2 * kTileBytes;                           // K tile + V tile
+    static constexpr int kScratchOff = kFp8 ? (kStages * kStageBytes + 127) / 128 * 128 : 0;
+    static constexpr int kWarpRingBytes = kFp8 ? kScratchOff + 2 * kTileBytes : kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
     static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA

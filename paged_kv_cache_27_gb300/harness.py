@@ -33,10 +33,8 @@ def poisoned_pool(shape, device) -> torch.Tensor:
 class DecodeSession:
     """A paged cache holding a DecodeWorkload's history, ready for decode steps on every layer."""
 
-    def __init__(self, wl, device="cuda", out_dtype=torch.float32, blocks_per_split=0, poison=True,
-                 prefetch_next=True):
+    def __init__(self, wl, device="cuda", out_dtype=torch.float32, blocks_per_split=0, poison=True):
         self.wl = wl
-        self.prefetch_next = prefetch_next
         self.device = device
         cfg = KvcConfig(num_layers=wl.L, num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_dim=wl.D, block_size=wl.bs)
         self.cfg = cfg
@@ -78,15 +76,11 @@ class DecodeSession:
                                self.blocks_per_split, stream=stream)
 
     def decode_append(self, layer, stream=None):
-        """Fused append + decode of one layer; with prefetch_next the next layer's (cyclically) blocks go to L2."""
-        nxt = (layer + 1) % self.wl.L
-        pf = self.prefetch_next and self.wl.L > 1
-        k_next = self.k_pool[nxt] if pf else None
-        v_next = self.v_pool[nxt] if pf else None
+        """Fused append + decode of one layer."""
         paged_decode_append_attention(self.q[layer], self.k_new[layer], self.v_new[layer], self.k_pool[layer],
                                       self.v_pool[layer], self.block_table, self.context_lens, self.wl.scale,
                                       self.out[layer], self.workspace, self.max_ctx, self.blocks_per_split,
-                                      stream=stream, k_next=k_next, v_next=v_next)
+                                      stream=stream)
 
     def step(self, stream=None, fused=False):
         """One decode step: for every layer, append the new token's K/V, then attend.
