@@ -288,6 +288,35 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
                                         int max_context_len, float scale, void* out, int out_dtype, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
+/* Quantized (fp8) KV cache — an extension: the pages quantize weights, not
+ * the KV cache, and fix no quantized format.  A layer's cache is e4m3 codes
+ * (1 sign, 4 exponent bits with bias 7, 3 fraction bits; largest 448)
+ * k_codes / v_codes [NB][Hkv][bs][D] (1 byte each) and one float scale per
+ * (slot, KV head) row, k_scales / v_scales [NB][Hkv][bs]; a cached value is
+ * code value * scale.  Per-row scales mean that appending a token never
+ * re-quantizes the rest of its block.  The bytes per token are 53 % of the
+ * fp16 cache's (D = 64).
+ *
+ * kv_append_fp8: quantize k_new / v_new (device fp16 [n][Hkv][D]) and write
+ * them to their slots: scale = absmax / 448 of the row (IEEE division; 1 for
+ * an all-zero row), code = e4m3(x / scale) rounded to nearest even.  Slots as
+ * in kv_append (negative = skip, >= NB*bs sets KVC_DEVERR_SLOT).  All device
+ * pointers 16-byte aligned. */
+kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n, void* k_codes,
+                         void* v_codes, float* k_scales, float* v_scales, int num_blocks, int Hkv, int head_dim,
+                         int block_size, void* stream);
+/* paged_decode_attention over an fp8 cache: the same result definition with
+ * every cached value code value * scale; workspace as paged_decode_plan's.
+ * Codes convert to fp16 exactly; the K scale multiplies the scores and the
+ * V scale the probabilities in fp32, so the arithmetic matches the fp16
+ * kernel's. */
+kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                                      const float* v_scales, int num_blocks, const int32_t* block_table,
+                                      int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv,
+                                      int head_dim, int block_size, int max_context_len, float scale, void* out,
+                                      int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
+                                      void* stream);
+
 /* Launch overlap (process-wide, default off).  When on, decode kernels are
  * launched as programmatic dependents of the kernel before them on the
  * stream: they read block tables, context lengths and the cached K/V

@@ -30,7 +30,7 @@ __all__ = [
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
     "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
-    "paged_decode_multi_plan", "paged_decode_multi_attention",
+    "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
     "prefill_attention", "DEVERR",
 ]
 
@@ -114,6 +114,9 @@ def _load():
         "paged_decode_cascade_plan": (I, [I, I, I, I, I, I, I, I, PSZ]),
         "kv_cascade_groups": (I, [P, I, I, P, I, I, P, PI, P, PI]),
         "paged_decode_multi_plan": (I, [I, I, I, I, I, I, I, PSZ]),
+        "kv_append_fp8": (I, [P, P, P, I, P, P, P, P, I, I, I, I, P]),
+        "paged_decode_attention_fp8": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ,
+                                           I, P]),
         "paged_decode_multi_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ,
                                              P]),
         "paged_decode_cascade_attention": (I, [P, P, P, I, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P,
@@ -462,6 +465,50 @@ def paged_decode_multi_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache
         block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), T, B, Hq, Hkv, D, bs,
         int(max_context_len), float(scale), _dptr(out, None, "out"), od, _dptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream, q)), "paged_decode_multi_attention")
+
+
+def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
+                  v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor, stream=None) -> None:
+    """Quantize k_new / v_new (fp16 [n][Hkv][D]) into an fp8 cache layer: codes uint8 [NB][Hkv][bs][D], scales
+    float32 [NB][Hkv][bs] (one per row; value = e4m3 code value * scale); slot_mapping int64 [n]."""
+    n, Hkv, D = k_new.shape
+    NB, Hkv2, bs, D2 = k_codes.shape
+    if (Hkv2, D2) != (Hkv, D) or v_codes.shape != k_codes.shape or k_scales.shape != (NB, Hkv, bs) or \
+            v_scales.shape != k_scales.shape or v_new.shape != k_new.shape or slot_mapping.numel() != n:
+        raise ValueError("fp8 cache shapes do not match")
+    _check(_lib.kv_append_fp8(
+        _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
+        _dptr(slot_mapping, torch.int64, "slot_mapping"), n, _dptr(k_codes, torch.uint8, "k_codes"),
+        _dptr(v_codes, torch.uint8, "v_codes"), _dptr(k_scales, torch.float32, "k_scales"),
+        _dptr(v_scales, torch.float32, "v_scales"), NB, Hkv, D, bs, _stream(stream, k_new)), "kv_append_fp8")
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
+                               k_scales: torch.Tensor, v_scales: torch.Tensor, block_table: torch.Tensor,
+                               context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                               workspace: Optional[torch.Tensor], max_context_len: int, blocks_per_split: int = 0,
+                               stream=None) -> None:
+    """paged_decode_attention over an fp8 cache layer (codes uint8 [NB][Hkv][bs][D], scales float32 [NB][Hkv][bs])."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, Dk = k_codes.shape
+    if Dk != D or v_codes.shape != k_codes.shape or k_scales.shape != (NB, Hkv, bs) or v_scales.shape != k_scales.shape:
+        raise ValueError("fp8 cache shapes do not match q")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_table / context_lens do not match B")
+    od = {torch.float16: KVC_F16, torch.float32: KVC_F32}.get(out.dtype)
+    if od is None:
+        raise TypeError("out must be float16 or float32")
+    ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.paged_decode_attention_fp8(
+        _dptr(q, torch.float16, "q"), _dptr(k_codes, torch.uint8, "k_codes"), _dptr(v_codes, torch.uint8, "v_codes"),
+        _dptr(k_scales, torch.float32, "k_scales"), _dptr(v_scales, torch.float32, "v_scales"), NB,
+        _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
+        _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),
+        "paged_decode_attention_fp8")
 
 
 def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,

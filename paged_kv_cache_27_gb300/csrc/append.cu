@@ -15,6 +15,7 @@
 
 #include "../../include/kvc.h"
 #include "kvc_internal.h"
+#include "ptx.cuh"
 
 namespace kvc {
 
@@ -76,6 +77,81 @@ cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_
     kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new), slots, n,
         reinterpret_cast<uint4*>(k_layer), reinterpret_cast<uint4*>(v_layer), num_blocks, Hkv, cpr, err);
+    return cudaGetLastError();
+}
+
+// Quantized cache (an extension; the pages fix no quantized format): rows of D fp16 values become e4m3 codes
+// with one float scale per (token, KV head) row, so that appending a token never re-quantizes the rest of its
+// block. One warp per (token, KV head, K or V) row: scale = absmax / 448 with IEEE division (1 for an all-zero
+// row), code_i = e4m3(x_i / scale) rounded to nearest even, saturating at 448. Codes go to the slot's row of
+// k_codes / v_codes [NB][Hkv][16][D], the scale to k_scales / v_scales [NB][Hkv][16].
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __half* __restrict__ k_new,
+                                                            const __half* __restrict__ v_new,
+                                                            const int64_t* __restrict__ slots, int n,
+                                                            uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                                                            float* __restrict__ k_scales, float* __restrict__ v_scales,
+                                                            int num_blocks, int Hkv, unsigned* err) {
+    constexpr int PER = D / 32;  // values per lane
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= static_cast<int64_t>(n) * Hkv * 2) return;  // whole warps
+    const int kv = static_cast<int>(w & 1);
+    const int64_t row = w >> 1;  // t * Hkv + h
+    const int h = static_cast<int>(row % Hkv);
+    const int64_t slot = slots[row / Hkv];
+    if (slot < 0) return;
+    if (slot >= static_cast<int64_t>(num_blocks) * kBlockSize) {
+        if (lane == 0 && kv == 0) atomicOr(err, KVC_DEVERR_SLOT);
+        return;
+    }
+    const __half* src = (kv ? v_new : k_new) + row * D + lane * PER;
+    float x[PER];
+    if constexpr (PER == 2) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(src));
+        x[0] = f.x;
+        x[1] = f.y;
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = c.x;
+        x[3] = c.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const int64_t dst_row = ((slot / kBlockSize) * Hkv + h) * kBlockSize + slot % kBlockSize;
+    uint8_t* dst = (kv ? v_codes : k_codes) + dst_row * D + lane * PER;
+    const uint32_t c01 = float2_to_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
+    if constexpr (PER == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c01);
+    } else {
+        const uint32_t c23 = float2_to_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc));
+        *reinterpret_cast<uint32_t*>(dst) = c01 | (c23 << 16);
+    }
+    if (lane == 0) (kv ? v_scales : k_scales)[dst_row] = sc;
+}
+
+cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const int64_t* slots, int n,
+                              uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales, int num_blocks,
+                              int Hkv, int D, unsigned* err, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t warps = static_cast<int64_t>(n) * Hkv * 2;
+    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+    if (D == 64)
+        kv_append_fp8_kernel<64><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, k_codes, v_codes, k_scales,
+                                                             v_scales, num_blocks, Hkv, err);
+    else if (D == 128)
+        kv_append_fp8_kernel<128><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, k_codes, v_codes, k_scales,
+                                                              v_scales, num_blocks, Hkv, err);
+    else
+        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

@@ -68,6 +68,8 @@ struct DecodeKernelParams {
     // part_base + c of part_ml / part_acc
     int part_base, part_stride;
     const int32_t* blk_off;  // suffix pass: per sequence, the leading blocks of its table row attended elsewhere
+    const float* k_scales;   // fp8 cache: per (slot, KV head) row scales of the codes, [NB][Hkv][16]
+    const float* v_scales;
     int out_f32;
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
@@ -137,11 +139,14 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 // kSuffix: the cascade's suffix pass (per-sequence block offset, partial states only); the plain decode
 // is compiled without either
-template <int D, bool kSuffix>
-__global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
+// kFp8: the cache holds e4m3 codes with per-row scales (tmK / tmV map the codes); each block's codes are
+// converted to fp16 (exact) in the warp's scratch, the K scale multiplies the scores and the V scale the
+// probabilities before the P V product, so the arithmetic is the fp16 path's
+template <int D, bool kSuffix, bool kFp8 = false>
+__global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeKernelParams p) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, kFp8>;
     constexpr int NW = C::kWarps, ST = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -230,10 +235,17 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
         uint8_t* st = wring + s * C::kStageBytes;
         mbar_arrive_expect_tx(bar, C::kStageBytes);
         const int y = (phys * p.Hkv + kvh) * kBlockSize;
+        if constexpr (kFp8) {  // K codes, V codes (16 rows x D bytes each), then the 16 K and 16 V scales
+            tma_load_2d(st, &tmK, bar, 0, y, policy);
+            tma_load_2d(st + C::kCodeTileBytes, &tmV, bar, 0, y, policy);
+            bulk_load(st + 2 * C::kCodeTileBytes, p.k_scales + y, C::kScaleBytes, bar);
+            bulk_load(st + 2 * C::kCodeTileBytes + C::kScaleBytes, p.v_scales + y, C::kScaleBytes, bar);
+        } else {
 #pragma unroll
-        for (int x = 0; x < D; x += 64) {
-            tma_load_2d(st + (x / 64) * 2048, &tmK, bar, x, y, policy);
-            tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
+            for (int x = 0; x < D; x += 64) {
+                tma_load_2d(st + (x / 64) * 2048, &tmK, bar, x, y, policy);
+                tma_load_2d(st + C::kTileBytes + (x / 64) * 2048, &tmV, bar, x, y, policy);
+            }
         }
     };
     // lane 0 issues the warp's static first round (stage s gets block cb0 + gw + s * warps-in-the-
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
     }
     // fused append: any warp of the last cluster may get the block of position ctx-1; each holds the
     // new row (lanes 0-15: K chunks, 16-31: V chunks) to write it to the cache and patch its tile
-    const int app_blk = p.k_new != nullptr && cidx == nclus - 1 ? nblk - 1 : -1;
+    const int app_blk = !kFp8 && p.k_new != nullptr && cidx == nclus - 1 ? nblk - 1 : -1;
     const int app_row = (ctx - 1) % kBlockSize;
     uint4 app_val = make_uint4(0, 0, 0, 0);
     if (app_blk >= 0 && (lane & 15) < D / 8) {
@@ -327,8 +339,56 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
             }
             const int phys = s_table[jj - cb0];
             if (phys >= 0 && phys < p.num_blocks) {
-                const uint32_t kbase = smem_u32(wring + s * C::kStageBytes);
-                const uint32_t vbase = kbase + C::kTileBytes;
+                const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
+                uint32_t kbase, vbase;
+                // scores of tokens g and g+8 carry sl2 (times their K scales with an fp8 cache); the V scales
+                // of tokens g and g+8 (0 past the context) multiply their probabilities before P V
+                float sl2g = sl2, sl2g8 = sl2, vsg = 1.f, vsg8 = 1.f;
+                if constexpr (kFp8) {
+                    const uint8_t* stg = wring + s * C::kStageBytes;
+                    const float* sk = reinterpret_cast<const float*>(stg + 2 * C::kCodeTileBytes);
+                    const float* sv = sk + kBlockSize;
+                    sl2g = sl2 * sk[g];
+                    sl2g8 = sl2 * sk[g + 8];
+                    vsg = g < rem ? sv[g] : 0.f;
+                    vsg8 = g + 8 < rem ? sv[g + 8] : 0.f;
+                    // lane: row lane / 2, half lane % 2 of the K and V code tiles -> fp16 in the swizzle
+                    uint8_t* scr = wring + C::kScratchOff;
+                    const int r = lane >> 1, hf = lane & 1;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint8_t* src = stg + t * C::kCodeTileBytes + r * D + hf * (D / 2);
+                        const uint32_t dst = smem_u32(scr + t * C::kTileBytes);
+#pragma unroll
+                        for (int qq = 0; qq < D / 32; ++qq) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * qq);
+                            const int c0 = hf * (D / 16) + 2 * qq;
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(r, c0)),
+                                         "r"(e4m3x2_to_half2(w.x)), "r"(e4m3x2_to_half2(w.x >> 16)),
+                                         "r"(e4m3x2_to_half2(w.y)), "r"(e4m3x2_to_half2(w.y >> 16))
+                                         : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(r, c0 + 1)),
+                                         "r"(e4m3x2_to_half2(w.z)), "r"(e4m3x2_to_half2(w.z >> 16)),
+                                         "r"(e4m3x2_to_half2(w.w)), "r"(e4m3x2_to_half2(w.w >> 16))
+                                         : "memory");
+                        }
+                    }
+                    {
+                        // the stage may be refilled once its scales have been read too
+                        uint32_t dep = 0;
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g8)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg8)));
+                    }
+                    refill(s);  // the stage's codes and scales are read: its next block goes out now
+                    refilled = true;
+                    kbase = smem_u32(scr);
+                    vbase = kbase + C::kTileBytes;
+                } else {
+                    kbase = smem_u32(wring + s * C::kStageBytes);
+                    vbase = kbase + C::kTileBytes;
+                }
                 if (jj == app_blk) {
                     const int c = lane & 15;
                     if (c < D / 8) {
@@ -351,7 +411,6 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                     ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                     mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
                 }
-                const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
                 // rows of V past the context may hold any bits (even NaN): zero them in registers
                 uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
                 if (rem < kBlockSize) {
@@ -370,7 +429,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                     va[mt][2] &= keep1;
                     va[mt][3] &= keep1;
                 }
-                {
+                if constexpr (!kFp8) {
                     // the copy may overwrite the stage only once the warp's reads of it have returned: fold
                     // the loaded registers (the K fragments were consumed by the S products above)
                     uint32_t dep = 0;
@@ -378,16 +437,16 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                     for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
+                    refill(s);
+                    refilled = true;
                 }
-                refill(s);
-                refilled = true;
 #endif
                 // ---- online softmax per head (column): this lane holds tokens g, g+8 of heads 2*t4, 2*t4+1 ----
                 float x[4];
-                x[0] = g < rem ? sc[0] * sl2 : -INFINITY;
-                x[1] = g < rem ? sc[1] * sl2 : -INFINITY;
-                x[2] = g + 8 < rem ? sc[2] * sl2 : -INFINITY;
-                x[3] = g + 8 < rem ? sc[3] * sl2 : -INFINITY;
+                x[0] = g < rem ? sc[0] * sl2g : -INFINITY;
+                x[1] = g < rem ? sc[1] * sl2g : -INFINITY;
+                x[2] = g + 8 < rem ? sc[2] * sl2g8 : -INFINITY;
+                x[3] = g + 8 < rem ? sc[3] * sl2g8 : -INFINITY;
                 float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
@@ -410,11 +469,12 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads, KVC_DEC_MIN_CTAS)
                 }
                 // P^T as the B operand (k = tokens, n = heads): transpose the two 8x8 halves in registers;
                 // P = hi + lo, both fp16, so the P V product keeps ~fp32 accuracy
-                const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
+                const float q0 = p0 * vsg, q1 = p1 * vsg, q2 = p2 * vsg8, q3 = p3 * vsg8;
+                const uint32_t h01 = pack_half2(q0, q1), h23 = pack_half2(q2, q3);
                 const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
                 const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-                const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
-                const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+                const uint32_t bl0 = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
+                const uint32_t bl1 = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
                 // ---- O^T += V^T P^T, one m-tile per 16 dims ----
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
@@ -659,6 +719,12 @@ static cudaError_t decode_setup() {
             if (err == cudaSuccess && kMaxCluster > 8)
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         }
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(paged_decode_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DecodeCfg<D, true>::smem_bytes(kMaxCluster, 8));
+        if (err == cudaSuccess && kMaxCluster > 8)
+            err = cudaFuncSetAttribute(paged_decode_kernel<D, false, true>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     return err;
 }
@@ -772,6 +838,8 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.part_base = 0;
     p.part_stride = plan.num_parts;
     p.blk_off = nullptr;
+    p.k_scales = a.k_scales;
+    p.v_scales = a.v_scales;
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kLog2e;
     static std::atomic<unsigned> launch_seq{0};
@@ -785,10 +853,11 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     cudaError_t e = decode_setup<D>();
     if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
+    const bool fp8 = a.k_codes != nullptr;
     CUtensorMap tmK, tmV;
-    e = make_tile_map(&tmK, a.k_cache, D, rows);
+    e = fp8 ? make_code_map(&tmK, a.k_codes, D, rows) : make_tile_map(&tmK, a.k_cache, D, rows);
     if (e != cudaSuccess) return e;
-    e = make_tile_map(&tmV, a.v_cache, D, rows);
+    e = fp8 ? make_code_map(&tmV, a.v_codes, D, rows) : make_tile_map(&tmV, a.v_cache, D, rows);
     if (e != cudaSuccess) return e;
 
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
@@ -796,8 +865,13 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     const DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv, a.B);
-    e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream, pdl,
-               static_cast<unsigned>(plan.cluster), tmK, tmV, p);
+    if (fp8)
+        e = launch(paged_decode_kernel<D, false, true>, grid, dim3(DecodeCfg<D, true>::kThreads),
+                   DecodeCfg<D, true>::smem_bytes(plan.cluster, p.G), stream, pdl, static_cast<unsigned>(plan.cluster),
+                   tmK, tmV, p);
+    else
+        e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream,
+                   pdl, static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
         CombineParams c;

@@ -151,6 +151,21 @@ inline cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D view of one layer's e4m3 code pool: rows of D bytes, boxes of 16 rows x D bytes, no swizzle (the codes
+// are converted into swizzled fp16 tiles in shared memory).
+inline cudaError_t make_code_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(D)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename Kern, typename... Args>
 inline cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
                           unsigned cluster_x, Args... args) {

@@ -16,6 +16,10 @@ cudaError_t device_error_word(unsigned** ptr);
 // ---- append / block copy (append.cu) ---------------------------------------
 cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_t* slots, int n, __half* k_layer,
                           __half* v_layer, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream);
+// quantizing append: e4m3 codes [NB][Hkv][16][D] and one float scale per (slot, KV head) row
+cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const int64_t* slots, int n,
+                              uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales, int num_blocks,
+                              int Hkv, int D, unsigned* err, cudaStream_t stream);
 // copies whole blocks src[i] -> dst[i] for every layer (pools [L][NB][block_elems])
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __half* k_pool, __half* v_pool,
                                int L, int num_blocks, int64_t block_elems, cudaStream_t stream);
@@ -51,6 +55,12 @@ struct DecodeArgs {
     size_t workspace_bytes;
     int blocks_per_split;  // blocks per cluster, 0 = automatic
     unsigned* err;
+    // fp8 cache instead of k_cache / v_cache when k_codes is set: e4m3 codes [NB][Hkv][16][D] and per-row
+    // float scales [NB][Hkv][16]
+    const uint8_t* k_codes = nullptr;
+    const uint8_t* v_codes = nullptr;
+    const float* k_scales = nullptr;
+    const float* v_scales = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

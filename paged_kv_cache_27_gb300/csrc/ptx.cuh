@@ -1,6 +1,6 @@
-// Inline-PTX helpers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// ldmatrix, warp-level mma, ex2.  Everything here is a thin wrapper around
-// one documented PTX instruction.
+// Inline-PTX helpers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor) and
+// bulk copies, ldmatrix, warp-level mma, ex2, fp8 conversions.  Everything
+// here is a thin wrapper around one documented PTX instruction.
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -72,6 +72,14 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to shared memory,
+// completion counted on the mbarrier in bytes.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 // Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned address) from global memory into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
@@ -117,6 +125,20 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Two e4m3 codes (low byte first) -> f16x2 (low half first); exact, every e4m3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t h = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+// Two floats -> two e4m3 codes, round to nearest even, saturating at +-448 (lo in the low byte).
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
