@@ -21,6 +21,12 @@ namespace kvc {
 #ifndef KVC_DEC_STAGES64
 #define KVC_DEC_STAGES64 2
 #endif
+#ifndef KVC_DEC_STAGES64_FP8  // stages per warp with an fp8 cache (a stage is half the bytes)
+#define KVC_DEC_STAGES64_FP8 2
+#endif
+#ifndef KVC_DEC_STAGES128_FP8
+#define KVC_DEC_STAGES128_FP8 2
+#endif
 #ifndef KVC_DEC_WARPS128
 #define KVC_DEC_WARPS128 4
 #endif
@@ -54,7 +60,8 @@ constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (i
 template <int D, bool kFp8 = false>
 struct DecodeCfg {
     static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
-    static constexpr int kStages = D == 64 ? KVC_DEC_STAGES64 : KVC_DEC_STAGES128;
+    static constexpr int kStages = kFp8 ? (D == 64 ? KVC_DEC_STAGES64_FP8 : KVC_DEC_STAGES128_FP8)
+                                        : (D == 64 ? KVC_DEC_STAGES64 : KVC_DEC_STAGES128);
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kTileBytes = kBlockSize * D * 2;    // one 16 x D fp16 tile
     static constexpr int kCodeTileBytes = kBlockSize * D;    // one 16 x D e4m3 tile
