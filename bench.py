@@ -59,7 +59,7 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "883db2c17a074a6a85cb83e8418d9ab34a45fa9d12630a175d1025e718bbac9d",
+NCU_DECODE_TRAFFIC = {"sources_sha256": "29d80145cbd6e9ab39a6d02fc735964a9f4cf817ce24dc703145bc75850d4803",
                       "bytes_per_launch": 33674624 + 0}
 
 
