@@ -7,21 +7,21 @@
 // KV head h / (Hq / Hkv).  Per row: softmax(q K^T * scale) V, with the
 // running-max / exp-sum rule of the FlashAttention article over key tiles.
 //
-// Design: one CTA per (128-row query tile of a segment, query head), five
-// warps.  Lane 0 of warp 4 issues every TMA copy and every tcgen05.mma;
-// warps 0-3 own the 128 query rows (thread = row = TMEM lane) and run the
-// softmax.  Per 64-key tile j:
-//   S = Q K^T   tcgen05.mma M=128 x N=64, Q and K K-major in shared memory
-//               (128-byte swizzle, as TMA writes them), fp32 accumulator in TMEM
-//   softmax     the row threads read S from TMEM, mask (segment end, causal),
-//               keep the running max until it has grown by 2^8 (then rescale
-//               O in TMEM), and write P = hi + lo (two fp16 parts, so the
-//               product keeps ~fp32 accuracy) to shared memory, K-major
-//   O += P V    tcgen05.mma M=128 x N=64 per 64-dim chunk, V MN-major; O stays
-//               in TMEM across tiles
-// K and V have two-stage rings of their own; S(j+1) is issued as soon as the
-// row threads have read S(j), so the tensor cores work on it during softmax(j).
-// Every wait is bounded; a timeout sets an error bit and drains the CTA.
+// Design: one CTA per (256 query rows of a segment, query head) = two 128-row query tiles A and B that
+// share every K/V tile; nine warps.  Lane 0 of warp 8 issues every TMA copy and every tcgen05.mma; warps
+// 0-3 own tile A's rows and warps 4-7 tile B's (thread = row = TMEM lane) and run the softmax.  Per
+// 64-key tile j and query tile X:
+//   S_X = Q_X K^T   tcgen05.mma M=128 x N=64, Q and K K-major in shared memory (128-byte swizzle, as
+//                   TMA writes them), fp32 accumulator in TMEM
+//   softmax         the row threads read S_X from TMEM, mask only on tiles that cross the causal diagonal
+//                   or the segment end, keep the running max until it has grown by 2^8 (then rescale O_X
+//                   in TMEM), and write P_X = hi + lo (two fp16 parts, so the product keeps ~fp32
+//                   accuracy) to shared memory, K-major
+//   O_X += P_X V    tcgen05.mma M=128 x N=64 per 64-dim chunk, V MN-major; O_X stays in TMEM
+// The products go out in the order S_A(j+1), S_B(j+1), P_A V(j), P_B V(j): while one group of row warps
+// runs its softmax, the tensor cores work on the other group's products, and each group's S(j+1) runs
+// during its own softmax(j).  K and V have three-stage rings of their own.  Every wait is bounded; a
+// timeout sets an error bit and drains the CTA.
 #include <algorithm>
 #include <cmath>
 #include <cudaTypedefs.h>
@@ -34,9 +34,11 @@
 
 namespace kvc {
 
-constexpr int kPfRows = 128;  // query rows per CTA: the MMA's M, one TMEM lane each
-constexpr int kPfKeys = 64;   // keys per K/V tile: N of S, K of P V
-constexpr int kPfRowWarps = 4;
+constexpr int kPfRows = 128;   // rows of one query tile: the MMA's M, one TMEM lane each
+constexpr int kPfQTiles = 2;   // query tiles per CTA, A and B
+constexpr int kPfCtaRows = kPfRows * kPfQTiles;
+constexpr int kPfKeys = 128;   // keys per K/V tile: N of S, K of P V
+constexpr int kPfRowWarps = 4 * kPfQTiles;
 constexpr int kPfThreads = (kPfRowWarps + 1) * 32;
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 constexpr float kPfLog2e = 1.4426950408889634f;
@@ -45,21 +47,24 @@ constexpr float kPfRescaleLog2 = 8.f;  // P stays below 2^8, far inside fp16
 template <int D>
 struct PfGeom {
     static constexpr int kChunks = D / 64;                    // 64-dim (128-byte) column chunks
+    static constexpr int kKStages = D == 64 ? 4 : 3;          // K ring depth
+    static constexpr int kVStages = D == 64 ? 4 : 2;          // V ring depth
     static constexpr int kQChunk = kPfRows * 128;             // 16 KiB
-    static constexpr int kKVChunk = kPfKeys * 128;            // 8 KiB
-    static constexpr int kQBytes = kChunks * kQChunk;
+    static constexpr int kKVChunk = kPfKeys * 128;            // 16 KiB
+    static constexpr int kQBytes = kChunks * kQChunk;         // one query tile
     static constexpr int kKVBytes = kChunks * kKVChunk;       // one K or V tile
-    static constexpr int kPBytes = kPfRows * kPfKeys * 2;     // 16 KiB
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kQBytes;             // 2 stages
-    static constexpr int kVOff = kKOff + 2 * kKVBytes;        // 2 stages
-    static constexpr int kPhiOff = kVOff + 2 * kKVBytes;
-    static constexpr int kPloOff = kPhiOff + kPBytes;
-    static constexpr int kBarOff = kPloOff + kPBytes;
-    static constexpr int kSmemBytes = kBarOff + 128 + 1024;  // barriers, TMEM address, abort flag; alignment
-    static constexpr int kTmemS = 0;                          // S: columns [0, 64)
-    static constexpr int kTmemO = kPfKeys;                    // O: columns [64, 64 + D)
-    static constexpr uint32_t kTmemCols = kPfKeys + D <= 128 ? 128 : 256;
+    static constexpr int kQOff = 0;                           // Q_A, Q_B
+    static constexpr int kKOff = kQOff + kPfQTiles * kQBytes;
+    static constexpr int kVOff = kKOff + kKStages * kKVBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kKVBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers, TMEM address, abort flag; alignment
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+    // TMEM columns: S_A / P_A [0, 128), S_B / P_B [128, 256), O_A [256, 256 + D), O_B [256 + D, 256 + 2D).
+    // P_X is written over S_X once the row warps have read S_X: per 64-key half h, the high fp16 parts in
+    // columns [64h, 64h + 32) and the residuals in [64h + 32, 64h + 64), two keys per column.
+    static constexpr int kTmemO = kPfQTiles * kPfKeys;
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kTmemO + kPfQTiles * D <= 512, "tensor memory");
 };
 
 struct PrefillKernelParams {
@@ -85,6 +90,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Wait for a phase; gives up when another thread of the CTA has given up (abort flag) or after the limit,
 // in which case it raises the flag itself.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -100,31 +116,41 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile
     }
 }
 
+// number of key tiles query tile X (first row rx) reads; 0 when it has no row in the segment
+__device__ __forceinline__ int pf_key_tiles(int rx, int len, int causal) {
+    if (rx >= len) return 0;
+    const int kv_len = causal ? min(len, rx + kPfRows) : len;
+    return (kv_len + kPfKeys - 1) / kPfKeys;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                             const __grid_constant__ CUtensorMap tmK,
-                                                             const __grid_constant__ CUtensorMap tmV,
-                                                             const PrefillKernelParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                const __grid_constant__ CUtensorMap tmK,
+                                                                const __grid_constant__ CUtensorMap tmV,
+                                                                const PrefillKernelParams p) {
     using Geo = PfGeom<D>;
+    constexpr int KS = Geo::kKStages, VS = Geo::kVStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Geo::kBarOff);
     uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;   // [2] K tile landed
-    uint64_t* v_full = bars + 3;   // [2] V tile landed
-    uint64_t* k_empty = bars + 5;  // [2] S products of the stage's tile done
-    uint64_t* v_empty = bars + 7;  // [2] P V products of the stage's tile done
-    uint64_t* s_full = bars + 9;   // S of the current tile in TMEM
-    uint64_t* s_free = bars + 10;  // the row warps have read S (4 arrivals)
-    uint64_t* p_full = bars + 11;  // P of the current tile in shared memory (4 arrivals)
-    uint64_t* o_full = bars + 12;  // P V of the current tile done
-    uint64_t* fin = bars + 13;     // every MMA issued so far done
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 14);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 14) + 1;
+    uint64_t* k_full = bars + 1;        // [KS] K tile landed
+    uint64_t* k_empty = bars + 1 + KS;  // [KS] S products of the stage's tile done
+    uint64_t* v_full = bars + 1 + 2 * KS;        // [VS] V tile landed
+    uint64_t* v_empty = bars + 1 + 2 * KS + VS;  // [VS] P V products of the stage's tile done
+    uint64_t* s_full = bars + 1 + 2 * KS + 2 * VS;  // [2] S_X of the current key tile in TMEM
+    uint64_t* p_full = s_full + 2;                  // [2] P_X of the current key tile in TMEM (4 arrivals)
+    uint64_t* o_full = s_full + 4;                  // [2] P_X V of the current key tile done
+    uint64_t* fin = s_full + 6;                     // every MMA issued so far done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_full + 7);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_full + 7) + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int seg = blockIdx.x / p.tiles_per_seq, tile = blockIdx.x % p.tiles_per_seq;
-    const int h = blockIdx.y, hk = h / p.G;
+    // heaviest causal row blocks first: block index = ((last row block - row block) * nseq + segment) * Hq + head
+    const int per_block = p.nseq * p.Hq;
+    const int tile = p.tiles_per_seq - 1 - static_cast<int>(blockIdx.x / per_block);
+    const int seg = static_cast<int>(blockIdx.x % per_block) / p.Hq, h = static_cast<int>(blockIdx.x % per_block) % p.Hq;
+    const int hk = h / p.G;
 
     const int beg = p.cu_seqlens[seg], end = p.cu_seqlens[seg + 1];
     const int len = end - beg;
@@ -132,31 +158,33 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
         if (threadIdx.x == 0 && tile == 0 && h == 0) atomicOr(p.err, KVC_DEVERR_SEQLENS);
         return;
     }
-    if (tile == 0 && h == 0 && threadIdx.x == 0 && len > p.tiles_per_seq * kPfRows)
+    if (tile == 0 && h == 0 && threadIdx.x == 0 && len > p.tiles_per_seq * kPfCtaRows)
         atomicOr(p.err, KVC_DEVERR_SEQLENS);  // rows past max_seqlen are not computed
-    const int r0 = tile * kPfRows;
+    const int r0 = tile * kPfCtaRows;
     if (r0 >= len) return;
-    const int kv_len = p.causal ? min(len, r0 + kPfRows) : len;
-    const int ntiles = (kv_len + kPfKeys - 1) / kPfKeys;
+    const int nt0 = pf_key_tiles(r0, len, p.causal), nt1 = pf_key_tiles(r0 + kPfRows, len, p.causal);
+    const int nq = nt1 > 0 ? 2 : 1;       // query tiles with rows in the segment
+    const int ntiles = max(nt0, nt1);     // key tiles of the CTA (tile B reads at least as many as A)
 
-    uint8_t* qs = smem + Geo::kQOff;
-    uint8_t* phi = smem + Geo::kPhiOff;
-    uint8_t* plo = smem + Geo::kPloOff;
+    auto qs = [&](int x) { return smem + Geo::kQOff + x * Geo::kQBytes; };
     auto kst = [&](int st) { return smem + Geo::kKOff + st * Geo::kKVBytes; };
     auto vst = [&](int st) { return smem + Geo::kVOff + st * Geo::kKVBytes; };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&v_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
+            mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, kPfRowWarps);
-        mbar_init(p_full, kPfRowWarps);
-        mbar_init(o_full, 1);
+        for (int x = 0; x < kPfQTiles; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 4);
+            mbar_init(&o_full[x], 1);
+        }
         mbar_init(fin, 1);
         *s_abort = 0;
         fence_barrier_init();
@@ -169,72 +197,71 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tS = tmem + Geo::kTmemS, tO = tmem + Geo::kTmemO;
 
     if (warp == kPfRowWarps) {
         // ================= producer: TMA copies and tensor-core products (one thread) =================
         if (lane == 0) {
             auto load_k = [&](int t) {
-                uint64_t* bar = &k_full[t & 1];
+                uint64_t* bar = &k_full[t % KS];
                 mbar_arrive_expect_tx(bar, Geo::kKVBytes);
 #pragma unroll
                 for (int c = 0; c < Geo::kChunks; ++c)
-                    tma_load_3d(kst(t & 1) + c * Geo::kKVChunk, &tmK, bar, c * 64, hk, beg + t * kPfKeys);
+                    tma_load_3d(kst(t % KS) + c * Geo::kKVChunk, &tmK, bar, c * 64, hk, beg + t * kPfKeys);
             };
             auto load_v = [&](int t) {
-                uint64_t* bar = &v_full[t & 1];
+                uint64_t* bar = &v_full[t % VS];
                 mbar_arrive_expect_tx(bar, Geo::kKVBytes);
 #pragma unroll
                 for (int c = 0; c < Geo::kChunks; ++c)
-                    tma_load_3d(vst(t & 1) + c * Geo::kKVChunk, &tmV, bar, c * 64, hk, beg + t * kPfKeys);
+                    tma_load_3d(vst(t % VS) + c * Geo::kKVChunk, &tmV, bar, c * 64, hk, beg + t * kPfKeys);
             };
             prefetch_tensormap(&tmQ);
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
-            mbar_arrive_expect_tx(q_full, Geo::kQBytes);
+            mbar_arrive_expect_tx(q_full, nq * Geo::kQBytes);
+            for (int x = 0; x < nq; ++x)
 #pragma unroll
-            for (int c = 0; c < Geo::kChunks; ++c)
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(qs + c * Geo::kQChunk + half * 64 * 128, &tmQ, q_full, c * 64, h, beg + r0 + half * 64);
+                for (int c = 0; c < Geo::kChunks; ++c)
+                    tma_load_3d(qs(x) + c * Geo::kQChunk, &tmQ, q_full, c * 64, h, beg + r0 + x * kPfRows);
             int k_issued = 0, v_issued = 0;  // tiles whose copies were issued
-            for (; k_issued < min(ntiles, 2); ++k_issued) load_k(k_issued);
-            for (; v_issued < min(ntiles, 2); ++v_issued) load_v(v_issued);
+            for (; k_issued < min(ntiles, KS); ++k_issued) load_k(k_issued);
+            for (; v_issued < min(ntiles, VS); ++v_issued) load_v(v_issued);
             int k_done = 0, v_done = 0;  // tiles whose copies were waited for
             bool q_done = false;
 
             constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, 0, 0);
-            constexpr uint32_t idPV = umma_idesc_f16(kPfRows, 64, 0, 1);
-            const uint32_t q_addr = smem_u32(qs);
-            // S(j) = Q K(j)^T over D / 16 steps of 16 dims
-            auto mma_s = [&](int j) {
-                const uint32_t k_addr = smem_u32(kst(j & 1));
+            constexpr uint32_t idPV = umma_idesc_f16(kPfRows, D, 0, 1);
+            // Descriptors are built once per operand; within a tile only the start-address field moves, by
+            // compile-time offsets (every shared-memory address is below 2^18, so the 14-bit field
+            // (address >> 4) never carries into the next field).
+            const uint64_t dQ = umma_smem_desc(smem_u32(qs(0)), 16, 1024);
+            const uint64_t dK = umma_smem_desc(smem_u32(kst(0)), 16, 1024);
+            // V as the MN-major B operand: 8-key groups 1024 bytes apart, 64-dim atoms one chunk apart
+            const uint64_t dV = umma_smem_desc(smem_u32(vst(0)), Geo::kKVChunk, 1024);
+            // S_X(j) = Q_X K(j)^T over D / 16 steps of 16 dims: M = 128 rows, N = 128 keys
+            auto mma_s = [&](int x, int st) {
+                const uint64_t a0 = dQ + static_cast<uint64_t>(x * (Geo::kQBytes >> 4));
+                const uint64_t b0 = dK + static_cast<uint64_t>(st * (Geo::kKVBytes >> 4));
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const int c = ks >> 2, kk = ks & 3;
-                    const uint64_t a = umma_smem_desc(q_addr + c * Geo::kQChunk + kk * 32, 16, 1024);
-                    const uint64_t b = umma_smem_desc(k_addr + c * Geo::kKVChunk + kk * 32, 16, 1024);
-                    umma_f16_ss(tS, a, b, idS, ks > 0);
+                    umma_f16_ss(tmem + x * kPfKeys, a0 + ((c * Geo::kQChunk + kk * 32) >> 4),
+                                b0 + ((c * Geo::kKVChunk + kk * 32) >> 4), idS, ks > 0);
                 }
-                umma_commit(s_full);
-                umma_commit(&k_empty[j & 1]);
+                umma_commit(&s_full[x]);
             };
-            // O += P(j) V(j): per 64-dim chunk, 4 steps of 16 keys, high and residual parts of P
-            auto mma_pv = [&](int j) {
-                const uint32_t v_addr = smem_u32(vst(j & 1));
+            // O_X += P_X(j) V(j): 8 steps of 16 keys, high and residual parts of P read from TMEM, N = D
+            auto mma_pv = [&](int x, int st, bool first) {
+                const uint64_t v0 = dV + static_cast<uint64_t>(st * (Geo::kKVBytes >> 4));
+                const uint32_t tP = tmem + x * kPfKeys, tO = tmem + Geo::kTmemO + x * D;
 #pragma unroll
-                for (int c = 0; c < Geo::kChunks; ++c)
-#pragma unroll
-                    for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-                        // V MN-major: 16 keys = two 8-row groups of 1024 bytes (one 64-dim atom wide)
-                        const uint64_t b = umma_smem_desc(v_addr + c * Geo::kKVChunk + kk * 2048, 1024, 1024);
-                        const uint64_t ah = umma_smem_desc(smem_u32(phi) + kk * 32, 16, 1024);
-                        const uint64_t al = umma_smem_desc(smem_u32(plo) + kk * 32, 16, 1024);
-                        umma_f16_ss(tO + c * 64, ah, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                        umma_f16_ss(tO + c * 64, al, b, idPV, 1u);
-                    }
-                umma_commit(o_full);
-                umma_commit(&v_empty[j & 1]);
+                for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+                    const uint64_t b = v0 + ((kk * 2048) >> 4);
+                    const uint32_t tPk = tP + (kk >> 2) * 64 + (kk & 3) * 8;  // hi; lo 32 columns on
+                    umma_f16_ts(tO, tPk, b, idPV, (!first || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tO, tPk + 32, b, idPV, 1u);
+                }
+                umma_commit(&o_full[x]);
             };
 
             bool ok = pf_wait(q_full, 0, s_abort);
@@ -243,33 +270,45 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
             if (ok) {
                 k_done = 1;
                 tc_fence_after();
-                mma_s(0);
+                for (int x = 0; x < nq; ++x) mma_s(x, 0);
+                umma_commit(&k_empty[0]);
             }
             for (int j = 0; ok && j < ntiles; ++j) {
-                // the K stage of tile j is free once S(j) is done: refill it with tile j + 2
-                if (j + 2 < ntiles) {
-                    if (!(ok = pf_wait(&k_empty[j & 1], (j >> 1) & 1, s_abort))) break;
-                    load_k(j + 2);
-                    k_issued = j + 3;
-                }
-                // S(j + 1) once its K tile has landed and the row warps have read S(j)
-                if (j + 1 < ntiles) {
-                    if (!(ok = pf_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, s_abort))) break;
-                    k_done = j + 2;
-                    if (!(ok = pf_wait(s_free, j & 1, s_abort))) break;
-                    tc_fence_after();
-                    mma_s(j + 1);
-                }
-                // P(j) V(j) once P(j) is written and V(j) has landed
-                if (!(ok = pf_wait(&v_full[j & 1], (j >> 1) & 1, s_abort))) break;
+                if (!(ok = pf_wait(&v_full[j % VS], (j / VS) & 1, s_abort))) break;
                 v_done = j + 1;
-                if (!(ok = pf_wait(p_full, j & 1, s_abort))) break;
-                tc_fence_after();
-                mma_pv(j);
-                if (j + 2 < ntiles) {
-                    if (!(ok = pf_wait(&v_empty[j & 1], (j >> 1) & 1, s_abort))) break;
-                    load_v(j + 2);
-                    v_issued = j + 3;
+                bool k_next = false;
+                // per query tile: P_X(j) V(j) once P_X(j) is in TMEM; then S_X(j + 1) into the same columns
+                // once that product has read P_X(j)
+                for (int x = 0; ok && x < nq; ++x) {
+                    const int ntx = x == 0 ? nt0 : nt1;
+                    if (j >= ntx) continue;
+                    if (!(ok = pf_wait(&p_full[x], j & 1, s_abort))) break;
+                    tc_fence_after();
+                    mma_pv(x, j % VS, j == 0);
+                    if (j + 1 < ntx) {
+                        if (!k_next) {
+                            if (!(ok = pf_wait(&k_full[(j + 1) % KS], ((j + 1) / KS) & 1, s_abort))) break;
+                            k_done = j + 2;
+                            k_next = true;
+                        }
+                        if (!(ok = pf_wait(&o_full[x], j & 1, s_abort))) break;
+                        tc_fence_after();
+                        mma_s(x, (j + 1) % KS);
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&v_empty[j % VS]);
+                if (j + 1 < ntiles) umma_commit(&k_empty[(j + 1) % KS]);
+                // refills: the stages of tile j are free once its S and P V products are done
+                if (j + KS < ntiles) {
+                    if (!(ok = pf_wait(&k_empty[j % KS], (j / KS) & 1, s_abort))) break;
+                    load_k(j + KS);
+                    k_issued = j + KS + 1;
+                }
+                if (j + VS < ntiles) {
+                    if (!(ok = pf_wait(&v_empty[j % VS], (j / VS) & 1, s_abort))) break;
+                    load_v(j + VS);
+                    v_issued = j + VS + 1;
                 }
             }
             // every product issued is complete before the tensor memory is released
@@ -279,102 +318,151 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
                 atomicOr(p.err, KVC_DEVERR_TIMEOUT);
                 // copies still in flight land before the shared memory is released
                 if (!q_done) mbar_wait_bounded(q_full, 0, kPfWaitNs / 8);
-                for (int t = k_done; t < k_issued; ++t) mbar_wait_bounded(&k_full[t & 1], (t >> 1) & 1, kPfWaitNs / 8);
-                for (int t = v_done; t < v_issued; ++t) mbar_wait_bounded(&v_full[t & 1], (t >> 1) & 1, kPfWaitNs / 8);
+                for (int t = k_done; t < k_issued; ++t)
+                    mbar_wait_bounded(&k_full[t % KS], (t / KS) & 1, kPfWaitNs / 8);
+                for (int t = v_done; t < v_issued; ++t)
+                    mbar_wait_bounded(&v_full[t % VS], (t / VS) & 1, kPfWaitNs / 8);
             }
         }
-    } else {
+    } else if (warp / 4 < nq) {
         // ================= row warps: softmax and output; thread = query row = TMEM lane =================
-        const int row = threadIdx.x;
-        const int qi = r0 + row;  // row of the segment
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int x = warp / 4, wq = warp & 3;
+        const int rx = r0 + x * kPfRows;        // first row of this query tile
+        const int row = wq * 32 + lane;
+        const int qi = rx + row;                // row of the segment
+        const int nt = x == 0 ? nt0 : nt1;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + x * kPfKeys + lane_base, tO = tmem + Geo::kTmemO + x * D + lane_base;
+        const float sl2 = p.scale_log2;
+        const bool neg_scale = sl2 < 0.f;  // then the largest scaled score comes from the smallest raw one
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            ok = __all_sync(0xffffffffu, pf_wait(s_full, j & 1, s_abort));
+        for (int j = 0; j < nt; ++j) {
+            // S_X(j) complete also means P_X(j-1) V(j-1) complete: it was issued before S_X(j)
+            ok = __all_sync(0xffffffffu, pf_wait(&s_full[x], j & 1, s_abort));
             if (!ok) break;
             tc_fence_after();
-            float s[2][32];  // keys c = 32 * (c >> 5) + (c & 31)
-            tmem_ld32(tS + lane_base, s[0]);
-            tmem_ld32(tS + lane_base + 32, s[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
-
             const int k0 = j * kPfKeys;
-            float mx = -INFINITY;
+            // a tile that crosses the causal diagonal or the segment end needs the mask; the others do not
+            const bool masked = k0 + kPfKeys > len || (p.causal && k0 + kPfKeys - 1 > rx);
+            // pass 1: the row's extreme raw score over the tile, one 64-key half at a time (registers)
+            const float fill = neg_scale ? INFINITY : -INFINITY;
+            float ext = fill;
 #pragma unroll
-            for (int c = 0; c < kPfKeys; ++c) {
-                const int kj = k0 + c;
-                const bool valid = kj < len && (!p.causal || kj <= qi);
-                float& x = s[c >> 5][c & 31];
-                x = valid ? x * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x);
+            for (int hh = 0; hh < 2; ++hh) {
+                float s[64];
+                tmem_ld64(tS + hh * 64, s);
+                float e[4];
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = fill;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int kj = k0 + hh * 64 + c;
+                        const bool valid = kj < len && (!p.causal || kj <= qi);
+                        const float v = valid ? s[c] : fill;
+                        e[c & 3] = neg_scale ? fminf(e[c & 3], v) : fmaxf(e[c & 3], v);
+                    }
+                } else if (!neg_scale) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = max3f(s[i], s[4 + i], s[8 + i]);
+#pragma unroll
+                    for (int c = 12; c + 8 <= 64; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e[i] = max3f(e[i], s[c + i], s[c + 4 + i]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = fmaxf(e[i], s[60 + i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = min3f(s[i], s[4 + i], s[8 + i]);
+#pragma unroll
+                    for (int c = 12; c + 8 <= 64; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) e[i] = min3f(e[i], s[c + i], s[c + 4 + i]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e[i] = fminf(e[i], s[60 + i]);
+                }
+                ext = neg_scale ? fminf(ext, fminf(fminf(e[0], e[1]), fminf(e[2], e[3])))
+                                : fmaxf(ext, fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])));
             }
+            // the tile's largest scaled score (-inf when every key is masked)
+            const float mx = (masked && ext == fill) ? -INFINITY : ext * sl2;
             // the running max moves only when it has grown by 2^8 (or from -inf): then l and O are rescaled
             float alpha = 1.f;
             if (mx > m_used + kPfRescaleLog2) {  // includes the first finite max (m_used = -inf)
                 alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mx);
                 m_used = mx;
             }
-            float ls = 0.f;
+            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+            // pass 2, per 64-key half: P = 2^(s * scale * log2 e - m) and its row sum; P = hi + lo in fp16
+            // written over the half's own S columns: hi of keys (2i, 2i + 1) in column i, lo in column 32 + i
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < kPfKeys; ++c) {
-                float& x = s[c >> 5][c & 31];
-                x = m_used == -INFINITY ? 0.f : ex2(x - m_used);
-                ls += x;
-            }
-            l = l * alpha + ls;
-            // P(j-1) V(j-1) must be done before O is rescaled and P is overwritten
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, pf_wait(o_full, (j - 1) & 1, s_abort));
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        float o[32];
-                        tmem_ld32(tO + lane_base + c, o);
+            for (int hh = 0; hh < 2; ++hh) {
+                float s[64];
+                tmem_ld64(tS + hh * 64, s);
+                if (masked) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tO + lane_base + c, o);
+                    for (int c = 0; c < 64; ++c) {
+                        const int kj = k0 + hh * 64 + c;
+                        const bool valid = kj < len && (!p.causal || kj <= qi);
+                        s[c] = valid ? ex2(fmaf(s[c], sl2, neg_m)) : 0.f;
+                        ls[c & 3] += s[c];
                     }
-                    tmem_wait_st();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        s[c] = ex2(fmaf(s[c], sl2, neg_m));
+                        ls[c & 3] += s[c];
+                    }
+                }
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    uint32_t hv[16], lv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = qq * 32 + 2 * e;
+                        hv[e] = pack_half2(s[c], s[c + 1]);
+                        const float2 f = unpack_half2(hv[e]);
+                        lv[e] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
+                    }
+                    tmem_st16(tS + hh * 64 + qq * 16, hv);
+                    tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
                 }
             }
-            // the last tile of a segment: V rows past its end (the next segment's tokens) are zeroed, so
-            // that whatever they hold cannot reach this segment's output through a zero weight
+            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            // O_X is idle here (P_X(j-1) V(j-1) is complete, P_X(j) V(j) not issued): rescale it in place
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    float o[32];
+                    tmem_ld32(tO + c, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(tO + c, o);
+                }
+            }
+            // the segment's last key tile: V rows past its end (the next segment's tokens) are zeroed, so that
+            // whatever they hold cannot reach this segment's output through a zero weight.  The first query
+            // tile that reads this key tile does it; its P V products are issued before the other tile's.
             const int vrem = len - k0;
-            if (vrem < kPfKeys && warp == 0) {
-                ok = __all_sync(0xffffffffu, pf_wait(&v_full[j & 1], (j >> 1) & 1, s_abort));
+            if (vrem < kPfKeys && wq == 0 && (x == 0 || j >= nt0)) {
+                ok = __all_sync(0xffffffffu, pf_wait(&v_full[j % VS], (j / VS) & 1, s_abort));
                 if (!ok) break;
-                uint8_t* vt = vst(j & 1);
+                uint8_t* vt = vst(j % VS);
                 for (int e = lane; e < (kPfKeys - vrem) * 8 * Geo::kChunks; e += 32) {
                     const int r = vrem + e / (8 * Geo::kChunks), rest = e % (8 * Geo::kChunks);
                     *reinterpret_cast<uint4*>(vt + (rest / 8) * Geo::kKVChunk + sw128(r, rest % 8)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
             }
-            // P = hi + lo in fp16, row `row`, 64 keys = 8 chunks of 16 bytes, 128-byte swizzle
-#pragma unroll
-            for (int cc = 0; cc < kPfKeys / 8; ++cc) {
-                uint32_t hv[4], lv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = cc * 8 + 2 * e;
-                    const float p0 = s[c >> 5][c & 31], p1 = s[(c + 1) >> 5][(c + 1) & 31];
-                    hv[e] = pack_half2(p0, p1);
-                    const float2 f = unpack_half2(hv[e]);
-                    lv[e] = pack_half2(p0 - f.x, p1 - f.y);
-                }
-                *reinterpret_cast<uint4*>(phi + sw128(row, cc)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4*>(plo + sw128(row, cc)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-            }
-            fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
-        if (ok) ok = __all_sync(0xffffffffu, pf_wait(o_full, (ntiles - 1) & 1, s_abort));
+        if (ok) ok = __all_sync(0xffffffffu, pf_wait(&o_full[x], (nt - 1) & 1, s_abort));
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -382,7 +470,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 float o[32];
-                tmem_ld32(tO + lane_base + c, o);
+                tmem_ld32(tO + c, o);
                 if (qi < len) {
                     if (p.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base + c);
@@ -428,13 +516,13 @@ static EncodeTiledFnP encode_fn_p() {
     return fn;
 }
 
-// [T][H][D] fp16 viewed as (dim, head, token); boxes of 64 dims x 1 head x 64 tokens, 128-byte swizzle
+// [T][H][D] fp16 viewed as (dim, head, token); boxes of 64 dims x 1 head x 128 tokens, 128-byte swizzle
 static cudaError_t make_packed_map(CUtensorMap* map, const void* base, int D, int H, int T) {
     EncodeTiledFnP fn = encode_fn_p();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t gdim[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     cuuint64_t gstride[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box[3] = {64, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -463,15 +551,16 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     p.err = a.err;
     p.nseq = a.nseq;
     p.total_tokens = a.total_tokens;
-    p.tiles_per_seq = (a.max_seqlen + kPfRows - 1) / kPfRows;
+    p.tiles_per_seq = (a.max_seqlen + kPfCtaRows - 1) / kPfCtaRows;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.G = a.Hq / a.Hkv;
     p.causal = a.causal;
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kPfLog2e;
-    dim3 grid(a.nseq * p.tiles_per_seq, a.Hq);
-    prefill_kernel<D><<<grid, kPfThreads, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
+    const int64_t nblocks = static_cast<int64_t>(p.tiles_per_seq) * a.nseq * a.Hq;
+    if (nblocks > 2147483647LL) return cudaErrorInvalidConfiguration;
+    prefill_kernel<D><<<static_cast<unsigned>(nblocks), kPfThreads, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

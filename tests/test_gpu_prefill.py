@@ -48,6 +48,8 @@ def test_config5(make, causal, out_dtype):
     ((63, 64, 65, 1, 130), 4, 2, 64),
     ((200, 3, 129), 8, 8, 128),
     ((333,), 14, 2, 64),
+    ((255, 256, 257, 384, 129, 128, 1, 640), 4, 2, 64),  # around the 256-row blocks of two query tiles
+    ((600, 250, 513, 64), 8, 2, 128),
 ])
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_ragged(seqlens, Hq, Hkv, D, causal):
@@ -83,3 +85,21 @@ def test_prefill_long_peaked(D, causal):
     assert kvc.kvc_device_error_flags(clear=True) == 0
     ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
     check_attention(out, ref, f"prefill peaked D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.5])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_scale_sign(scale, causal):
+    """Any real scale: a negative one makes the smallest raw score the largest scaled one; zero gives
+    uniform weights over the visible keys."""
+    import paged_kv_cache_27_gb300 as kvc
+    seqlens = (300, 77, 520)
+    wl = workloads._prefill("scale", [11, sum(seqlens), 64], seqlens, 4, 1, 64)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
+    cu = torch.from_numpy(wl.cu_seqlens).cuda()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    kvc.prefill_attention(q, k, v, cu, max(seqlens), scale, causal, out)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, scale, causal=causal)
+    check_attention(out, ref, f"prefill scale={scale} causal={causal}")
