@@ -688,7 +688,7 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
     import paged_kv_cache_27_gb300 as kvc
 
     # config 5 and larger prefill shapes: causal varlen prefill on the tensor cores
-    def prefill_case(name, seqlens, Hq, Hkv, D, causal=True):
+    def prefill_case(name, seqlens, Hq, Hkv, D, causal=True, precise=False):
         T = sum(seqlens)
         gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
         qq = torch.randn((T, Hq, D), generator=gen, device=device).half()
@@ -696,15 +696,17 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
         vv = torch.randn((T, Hkv, D), generator=gen, device=device).half()
         cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
         oo = torch.empty((T, Hq, D), dtype=torch.float16, device=device)
-        fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo)
+        fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo,
+                                           precise=precise)
         us = _timed_calls(fn, 20, flush, stream)
         pairs = sum(s * (s + 1) // 2 for s in seqlens) if causal else sum(s * s for s in seqlens)
         flops = 4 * D * Hq * pairs
         tf = flops / (us * 1e-6) / 1e12
-        emit({"config": name, "us_per_call": us, "TFLOPs": tf, "pct_tensor_peak": tf / tflops_peak * 100,
+        emit({"config": name, "p_precision": "split (fp16 high part + residual)" if precise else "fp16",
+              "us_per_call": us, "TFLOPs": tf, "pct_tensor_peak": tf / tflops_peak * 100,
               "flops": flops, "peak_TFLOPs": tflops_peak, "peak_kind": tflops_kind,
-              "note": "algorithmic flops (masked half not counted); the kernel's tensor work is 1.5x that "
-                      "(P V runs for the fp16 high part and the residual of P)"})
+              "note": "algorithmic flops (masked half not counted)" + (
+                  "; the split form's tensor work is 1.5x that (P V runs for both parts of P)" if precise else "")})
 
     prefill_case("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal", (37, 120, 8, 200), 8, 8, 64)
     prefill_case("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2, 64)
@@ -712,6 +714,10 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
                  (592, 1920, 128, 3200), 8, 8, 64)
     prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",
                  (4096,) * 4, 32, 8, 128)
+    prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",
+                 (4096,) * 4, 32, 8, 128, precise=True)
+    prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, non-causal",
+                 (4096,) * 4, 32, 8, 128, causal=False)
 
 
 def main():

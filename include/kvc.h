@@ -379,6 +379,22 @@ kvc_status prefill_attention(const void* q, const void* k, const void* v, const 
                              int nseq, int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim,
                              float scale, int causal, void* out, int out_dtype, void* stream);
 
+/* Precision of P, the softmax weights that multiply V on the tensor cores in prefill_attention_ex.
+ *   KVC_PREFILL_P_F16    P rounded to fp16 (its exponent base is the running row max, so P <= 2^8), and
+ *                        the normaliser l sums the rounded weights: every output row is an exact convex
+ *                        combination of V rows with weights perturbed by at most 2^-11 relative.  Observed
+ *                        error vs an fp64 softmax: ~5e-4 max-abs on unit-variance inputs.  The default.
+ *   KVC_PREFILL_P_SPLIT  P = fp16 high part + fp16 residual, both multiplied by V (twice the P V products):
+ *                        the weights carry ~22 bits, observed error ~5e-6 max-abs. */
+#define KVC_PREFILL_P_F16 0
+#define KVC_PREFILL_P_SPLIT 1
+
+/* prefill_attention with a choice of P precision (above); prefill_attention is this call with
+ * KVC_PREFILL_P_F16.  KVC_ERR_INVALID for any other p_precision; everything else as prefill_attention. */
+kvc_status prefill_attention_ex(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                int nseq, int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim,
+                                float scale, int causal, int p_precision, void* out, int out_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

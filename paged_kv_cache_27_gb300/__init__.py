@@ -35,6 +35,7 @@ __all__ = [
 ]
 
 KVC_F16, KVC_F32 = 0, 1
+KVC_PREFILL_P_F16, KVC_PREFILL_P_SPLIT = 0, 1
 STATUS = {0: "KVC_OK", 1: "KVC_ERR_INVALID", 2: "KVC_ERR_OOM", 3: "KVC_ERR_CAPACITY", 4: "KVC_ERR_CUDA",
           5: "KVC_ERR_UNSUPPORTED"}
 DEVERR = {"BLOCK_ID": 0x1, "CONTEXT": 0x2, "SLOT": 0x4, "TIMEOUT": 0x8, "SEQLENS": 0x10}
@@ -122,6 +123,7 @@ def _load():
         "paged_decode_cascade_attention": (I, [P, P, P, I, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P,
                                                I, P, SZ, P]),
         "prefill_attention": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]),
+        "prefill_attention_ex": (I, [P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, I, P, I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -583,9 +585,11 @@ def paged_decode_attention_raw(q_ptr: int, k_ptr: int, v_ptr: int, num_blocks: i
                                        blocks_per_split, stream), "paged_decode_attention")
 
 
-def prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
-                      scale: float, causal: bool, out: torch.Tensor, stream=None) -> None:
-    """Packed varlen prefill: q [T][Hq][D], k/v [T][Hkv][D] fp16, cu_seqlens int32 [nseq+1] -> out [T][Hq][D]."""
+def prefill_attention_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                         max_seqlen: int, scale: float, causal: bool, p_precision: int, out: torch.Tensor,
+                         stream=None) -> None:
+    """Packed varlen prefill with a choice of P precision (KVC_PREFILL_P_F16 or KVC_PREFILL_P_SPLIT):
+    q [T][Hq][D], k/v [T][Hkv][D] fp16, cu_seqlens int32 [nseq+1] -> out [T][Hq][D]."""
     T, Hq, D = q.shape
     Hkv = k.shape[1]
     if k.shape != (T, Hkv, D) or v.shape != k.shape or out.shape != q.shape:
@@ -593,8 +597,19 @@ def prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seql
     od = KVC_F16 if out.dtype == torch.float16 else KVC_F32 if out.dtype == torch.float32 else None
     if od is None:
         raise TypeError("out must be float16 or float32")
-    _check(_lib.prefill_attention(_dptr(q, torch.float16, "q"), _dptr(k, torch.float16, "k"),
-                                  _dptr(v, torch.float16, "v"), _dptr(cu_seqlens, torch.int32, "cu_seqlens"),
-                                  cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, D, float(scale),
-                                  int(bool(causal)), _dptr(out, None, "out"), od, _stream(stream, q)),
-           "prefill_attention")
+    _check(_lib.prefill_attention_ex(_dptr(q, torch.float16, "q"), _dptr(k, torch.float16, "k"),
+                                     _dptr(v, torch.float16, "v"), _dptr(cu_seqlens, torch.int32, "cu_seqlens"),
+                                     cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, D, float(scale),
+                                     int(bool(causal)), int(p_precision), _dptr(out, None, "out"), od,
+                                     _stream(stream, q)),
+           "prefill_attention_ex")
+
+
+def prefill_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                      scale: float, causal: bool, out: torch.Tensor, stream=None, precise: bool = False) -> None:
+    """Packed varlen prefill: q [T][Hq][D], k/v [T][Hkv][D] fp16, cu_seqlens int32 [nseq+1] -> out [T][Hq][D].
+
+    precise=False rounds the softmax weights P to fp16 (KVC_PREFILL_P_F16); precise=True multiplies V by
+    P's fp16 high part and residual (KVC_PREFILL_P_SPLIT)."""
+    prefill_attention_ex(q, k, v, cu_seqlens, max_seqlen, scale, causal,
+                         KVC_PREFILL_P_SPLIT if precise else KVC_PREFILL_P_F16, out, stream)

@@ -718,9 +718,11 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
     return KVC_OK;
 }
 
-kvc_status prefill_attention(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int nseq,
-                             int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim, float scale, int causal,
-                             void* out, int out_dtype, void* stream) {
+kvc_status prefill_attention_ex(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int nseq,
+                                int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim, float scale,
+                                int causal, int p_precision, void* out, int out_dtype, void* stream) {
+    if (p_precision != KVC_PREFILL_P_F16 && p_precision != KVC_PREFILL_P_SPLIT)
+        return fail(KVC_ERR_INVALID, "bad p_precision %d", p_precision);
     if (nseq < 0 || total_tokens < 0 || max_seqlen < 0 || Hq < 1 || Hkv < 1) return fail(KVC_ERR_INVALID, "bad sizes");
     if (Hq % Hkv) return fail(KVC_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
     if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
@@ -755,11 +757,19 @@ kvc_status prefill_attention(const void* q, const void* k, const void* v, const 
     a.causal = causal ? 1 : 0;
     a.out = out;
     a.out_f32 = out_dtype == KVC_F32;
+    a.split_p = p_precision == KVC_PREFILL_P_SPLIT;
     cudaError_t e = kvc::device_error_word(&a.err);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     e = kvc::launch_prefill(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill_attention launch");
     return KVC_OK;
+}
+
+kvc_status prefill_attention(const void* q, const void* k, const void* v, const int32_t* cu_seqlens, int nseq,
+                             int total_tokens, int max_seqlen, int Hq, int Hkv, int head_dim, float scale, int causal,
+                             void* out, int out_dtype, void* stream) {
+    return prefill_attention_ex(q, k, v, cu_seqlens, nseq, total_tokens, max_seqlen, Hq, Hkv, head_dim, scale, causal,
+                                KVC_PREFILL_P_F16, out, out_dtype, stream);
 }
 
 }  // extern "C"

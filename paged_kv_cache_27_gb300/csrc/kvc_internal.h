@@ -134,6 +134,7 @@ struct PrefillArgs {
     int causal;
     void* out;
     int out_f32;
+    int split_p;  // P as fp16 high part + fp16 residual (else one fp16 value)
     unsigned* err;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);

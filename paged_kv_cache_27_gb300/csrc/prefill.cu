@@ -60,8 +60,9 @@ struct PfGeom {
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers, TMEM address, abort flag; alignment
     static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
     // TMEM columns: S_A / P_A [0, 128), S_B / P_B [128, 256), O_A [256, 256 + D), O_B [256 + D, 256 + 2D).
-    // P_X is written over S_X once the row warps have read S_X: per 64-key half h, the high fp16 parts in
-    // columns [64h, 64h + 32) and the residuals in [64h + 32, 64h + 64), two keys per column.
+    // P_X is written over S_X once the row warps have read S_X: per 64-key half h, P in fp16 (or its high
+    // fp16 part) in columns [64h, 64h + 32), the residuals of the split form in [64h + 32, 64h + 64), two keys
+    // per column.
     static constexpr int kTmemO = kPfQTiles * kPfKeys;
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kTmemO + kPfQTiles * D <= 512, "tensor memory");
@@ -123,7 +124,7 @@ __device__ __forceinline__ int pf_key_tiles(int rx, int len, int causal) {
     return (kv_len + kPfKeys - 1) / kPfKeys;
 }
 
-template <int D>
+template <int D, bool kSplitP>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                 const __grid_constant__ CUtensorMap tmK,
                                                                 const __grid_constant__ CUtensorMap tmV,
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 }
                 umma_commit(&s_full[x]);
             };
-            // O_X += P_X(j) V(j): 8 steps of 16 keys, high and residual parts of P read from TMEM, N = D
+            // O_X += P_X(j) V(j): 8 steps of 16 keys, P read from TMEM (fp16, or high and residual parts), N = D
             auto mma_pv = [&](int x, int st, bool first) {
                 const uint64_t v0 = dV + static_cast<uint64_t>(st * (Geo::kKVBytes >> 4));
                 const uint32_t tP = tmem + x * kPfKeys, tO = tmem + Geo::kTmemO + x * D;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     const uint64_t b = v0 + ((kk * 2048) >> 4);
                     const uint32_t tPk = tP + (kk >> 2) * 64 + (kk & 3) * 8;  // hi; lo 32 columns on
                     umma_f16_ts(tO, tPk, b, idPV, (!first || kk > 0) ? 1u : 0u);
-                    umma_f16_ts(tO, tPk + 32, b, idPV, 1u);
+                    if constexpr (kSplitP) umma_f16_ts(tO, tPk + 32, b, idPV, 1u);
                 }
                 umma_commit(&o_full[x]);
             };
@@ -394,8 +395,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 m_used = mx;
             }
             const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-            // pass 2, per 64-key half: P = 2^(s * scale * log2 e - m) and its row sum; P = hi + lo in fp16
-            // written over the half's own S columns: hi of keys (2i, 2i + 1) in column i, lo in column 32 + i
+            // pass 2, per 64-key half: P = 2^(s * scale * log2 e - m), written over the half's own S columns
+            // in fp16, keys (2i, 2i + 1) in column i.  Split: P = hi + lo (fp16 high part and fp16 residual,
+            // the residual in column 32 + i) and l sums P in fp32.  Otherwise l sums the fp16-rounded P, so
+            // that the weights that reach V are exactly the ones normalised.
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -407,14 +410,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                         const int kj = k0 + hh * 64 + c;
                         const bool valid = kj < len && (!p.causal || kj <= qi);
                         s[c] = valid ? ex2(fmaf(s[c], sl2, neg_m)) : 0.f;
-                        ls[c & 3] += s[c];
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        s[c] = ex2(fmaf(s[c], sl2, neg_m));
-                        ls[c & 3] += s[c];
-                    }
+                    for (int c = 0; c < 64; ++c) s[c] = ex2(fmaf(s[c], sl2, neg_m));
                 }
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
@@ -423,11 +422,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     for (int e = 0; e < 16; ++e) {
                         const int c = qq * 32 + 2 * e;
                         hv[e] = pack_half2(s[c], s[c + 1]);
-                        const float2 f = unpack_half2(hv[e]);
-                        lv[e] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
+                        if constexpr (kSplitP) {
+                            const float2 f = unpack_half2(hv[e]);
+                            lv[e] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
+                            ls[e & 3] += s[c] + s[c + 1];
+                        } else {
+                            const float2 f = unpack_half2(hv[e]);
+                            ls[e & 3] += f.x + f.y;
+                        }
                     }
                     tmem_st16(tS + hh * 64 + qq * 16, hv);
-                    tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
+                    if constexpr (kSplitP) tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
                 }
             }
             l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
@@ -530,13 +535,13 @@ static cudaError_t make_packed_map(CUtensorMap* map, const void* base, int D, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool kSplitP>
 static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     using Geo = PfGeom<D>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(prefill_kernel<D, kSplitP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         Geo::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -560,15 +565,17 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     p.scale_log2 = a.scale * kPfLog2e;
     const int64_t nblocks = static_cast<int64_t>(p.tiles_per_seq) * a.nseq * a.Hq;
     if (nblocks > 2147483647LL) return cudaErrorInvalidConfiguration;
-    prefill_kernel<D><<<static_cast<unsigned>(nblocks), kPfThreads, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, kSplitP><<<static_cast<unsigned>(nblocks), kPfThreads, Geo::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (a.nseq <= 0 || a.total_tokens <= 0 || a.max_seqlen <= 0) return cudaSuccess;
-    switch (a.D) {
-        case 64: return launch_prefill_d<64>(a, stream);
-        case 128: return launch_prefill_d<128>(a, stream);
+    switch (a.D * 2 + (a.split_p ? 1 : 0)) {
+        case 128: return launch_prefill_d<64, false>(a, stream);
+        case 129: return launch_prefill_d<64, true>(a, stream);
+        case 256: return launch_prefill_d<128, false>(a, stream);
+        case 257: return launch_prefill_d<128, true>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -52,22 +52,26 @@ def test_config5(make, causal, out_dtype):
     ((600, 250, 513, 64), 8, 2, 128),
 ])
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_ragged(seqlens, Hq, Hkv, D, causal):
+@pytest.mark.parametrize("precise", [False, True])
+def test_prefill_ragged(seqlens, Hq, Hkv, D, causal, precise):
     import paged_kv_cache_27_gb300 as kvc
     wl = workloads._prefill("ragged", [99, sum(seqlens), D], seqlens, Hq, Hkv, D)
     q, k, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
     cu = torch.from_numpy(wl.cu_seqlens).cuda()
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-    kvc.prefill_attention(q, k, v, cu, max(seqlens), wl.scale, causal, out)
+    kvc.prefill_attention(q, k, v, cu, max(seqlens), wl.scale, causal, out, precise=precise)
     torch.cuda.synchronize()
     assert kvc.kvc_device_error_flags(clear=True) == 0
     ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
-    check_attention(out, ref, f"prefill {seqlens}")
+    err = check_attention(out, ref, f"prefill {seqlens}")
+    if precise:  # fp16 high part + residual: the weights keep ~22 bits
+        assert err < 5e-5, err
 
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_long_peaked(D, causal):
+@pytest.mark.parametrize("precise", [False, True])
+def test_prefill_long_peaked(D, causal, precise):
     """Long segments whose scores jump by far more than 2^8 between key tiles (keys scaled x6 every 97
     positions, growing along the segment): the running max moves and O is rescaled in place many times."""
     import paged_kv_cache_27_gb300 as kvc
@@ -80,11 +84,13 @@ def test_prefill_long_peaked(D, causal):
     q, kk, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
     cu = torch.from_numpy(wl.cu_seqlens).cuda()
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-    kvc.prefill_attention(q, kk, v, cu, max(seqlens), wl.scale, causal, out)
+    kvc.prefill_attention(q, kk, v, cu, max(seqlens), wl.scale, causal, out, precise=precise)
     torch.cuda.synchronize()
     assert kvc.kvc_device_error_flags(clear=True) == 0
     ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
-    check_attention(out, ref, f"prefill peaked D={D} causal={causal}")
+    err = check_attention(out, ref, f"prefill peaked D={D} causal={causal}")
+    if precise:
+        assert err < 5e-5, err
 
 
 @pytest.mark.parametrize("scale", [-0.09, 0.0, 0.5])
@@ -103,3 +109,14 @@ def test_prefill_scale_sign(scale, causal):
     assert kvc.kvc_device_error_flags(clear=True) == 0
     ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, scale, causal=causal)
     check_attention(out, ref, f"prefill scale={scale} causal={causal}")
+
+
+def test_prefill_bad_precision_rejected():
+    import paged_kv_cache_27_gb300 as kvc
+    q = torch.zeros((4, 2, 64), dtype=torch.float16, device="cuda")
+    k = torch.zeros((4, 1, 64), dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+    out = torch.empty((4, 2, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.prefill_attention_ex(q, k, k, cu, 4, 0.125, True, 7, out)
+    assert "KVC_ERR_INVALID" in str(e.value)
