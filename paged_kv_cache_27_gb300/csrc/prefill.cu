@@ -39,7 +39,9 @@ constexpr int kPfQTiles = 2;   // query tiles per CTA, A and B
 constexpr int kPfCtaRows = kPfRows * kPfQTiles;
 constexpr int kPfKeys = 128;   // keys per K/V tile: N of S, K of P V
 constexpr int kPfRowWarps = 4 * kPfQTiles;
-constexpr int kPfThreads = (kPfRowWarps + 1) * 32;
+constexpr int kPfMmaWarp = kPfRowWarps;       // issues the tensor-core products
+constexpr int kPfLoadWarp = kPfRowWarps + 1;  // issues the TMA copies
+constexpr int kPfThreads = (kPfRowWarps + 2) * 32;
 constexpr uint64_t kPfWaitNs = 1000000000ull;
 constexpr float kPfLog2e = 1.4426950408889634f;
 constexpr float kPfRescaleLog2 = 8.f;  // P stays below 2^8, far inside fp16
@@ -100,6 +102,15 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
     float r;
     asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// acc + the two fp16 halves of h (each converted exactly), as two rounded fp32 additions
+__device__ __forceinline__ float add_f16x2_to_f32(uint32_t h, float acc) {
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(h));
+    return acc;
 }
 
 // Wait for a phase; gives up when another thread of the CTA has given up (abort flag) or after the limit,
@@ -199,8 +210,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == kPfRowWarps) {
-        // ================= producer: TMA copies and tensor-core products (one thread) =================
+    if (warp == kPfLoadWarp) {
+        // ================= loads: every TMA copy (one thread) =================
         if (lane == 0) {
             auto load_k = [&](int t) {
                 uint64_t* bar = &k_full[t % KS];
@@ -224,12 +235,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
                 for (int c = 0; c < Geo::kChunks; ++c)
                     tma_load_3d(qs(x) + c * Geo::kQChunk, &tmQ, q_full, c * 64, h, beg + r0 + x * kPfRows);
-            int k_issued = 0, v_issued = 0;  // tiles whose copies were issued
-            for (; k_issued < min(ntiles, KS); ++k_issued) load_k(k_issued);
-            for (; v_issued < min(ntiles, VS); ++v_issued) load_v(v_issued);
-            int k_done = 0, v_done = 0;  // tiles whose copies were waited for
-            bool q_done = false;
-
+            // tile t goes into the stage of tile t - stages once that tile's products are done
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int t = 0; ok && t < ntiles; ++t) {
+                if (t >= KS && !(ok = pf_wait(&k_empty[t % KS], ((t - KS) / KS) & 1, s_abort))) break;
+                load_k(t);
+                k_issued = t + 1;
+                if (t >= VS && !(ok = pf_wait(&v_empty[t % VS], ((t - VS) / VS) & 1, s_abort))) break;
+                load_v(t);
+                v_issued = t + 1;
+            }
+            // copies still in flight land before the shared memory is released (immediate unless aborted:
+            // the products consumed every tile)
+            mbar_wait_bounded(q_full, 0, kPfWaitNs / 8);
+            for (int t = max(0, k_issued - KS); t < k_issued; ++t)
+                mbar_wait_bounded(&k_full[t % KS], (t / KS) & 1, kPfWaitNs / 8);
+            for (int t = max(0, v_issued - VS); t < v_issued; ++t)
+                mbar_wait_bounded(&v_full[t % VS], (t / VS) & 1, kPfWaitNs / 8);
+        }
+    } else if (warp == kPfMmaWarp) {
+        // ================= tensor-core products (one thread) =================
+        if (lane == 0) {
             constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, 0, 0);
             constexpr uint32_t idPV = umma_idesc_f16(kPfRows, D, 0, 1);
             // Descriptors are built once per operand; within a tile only the start-address field moves, by
@@ -265,18 +292,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 umma_commit(&o_full[x]);
             };
 
-            bool ok = pf_wait(q_full, 0, s_abort);
-            q_done = ok;
-            ok = ok && pf_wait(&k_full[0], 0, s_abort);
+            bool ok = pf_wait(q_full, 0, s_abort) && pf_wait(&k_full[0], 0, s_abort);
             if (ok) {
-                k_done = 1;
                 tc_fence_after();
                 for (int x = 0; x < nq; ++x) mma_s(x, 0);
                 umma_commit(&k_empty[0]);
             }
             for (int j = 0; ok && j < ntiles; ++j) {
                 if (!(ok = pf_wait(&v_full[j % VS], (j / VS) & 1, s_abort))) break;
-                v_done = j + 1;
                 bool k_next = false;
                 // per query tile: P_X(j) V(j) once P_X(j) is in TMEM; then S_X(j + 1) into the same columns
                 // once that product has read P_X(j)
@@ -289,7 +312,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     if (j + 1 < ntx) {
                         if (!k_next) {
                             if (!(ok = pf_wait(&k_full[(j + 1) % KS], ((j + 1) / KS) & 1, s_abort))) break;
-                            k_done = j + 2;
                             k_next = true;
                         }
                         if (!(ok = pf_wait(&o_full[x], j & 1, s_abort))) break;
@@ -300,30 +322,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 if (!ok) break;
                 umma_commit(&v_empty[j % VS]);
                 if (j + 1 < ntiles) umma_commit(&k_empty[(j + 1) % KS]);
-                // refills: the stages of tile j are free once its S and P V products are done
-                if (j + KS < ntiles) {
-                    if (!(ok = pf_wait(&k_empty[j % KS], (j / KS) & 1, s_abort))) break;
-                    load_k(j + KS);
-                    k_issued = j + KS + 1;
-                }
-                if (j + VS < ntiles) {
-                    if (!(ok = pf_wait(&v_empty[j % VS], (j / VS) & 1, s_abort))) break;
-                    load_v(j + VS);
-                    v_issued = j + VS + 1;
-                }
             }
             // every product issued is complete before the tensor memory is released
             umma_commit(fin);
             mbar_wait_bounded(fin, 0, kPfWaitNs);
-            if (!ok) {
-                atomicOr(p.err, KVC_DEVERR_TIMEOUT);
-                // copies still in flight land before the shared memory is released
-                if (!q_done) mbar_wait_bounded(q_full, 0, kPfWaitNs / 8);
-                for (int t = k_done; t < k_issued; ++t)
-                    mbar_wait_bounded(&k_full[t % KS], (t / KS) & 1, kPfWaitNs / 8);
-                for (int t = v_done; t < v_issued; ++t)
-                    mbar_wait_bounded(&v_full[t % VS], (t / VS) & 1, kPfWaitNs / 8);
-            }
+            if (!ok) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
         }
     } else if (warp / 4 < nq) {
         // ================= row warps: softmax and output; thread = query row = TMEM lane =================
@@ -336,6 +339,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const uint32_t tS = tmem + x * kPfKeys + lane_base, tO = tmem + Geo::kTmemO + x * D + lane_base;
         const float sl2 = p.scale_log2;
         const bool neg_scale = sl2 < 0.f;  // then the largest scaled score comes from the smallest raw one
+        const float fill = neg_scale ? INFINITY : -INFINITY;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
@@ -346,9 +350,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             const int k0 = j * kPfKeys;
             // a tile that crosses the causal diagonal or the segment end needs the mask; the others do not
             const bool masked = k0 + kPfKeys > len || (p.causal && k0 + kPfKeys - 1 > rx);
-            // pass 1: the row's extreme raw score over the tile, one 64-key half at a time (registers)
-            const float fill = neg_scale ? INFINITY : -INFINITY;
-            float ext = fill;
+            float alpha = 1.f;       // rescale of O and of the l of earlier tiles
+            float lsum[2] = {0.f, 0.f};  // per 64-key half: sum of the weights written
+            // One pass per 64-key half: the half's extreme score, the lazy running max (it moves only when the
+            // max has grown by 2^8, or from -inf), then P = 2^(s * scale * log2 e - m) written over the half's
+            // own S columns in fp16, keys (2i, 2i + 1) in column i (split form: the high part there, the
+            // residual in column 32 + i).  l sums the fp16 weights written (split form: P in fp32).
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float s[64];
@@ -383,27 +390,45 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
                     for (int i = 0; i < 4; ++i) e[i] = fminf(e[i], s[60 + i]);
                 }
-                ext = neg_scale ? fminf(ext, fminf(fminf(e[0], e[1]), fminf(e[2], e[3])))
-                                : fmaxf(ext, fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])));
-            }
-            // the tile's largest scaled score (-inf when every key is masked)
-            const float mx = (masked && ext == fill) ? -INFINITY : ext * sl2;
-            // the running max moves only when it has grown by 2^8 (or from -inf): then l and O are rescaled
-            float alpha = 1.f;
-            if (mx > m_used + kPfRescaleLog2) {  // includes the first finite max (m_used = -inf)
-                alpha = m_used == -INFINITY ? 0.f : ex2(m_used - mx);
-                m_used = mx;
-            }
-            const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-            // pass 2, per 64-key half: P = 2^(s * scale * log2 e - m), written over the half's own S columns
-            // in fp16, keys (2i, 2i + 1) in column i.  Split: P = hi + lo (fp16 high part and fp16 residual,
-            // the residual in column 32 + i) and l sums P in fp32.  Otherwise l sums the fp16-rounded P, so
-            // that the weights that reach V are exactly the ones normalised.
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                const float ext = neg_scale ? fminf(fminf(e[0], e[1]), fminf(e[2], e[3]))
+                                            : fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
+                const float mx = ext == fill ? -INFINITY : ext * sl2;  // -inf when every key is masked
+                float a_h = 1.f;
+                if (mx > m_used + kPfRescaleLog2) {  // includes the first finite max (m_used = -inf)
+                    a_h = m_used == -INFINITY ? 0.f : ex2(m_used - mx);
+                    m_used = mx;
+                }
+                if (hh == 1 && __any_sync(0xffffffffu, a_h != 1.f)) {
+                    // the max moved inside the tile: the first half's weights, already written, are scaled to
+                    // the new base and re-rounded (l takes their new sum); then this half's scores are read again
+                    float w[32], r[32];
+                    tmem_ld32(tS, w);
+                    if constexpr (kSplitP) tmem_ld32(tS + 32, r);
+                    float s0 = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float s[64];
-                tmem_ld64(tS + hh * 64, s);
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 f = unpack_half2(__float_as_uint(w[i]));
+                        if constexpr (kSplitP) {
+                            const float2 g = unpack_half2(__float_as_uint(r[i]));
+                            const float p0 = (f.x + g.x) * a_h, p1 = (f.y + g.y) * a_h;
+                            const uint32_t hi = pack_half2(p0, p1);
+                            const float2 hf = unpack_half2(hi);
+                            w[i] = __uint_as_float(hi);
+                            r[i] = __uint_as_float(pack_half2(p0 - hf.x, p1 - hf.y));
+                            s0 += p0 + p1;
+                        } else {
+                            const uint32_t hi = pack_half2(f.x * a_h, f.y * a_h);
+                            w[i] = __uint_as_float(hi);
+                            s0 = add_f16x2_to_f32(hi, s0);
+                        }
+                    }
+                    tmem_st32(tS, w);
+                    if constexpr (kSplitP) tmem_st32(tS + 32, r);
+                    if (a_h != 1.f) lsum[0] = s0;
+                    tmem_ld64(tS + 64, s);
+                }
+                alpha *= a_h;
+                const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
                 if (masked) {
 #pragma unroll
                     for (int c = 0; c < 64; ++c) {
@@ -415,27 +440,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = ex2(fmaf(s[c], sl2, neg_m));
                 }
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
                     uint32_t hv[16], lv[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = qq * 32 + 2 * e;
-                        hv[e] = pack_half2(s[c], s[c + 1]);
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const int c = qq * 32 + 2 * e2;
+                        hv[e2] = pack_half2(s[c], s[c + 1]);
                         if constexpr (kSplitP) {
-                            const float2 f = unpack_half2(hv[e]);
-                            lv[e] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
-                            ls[e & 3] += s[c] + s[c + 1];
+                            const float2 f = unpack_half2(hv[e2]);
+                            lv[e2] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
+                            ls4[e2 & 3] += s[c] + s[c + 1];
                         } else {
-                            const float2 f = unpack_half2(hv[e]);
-                            ls[e & 3] += f.x + f.y;
+                            ls4[e2 & 3] = add_f16x2_to_f32(hv[e2], ls4[e2 & 3]);
                         }
                     }
                     tmem_st16(tS + hh * 64 + qq * 16, hv);
                     if constexpr (kSplitP) tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
                 }
+                lsum[hh] = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             }
-            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            l = l * alpha + (lsum[0] + lsum[1]);
             // O_X is idle here (P_X(j-1) V(j-1) is complete, P_X(j) V(j) not issued): rescale it in place
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
