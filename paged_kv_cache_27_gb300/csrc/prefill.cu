@@ -115,13 +115,26 @@ __device__ __forceinline__ float add_f16x2_to_f32(uint32_t h, float acc) {
 
 // Wait for a phase; gives up when another thread of the CTA has given up (abort flag) or after the limit,
 // in which case it raises the flag itself.
+// The waiting thread sleeps in the hardware until the phase completes or 20 us pass, so waiting warps do not
+// take issue slots from working ones.
+__device__ __forceinline__ bool pf_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (;;) {
+        if (pf_try_wait_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((i & 63u) == 63u && global_timer_ns() - t0 > kPfWaitNs) {
+        if (global_timer_ns() - t0 > kPfWaitNs) {
             *abort_flag = 1;
             return false;
         }
