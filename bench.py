@@ -573,7 +573,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
     k16 = [kp0] + [torch.randn(kp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
     v16 = [vp0] + [torch.randn(vp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
     k8 = [torch.empty(kp0.shape, dtype=torch.uint8, device=device) for _ in range(Lq)]
-    v8 = [torch.empty(kp0.shape, dtype=torch.uint8, device=device) for _ in range(Lq)]
+    v8 = [torch.empty(kp0.shape[:2] + (64, 16), dtype=torch.uint8, device=device) for _ in range(Lq)]  # V^T rows
     ks8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
     vs8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
     all_slots = torch.arange(NBq * 16, dtype=torch.int64, device=device)
@@ -630,7 +630,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
         kpl, vpl, tbl, ctl, ql, _, _ = _decode_state(Bl, Cl, 14, 2, 64, device, seed=Bl + Cl)
         NBl = kpl.shape[0]
         k8l = torch.empty(kpl.shape, dtype=torch.uint8, device=device)
-        v8l = torch.empty(kpl.shape, dtype=torch.uint8, device=device)
+        v8l = torch.empty(kpl.shape[:2] + (64, 16), dtype=torch.uint8, device=device)
         ks8l = torch.empty(kpl.shape[:3], dtype=torch.float32, device=device)
         vs8l = torch.empty(kpl.shape[:3], dtype=torch.float32, device=device)
         rows = lambda t: t.permute(0, 2, 1, 3).reshape(NBl * 16, 2, 64).contiguous()

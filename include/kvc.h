@@ -290,12 +290,17 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
 
 /* Quantized (fp8) KV cache — an extension: the pages quantize weights, not
  * the KV cache, and fix no quantized format.  A layer's cache is e4m3 codes
- * (1 sign, 4 exponent bits with bias 7, 3 fraction bits; largest 448)
- * k_codes / v_codes [NB][Hkv][bs][D] (1 byte each) and one float scale per
- * (slot, KV head) row, k_scales / v_scales [NB][Hkv][bs]; a cached value is
- * code value * scale.  Per-row scales mean that appending a token never
- * re-quantizes the rest of its block.  The bytes per token are 53 % of the
- * fp16 cache's (D = 64).
+ * (1 sign, 4 exponent bits with bias 7, 3 fraction bits; largest 448), one
+ * byte each, and one float scale per (slot, KV head) row, k_scales / v_scales
+ * [NB][Hkv][bs]; a cached value is code value * scale.  k_codes is
+ * [NB][Hkv][bs][D] (a row of D codes per token, as the fp16 cache);
+ * v_codes is [NB][Hkv][D][bs]: per block and KV head, one row of 16 token
+ * codes per dim, token tau (0..15) at byte
+ *   4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1)
+ * of the row (tokens 2t, 2t+1, 2t+8, 2t+9 are bytes 4t..4t+3: the decode
+ * kernel loads its matrix-multiply fragments with one 32-bit read per row).
+ * Per-row scales mean that appending a token never re-quantizes the rest of
+ * its block.  The bytes per token are 53 % of the fp16 cache's (D = 64).
  *
  * kv_append_fp8: quantize k_new / v_new (device fp16 [n][Hkv][D]) and write
  * them to their slots: scale = absmax / 448 of the row (IEEE division; 1 for

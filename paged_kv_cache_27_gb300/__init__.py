@@ -31,7 +31,7 @@ __all__ = [
     "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
-    "prefill_attention", "DEVERR",
+    "prefill_attention", "prefill_attention_ex", "fp8_v_position", "DEVERR",
 ]
 
 KVC_F16, KVC_F32 = 0, 1
@@ -469,13 +469,19 @@ def paged_decode_multi_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache
         workspace.numel() * workspace.element_size(), _stream(stream, q)), "paged_decode_multi_attention")
 
 
+def fp8_v_position(tau: int) -> int:
+    """Byte position of token tau (0..15) of a block within each 16-byte dim row of the fp8 V code pool."""
+    return 4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1)
+
+
 def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
                   v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor, stream=None) -> None:
-    """Quantize k_new / v_new (fp16 [n][Hkv][D]) into an fp8 cache layer: codes uint8 [NB][Hkv][bs][D], scales
-    float32 [NB][Hkv][bs] (one per row; value = e4m3 code value * scale); slot_mapping int64 [n]."""
+    """Quantize k_new / v_new (fp16 [n][Hkv][D]) into an fp8 cache layer: K codes uint8 [NB][Hkv][bs][D], V codes
+    uint8 [NB][Hkv][D][bs] (token tau of a block at position fp8_v_position(tau) of each dim row), scales float32
+    [NB][Hkv][bs] (one per (slot, KV head); value = e4m3 code value * scale); slot_mapping int64 [n]."""
     n, Hkv, D = k_new.shape
     NB, Hkv2, bs, D2 = k_codes.shape
-    if (Hkv2, D2) != (Hkv, D) or v_codes.shape != k_codes.shape or k_scales.shape != (NB, Hkv, bs) or \
+    if (Hkv2, D2) != (Hkv, D) or v_codes.shape != (NB, Hkv, D, bs) or k_scales.shape != (NB, Hkv, bs) or \
             v_scales.shape != k_scales.shape or v_new.shape != k_new.shape or slot_mapping.numel() != n:
         raise ValueError("fp8 cache shapes do not match")
     _check(_lib.kv_append_fp8(
@@ -490,10 +496,11 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: 
                                context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                                workspace: Optional[torch.Tensor], max_context_len: int, blocks_per_split: int = 0,
                                stream=None) -> None:
-    """paged_decode_attention over an fp8 cache layer (codes uint8 [NB][Hkv][bs][D], scales float32 [NB][Hkv][bs])."""
+    """paged_decode_attention over an fp8 cache layer (K codes uint8 [NB][Hkv][bs][D], V codes uint8
+    [NB][Hkv][D][bs] as kv_append_fp8 writes them, scales float32 [NB][Hkv][bs])."""
     B, Hq, D = q.shape
     NB, Hkv, bs, Dk = k_codes.shape
-    if Dk != D or v_codes.shape != k_codes.shape or k_scales.shape != (NB, Hkv, bs) or v_scales.shape != k_scales.shape:
+    if Dk != D or v_codes.shape != (NB, Hkv, D, bs) or k_scales.shape != (NB, Hkv, bs) or v_scales.shape != k_scales.shape:
         raise ValueError("fp8 cache shapes do not match q")
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")

@@ -127,13 +127,19 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __half* __rest
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
     const int64_t dst_row = ((slot / kBlockSize) * Hkv + h) * kBlockSize + slot % kBlockSize;
-    uint8_t* dst = (kv ? v_codes : k_codes) + dst_row * D + lane * PER;
-    const uint32_t c01 = float2_to_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
-    if constexpr (PER == 2) {
-        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c01);
-    } else {
-        const uint32_t c23 = float2_to_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc));
-        *reinterpret_cast<uint32_t*>(dst) = c01 | (c23 << 16);
+    uint32_t codes = float2_to_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
+    if constexpr (PER == 4) codes |= static_cast<uint32_t>(float2_to_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc))) << 16;
+    if (kv == 0) {  // K: the token's row of D codes
+        uint8_t* dst = k_codes + dst_row * D + lane * PER;
+        if constexpr (PER == 2)
+            *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
+        else
+            *reinterpret_cast<uint32_t*>(dst) = codes;
+    } else {  // V: one byte in each of the block's D dim rows of 16 tokens, at the token's position
+        uint8_t* dst = v_codes + ((slot / kBlockSize) * Hkv + h) * static_cast<int64_t>(D) * kBlockSize +
+                       vt_pos(static_cast<int>(slot % kBlockSize));
+#pragma unroll
+        for (int i = 0; i < PER; ++i) dst[(lane * PER + i) * kBlockSize] = static_cast<uint8_t>(codes >> (8 * i));
     }
     if (lane == 0) (kv ? v_scales : k_scales)[dst_row] = sc;
 }

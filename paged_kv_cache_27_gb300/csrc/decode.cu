@@ -139,9 +139,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 // kSuffix: the cascade's suffix pass (per-sequence block offset, partial states only); the plain decode
 // is compiled without either
-// kFp8: the cache holds e4m3 codes with per-row scales (tmK / tmV map the codes); each block's codes are
-// converted to fp16 (exact) in the warp's scratch, the K scale multiplies the scores and the V scale the
-// probabilities before the P V product, so the arithmetic is the fp16 path's
+// kFp8: the cache holds e4m3 codes with per-row scales (tmK / tmV map the codes; V codes are stored per dim,
+// 16 token bytes in the order vt_pos gives).  The mma.sync fragments are read from the code tiles with one
+// 32-bit load per fragment row and converted to fp16 (exact) in registers: for K, the MMA's k index runs over
+// the head dims permuted within each group of 16 so that lane t's four dims are bytes 4t..4t+3 (q's fragments
+// follow the same permutation, which leaves the dot products unchanged); for V the token order of the rows
+// does the same.  The K scale multiplies the scores and the V scale the probabilities before the P V product,
+// so the arithmetic is the fp16 path's
 template <int D, bool kSuffix, bool kFp8 = false>
 __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -233,13 +237,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
             return;
         }
         uint8_t* st = wring + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bar, C::kStageBytes);
+        mbar_arrive_expect_tx(bar, C::kStageBytes + (kFp8 ? 2 * C::kScaleBytes : 0));
         const int y = (phys * p.Hkv + kvh) * kBlockSize;
-        if constexpr (kFp8) {  // K codes, V codes (16 rows x D bytes each), then the 16 K and 16 V scales
+        if constexpr (kFp8) {  // K codes (16 x D bytes), V codes (D x 16 bytes); the 16 K and 16 V scales
+            uint8_t* sc = wring + C::kScaleOff + s * 2 * C::kScaleBytes;
             tma_load_2d(st, &tmK, bar, 0, y, policy);
-            tma_load_2d(st + C::kCodeTileBytes, &tmV, bar, 0, y, policy);
-            bulk_load(st + 2 * C::kCodeTileBytes, p.k_scales + y, C::kScaleBytes, bar);
-            bulk_load(st + 2 * C::kCodeTileBytes + C::kScaleBytes, p.v_scales + y, C::kScaleBytes, bar);
+            tma_load_2d(st + C::kCodeTileBytes, &tmV, bar, 0, (phys * p.Hkv + kvh) * D, policy);
+            bulk_load(sc, p.k_scales + y, C::kScaleBytes, bar);
+            bulk_load(sc + C::kScaleBytes, p.v_scales + y, C::kScaleBytes, bar);
         } else {
 #pragma unroll
             for (int x = 0; x < D; x += 64) {
@@ -284,8 +289,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         const __half* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (row_ok ? g : 0)) * D;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t4) : 0u;
-            qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t4) : 0u;
+            // fp8: k indices 2t, 2t+1 / 2t+8, 2t+9 of the group are dims 4t, 4t+1 / 4t+2, 4t+3 (see above)
+            const int c0 = kFp8 ? 4 * t4 : 2 * t4, c1 = kFp8 ? 4 * t4 + 2 : 8 + 2 * t4;
+            qa[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + c0) : 0u;
+            qa[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + c1) : 0u;
         }
     }
     // fused append: any warp of the last cluster may get the block of position ctx-1; each holds the
@@ -340,96 +347,98 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
             const int phys = s_table[jj - cb0];
             if (phys >= 0 && phys < p.num_blocks) {
                 const int rem = ctx - jj * kBlockSize;  // valid tokens in this block (>= 1)
-                uint32_t kbase, vbase;
                 // scores of tokens g and g+8 carry sl2 (times their K scales with an fp8 cache); the V scales
                 // of tokens g and g+8 (0 past the context) multiply their probabilities before P V
                 float sl2g = sl2, sl2g8 = sl2, vsg = 1.f, vsg8 = 1.f;
-                if constexpr (kFp8) {
-                    const uint8_t* stg = wring + s * C::kStageBytes;
-                    const float* sk = reinterpret_cast<const float*>(stg + 2 * C::kCodeTileBytes);
-                    const float* sv = sk + kBlockSize;
-                    sl2g = sl2 * sk[g];
-                    sl2g8 = sl2 * sk[g + 8];
-                    vsg = g < rem ? sv[g] : 0.f;
-                    vsg8 = g + 8 < rem ? sv[g + 8] : 0.f;
-                    // lane: row lane / 2, half lane % 2 of the K and V code tiles -> fp16 in the swizzle
-                    uint8_t* scr = wring + C::kScratchOff;
-                    const int r = lane >> 1, hf = lane & 1;
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const uint8_t* src = stg + t * C::kCodeTileBytes + r * D + hf * (D / 2);
-                        const uint32_t dst = smem_u32(scr + t * C::kTileBytes);
-#pragma unroll
-                        for (int qq = 0; qq < D / 32; ++qq) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * qq);
-                            const int c0 = hf * (D / 16) + 2 * qq;
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(r, c0)),
-                                         "r"(e4m3x2_to_half2(w.x)), "r"(e4m3x2_to_half2(w.x >> 16)),
-                                         "r"(e4m3x2_to_half2(w.y)), "r"(e4m3x2_to_half2(w.y >> 16))
-                                         : "memory");
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + swz(r, c0 + 1)),
-                                         "r"(e4m3x2_to_half2(w.z)), "r"(e4m3x2_to_half2(w.z >> 16)),
-                                         "r"(e4m3x2_to_half2(w.w)), "r"(e4m3x2_to_half2(w.w >> 16))
-                                         : "memory");
-                        }
-                    }
-                    {
-                        // the stage may be refilled once its scales have been read too
-                        uint32_t dep = 0;
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g8)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg8)));
-                    }
-                    refill(s);  // the stage's codes and scales are read: its next block goes out now
-                    refilled = true;
-                    kbase = smem_u32(scr);
-                    vbase = kbase + C::kTileBytes;
-                } else {
-                    kbase = smem_u32(wring + s * C::kStageBytes);
-                    vbase = kbase + C::kTileBytes;
-                }
-                if (jj == app_blk) {
-                    const int c = lane & 15;
-                    if (c < D / 8) {
-                        const uint32_t a = (lane >= 16 ? vbase : kbase) + swz(app_row, c);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(app_val.x),
-                                     "r"(app_val.y), "r"(app_val.z), "r"(app_val.w)
-                                     : "memory");
-                        __half* dst = (lane >= 16 ? p.v_cache : p.k_cache) +
-                                      ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D + c * 8;
-                        *reinterpret_cast<uint4*>(dst) = app_val;
-                    }
-                    __syncwarp();
-                }
-                // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots ----
-                const int mi = lane >> 3;
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                    mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
-                }
                 // rows of V past the context may hold any bits (even NaN): zero them in registers
                 uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
                 if (rem < kBlockSize) {
                     keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
                     keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
                 }
-#if KVC_DEC_EARLY_REFILL
-                // V^T fragments now; the stage is then free and its refill goes out before the softmax
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
                 uint32_t va[D / 16][4];
+                uint32_t vbase = 0;
+                const int mi = lane >> 3;
+                if constexpr (kFp8) {
+                    const uint8_t* kt = wring + s * C::kStageBytes;  // K codes, a (swizzled) row per token
+                    const uint8_t* vt = kt + C::kCodeTileBytes;       // V codes, a row of 16 tokens per dim
+                    const float* sk = reinterpret_cast<const float*>(wring + C::kScaleOff + s * 2 * C::kScaleBytes);
+                    const float* sv = sk + kBlockSize;
+                    sl2g = sl2 * sk[g];
+                    sl2g8 = sl2 * sk[g + 8];
+                    vsg = g < rem ? sv[g] : 0.f;
+                    vsg8 = g + 8 < rem ? sv[g + 8] : 0.f;
+                    // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots; lane (g, t) reads
+                    // dims 4t..4t+3 of the group for tokens g and g+8 ----
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), va[mt][0], va[mt][1],
-                              va[mt][2], va[mt][3]);
-                    va[mt][0] &= keep0;
-                    va[mt][1] &= keep0;
-                    va[mt][2] &= keep1;
-                    va[mt][3] &= keep1;
-                }
-                if constexpr (!kFp8) {
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + code_swz<D>(g, 16 * ks + 4 * t4));
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + code_swz<D>(g + 8, 16 * ks + 4 * t4));
+                        mma_f16_16816(sc, e4m3x2_to_half2(w0), e4m3x2_to_half2(w1), e4m3x2_to_half2(w0 >> 16),
+                                      e4m3x2_to_half2(w1 >> 16), qa[ks][0], qa[ks][1]);
+                    }
+                    // V^T fragments: dims g, g+8 of each group of 16, tokens 2t, 2t+1 | 2t+8, 2t+9 (bytes 4t..4t+3)
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + (16 * mt + g) * kBlockSize + 4 * t4);
+                        const uint32_t w1 =
+                            *reinterpret_cast<const uint32_t*>(vt + (16 * mt + g + 8) * kBlockSize + 4 * t4);
+                        va[mt][0] = e4m3x2_to_half2(w0) & keep0;
+                        va[mt][1] = e4m3x2_to_half2(w1) & keep0;
+                        va[mt][2] = e4m3x2_to_half2(w0 >> 16) & keep1;
+                        va[mt][3] = e4m3x2_to_half2(w1 >> 16) & keep1;
+                    }
+                    {
+                        // the stage may be refilled once its codes and scales are in registers
+                        uint32_t dep = 0;
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g8)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg)));
+                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg8)));
+                    }
+                    refill(s);
+                    refilled = true;
+                } else {
+                    const uint32_t kbase = smem_u32(wring + s * C::kStageBytes);
+                    vbase = kbase + C::kTileBytes;
+                    if (jj == app_blk) {
+                        const int c = lane & 15;
+                        if (c < D / 8) {
+                            const uint32_t a = (lane >= 16 ? vbase : kbase) + swz(app_row, c);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(app_val.x),
+                                         "r"(app_val.y), "r"(app_val.z), "r"(app_val.w)
+                                         : "memory");
+                            __half* dst = (lane >= 16 ? p.v_cache : p.k_cache) +
+                                          ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D +
+                                          c * 8;
+                            *reinterpret_cast<uint4*>(dst) = app_val;
+                        }
+                        __syncwarp();
+                    }
+                    // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots ----
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                        mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
+                    }
+#if KVC_DEC_EARLY_REFILL
+                    // V^T fragments now; the stage is then free and its refill goes out before the softmax
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), va[mt][0], va[mt][1],
+                                  va[mt][2], va[mt][3]);
+                        va[mt][0] &= keep0;
+                        va[mt][1] &= keep0;
+                        va[mt][2] &= keep1;
+                        va[mt][3] &= keep1;
+                    }
                     // the copy may overwrite the stage only once the warp's reads of it have returned: fold
                     // the loaded registers (the K fragments were consumed by the S products above)
                     uint32_t dep = 0;
@@ -439,8 +448,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                         for (int k = 0; k < 4; ++k) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
                     refill(s);
                     refilled = true;
-                }
 #endif
+                }
                 // ---- online softmax per head (column): this lane holds tokens g, g+8 of heads 2*t4, 2*t4+1 ----
                 float x[4];
                 x[0] = g < rem ? sc[0] * sl2g : -INFINITY;
@@ -478,15 +487,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                 // ---- O^T += V^T P^T, one m-tile per 16 dims ----
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
-#if KVC_DEC_EARLY_REFILL
-                    const uint32_t a0 = va[mt][0], a1 = va[mt][1], a2 = va[mt][2], a3 = va[mt][3];
-#else
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                    a0 &= keep0;
-                    a1 &= keep0;
-                    a2 &= keep1;
-                    a3 &= keep1;
+                    uint32_t a0 = va[mt][0], a1 = va[mt][1], a2 = va[mt][2], a3 = va[mt][3];
+#if !KVC_DEC_EARLY_REFILL
+                    if constexpr (!kFp8) {
+                        ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                        a0 &= keep0;
+                        a1 &= keep0;
+                        a2 &= keep1;
+                        a3 &= keep1;
+                    }
 #endif
                     mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
                     mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
@@ -857,7 +866,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     CUtensorMap tmK, tmV;
     e = fp8 ? make_code_map(&tmK, a.k_codes, D, rows) : make_tile_map(&tmK, a.k_cache, D, rows);
     if (e != cudaSuccess) return e;
-    e = fp8 ? make_code_map(&tmV, a.v_codes, D, rows) : make_tile_map(&tmV, a.v_cache, D, rows);
+    e = fp8 ? make_vt_code_map(&tmV, a.v_codes, D, rows / kBlockSize * D) : make_tile_map(&tmV, a.v_cache, D, rows);
     if (e != cudaSuccess) return e;
 
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;

@@ -55,8 +55,9 @@ constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
 constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
 
 // Tile configuration per head dim. With kFp8 the cache holds e4m3 codes and a float scale per (token, KV
-// head) row: a stage is the block's K codes, V codes, K scales and V scales, and every warp also owns a
-// scratch pair of fp16 tiles (the codes converted, in the 128-byte swizzle the fp16 stages have).
+// head) row: a stage is the block's K codes (16 token rows of D bytes, in the swizzle of a D-byte row) and V
+// codes (D dim rows of 16 token bytes), and the warp's ring ends with the stages' K and V scales.  The codes
+// go from shared memory straight into the mma.sync fragments (one 32-bit load per fragment row).
 template <int D, bool kFp8 = false>
 struct DecodeCfg {
     static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
@@ -66,10 +67,12 @@ struct DecodeCfg {
     static constexpr int kTileBytes = kBlockSize * D * 2;    // one 16 x D fp16 tile
     static constexpr int kCodeTileBytes = kBlockSize * D;    // one 16 x D e4m3 tile
     static constexpr int kScaleBytes = kBlockSize * 4;       // 16 float scales
-    static constexpr int kStageBytes = kFp8 ? 2 * kCodeTileBytes + 2 * kScaleBytes  // K, V codes; K, V scales
-                                            : 2 * kTileBytes;                           // K tile + V tile
-    static constexpr int kScratchOff = kFp8 ? (kStages * kStageBytes + 127) / 128 * 128 : 0;
-    static constexpr int kWarpRingBytes = kFp8 ? kScratchOff + 2 * kTileBytes : kStages * kStageBytes;
+    static constexpr int kStageBytes = kFp8 ? 2 * kCodeTileBytes  // K codes, V codes
+                                            : 2 * kTileBytes;     // K tile + V tile
+    static constexpr int kScaleOff = kStages * kStageBytes;       // fp8: per stage, 16 K then 16 V scales
+    // a warp's ring starts on a 1024-byte boundary (the swizzle patterns repeat every 1024 bytes)
+    static constexpr int kWarpRingBytes = kFp8 ? (kScaleOff + kStages * 2 * kScaleBytes + 1023) / 1024 * 1024
+                                               : kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     static constexpr int kBarBytes = kWarps * kStages * 8;
     static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA
@@ -158,8 +161,9 @@ inline cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 2-D view of one layer's e4m3 code pool: rows of D bytes, boxes of 16 rows x D bytes, no swizzle (the codes
-// are converted into swizzled fp16 tiles in shared memory).
+// 2-D view of one layer's e4m3 K code pool: rows of D bytes (one per (block, KV head, token)), boxes of 16
+// rows, swizzled so that the 16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3) (64-byte rows) or
+// c ^ (r & 7) (128-byte rows): the fragment loads of 8 rows x 4 lanes then hit 32 different banks.
 inline cudaError_t make_code_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -168,10 +172,31 @@ inline cudaError_t make_code_map(CUtensorMap* map, const void* base, int D, int6
     cuuint32_t box[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlockSize)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+// 2-D view of one layer's e4m3 V code pool: rows of 16 token bytes (one per (block, KV head, dim)), boxes of D
+// rows (the block's V^T for one KV head), no swizzle.
+inline cudaError_t make_vt_code_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kBlockSize), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kBlockSize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockSize), static_cast<cuuint32_t>(D)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+// byte offset of byte x of row r in a K code tile as the map above writes it
+template <int D>
+__device__ __forceinline__ uint32_t code_swz(int r, int x) {
+    const int sw = D == 64 ? ((r >> 1) & 3) : (r & 7);
+    return static_cast<uint32_t>(r * D + ((((x >> 4) ^ sw) << 4) | (x & 15)));
+}
+
 
 template <typename Kern, typename... Args>
 inline cudaError_t launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,

@@ -17,6 +17,9 @@ cudaError_t device_error_word(unsigned** ptr);
 cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_t* slots, int n, __half* k_layer,
                           __half* v_layer, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream);
 // quantizing append: e4m3 codes [NB][Hkv][16][D] and one float scale per (slot, KV head) row
+// fp8 V code pool: per (block, KV head), D rows (one per dim) of 16 token codes; token tau (0..15) sits at byte
+// vt_pos(tau) of its row, so that the mma.sync fragment of lane t (tokens 2t, 2t+1, 2t+8, 2t+9) is the 4 bytes at 4t
+__host__ __device__ constexpr int vt_pos(int tau) { return 4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1); }
 cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const int64_t* slots, int n,
                               uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales, int num_blocks,
                               int Hkv, int D, unsigned* err, cudaStream_t stream);

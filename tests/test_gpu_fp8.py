@@ -20,6 +20,25 @@ def used_slots(wl):
     return np.array(slots, dtype=np.int64)
 
 
+# the fp8 V pool's layout as the header states it: per (block, KV head), a row of 16 token codes per dim, token
+# tau at byte 4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1)
+VT_POS = np.array([4 * ((t & 7) >> 1) + 2 * (t >> 3) + (t & 1) for t in range(16)])
+
+
+def v_natural(vc):
+    """Device V codes [NB][Hkv][D][16] -> [NB][Hkv][16][D] in token order (host numpy)."""
+    v = vc.cpu().numpy()
+    return np.ascontiguousarray(v[:, :, :, VT_POS].transpose(0, 1, 3, 2))
+
+
+def test_v_positions_are_a_permutation():
+    import paged_kv_cache_27_gb300 as kvc
+    assert sorted(VT_POS) == list(range(16))
+    assert [kvc.fp8_v_position(t) for t in range(16)] == list(VT_POS)
+    for t in range(4):  # lane t's mma fragment (tokens 2t, 2t+1, 2t+8, 2t+9) is bytes 4t..4t+3
+        assert [VT_POS[2 * t], VT_POS[2 * t + 1], VT_POS[2 * t + 8], VT_POS[2 * t + 9]] == [4 * t + i for i in range(4)]
+
+
 def quantized_cache(wl, dev="cuda"):
     """The workload's used rows quantized on the GPU into NaN-poisoned fp8 pools; returns device codes/scales
     and the host rows that were appended."""
@@ -30,7 +49,7 @@ def quantized_cache(wl, dev="cuda"):
     v_rows = wl.v_pool[blk, :, off]
     shape = wl.k_pool.shape
     kc = torch.full(shape, 0x7F, dtype=torch.uint8, device=dev)  # 0x7F is an e4m3 NaN
-    vc = torch.full(shape, 0x7F, dtype=torch.uint8, device=dev)
+    vc = torch.full(shape[:2] + (shape[3], shape[2]), 0x7F, dtype=torch.uint8, device=dev)
     ks = torch.full(shape[:3], float("nan"), dtype=torch.float32, device=dev)
     vs = torch.full(shape[:3], float("nan"), dtype=torch.float32, device=dev)
     kvc.kv_append_fp8(torch.from_numpy(np.ascontiguousarray(k_rows)).to(dev),
@@ -55,8 +74,7 @@ def test_append_fp8_bit_exact(D):
     blk, off = slots // wl.bs, slots % wl.bs
     used = np.zeros(wl.k_pool.shape[:3], bool)
     used[blk, :, off] = True
-    for got, ref in ((kc, rk), (vc, rv)):
-        g = got.cpu().numpy()
+    for g, ref in ((kc.cpu().numpy(), rk), (v_natural(vc), rv)):
         assert np.array_equal(g[used], ref[used])
         assert np.all(g[~used] == 0x7F)  # untouched rows keep the poison
     for got, ref in ((ks, rks), (vs, rvs)):
@@ -101,7 +119,7 @@ def test_decode_fp8_matches_oracle(case, out_dtype):
                                    torch.full((max(ws, 16),), 0x7F, dtype=torch.uint8, device=dev), max_ctx, bps)
     torch.cuda.synchronize()
     assert kvc.kvc_device_error_flags(clear=True) == 0
-    ref = oracle.decode_fp8(wl.q[:, 0], kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy(),
+    ref = oracle.decode_fp8(wl.q[:, 0], kc.cpu().numpy(), v_natural(vc), ks.cpu().numpy(), vs.cpu().numpy(),
                             wl.block_table, wl.ctx, wl.scale)
     check_attention(out, ref, f"fp8 decode case {case}")
 
@@ -119,6 +137,6 @@ def test_decode_fp8_config2_shape():
                                    torch.from_numpy(wl.ctx).to(dev), wl.scale, out,
                                    torch.empty(max(ws, 16), dtype=torch.uint8, device=dev), 2048)
     torch.cuda.synchronize()
-    ref = oracle.decode_fp8(wl.q[:, 0], kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy(),
+    ref = oracle.decode_fp8(wl.q[:, 0], kc.cpu().numpy(), v_natural(vc), ks.cpu().numpy(), vs.cpu().numpy(),
                             wl.block_table, wl.ctx, wl.scale)
     check_attention(out, ref, "fp8 decode, 32 x 2048")
