@@ -53,6 +53,7 @@ struct DecodeKernelParams {
     const __half* v_new;
     __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
     __half* v_cache;
+    const uint8_t* v_codes;  // fp8: the layer's V code pool (a block's codes for one KV head are contiguous)
     const __half* k_next;  // the next layer's pools (accepted, unused: the L2 prefetch measured no gain)
     const __half* v_next;
     const int32_t* block_table;
@@ -242,7 +243,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         if constexpr (kFp8) {  // K codes (16 x D bytes), V codes (D x 16 bytes); the 16 K and 16 V scales
             uint8_t* sc = wring + C::kScaleOff + s * 2 * C::kScaleBytes;
             tma_load_2d(st, &tmK, bar, 0, y, policy);
-            tma_load_2d(st + C::kCodeTileBytes, &tmV, bar, 0, (phys * p.Hkv + kvh) * D, policy);
+            bulk_load(st + C::kCodeTileBytes, p.v_codes + static_cast<int64_t>(phys * p.Hkv + kvh) * D * kBlockSize,
+                      C::kCodeTileBytes, bar);
             bulk_load(sc, p.k_scales + y, C::kScaleBytes, bar);
             bulk_load(sc + C::kScaleBytes, p.v_scales + y, C::kScaleBytes, bar);
         } else {
@@ -307,6 +309,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     }
 
     int next_j = cb0 + gw + ST * nwarps_cl;  // fixed round-robin: this warp's blocks are gw mod (warps)
+    // fp8: byte offsets in a K code tile of lane (g, t)'s 4 codes per 16-dim group, row g (row g + 8 is 8 * D
+    // further: its swizzle term is the same)
+    uint32_t koff[D / 16];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) koff[ks] = code_swz<D>(g, 16 * ks + 4 * t4);
 
     // O^T accumulators: o[mt] = dims mt*16 + g (+8) x heads 2*t4, 2*t4+1; running max / sum per head pair
     float o[D / 16][4];
@@ -373,8 +380,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                     // dims 4t..4t+3 of the group for tokens g and g+8 ----
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + code_swz<D>(g, 16 * ks + 4 * t4));
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + code_swz<D>(g + 8, 16 * ks + 4 * t4));
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + koff[ks]);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + koff[ks] + 8 * D);
                         mma_f16_16816(sc, e4m3x2_to_half2(w0), e4m3x2_to_half2(w1), e4m3x2_to_half2(w0 >> 16),
                                       e4m3x2_to_half2(w1 >> 16), qa[ks][0], qa[ks][1]);
                     }
@@ -384,23 +391,32 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                         const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + (16 * mt + g) * kBlockSize + 4 * t4);
                         const uint32_t w1 =
                             *reinterpret_cast<const uint32_t*>(vt + (16 * mt + g + 8) * kBlockSize + 4 * t4);
-                        va[mt][0] = e4m3x2_to_half2(w0) & keep0;
-                        va[mt][1] = e4m3x2_to_half2(w1) & keep0;
-                        va[mt][2] = e4m3x2_to_half2(w0 >> 16) & keep1;
-                        va[mt][3] = e4m3x2_to_half2(w1 >> 16) & keep1;
+                        va[mt][0] = e4m3x2_to_half2(w0);
+                        va[mt][1] = e4m3x2_to_half2(w1);
+                        va[mt][2] = e4m3x2_to_half2(w0 >> 16);
+                        va[mt][3] = e4m3x2_to_half2(w1 >> 16);
+                    }
+                    if (rem < kBlockSize) {
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            va[mt][0] &= keep0;
+                            va[mt][1] &= keep0;
+                            va[mt][2] &= keep1;
+                            va[mt][3] &= keep1;
+                        }
                     }
                     {
                         // the stage may be refilled once its codes and scales are in registers
                         uint32_t dep = 0;
 #pragma unroll
-                        for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(sl2g8)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg)));
-                        asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(__float_as_uint(vsg8)));
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(dep) : "r"(va[mt][0]), "r"(va[mt][1]));
+                            asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(dep) : "r"(va[mt][2]), "r"(va[mt][3]));
+                        }
+                        asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(dep)
+                                     : "r"(__float_as_uint(sl2g)), "r"(__float_as_uint(sl2g8)));
+                        asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(dep)
+                                     : "r"(__float_as_uint(vsg)), "r"(__float_as_uint(vsg8)));
                     }
                     refill(s);
                     refilled = true;
@@ -849,6 +865,7 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.blk_off = nullptr;
     p.k_scales = a.k_scales;
     p.v_scales = a.v_scales;
+    p.v_codes = static_cast<const uint8_t*>(a.v_codes);
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kLog2e;
     static std::atomic<unsigned> launch_seq{0};
@@ -866,7 +883,8 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     CUtensorMap tmK, tmV;
     e = fp8 ? make_code_map(&tmK, a.k_codes, D, rows) : make_tile_map(&tmK, a.k_cache, D, rows);
     if (e != cudaSuccess) return e;
-    e = fp8 ? make_vt_code_map(&tmV, a.v_codes, D, rows / kBlockSize * D) : make_tile_map(&tmV, a.v_cache, D, rows);
+    // fp8: V codes come by bulk copy (a block's V^T for one KV head is 16 * D contiguous bytes); tmV is unused
+    e = fp8 ? make_code_map(&tmV, a.k_codes, D, rows) : make_tile_map(&tmV, a.v_cache, D, rows);
     if (e != cudaSuccess) return e;
 
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;

@@ -55,8 +55,9 @@ constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
 constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
 
 // Tile configuration per head dim. With kFp8 the cache holds e4m3 codes and a float scale per (token, KV
-// head) row: a stage is the block's K codes (16 token rows of D bytes, in the swizzle of a D-byte row) and V
-// codes (D dim rows of 16 token bytes), and the warp's ring ends with the stages' K and V scales.  The codes
+// head) row: a stage is the block's K codes (16 token rows of D bytes, in the swizzle of a D-byte row, by TMA)
+// and V codes (D dim rows of 16 token bytes, one bulk copy), and the warp's ring ends with the stages' K and V
+// scales.  The codes
 // go from shared memory straight into the mma.sync fragments (one 32-bit load per fragment row).
 template <int D, bool kFp8 = false>
 struct DecodeCfg {
@@ -174,20 +175,6 @@ inline cudaError_t make_code_map(CUtensorMap* map, const void* base, int D, int6
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-// 2-D view of one layer's e4m3 V code pool: rows of 16 token bytes (one per (block, KV head, dim)), boxes of D
-// rows (the block's V^T for one KV head), no swizzle.
-inline cudaError_t make_vt_code_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kBlockSize), static_cast<cuuint64_t>(rows)};
-    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kBlockSize)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockSize), static_cast<cuuint32_t>(D)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 // byte offset of byte x of row r in a K code tile as the map above writes it
