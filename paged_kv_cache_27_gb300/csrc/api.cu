@@ -731,7 +731,7 @@ kvc_status prefill_attention_ex(const void* q, const void* k, const void* v, con
     if (!q || !k || !v || !cu_seqlens || !out) return fail(KVC_ERR_INVALID, "null pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(KVC_ERR_INVALID, "q, k, v and out must be 16-byte aligned");
-    if (static_cast<int64_t>(nseq) * ((max_seqlen + 255) / 256) * Hq > 2147483647LL)
+    if (static_cast<int64_t>(nseq) * ((max_seqlen + 127) / 128) * Hq > 2147483647LL)
         return fail(KVC_ERR_UNSUPPORTED, "grid too large");
     if (g_checked.load()) {
         std::vector<int32_t> cu;

@@ -141,5 +141,7 @@ struct PrefillArgs {
     unsigned* err;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// head dim 64: one 128-row query tile per CTA, S double-buffered in TMEM (prefill_1t.cu)
+cudaError_t launch_prefill_1t(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace kvc

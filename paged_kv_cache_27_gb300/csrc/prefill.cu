@@ -7,21 +7,22 @@
 // KV head h / (Hq / Hkv).  Per row: softmax(q K^T * scale) V, with the
 // running-max / exp-sum rule of the FlashAttention article over key tiles.
 //
-// Design: one CTA per (256 query rows of a segment, query head) = two 128-row query tiles A and B that
-// share every K/V tile; nine warps.  Lane 0 of warp 8 issues every TMA copy and every tcgen05.mma; warps
-// 0-3 own tile A's rows and warps 4-7 tile B's (thread = row = TMEM lane) and run the softmax.  Per
-// 64-key tile j and query tile X:
-//   S_X = Q_X K^T   tcgen05.mma M=128 x N=64, Q and K K-major in shared memory (128-byte swizzle, as
-//                   TMA writes them), fp32 accumulator in TMEM
-//   softmax         the row threads read S_X from TMEM, mask only on tiles that cross the causal diagonal
-//                   or the segment end, keep the running max until it has grown by 2^8 (then rescale O_X
-//                   in TMEM), and write P_X = hi + lo (two fp16 parts, so the product keeps ~fp32
-//                   accuracy) to shared memory, K-major
-//   O_X += P_X V    tcgen05.mma M=128 x N=64 per 64-dim chunk, V MN-major; O_X stays in TMEM
-// The products go out in the order S_A(j+1), S_B(j+1), P_A V(j), P_B V(j): while one group of row warps
-// runs its softmax, the tensor cores work on the other group's products, and each group's S(j+1) runs
-// during its own softmax(j).  K and V have three-stage rings of their own.  Every wait is bounded; a
-// timeout sets an error bit and drains the CTA.
+// Design (head dim 128; head dim 64 runs prefill_1t.cu): one CTA per (256 query rows of a segment, query
+// head) = two 128-row query tiles A and B that share every K/V tile; ten warps.  Warps 0-3 own tile A's rows
+// and warps 4-7 tile B's (thread = row = TMEM lane) and run the softmax; lane 0 of warp 8 issues every
+// tcgen05.mma, lane 0 of warp 9 every TMA copy.  Per 128-key tile j and query tile X:
+//   S_X = Q_X K^T   tcgen05.mma M=128 x N=128, Q and K K-major in shared memory (128-byte swizzle, as TMA
+//                   writes them), fp32 accumulator in TMEM
+//   softmax         the row threads read S_X from TMEM one 64-key half at a time, mask only on tiles that
+//                   cross the causal diagonal or the segment end, keep the running max until it has grown by
+//                   2^8 (then rescale O_X in TMEM), and write P_X over S_X in fp16 (or as an fp16 high part and
+//                   residual, so the product keeps ~fp32 weights)
+//   O_X += P_X V    tcgen05.mma M=128 x N=D with P read from TMEM (the A operand) and V MN-major in shared
+//                   memory; O_X stays in TMEM
+// The products go out in the order P_A V(j), S_A(j+1), P_B V(j), S_B(j+1): S_X(j+1) reuses P_X(j)'s columns,
+// so it waits for the commit of P_X V(j); while one group of row warps runs its softmax, the tensor cores work
+// on the other group's products.  K and V have rings of their own.  Every wait is bounded; a timeout sets an
+// error bit and drains the CTA.
 #include <algorithm>
 #include <cmath>
 #include <cudaTypedefs.h>
@@ -610,9 +611,8 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (a.nseq <= 0 || a.total_tokens <= 0 || a.max_seqlen <= 0) return cudaSuccess;
+    if (a.D == 64) return launch_prefill_1t(a, stream);  // one query tile per CTA (prefill_1t.cu)
     switch (a.D * 2 + (a.split_p ? 1 : 0)) {
-        case 128: return launch_prefill_d<64, false>(a, stream);
-        case 129: return launch_prefill_d<64, true>(a, stream);
         case 256: return launch_prefill_d<128, false>(a, stream);
         case 257: return launch_prefill_d<128, true>(a, stream);
         default: return cudaErrorInvalidValue;
