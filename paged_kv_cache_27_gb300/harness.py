@@ -125,7 +125,10 @@ class DecodeSession:
 
 
 def serving_mix(mix, device="cuda", out_dtype=torch.float32, poison=True):
-    """The serving-mix protocol on the library's block pool (see the design doc for the protocol).
+    """The serving-mix protocol on the library's block pool: groups of `mix.group` sequences share the blocks of a
+    common prompt prefix (refcounted, allocated once per group), each sequence owns the blocks of its private
+    tail, and one decode step appends a token per sequence — a sequence whose last block is shared gets a
+    private copy first (copy-on-write) — and then runs paged decode over the new tables.
 
     Returns a dict: block tables before/after the step, copy pairs, slots, pools and the output."""
     bs = mix.bs
