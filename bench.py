@@ -194,7 +194,7 @@ def run_reference(args):
         return 0
     import oracle
     import workloads
-    wl = workloads.config2(L=1)
+    wl = workloads.model_decode_step(L=1)
     seqs = 8
     cores = oracle.default_threads()
     for _ in range(args.warmup):
@@ -233,7 +233,7 @@ def run_ours(args):
     from paged_kv_cache_27_gb300.harness import DecodeSession, _dev
     import workloads
 
-    wl = workloads.config2()
+    wl = workloads.model_decode_step()
     sess = DecodeSession(wl, device=device, out_dtype=torch.float16, blocks_per_split=args.blocks_per_split).fill()
     ctx_total = int(wl.ctx.astype(np.int64).sum())
     nblocks_total = int(sum(-(-int(c) // 16) for c in wl.ctx))
@@ -459,8 +459,8 @@ def run_suite_decode(device, stream, flush, emit, peak):
     import workloads
     from paged_kv_cache_27_gb300 import harness
 
-    # config 1: one sequence at context 256 (L2-resident, latency-bound)
-    wl = workloads.config1()
+    # one sequence at context 256 (L2-resident, latency-bound)
+    wl = workloads.single_sequence_256()
     sess = harness.DecodeSession(wl, device=device, out_dtype=torch.float32).fill()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
@@ -474,12 +474,12 @@ def run_suite_decode(device, stream, flush, emit, peak):
         g.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    emit({"config": "1: B=1, 1 q / 1 KV head, D=64, context 256", "us_per_decode": e0.elapsed_time(e1) * 1e3 / 1000,
+    emit({"config": "single sequence: B=1, 1 q / 1 KV head, D=64, context 256", "us_per_decode": e0.elapsed_time(e1) * 1e3 / 1000,
           "note": "100 back-to-back calls in a CUDA graph; latency-bound, the 64 KiB context sits in L2"})
     sess.close()
 
-    # config 3: 200 sequences, groups of 8 share a 512-token prefix (refcounted blocks)
-    mix = workloads.config3()
+    # shared-prefix serving mix: 200 sequences, groups of 8 share a 512-token prefix (refcounted blocks)
+    mix = workloads.shared_prefix_mix()
     res = harness.serving_mix(mix, device=device, poison=False)
     table = torch.from_numpy(res["block_table"]).to(device)
     ctx = torch.from_numpy(mix.ctx).to(device)
@@ -498,14 +498,14 @@ def run_suite_decode(device, stream, flush, emit, peak):
     for b in range(mix.B):
         used.update(res["block_table"][b, :-(-int(mix.ctx[b]) // 16)].tolist())
     unique = len(used) * 16 * row
-    emit({"config": "3: B=200, 14 q / 2 KV heads, D=64, ctx ~ U{16..4096}, groups of 8 share a 512-token prefix",
+    emit({"config": "shared-prefix serving mix: B=200, 14 q / 2 KV heads, D=64, ctx ~ U{16..4096}, groups of 8 share a 512-token prefix",
           "us_per_step": us, "tokens_per_s": mix.B / (us * 1e-6),
           "logical_GBps": logical / (us * 1e-6) / 1e9, "unique_GBps": unique / (us * 1e-6) / 1e9,
           "logical_bytes": logical, "unique_bytes": unique, "pct_hbm_peak_unique": unique / (us * 1e-6) / 1e9 / peak * 100,
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
                   "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
 
-    # config 3, attention only: the plain decode vs the cascade (each group's shared prefix read once)
+    # the shared-prefix mix, attention only: the plain decode vs the cascade (each group's shared prefix read once)
     _, _, pws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
     pwsb = torch.zeros(max(pws, 16), dtype=torch.uint8, device=device)
     plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, pwsb,
@@ -565,7 +565,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
         del kp, vp
 
     # quantized cache (NEXT-4): 24-layer decode-only graphs with launch overlap, fp16 pools vs the same pools
-    # quantized to fp8 e4m3 with per-row scales (config 2 shape: 32 x 2048, 14 / 2 heads, D = 64)
+    # quantized to fp8 e4m3 with per-row scales (the model step's shape: 32 x 2048, 14 / 2 heads, D = 64)
     Lq, Bq, Cq = 24, 32, 2048
     kp0, vp0, tbq, ctq, _, _, _ = _decode_state(Bq, Cq, 14, 2, 64, device, seed=2024)
     NBq = kp0.shape[0]
@@ -666,7 +666,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
               "kv_bytes": nbytes})
         del kp, vp
 
-    # config 4: long contexts, B in {1, 4, 16} x ctx in {4k, 16k, 64k, 128k}
+    # long contexts, B in {1, 4, 16} x ctx in {4k, 16k, 64k, 128k}
     for B in (1, 4, 16):
         for c in (4096, 16384, 65536, 131072):
             kp, vp, tb, ct, q4, kn4, vn4 = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
@@ -676,7 +676,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
             fn = lambda: kvc.paged_decode_append_attention(q4, kn4, vn4, kp, vp, tb, ct, 0.125, o4, w4, c)
             us = _timed_calls(fn, 20, flush, stream)
             nbytes = B * c * 2 * 2 * 64 * 2
-            emit({"config": f"4: B={B}, ctx={c}, 14 q / 2 KV heads, D=64", "us_per_call": us,
+            emit({"config": f"long context: B={B}, ctx={c}, 14 q / 2 KV heads, D=64", "us_per_call": us,
                   "GBps": nbytes / (us * 1e-6) / 1e9, "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100,
                   "splits": ns, "blocks_per_split": bps, "kv_bytes": nbytes})
             del kp, vp
@@ -687,7 +687,7 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
     import torch
     import paged_kv_cache_27_gb300 as kvc
 
-    # config 5 and larger prefill shapes: causal varlen prefill on the tensor cores
+    # prefill shapes: causal varlen prefill on the tensor cores
     def prefill_case(name, seqlens, Hq, Hkv, D, causal=True, precise=False):
         T = sum(seqlens)
         gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
@@ -708,8 +708,8 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
               "note": "algorithmic flops (masked half not counted)" + (
                   "; the split form's tensor work is 1.5x that (P V runs for both parts of P)" if precise else "")})
 
-    prefill_case("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal", (37, 120, 8, 200), 8, 8, 64)
-    prefill_case("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2, 64)
+    prefill_case("varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal", (37, 120, 8, 200), 8, 8, 64)
+    prefill_case("GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2, 64)
     prefill_case("supplementary (not a listed config): varlen x16, seqlens 592/1920/128/3200, 8/8, D=64, causal",
                  (592, 1920, 128, 3200), 8, 8, 64)
     prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",

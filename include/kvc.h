@@ -60,7 +60,7 @@ typedef enum {
     KVC_ERR_OOM = 2,         /* the block pool has no free block ("OOM -- no free pages") */
     KVC_ERR_CAPACITY = 3,    /* a position/context beyond the block table or the pool */
     KVC_ERR_CUDA = 4,        /* a CUDA runtime call failed */
-    KVC_ERR_UNSUPPORTED = 5  /* a shape this build does not compile (head_dim, block_size, group) */
+    KVC_ERR_UNSUPPORTED = 5  /* a shape the library has no kernel for (head_dim, block_size, group) */
 } kvc_status;
 
 typedef enum { KVC_F16 = 0, KVC_F32 = 1 } kvc_dtype;

@@ -162,7 +162,7 @@ def run_protocol_host(mix):
                                 dict(B=37, group=8, prefix_len=48, ctx_lo=1, ctx_hi=90),
                                 dict()])
 def test_step_prepare_matches_oracle_protocol(kw):
-    mix = workloads.config3(**kw)
+    mix = workloads.shared_prefix_mix(**kw)
     table, slots, copies, rc = run_protocol_host(mix)
     ref = opaging.serving_mix(mix) if mix.B <= 40 else None
     if ref is None:

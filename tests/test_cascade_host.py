@@ -99,10 +99,10 @@ def test_groups_of_generated_structures():
 
 
 def test_groups_on_serving_mix_tables():
-    """Config 3 after its step (the oracle's pool protocol): groups of at most 8 that share the prefix
+    """The shared-prefix mix after its step (the oracle's pool protocol): groups of at most 8 that share the prefix
     blocks the copy-on-write left shared."""
     import paged_kv_cache_27_gb300 as kvc
-    mix = workloads.config3()
+    mix = workloads.shared_prefix_mix()
     ref = opaging.serving_mix(mix)
     table = ref["block_table"]
     gs, sh, mx = kvc.kv_cascade_groups(table, mix.ctx)

@@ -73,10 +73,10 @@ def test_cascade_matches_oracle(case, out_dtype):
 
 
 def test_cascade_serving_mix():
-    """Config 3 after its step: the groups the pool left sharing their prefix blocks, read once each."""
+    """The shared-prefix mix after its step: the groups the pool left sharing their prefix blocks, read once each."""
     import paged_kv_cache_27_gb300 as kvc
     from paged_kv_cache_27_gb300 import harness
-    mix = workloads.config3()
+    mix = workloads.shared_prefix_mix()
     got = harness.serving_mix(mix)
     ref = opaging.serving_mix(mix)
     table = got["block_table"]

@@ -52,8 +52,8 @@ def check_workload(kvc, wl, out_dtype=torch.float32, bps=0, layers=None, cache_b
     return max(errs)
 
 
-def test_config1_single_sequence(kvc):
-    wl = workloads.config1()
+def test_single_sequence_256(kvc):
+    wl = workloads.single_sequence_256()
     for dt in (torch.float32, torch.float16):
         check_workload(kvc, wl, dt)
     # the cached row equals the last row of the full 256 x 256 causal recompute
@@ -63,7 +63,7 @@ def test_config1_single_sequence(kvc):
     Q = np.zeros_like(K)
     Q[-1] = wl.q[0, 0, 0].astype(np.float64)
     full = oracle.causal_attention(Q, K, V, wl.scale)
-    check_attention(s.out[0, 0], full[-1:], "config 1 vs 256x256 causal")
+    check_attention(s.out[0, 0], full[-1:], "single sequence vs 256x256 causal")
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,ctx", [
@@ -98,24 +98,24 @@ def test_long_context_cluster_slices(kvc, bps):
     check_workload(kvc, wl, torch.float32, bps=bps, fused=True)
 
 
-def test_config2_full_as_benchmarked(kvc):
+def test_model_step_full_as_benchmarked(kvc):
     """24 layers x 32 sequences x context 2048, 14 q / 2 KV heads, in the benchmark's launch configuration
     (fused append + decode, CUDA graph, launch overlap): every layer and the whole cache against the oracle."""
-    wl = workloads.config2()
+    wl = workloads.model_decode_step()
     err = check_workload(kvc, wl, torch.float16, layers=range(wl.L), cache_bits=True, fused=True, graph=True,
                          overlap=True)
     assert err < 2e-3
 
 
-def test_config2_fp32_out_unfused_sampled_layers(kvc):
-    wl = workloads.config2()
+def test_model_step_fp32_out_unfused_sampled_layers(kvc):
+    wl = workloads.model_decode_step()
     check_workload(kvc, wl, torch.float32, layers=[0, 11, 23], cache_bits=False)
 
 
 @pytest.mark.parametrize("B", [1, 4, 16])
 @pytest.mark.parametrize("ctx", [4096, 16384, 65536, 131072])
-def test_config4_long_context(kvc, B, ctx):
-    wl = workloads.config4(B, ctx)
+def test_long_context(kvc, B, ctx):
+    wl = workloads.long_context(B, ctx)
     check_workload(kvc, wl, torch.float32, cache_bits=(B * ctx <= 4 * 65536), fused=True, graph=True, overlap=True)
 
 

@@ -124,7 +124,7 @@ def test_decode_fp8_matches_oracle(case, out_dtype):
     check_attention(out, ref, f"fp8 decode case {case}")
 
 
-def test_decode_fp8_config2_shape():
+def test_decode_fp8_model_step_shape():
     """One layer of the 24-layer benchmark shape (32 x 2048, 14 / 2 heads) on an fp8 cache."""
     import paged_kv_cache_27_gb300 as kvc
     wl = workloads.multi_token_decode(77, [2048] * 32, 1)

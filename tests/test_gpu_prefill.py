@@ -27,10 +27,10 @@ def oracle_flow(wl, causal):
     return out, dec, kc, vc, ctx
 
 
-@pytest.mark.parametrize("make", [workloads.config5_varlen, workloads.config5_gqa])
+@pytest.mark.parametrize("make", [workloads.varlen_prefill, workloads.gqa_prefill])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
-def test_config5(make, causal, out_dtype):
+def test_small_prefills(make, causal, out_dtype):
     from paged_kv_cache_27_gb300 import harness, kvc_device_error_flags
     wl = make()
     got = harness.prefill_then_decode(wl, causal=causal, out_dtype=out_dtype)

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("kw", [dict(B=20, group=4, prefix_len=64, ctx_lo=2, ctx_hi=140), dict()])
 def test_serving_mix(kw):
     from paged_kv_cache_27_gb300 import harness, kvc_device_error_flags
-    mix = workloads.config3(**kw)
+    mix = workloads.shared_prefix_mix(**kw)
     got = harness.serving_mix(mix)
     ref = opaging.serving_mix(mix)
     assert kvc_device_error_flags(clear=True) == 0

@@ -301,7 +301,7 @@ def test_merge_rescales_by_max_difference():
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_segments_vs_torch_sdpa(causal):
     """Every packed segment equals standalone attention on it (xformers article, part 4)."""
-    wl = workloads.config5_varlen()
+    wl = workloads.varlen_prefill()
     out = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
     for s in range(len(wl.seqlens)):
         a, b = wl.cu_seqlens[s], wl.cu_seqlens[s + 1]
@@ -313,7 +313,7 @@ def test_prefill_segments_vs_torch_sdpa(causal):
 
 
 def test_prefill_gqa_vs_torch_sdpa():
-    wl = workloads.config5_gqa()
+    wl = workloads.gqa_prefill()
     G = wl.Hq // wl.Hkv
     for causal in (True, False):
         out = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=causal)
@@ -328,7 +328,7 @@ def test_prefill_gqa_vs_torch_sdpa():
 
 def test_prefill_last_row_equals_paged_decode():
     """The causal prefill's last row of a segment equals the decode over a cache holding that segment."""
-    wl = workloads.config5_gqa(B=1, M=100)
+    wl = workloads.gqa_prefill(B=1, M=100)
     out = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=True)
     kc, vc, table = paged_single(wl.k, wl.v, perm_seed=3)
     dec = oracle.decode(wl.q[-1:], kc, vc, table, np.array([100], np.int32), wl.scale)

@@ -126,7 +126,7 @@ def test_paged_utilisation_near_98_percent():
 
 def test_serving_mix_protocol_small():
     """The serving-mix protocol: refcounts, copy-on-write and the decode result vs private contiguous K/V."""
-    mix = workloads.config3(B=20, group=4, prefix_len=64, ctx_lo=2, ctx_hi=140, Hq=4, Hkv=2, D=32)
+    mix = workloads.shared_prefix_mix(B=20, group=4, prefix_len=64, ctx_lo=2, ctx_hi=140, Hq=4, Hkv=2, D=32)
     r = paging.serving_mix(mix)
     tables = [list(t[t >= 0]) for t in r["block_table"]]
     # every live page's refcount equals the number of tables naming it

@@ -140,24 +140,24 @@ def _decode(name, seed, L, B, Hq, Hkv, D, ctx, bs=16, NB=None, peak_frac=0.0, pe
         extra={"peaks": peaks, "seed": seed})
 
 
-def config1() -> DecodeWorkload:
+def single_sequence_256() -> DecodeWorkload:
     """1 sequence, Hq = Hkv = 1, D = 64, context 256, 16 permuted blocks, 1 layer."""
-    return _decode("cfg1_single_seq_ctx256", BASE_SEED + 1, L=1, B=1, Hq=1, Hkv=1, D=64, ctx=[256])
+    return _decode("single_seq_ctx256", BASE_SEED + 1, L=1, B=1, Hq=1, Hkv=1, D=64, ctx=[256])
 
 
-def config2(L=24, B=32, ctx=2048, Hq=14, Hkv=2, D=64) -> DecodeWorkload:
+def model_decode_step(L=24, B=32, ctx=2048, Hq=14, Hkv=2, D=64) -> DecodeWorkload:
     """24 layers, 32 sequences at context 2048, 14 q / 2 KV heads, D = 64.
 
     The pool holds exactly B * ctx tokens (32 x 2048 = 4096 blocks of 16)."""
-    return _decode(f"cfg2_L{L}_B{B}_ctx{ctx}_gqa{Hq}x{Hkv}", BASE_SEED + 2, L=L, B=B, Hq=Hq, Hkv=Hkv,
+    return _decode(f"model_step_L{L}_B{B}_ctx{ctx}_gqa{Hq}x{Hkv}", BASE_SEED + 2, L=L, B=B, Hq=Hq, Hkv=Hkv,
                    D=D, ctx=[ctx] * B)
 
 
-def config4(B: int, ctx: int, Hq=14, Hkv=2, D=64) -> DecodeWorkload:
+def long_context(B: int, ctx: int, Hq=14, Hkv=2, D=64) -> DecodeWorkload:
     """Long context: B sequences at one context length, keys x3 on 1 % of positions."""
     cells = [(b, c) for b in (1, 4, 16) for c in (4096, 16384, 65536, 131072)]
     cell = cells.index((B, ctx)) if (B, ctx) in cells else 100 + B * 7 + ctx
-    return _decode(f"cfg4_B{B}_ctx{ctx}_peaked", [BASE_SEED + 4, cell], L=1, B=B, Hq=Hq, Hkv=Hkv,
+    return _decode(f"long_ctx_B{B}_ctx{ctx}_peaked", [BASE_SEED + 4, cell], L=1, B=B, Hq=Hq, Hkv=Hkv,
                    D=D, ctx=[ctx] * B, peak_frac=0.01)
 
 
@@ -193,7 +193,7 @@ class ServingMix:
     v_new: np.ndarray
 
 
-def config3(B=200, group=8, prefix_len=512, ctx_lo=16, ctx_hi=4096, Hq=14, Hkv=2, D=64,
+def shared_prefix_mix(B=200, group=8, prefix_len=512, ctx_lo=16, ctx_hi=4096, Hq=14, Hkv=2, D=64,
             bs=16) -> ServingMix:
     rng = np.random.default_rng(BASE_SEED + 3)
     ctx = rng.integers(ctx_lo, ctx_hi + 1, size=B).astype(np.int32)
@@ -213,7 +213,7 @@ def config3(B=200, group=8, prefix_len=512, ctx_lo=16, ctx_hi=4096, Hq=14, Hkv=2
     k_new = normal_f16(rng, (B, Hkv, D))
     v_new = normal_f16(rng, (B, Hkv, D))
     return ServingMix(
-        name=f"cfg3_serving_B{B}_ctx{ctx_lo}-{ctx_hi}_prefix{prefix_len}x{group}", B=B, Hq=Hq,
+        name=f"shared_prefix_B{B}_ctx{ctx_lo}-{ctx_hi}_prefix{prefix_len}x{group}", B=B, Hq=Hq,
         Hkv=Hkv, D=D, bs=bs, NB=NB, scale=1.0 / float(np.sqrt(D)), group=group,
         prefix_len=prefix_len, ctx=ctx, free_order=free_order, prefix_k=prefix_k,
         prefix_v=prefix_v, suffix_off=suffix_off, suffix_k=suffix_k, suffix_v=suffix_v, q=q,
@@ -261,12 +261,12 @@ def _prefill(name, seed, seqlens, Hq, Hkv, D, bs=16) -> PrefillWorkload:
         v_dec=normal_f16(rng, (n, Hkv, D)))
 
 
-def config5_varlen(seqlens=(37, 120, 8, 200), H=8, D=64) -> PrefillWorkload:
-    return _prefill("cfg5_varlen_" + "-".join(map(str, seqlens)), [BASE_SEED + 5, 0], seqlens, H, H, D)
+def varlen_prefill(seqlens=(37, 120, 8, 200), H=8, D=64) -> PrefillWorkload:
+    return _prefill("varlen_prefill_" + "-".join(map(str, seqlens)), [BASE_SEED + 5, 0], seqlens, H, H, D)
 
 
-def config5_gqa(B=2, M=256, Hq=8, Hkv=2, D=64) -> PrefillWorkload:
-    return _prefill(f"cfg5_gqa_B{B}_M{M}_{Hq}x{Hkv}", [BASE_SEED + 5, 1], (M,) * B, Hq, Hkv, D)
+def gqa_prefill(B=2, M=256, Hq=8, Hkv=2, D=64) -> PrefillWorkload:
+    return _prefill(f"gqa_prefill_B{B}_M{M}_{Hq}x{Hkv}", [BASE_SEED + 5, 1], (M,) * B, Hq, Hkv, D)
 
 
 def small_decode(seed, B, Hq, Hkv, D, ctx, L=1, bs=16, peak_frac=0.0) -> DecodeWorkload:
