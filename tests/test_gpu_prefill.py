@@ -120,3 +120,22 @@ def test_prefill_bad_precision_rejected():
     with pytest.raises(kvc.KvcError) as e:
         kvc.prefill_attention_ex(q, k, k, cu, 4, 0.125, True, 7, out)
     assert "KVC_ERR_INVALID" in str(e.value)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("precise", [False, True])
+def test_prefill_empty_segments(D, precise):
+    """Zero-length segments anywhere in cu_seqlens (first, middle, last, repeated) are no-ops; the others are
+    computed as usual and no output row is left unwritten."""
+    import paged_kv_cache_27_gb300 as kvc
+    seqlens = (0, 130, 0, 0, 1, 257, 0)
+    wl = workloads._prefill("empty", [12, sum(seqlens), D], seqlens, 4, 2, D)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (wl.q, wl.k, wl.v))
+    cu = torch.from_numpy(wl.cu_seqlens).cuda()
+    assert list(wl.cu_seqlens) == [0, 0, 130, 130, 130, 131, 388, 388]
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    kvc.prefill_attention(q, k, v, cu, max(seqlens), wl.scale, True, out, precise=precise)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.prefill(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.scale, causal=True)
+    check_attention(out, ref, f"prefill with empty segments D={D}")
