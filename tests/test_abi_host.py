@@ -216,3 +216,42 @@ def test_checked_mode_and_version():
     assert kvc.kvc_version() >= 100
     kvc.kvc_set_checked_mode(True)
     kvc.kvc_set_checked_mode(False)
+
+
+def test_cache_layer_pointers_and_errors():
+    """kv_cache_layer is pointer arithmetic over the caller's pools (never dereferenced here): layer l of a
+    [L][NB][Hkv][bs][D] fp16 pool starts l * NB * Hkv * bs * D * 2 bytes in."""
+    import ctypes
+    import paged_kv_cache_27_gb300 as kvc
+    L, NB, Hkv, D = 3, 10, 2, 64
+    cfg = kvc._Config(L, NB, 16, Hkv, D, kvc.KVC_F16)
+    kbase, vbase = 1 << 40, 1 << 41  # aligned addresses that are never touched
+    h = ctypes.c_void_p()
+    assert kvc._lib.kv_cache_create(ctypes.byref(cfg), ctypes.c_void_p(kbase), ctypes.c_void_p(vbase),
+                                    ctypes.byref(h)) == 0
+    try:
+        per = NB * Hkv * 16 * D * 2
+        for layer in range(L):
+            assert kvc.kv_cache_layer(h.value, layer) == (kbase + per * layer, vbase + per * layer)
+        for bad in (-1, L):
+            with pytest.raises(kvc.KvcError) as e:
+                kvc.kv_cache_layer(h.value, bad)
+            assert "KVC_ERR_INVALID" in str(e.value)
+    finally:
+        kvc.kv_cache_destroy(h.value)
+    # misaligned pools are refused; a host-only cache has no layers
+    assert kvc._lib.kv_cache_create(ctypes.byref(cfg), ctypes.c_void_p(kbase + 8), ctypes.c_void_p(vbase),
+                                    ctypes.byref(h)) != 0
+    hh = kvc.kv_cache_create(kvc.KvcConfig(num_layers=L, num_blocks=NB, num_kv_heads=Hkv, head_dim=D))
+    try:
+        with pytest.raises(kvc.KvcError):
+            kvc.kv_cache_layer(hh, 0)
+    finally:
+        kvc.kv_cache_destroy(hh)
+
+
+def test_trace_read_needs_a_trace_build():
+    import paged_kv_cache_27_gb300 as kvc
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_trace_read(16)
+    assert "KVC_ERR_UNSUPPORTED" in str(e.value)
