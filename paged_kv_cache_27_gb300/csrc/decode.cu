@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     if (threadIdx.x == 0)
         for (int q_ = 0; q_ < 8; ++q_) s_trace_t[q_] = 0;
 #endif
-#if KVC_DEC_EARLY_TRIGGER
+#if KVC_DEC_TRIGGER == 0
     grid_dependents_launch();
 #endif
     KVC_TRACE_MARK(0);
@@ -283,6 +283,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // ---- everything below may read what the previous kernel wrote ----
     grid_dependency_wait();
     KVC_TRACE_MARK(2);
+#if KVC_DEC_TRIGGER == 1
+    grid_dependents_launch();
+#endif
 
     // query fragments (A operand, rows = the G heads of this KV head; rows >= G are zero)
     uint32_t qa[D / 16][2];
@@ -330,6 +333,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         const int nj = next_j;
         next_j += nwarps_cl;
         if (nj < cb1 && lane == 0) issue(s, s_table[nj - cb0]);
+#if KVC_DEC_TRIGGER == 3
+        if (nj >= cb1 && nj < cb1 + nwarps_cl) grid_dependents_launch();  // this warp's last copy is out
+#elif KVC_DEC_TRIGGER == 2
+        if (nj == cb0 + gw + ST * nwarps_cl) grid_dependents_launch();  // this warp's first refill
+#endif
 #pragma unroll
         for (int k = 0; k < ST; ++k)
             if (k == s) blk[k] = nj < cb1 ? nj : -1;
@@ -520,7 +528,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
             if (!refilled) refill(s);
         }
     }
-#if !KVC_DEC_EARLY_TRIGGER
+#if KVC_DEC_TRIGGER == 4
     grid_dependents_launch();  // the next kernel may start its prologue while this one finishes
 #endif
     KVC_TRACE_MARK(3);
@@ -561,6 +569,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     }
     __syncthreads();
     KVC_TRACE_MARK(4);
+#if KVC_DEC_TRIGGER == 5
+    grid_dependents_launch();
+#endif
 
     const bool final_here = nclus == 1 && !kSuffix;  // this cluster's result is the output
     const bool direct = final_here && cs == 1;                  // a single CTA holds the whole range

@@ -36,8 +36,17 @@ namespace kvc {
 #ifndef KVC_DEC_MAX_CLUSTER
 #define KVC_DEC_MAX_CLUSTER 8
 #endif
-#ifndef KVC_DEC_EARLY_TRIGGER  // let the next kernel launch as soon as every CTA of this one has started
-#define KVC_DEC_EARLY_TRIGGER 1
+// Where a decode kernel lets the next kernel on the stream launch (programmatic dependent launch): 0 at its
+// start, 1 after its own dependency wait, 2 when a warp refills its first stage (its first block is consumed),
+// 3 when a warp has issued its last copy, 4 after the block loop, 5 after the CTA merge, 6 not at all (at exit).
+// A 24-layer decode step (32 x 2048) measured 4388 / 4410 / 4555 / 4545 / 4472 / 4317 / 3932 GB/s: a trigger
+// before the dependency wait lets every queued layer launch at once (their CTAs hold SM slots while they wait);
+// one well after the first block leaves the next layer's first copies too late.
+#ifndef KVC_DEC_TRIGGER
+#define KVC_DEC_TRIGGER 2
+#endif
+#ifndef KVC_GROUP_EARLY_TRIGGER  // the group kernel lets the next kernel launch as soon as it starts
+#define KVC_GROUP_EARLY_TRIGGER 1
 #endif
 #ifndef KVC_DEC_EARLY_REFILL  // 1: refill a stage once its K and V are in registers, before the softmax
 #define KVC_DEC_EARLY_REFILL 1

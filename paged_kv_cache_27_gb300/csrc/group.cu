@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int grp = blockIdx.x / p.nchunks, chunk = blockIdx.x % p.nchunks, kvh = blockIdx.y;
-#if KVC_DEC_EARLY_TRIGGER
+#if KVC_GROUP_EARLY_TRIGGER
     grid_dependents_launch();
 #endif
     // the group: its members (warps), the rows they attend through, and the block range [j0, j1)
