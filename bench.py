@@ -62,8 +62,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "d1855564d750c01d3112f525bd6d3151882c62013315ba3c3e044ef8d3326e9d",
-                      "bytes_per_launch": 33674496}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "278e97ed3a1efefb49104155e21c8003eee652d1a938eea6db6a4d5d4a15ec4e",
+                      "bytes_per_launch": 33674752}
 
 
 def decode_sources_sha256() -> str:
