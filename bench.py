@@ -547,7 +547,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
                                                       mix.scale, out, cwsb, max_ctx)
     us_casc = _timed_calls(casc, 20, flush, stream)
     shared_reads = int(sum(int(sh[b]) for b in range(mix.B)) - sum(int(sh[gs[g]]) for g in range(len(gs) - 1)))
-    emit({"config": "3, attention only: plain decode vs cascade (shared prefix blocks read once per group)",
+    emit({"config": "shared-prefix mix, attention only: plain decode vs cascade (shared prefix blocks read once per group)",
           "us_plain": us_plain, "us_cascade": us_casc, "speedup": us_plain / us_casc,
           "groups": len(gs) - 1, "max_shared_blocks": mxs,
           "block_reads_saved": shared_reads * mix.Hkv, "bytes_saved": shared_reads * 16 * row,
