@@ -278,8 +278,10 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
  *                 (q_len <= ctx <= min(max_blocks * bs, max_context_len))
  *   workspace     device, 16-byte aligned, >= paged_decode_multi_plan's bytes
  * Other arguments as in paged_decode_attention; the new tokens' K/V must be
- * in the cache already (kv_append with their slots).  Each chunk of a
- * sequence's blocks is read once for all q_len tokens.  Two kernel launches. */
+ * in the cache already (kv_append with their slots).  Each block is read
+ * once for all q_len tokens.  One kernel launch where a thread-block cluster
+ * covers the longest context (the plan's workspace is then 0 bytes), else two
+ * (partial states per cluster, then their merge). */
 kvc_status paged_decode_multi_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                                    int q_len, size_t* workspace_bytes);
 kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
@@ -328,11 +330,11 @@ kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const 
  * history before that kernel has finished, and q, k_new, v_new, the
  * workspace and out only after.  A decode kernel releases its own
  * dependents once its dependency wait has passed and its warps have taken
- * their first blocks (the cascade and multi-token kernels as soon as they
- * start), so in an unbroken run of decode calls on one stream (no other
- * kernel, copy or event between them) a call may start before earlier calls
- * of the run have finished.  Contract: no kernel of
- * that run, nor the kernel launched just before the run, writes a call's
+ * their first blocks (the cascade kernel as soon as it starts), so in an
+ * unbroken run of decode calls on one stream (no other kernel, copy or event
+ * between them) a call may start before earlier calls of the run have
+ * finished.  Contract: no kernel of that run, nor the kernel launched just
+ * before the run, writes a call's
  * block table, context lengths or the cache rows it reads (other than
  * through that call's own append).  One call per layer, every layer a
  * different cache, meets this; calls on the same layer need something

@@ -120,24 +120,6 @@ __device__ unsigned g_trace_n;
     } while (0)
 #endif
 
-// byte offset of 16-byte chunk `chunk` (8 fp16 columns) of row `row` inside a
-// tile loaded as boxes of 16 rows x 64 columns with the 128-byte swizzle.
-// ---- thread-block cluster helpers ------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// shared::cluster address of the same shared variable in CTA `rank` of this cluster
-__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 // kSuffix: the cascade's suffix pass (per-sequence block offset, partial states only); the plain decode
 // is compiled without either
 // kFp8: the cache holds e4m3 codes with per-row scales (tmK / tmV map the codes; V codes are stored per dim,

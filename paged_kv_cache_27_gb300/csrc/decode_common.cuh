@@ -94,6 +94,8 @@ struct DecodeCfg {
     static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
 };
 
+// byte offset of 16-byte chunk `chunk` (8 fp16 columns) of row `row` inside a tile loaded as boxes of 16
+// rows x 64 columns with the 128-byte swizzle
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(((chunk >> 3) << 11) + (row << 7) + (((chunk & 7) ^ (row & 7)) << 4));
 }

@@ -1,24 +1,20 @@
-// Decode kernels for query groups that share their key blocks, on sm_103a: the cascade (shared-prefix)
-// decode and the multi-token decode.  One CTA streams a range of paged K/V blocks once through a ring in
-// shared memory and several warps, each with its own query rows, attend over it; partial states are merged
-// by the decode side's combine kernel (decode.cu).  What each computes, and its citations, is stated at
-// the kernel and in include/kvc.h.
+// The cascade (shared-prefix) decode on sm_103a: one CTA streams a range of a group's shared K/V blocks once
+// through a ring in shared memory and several warps, one per sequence of the group, attend over it; partial
+// states are merged by the decode side's combine kernel (decode.cu).  What it computes, and its citations,
+// is stated at the kernel and in include/kvc.h.
 #include "decode_common.cuh"
 
 namespace kvc {
 
-// ---- query groups that share their key blocks --------------------------------------------------------
+// ---- groups of sequences that share their first blocks ----------------------------------------------
 //
-// One CTA streams a range of K/V blocks once through a ring in shared memory (thread 0 issues the copies);
-// warp w attends its own query rows (the G heads of one query token) over every block of the range with the
-// decode kernel's block math (S^T = K Q^T, online softmax in base 2, O^T += V^T (P_hi + P_lo)^T) and
-// writes its partial state (m, l, acc) as part `chunk` of its rows; the combine kernel merges the parts.
-//  - cascade prefix (kMulti = false): the group is sequences g0 .. g1-1 (at most 8) whose block-table rows
-//    begin with the same `nsh` blocks; warp w is sequence g0 + w; the range is a chunk of those blocks, all
-//    of them inside every member's context, so nothing is masked.
-//  - multi-token decode (kMulti = true): the group is the q_len new tokens of one sequence; warp t
-//    is token t at position ctx - q_len + t, which sees keys 0 .. ctx - q_len + t (causal among the new
-//    tokens); the range is a chunk of the sequence's blocks.
+// One CTA streams a range of K/V blocks once through a ring in shared memory (thread 0 issues the copies).
+// The group is sequences g0 .. g1-1 (at most 8) whose block-table rows begin with the same `nsh` blocks;
+// warp w is sequence g0 + w and attends its query rows (the G heads of the sequence's KV head) over every
+// block of the range with the decode kernel's block math (S^T = K Q^T, online softmax in base 2,
+// O^T += V^T (P_hi + P_lo)^T), then writes its partial state (m, l, acc) as part `chunk` of its rows; the
+// combine kernel merges the parts.  The range is a chunk of the shared blocks, all of them inside every
+// member's context, so nothing is masked.
 #ifndef KVC_PREFIX_STAGES  // blocks in flight per group CTA
 #define KVC_PREFIX_STAGES 12
 #endif
@@ -37,20 +33,19 @@ constexpr size_t group_smem_bytes(int stages, int chunk) {
 }
 
 struct GroupKernelParams {
-    const __half* q;             // [B][Hq][D] (cascade) or [B][q_len][Hq][D] (multi-token)
+    const __half* q;             // [B][Hq][D]
     const int32_t* block_table;
-    const int32_t* group_start;  // cascade: [n_groups + 1]
-    const int32_t* blk_off;      // cascade: per sequence, its group's shared blocks
-    const int32_t* context_lens; // multi-token: per sequence, including its q_len new tokens
+    const int32_t* group_start;  // [n_groups + 1]
+    const int32_t* blk_off;      // per sequence, its group's shared blocks
     float* part_ml;
     float* part_acc;
     unsigned* err;
-    int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride, q_len, max_ctx;
+    int max_blocks, num_blocks, Hq, Hkv, G, chunk, nchunks, part_stride;
     int stages;  // ring depth of this launch, 1 .. kGroupStages
     float scale_log2;
 };
 
-template <int D, bool kMulti>
+template <int D>
 __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const GroupKernelParams p) {
@@ -70,29 +65,16 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
 #if KVC_GROUP_EARLY_TRIGGER
     grid_dependents_launch();
 #endif
-    // the group: its members (warps), the rows they attend through, and the block range [j0, j1)
-    int nmem, nblk, ctx = 0;
-    const int32_t* table;
-    if constexpr (kMulti) {
-        nmem = p.q_len;
-        ctx = p.context_lens[grp];
-        if (ctx < p.q_len || ctx > p.max_blocks * kBlockSize || ctx > p.max_ctx) {
-            if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-            return;  // the combine kernel writes this sequence's zeros
-        }
-        nblk = (ctx + kBlockSize - 1) / kBlockSize;
-        table = p.block_table + static_cast<int64_t>(grp) * p.max_blocks;
-    } else {
-        const int g0 = p.group_start[grp];
-        nmem = p.group_start[grp + 1] - g0;
-        if (nmem < 1) return;
-        nblk = p.blk_off[g0];
-        if (nmem > NW || nblk < 0 || nblk > p.max_blocks) {
-            if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-            return;
-        }
-        table = p.block_table + static_cast<int64_t>(g0) * p.max_blocks;  // the first member's row
+    // the group: its members (warps), the table row they share blocks through, and the block range [j0, j1)
+    const int g0 = p.group_start[grp];
+    const int nmem = p.group_start[grp + 1] - g0;
+    if (nmem < 1) return;
+    const int nblk = p.blk_off[g0];
+    if (nmem > NW || nblk < 0 || nblk > p.max_blocks) {
+        if (threadIdx.x == 0 && chunk == 0 && kvh == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+        return;
     }
+    const int32_t* table = p.block_table + static_cast<int64_t>(g0) * p.max_blocks;  // the first member's row
     const int j0 = chunk * p.chunk, j1 = min(nblk, j0 + p.chunk);
     if (j0 >= j1) return;  // the range is shorter
     const int n = j1 - j0;
@@ -133,10 +115,7 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
     grid_dependency_wait();  // q may come from the previous kernel
 
     const bool member = warp < nmem;
-    const int64_t qrow = kMulti ? static_cast<int64_t>(grp) * p.q_len + (member ? warp : 0)
-                                : static_cast<int64_t>(p.group_start[grp]) + (member ? warp : 0);
-    // multi-token: the last key position this warp's token sees
-    const int last_key = kMulti ? ctx - p.q_len + (member ? warp : 0) : 0;
+    const int64_t qrow = static_cast<int64_t>(g0) + (member ? warp : 0);
     uint32_t qa[D / 16][2];
     {
         const bool row_ok = member && g < p.G;
@@ -176,10 +155,6 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
         if (member) {
             const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
             const uint32_t vbase = kbase + C::kTileBytes;
-            const int k0 = (j0 + i) * kBlockSize;  // first key position of the block
-            // keys this warp's token sees in the block, and rows of the block inside the context
-            const int vis = kMulti ? last_key - k0 + 1 : kBlockSize;
-            const int rem = kMulti ? ctx - k0 : kBlockSize;
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -187,8 +162,8 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
                 ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                 mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
             }
-            const float x0 = g < vis ? sc[0] * sl2 : -INFINITY, x1 = g < vis ? sc[1] * sl2 : -INFINITY;
-            const float x2 = g + 8 < vis ? sc[2] * sl2 : -INFINITY, x3 = g + 8 < vis ? sc[3] * sl2 : -INFINITY;
+            // every key of a shared block is inside every member's context
+            const float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) {
@@ -196,13 +171,10 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
             }
             const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-            // a block with no visible key (m stays -inf) leaves the state unchanged
-            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[0] - mn0);
-            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[1] - mn1);
+            const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);  // 0 on the first block
             m_run[0] = mn0;
             m_run[1] = mn1;
-            const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0), p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
-            const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1), p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
+            const float p0 = ex2(x0 - mn0), p2 = ex2(x2 - mn0), p1 = ex2(x1 - mn1), p3 = ex2(x3 - mn1);
             l_run[0] = l_run[0] * al0 + p0 + p2;
             l_run[1] = l_run[1] * al1 + p1 + p3;
 #pragma unroll
@@ -217,20 +189,10 @@ __global__ void __launch_bounds__(256) paged_decode_group_kernel(const __grid_co
             const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
             const uint32_t bl0 = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
             const uint32_t bl1 = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
-            // rows of V past the context may hold any bits (even NaN): zero them in registers
-            uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
-            if (rem < kBlockSize) {
-                keep0 = (2 * t4 < rem ? 0x0000ffffu : 0u) | (2 * t4 + 1 < rem ? 0xffff0000u : 0u);
-                keep1 = (8 + 2 * t4 < rem ? 0x0000ffffu : 0u) | (9 + 2 * t4 < rem ? 0xffff0000u : 0u);
-            }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                a0 &= keep0;
-                a1 &= keep0;
-                a2 &= keep1;
-                a3 &= keep1;
                 mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
                 mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
@@ -286,9 +248,7 @@ static cudaError_t group_setup() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        for (auto kern : {paged_decode_group_kernel<D, false>, paged_decode_group_kernel<D, true>})
-            if (err == cudaSuccess)
-                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupMaxSmem);
+        err = cudaFuncSetAttribute(paged_decode_group_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupMaxSmem);
     });
     return err;
 }
@@ -347,12 +307,9 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
         pp.chunk = cp.chunk;
         pp.nchunks = cp.nchunks;
         pp.part_stride = cp.part_stride;
-        pp.context_lens = nullptr;
-        pp.q_len = 1;
-        pp.max_ctx = a.max_context_len;
         pp.scale_log2 = a.scale * kLog2e;
         pp.stages = kGroupStages;
-        e = launch(paged_decode_group_kernel<D, false>, dim3(n_groups * cp.nchunks, a.Hkv),
+        e = launch(paged_decode_group_kernel<D>, dim3(n_groups * cp.nchunks, a.Hkv),
                    dim3(32 * kMaxGroupSize), group_smem_bytes<D>(kGroupStages, cp.chunk), stream, pdl,
                    1u, tmK, tmV, pp);
         if (e != cudaSuccess) return e;
@@ -390,100 +347,6 @@ cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, cons
     switch (a.D) {
         case 64: return launch_cascade_d<64>(a, group_start, shared_blocks, n_groups, cp, stream);
         case 128: return launch_cascade_d<128>(a, group_start, shared_blocks, n_groups, cp, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-// ---- multi-token decode ------------------------------------------------------------------------------
-cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, MultiPlan* plan) {
-    const int sms = sm_count();
-    if (sms <= 0) return cudaErrorNoDevice;
-    const int64_t nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
-    // about KVC_PREFIX_CTAS CTAs per SM over all (sequence, KV head) pairs, at least 4 blocks each (measured
-    // better than sizing by warps: smaller chunks add per-CTA start-up and parts to merge); the ring holds a
-    // whole chunk up to kGroupStages blocks
-    const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
-    const int64_t per_pair = std::max<int64_t>(1, KVC_PREFIX_CTAS * static_cast<int64_t>(sms) / pairs);
-    plan->chunk = static_cast<int>(std::min<int64_t>(kGroupMaxChunk, std::max<int64_t>(4, (nblk + per_pair - 1) / per_pair)));
-    plan->nchunks = static_cast<int>((nblk + plan->chunk - 1) / plan->chunk);
-    plan->stages = std::min(plan->chunk, kGroupStages);
-    plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * q_len * Hq * plan->nchunks, D);
-    if (q_len == 1) {  // a single new token is the plain decode
-        DecodePlan dp;
-        cudaError_t e = decode_plan(B, Hq, Hkv, D, max_ctx, 0, &dp);
-        if (e != cudaSuccess) return e;
-        plan->workspace_bytes = dp.workspace_bytes;
-    }
-    return cudaSuccess;
-}
-
-template <int D>
-static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPlan& mp, cudaStream_t stream) {
-    cudaError_t e = group_setup<D>();
-    if (e != cudaSuccess) return e;
-    const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
-    CUtensorMap tmK, tmV;
-    e = make_tile_map(&tmK, a.k_cache, D, rows);
-    if (e != cudaSuccess) return e;
-    e = make_tile_map(&tmV, a.v_cache, D, rows);
-    if (e != cudaSuccess) return e;
-    const size_t nrow = static_cast<size_t>(a.B) * q_len * a.Hq * mp.nchunks;
-    float* part_ml = static_cast<float*>(a.workspace);
-    float* part_acc = partials_acc(part_ml, nrow);
-    const bool pdl = launch_overlap() != 0;
-    GroupKernelParams gp;
-    gp.q = a.q;
-    gp.block_table = a.block_table;
-    gp.group_start = nullptr;
-    gp.blk_off = nullptr;
-    gp.context_lens = a.context_lens;
-    gp.part_ml = part_ml;
-    gp.part_acc = part_acc;
-    gp.err = a.err;
-    gp.max_blocks = a.max_blocks;
-    gp.num_blocks = a.num_blocks;
-    gp.Hq = a.Hq;
-    gp.Hkv = a.Hkv;
-    gp.G = a.Hq / a.Hkv;
-    gp.chunk = mp.chunk;
-    gp.nchunks = mp.nchunks;
-    gp.part_stride = mp.nchunks;
-    gp.q_len = q_len;
-    gp.max_ctx = a.max_context_len;
-    gp.scale_log2 = a.scale * kLog2e;
-    gp.stages = mp.stages;
-    e = launch(paged_decode_group_kernel<D, true>, dim3(a.B * mp.nchunks, a.Hkv), dim3(32 * q_len),
-               group_smem_bytes<D>(mp.stages, mp.chunk), stream, pdl, 1u, tmK, tmV, gp);
-    if (e != cudaSuccess) return e;
-    CombineParams c;
-    c.part_ml = part_ml;
-    c.part_acc = part_acc;
-    c.context_lens = a.context_lens;
-    c.blk_off = nullptr;
-    c.out = a.out;
-    c.err = a.err;
-    c.Hq = a.Hq;
-    c.part_stride = mp.nchunks;
-    c.part_base = 0;
-    c.bpc = mp.chunk;
-    c.max_blocks = a.max_blocks;
-    c.max_ctx = a.max_context_len;
-    c.out_f32 = a.out_f32;
-    c.prefix_chunk = 0;
-    c.cascade = 1;
-    c.q_len = q_len;
-    return launch_combine(c, D, a.B * q_len, stream);
-}
-
-cudaError_t launch_multi(const DecodeArgs& a, int q_len, cudaStream_t stream) {
-    MultiPlan mp;
-    cudaError_t e = multi_plan(a.B, a.Hq, a.Hkv, a.D, a.max_context_len, q_len, &mp);
-    if (e != cudaSuccess) return e;
-    if (mp.workspace_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
-    if (q_len == 1) return launch_decode(a, stream);  // q [B][1][Hq][D] is the plain decode's q
-    switch (a.D) {
-        case 64: return launch_multi_d<64>(a, q_len, mp, stream);
-        case 128: return launch_multi_d<128>(a, q_len, mp, stream);
         default: return cudaErrorInvalidValue;
     }
 }

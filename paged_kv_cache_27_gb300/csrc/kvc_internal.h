@@ -103,14 +103,17 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);
 
-// Multi-token decode: q_len (1..8) new tokens per sequence, causal among them (token t at position
-// ctx - q_len + t); q and out are [B][q_len][Hq][D]. The group kernel streams each chunk of a sequence's
-// blocks once for all its tokens; the combine kernel merges the chunks.
+// Multi-token decode (multi.cu): q_len (1..8) new tokens per sequence, causal among them (token t at
+// position ctx - q_len + t); q and out are [B][q_len][Hq][D]. A CTA's warps split a chunk of a sequence's
+// blocks and each carries all the tokens' query rows of its KV head, so every block is read once for all
+// tokens; the CTAs of a cluster merge in distributed shared memory, and the combine kernel merges the
+// clusters where a context needs more than one.
 constexpr int kMaxQueryTokens = 8;
 struct MultiPlan {
     int chunk;    // blocks per CTA
-    int nchunks;  // parts per (token, head): chunks of the longest context
-    int stages;   // ring depth
+    int cluster;  // CTAs per cluster
+    int nclus;    // clusters per context (of the longest); > 1: partial states and the combine kernel
+    int stages;   // blocks in flight per warp
     size_t workspace_bytes;
 };
 cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_context_len, int q_len, MultiPlan* plan);

@@ -52,6 +52,10 @@ CASES = [
     (5, [3, 15, 16, 17, 20000], 3, 14, 2, 64),
     (6, [8, 9, 23, 24, 25, 31, 32, 33], 8, 14, 2, 64),
     (7, [130, 5000], 5, 16, 2, 128),
+    # 64 query rows (two row groups of four n-tiles), 8 rows (one n-tile) at D=128, 18 rows over two row groups
+    (8, [8, 100, 2049], 8, 16, 2, 64),
+    (9, [2, 31, 32, 33, 9000], 2, 16, 4, 128),
+    (10, [6, 64, 65, 3000], 6, 12, 4, 128),
 ]
 
 
