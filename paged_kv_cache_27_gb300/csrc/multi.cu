@@ -28,6 +28,9 @@ namespace kvc {
 #ifndef KVC_MULTI_STAGES128
 #define KVC_MULTI_STAGES128 2
 #endif
+#ifndef KVC_MULTI_MAX_TILES64  // n-tiles per warp at most, head_dim 64 (more rows make more row groups)
+#define KVC_MULTI_MAX_TILES64 4
+#endif
 #ifndef KVC_MULTI_EARLY_REFILL  // 1: refill a stage once its V fragments are in registers, before the softmax
 #define KVC_MULTI_EARLY_REFILL 1
 #endif
@@ -455,7 +458,7 @@ __global__ void __launch_bounds__(MultiCfg<D, NT>::kThreads, MultiCfg<D, NT>::kM
 // n-tiles per warp and row groups for q_len tokens of G heads
 static void multi_tiles(int D, int q_len, int G, int* nt, int* nrg) {
     const int R = q_len * G;
-    const int maxt = D == 64 ? 4 : 2;  // accumulators: NT * D / 2 floats a lane
+    const int maxt = D == 64 ? KVC_MULTI_MAX_TILES64 : 2;  // accumulators: NT * D / 2 floats a lane
     *nt = std::min(maxt, (R + 7) / 8);
     *nrg = (R + 8 * *nt - 1) / (8 * *nt);
 }
