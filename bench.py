@@ -62,8 +62,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "278e97ed3a1efefb49104155e21c8003eee652d1a938eea6db6a4d5d4a15ec4e",
-                      "bytes_per_launch": 33674752}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "5984d6bd262edff8fd490dd7b147c4276678c81fd39ad6b8dca9f599e8b6fe5f",
+                      "bytes_per_launch": 33674496}
 
 
 def decode_sources_sha256() -> str:
@@ -476,6 +476,8 @@ def run_suite(args):
 
     if args.suite_part in ("all", "decode"):
         run_suite_decode(device, stream, flush, emit, peak)
+    elif args.suite_part == "multi":
+        run_suite_multi(device, stream, flush, emit, peak)
     if args.suite_part in ("all", "prefill"):
         run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind)
     return 0
@@ -577,55 +579,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "logical_GBps_plain": lb / (us_p * 1e-6) / 1e9, "unique_GBps_cascade": ub / (us_c * 1e-6) / 1e9})
     del ckp, cvp
 
-    # multi-token decode (speculative verification): T new tokens per sequence, B=32, context 2048; one call
-    # with L2 flushed (host marshalling and launch included), and a 24-layer graph with launch overlap
-    # (device time per layer; the pools of the 24 layers together exceed L2)
-    Lm = 24
-    kpm0, vpm0, tbm, ctm, _, _, _ = _decode_state(32, 2048, 14, 2, 64, device, seed=77)
-    genm = torch.Generator(device=device).manual_seed(78)
-    kml = [kpm0] + [torch.randn(kpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
-    vml = [vpm0] + [torch.randn(vpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
-    nbytes = 32 * 2048 * 2 * 2 * 64 * 2
-    for T in (1, 2, 4, 8):
-        qms = [torch.randn((32, T, 14, 64), generator=genm, device=device).half() for _ in range(Lm)]
-        om = torch.empty((32, T, 14, 64), dtype=torch.float16, device=device)
-        wsm = torch.zeros(max(kvc.paged_decode_multi_plan(32, 14, 2, 64, 2048, T), 16), dtype=torch.uint8,
-                          device=device)
-        us = _timed_calls(lambda: kvc.paged_decode_multi_attention(qms[0], kml[0], vml[0], tbm, ctm, 0.125, om, wsm,
-                                                                   2048), 20, flush, stream)
-
-        def body():
-            for l in range(Lm):
-                kvc.paged_decode_multi_attention(qms[l], kml[l], vml[l], tbm, ctm, 0.125, om, wsm, 2048)
-        kvc.kvc_set_launch_overlap(True)
-        try:
-            body()
-            torch.cuda.synchronize()
-            gm = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream(device)
-            with torch.cuda.stream(side):
-                with torch.cuda.graph(gm, stream=side):
-                    body()
-            for _ in range(5):
-                gm.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(50):
-                gm.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            us_g = e0.elapsed_time(e1) * 1e3 / (50 * Lm)
-        finally:
-            kvc.kvc_set_launch_overlap(False)
-        emit({"config": f"multi-token decode: T={T} new tokens per sequence, B=32, ctx=2048, 14 q / 2 KV heads, D=64",
-              "us_per_call": us, "GBps": nbytes / (us * 1e-6) / 1e9,
-              "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100, "tokens_per_s": 32 * T / (us * 1e-6),
-              "us_per_layer_graph": us_g, "GBps_graph": nbytes / (us_g * 1e-6) / 1e9,
-              "pct_hbm_peak_graph": nbytes / (us_g * 1e-6) / 1e9 / peak * 100,
-              "tokens_per_s_graph": 32 * T / (us_g * Lm * 1e-6)})
-        del qms
-    del kml, vml, kpm0, vpm0
+    run_suite_multi(device, stream, flush, emit, peak)
 
     # quantized cache (NEXT-4): 24-layer decode-only graphs with launch overlap, fp16 pools vs the same pools
     # quantized to fp8 e4m3 with per-row scales (the model step's shape: 32 x 2048, 14 / 2 heads, D = 64)
@@ -746,6 +700,61 @@ def run_suite_decode(device, stream, flush, emit, peak):
 
 
 
+def run_suite_multi(device, stream, flush, emit, peak):
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+
+    # multi-token decode (speculative verification): T new tokens per sequence, B=32, context 2048; one call
+    # with L2 flushed (host marshalling and launch included), and a 24-layer graph with launch overlap
+    # (device time per layer; the pools of the 24 layers together exceed L2)
+    Lm = 24
+    kpm0, vpm0, tbm, ctm, _, _, _ = _decode_state(32, 2048, 14, 2, 64, device, seed=77)
+    genm = torch.Generator(device=device).manual_seed(78)
+    kml = [kpm0] + [torch.randn(kpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
+    vml = [vpm0] + [torch.randn(vpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
+    nbytes = 32 * 2048 * 2 * 2 * 64 * 2
+    for T in (1, 2, 3, 4, 8):
+        qms = [torch.randn((32, T, 14, 64), generator=genm, device=device).half() for _ in range(Lm)]
+        om = torch.empty((32, T, 14, 64), dtype=torch.float16, device=device)
+        wsm = torch.zeros(max(kvc.paged_decode_multi_plan(32, 14, 2, 64, 2048, T), 16), dtype=torch.uint8,
+                          device=device)
+        us = _timed_calls(lambda: kvc.paged_decode_multi_attention(qms[0], kml[0], vml[0], tbm, ctm, 0.125, om, wsm,
+                                                                   2048), 20, flush, stream)
+
+        def body():
+            for l in range(Lm):
+                kvc.paged_decode_multi_attention(qms[l], kml[l], vml[l], tbm, ctm, 0.125, om, wsm, 2048)
+        kvc.kvc_set_launch_overlap(True)
+        try:
+            body()
+            torch.cuda.synchronize()
+            gm = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(gm, stream=side):
+                    body()
+            for _ in range(5):
+                gm.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(50):
+                gm.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us_g = e0.elapsed_time(e1) * 1e3 / (50 * Lm)
+        finally:
+            kvc.kvc_set_launch_overlap(False)
+        emit({"config": f"multi-token decode: T={T} new tokens per sequence, B=32, ctx=2048, 14 q / 2 KV heads, D=64",
+              "us_per_call": us, "GBps": nbytes / (us * 1e-6) / 1e9,
+              "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100, "tokens_per_s": 32 * T / (us * 1e-6),
+              "us_per_layer_graph": us_g, "GBps_graph": nbytes / (us_g * 1e-6) / 1e9,
+              "pct_hbm_peak_graph": nbytes / (us_g * 1e-6) / 1e9 / peak * 100,
+              "tokens_per_s_graph": 32 * T / (us_g * Lm * 1e-6)})
+        del qms
+    del kml, vml, kpm0, vpm0
+
+
 def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
     import torch
     import paged_kv_cache_27_gb300 as kvc
@@ -796,7 +805,8 @@ def main():
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
     ap.add_argument("--suite", action="store_true",
                     help="instead of the headline line: one JSON line per further configuration (1, 3, 4, 5)")
-    ap.add_argument("--suite-part", choices=["all", "decode", "prefill"], default="all")
+    ap.add_argument("--suite-part", choices=["all", "decode", "prefill", "multi"], default="all",
+                    help="decode: every decode configuration (multi-token included); multi: the multi-token lines only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
