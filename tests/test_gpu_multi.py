@@ -1,4 +1,6 @@
 """Multi-token decode (several new tokens per sequence, causal among them) on the GPU vs the oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -99,3 +101,28 @@ def test_multi_token_argument_errors():
     assert torch.all(out[0] == 0)
     ref = oracle.decode_multi(wl.q[1:], wl.k_pool, wl.v_pool, wl.block_table[1:], wl.ctx[1:], wl.scale)
     check_attention(out[1:].reshape(-1, wl.Hq, wl.D), ref.reshape(-1, wl.Hq, wl.D), "multi-token, other sequence")
+
+
+def test_multi_token_bad_inputs_flagged_without_faulting():
+    """Unchecked bad inputs with several clusters per context (partials + combine): a context shorter than the
+    new tokens gives zero rows, an out-of-range block id is skipped; both are flagged, the rest is right."""
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_device_error_flags(clear=True)
+    wl = workloads.multi_token_decode(13, [20000, 5000, 700], 3)
+    assert kvc.paged_decode_multi_plan(3, wl.Hq, wl.Hkv, wl.D, 20000, 3) > 0  # partial states: several clusters
+    ctx = np.array(wl.ctx, np.int32)
+    ctx[1] = 2
+    out = run_multi(wl, ctx=ctx)[0]
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["CONTEXT"]
+    assert torch.all(out[1] == 0)
+    ref = oracle.decode_multi(wl.q, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+    check_attention(out[0].reshape(-1, wl.Hq, wl.D), ref[0].reshape(-1, wl.Hq, wl.D), "multi-token, long context")
+    check_attention(out[2].reshape(-1, wl.Hq, wl.D), ref[2].reshape(-1, wl.Hq, wl.D), "multi-token, third sequence")
+    # an out-of-range block id in the first sequence's table: skipped and flagged, every output finite
+    bad_table = wl.block_table.copy()
+    bad_table[0, 3] = -5
+    wl2 = dataclasses.replace(wl, block_table=bad_table)
+    out2 = run_multi(wl2)[0]
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["BLOCK_ID"]
+    assert torch.isfinite(out2).all()
+    check_attention(out2[1:].reshape(-1, wl.Hq, wl.D), ref[1:].reshape(-1, wl.Hq, wl.D), "multi-token, other rows")
