@@ -436,6 +436,25 @@ def _timed_calls(fn, reps, flush_buf, stream):
     return total / reps
 
 
+def _graph_of(fn, device):
+    """fn() captured once in a CUDA graph with programmatic dependent launch between its kernels; returns the
+    graph's replay (inputs must stay at the same addresses)."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_set_launch_overlap(True)
+    try:
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+    finally:
+        kvc.kvc_set_launch_overlap(False)
+    return g.replay
+
+
 def _decode_state(B, ctx, Hq, Hkv, D, device, seed):
     """Seeded synthetic decode state made on the device (K/V N(0,1) fp16, permuted block tables)."""
     import torch
@@ -478,6 +497,8 @@ def run_suite(args):
         run_suite_decode(device, stream, flush, emit, peak)
     elif args.suite_part == "multi":
         run_suite_multi(device, stream, flush, emit, peak)
+    elif args.suite_part == "cascade":
+        run_suite_cascade(device, stream, flush, emit, peak)
     if args.suite_part in ("all", "prefill"):
         run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind)
     return 0
@@ -535,49 +556,7 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
                   "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
 
-    # the shared-prefix mix, attention only: the plain decode vs the cascade (each group's shared prefix read once)
-    _, _, pws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
-    pwsb = torch.zeros(max(pws, 16), dtype=torch.uint8, device=device)
-    plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, pwsb,
-                                               max_ctx)
-    us_plain = _timed_calls(plain, 20, flush, stream)
-    gs, sh, mxs = kvc.kv_cascade_groups(res["block_table"], mix.ctx)
-    gs_d, sh_d = torch.from_numpy(gs).to(device), torch.from_numpy(sh).to(device)
-    cws = kvc.paged_decode_cascade_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx, len(gs) - 1, mxs)
-    cwsb = torch.zeros(max(cws, 16), dtype=torch.uint8, device=device)
-    casc = lambda: kvc.paged_decode_cascade_attention(q, res["k_cache"], res["v_cache"], table, ctx, gs_d, sh_d, mxs,
-                                                      mix.scale, out, cwsb, max_ctx)
-    us_casc = _timed_calls(casc, 20, flush, stream)
-    shared_reads = int(sum(int(sh[b]) for b in range(mix.B)) - sum(int(sh[gs[g]]) for g in range(len(gs) - 1)))
-    emit({"config": "shared-prefix mix, attention only: plain decode vs cascade (shared prefix blocks read once per group)",
-          "us_plain": us_plain, "us_cascade": us_casc, "speedup": us_plain / us_casc,
-          "groups": len(gs) - 1, "max_shared_blocks": mxs,
-          "block_reads_saved": shared_reads * mix.Hkv, "bytes_saved": shared_reads * 16 * row,
-          "logical_GBps_plain": logical / (us_plain * 1e-6) / 1e9,
-          "logical_GBps_cascade": logical / (us_casc * 1e-6) / 1e9})
-
-    # a long shared prefix (not a listed config): 8 groups x 8 sequences share 8192 tokens, 1..200 private
-    cw = workloads.cascade_decode(4242, [8] * 8, [512] * 8, list(np.random.default_rng(7).integers(1, 201, size=64)))
-    cq, ckp, cvp = (torch.from_numpy(x).to(device) for x in (cw.q, cw.k_pool, cw.v_pool))
-    ctb, cct = torch.from_numpy(cw.block_table).to(device), torch.from_numpy(cw.ctx).to(device)
-    cgs, csh = torch.from_numpy(cw.group_start).to(device), torch.from_numpy(cw.shared_blocks).to(device)
-    cout = torch.empty((64, cw.Hq, cw.D), dtype=torch.float16, device=device)
-    cmax = int(cw.ctx.max())
-    _, _, pws2 = kvc.paged_decode_plan(64, cw.Hq, cw.Hkv, cw.D, cmax)
-    pw2 = torch.zeros(max(pws2, 16), dtype=torch.uint8, device=device)
-    cws2 = kvc.paged_decode_cascade_plan(64, cw.Hq, cw.Hkv, cw.D, cmax, 8, 512)
-    cw2 = torch.zeros(max(cws2, 16), dtype=torch.uint8, device=device)
-    us_p = _timed_calls(lambda: kvc.paged_decode_attention(cq, ckp, cvp, ctb, cct, cw.scale, cout, pw2, cmax), 20,
-                        flush, stream)
-    us_c = _timed_calls(lambda: kvc.paged_decode_cascade_attention(cq, ckp, cvp, ctb, cct, cgs, csh, 512, cw.scale,
-                                                                   cout, cw2, cmax), 20, flush, stream)
-    lb = int(cw.ctx.astype(np.int64).sum()) * row
-    ub = (8 * 512 * 16 + int(sum(int(c) - 8192 for c in cw.ctx))) * row
-    emit({"config": "supplementary (not a listed config): 8 groups x 8 sequences sharing an 8192-token prefix, "
-                    "1..200 private tokens each, 14 q / 2 KV heads, D=64",
-          "us_plain": us_p, "us_cascade": us_c, "speedup": us_p / us_c, "logical_bytes": lb, "unique_bytes": ub,
-          "logical_GBps_plain": lb / (us_p * 1e-6) / 1e9, "unique_GBps_cascade": ub / (us_c * 1e-6) / 1e9})
-    del ckp, cvp
+    run_suite_cascade(device, stream, flush, emit, peak, mix, res)
 
     run_suite_multi(device, stream, flush, emit, peak)
 
@@ -700,6 +679,77 @@ def run_suite_decode(device, stream, flush, emit, peak):
 
 
 
+def run_suite_cascade(device, stream, flush, emit, peak, mix=None, res=None):
+    """Cascade decode against the plain decode: per call with L2 flushed, and the same call replayed from a CUDA
+    graph (launch overlap between its kernels), L2 flushed before each replay."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    import workloads
+    from paged_kv_cache_27_gb300 import harness
+
+    if mix is None:
+        mix = workloads.shared_prefix_mix()
+        res = harness.serving_mix(mix, device=device, poison=False)
+    table = torch.from_numpy(res["block_table"]).to(device)
+    ctx = torch.from_numpy(mix.ctx).to(device)
+    q = torch.from_numpy(mix.q).to(device)
+    out = torch.empty((mix.B, mix.Hq, mix.D), dtype=torch.float16, device=device)
+    max_ctx = int(mix.ctx.max())
+    row = 2 * mix.Hkv * mix.D * 2  # K + V bytes per token
+    logical = int(mix.ctx.astype(np.int64).sum()) * row
+    # the shared-prefix mix, attention only: the plain decode vs the cascade (each group's shared prefix read once)
+    _, _, pws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
+    pwsb = torch.zeros(max(pws, 16), dtype=torch.uint8, device=device)
+    plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, pwsb,
+                                               max_ctx)
+    us_plain = _timed_calls(plain, 20, flush, stream)
+    gs, sh, mxs = kvc.kv_cascade_groups(res["block_table"], mix.ctx)
+    gs_d, sh_d = torch.from_numpy(gs).to(device), torch.from_numpy(sh).to(device)
+    cws = kvc.paged_decode_cascade_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx, len(gs) - 1, mxs)
+    cwsb = torch.zeros(max(cws, 16), dtype=torch.uint8, device=device)
+    casc = lambda: kvc.paged_decode_cascade_attention(q, res["k_cache"], res["v_cache"], table, ctx, gs_d, sh_d, mxs,
+                                                      mix.scale, out, cwsb, max_ctx)
+    us_casc = _timed_calls(casc, 20, flush, stream)
+    us_plain_g = _timed_calls(_graph_of(plain, device), 20, flush, stream)
+    us_casc_g = _timed_calls(_graph_of(casc, device), 20, flush, stream)
+    shared_reads = int(sum(int(sh[b]) for b in range(mix.B)) - sum(int(sh[gs[g]]) for g in range(len(gs) - 1)))
+    emit({"config": "shared-prefix mix, attention only: plain decode vs cascade (shared prefix blocks read once per group)",
+          "us_plain": us_plain, "us_cascade": us_casc, "speedup": us_plain / us_casc,
+          "us_plain_graph": us_plain_g, "us_cascade_graph": us_casc_g, "speedup_graph": us_plain_g / us_casc_g,
+          "groups": len(gs) - 1, "max_shared_blocks": mxs,
+          "block_reads_saved": shared_reads * mix.Hkv, "bytes_saved": shared_reads * 16 * row,
+          "logical_GBps_plain": logical / (us_plain * 1e-6) / 1e9,
+          "logical_GBps_cascade": logical / (us_casc * 1e-6) / 1e9})
+
+    # a long shared prefix (not a listed config): 8 groups x 8 sequences share 8192 tokens, 1..200 private
+    cw = workloads.cascade_decode(4242, [8] * 8, [512] * 8, list(np.random.default_rng(7).integers(1, 201, size=64)))
+    cq, ckp, cvp = (torch.from_numpy(x).to(device) for x in (cw.q, cw.k_pool, cw.v_pool))
+    ctb, cct = torch.from_numpy(cw.block_table).to(device), torch.from_numpy(cw.ctx).to(device)
+    cgs, csh = torch.from_numpy(cw.group_start).to(device), torch.from_numpy(cw.shared_blocks).to(device)
+    cout = torch.empty((64, cw.Hq, cw.D), dtype=torch.float16, device=device)
+    cmax = int(cw.ctx.max())
+    _, _, pws2 = kvc.paged_decode_plan(64, cw.Hq, cw.Hkv, cw.D, cmax)
+    pw2 = torch.zeros(max(pws2, 16), dtype=torch.uint8, device=device)
+    cws2 = kvc.paged_decode_cascade_plan(64, cw.Hq, cw.Hkv, cw.D, cmax, 8, 512)
+    cw2 = torch.zeros(max(cws2, 16), dtype=torch.uint8, device=device)
+    us_p = _timed_calls(lambda: kvc.paged_decode_attention(cq, ckp, cvp, ctb, cct, cw.scale, cout, pw2, cmax), 20,
+                        flush, stream)
+    plain2 = lambda: kvc.paged_decode_attention(cq, ckp, cvp, ctb, cct, cw.scale, cout, pw2, cmax)
+    casc2 = lambda: kvc.paged_decode_cascade_attention(cq, ckp, cvp, ctb, cct, cgs, csh, 512, cw.scale, cout, cw2, cmax)
+    us_c = _timed_calls(casc2, 20, flush, stream)
+    us_pg = _timed_calls(_graph_of(plain2, device), 20, flush, stream)
+    us_cg = _timed_calls(_graph_of(casc2, device), 20, flush, stream)
+    lb = int(cw.ctx.astype(np.int64).sum()) * row
+    ub = (8 * 512 * 16 + int(sum(int(c) - 8192 for c in cw.ctx))) * row
+    emit({"config": "supplementary (not a listed config): 8 groups x 8 sequences sharing an 8192-token prefix, "
+                    "1..200 private tokens each, 14 q / 2 KV heads, D=64",
+          "us_plain": us_p, "us_cascade": us_c, "speedup": us_p / us_c,
+          "us_plain_graph": us_pg, "us_cascade_graph": us_cg, "speedup_graph": us_pg / us_cg,
+          "logical_bytes": lb, "unique_bytes": ub,
+          "logical_GBps_plain": lb / (us_p * 1e-6) / 1e9, "unique_GBps_cascade": ub / (us_c * 1e-6) / 1e9})
+    del ckp, cvp
+
+
 def run_suite_multi(device, stream, flush, emit, peak):
     import torch
     import paged_kv_cache_27_gb300 as kvc
@@ -805,8 +855,9 @@ def main():
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")
     ap.add_argument("--suite", action="store_true",
                     help="instead of the headline line: one JSON line per further configuration (1, 3, 4, 5)")
-    ap.add_argument("--suite-part", choices=["all", "decode", "prefill", "multi"], default="all",
-                    help="decode: every decode configuration (multi-token included); multi: the multi-token lines only")
+    ap.add_argument("--suite-part", choices=["all", "decode", "prefill", "multi", "cascade"], default="all",
+                    help="decode: every decode configuration (multi-token and cascade included); multi / cascade: "
+                         "those lines only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -330,10 +330,9 @@ kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const 
  * history before that kernel has finished, and q, k_new, v_new, the
  * workspace and out only after.  A decode kernel releases its own
  * dependents once its dependency wait has passed and its warps have taken
- * their first blocks (the cascade kernel as soon as it starts), so in an
- * unbroken run of decode calls on one stream (no other kernel, copy or event
- * between them) a call may start before earlier calls of the run have
- * finished.  Contract: no kernel of that run, nor the kernel launched just
+ * their first blocks, so in an unbroken run of decode calls on one stream (no
+ * other kernel, copy or event between them) a call may start before earlier
+ * calls of the run have finished.  Contract: no kernel of that run, nor the kernel launched just
  * before the run, writes a call's
  * block table, context lengths or the cache rows it reads (other than
  * through that call's own append).  One call per layer, every layer a

@@ -87,13 +87,14 @@ cudaError_t launch_decode_suffix(const DecodeArgs& a, const DecodePlan& plan, co
                                  int part_stride, float* part_ml, float* part_acc, cudaStream_t stream);
 
 // Cascade decode: groups of at most 8 consecutive sequences whose block-table rows begin with the same
-// shared blocks. The prefix kernel reads those blocks once per group; the decode kernel covers each
-// sequence's remaining blocks; the combine kernel merges both.
+// shared blocks. The group kernel (group.cu) reads those blocks once per group for all its sequences; the
+// decode kernel covers each sequence's remaining blocks; the combine kernel merges both.
 constexpr int kMaxGroupSize = 8;
 struct CascadePlan {
     DecodePlan suffix;  // the decode kernel over every sequence's blocks past its shared prefix
     int chunk;          // shared blocks per prefix CTA
-    int nchunks;        // prefix parts per (sequence, head): chunks of the longest shared prefix
+    int cluster;        // prefix CTAs per cluster (one prefix part per cluster)
+    int nchunks;        // prefix parts per (sequence, head): clusters over the longest shared prefix
     int part_stride;    // partial rows per (sequence, head): nchunks + suffix.num_parts
     size_t workspace_bytes;
 };
@@ -103,7 +104,7 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);
 
-// Multi-token decode (multi.cu): q_len (1..8) new tokens per sequence, causal among them (token t at
+// Multi-token decode (group.cu): q_len (1..8) new tokens per sequence, causal among them (token t at
 // position ctx - q_len + t); q and out are [B][q_len][Hq][D]. A CTA's warps split a chunk of a sequence's
 // blocks and each carries all the tokens' query rows of its KV head, so every block is read once for all
 // tokens; the CTAs of a cluster merge in distributed shared memory, and the combine kernel merges the
