@@ -62,8 +62,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "5984d6bd262edff8fd490dd7b147c4276678c81fd39ad6b8dca9f599e8b6fe5f",
-                      "bytes_per_launch": 33674496}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "405de94d82f6c3dbb265bbda0dcf7159e4e6c132b58a26f93031530ac65a3019",
+                      "bytes_per_launch": 33675520}
 
 
 def decode_sources_sha256() -> str:
