@@ -1,5 +1,6 @@
 // Decode over query rows that share their key blocks, on sm_103a: the multi-token decode (the q_len new tokens of
-// one sequence) and the cascade decode's shared-prefix pass (the sequences of one group).
+// one sequence) and the cascade decode's shared-prefix pass (the sequences of one group; with head dim 64 and
+// groups of 17 or more query rows that pass runs on the tensor cores instead, group_tc.cu).
 //
 // Multi-token decode: q_len new tokens per sequence attend over the paged cache at once, causally among
 // themselves (token t sits at position ctx - q_len + t and sees keys 0 .. ctx - q_len + t).  Speculative
@@ -20,6 +21,7 @@
 // multi-token cluster that covers the whole context writes the output; otherwise each cluster writes a partial
 // state and the combine kernel (decode.cu) merges them.
 #include "decode_common.cuh"
+#include "group_tc.h"
 
 namespace kvc {
 
@@ -43,6 +45,9 @@ namespace kvc {
 #endif
 #ifndef KVC_MULTI_CTAS  // CTAs per SM the chunking aims for (one where a CTA needs the SM's registers)
 #define KVC_MULTI_CTAS 2
+#endif
+#ifndef KVC_PREFIX_TC_MIN_ROWS  // cascade prefix, head dim 64: groups of this many query rows run on the tensor cores
+#define KVC_PREFIX_TC_MIN_ROWS 17
 #endif
 
 constexpr int kMultiMaxChunk = 2048;  // blocks per CTA at most (their ids are in shared memory)
@@ -563,6 +568,40 @@ static GroupKernelParams group_params(const DecodeArgs& a, float* part_ml, float
     return p;
 }
 
+// the cascade prefix on the tensor cores (group_tc.cu): head dim 64, groups of up to `rows` query rows
+static bool use_tc_prefix(int D, int rows) { return D == gtc::D && rows >= KVC_PREFIX_TC_MIN_ROWS; }
+
+// chunking for the tensor-core prefix pass: one CTA per SM over all (group, KV head) pairs, whole 128-key tiles
+static void tc_chunks(int64_t units, int64_t nblk, int sms, int* chunk, int* nchunks) {
+    const int64_t per_unit = std::max<int64_t>(1, sms / std::max<int64_t>(1, units));
+    int64_t c = (std::max<int64_t>(1, nblk) + per_unit - 1) / per_unit;
+    c = (c + gtc::kChunkAlign - 1) / gtc::kChunkAlign * gtc::kChunkAlign;
+    *chunk = static_cast<int>(std::min<int64_t>(gtc::kMaxChunk, c));
+    *nchunks = static_cast<int>((std::max<int64_t>(1, nblk) + *chunk - 1) / *chunk);
+}
+
+static gtc::Params tc_params(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
+                             float* part_ml, float* part_acc, int chunk, int nchunks, int part_stride) {
+    gtc::Params p;
+    p.q = a.q;
+    p.block_table = a.block_table;
+    p.group_start = group_start;
+    p.blk_off = shared_blocks;
+    p.part_ml = part_ml;
+    p.part_acc = part_acc;
+    p.err = a.err;
+    p.max_blocks = a.max_blocks;
+    p.num_blocks = a.num_blocks;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.chunk = chunk;
+    p.nchunks = nchunks;
+    p.part_stride = part_stride;
+    p.scale_log2 = a.scale * kLog2e;
+    return p;
+}
+
 // ---- multi-token decode ------------------------------------------------------------------------------
 cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, MultiPlan* plan) {
     const int sms = sm_count();
@@ -594,8 +633,9 @@ static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPla
     if (e != cudaSuccess) return e;
     const size_t nrow = static_cast<size_t>(a.B) * q_len * a.Hq * mp.nclus;
     float* part_ml = static_cast<float*>(a.workspace);
-    float* part_acc = mp.nclus > 1 ? partials_acc(part_ml, nrow) : nullptr;
-    GroupKernelParams p = group_params(a, mp.nclus > 1 ? part_ml : nullptr, part_acc);
+    const bool parts = mp.nclus > 1;  // partial states and the combine kernel
+    float* part_acc = parts ? partials_acc(part_ml, nrow) : nullptr;
+    GroupKernelParams p = group_params(a, parts ? part_ml : nullptr, part_acc);
     p.q_len = q_len;
     p.chunk = mp.chunk;
     p.cs = mp.cluster;
@@ -605,7 +645,7 @@ static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPla
     group_tiles(D, q_len * p.G, &nt, &nrg);
     e = launch_group_nt<D, false>(nt, tmK, tmV, p, dim3(nrg * mp.nclus * mp.cluster, a.Hkv, a.B),
                                   launch_overlap() != 0, stream);
-    if (e != cudaSuccess || mp.nclus == 1) return e;
+    if (e != cudaSuccess || !parts) return e;
     // several clusters per context: merge their partial states
     CombineParams c;
     c.part_ml = part_ml;
@@ -650,8 +690,14 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_group
     // prefix rows: up to kMaxGroupSize sequences x G heads per (group, KV head)
     int nt, nrg;
     group_tiles(D, kMaxGroupSize * (Hq / Hkv), &nt, &nrg);
-    group_chunks(D, nt, static_cast<int64_t>(std::max(n_groups, 1)) * Hkv * nrg, max_shared_blocks, sms, &plan->chunk,
-                 &plan->cluster, &plan->nchunks);
+    if (use_tc_prefix(D, kMaxGroupSize * (Hq / Hkv))) {
+        tc_chunks(static_cast<int64_t>(std::max(n_groups, 1)) * Hkv, max_shared_blocks, sms, &plan->chunk,
+                  &plan->nchunks);
+        plan->cluster = 1;
+    } else {
+        group_chunks(D, nt, static_cast<int64_t>(std::max(n_groups, 1)) * Hkv * nrg, max_shared_blocks, sms,
+                     &plan->chunk, &plan->cluster, &plan->nchunks);
+    }
     if (max_shared_blocks <= 0) plan->nchunks = 0;
     plan->part_stride = plan->nchunks + plan->suffix.num_parts;
     plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * Hq * plan->part_stride, D);
@@ -673,17 +719,23 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
         if (e != cudaSuccess) return e;
         e = make_tile_map(&tmV, a.v_cache, D, rows);
         if (e != cudaSuccess) return e;
-        GroupKernelParams p = group_params(a, part_ml, part_acc);
-        p.group_start = group_start;
-        p.blk_off = shared_blocks;
-        p.chunk = cp.chunk;
-        p.cs = cp.cluster;
-        p.nclus = cp.nchunks;
-        p.part_stride = cp.part_stride;
-        int nt, nrg;
-        group_tiles(D, kMaxGroupSize * p.G, &nt, &nrg);
-        e = launch_group_nt<D, true>(nt, tmK, tmV, p, dim3(nrg * cp.nchunks * cp.cluster, a.Hkv, n_groups),
-                                     launch_overlap() != 0, stream);
+        if (use_tc_prefix(D, kMaxGroupSize * (a.Hq / a.Hkv))) {  // as cascade_plan chose
+            const gtc::Params tp = tc_params(a, group_start, shared_blocks, part_ml, part_acc, cp.chunk, cp.nchunks,
+                                             cp.part_stride);
+            e = gtc::launch(tmK, tmV, tp, dim3(cp.nchunks, a.Hkv, n_groups), launch_overlap() != 0, stream);
+        } else {
+            GroupKernelParams p = group_params(a, part_ml, part_acc);
+            p.group_start = group_start;
+            p.blk_off = shared_blocks;
+            p.chunk = cp.chunk;
+            p.cs = cp.cluster;
+            p.nclus = cp.nchunks;
+            p.part_stride = cp.part_stride;
+            int nt, nrg;
+            group_tiles(D, kMaxGroupSize * p.G, &nt, &nrg);
+            e = launch_group_nt<D, true>(nt, tmK, tmV, p, dim3(nrg * cp.nchunks * cp.cluster, a.Hkv, n_groups),
+                                         launch_overlap() != 0, stream);
+        }
         if (e != cudaSuccess) return e;
     }
     // 2. every sequence past its shared blocks: suffix parts from nchunks on
