@@ -123,3 +123,20 @@ def test_cascade_unchecked_oversized_group_sets_flag():
     wl9 = workloads.cascade_decode(9, [9], [2], [3] * 9)
     run_cascade(wl9, checked=False)
     assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["CONTEXT"]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 14, 2), (128, 8, 8)])
+def test_cascade_unchecked_bad_shared_block_flagged(D, Hq, Hkv):
+    """Unchecked, an out-of-range id among a group's shared blocks is skipped and flagged, every output stays finite,
+    and the other group is still right (D = 64 runs the tensor-core prefix pass, D = 128 the mma.sync one)."""
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_device_error_flags(clear=True)
+    wl = workloads.cascade_decode(21, [4, 4], [6, 3], [5] * 8, Hq=Hq, Hkv=Hkv, D=D)
+    bad = wl.block_table.copy()
+    bad[:4, 2] = wl.NB + 7  # the first group's third shared block, in every member's row
+    wl_bad = workloads.CascadeWorkload(**{**wl.__dict__, "block_table": bad})
+    out, _ = run_cascade(wl_bad, checked=False)
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["BLOCK_ID"]
+    assert torch.isfinite(out).all()
+    ref = oracle_out(wl)
+    check_attention(out[4:], ref[4:], f"cascade D={D}, the group without the bad block")
