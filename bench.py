@@ -821,11 +821,13 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
         fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo,
                                            precise=precise)
         us = _timed_calls(fn, 20, flush, stream)
+        us_g = _timed_calls(_graph_of(fn, device), 20, flush, stream)  # device time: the call replayed from a graph
         pairs = sum(s * (s + 1) // 2 for s in seqlens) if causal else sum(s * s for s in seqlens)
         flops = 4 * D * Hq * pairs
         tf = flops / (us * 1e-6) / 1e12
         emit({"config": name, "p_precision": "split (fp16 high part + residual)" if precise else "fp16",
               "us_per_call": us, "TFLOPs": tf, "pct_tensor_peak": tf / tflops_peak * 100,
+              "us_per_call_graph": us_g, "TFLOPs_graph": flops / (us_g * 1e-6) / 1e12,
               "flops": flops, "peak_TFLOPs": tflops_peak, "peak_kind": tflops_kind,
               "note": "algorithmic flops (masked half not counted)" + (
                   "; the split form's tensor work is 1.5x that (P V runs for both parts of P)" if precise else "")})
