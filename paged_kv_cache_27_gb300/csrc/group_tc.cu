@@ -115,10 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_tc_kernel(const __grid_con
         if (chunk == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
         return;  // the combine kernel writes these sequences' rows
     }
-    const int ctx = nsh * kBlockSize;
-    const int R = T * p.G;  // query rows, at most kMaxGroupSize x 8 = 64
-    const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
-    const int j0 = chunk * p.chunk;  // this CTA's blocks [j0, j0 + n) of the shared blocks
+    const int ctx = nsh * kBlockSize, nblk = nsh;  // keys and blocks of the shared prefix
+    const int R = T * p.G;                          // query rows, at most kMaxGroupSize x 8 = 64
+    const int j0 = chunk * p.chunk;                 // this CTA's blocks [j0, j0 + n) of the shared blocks
     if (j0 >= nblk) return;          // the group shares fewer blocks
     const int n = min(nblk, j0 + p.chunk) - j0;
     const int nt = (n + kTileBlocks - 1) / kTileBlocks;  // key tiles
