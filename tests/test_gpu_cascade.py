@@ -140,3 +140,17 @@ def test_cascade_unchecked_bad_shared_block_flagged(D, Hq, Hkv):
     assert torch.isfinite(out).all()
     ref = oracle_out(wl)
     check_attention(out[4:], ref[4:], f"cascade D={D}, the group without the bad block")
+
+
+@pytest.mark.parametrize("scale_sign", [1.0, -1.0])
+def test_cascade_full_group_rows_and_scale_sign(scale_sign):
+    """Groups of 8 sequences with 8 query heads per KV head: 64 query rows, two full TMEM lane quarters of the
+    tensor-core prefix pass; a negative scale as well (the running max then comes from the smallest score)."""
+    import dataclasses
+    extra = list(np.random.default_rng(31).integers(1, 300, size=19))
+    wl = workloads.cascade_decode(31, [8, 8, 3], [40, 9, 17], extra, Hq=16, Hkv=2, D=64)
+    wl = dataclasses.replace(wl, scale=scale_sign * wl.scale)
+    out, pout = run_cascade(wl)
+    ref = oracle_out(wl)
+    check_attention(out, ref, f"cascade, 64 rows, scale sign {scale_sign}")
+    assert (out - pout).abs().max().item() < 1e-4
