@@ -1,0 +1,94 @@
+"""Launch overlap (programmatic dependent launch) on the multi-token and cascade paths: calls chained in a CUDA
+graph, each call's q being the previous call's output, so a kernel that read q before its dependency wait would
+see the previous replay's values.  Each call is checked against the oracle on the q it actually received."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def _graph(fn):
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_set_launch_overlap(True)
+    try:
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+    finally:
+        kvc.kvc_set_launch_overlap(False)
+    return g
+
+
+@pytest.mark.parametrize("T,ctx", [(2, [40, 2049, 300]), (5, [5, 16, 17, 20000])])
+def test_multi_token_chain_in_graph(T, ctx):
+    import paged_kv_cache_27_gb300 as kvc
+    wl = workloads.multi_token_decode(41 + T, ctx, T)
+    dev = "cuda"
+    kp, vp = torch.from_numpy(wl.k_pool).to(dev), torch.from_numpy(wl.v_pool).to(dev)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
+    max_ctx = int(wl.ctx.max())
+    ws = torch.zeros(max(kvc.paged_decode_multi_plan(len(ctx), wl.Hq, wl.Hkv, wl.D, max_ctx, T), 16),
+                     dtype=torch.uint8, device=dev)
+    q0 = torch.from_numpy(wl.q).to(dev)
+    outs = [torch.empty_like(q0) for _ in range(3)]  # call i reads outs[i - 1] (q0 for the first)
+
+    def chain():
+        src = q0
+        for o in outs:
+            kvc.paged_decode_multi_attention(src, kp, vp, table, ctx_d, wl.scale, o, ws, max_ctx)
+            src = o
+    g = _graph(chain)
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    src = wl.q
+    for i, o in enumerate(outs):
+        ref = oracle.decode_multi(src, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+        check_attention(o.reshape(-1, wl.Hq, wl.D), ref.reshape(-1, wl.Hq, wl.D), f"multi-token chain call {i}")
+        src = o.cpu().numpy()  # the next call's q, as the GPU wrote it
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 14, 2), (128, 8, 8)])
+def test_cascade_chain_in_graph(D, Hq, Hkv):
+    import paged_kv_cache_27_gb300 as kvc
+    extra = list(np.random.default_rng(5).integers(1, 200, size=16))
+    wl = workloads.cascade_decode(43, [8, 5, 3], [40, 7, 0], extra, Hq=Hq, Hkv=Hkv, D=D)
+    dev = "cuda"
+    B = len(extra)
+    kp, vp = torch.from_numpy(wl.k_pool).to(dev), torch.from_numpy(wl.v_pool).to(dev)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
+    gs, sh = torch.from_numpy(wl.group_start).to(dev), torch.from_numpy(wl.shared_blocks).to(dev)
+    mx = int(wl.shared_blocks.max())
+    max_ctx = int(wl.ctx.max())
+    ws = torch.zeros(max(kvc.paged_decode_cascade_plan(B, Hq, Hkv, D, max_ctx, len(wl.group_start) - 1, mx), 16),
+                     dtype=torch.uint8, device=dev)
+    q0 = torch.from_numpy(wl.q).to(dev)
+    outs = [torch.empty_like(q0) for _ in range(3)]
+
+    def chain():
+        src = q0
+        for o in outs:
+            kvc.paged_decode_cascade_attention(src, kp, vp, table, ctx_d, gs, sh, mx, wl.scale, o, ws, max_ctx)
+            src = o
+    g = _graph(chain)
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    src = wl.q
+    for i, o in enumerate(outs):
+        ref = oracle.decode(src, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+        check_attention(o, ref, f"cascade chain call {i}, D={D}")
+        src = o.cpu().numpy()
