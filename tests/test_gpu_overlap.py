@@ -1,4 +1,4 @@
-"""Launch overlap (programmatic dependent launch) on the multi-token and cascade paths: calls chained in a CUDA
+"""Launch overlap (programmatic dependent launch) on the multi-token, cascade and fp8 paths: calls chained in a CUDA
 graph, each call's q being the previous call's output, so a kernel that read q before its dependency wait would
 see the previous replay's values.  Each call is checked against the oracle on the q it actually received."""
 import numpy as np
@@ -91,4 +91,38 @@ def test_cascade_chain_in_graph(D, Hq, Hkv):
     for i, o in enumerate(outs):
         ref = oracle.decode(src, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
         check_attention(o, ref, f"cascade chain call {i}, D={D}")
+        src = o.cpu().numpy()
+
+
+def test_fp8_decode_chain_in_graph():
+    """The fp8-cache decode chained the same way (contexts over one cluster, so the combine kernel runs too)."""
+    import paged_kv_cache_27_gb300 as kvc
+    from test_gpu_fp8 import quantized_cache, v_natural
+    wl = workloads.multi_token_decode(47, [3000, 17, 40000, 2048], 1)
+    kc, vc, ks, vs, _ = quantized_cache(wl)
+    dev = "cuda"
+    B = len(wl.ctx)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
+    max_ctx = int(wl.ctx.max())
+    _, _, w = kvc.paged_decode_plan(B, wl.Hq, wl.Hkv, wl.D, max_ctx)
+    ws = torch.zeros(max(w, 16), dtype=torch.uint8, device=dev)
+    q0 = torch.from_numpy(np.ascontiguousarray(wl.q[:, 0])).to(dev)
+    outs = [torch.empty_like(q0) for _ in range(3)]
+
+    def chain():
+        src = q0
+        for o in outs:
+            kvc.paged_decode_attention_fp8(src, kc, vc, ks, vs, table, ctx_d, wl.scale, o, ws, max_ctx)
+            src = o
+    g = _graph(chain)
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    src = wl.q[:, 0]
+    for i, o in enumerate(outs):
+        ref = oracle.decode_fp8(src, kc.cpu().numpy(), v_natural(vc), ks.cpu().numpy(), vs.cpu().numpy(),
+                                wl.block_table, wl.ctx, wl.scale)
+        check_attention(o, ref, f"fp8 chain call {i}")
         src = o.cpu().numpy()
