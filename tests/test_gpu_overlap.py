@@ -1,6 +1,7 @@
 """Launch overlap (programmatic dependent launch) on the multi-token, cascade and fp8 paths: calls chained in a CUDA
-graph, each call's q being the previous call's output, so a kernel that read q before its dependency wait would
-see the previous replay's values.  Each call is checked against the oracle on the q it actually received."""
+graph, each call's q being the previous call's output (filled with NaN before the replay), so a kernel that read
+q before its dependency wait would see NaN or a partly written q.  Each call is checked against the oracle on the q
+it actually received."""
 import numpy as np
 import pytest
 import torch
