@@ -665,23 +665,26 @@ template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const CombineParams p) {
     constexpr int V = D / 32;  // dims per lane
     __shared__ float sM[8], sL[8], sO[8][D];
-    grid_dependency_wait();
     const int h = blockIdx.x, y = blockIdx.y, b = y / p.q_len;  // y: the query row (a sequence's token)
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // context lengths and prefix offsets are never written by the kernel before (the launch-overlap contract):
+    // they are read before the dependency wait, the parts and the output only after it
     const int ctx_full = p.context_lens[b];
     const int off = p.blk_off != nullptr ? p.blk_off[b] : 0;
     const int ctx = ctx_full - off * kBlockSize;  // tokens of the suffix parts
-    if (off < 0 || off >= p.max_blocks || ctx_full < p.q_len || ctx_full > p.max_blocks * kBlockSize ||
-        ctx_full > p.max_ctx || ctx < 1) {
+    const bool bad = off < 0 || off >= p.max_blocks || ctx_full < p.q_len || ctx_full > p.max_blocks * kBlockSize ||
+                     ctx_full > p.max_ctx || ctx < 1;
+    const int nsuf = bad ? 0 : ((ctx + kBlockSize - 1) / kBlockSize + p.bpc - 1) / p.bpc;
+    const int npre = off > 0 && p.prefix_chunk > 0 ? (off + p.prefix_chunk - 1) / p.prefix_chunk : 0;
+    if (!bad && !p.cascade && nsuf <= 1) return;  // the cluster wrote the output itself
+    grid_dependency_wait();
+    if (bad) {
         if (p.cascade) {  // the attention kernels left this row to us
             if (h == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
             if (threadIdx.x < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + threadIdx.x, 0.f);
         }
         return;
     }
-    const int nsuf = ((ctx + kBlockSize - 1) / kBlockSize + p.bpc - 1) / p.bpc;
-    const int npre = off > 0 && p.prefix_chunk > 0 ? (off + p.prefix_chunk - 1) / p.prefix_chunk : 0;
-    if (!p.cascade && nsuf <= 1) return;  // the cluster wrote the output itself
     const int64_t row0 = (static_cast<int64_t>(y) * p.Hq + h) * p.part_stride;
     float M = -INFINITY, L = 0.f, O[V];
 #pragma unroll
