@@ -62,8 +62,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "405de94d82f6c3dbb265bbda0dcf7159e4e6c132b58a26f93031530ac65a3019",
-                      "bytes_per_launch": 33675520}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "a0cd586161d6516ebf4d80e1dc9454c0642f8df9da0f7bf6f4420ddf1985d0aa",
+                      "bytes_per_launch": 33675008}
 
 
 def decode_sources_sha256() -> str:
