@@ -324,21 +324,45 @@ kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const 
                                       int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
                                       void* stream);
 
-/* Launch overlap (process-wide, default off).  When on, decode kernels are
- * launched as programmatic dependents of the kernel before them on the
- * stream: they read block tables, context lengths and the cached K/V
- * history before that kernel has finished, and q, k_new, v_new, the
- * workspace and out only after.  A decode kernel releases its own
+/* Launch overlap (process-wide, default off).  When on, decode kernels (and
+ * kvc_copy_async's copies) are launched as programmatic dependents of the
+ * kernel before them on the stream: they read block tables, context lengths
+ * and the cached K/V history before that kernel has finished, and q, k_new,
+ * v_new, the workspace and out only after.  A decode kernel releases its own
  * dependents once its dependency wait has passed and its warps have taken
  * their first blocks, so in an unbroken run of decode calls on one stream (no
- * other kernel, copy or event between them) a call may start before earlier
- * calls of the run have finished.  Contract: no kernel of that run, nor the kernel launched just
- * before the run, writes a call's
- * block table, context lengths or the cache rows it reads (other than
- * through that call's own append).  One call per layer, every layer a
- * different cache, meets this; calls on the same layer need something
- * between them (a copy, an event, another kernel). */
+ * other kernel, copy or event between them; kvc_copy_async calls excepted) a
+ * call may start before earlier calls of the run have finished.  Contract: no
+ * kernel of that run, nor the kernel launched just before the run, writes a
+ * call's block table, context lengths or the cache rows it reads (other than
+ * through that call's own append); a kvc_copy_async without KVC_COPY_AHEAD
+ * may, since it finishes its copy before anything after it starts.  One call
+ * per layer, every layer a different cache, meets this; calls on the same
+ * layer need something between them (a copy, an event, another kernel). */
 kvc_status kvc_set_launch_overlap(int on);
+
+/* Staging copy (no counterpart in the pages: an interface choice of this
+ * library, for steps whose inputs arrive in host memory).  Copies `bytes`
+ * from src to dst with a kernel on `stream`.  src and dst may each be device
+ * memory or pinned host memory (cudaHostAlloc / cudaHostRegister), which the
+ * GPU reads and writes directly over the host link; pageable host memory is
+ * refused.  Both 16-byte aligned, bytes a multiple of 16 (0: nothing to do),
+ * no overlap.  Being a kernel, the copy chains with the decode kernels under
+ * launch overlap with no copy-to-kernel dependency to resolve:
+ *   flags 0: the copy starts once the kernel before it on the stream has
+ *     finished, and the kernel after it may read the copied bytes at once,
+ *     even before its dependency wait (so block tables and context lengths
+ *     may be staged this way);
+ *   KVC_COPY_AHEAD: the copy starts at once, alongside the kernel before it,
+ *     which must neither read nor write src or dst; the call still counts as
+ *     finished only once that kernel has.  Later kernels may read the bytes
+ *     only after their dependency wait (q, k_new, v_new; not block tables,
+ *     context lengths or cache rows).
+ * With launch overlap off both forms are plain stream-ordered copies.
+ * Errors (synchronous): KVC_ERR_INVALID for null, misaligned, overlapping or
+ * pageable buffers and unknown flags; KVC_ERR_CUDA if the launch fails. */
+#define KVC_COPY_AHEAD 1u
+kvc_status kvc_copy_async(void* dst, const void* src, size_t bytes, unsigned flags, void* stream);
 
 /* Per-CTA timeline of decode launches (builds with -DKVC_TRACE=1 only;
  * otherwise KVC_ERR_UNSUPPORTED).  Each 80-byte record holds eight global-timer

@@ -28,7 +28,7 @@ __all__ = [
     "kv_block_release", "kv_block_refcount", "kv_block_num_free", "kv_cache_utilisation",
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
-    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_trace_read",
+    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_copy_async", "KVC_COPY_AHEAD", "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
     "prefill_attention", "prefill_attention_ex", "fp8_v_position", "DEVERR",
@@ -109,6 +109,7 @@ def _load():
         "paged_decode_append_attention": (I, [P, P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
                                               I, P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
+        "kvc_copy_async": (I, [P, P, SZ, ctypes.c_uint, P]),
         "paged_decode_attention_static_workspace": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
                                                         I, P]),
         "kvc_trace_read": (I, [P, I, PI, I]),
@@ -183,6 +184,31 @@ def kvc_set_checked_mode(on: bool) -> None:
 def kvc_set_launch_overlap(on: bool) -> None:
     """Launch decode kernels as programmatic dependents of the previous kernel (see include/kvc.h)."""
     _check(_lib.kvc_set_launch_overlap(int(bool(on))), "kvc_set_launch_overlap")
+
+
+KVC_COPY_AHEAD = 1
+
+
+def _stage_ptr(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not (t.is_cuda or t.device.type == "cpu"):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def kvc_copy_async(dst: torch.Tensor, src: torch.Tensor, ahead: bool = False, stream=None) -> None:
+    """Copy src's bytes into dst with the library's staging kernel (see include/kvc.h for the two orderings).
+
+    Each of dst and src is a CUDA tensor or a pinned CPU tensor; both hold the same number of bytes, a multiple
+    of 16, at 16-byte aligned addresses."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must hold the same number of bytes")
+    _check(_lib.kvc_copy_async(_stage_ptr(dst, "dst"), _stage_ptr(src, "src"), nbytes,
+                               KVC_COPY_AHEAD if ahead else 0, _stream(stream, dst, src)), "kvc_copy_async")
 
 
 TRACE_DTYPE = np.dtype([("t", "<u8", (8,)), ("seq", "<u4"), ("smid", "<u4"), ("x", "<u4"), ("yz", "<u4")])

@@ -377,6 +377,38 @@ kvc_status kvc_set_launch_overlap(int on) {
     return KVC_OK;
 }
 
+// The address the current device uses for p: device and managed memory as they are, pinned host memory
+// through its mapping.  False for pageable host memory and unknown pointers.
+static bool device_address(const void* p, void** out) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged && a.type != cudaMemoryTypeHost)
+        return false;
+    if (!a.devicePointer) return false;
+    *out = a.devicePointer;
+    return true;
+}
+
+kvc_status kvc_copy_async(void* dst, const void* src, size_t bytes, unsigned flags, void* stream) {
+    if (flags & ~KVC_COPY_AHEAD) return fail(KVC_ERR_INVALID, "unknown flags 0x%x", flags);
+    if (bytes == 0) return KVC_OK;
+    if (!dst || !src) return fail(KVC_ERR_INVALID, "null buffer");
+    if ((bytes & 15u) || !aligned16(dst) || !aligned16(src))
+        return fail(KVC_ERR_INVALID, "both buffers 16-byte aligned and bytes a multiple of 16 (got %zu)", bytes);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst), s0 = reinterpret_cast<uintptr_t>(src);
+    if (d0 < s0 + bytes && s0 < d0 + bytes) return fail(KVC_ERR_INVALID, "source and destination overlap");
+    void *ddev = nullptr, *sdev = nullptr;
+    if (!device_address(dst, &ddev)) return fail(KVC_ERR_INVALID, "dst is neither device nor pinned host memory");
+    if (!device_address(src, &sdev)) return fail(KVC_ERR_INVALID, "src is neither device nor pinned host memory");
+    cudaError_t e = kvc::launch_stage_copy(ddev, sdev, bytes, (flags & KVC_COPY_AHEAD) != 0,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "staging copy launch");
+    return KVC_OK;
+}
+
 static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
                                 const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
                                 const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,

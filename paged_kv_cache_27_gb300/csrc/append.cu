@@ -10,10 +10,13 @@
 // shared block first gets a private copy of the whole block.
 //
 // Both kernels are pure bandwidth: 16-byte vector loads/stores, consecutive
-// threads on consecutive 16-byte chunks of a row.
+// threads on consecutive 16-byte chunks of a row.  So is the staging copy at
+// the end of this file, which moves a decode step's inputs in from pinned host
+// memory (and its output back) inside the stream's kernel sequence.
 #include <atomic>
 
 #include "../../include/kvc.h"
+#include "decode_common.cuh"
 #include "kvc_internal.h"
 #include "ptx.cuh"
 
@@ -196,6 +199,59 @@ cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Copy of n16 16-byte vectors between device-accessible buffers (device memory, or pinned host memory that
+// the GPU reaches directly over the C2C link).  Four vectors in flight per thread: the loads of a host source
+// cross the link, so many requests must be outstanding to cover its latency.
+// ahead = 0: wait for the kernel before on the stream, copy, make the copy visible device-wide, then let the
+//   next kernel launch; that kernel may read the bytes even before its own dependency wait.
+// ahead = 1: let the next kernel launch and copy at once, then wait for the kernel before, so that this grid
+//   completes only after that one has; the next kernel may read the bytes after its dependency wait.
+// Without launch overlap both forms are plain stream-ordered copies (the waits return at once).
+constexpr int kCopyThreads = 128;
+constexpr int kCopyVec = 4;
+
+__global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(const uint4* __restrict__ src,
+                                                                  uint4* __restrict__ dst, int64_t n16,
+                                                                  int ahead) {
+    if (ahead)
+        grid_dependents_launch();
+    else
+        grid_dependency_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kCopyThreads * kCopyVec;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kCopyThreads * kCopyVec + threadIdx.x; base < n16;
+         base += stride) {
+        uint4 v[kCopyVec];
+#pragma unroll
+        for (int k = 0; k < kCopyVec; ++k) {
+            const int64_t i = base + static_cast<int64_t>(k) * kCopyThreads;
+            if (i < n16) v[k] = src[i];
+        }
+#pragma unroll
+        for (int k = 0; k < kCopyVec; ++k) {
+            const int64_t i = base + static_cast<int64_t>(k) * kCopyThreads;
+            if (i < n16) dst[i] = v[k];
+        }
+    }
+    if (ahead) {
+        grid_dependency_wait();
+    } else {
+        __threadfence();
+        __syncthreads();
+        grid_dependents_launch();
+    }
+}
+
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, bool ahead, cudaStream_t stream) {
+    const int64_t n16 = static_cast<int64_t>(bytes / 16);
+    const int64_t per_cta = static_cast<int64_t>(kCopyThreads) * kCopyVec;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t want = (n16 + per_cta - 1) / per_cta;
+    const unsigned grid = static_cast<unsigned>(want < 2 * sms ? want : 2 * sms);
+    return launch(stage_copy_kernel, dim3(grid), dim3(kCopyThreads), 0, stream, launch_overlap() != 0, 1u,
+                  static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16, ahead ? 1 : 0);
 }
 
 }  // namespace kvc

@@ -12,8 +12,9 @@ import numpy as np
 import torch
 
 from . import (KvcConfig, kv_append, kv_block_alloc, kv_block_release, kv_block_share, kv_cache_create,
-               kv_cache_destroy, kv_copy_blocks, kv_slot_mapping, kv_step_prepare, paged_decode_append_attention,
-               paged_decode_attention, paged_decode_plan, paged_decode_workspace_init, prefill_attention)
+               kv_cache_destroy, kv_copy_blocks, kvc_copy_async, kv_slot_mapping, kv_step_prepare,
+               paged_decode_append_attention, paged_decode_attention, paged_decode_plan, paged_decode_workspace_init,
+               prefill_attention)
 
 F16_NAN = 0x7E00  # a quiet-NaN bit pattern used to poison cache slots nobody owns
 
@@ -222,3 +223,88 @@ def prefill_then_decode(wl, causal=True, device="cuda", out_dtype=torch.float32,
         return {"prefill_out": out, "decode_out": dec, "k_cache": k_pool[0], "v_cache": v_pool[0]}
     finally:
         kv_cache_destroy(h)
+
+
+def _align16(n: int) -> int:
+    return (n + 15) & ~15
+
+
+class HostStep:
+    """A DecodeSession's step fed from pinned host memory, its output returned there, with the copies overlapped
+    with the calls as a serving loop whose inputs arrive from the host would run it.
+
+    The step's inputs sit in one pinned host buffer: a header (block table, context lengths, append slots),
+    then per layer that layer's q, k_new and v_new, each 16-byte aligned.  A device buffer has the same layout
+    and every call receives views into it.  Every copy is a staging copy (kvc_copy_async: a kernel that reads or
+    writes the pinned buffer over the host link) in the stream's kernel sequence.  In: the header with layers 0
+    and 1 before layer 0's call, every later layer ahead, alongside layer 0's call.  Out: the outputs of layers
+    [lo, hi) ahead, alongside layer hi's call (a decode call lets the next kernel start only once the calls before
+    it have finished, so those outputs are final), eight layers at a time; the last layer's after its call."""
+
+    GROUP = 8  # layers per device-to-host copy
+
+    def __init__(self, sess: DecodeSession):
+        wl, dev = sess.wl, sess.device
+        self.sess, self.device, self.L = sess, dev, wl.L
+        parts = [("block_table", np.ascontiguousarray(wl.block_table, np.int32)),
+                 ("context_lens", np.ascontiguousarray(wl.ctx, np.int32)),
+                 ("slots", np.ascontiguousarray(sess.step_slots_host, np.int64))]
+        for layer in range(wl.L):
+            parts += [(("q", layer), np.ascontiguousarray(wl.q[layer], np.float16)),
+                      (("k_new", layer), np.ascontiguousarray(wl.k_new[layer], np.float16)),
+                      (("v_new", layer), np.ascontiguousarray(wl.v_new[layer], np.float16))]
+        offs, pos, layer_end = {}, 0, []
+        for name, a in parts:
+            offs[name] = pos
+            pos = _align16(pos + a.nbytes)
+            if name[0] == "v_new":
+                layer_end.append(pos)
+        self.h_buf = torch.empty(pos, dtype=torch.uint8).pin_memory()
+        hb = self.h_buf.numpy()
+        hb[:] = 0
+        for name, a in parts:
+            hb[offs[name]:offs[name] + a.nbytes] = a.reshape(-1).view(np.uint8)
+        self.d_buf = torch.zeros(pos, dtype=torch.uint8, device=dev)
+        tdt = {np.dtype(np.int32): torch.int32, np.dtype(np.int64): torch.int64, np.dtype(np.float16): torch.float16}
+
+        def view(name, a):
+            return self.d_buf[offs[name]:offs[name] + a.nbytes].view(tdt[a.dtype]).view(a.shape)
+        arrays = dict(parts)
+        self.block_table, self.context_lens, self.slots = (view(n, arrays[n])
+                                                          for n in ("block_table", "context_lens", "slots"))
+        self.q, self.k_new, self.v_new = ([view((n, layer), arrays[(n, layer)]) for layer in range(wl.L)]
+                                          for n in ("q", "k_new", "v_new"))
+        self.k_pool = [sess.k_pool[layer] for layer in range(wl.L)]
+        self.v_pool = [sess.v_pool[layer] for layer in range(wl.L)]
+        self.out = [sess.out[layer] for layer in range(wl.L)]
+        self.h_out = torch.empty(sess.out.shape, dtype=sess.out.dtype).pin_memory()
+        self.h_out_layers = [self.h_out[layer] for layer in range(wl.L)]
+        cut = layer_end[min(1, wl.L - 1)]  # header + layers 0 and 1 | the rest
+        self.first = (self.d_buf[:cut], self.h_buf[:cut])
+        self.rest = (self.d_buf[cut:], self.h_buf[cut:]) if cut < pos else None
+        # device-to-host groups [lo, hi) of all layers but the last, each sent alongside layer hi's call
+        self.groups = {min(g + self.GROUP, wl.L - 1): (self.h_out[g:min(g + self.GROUP, wl.L - 1)],
+                                                       sess.out[g:min(g + self.GROUP, wl.L - 1)])
+                       for g in range(0, wl.L - 1, self.GROUP)}
+        self.h2d_bytes = pos
+        self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+
+    def run(self, fused=True):
+        """One step on the current stream: copies in, every layer's call(s), copies out (all asynchronous)."""
+        s, wl, cs = self.sess, self.sess.wl, torch.cuda.current_stream(self.device)
+        kvc_copy_async(*self.first, stream=cs)
+        for layer in range(self.L):
+            if fused:
+                paged_decode_append_attention(self.q[layer], self.k_new[layer], self.v_new[layer], self.k_pool[layer],
+                                              self.v_pool[layer], self.block_table, self.context_lens, wl.scale,
+                                              self.out[layer], s.workspace, s.max_ctx, s.blocks_per_split, stream=cs)
+            else:
+                kv_append(s.h, layer, self.k_new[layer], self.v_new[layer], self.slots, stream=cs)
+                paged_decode_attention(self.q[layer], self.k_pool[layer], self.v_pool[layer], self.block_table,
+                                       self.context_lens, wl.scale, self.out[layer], s.workspace, s.max_ctx,
+                                       s.blocks_per_split, stream=cs)
+            if layer == 0 and self.rest is not None:
+                kvc_copy_async(*self.rest, ahead=True, stream=cs)
+            if layer in self.groups:
+                kvc_copy_async(*self.groups[layer], ahead=True, stream=cs)
+        kvc_copy_async(self.h_out_layers[-1], self.out[-1], stream=cs)

@@ -255,3 +255,20 @@ def test_trace_read_needs_a_trace_build():
     with pytest.raises(kvc.KvcError) as e:
         kvc.kvc_trace_read(16)
     assert "KVC_ERR_UNSUPPORTED" in str(e.value)
+
+
+def test_copy_async_argument_errors():
+    """kvc_copy_async refuses bad arguments synchronously, before any device work (no GPU needed)."""
+    import paged_kv_cache_27_gb300 as kvc
+    f = kvc._lib.kvc_copy_async
+    buf = np.zeros(256, dtype=np.uint8)
+    base = (buf.ctypes.data + 15) & ~15  # a 16-byte aligned pageable host address
+    assert f(base, base + 64, 0, 0, None) == 0  # nothing to copy
+    assert f(base, base + 64, 16, 2, None) == 1  # unknown flag
+    assert f(None, base, 16, 0, None) == 1
+    assert f(base, None, 16, 0, None) == 1
+    assert f(base, base + 64, 24, 0, None) == 1  # not a multiple of 16
+    assert f(base + 8, base + 64, 16, 0, None) == 1  # misaligned
+    assert f(base, base + 16, 32, 0, None) == 1  # overlapping
+    assert f(base, base + 64, 32, kvc.KVC_COPY_AHEAD, None) == 1  # pageable host memory
+    assert "pinned" in kvc._lib.kvc_last_error_string().decode()

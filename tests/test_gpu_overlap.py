@@ -1,7 +1,7 @@
 """Launch overlap (programmatic dependent launch) on the multi-token, cascade and fp8 paths: calls chained in a CUDA
 graph, each call's q being the previous call's output (filled with NaN before the replay), so a kernel that read
 q before its dependency wait would see NaN or a partly written q.  Each call is checked against the oracle on the q
-it actually received."""
+it actually received.  Also the decode step fed from pinned host memory with its copies overlapped with the calls."""
 import numpy as np
 import pytest
 import torch
@@ -127,3 +127,80 @@ def test_fp8_decode_chain_in_graph():
                                 wl.block_table, wl.ctx, wl.scale)
         check_attention(o, ref, f"fp8 chain call {i}")
         src = o.cpu().numpy()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_host_step_copies_overlapped_with_calls(fused):
+    """The step fed from pinned host memory with its copies overlapped with the calls (HostStep: inputs in three
+    copies on two streams, each layer's output copied back as soon as its call ends), replayed from a CUDA graph
+    with launch overlap and then run eagerly.  Before each run the device inputs hold wrong but valid values
+    (block 0, context 1, slot 0, NaN activations) and the device and host outputs NaN, so a call that ran ahead
+    of its input copy, or a copy back that ran ahead of its call, shows up."""
+    from oracle import paging as opaging
+    from parity import check_cache_bits, owned_slots
+    from paged_kv_cache_27_gb300.harness import DecodeSession, HostStep
+    import paged_kv_cache_27_gb300 as kvc
+    wl = workloads.small_decode(61, B=5, Hq=14, Hkv=2, D=64, ctx=[3000, 17, 40000, 2048, 1], L=4)
+    s = DecodeSession(wl, out_dtype=torch.float16).fill()
+    hs = HostStep(s)
+    g = _graph(lambda: hs.run(fused))
+
+    def poison():
+        torch.cuda.synchronize()
+        hs.block_table.zero_()
+        hs.context_lens.fill_(1)
+        hs.slots.zero_()
+        for t in hs.q + hs.k_new + hs.v_new:
+            t.fill_(float("nan"))
+        s.out.fill_(float("nan"))
+        hs.h_out.fill_(float("nan"))
+
+    refs = [opaging.decode_step(wl, layer) for layer in range(wl.L)]
+    slots = owned_slots(wl.block_table, wl.ctx, wl.bs)
+    for how in ("graph", "eager"):
+        poison()
+        kvc.kvc_set_launch_overlap(True)
+        try:
+            g.replay() if how == "graph" else hs.run(fused)
+        finally:
+            kvc.kvc_set_launch_overlap(False)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_error_flags(clear=True) == 0
+        for layer, (ref, kc, vc) in enumerate(refs):
+            check_attention(hs.h_out[layer], ref, f"{how}, fused={fused}, layer {layer}")
+            check_cache_bits(s.k_pool[layer], kc, slots)
+            check_cache_bits(s.v_pool[layer], vc, slots)
+    s.close()
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096 + 16, 3 * (1 << 20) + 48])
+@pytest.mark.parametrize("ahead", [False, True])
+def test_staging_copy_directions(nbytes, ahead):
+    """kvc_copy_async between pinned host and device memory both ways and device to device, byte for byte, at
+    sizes that leave a ragged last pass of the kernel's grid."""
+    import paged_kv_cache_27_gb300 as kvc
+    rng = np.random.default_rng(nbytes)
+    host = torch.from_numpy(rng.integers(0, 256, size=nbytes, dtype=np.uint8)).pin_memory()
+    dev_a = torch.full((nbytes,), 7, dtype=torch.uint8, device="cuda")
+    dev_b = torch.zeros_like(dev_a)
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    kvc.kvc_set_launch_overlap(ahead)
+    try:
+        kvc.kvc_copy_async(dev_a, host, ahead=ahead)
+        kvc.kvc_copy_async(dev_b, dev_a, ahead=False)
+        kvc.kvc_copy_async(back, dev_b, ahead=False)
+    finally:
+        kvc.kvc_set_launch_overlap(False)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_a.cpu(), host)
+    assert torch.equal(back, host)
+
+
+def test_staging_copy_refuses_pageable_memory():
+    import paged_kv_cache_27_gb300 as kvc
+    dev = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_copy_async(dev, torch.zeros(64, dtype=torch.uint8))
+    assert "pinned" in str(e.value)
+    with pytest.raises(ValueError):
+        kvc.kvc_copy_async(dev, torch.zeros(48, dtype=torch.uint8, device="cuda"))
