@@ -14,6 +14,7 @@
 #include "../../include/kvc.h"
 #include "block_pool.h"
 #include "kvc_internal.h"
+#include "stage_copy.h"
 
 struct kvc_cache {
     kvc_config cfg;

@@ -19,6 +19,7 @@
 #include "decode_common.cuh"
 #include "kvc_internal.h"
 #include "ptx.cuh"
+#include "stage_copy.h"
 
 namespace kvc {
 

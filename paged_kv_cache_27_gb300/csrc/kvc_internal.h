@@ -26,8 +26,6 @@ cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const in
 // copies whole blocks src[i] -> dst[i] for every layer (pools [L][NB][block_elems])
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __half* k_pool, __half* v_pool,
                                int L, int num_blocks, int64_t block_elems, cudaStream_t stream);
-// kvc_copy_async: bytes (a multiple of 16, both addresses 16-byte aligned and device-accessible, bytes > 0)
-cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, bool ahead, cudaStream_t stream);
 
 // ---- decode (decode.cu) ------------------------------------------------------
 struct DecodePlan {
