@@ -237,7 +237,9 @@ class HostStep:
     then per layer that layer's q, k_new and v_new, each 16-byte aligned.  A device buffer has the same layout
     and every call receives views into it.  Every copy is a staging copy (kvc_copy_async: a kernel that reads or
     writes the pinned buffer over the host link) in the stream's kernel sequence.  In: the header with layers 0
-    and 1 before layer 0's call, every later layer ahead, alongside layer 0's call.  Out: the outputs of layers
+    and 1 before layer 0's call; the later layers ahead, in pieces of growing size, each alongside an earlier
+    layer's call (layers 2-3 alongside layer 0's, 4-7 alongside layer 1's, the rest alongside layer 3's; one
+    piece for all of them made layer 1 wait for it).  Out: the outputs of layers
     [lo, hi) ahead, alongside layer hi's call (a decode call lets the next kernel start only once the calls before
     it have finished, so those outputs are final), eight layers at a time; the last layer's after its call."""
 
@@ -279,9 +281,15 @@ class HostStep:
         self.out = [sess.out[layer] for layer in range(wl.L)]
         self.h_out = torch.empty(sess.out.shape, dtype=sess.out.dtype).pin_memory()
         self.h_out_layers = [self.h_out[layer] for layer in range(wl.L)]
-        cut = layer_end[min(1, wl.L - 1)]  # header + layers 0 and 1 | the rest
+        cut = layer_end[min(1, wl.L - 1)]  # header + layers 0 and 1
         self.first = (self.d_buf[:cut], self.h_buf[:cut])
-        self.rest = (self.d_buf[cut:], self.h_buf[cut:]) if cut < pos else None
+        # layers [a, b) staged ahead alongside layer a / 2 - 1's call
+        starts = [a for a in (2, 4, 8) if a < wl.L]
+        self.ahead_in = {}
+        for i, a in enumerate(starts):
+            b = starts[i + 1] if i + 1 < len(starts) else wl.L
+            lo, hi = layer_end[a - 1], layer_end[b - 1]
+            self.ahead_in[a // 2 - 1] = (self.d_buf[lo:hi], self.h_buf[lo:hi])
         # device-to-host groups [lo, hi) of all layers but the last, each sent alongside layer hi's call
         self.groups = {min(g + self.GROUP, wl.L - 1): (self.h_out[g:min(g + self.GROUP, wl.L - 1)],
                                                        sess.out[g:min(g + self.GROUP, wl.L - 1)])
@@ -303,8 +311,8 @@ class HostStep:
                 paged_decode_attention(self.q[layer], self.k_pool[layer], self.v_pool[layer], self.block_table,
                                        self.context_lens, wl.scale, self.out[layer], s.workspace, s.max_ctx,
                                        s.blocks_per_split, stream=cs)
-            if layer == 0 and self.rest is not None:
-                kvc_copy_async(*self.rest, ahead=True, stream=cs)
+            if layer in self.ahead_in:
+                kvc_copy_async(*self.ahead_in[layer], ahead=True, stream=cs)
             if layer in self.groups:
                 kvc_copy_async(*self.groups[layer], ahead=True, stream=cs)
         kvc_copy_async(self.h_out_layers[-1], self.out[-1], stream=cs)
