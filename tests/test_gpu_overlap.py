@@ -140,7 +140,9 @@ def test_host_step_copies_overlapped_with_calls(fused):
     from parity import check_cache_bits, owned_slots
     from paged_kv_cache_27_gb300.harness import DecodeSession, HostStep
     import paged_kv_cache_27_gb300 as kvc
-    wl = workloads.small_decode(61, B=5, Hq=14, Hkv=2, D=64, ctx=[3000, 17, 40000, 2048, 1], L=4)
+    # 10 layers: inputs staged in all four pieces (layers 0-1, 2-3, 4-7, 8-9), outputs of layers 0-7 copied
+    # back alongside layer 8's call with layer 9's still to come; the 40000-token context adds the combine kernel
+    wl = workloads.small_decode(61, B=5, Hq=14, Hkv=2, D=64, ctx=[3000, 17, 40000, 2048, 1], L=10)
     s = DecodeSession(wl, out_dtype=torch.float16).fill()
     hs = HostStep(s)
     g = _graph(lambda: hs.run(fused))
