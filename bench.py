@@ -334,7 +334,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     ms_e2e = (time.perf_counter() - w0) * 1e3 / e2e_steps
     ms_e2e = barrier_max(ms_e2e, world, device)
-    # (b) the same calls issued one by one from Python (host-bound: ~10 us of binding and launch work per call)
+    # (b) the same calls issued one by one from Python, no graph (prepared calls: ~4.5 us of host time each)
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     for _ in range(e2e_steps):

@@ -28,7 +28,8 @@ __all__ = [
     "kv_block_release", "kv_block_refcount", "kv_block_num_free", "kv_cache_utilisation",
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
-    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_copy_async", "KVC_COPY_AHEAD", "kvc_trace_read",
+    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_copy_async", "KVC_COPY_AHEAD", "PreparedCall",
+    "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
     "prefill_attention", "prefill_attention_ex", "fp8_v_position", "DEVERR",
@@ -141,11 +142,17 @@ def _check(status: int, func: str):
         raise KvcError(status, func, _lib.kvc_last_error_string().decode(errors="replace"))
 
 
+# the current stream of a device as a raw handle, without building a torch.cuda.Stream object (a few µs per call)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, *tensors) -> Optional[int]:
     if stream is not None:
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     for t in tensors:
         if isinstance(t, torch.Tensor) and t.is_cuda:
+            if _raw_stream is not None:
+                return _raw_stream(t.get_device())
             return torch.cuda.current_stream(t.device).cuda_stream
     return None
 
@@ -153,15 +160,45 @@ def _stream(stream, *tensors) -> Optional[int]:
 def _dptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
     if t is None:
         return None
+    # the common case in one expression (dtypes are singletons); the checks below only name the failure
+    if isinstance(t, torch.Tensor) and t.is_cuda and (dtype is None or t.dtype is dtype) and t.is_contiguous():
+        return t.data_ptr()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return t.data_ptr()
+    raise ValueError(f"{name} must be contiguous")
+
+
+class PreparedCall:
+    """One library call whose arguments were checked and converted once (the `prepare=True` form of a launching
+    call): calling it launches that call again, on `stream` or else the current stream of the call's device.  It
+    keeps its tensors alive; their contents may change between launches, their storage must stay where it is.
+    Saves the per-call checks and conversions (~5 µs of host time per decode call)."""
+    __slots__ = ("_fn", "_args", "_name", "_device", "_keep")
+
+    def __init__(self, fn, args, name, device, keep):
+        self._fn, self._name, self._device, self._keep = fn, name, device, keep
+        self._args = tuple(a if a is None else at(a) for a, at in zip(args, fn.argtypes))
+
+    def __call__(self, stream=None) -> None:
+        if stream is not None:
+            st = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        elif _raw_stream is not None:
+            st = _raw_stream(self._device)
+        else:
+            st = torch.cuda.current_stream(self._device).cuda_stream
+        _check(self._fn(*self._args, st), self._name)
+
+
+def _launch(fn, args, name, stream, prepare, keep):
+    """Launch fn(*args, stream), or return it as a PreparedCall; keep[0] is a CUDA tensor of the call."""
+    if prepare:
+        return PreparedCall(fn, args, name, keep[0].get_device(), keep)
+    _check(fn(*args, _stream(stream, keep[0])), name)
+    return None
 
 
 def _host(a, dtype) -> np.ndarray:
@@ -199,16 +236,20 @@ def _stage_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
-def kvc_copy_async(dst: torch.Tensor, src: torch.Tensor, ahead: bool = False, stream=None) -> None:
+def kvc_copy_async(dst: torch.Tensor, src: torch.Tensor, ahead: bool = False, stream=None, prepare: bool = False):
     """Copy src's bytes into dst with the library's staging kernel (see include/kvc.h for the two orderings).
 
     Each of dst and src is a CUDA tensor or a pinned CPU tensor; both hold the same number of bytes, a multiple
-    of 16, at 16-byte aligned addresses."""
+    of 16, at 16-byte aligned addresses.  prepare=True returns a PreparedCall instead of launching."""
     nbytes = src.numel() * src.element_size()
     if dst.numel() * dst.element_size() != nbytes:
         raise ValueError("dst and src must hold the same number of bytes")
-    _check(_lib.kvc_copy_async(_stage_ptr(dst, "dst"), _stage_ptr(src, "src"), nbytes,
-                               KVC_COPY_AHEAD if ahead else 0, _stream(stream, dst, src)), "kvc_copy_async")
+    args = (_stage_ptr(dst, "dst"), _stage_ptr(src, "src"), nbytes, KVC_COPY_AHEAD if ahead else 0)
+    if prepare:
+        cuda = dst if dst.is_cuda else src
+        return PreparedCall(_lib.kvc_copy_async, args, "kvc_copy_async",
+                            cuda.get_device() if cuda.is_cuda else torch.cuda.current_device(), (dst, src))
+    _check(_lib.kvc_copy_async(*args, _stream(stream, dst, src)), "kvc_copy_async")
 
 
 TRACE_DTYPE = np.dtype([("t", "<u8", (8,)), ("seq", "<u4"), ("smid", "<u4"), ("x", "<u4"), ("yz", "<u4")])
@@ -340,14 +381,16 @@ def kv_step_prepare(h: int, block_table: np.ndarray, num_blocks: np.ndarray, pos
 
 # ------------------------------------------------------------ device ops
 def kv_append(h: int, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
-              stream=None) -> None:
-    """Scatter rows of k_new/v_new ([n][Hkv][D] fp16) to slot_mapping (int64 [n]) of one layer."""
+              stream=None, prepare: bool = False):
+    """Scatter rows of k_new/v_new ([n][Hkv][D] fp16) to slot_mapping (int64 [n]) of one layer.
+
+    prepare=True returns a PreparedCall instead of launching."""
     n = k_new.shape[0]
     if v_new.shape != k_new.shape or slot_mapping.numel() != n:
         raise ValueError("k_new, v_new and slot_mapping must agree in n")
-    _check(_lib.kv_append(h, layer, _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
-                          _dptr(slot_mapping, torch.int64, "slot_mapping"), n, _stream(stream, k_new)),
-           "kv_append")
+    args = (h, layer, _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
+            _dptr(slot_mapping, torch.int64, "slot_mapping"), n)
+    return _launch(_lib.kv_append, args, "kv_append", stream, prepare, (k_new, v_new, slot_mapping))
 
 
 def paged_decode_plan(B: int, Hq: int, Hkv: int, head_dim: int, max_context_len: int, blocks_per_split: int = 0,
@@ -367,11 +410,12 @@ def paged_decode_workspace_init(workspace: torch.Tensor, stream=None) -> None:
 def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
                            context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                            workspace: Optional[torch.Tensor], max_context_len: int, blocks_per_split: int = 0,
-                           stream=None) -> None:
+                           stream=None, prepare: bool = False):
     """out = softmax(q K^T * scale) V per sequence over its paged context.
 
     q [B][Hq][D] fp16; k_cache/v_cache [NB][Hkv][bs][D] fp16 (one layer); block_table int32 [B][max_blocks];
     context_lens int32 [B]; out [B][Hq][D] fp16 or fp32; workspace: paged_decode_plan(...) bytes (uint8/any).
+    prepare=True returns a PreparedCall instead of launching.
     """
     B, Hq, D = q.shape
     NB, Hkv, bs, Dk = k_cache.shape
@@ -389,12 +433,13 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         raise TypeError("out must be float16 or float32")
     ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(_lib.paged_decode_attention(
-        _dptr(q, torch.float16, "q"), _dptr(k_cache, torch.float16, "k_cache"),
-        _dptr(v_cache, torch.float16, "v_cache"), NB, _dptr(block_table, torch.int32, "block_table"),
-        block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs,
-        int(max_context_len), float(scale), _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split),
-        _stream(stream, q)), "paged_decode_attention")
+    args = (_dptr(q, torch.float16, "q"), _dptr(k_cache, torch.float16, "k_cache"),
+            _dptr(v_cache, torch.float16, "v_cache"), NB, _dptr(block_table, torch.int32, "block_table"),
+            block_table.shape[1], _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs,
+            int(max_context_len), float(scale), _dptr(out, None, "out"), od, ws_ptr, ws_bytes,
+            int(blocks_per_split))
+    return _launch(_lib.paged_decode_attention, args, "paged_decode_attention", stream, prepare,
+                   (q, k_cache, v_cache, block_table, context_lens, out, workspace))
 
 
 def kv_cascade_groups(block_table: np.ndarray, context_lens, max_group: int = 8, block_size: int = 16):
@@ -550,11 +595,12 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
                                   v_cache: torch.Tensor, block_table: torch.Tensor, context_lens: torch.Tensor,
                                   scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor],
                                   max_context_len: int, blocks_per_split: int = 0, stream=None,
-                                  k_next: Optional[torch.Tensor] = None, v_next: Optional[torch.Tensor] = None) -> None:
+                                  k_next: Optional[torch.Tensor] = None, v_next: Optional[torch.Tensor] = None,
+                                  prepare: bool = False):
     """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel).
 
     k_next/v_next: the next layer's pools (same shape as k_cache); accepted and unused (the L2 prefetch they were
-    for measured no gain)."""
+    for measured no gain).  prepare=True returns a PreparedCall instead of launching."""
     if (k_next is None) != (v_next is None):
         raise ValueError("k_next and v_next: both or neither")
     if k_next is not None and (k_next.shape != k_cache.shape or v_next.shape != k_cache.shape):
@@ -572,14 +618,14 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
         raise TypeError("out must be float16 or float32")
     ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(_lib.paged_decode_append_attention(
-        _dptr(q, torch.float16, "q"), _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
-        _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"),
-        _dptr(k_next, torch.float16, "k_next"), _dptr(v_next, torch.float16, "v_next"), NB,
-        _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-        _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
-        _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),
-        "paged_decode_append_attention")
+    args = (_dptr(q, torch.float16, "q"), _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
+            _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"),
+            _dptr(k_next, torch.float16, "k_next"), _dptr(v_next, torch.float16, "v_next"), NB,
+            _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+            _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
+            _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split))
+    return _launch(_lib.paged_decode_append_attention, args, "paged_decode_append_attention", stream, prepare,
+                   (q, k_new, v_new, k_cache, v_cache, block_table, context_lens, out, workspace, k_next, v_next))
 
 
 def paged_decode_attention_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -241,7 +241,8 @@ class HostStep:
     layer's call (layers 2-3 alongside layer 0's, 4-7 alongside layer 1's, the rest alongside layer 3's; one
     piece for all of them made layer 1 wait for it).  Out: the outputs of layers
     [lo, hi) ahead, alongside layer hi's call (a decode call lets the next kernel start only once the calls before
-    it have finished, so those outputs are final), eight layers at a time; the last layer's after its call."""
+    it have finished, so those outputs are final), eight layers at a time; the last layer's after its call.
+    Every call is checked and converted once, at construction (the prepare=True form of the API)."""
 
     GROUP = 8  # layers per device-to-host copy
 
@@ -296,23 +297,35 @@ class HostStep:
                        for g in range(0, wl.L - 1, self.GROUP)}
         self.h2d_bytes = pos
         self.d2h_bytes = self.h_out.numel() * self.h_out.element_size()
+        # every call of the step checked and converted once (PreparedCall); run() only launches them
+        self._first = kvc_copy_async(*self.first, prepare=True)
+        self._ahead_in = {k: kvc_copy_async(*v, ahead=True, prepare=True) for k, v in self.ahead_in.items()}
+        self._groups = {k: kvc_copy_async(*v, ahead=True, prepare=True) for k, v in self.groups.items()}
+        self._last = kvc_copy_async(self.h_out_layers[-1], self.out[-1], prepare=True)
+        self._fused = [paged_decode_append_attention(self.q[layer], self.k_new[layer], self.v_new[layer],
+                                                     self.k_pool[layer], self.v_pool[layer], self.block_table,
+                                                     self.context_lens, wl.scale, self.out[layer], sess.workspace,
+                                                     sess.max_ctx, sess.blocks_per_split, prepare=True)
+                       for layer in range(wl.L)]
+        self._unfused = [(kv_append(sess.h, layer, self.k_new[layer], self.v_new[layer], self.slots, prepare=True),
+                          paged_decode_attention(self.q[layer], self.k_pool[layer], self.v_pool[layer],
+                                                 self.block_table, self.context_lens, wl.scale, self.out[layer],
+                                                 sess.workspace, sess.max_ctx, sess.blocks_per_split, prepare=True))
+                         for layer in range(wl.L)]
 
     def run(self, fused=True):
         """One step on the current stream: copies in, every layer's call(s), copies out (all asynchronous)."""
-        s, wl, cs = self.sess, self.sess.wl, torch.cuda.current_stream(self.device)
-        kvc_copy_async(*self.first, stream=cs)
+        cs = torch.cuda.current_stream(self.device)
+        self._first(cs)
         for layer in range(self.L):
             if fused:
-                paged_decode_append_attention(self.q[layer], self.k_new[layer], self.v_new[layer], self.k_pool[layer],
-                                              self.v_pool[layer], self.block_table, self.context_lens, wl.scale,
-                                              self.out[layer], s.workspace, s.max_ctx, s.blocks_per_split, stream=cs)
+                self._fused[layer](cs)
             else:
-                kv_append(s.h, layer, self.k_new[layer], self.v_new[layer], self.slots, stream=cs)
-                paged_decode_attention(self.q[layer], self.k_pool[layer], self.v_pool[layer], self.block_table,
-                                       self.context_lens, wl.scale, self.out[layer], s.workspace, s.max_ctx,
-                                       s.blocks_per_split, stream=cs)
-            if layer in self.ahead_in:
-                kvc_copy_async(*self.ahead_in[layer], ahead=True, stream=cs)
-            if layer in self.groups:
-                kvc_copy_async(*self.groups[layer], ahead=True, stream=cs)
-        kvc_copy_async(self.h_out_layers[-1], self.out[-1], stream=cs)
+                append, decode = self._unfused[layer]
+                append(cs)
+                decode(cs)
+            if layer in self._ahead_in:
+                self._ahead_in[layer](cs)
+            if layer in self._groups:
+                self._groups[layer](cs)
+        self._last(cs)

@@ -206,3 +206,28 @@ def test_staging_copy_refuses_pageable_memory():
     assert "pinned" in str(e.value)
     with pytest.raises(ValueError):
         kvc.kvc_copy_async(dev, torch.zeros(48, dtype=torch.uint8, device="cuda"))
+
+
+def test_prepared_call_matches_direct_call():
+    """A decode call in its prepare=True form launches the same work as the direct call (bit for bit), on the
+    current stream or a given one."""
+    import paged_kv_cache_27_gb300 as kvc
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    wl = workloads.small_decode(63, B=3, Hq=14, Hkv=2, D=64, ctx=[100, 30000, 1])
+    s = DecodeSession(wl).fill()
+    s.append(0)  # the new token's K/V (without it the last slot of every context still holds the NaN poison)
+    s.decode(0)
+    torch.cuda.synchronize()
+    ref = s.out[0].clone()
+    assert torch.isfinite(ref).all()
+    call = kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
+                                      s.out[0], s.workspace, s.max_ctx, prepare=True)
+    assert isinstance(call, kvc.PreparedCall)
+    for stream in (None, torch.cuda.Stream()):
+        s.out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        call(stream)
+        torch.cuda.synchronize()
+        assert torch.equal(s.out[0], ref)
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    s.close()
