@@ -381,10 +381,12 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(step_bytes, world, ms_e2e) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "host wall clock per step: H2D of the step's inputs from one pinned buffer (block table, "
-                       "context lengths, slots, then per layer q / k_new / v_new) in three copies, the 24 public-API "
-                       "calls, D2H of each layer's output as soon as its call ends, copies overlapped with the "
-                       "calls on two copy streams, captured once in a CUDA graph and replayed",
+                "how": "host wall clock per step: the step's inputs (block table, context lengths, slots, then "
+                       "per layer q / k_new / v_new) read from one pinned host buffer and the outputs written back "
+                       "to pinned host memory by kvc_copy_async staging kernels in the same stream as the 24 "
+                       "public-API calls (header and layers 0-1 before the first call, later layers in pieces "
+                       "alongside earlier calls, outputs eight layers at a time alongside a later call, the last "
+                       "layer's after its call), captured once in a CUDA graph and replayed",
                 "eager_value": whole_job_rate(step_bytes, world, ms_e2e_eager) / 1e9,
                 "eager_ms_per_step": ms_e2e_eager},
         "gpu_launches": launches_per_step * args.steps,

@@ -131,6 +131,10 @@ kvc_status kv_block_cow(kvc_handle h, int32_t block, int32_t* new_block, void* s
 kvc_status kv_copy_blocks(kvc_handle h, const int32_t* src, const int32_t* dst, int n, void* stream);
 
 /* ---- slot arithmetic (host) -----------------------------------------
+ * The PagedAttention article of the chatgpz.de feed, SECTION 2 (PagedRequest:
+ * token position p lives in page block_table[p / page_size] at offset
+ * p % page_size), and the neuralialabs.com PagedAttention paragraph (a block
+ * table maps a sequence's logical blocks to physical ones).
  * Slots of positions first_pos[b] .. first_pos[b]+count[b]-1 of every
  * sequence b, packed in order into slots (host, sum(count) entries):
  *     slot = block_table[b][pos / bs] * bs + pos % bs.
@@ -139,8 +143,11 @@ kvc_status kv_copy_blocks(kvc_handle h, const int32_t* src, const int32_t* dst, 
 kvc_status kv_slot_mapping(const int32_t* block_table, int max_blocks, int B, const int32_t* first_pos,
                            const int32_t* count, int block_size, int64_t* slots);
 
-/* One decode step's block management for B sequences (host; the
- * PagedRequest rule plus copy-on-write): for each sequence b in order, the
+/* One decode step's block management for B sequences (host).  Follows the
+ * chatgpz.de PagedAttention article: SECTION 2 (PagedRequest claims a new
+ * page from the FIFO pool when a token starts a page) and SECTION 3
+ * (copy-on-write: a token written into a page whose refcount is above one
+ * first gets a private copy of that page).  For each sequence b in order, the
  * new token goes to position positions[b]; if that position starts a new
  * block (positions[b] == num_blocks[b] * bs) a block is allocated and
  * appended to the table; otherwise, if its block has refcount > 1, a new
@@ -177,7 +184,12 @@ kvc_status paged_decode_plan(int B, int Hq, int Hkv, int head_dim, int block_siz
  * overlap in time (same stream, or ordered by events). */
 kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stream);
 
-/* Paged GQA decode attention for one token per sequence:
+/* Paged GQA decode attention for one token per sequence ("La caché de
+ * claves y valores", gustavoai.dev, section "Las claves y los valores de una
+ * posición no cambian": the new query row attends, unmasked, over every
+ * cached row; neuralialabs.com PagedAttention and grouped-query attention
+ * paragraphs: the rows come through the sequence's block table and a group of
+ * query heads shares one KV head; xformers article part 5: contiguous groups):
  *   out[b][h] = softmax(q[b][h] . K_b^T * scale) V_b
  * over the context_lens[b] tokens of sequence b (the appended token
  * included), K_b/V_b gathered through block_table[b] from KV head
@@ -209,13 +221,9 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
  * position context_lens[b]-1 of the cache, i.e. slot
  * block_table[b][(ctx-1)/bs]*bs + (ctx-1)%bs, and take part in the attention
  * of that same call.  Bit-identical cache contents to kv_append with those
- * slots followed by paged_decode_attention.
- * k_next/v_next (both NULL, or both set, 16-byte aligned): the pools of the
- * layer the caller runs next.  Accepted for a prefetch of the next layer's
- * blocks into L2; that prefetch measured no gain on GB300 and is not issued,
- * so the arguments have no effect. */
+ * slots followed by paged_decode_attention. */
 kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
-                                         void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                         void* v_cache, int num_blocks,
                                          const int32_t* block_table, int max_blocks, const int32_t* context_lens,
                                          int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                                          float scale, void* out, int out_dtype, void* workspace,
@@ -358,6 +366,12 @@ kvc_status kvc_set_launch_overlap(int on);
  *     finished only once that kernel has.  Later kernels may read the bytes
  *     only after their dependency wait (q, k_new, v_new; not block tables,
  *     context lengths or cache rows).
+ * The flags-0 promise (a kernel may read the bytes before its dependency
+ * wait) rests on the copy making its writes visible device-wide (a fence and
+ * a CTA barrier) before it lets the next kernel launch.  CUDA documents the
+ * visibility of a preceding kernel's writes only after the dependency wait,
+ * so this ordering is established by test (the host-step test poisons every
+ * staged input before each run), not by a documented guarantee.
  * With launch overlap off both forms are plain stream-ordered copies.
  * Errors (synchronous): KVC_ERR_INVALID for null, misaligned, overlapping or
  * pageable buffers and unknown flags; KVC_ERR_CUDA if the launch fails. */
@@ -385,7 +399,9 @@ kvc_status kvc_trace_read(void* records, int capacity, int* count, int clear);
  * The call itself allocates nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: it does not survive cudaDeviceReset (or any other reset of the
+ *    device's primary context), after which this call must not be used.
  *  - All calls on a device share the one array: calls that can overlap on
  *    the GPU (other streams, concurrent graphs) race on it.  Nothing in it
  *    needs to start at zero: every word a call reads, the same call writes first.

@@ -107,7 +107,7 @@ def _load():
         "paged_decode_plan": (I, [I, I, I, I, I, I, I, PI, PI, PSZ]),
         "paged_decode_workspace_init": (I, [P, SZ, P]),
         "paged_decode_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ, I, P]),
-        "paged_decode_append_attention": (I, [P, P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
+        "paged_decode_append_attention": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P,
                                               I, P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
         "kvc_copy_async": (I, [P, P, SZ, ctypes.c_uint, P]),
@@ -595,16 +595,10 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
                                   v_cache: torch.Tensor, block_table: torch.Tensor, context_lens: torch.Tensor,
                                   scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor],
                                   max_context_len: int, blocks_per_split: int = 0, stream=None,
-                                  k_next: Optional[torch.Tensor] = None, v_next: Optional[torch.Tensor] = None,
                                   prepare: bool = False):
     """Append k_new/v_new ([B][Hkv][D] fp16) at position ctx-1 of every sequence, then attend (one kernel).
 
-    k_next/v_next: the next layer's pools (same shape as k_cache); accepted and unused (the L2 prefetch they were
-    for measured no gain).  prepare=True returns a PreparedCall instead of launching."""
-    if (k_next is None) != (v_next is None):
-        raise ValueError("k_next and v_next: both or neither")
-    if k_next is not None and (k_next.shape != k_cache.shape or v_next.shape != k_cache.shape):
-        raise ValueError("k_next/v_next must have k_cache's shape")
+    prepare=True returns a PreparedCall instead of launching."""
     B, Hq, D = q.shape
     NB, Hkv, bs, Dk = k_cache.shape
     if Dk != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
@@ -619,13 +613,12 @@ def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: t
     ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     args = (_dptr(q, torch.float16, "q"), _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
-            _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"),
-            _dptr(k_next, torch.float16, "k_next"), _dptr(v_next, torch.float16, "v_next"), NB,
+            _dptr(k_cache, torch.float16, "k_cache"), _dptr(v_cache, torch.float16, "v_cache"), NB,
             _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
             _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
             _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split))
     return _launch(_lib.paged_decode_append_attention, args, "paged_decode_append_attention", stream, prepare,
-                   (q, k_new, v_new, k_cache, v_cache, block_table, context_lens, out, workspace, k_next, v_next))
+                   (q, k_new, v_new, k_cache, v_cache, block_table, context_lens, out, workspace))
 
 
 def paged_decode_attention_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

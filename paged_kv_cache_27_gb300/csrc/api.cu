@@ -411,7 +411,7 @@ kvc_status kvc_copy_async(void* dst, const void* src, size_t bytes, unsigned fla
 }
 
 static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                const void* v_cache, int num_blocks,
                                 const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
                                 int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
                                 int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
@@ -422,22 +422,20 @@ kvc_status paged_decode_attention(const void* q, const void* k_cache, const void
                                   int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
                                   int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
                                   void* stream) {
-    return decode_common(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table, max_blocks,
+    return decode_common(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_table, max_blocks,
                          context_lens, B, Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype,
                          workspace, workspace_bytes, blocks_per_split, stream);
 }
 
 kvc_status paged_decode_append_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
-                                         void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                         void* v_cache, int num_blocks,
                                          const int32_t* block_table, int max_blocks, const int32_t* context_lens,
                                          int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                                          float scale, void* out, int out_dtype, void* workspace,
                                          size_t workspace_bytes, int blocks_per_split, void* stream) {
     if (B > 0 && (!k_new || !v_new)) return fail(KVC_ERR_INVALID, "null k_new/v_new");
     if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVC_ERR_INVALID, "k_new/v_new must be 16-byte aligned");
-    if ((k_next == nullptr) != (v_next == nullptr)) return fail(KVC_ERR_INVALID, "k_next and v_next: both or neither");
-    if (!aligned16(k_next) || !aligned16(v_next)) return fail(KVC_ERR_INVALID, "k_next/v_next must be 16-byte aligned");
-    return decode_common(q, k_new, v_new, k_cache, v_cache, k_next, v_next, num_blocks, block_table, max_blocks,
+    return decode_common(q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks,
                          context_lens, B, Hq, Hkv, head_dim, block_size, max_context_len, scale, out, out_dtype,
                          workspace, workspace_bytes, blocks_per_split, stream);
 }
@@ -480,7 +478,7 @@ static kvc_status decode_validate(const void* q, const void* k_cache, const void
 }
 
 static kvc::DecodeArgs decode_args(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                   const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                   const void* v_cache, int num_blocks,
                                    const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B,
                                    int Hq, int Hkv, int head_dim, int max_context_len, float scale, void* out,
                                    int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split) {
@@ -488,8 +486,6 @@ static kvc::DecodeArgs decode_args(const void* q, const void* k_new, const void*
     a.q = static_cast<const __half*>(q);
     a.k_new = static_cast<const __half*>(k_new);
     a.v_new = static_cast<const __half*>(v_new);
-    a.k_next = static_cast<const __half*>(k_next);
-    a.v_next = static_cast<const __half*>(v_next);
     a.k_cache = static_cast<const __half*>(k_cache);
     a.v_cache = static_cast<const __half*>(v_cache);
     a.num_blocks = num_blocks;
@@ -519,7 +515,7 @@ static kvc_status check_workspace(size_t need, const void* workspace, size_t wor
 }
 
 static kvc_status decode_common(const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                                const void* v_cache, const void* k_next, const void* v_next, int num_blocks,
+                                const void* v_cache, int num_blocks,
                                 const int32_t* block_table, int max_blocks, const int32_t* context_lens, int B, int Hq,
                                 int Hkv, int head_dim, int block_size, int max_context_len, float scale, void* out,
                                 int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
@@ -529,7 +525,7 @@ static kvc_status decode_common(const void* q, const void* k_new, const void* v_
                                    head_dim, block_size, max_context_len, out, out_dtype, blocks_per_split, stream, ctx,
                                    table);
     if (s != KVC_OK || B == 0) return s;
-    kvc::DecodeArgs a = decode_args(q, k_new, v_new, k_cache, v_cache, k_next, v_next, num_blocks, block_table,
+    kvc::DecodeArgs a = decode_args(q, k_new, v_new, k_cache, v_cache, num_blocks, block_table,
                                     max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
                                     out_dtype, workspace, workspace_bytes, blocks_per_split);
     kvc::DecodePlan plan;
@@ -631,7 +627,7 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
             }
         }
     }
-    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table,
+    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_table,
                                     max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
                                     out_dtype, workspace, workspace_bytes, 0);
     kvc::CascadePlan plan;
@@ -689,7 +685,7 @@ kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const 
     if (s != KVC_OK || B == 0) return s;
     if (!k_scales || !v_scales) return fail(KVC_ERR_INVALID, "null scales");
     if (!aligned16(k_scales) || !aligned16(v_scales)) return fail(KVC_ERR_INVALID, "scales must be 16-byte aligned");
-    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, num_blocks, block_table,
+    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, nullptr, nullptr, num_blocks, block_table,
                                     max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
                                     out_dtype, workspace, workspace_bytes, blocks_per_split);
     a.k_codes = static_cast<const uint8_t*>(k_codes);
@@ -736,7 +732,7 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
         for (int b = 0; b < B; ++b)
             if (ctx[b] < q_len)
                 return fail(KVC_ERR_CAPACITY, "sequence %d: context length %d below q_len %d", b, ctx[b], q_len);
-    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, num_blocks, block_table,
+    kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, k_cache, v_cache, num_blocks, block_table,
                                     max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
                                     out_dtype, workspace, workspace_bytes, 0);
     kvc::MultiPlan plan;

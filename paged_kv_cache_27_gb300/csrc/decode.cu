@@ -54,8 +54,6 @@ struct DecodeKernelParams {
     __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
     __half* v_cache;
     const uint8_t* v_codes;  // fp8: the layer's V code pool (a block's codes for one KV head are contiguous)
-    const __half* k_next;  // the next layer's pools (accepted, unused: the L2 prefetch measured no gain)
-    const __half* v_next;
     const int32_t* block_table;
     const int32_t* context_lens;
     void* out;
@@ -676,7 +674,10 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
                      ctx_full > p.max_ctx || ctx < 1;
     const int nsuf = bad ? 0 : ((ctx + kBlockSize - 1) / kBlockSize + p.bpc - 1) / p.bpc;
     const int npre = off > 0 && p.prefix_chunk > 0 ? (off + p.prefix_chunk - 1) / p.prefix_chunk : 0;
-    if (!bad && !p.cascade && nsuf <= 1) return;  // the cluster wrote the output itself
+    if (!bad && !p.cascade && nsuf <= 1) {  // the cluster wrote the output itself
+        leave_before_dependency_wait();
+        return;
+    }
     grid_dependency_wait();
     if (bad) {
         if (p.cascade) {  // the attention kernels left this row to us
@@ -839,8 +840,6 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.v_new = a.v_new;
     p.k_cache = const_cast<__half*>(a.k_cache);
     p.v_cache = const_cast<__half*>(a.v_cache);
-    p.k_next = a.k_next;
-    p.v_next = a.v_next;
     p.block_table = a.block_table;
     p.context_lens = a.context_lens;
     p.out = a.out;
@@ -1058,8 +1057,6 @@ extern "C" kvc_status paged_decode_attention_static_workspace(
     a.v_new = nullptr;
     a.k_cache = static_cast<const __half*>(k_cache);
     a.v_cache = static_cast<const __half*>(v_cache);
-    a.k_next = nullptr;
-    a.v_next = nullptr;
     a.num_blocks = num_blocks;
     a.block_table = block_table;
     a.max_blocks = max_blocks;

@@ -125,10 +125,14 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
     if constexpr (kPrefix) {
         s0 = p.group_start[u];
         T = p.group_start[u + 1] - s0;
-        if (T < 1 || r0 >= T * p.G) return;  // an empty group, or no rows in this row group
+        if (T < 1 || r0 >= T * p.G) {  // an empty group, or no rows in this row group
+            leave_before_dependency_wait();
+            return;
+        }
         const int nsh = p.blk_off[s0];
         if (T > kMaxGroupSize || nsh < 0 || nsh > p.max_blocks) {
             if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+            leave_before_dependency_wait();
             return;  // the combine kernel writes these sequences' rows
         }
         ctx = nsh * kBlockSize;  // the shared blocks lie inside every member's context: no key is masked
@@ -157,7 +161,10 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
         return seq_row * p.Hq + kvh * p.G + r % p.G;
     };
     const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
-    if (cidx * cs * p.chunk >= nblk) return;  // the whole cluster is past this context
+    if (cidx * cs * p.chunk >= nblk) {  // the whole cluster is past this context (or no block is shared)
+        leave_before_dependency_wait();
+        return;
+    }
     // this CTA's blocks [j0, j0 + n); a CTA of a live cluster may have none and still takes part in its merge
     const int j0 = (cidx * cs + rank) * p.chunk;
     const int n = max(0, min(nblk, j0 + p.chunk) - j0);

@@ -109,16 +109,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_tc_kernel(const __grid_con
     // member's row), every key of them inside every member's context; the exits below are uniform over the CTA
     const int s0 = p.group_start[u];
     const int T = p.group_start[u + 1] - s0;
-    if (T < 1) return;
+    if (T < 1) {
+        leave_before_dependency_wait();
+        return;
+    }
     const int nsh = p.blk_off[s0];
     if (T > kMaxGroupSize || nsh < 0 || nsh > p.max_blocks) {
         if (chunk == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+        leave_before_dependency_wait();
         return;  // the combine kernel writes these sequences' rows
     }
     const int ctx = nsh * kBlockSize, nblk = nsh;  // keys and blocks of the shared prefix
     const int R = T * p.G;                          // query rows, at most kMaxGroupSize x 8 = 64
     const int j0 = chunk * p.chunk;                 // this CTA's blocks [j0, j0 + n) of the shared blocks
-    if (j0 >= nblk) return;          // the group shares fewer blocks
+    if (j0 >= nblk) {  // the group shares fewer blocks
+        leave_before_dependency_wait();
+        return;
+    }
     const int n = min(nblk, j0 + p.chunk) - j0;
     const int nt = (n + kTileBlocks - 1) / kTileBlocks;  // key tiles
     const int32_t* table = p.block_table + static_cast<int64_t>(s0) * p.max_blocks + j0;

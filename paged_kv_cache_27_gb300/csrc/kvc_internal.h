@@ -43,8 +43,6 @@ struct DecodeArgs {
     const __half* v_new;
     const __half* k_cache;
     const __half* v_cache;
-    const __half* k_next;  // null, or the next layer's pools: this call's blocks of them are prefetched to L2
-    const __half* v_next;
     int num_blocks;
     const int32_t* block_table;
     int max_blocks;

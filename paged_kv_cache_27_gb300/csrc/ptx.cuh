@@ -178,5 +178,12 @@ __device__ __forceinline__ void grid_dependency_wait() {
 __device__ __forceinline__ void grid_dependents_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// For a CTA that leaves before its dependency wait.  A grid whose CTAs all left without waiting would complete
+// while the kernel it depends on still runs, and the next kernel's dependency wait (which waits for this grid)
+// would then no longer cover that kernel.  The grid's first CTA therefore waits before it leaves; the others
+// leave at once.
+__device__ __forceinline__ void leave_before_dependency_wait() {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) grid_dependency_wait();
+}
 
 }  // namespace kvc

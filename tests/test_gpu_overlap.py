@@ -129,11 +129,94 @@ def test_fp8_decode_chain_in_graph():
         src = o.cpu().numpy()
 
 
+def test_decode_chain_with_idle_combine_in_graph():
+    """Decode calls planned for a context far longer than any actual one (forced short splits, so the plan has many
+    parts and the combine kernel is launched) while every context fits one split: every combine CTA has nothing to
+    merge.  The combine grid must still complete only after the decode kernel it follows, or the next call in the
+    chain could read its q (the previous output) before it is written."""
+    import paged_kv_cache_27_gb300 as kvc
+    from oracle import paging as opaging
+    from paged_kv_cache_27_gb300.harness import DecodeSession
+    B, Hq, Hkv, D = 96, 14, 2, 64
+    wl = workloads.small_decode(67, B=B, Hq=Hq, Hkv=Hkv, D=D, ctx=[16 + (7 * b) % 240 for b in range(B)])
+    s = DecodeSession(wl).fill()
+    s.append(0)
+    _, kc, vc = opaging.decode_step(wl, 0)  # the pools after the step's append
+    dev = "cuda"
+    bps = 16  # blocks per split: 256 tokens, more than any context here
+    max_ctx = 8192
+    _, got_bps, wsb = kvc.paged_decode_plan(B, Hq, Hkv, D, max_ctx, bps)
+    assert got_bps == bps and wsb > 0  # several parts: the combine kernel is part of every call
+    wide = np.full((B, max_ctx // 16), -1, dtype=np.int32)
+    wide[:, :wl.block_table.shape[1]] = wl.block_table
+    table = torch.from_numpy(wide).to(dev)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    q0 = s.q[0]
+    outs = [torch.empty_like(q0) for _ in range(4)]
+
+    def chain():
+        src = q0
+        for o in outs:
+            kvc.paged_decode_attention(src, s.k_pool[0], s.v_pool[0], table, s.context_lens, wl.scale, o, ws, max_ctx,
+                                       bps)
+            src = o
+    g = _graph(chain)
+    for rep in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_error_flags(clear=True) == 0
+        src = wl.q[0]
+        for i, o in enumerate(outs):
+            ref = oracle.decode(src, kc, vc, wl.block_table, wl.ctx, wl.scale)
+            check_attention(o, ref, f"idle-combine chain call {i}, replay {rep}")
+            src = o.cpu().numpy()
+    s.close()
+
+
+def test_cascade_chain_without_shared_blocks_in_graph():
+    """A cascade call told to expect shared prefixes when no group shares a block: every CTA of the prefix pass
+    leaves at once.  Chained calls in a graph still see the previous call's complete output."""
+    import paged_kv_cache_27_gb300 as kvc
+    extra = list(np.random.default_rng(9).integers(1, 300, size=12))
+    wl = workloads.cascade_decode(45, [4, 4, 4], [0, 0, 0], extra)
+    dev = "cuda"
+    B = len(extra)
+    kp, vp = torch.from_numpy(wl.k_pool).to(dev), torch.from_numpy(wl.v_pool).to(dev)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
+    gs, sh = torch.from_numpy(wl.group_start).to(dev), torch.from_numpy(wl.shared_blocks).to(dev)
+    mx = 8  # an upper bound the groups do not reach
+    max_ctx = int(wl.ctx.max())
+    ws = torch.zeros(max(kvc.paged_decode_cascade_plan(B, wl.Hq, wl.Hkv, wl.D, max_ctx, len(wl.group_start) - 1, mx),
+                         16), dtype=torch.uint8, device=dev)
+    q0 = torch.from_numpy(wl.q).to(dev)
+    outs = [torch.empty_like(q0) for _ in range(3)]
+
+    def chain():
+        src = q0
+        for o in outs:
+            kvc.paged_decode_cascade_attention(src, kp, vp, table, ctx_d, gs, sh, mx, wl.scale, o, ws, max_ctx)
+            src = o
+    g = _graph(chain)
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    src = wl.q
+    for i, o in enumerate(outs):
+        ref = oracle.decode(src, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+        check_attention(o, ref, f"cascade chain without shared blocks, call {i}")
+        src = o.cpu().numpy()
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_host_step_copies_overlapped_with_calls(fused):
-    """The step fed from pinned host memory with its copies overlapped with the calls (HostStep: inputs in three
-    copies on two streams, each layer's output copied back as soon as its call ends), replayed from a CUDA graph
-    with launch overlap and then run eagerly.  Before each run the device inputs hold wrong but valid values
+    """The step fed from pinned host memory with its copies overlapped with the calls (HostStep: staging-copy
+    kernels in the calls' stream bring the inputs in, in pieces alongside earlier calls, and take the outputs back,
+    eight layers at a time alongside a later call), replayed from a CUDA graph with launch overlap and then run
+    eagerly.  Before each run the device inputs hold wrong but valid values
     (block 0, context 1, slot 0, NaN activations) and the device and host outputs NaN, so a call that ran ahead
     of its input copy, or a copy back that ran ahead of its call, shows up."""
     from oracle import paging as opaging
