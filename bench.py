@@ -192,6 +192,26 @@ def oracle_sample(wl, seqs: int, layers, nthreads=None):
     return secs, nbytes
 
 
+def oracle_single_sequence_one_thread(seconds=1.0):
+    """The oracle's decode of the single-sequence workload (context 256, 1 q / 1 KV head) on one thread: time per
+    call over about `seconds` of repeated calls."""
+    import oracle
+    from oracle import paging
+    import workloads
+    wl = workloads.single_sequence_256()
+    kc, vc = paging.fill_layer(wl, 0)
+    oracle.append(kc, vc, wl.k_new[0], wl.v_new[0], paging.step_slots(wl.block_table, wl.ctx, wl.bs))
+    n, t = 0, 0.0
+    while t < seconds:
+        t0 = time.perf_counter()
+        oracle.decode(wl.q[0], kc, vc, wl.block_table, wl.ctx, wl.scale, nthreads=1)
+        t += time.perf_counter() - t0
+        n += 1
+    us = t / n * 1e6
+    return {"us_per_call": us, "GBps": wl.kv_tokens * wl.Hkv * wl.D * 2 * 2 / (us * 1e-6) / 1e9, "cores": 1,
+            "calls": n}
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -355,9 +375,14 @@ def run_ours(args):
             layers += 1
         cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": oracle.default_threads(), "kind": "oracle",
                "sample": f"{layers} layer decodes of the 24-layer step (all 32 sequences, cycling layers), fp64, "
-                         f"{secs:.1f} s of oracle time"}
+                         f"{secs:.1f} s of oracle time",
+               "single_sequence_ctx256_one_thread": oracle_single_sequence_one_thread()}
 
     peak, peak_kind = load_peaks()
+    # the other listed workloads, measured after the headline (rank 0 at N = 1; not part of the timed step)
+    suite = None
+    if rank == 0 and world == 1 and not args.no_suite:
+        suite = config_summary(device, peak, load_tflops_peak()[0])
     gbs = whole_job_rate(step_bytes, world, ms_step) / 1e9
     call_bytes = decode_call_bytes(ctx_total, nblocks_total) + (B * HKV * D * 2 * 2 * 2 if fused else 0)
     achieved = call_bytes / (us_decode * 1e-6) / 1e9
@@ -379,6 +404,7 @@ def run_ours(args):
                                + " call, one layer (split merge inside the kernel, on chip)",
                      "bytes_per_launch": call_bytes, "us_per_launch": us_decode},
         "cpu_baseline": cpu,
+        "suite": suite,
         "e2e": {"value": whole_job_rate(step_bytes, world, ms_e2e) / 1e9, "unit": "GB/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "host wall clock per step: the step's inputs (block table, context lengths, slots, then "
@@ -464,18 +490,159 @@ def _decode_state(B, ctx, Hq, Hkv, D, device, seed):
     return k_pool, v_pool, table, ctx_t, q, kn, vn
 
 
+def _cfg1_us_per_call(device, stream):
+    """Single sequence at context 256 (1 q / 1 KV head): the fused append + decode call, 100 back to back in a CUDA
+    graph (latency-bound; the 64 KiB context stays in L2)."""
+    import torch
+    import workloads
+    from paged_kv_cache_27_gb300 import harness
+    wl = workloads.single_sequence_256()
+    sess = harness.DecodeSession(wl, device=device, out_dtype=torch.float32).fill()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(100):
+            sess.decode_append(0)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(10):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sess.close()
+    return e0.elapsed_time(e1) * 1e3 / 1000, wl.kv_tokens * wl.Hkv * wl.D * 2 * 2
+
+
+def _cfg3_serving_mix(device, stream, flush):
+    """The shared-prefix serving mix after its step's block management: the fused append + decode call with L2
+    flushed, and attention alone through the plain decode and the cascade call."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    import workloads
+    from paged_kv_cache_27_gb300 import harness
+    mix = workloads.shared_prefix_mix()
+    res = harness.serving_mix(mix, device=device, poison=False)
+    table = torch.from_numpy(res["block_table"]).to(device)
+    ctx = torch.from_numpy(mix.ctx).to(device)
+    q = torch.from_numpy(mix.q).to(device)
+    kn, vn = torch.from_numpy(mix.k_new).to(device), torch.from_numpy(mix.v_new).to(device)
+    out = torch.empty((mix.B, mix.Hq, mix.D), dtype=torch.float16, device=device)
+    max_ctx = int(mix.ctx.max())
+    _, _, ws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
+    wsb = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+    step = lambda: kvc.paged_decode_append_attention(q, kn, vn, res["k_cache"], res["v_cache"], table, ctx,
+                                                      mix.scale, out, wsb, max_ctx)
+    us_step = _timed_calls(step, 20, flush, stream)
+    plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, wsb,
+                                               max_ctx)
+    us_plain = _timed_calls(plain, 20, flush, stream)
+    gs, sh, mxs = kvc.kv_cascade_groups(res["block_table"], mix.ctx)
+    gs_d, sh_d = torch.from_numpy(gs).to(device), torch.from_numpy(sh).to(device)
+    cws = kvc.paged_decode_cascade_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx, len(gs) - 1, mxs)
+    cwsb = torch.zeros(max(cws, 16), dtype=torch.uint8, device=device)
+    casc = lambda: kvc.paged_decode_cascade_attention(q, res["k_cache"], res["v_cache"], table, ctx, gs_d, sh_d, mxs,
+                                                      mix.scale, out, cwsb, max_ctx)
+    us_casc = _timed_calls(casc, 20, flush, stream)
+    row = 2 * mix.Hkv * mix.D * 2
+    logical = int(mix.ctx.astype(np.int64).sum()) * row
+    used = set()
+    for b in range(mix.B):
+        used.update(res["block_table"][b, :-(-int(mix.ctx[b]) // 16)].tolist())
+    unique = len(used) * 16 * row
+    return {"us_step": us_step, "logical_bytes": logical, "unique_bytes": unique, "tokens": mix.B,
+            "us_decode_plain": us_plain, "us_decode_cascade": us_casc}
+
+
+def _cfg4_cell_us(B, c, device, stream, flush):
+    """One long-context cell: the fused append + decode call with L2 flushed; returns (us, splits, blocks/split)."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    kp, vp, tb, ct, q4, kn4, vn4 = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
+    o4 = torch.empty((B, 14, 64), dtype=torch.float16, device=device)
+    ns, bps, ws = kvc.paged_decode_plan(B, 14, 2, 64, c)
+    w4 = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+    fn = lambda: kvc.paged_decode_append_attention(q4, kn4, vn4, kp, vp, tb, ct, 0.125, o4, w4, c)
+    us = _timed_calls(fn, 20, flush, stream)
+    del kp, vp
+    return us, ns, bps
+
+
+def _prefill_us(seqlens, Hq, Hkv, D, causal, precise, device, stream, flush):
+    """A varlen prefill call with L2 flushed, per call and replayed from a graph; returns (us, us_graph, flops)."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    T = sum(seqlens)
+    gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
+    qq = torch.randn((T, Hq, D), generator=gen, device=device).half()
+    kk = torch.randn((T, Hkv, D), generator=gen, device=device).half()
+    vv = torch.randn((T, Hkv, D), generator=gen, device=device).half()
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
+    oo = torch.empty((T, Hq, D), dtype=torch.float16, device=device)
+    fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo, precise=precise)
+    us = _timed_calls(fn, 20, flush, stream)
+    us_g = _timed_calls(_graph_of(fn, device), 20, flush, stream)
+    pairs = sum(s * (s + 1) // 2 for s in seqlens) if causal else sum(s * s for s in seqlens)
+    return us, us_g, 4 * D * Hq * pairs
+
+
+def config_summary(device, peak, tflops_peak):
+    """Compact figures for the other listed workloads, taken after the headline measurement (one GPU): single
+    sequence, shared-prefix serving mix, the 12 long-context cells, and the two prefill shapes."""
+    import torch
+    t0 = time.perf_counter()
+    stream = torch.cuda.current_stream(device)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=device)
+    gbs = lambda nbytes, us: nbytes / (us * 1e-6) / 1e9
+    out = {"timing": "device time (CUDA events) per call; L2 flushed (256 MiB written) before each timed call, "
+                     "except the single sequence (100 calls in a graph, L2-resident)"}
+    us, nb = _cfg1_us_per_call(device, stream)
+    out["single_sequence_ctx256"] = {"us_per_call": round(us, 3), "GBps": round(gbs(nb, us), 1), "kv_bytes": nb}
+    c3 = _cfg3_serving_mix(device, stream, flush)
+    out["serving_mix_B200"] = {
+        "us_per_step": round(c3["us_step"], 2), "tokens_per_s": round(c3["tokens"] / (c3["us_step"] * 1e-6)),
+        "logical_GBps": round(gbs(c3["logical_bytes"], c3["us_step"]), 1),
+        "unique_GBps": round(gbs(c3["unique_bytes"], c3["us_step"]), 1),
+        "pct_hbm_peak_unique": round(gbs(c3["unique_bytes"], c3["us_step"]) / peak * 100, 2),
+        "us_decode_plain": round(c3["us_decode_plain"], 2), "us_decode_cascade": round(c3["us_decode_cascade"], 2),
+        "cascade_speedup": round(c3["us_decode_plain"] / c3["us_decode_cascade"], 3),
+        "logical_bytes": c3["logical_bytes"], "unique_bytes": c3["unique_bytes"]}
+    cells = []
+    for B in (1, 4, 16):
+        for c in (4096, 16384, 65536, 131072):
+            us, ns, bps = _cfg4_cell_us(B, c, device, stream, flush)
+            nb = B * c * 2 * 2 * 64 * 2
+            cells.append({"B": B, "ctx": c, "us_per_call": round(us, 2), "GBps": round(gbs(nb, us), 1),
+                          "pct_hbm_peak": round(gbs(nb, us) / peak * 100, 2), "splits": ns, "blocks_per_split": bps})
+    out["long_context"] = cells
+    for name, seqlens, hq, hkv in (("prefill_varlen_37_120_8_200_8x8_d64_causal", (37, 120, 8, 200), 8, 8),
+                                   ("prefill_gqa_2x256_8x2_d64_causal", (256, 256), 8, 2)):
+        us, us_g, fl = _prefill_us(seqlens, hq, hkv, 64, True, False, device, stream, flush)
+        out[name] = {"us_per_call": round(us, 2), "us_per_call_graph": round(us_g, 2),
+                     "TFLOPs_graph": round(fl / (us_g * 1e-6) / 1e12, 2),
+                     "pct_tensor_peak_graph": round(fl / (us_g * 1e-6) / 1e12 / tflops_peak * 100, 3),
+                     "flops": fl}
+    del flush
+    torch.cuda.synchronize()
+    out["seconds"] = round(time.perf_counter() - t0, 1)
+    return out
+
+
+def load_tflops_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 = fp16 tensor rate)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def run_suite(args):
     import torch
 
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     peak, peak_kind = load_peaks()
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            tflops_peak = float(json.load(f)["bf16_tflops"])
-        tflops_kind = "measured (bf16 = fp16 tensor rate)"
-    except Exception:
-        tflops_peak, tflops_kind = 1900.0, "fallback"
+    tflops_peak, tflops_kind = load_tflops_peak()
     stream = torch.cuda.current_stream(device)
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=device)
     emit = lambda d: print(json.dumps(dict(suite=True, **d)), flush=True)
@@ -498,52 +665,23 @@ def run_suite_decode(device, stream, flush, emit, peak):
     from paged_kv_cache_27_gb300 import harness
 
     # one sequence at context 256 (L2-resident, latency-bound)
-    wl = workloads.single_sequence_256()
-    sess = harness.DecodeSession(wl, device=device, out_dtype=torch.float32).fill()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(100):
-            sess.decode(0)
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(10):
-        g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    emit({"config": "single sequence: B=1, 1 q / 1 KV head, D=64, context 256", "us_per_decode": e0.elapsed_time(e1) * 1e3 / 1000,
-          "note": "100 back-to-back calls in a CUDA graph; latency-bound, the 64 KiB context sits in L2"})
-    sess.close()
+    us, _ = _cfg1_us_per_call(device, stream)
+    emit({"config": "single sequence: B=1, 1 q / 1 KV head, D=64, context 256", "us_per_decode": us,
+          "note": "fused append + decode, 100 back-to-back calls in a CUDA graph; latency-bound, the 64 KiB context "
+                  "sits in L2"})
 
     # shared-prefix serving mix: 200 sequences, groups of 8 share a 512-token prefix (refcounted blocks)
-    mix = workloads.shared_prefix_mix()
-    res = harness.serving_mix(mix, device=device, poison=False)
-    table = torch.from_numpy(res["block_table"]).to(device)
-    ctx = torch.from_numpy(mix.ctx).to(device)
-    q = torch.from_numpy(mix.q).to(device)
-    kn, vn = torch.from_numpy(mix.k_new).to(device), torch.from_numpy(mix.v_new).to(device)
-    out = torch.empty((mix.B, mix.Hq, mix.D), dtype=torch.float16, device=device)
-    max_ctx = int(mix.ctx.max())
-    _, _, ws = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, max_ctx)
-    wsb = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
-    step = lambda: kvc.paged_decode_append_attention(q, kn, vn, res["k_cache"], res["v_cache"], table, ctx,
-                                                      mix.scale, out, wsb, max_ctx)
-    us = _timed_calls(step, 20, flush, stream)
-    row = 2 * mix.Hkv * mix.D * 2  # K + V bytes per token
-    logical = int(mix.ctx.astype(np.int64).sum()) * row
-    used = set()
-    for b in range(mix.B):
-        used.update(res["block_table"][b, :-(-int(mix.ctx[b]) // 16)].tolist())
-    unique = len(used) * 16 * row
+    c3 = _cfg3_serving_mix(device, stream, flush)
+    us = c3["us_step"]
+    logical, unique = c3["logical_bytes"], c3["unique_bytes"]
     emit({"config": "shared-prefix serving mix: B=200, 14 q / 2 KV heads, D=64, ctx ~ U{16..4096}, groups of 8 share a 512-token prefix",
-          "us_per_step": us, "tokens_per_s": mix.B / (us * 1e-6),
+          "us_per_step": us, "tokens_per_s": c3["tokens"] / (us * 1e-6),
           "logical_GBps": logical / (us * 1e-6) / 1e9, "unique_GBps": unique / (us * 1e-6) / 1e9,
           "logical_bytes": logical, "unique_bytes": unique, "pct_hbm_peak_unique": unique / (us * 1e-6) / 1e9 / peak * 100,
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
                   "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
 
-    run_suite_cascade(device, stream, flush, emit, peak, mix, res)
+    run_suite_cascade(device, stream, flush, emit, peak)
 
     run_suite_multi(device, stream, flush, emit, peak)
 
@@ -652,18 +790,11 @@ def run_suite_decode(device, stream, flush, emit, peak):
     # long contexts, B in {1, 4, 16} x ctx in {4k, 16k, 64k, 128k}
     for B in (1, 4, 16):
         for c in (4096, 16384, 65536, 131072):
-            kp, vp, tb, ct, q4, kn4, vn4 = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
-            o4 = torch.empty((B, 14, 64), dtype=torch.float16, device=device)
-            ns, bps, ws = kvc.paged_decode_plan(B, 14, 2, 64, c)
-            w4 = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
-            fn = lambda: kvc.paged_decode_append_attention(q4, kn4, vn4, kp, vp, tb, ct, 0.125, o4, w4, c)
-            us = _timed_calls(fn, 20, flush, stream)
+            us, ns, bps = _cfg4_cell_us(B, c, device, stream, flush)
             nbytes = B * c * 2 * 2 * 64 * 2
             emit({"config": f"long context: B={B}, ctx={c}, 14 q / 2 KV heads, D=64", "us_per_call": us,
                   "GBps": nbytes / (us * 1e-6) / 1e9, "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100,
                   "splits": ns, "blocks_per_split": bps, "kv_bytes": nbytes})
-            del kp, vp
-
 
 
 def run_suite_cascade(device, stream, flush, emit, peak, mix=None, res=None):
@@ -798,19 +929,7 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
 
     # prefill shapes: causal varlen prefill on the tensor cores
     def prefill_case(name, seqlens, Hq, Hkv, D, causal=True, precise=False):
-        T = sum(seqlens)
-        gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
-        qq = torch.randn((T, Hq, D), generator=gen, device=device).half()
-        kk = torch.randn((T, Hkv, D), generator=gen, device=device).half()
-        vv = torch.randn((T, Hkv, D), generator=gen, device=device).half()
-        cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
-        oo = torch.empty((T, Hq, D), dtype=torch.float16, device=device)
-        fn = lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 1.0 / np.sqrt(D), causal, oo,
-                                           precise=precise)
-        us = _timed_calls(fn, 20, flush, stream)
-        us_g = _timed_calls(_graph_of(fn, device), 20, flush, stream)  # device time: the call replayed from a graph
-        pairs = sum(s * (s + 1) // 2 for s in seqlens) if causal else sum(s * s for s in seqlens)
-        flops = 4 * D * Hq * pairs
+        us, us_g, flops = _prefill_us(seqlens, Hq, Hkv, D, causal, precise, device, stream, flush)
         tf = flops / (us * 1e-6) / 1e12
         emit({"config": name, "p_precision": "split (fp16 high part + residual)" if precise else "fp16",
               "us_per_call": us, "TFLOPs": tf, "pct_tensor_peak": tf / tflops_peak * 100,
@@ -839,6 +958,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--blocks-per-split", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-suite", action="store_true", help="skip the other workloads' figures in the headline line")
     ap.add_argument("--unfused", action="store_true", help="separate kv_append + paged_decode_attention calls")
     ap.add_argument("--no-overlap", action="store_true", help="no programmatic dependent launch")
     ap.add_argument("--profile-only", action="store_true", help="replay warmup+steps graph steps, print nothing")

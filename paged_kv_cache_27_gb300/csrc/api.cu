@@ -378,6 +378,12 @@ kvc_status kvc_set_launch_overlap(int on) {
     return KVC_OK;
 }
 
+kvc_status kvc_set_cascade_min_shared_blocks(int blocks) {
+    if (blocks < 0) return fail(KVC_ERR_INVALID, "negative block count %d", blocks);
+    kvc::set_cascade_min_shared_blocks(blocks);
+    return KVC_OK;
+}
+
 // The address the current device uses for p: device and managed memory as they are, pinned host memory
 // through its mapping.  False for pageable host memory and unknown pointers.
 static bool device_address(const void* p, void** out) {

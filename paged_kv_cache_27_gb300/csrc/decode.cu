@@ -139,9 +139,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // the CTA's merged state: m[8], l[8], acc[8][D]
     // this CTA's merged state when it is cluster rank 0: m[8], l[8], acc[G][D] (the layout of an inbox slot)
     float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
-    int* s_table = reinterpret_cast<int*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
     // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like the state at s_m
-    float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes + C::kTableBytes);
+    float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
+    // the cluster's slice of the block table (bpc entries), after the inbox's cluster - 1 slots
+    int* s_table = reinterpret_cast<int*>(s_inbox + (p.csize - 1) * (16 + p.G * D));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -162,9 +163,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // each warp owns its barriers; lane 0 initialises them before it has any load outstanding, so
     // the release fence that publishes the initialisation has nothing to wait for
     uint64_t* wbars = bars + warp * ST;
+    // rank 0's inbox barrier: completes when the other CTAs' merged states have arrived (asynchronous pushes)
+    uint64_t* inbox_bar = bars + NW * ST;
+    // bytes one CTA pushes into an inbox slot: acc[G][D], and m and l of its G heads
+    const uint32_t push_bytes = static_cast<uint32_t>(p.G * D * 4 + p.G * 8);
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
+        if (KVC_DEC_ASYNC_PUSH && warp == 0 && cs > 1) mbar_init(inbox_bar, 1);
         fence_barrier_init();
+        // the one arrival of the inbox phase, with the bytes it waits for (they may land before or after it)
+        if (KVC_DEC_ASYNC_PUSH && warp == 0 && cs > 1 && rank == 0)
+            mbar_arrive_expect_tx(inbox_bar, static_cast<uint32_t>(cs - 1) * push_bytes);
     }
 
     // One round trip before the first copies: each warp's lane 0 fetches the table entries of its
@@ -558,12 +567,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     const int stride = 16 + p.G * D;  // floats per cluster merge slot: m[8], l[8], acc[G][D]
     // in a cluster this CTA's merged state goes to its slot in rank 0: rank 0's own state at s_m, or
     // inbox slot rank - 1 (same layout)
-    uint32_t slot = 0;
+    uint32_t slot = 0, remote_bar = 0;
     if (cs > 1) {
         // every CTA of the cluster has started (the prologue arrive), so rank 0's shared memory is live
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
         slot = map_to_rank(rank == 0 ? s_m : s_inbox + (rank - 1) * stride, 0);
+        remote_bar = map_to_rank(inbox_bar, 0);
     }
+    const bool push_async = KVC_DEC_ASYNC_PUSH && cs > 1 && rank != 0;
     // every thread merges the warps of this CTA for four consecutive outputs (head gg, dims d..d+3): it
     // takes the CTA maximum M of its head and the warp weights 2^(m_w - M) itself, so no further barrier
     // is needed
@@ -594,6 +605,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                     p.part_ml[row * 2 + 0] = M;
                     p.part_ml[row * 2 + 1] = L;
                 }
+            } else if (push_async) {
+                st_async_f32x4(slot + 4u * (16 + e), O, remote_bar);
+                if (d == 0) {
+                    st_async_f32(slot + 4u * gg, M, remote_bar);
+                    st_async_f32(slot + 4u * (8 + gg), L, remote_bar);
+                }
             } else {
                 asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(slot + 4u * (16 + e)),
                              "f"(O.x), "f"(O.y), "f"(O.z), "f"(O.w)
@@ -611,9 +628,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     }
     KVC_TRACE_MARK(5);
 
-    // ---- merge the CTAs of this cluster in rank 0: every CTA has pushed its state into its slot (remote
-    // stores, no round trip); it arrives on the cluster barrier (release) and leaves. Rank 0 waits for all
-    // arrivals (acquire), which makes every slot visible to it, and merges locally ----
+    // ---- merge the CTAs of this cluster in rank 0 ----
+#if KVC_DEC_ASYNC_PUSH
+    // every other CTA has issued its asynchronous pushes and leaves (nothing of it is read by others); rank 0
+    // waits until all their bytes have landed on its inbox barrier (acquire at cluster scope makes them visible)
+    // and its own state is in place, and merges locally
+    if (rank != 0) {
+        KVC_TRACE_MARK(6);
+        KVC_TRACE_END();
+        return;
+    }
+    __syncthreads();  // rank 0's own merged state (written by all its threads) is complete
+    if (!mbar_wait_cluster_bounded(inbox_bar, 0, 4 * kWaitLimitNs)) {
+        if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
+    }
+#else
+    // every CTA has pushed its state into its slot (remote stores, no round trip); it arrives on the cluster
+    // barrier (release) and leaves. Rank 0 waits for all arrivals (acquire), which makes every slot visible to
+    // it, and merges locally
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (rank != 0) {
         KVC_TRACE_MARK(6);
@@ -621,6 +653,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         return;  // nothing of this CTA is read by others
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+#endif
     KVC_TRACE_MARK(6);
     // slot c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c; a CTA without
     // blocks has l = 0 and takes no part
@@ -737,13 +770,13 @@ static cudaError_t decode_setup() {
         for (auto kern : {paged_decode_kernel<D, false>, paged_decode_kernel<D, true>}) {
             if (err == cudaSuccess)
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::smem_bytes(kMaxCluster, 8));
+                                           C::smem_bytes(kMaxCluster, 8, kMaxClusterBlocks));
             if (err == cudaSuccess && kMaxCluster > 8)
                 err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         }
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(paged_decode_kernel<D, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DecodeCfg<D, true>::smem_bytes(kMaxCluster, 8));
+                                       DecodeCfg<D, true>::smem_bytes(kMaxCluster, 8, kMaxClusterBlocks));
         if (err == cudaSuccess && kMaxCluster > 8)
             err = cudaFuncSetAttribute(paged_decode_kernel<D, false, true>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -794,7 +827,7 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
         // one wave of KVC_DEC_PLAN_CTAS CTAs per SM for all (sequence, KV head) pairs, at least one block per
         // warp; recomputed once if the chosen cluster's inbox lowers the occupancy below that
         int occ = 0;
-        cudaError_t e = decode_occupancy<D>(C::smem_bytes(1, G), &occ);
+        cudaError_t e = decode_occupancy<D>(C::smem_bytes(1, G, std::min(nblk, kMaxClusterBlocks)), &occ);
         if (e != cudaSuccess) return e;
         const int64_t segs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
         for (int pass = 0; pass < 2; ++pass) {
@@ -808,7 +841,7 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
             ncl = std::max<int64_t>(ncl, (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks);
             bpc = static_cast<int>((nblk + ncl - 1) / ncl);
             int occ2 = 0;
-            e = decode_occupancy<D>(C::smem_bytes(cs, G), &occ2);
+            e = decode_occupancy<D>(C::smem_bytes(cs, G, bpc), &occ2);
             if (e != cudaSuccess) return e;
             if (occ2 >= std::min(occ, KVC_DEC_PLAN_CTAS)) break;
             occ = occ2;
@@ -889,10 +922,12 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     dim3 grid(plan.num_splits, a.Hkv, a.B);
     if (fp8)
         e = launch(paged_decode_kernel<D, false, true>, grid, dim3(DecodeCfg<D, true>::kThreads),
-                   DecodeCfg<D, true>::smem_bytes(plan.cluster, p.G), stream, pdl, static_cast<unsigned>(plan.cluster),
+                   DecodeCfg<D, true>::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream, pdl,
+                   static_cast<unsigned>(plan.cluster),
                    tmK, tmV, p);
     else
-        e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads), C::smem_bytes(plan.cluster, p.G), stream,
+        e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads),
+                   C::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream,
                    pdl, static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
@@ -956,7 +991,8 @@ static cudaError_t launch_suffix_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.part_stride = part_stride;
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     return launch(paged_decode_kernel<D, true>, dim3(plan.num_splits, a.Hkv, a.B), dim3(C::kThreads),
-                  C::smem_bytes(plan.cluster, p.G), stream, pdl, static_cast<unsigned>(plan.cluster), tmK, tmV, p);
+                  C::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream, pdl,
+                  static_cast<unsigned>(plan.cluster), tmK, tmV, p);
 }
 
 cudaError_t launch_decode_suffix(const DecodeArgs& a, const DecodePlan& plan, const int32_t* blk_off, int part_base,

@@ -57,6 +57,11 @@ namespace kvc {
 #ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
 #define KVC_DEC_PLAN_CTAS 2
 #endif
+// 1: the CTAs of a cluster hand their merged states to rank 0 with st.async, whose bytes complete on an mbarrier
+// in rank 0 (senders leave at once); 0: remote stores, then a cluster barrier (release / acquire)
+#ifndef KVC_DEC_ASYNC_PUSH
+#define KVC_DEC_ASYNC_PUSH 1
+#endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -84,12 +89,15 @@ struct DecodeCfg {
     static constexpr int kWarpRingBytes = kFp8 ? (kScaleOff + kStages * 2 * kScaleBytes + 1023) / 1024 * 1024
                                                : kStages * kStageBytes;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
-    static constexpr int kBarBytes = kWarps * kStages * 8;
+    // the warps' stage barriers, then rank 0's inbox barrier (padded to keep what follows 16-byte aligned)
+    static constexpr int kBarBytes = kWarps * kStages * 8 + 16;
     static constexpr int kStateBytes = 8 * (D + 2) * 4;  // merged (m[8], l[8], acc[8][D]) of this CTA
-    static constexpr int kTableBytes = kMaxClusterBlocks * 4 + 16;  // table slice (+ 16 bytes of alignment)
-    // + the inbox of cluster rank 0 (one slot per other CTA of the cluster, sized at launch) + alignment slack
-    static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + kTableBytes + 1024;
-    static int smem_bytes(int cluster, int G) { return kBaseSmemBytes + (cluster - 1) * (16 + G * D) * 4; }
+    // + the inbox of cluster rank 0 (one slot per other CTA of the cluster) and the cluster's slice of the block
+    // table (bpc entries), both sized at launch, + alignment slack
+    static constexpr int kBaseSmemBytes = kRingBytes + kBarBytes + kStateBytes + 1024;
+    static int smem_bytes(int cluster, int G, int bpc) {
+        return kBaseSmemBytes + (cluster - 1) * (16 + G * D) * 4 + (bpc * 4 + 15) / 16 * 16;
+    }
     static constexpr int kMergeStride = D + 4;  // floats per parked row
     static_assert(16 * 4 + 8 * kMergeStride * 4 <= kWarpRingBytes, "warp state must fit a warp ring");
 };

@@ -46,6 +46,14 @@ namespace kvc {
 #ifndef KVC_MULTI_CTAS  // CTAs per SM the chunking aims for (one where a CTA needs the SM's registers)
 #define KVC_MULTI_CTAS 2
 #endif
+// A cascade call whose shared prefixes are shorter than this many blocks runs the plain decode instead: reading a
+// short prefix once per group saves less than the two extra launches cost (measured on the shared-prefix serving
+// mix and on longer shared prefixes)
+#ifndef KVC_CASCADE_MIN_SHARED_BLOCKS
+#define KVC_CASCADE_MIN_SHARED_BLOCKS 384
+#endif
+static std::atomic<int> g_cascade_min_shared{KVC_CASCADE_MIN_SHARED_BLOCKS};
+void set_cascade_min_shared_blocks(int blocks) { g_cascade_min_shared.store(blocks); }
 #ifndef KVC_PREFIX_TC_MIN_ROWS  // cascade prefix, head dim 64: groups of this many query rows run on the tensor cores
 #define KVC_PREFIX_TC_MIN_ROWS 17
 #endif
@@ -707,7 +715,11 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_group
     }
     if (max_shared_blocks <= 0) plan->nchunks = 0;
     plan->part_stride = plan->nchunks + plan->suffix.num_parts;
-    plan->workspace_bytes = partials_bytes(static_cast<size_t>(B) * Hq * plan->part_stride, D);
+    plan->plain = max_shared_blocks < g_cascade_min_shared.load(std::memory_order_relaxed);
+    // the plain decode over the full contexts is the suffix plan without block offsets: its workspace
+    // (plan->suffix.workspace_bytes) never exceeds the cascade's, so one size serves both routes
+    plan->workspace_bytes = plan->plain ? plan->suffix.workspace_bytes
+                                        : partials_bytes(static_cast<size_t>(B) * Hq * plan->part_stride, D);
     return cudaSuccess;
 }
 
@@ -775,6 +787,7 @@ cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, cons
     cudaError_t e = cascade_plan(a.B, a.Hq, a.Hkv, a.D, a.max_context_len, n_groups, max_shared_blocks, &cp);
     if (e != cudaSuccess) return e;
     if (cp.workspace_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    if (cp.plain) return launch_decode(a, stream);  // the same result, every block read per sequence
     switch (a.D) {
         case 64: return launch_cascade_d<64>(a, group_start, shared_blocks, n_groups, cp, stream);
         case 128: return launch_cascade_d<128>(a, group_start, shared_blocks, n_groups, cp, stream);

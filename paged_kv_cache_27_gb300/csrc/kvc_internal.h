@@ -94,10 +94,13 @@ struct CascadePlan {
     int cluster;        // prefix CTAs per cluster (one prefix part per cluster)
     int nchunks;        // prefix parts per (sequence, head): clusters over the longest shared prefix
     int part_stride;    // partial rows per (sequence, head): nchunks + suffix.num_parts
+    bool plain;         // shared prefixes too short to pay for the extra launches: run the plain decode
     size_t workspace_bytes;
 };
 cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int n_groups, int max_shared_blocks,
                          CascadePlan* plan);
+// process-wide: cascade calls with max_shared_blocks below this run the plain decode
+void set_cascade_min_shared_blocks(int blocks);
 // group_start: device [n_groups + 1]; shared_blocks: device [B], the shared blocks of each sequence's group
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);

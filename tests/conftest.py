@@ -13,7 +13,13 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: full-size case")
 
 
+LAST_MODULES = ("test_zz_no_alloc",)  # run after every other test (see that module's docstring)
+
+
 def pytest_collection_modifyitems(config, items):
+    # the allocation-free entry point's tests go last whatever the file order: if one of them fails, a run that
+    # stops at the first failure has already run every other test
+    items.sort(key=lambda it: getattr(it.module, "__name__", "").rsplit(".", 1)[-1] in LAST_MODULES)
     # GPU tests cannot run without a device; skip them cleanly when asked for them anyway
     try:
         import torch

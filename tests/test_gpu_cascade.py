@@ -10,6 +10,17 @@ from parity import check_attention
 
 pytestmark = pytest.mark.gpu
 
+DEFAULT_MIN_SHARED = 384  # the library's default routing threshold (blocks)
+
+
+@pytest.fixture(autouse=True)
+def always_cascade():
+    """These tests exercise the cascade kernels themselves: route every call to them, whatever its prefix."""
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_set_cascade_min_shared_blocks(0)
+    yield
+    kvc.kvc_set_cascade_min_shared_blocks(DEFAULT_MIN_SHARED)
+
 
 def run_cascade(wl, out_dtype=torch.float32, checked=False, group_start=None, shared=None, max_shared=None):
     import paged_kv_cache_27_gb300 as kvc
@@ -154,3 +165,22 @@ def test_cascade_full_group_rows_and_scale_sign(scale_sign):
     ref = oracle_out(wl)
     check_attention(out, ref, f"cascade, 64 rows, scale sign {scale_sign}")
     assert (out - pout).abs().max().item() < 1e-4
+
+
+def test_short_prefix_routes_to_plain_decode():
+    """With the default routing, a cascade call whose shared prefixes are short runs the plain decode kernel: its
+    output is bit-identical to paged_decode_attention's; forced onto the cascade kernels it agrees within the
+    tolerance.  Both are checked against the oracle."""
+    import paged_kv_cache_27_gb300 as kvc
+    wl = workloads.cascade_decode(71, [8, 8], [32, 20], list(np.random.default_rng(3).integers(1, 300, size=16)))
+    kvc.kvc_set_cascade_min_shared_blocks(DEFAULT_MIN_SHARED)
+    out, pout = run_cascade(wl)
+    assert torch.equal(out, pout)
+    kvc.kvc_set_cascade_min_shared_blocks(0)
+    out_c, _ = run_cascade(wl)
+    ref = oracle_out(wl)
+    check_attention(out, ref, "routed to the plain decode")
+    check_attention(out_c, ref, "forced cascade")
+    assert not torch.equal(out_c, pout)  # a different summation order: the cascade kernels really ran
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_set_cascade_min_shared_blocks(-1)

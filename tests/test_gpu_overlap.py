@@ -60,8 +60,16 @@ def test_multi_token_chain_in_graph(T, ctx):
         src = o.cpu().numpy()  # the next call's q, as the GPU wrote it
 
 
+@pytest.fixture
+def always_cascade():
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_set_cascade_min_shared_blocks(0)  # the cascade kernels, whatever the prefix length
+    yield
+    kvc.kvc_set_cascade_min_shared_blocks(384)
+
+
 @pytest.mark.parametrize("D,Hq,Hkv", [(64, 14, 2), (128, 8, 8)])
-def test_cascade_chain_in_graph(D, Hq, Hkv):
+def test_cascade_chain_in_graph(D, Hq, Hkv, always_cascade):
     import paged_kv_cache_27_gb300 as kvc
     extra = list(np.random.default_rng(5).integers(1, 200, size=16))
     wl = workloads.cascade_decode(43, [8, 5, 3], [40, 7, 0], extra, Hq=Hq, Hkv=Hkv, D=D)
@@ -175,7 +183,7 @@ def test_decode_chain_with_idle_combine_in_graph():
     s.close()
 
 
-def test_cascade_chain_without_shared_blocks_in_graph():
+def test_cascade_chain_without_shared_blocks_in_graph(always_cascade):
     """A cascade call told to expect shared prefixes when no group shares a block: every CTA of the prefix pass
     leaves at once.  Chained calls in a graph still see the previous call's complete output."""
     import paged_kv_cache_27_gb300 as kvc

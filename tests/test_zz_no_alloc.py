@@ -1,18 +1,25 @@
-"""The allocation-free decode entry point (runs last: its file name sorts after every other test file).
+"""The allocation-free decode entry point.
 
 Some callers cannot allocate device memory while they run (allocator code that
 would re-enter itself, plug-ins handed only their input and output buffers,
 serving loops that forbid cudaMalloc after start-up).  For them,
 paged_decode_attention_static_workspace keeps its split scratch in a fixed
 16 MiB array inside the library.  These tests call it through the C ABI and
-check it against paged_decode_attention with a caller workspace.
+check it against paged_decode_attention with a caller workspace and against
+the fp64 oracle.
+
+They run after every other test: the conftest moves this module to the end of
+the collected items (its file name also sorts last), so that if one of them
+fails, a run that stops at the first failure has already run the rest.  They
+pass the same way when run alone in a fresh process.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads
-from parity import ATOL
+from oracle import paging
+from parity import ATOL, check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +37,7 @@ def test_static_workspace_matches_caller_workspace_twice():
     ref = torch.empty_like(s.out[0])
     kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale, ref,
                                s.workspace, s.max_ctx, bps)
+    oracle_out, _, _ = paging.decode_step(wl, 0)  # the fp64 oracle after the same append
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         kvc.paged_decode_attention_static_workspace(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table,
@@ -38,6 +46,7 @@ def test_static_workspace_matches_caller_workspace_twice():
         assert torch.isfinite(out).all(), call
         err = (out.double() - ref.double()).abs().max().item()
         assert err <= ATOL, (call, err)
+        check_attention(out, oracle_out, f"static workspace, call {call}")
     assert kvc.kvc_device_error_flags(clear=True) == 0
     s.close()
 
