@@ -434,13 +434,20 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                         }
                         __syncwarp();
                     }
-                    // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots ----
+                    // ---- S^T = K Q^T: rows = the 16 tokens, columns = the 8 head slots; the head-dim steps go to
+                    // two accumulators in turn (two independent product chains), summed at the end ----
+                    float sc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(kbase + swz((mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                        mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
+                        if (ks & 1)
+                            mma_f16_16816(sc2, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
+                        else
+                            mma_f16_16816(sc, a0, a1, a2, a3, qa[ks][0], qa[ks][1]);
                     }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) sc[k] += sc2[k];
 #if KVC_DEC_EARLY_REFILL
                     // V^T fragments now; the stage is then free and its refill goes out before the softmax
 #pragma unroll
@@ -470,25 +477,33 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                 x[2] = g + 8 < rem ? sc[2] * sl2g8 : -INFINITY;
                 x[3] = g + 8 < rem ? sc[3] * sl2g8 : -INFINITY;
                 float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+                // the running maxima move only when a score exceeds them by more than 2^KVC_DEC_LAZY_MAX (always
+                // in the first block, where they are -inf); the weights below stay <= 2^KVC_DEC_LAZY_MAX
+                if (KVC_DEC_LAZY_MAX == 0 || __any_sync(0xffffffffu, mx0 > m_run[0] + KVC_DEC_LAZY_MAX ||
+                                                                      mx1 > m_run[1] + KVC_DEC_LAZY_MAX)) {
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-                const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
-                m_run[0] = mn0;
-                m_run[1] = mn1;
-                const float p0 = ex2(x[0] - mn0), p1 = ex2(x[1] - mn1), p2 = ex2(x[2] - mn0), p3 = ex2(x[3] - mn1);
-                l_run[0] = l_run[0] * al0 + p0 + p2;
-                l_run[1] = l_run[1] * al1 + p1 + p3;
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+                    const float al0 = ex2(m_run[0] - mn0), al1 = ex2(m_run[1] - mn1);
+                    m_run[0] = mn0;
+                    m_run[1] = mn1;
+                    l_run[0] *= al0;
+                    l_run[1] *= al1;
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[mt][0] *= al0;
+                        o[mt][1] *= al1;
+                        o[mt][2] *= al0;
+                        o[mt][3] *= al1;
+                    }
                 }
+                const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]), p2 = ex2(x[2] - m_run[0]),
+                            p3 = ex2(x[3] - m_run[1]);
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
                 // P^T as the B operand (k = tokens, n = heads): transpose the two 8x8 halves in registers;
                 // P = hi + lo, both fp16, so the P V product keeps ~fp32 accuracy
                 const float q0 = p0 * vsg, q1 = p1 * vsg, q2 = p2 * vsg8, q3 = p3 * vsg8;

@@ -62,6 +62,12 @@ namespace kvc {
 #ifndef KVC_DEC_ASYNC_PUSH
 #define KVC_DEC_ASYNC_PUSH 1
 #endif
+// Lazy running maximum in the decode kernel's online softmax: a block's scores are weighted against the running
+// maximum m as they are, 2^(x - m) <= 2^KVC_DEC_LAZY_MAX, unless one of them exceeds m by more than that; only
+// then is the block's maximum reduced across the lanes and the state rescaled.  0: every block moves the maximum.
+#ifndef KVC_DEC_LAZY_MAX
+#define KVC_DEC_LAZY_MAX 8
+#endif
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;

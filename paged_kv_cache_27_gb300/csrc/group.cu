@@ -202,9 +202,16 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
     };
     // each warp's lane 0 sets up its barriers and issues its first blocks straight from the table; the
     // chunk's ids go to shared memory meanwhile, for the refills
+    // rank 0's inbox barrier (in the padding after the stage barriers): completes when the other CTAs' merged
+    // states have arrived by asynchronous pushes of push_bytes each
+    uint64_t* inbox_bar = bars + NW * ST;
+    const uint32_t push_bytes = static_cast<uint32_t>(rows * D * 4 + rows * 8);
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
+        if (KVC_DEC_ASYNC_PUSH && warp == 0 && cs > 1) mbar_init(inbox_bar, 1);
         fence_barrier_init();
+        if (KVC_DEC_ASYNC_PUSH && warp == 0 && cs > 1 && rank == 0)
+            mbar_arrive_expect_tx(inbox_bar, static_cast<uint32_t>(cs - 1) * push_bytes);
         if (warp == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
@@ -426,11 +433,13 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
     __syncthreads();
     // in a cluster every CTA pushes its merged state into its slot of rank 0's inbox with remote stores, once
     // every CTA of the cluster has started (the arrive after the prologue), so rank 0's shared memory is live
-    uint32_t slot = 0;
+    uint32_t slot = 0, remote_bar = 0;
     if (cs > 1) {
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
         slot = map_to_rank(s_inbox + rank * C::kSlotFloats, 0);
+        remote_bar = map_to_rank(inbox_bar, 0);
     }
+    const bool push_async = KVC_DEC_ASYNC_PUSH && cs > 1 && rank != 0;
     // the output (or partial) row of query row c of this CTA
     auto out_row = [&](int c) -> int64_t { return q_row(r0 + c); };
     const bool final_out = !kPrefix && p.nclus == 1;  // this cluster's result is the output
@@ -454,7 +463,13 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
                 A = fma4(f, *reinterpret_cast<const float4*>(wp + 2 * RG + c * C::kRowStride + d), A);
             }
         }
-        if (cs > 1) {
+        if (push_async) {
+            st_async_f32x4(slot + 4u * (2 * RG + c * D + d), A, remote_bar);
+            if (d == 0) {
+                st_async_f32(slot + 4u * c, M, remote_bar);
+                st_async_f32(slot + 4u * (RG + c), L, remote_bar);
+            }
+        } else if (cs > 1) {
             st_cluster_f32x4(slot + 4u * (2 * RG + c * D + d), A);
             if (d == 0) {
                 st_cluster_f32(slot + 4u * c, M);
@@ -472,10 +487,20 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
         }
     }
     if (cs == 1) return;
+#if KVC_DEC_ASYNC_PUSH
+    // the other CTAs have issued their asynchronous pushes and leave; rank 0 waits until their bytes have landed
+    // on its inbox barrier and its own slot is written, then merges the slots
+    if (rank != 0) return;
+    __syncthreads();
+    if (!mbar_wait_cluster_bounded(inbox_bar, 0, 4 * kWaitLimitNs)) {
+        if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_TIMEOUT);
+    }
+#else
     // rank 0 merges the slots once every CTA has pushed its state (release / acquire); the others leave
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (rank != 0) return;
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+#endif
     for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
         const int c = idx / (D / 4), d = (idx % (D / 4)) * 4;
         float M = -INFINITY;
