@@ -586,6 +586,70 @@ def _prefill_us(seqlens, Hq, Hkv, D, causal, precise, device, stream, flush):
     return us, us_g, 4 * D * Hq * pairs
 
 
+def _fp8_vs_fp16_graph(device, stream, Lq=24, Bq=32, Cq=2048):
+    """24-layer decode-only CUDA graphs with launch overlap over the model step's shape (32 x 2048, 14 / 2 heads,
+    D = 64): fp16 pools, and the same pools quantized to fp8 e4m3 with per-row scales through kv_append_fp8 (24
+    different pools per form, more than L2).  Device time per layer of each form."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    kp0, vp0, tbq, ctq, _, _, _ = _decode_state(Bq, Cq, 14, 2, 64, device, seed=2024)
+    NBq = kp0.shape[0]
+    gen = torch.Generator(device=device).manual_seed(99)
+    k16 = [kp0] + [torch.randn(kp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
+    v16 = [vp0] + [torch.randn(vp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
+    k8 = [torch.empty(kp0.shape, dtype=torch.uint8, device=device) for _ in range(Lq)]
+    v8 = [torch.empty(kp0.shape[:2] + (64, 16), dtype=torch.uint8, device=device) for _ in range(Lq)]  # V^T rows
+    ks8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
+    vs8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
+    all_slots = torch.arange(NBq * 16, dtype=torch.int64, device=device)
+    for l in range(Lq):  # every pool row quantized through the library's append
+        rows = lambda t: t.permute(0, 2, 1, 3).reshape(NBq * 16, 2, 64).contiguous()
+        kvc.kv_append_fp8(rows(k16[l]), rows(v16[l]), all_slots, k8[l], v8[l], ks8[l], vs8[l])
+    qs = [torch.randn((Bq, 14, 64), generator=gen, device=device).half() for _ in range(Lq)]
+    outq = torch.empty((Bq, 14, 64), dtype=torch.float16, device=device)
+    _, _, wq = kvc.paged_decode_plan(Bq, 14, 2, 64, Cq)
+    wsq = torch.zeros(max(wq, 16), dtype=torch.uint8, device=device)
+    res_q = {}
+    kvc.kvc_set_launch_overlap(True)
+    try:
+        for name in ("fp16", "fp8"):
+            def body():
+                for l in range(Lq):
+                    if name == "fp16":
+                        kvc.paged_decode_attention(qs[l], k16[l], v16[l], tbq, ctq, 0.125, outq, wsq, Cq)
+                    else:
+                        kvc.paged_decode_attention_fp8(qs[l], k8[l], v8[l], ks8[l], vs8[l], tbq, ctq, 0.125, outq,
+                                                       wsq, Cq)
+            body()
+            torch.cuda.synchronize()
+            gq = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device)
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(gq, stream=side):
+                    body()
+            for _ in range(5):
+                gq.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(100):
+                gq.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res_q[name] = e0.elapsed_time(e1) * 1e3 / (100 * Lq)
+    finally:
+        kvc.kvc_set_launch_overlap(False)
+    del k16, v16, k8, v8
+    toks = Bq * Cq
+    b16 = toks * 2 * 2 * 64 * 2
+    b8 = toks * 2 * 2 * 64 + toks * 2 * 2 * 4
+    return {"us_per_layer_fp16": res_q["fp16"], "us_per_layer_fp8": res_q["fp8"],
+            "speedup": res_q["fp16"] / res_q["fp8"],
+            "GBps_fp16": b16 / (res_q["fp16"] * 1e-6) / 1e9, "GBps_fp8": b8 / (res_q["fp8"] * 1e-6) / 1e9,
+            "tokens_per_s_fp16": Bq / (res_q["fp16"] * Lq * 1e-6), "tokens_per_s_fp8": Bq / (res_q["fp8"] * Lq * 1e-6),
+            "bytes_per_layer_fp16": b16, "bytes_per_layer_fp8": b8}
+
+
 def config_summary(device, peak, tflops_peak):
     """Compact figures for the other listed workloads, taken after the headline measurement (one GPU): single
     sequence, shared-prefix serving mix, the 12 long-context cells, and the two prefill shapes."""
@@ -622,6 +686,12 @@ def config_summary(device, peak, tflops_peak):
                      "TFLOPs_graph": round(fl / (us_g * 1e-6) / 1e12, 2),
                      "pct_tensor_peak_graph": round(fl / (us_g * 1e-6) / 1e12 / tflops_peak * 100, 3),
                      "flops": fl}
+    q = _fp8_vs_fp16_graph(device, stream)
+    out["quantized_cache_fp8_vs_fp16_24L_B32_ctx2048"] = {
+        "us_per_layer_fp16": round(q["us_per_layer_fp16"], 3), "us_per_layer_fp8": round(q["us_per_layer_fp8"], 3),
+        "speedup": round(q["speedup"], 3), "GBps_fp8": round(q["GBps_fp8"], 1),
+        "pct_hbm_peak_fp8": round(q["GBps_fp8"] / peak * 100, 2),
+        "timing": "24-layer decode-only CUDA graphs with launch overlap, device time per layer"}
     del flush
     torch.cuda.synchronize()
     out["seconds"] = round(time.perf_counter() - t0, 1)
@@ -685,67 +755,10 @@ def run_suite_decode(device, stream, flush, emit, peak):
 
     run_suite_multi(device, stream, flush, emit, peak)
 
-    # quantized cache (NEXT-4): 24-layer decode-only graphs with launch overlap, fp16 pools vs the same pools
-    # quantized to fp8 e4m3 with per-row scales (the model step's shape: 32 x 2048, 14 / 2 heads, D = 64)
-    Lq, Bq, Cq = 24, 32, 2048
-    kp0, vp0, tbq, ctq, _, _, _ = _decode_state(Bq, Cq, 14, 2, 64, device, seed=2024)
-    NBq = kp0.shape[0]
-    gen = torch.Generator(device=device).manual_seed(99)
-    k16 = [kp0] + [torch.randn(kp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
-    v16 = [vp0] + [torch.randn(vp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
-    k8 = [torch.empty(kp0.shape, dtype=torch.uint8, device=device) for _ in range(Lq)]
-    v8 = [torch.empty(kp0.shape[:2] + (64, 16), dtype=torch.uint8, device=device) for _ in range(Lq)]  # V^T rows
-    ks8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
-    vs8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
-    all_slots = torch.arange(NBq * 16, dtype=torch.int64, device=device)
-    for l in range(Lq):  # every pool row quantized through the library's append
-        rows = lambda t: t.permute(0, 2, 1, 3).reshape(NBq * 16, 2, 64).contiguous()
-        kvc.kv_append_fp8(rows(k16[l]), rows(v16[l]), all_slots, k8[l], v8[l], ks8[l], vs8[l])
-    qs = [torch.randn((Bq, 14, 64), generator=gen, device=device).half() for _ in range(Lq)]
-    outq = torch.empty((Bq, 14, 64), dtype=torch.float16, device=device)
-    _, _, wq = kvc.paged_decode_plan(Bq, 14, 2, 64, Cq)
-    wsq = torch.zeros(max(wq, 16), dtype=torch.uint8, device=device)
-    kvc.kvc_set_launch_overlap(True)
-    try:
-        res_q = {}
-        for name in ("fp16", "fp8"):
-            def body():
-                for l in range(Lq):
-                    if name == "fp16":
-                        kvc.paged_decode_attention(qs[l], k16[l], v16[l], tbq, ctq, 0.125, outq, wsq, Cq)
-                    else:
-                        kvc.paged_decode_attention_fp8(qs[l], k8[l], v8[l], ks8[l], vs8[l], tbq, ctq, 0.125, outq,
-                                                       wsq, Cq)
-            body()
-            torch.cuda.synchronize()
-            gq = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream(device)
-            with torch.cuda.stream(side):
-                with torch.cuda.graph(gq, stream=side):
-                    body()
-            for _ in range(5):
-                gq.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(100):
-                gq.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            res_q[name] = e0.elapsed_time(e1) * 1e3 / (100 * Lq)
-    finally:
-        kvc.kvc_set_launch_overlap(False)
-    toks = Bq * Cq
-    b16 = toks * 2 * 2 * 64 * 2
-    b8 = toks * 2 * 2 * 64 + toks * 2 * 2 * 4
+    # quantized cache (NEXT-4): 24-layer decode-only graphs with launch overlap, fp16 vs fp8
+    qres = _fp8_vs_fp16_graph(device, stream)
     emit({"config": "quantized cache: 24-layer decode-only graph, 32 x 2048, 14 q / 2 KV heads, D=64, fp16 vs fp8 e4m3",
-          "us_per_layer_fp16": res_q["fp16"], "us_per_layer_fp8": res_q["fp8"],
-          "speedup": res_q["fp16"] / res_q["fp8"],
-          "GBps_fp16": b16 / (res_q["fp16"] * 1e-6) / 1e9, "GBps_fp8": b8 / (res_q["fp8"] * 1e-6) / 1e9,
-          "pct_hbm_peak_fp8": b8 / (res_q["fp8"] * 1e-6) / 1e9 / peak * 100,
-          "tokens_per_s_fp16": Bq / (res_q["fp16"] * Lq * 1e-6), "tokens_per_s_fp8": Bq / (res_q["fp8"] * Lq * 1e-6),
-          "bytes_per_layer_fp16": b16, "bytes_per_layer_fp8": b8})
-    del k16, v16, k8, v8
+          **qres, "pct_hbm_peak_fp8": qres["GBps_fp8"] / peak * 100})
     # long contexts, where streaming dominates: B=16 x 65536, one call each with L2 flushed
     for (Bl, Cl) in ((16, 65536), (4, 131072)):
         kpl, vpl, tbl, ctl, ql, _, _ = _decode_state(Bl, Cl, 14, 2, 64, device, seed=Bl + Cl)

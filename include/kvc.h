@@ -267,17 +267,19 @@ kvc_status kv_cascade_groups(const int32_t* block_table, int B, int max_blocks, 
                              int32_t* shared_blocks, int* max_shared);
 kvc_status paged_decode_cascade_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                                      int n_groups, int max_shared_blocks, size_t* workspace_bytes);
-/* Routing of cascade calls (process-wide): a call whose max_shared_blocks is
- * below `blocks` runs paged_decode_attention's kernel on the same arguments
- * (one launch, every block read per sequence) instead of the three cascade
- * launches, since reading a short shared prefix once per group saves less
- * time than the extra launches cost.  The result definition is the same
- * either way.  Default 384 blocks (6144 tokens at bs = 16), measured on
- * GB300; 0 always runs the cascade.  paged_decode_cascade_plan's workspace
- * size covers whichever route the current setting picks: change the setting
- * only between plan and call with care (re-plan after changing it).
- * KVC_ERR_INVALID for a negative count. */
-kvc_status kvc_set_cascade_min_shared_blocks(int blocks);
+/* Routing of cascade calls (process-wide).  A call saves at most
+ * (B - n_groups) * max_shared_blocks block reads per KV head against the
+ * plain decode; when that is below `blocks`, it runs paged_decode_attention's
+ * kernel on the same arguments (one launch, every block read per sequence)
+ * instead of the three cascade launches, which would cost more than they
+ * save.  The result definition is the same either way.  Default 36000,
+ * measured on GB300 (one call, L2 flushed): 8 groups x 8 sequences sharing
+ * 512 blocks (28,672 saved) ran 0.94x the plain decode, 25 x 8 sharing 256
+ * (44,800 saved) 1.13x.  0 always runs the cascade.
+ * paged_decode_cascade_plan's workspace size covers the route that the
+ * setting at plan time picks: plan again after changing it.  KVC_ERR_INVALID
+ * for a negative count. */
+kvc_status kvc_set_cascade_min_saved_blocks(int blocks);
 kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
                                           const int32_t* block_table, int max_blocks, const int32_t* context_lens,
                                           const int32_t* group_start, const int32_t* shared_blocks, int n_groups,

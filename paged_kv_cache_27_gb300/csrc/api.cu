@@ -337,7 +337,8 @@ kvc_status kv_append(kvc_handle h, int layer, const void* k_new, const void* v_n
 static kvc_status check_decode_shape(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len) {
     if (B < 0 || Hq < 1 || Hkv < 1 || max_context_len < 1) return fail(KVC_ERR_INVALID, "bad sizes");
     if (Hq % Hkv) return fail(KVC_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
-    if (Hq / Hkv > 8) return fail(KVC_ERR_UNSUPPORTED, "group size %d > 8 not supported", Hq / Hkv);
+    if (Hq / Hkv > kvc::kMaxGroupHeads)
+        return fail(KVC_ERR_UNSUPPORTED, "group size %d > %d not supported", Hq / Hkv, kvc::kMaxGroupHeads);
     if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
     if (block_size != kvc::kBlockSize) return fail(KVC_ERR_UNSUPPORTED, "block_size %d not supported", block_size);
     if (B > 65535 || Hkv > 65535) return fail(KVC_ERR_UNSUPPORTED, "B and Hkv must be <= 65535");
@@ -378,9 +379,9 @@ kvc_status kvc_set_launch_overlap(int on) {
     return KVC_OK;
 }
 
-kvc_status kvc_set_cascade_min_shared_blocks(int blocks) {
+kvc_status kvc_set_cascade_min_saved_blocks(int blocks) {
     if (blocks < 0) return fail(KVC_ERR_INVALID, "negative block count %d", blocks);
-    kvc::set_cascade_min_shared_blocks(blocks);
+    kvc::set_cascade_min_saved_blocks(blocks);
     return KVC_OK;
 }
 

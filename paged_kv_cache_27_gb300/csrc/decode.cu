@@ -61,6 +61,7 @@ struct DecodeKernelParams {
     float* part_acc;  // [B][Hq][nparts][D]
     unsigned* err;
     int max_blocks, num_blocks, B, Hq, Hkv, G, max_ctx;
+    int hchunks;  // chunks of at most 8 query heads per KV head: grid.y = Hkv * hchunks
     int bpc;     // blocks per cluster: a cluster covers context blocks [c * bpc, (c + 1) * bpc)
     int csize;   // CTAs per cluster
     // partial state of cluster c of (sequence b, query head h) goes to row (b * Hq + h) * part_stride +
@@ -141,12 +142,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     float* s_m = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes);
     // rank 0's inbox: slot c - 1 holds rank c's merged state, laid out like the state at s_m
     float* s_inbox = reinterpret_cast<float*>(smem + C::kRingBytes + C::kBarBytes + C::kStateBytes);
-    // the cluster's slice of the block table (bpc entries), after the inbox's cluster - 1 slots
-    int* s_table = reinterpret_cast<int*>(s_inbox + (p.csize - 1) * (16 + p.G * D));
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    const int kvh = blockIdx.y, b = blockIdx.z;
+    // a KV head's G query heads go in chunks of at most 8 (the mma tiles' 8 columns) to consecutive CTAs along y,
+    // which read the same K/V blocks at about the same time (the second read is mostly an L2 hit)
+    const int kvh = blockIdx.y / p.hchunks, hc = blockIdx.y - kvh * p.hchunks, b = blockIdx.z;
+    const int Gc = min(8, p.G - hc * 8);  // query heads of this CTA
+    const int h0 = kvh * p.G + hc * 8;    // its first query head
+    // the cluster's slice of the block table (bpc entries), after the inbox's cluster - 1 slots
+    int* s_table = reinterpret_cast<int*>(s_inbox + (p.csize - 1) * (16 + Gc * D));
     const int cs = p.csize;
     const int cidx = blockIdx.x / cs;                                    // this CTA's cluster along the context
     const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;   // == blockIdx.x % cs
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // rank 0's inbox barrier: completes when the other CTAs' merged states have arrived (asynchronous pushes)
     uint64_t* inbox_bar = bars + NW * ST;
     // bytes one CTA pushes into an inbox slot: acc[G][D], and m and l of its G heads
-    const uint32_t push_bytes = static_cast<uint32_t>(p.G * D * 4 + p.G * 8);
+    const uint32_t push_bytes = static_cast<uint32_t>(Gc * D * 4 + Gc * 8);
     if (lane == 0) {
         for (int s = 0; s < ST; ++s) mbar_init(&wbars[s], 1);
         if (KVC_DEC_ASYNC_PUSH && warp == 0 && cs > 1) mbar_init(inbox_bar, 1);
@@ -205,8 +209,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         // with forced partials the combine kernel checks the same and writes the zeros
         if (blockIdx.x == 0 && !kSuffix) {
             if (threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-            for (int e = threadIdx.x; e < p.G * D; e += blockDim.x)
-                store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + kvh * p.G + e / D) * D + e % D, 0.f);
+            for (int e = threadIdx.x; e < Gc * D; e += blockDim.x)
+                store_out(p.out, p.out_f32, (static_cast<int64_t>(b) * p.Hq + h0 + e / D) * D + e % D, 0.f);
         }
         return;
     }
@@ -279,8 +283,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // query fragments (A operand, rows = the G heads of this KV head; rows >= G are zero)
     uint32_t qa[D / 16][2];
     {
-        const bool row_ok = g < p.G;
-        const __half* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.G + (row_ok ? g : 0)) * D;
+        const bool row_ok = g < Gc;
+        const __half* qrow = p.q + (static_cast<int64_t>(b) * p.Hq + h0 + (row_ok ? g : 0)) * D;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             // fp8: k indices 2t, 2t+1 / 2t+8, 2t+9 of the group are dims 4t, 4t+1 / 4t+2, 4t+3 (see above)
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                             __half* dst = (lane >= 16 ? p.v_cache : p.k_cache) +
                                           ((static_cast<int64_t>(phys) * p.Hkv + kvh) * kBlockSize + app_row) * D +
                                           c * 8;
-                            *reinterpret_cast<uint4*>(dst) = app_val;
+                            if (hc == 0) *reinterpret_cast<uint4*>(dst) = app_val;  // one head chunk writes
                         }
                         __syncwarp();
                     }
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
 
     const bool final_here = nclus == 1 && !kSuffix;  // this cluster's result is the output
     const bool direct = final_here && cs == 1;                  // a single CTA holds the whole range
-    const int stride = 16 + p.G * D;  // floats per cluster merge slot: m[8], l[8], acc[G][D]
+    const int stride = 16 + Gc * D;  // floats per cluster merge slot: m[8], l[8], acc[Gc][D]
     // in a cluster this CTA's merged state goes to its slot in rank 0: rank 0's own state at s_m, or
     // inbox slot rank - 1 (same layout)
     uint32_t slot = 0, remote_bar = 0;
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     {
         constexpr int kRingF = C::kWarpRingBytes / 4;
         const float* wst = reinterpret_cast<const float*>(smem);  // warp w's parked state at w * kRingF
-        for (int e = 4 * threadIdx.x; e < p.G * D; e += 4 * C::kThreads) {
+        for (int e = 4 * threadIdx.x; e < Gc * D; e += 4 * C::kThreads) {
             const int gg = e / D, d = e % D;
             float M = -INFINITY;
 #pragma unroll
@@ -610,7 +614,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                 L += r[8 + gg] * wgt;
                 O = fma4(wgt, *reinterpret_cast<const float4*>(r + 16 + gg * C::kMergeStride + d), O);
             }
-            const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
+            const int64_t h = static_cast<int64_t>(b) * p.Hq + h0 + gg;
             if (direct) {
                 store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
             } else if (cs == 1) {  // one CTA per cluster: its state is the cluster's partial
@@ -673,7 +677,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // slot c of the merge: c == 0 is this CTA's own state, c >= 1 the inbox slot of rank c; a CTA without
     // blocks has l = 0 and takes no part
     auto src = [&](int c) -> const float* { return c == 0 ? s_m : s_inbox + (c - 1) * stride; };
-    for (int e = 4 * threadIdx.x; e < p.G * D; e += 4 * C::kThreads) {
+    for (int e = 4 * threadIdx.x; e < Gc * D; e += 4 * C::kThreads) {
         const int gg = e / D, d = e % D;
         float M = -INFINITY;
         for (int c = 0; c < cs; ++c)
@@ -687,7 +691,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
             L += l * w;
             O = fma4(w, *reinterpret_cast<const float4*>(r + 16 + e), O);
         }
-        const int64_t h = static_cast<int64_t>(b) * p.Hq + kvh * p.G + gg;
+        const int64_t h = static_cast<int64_t>(b) * p.Hq + h0 + gg;
         if (final_here) {
             store_out4(p.out, p.out_f32, h * D + d, scale4(O, L > 0.f ? 1.f / L : 0.f));
         } else {
@@ -827,40 +831,98 @@ static cudaError_t decode_occupancy(int smem, int* ctas) {
     return cudaSuccess;
 }
 
+// thread-block clusters of cs CTAs (smem bytes of dynamic shared memory each) that can be resident at once: the
+// clusters of one launch are placed within a GPC each, so this is below SMs x CTAs-per-SM / cs for larger clusters
+// (cached per (cs, smem))
+template <int D>
+static cudaError_t decode_resident_clusters(int cs, int smem, int* clusters) {
+    using C = DecodeCfg<D>;
+    static std::mutex mu;
+    static int cached_key[256] = {0}, cached_val[256] = {0};
+    cudaError_t e = decode_setup<D>();
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int key = ((dev * 32 + cs) << 20) + smem + 1;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < 256; ++i)
+        if (cached_key[i] == key) {
+            *clusters = cached_val[i];
+            return cudaSuccess;
+        }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(cs);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, paged_decode_kernel<D, false>, &cfg);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < 256; ++i)
+        if (cached_key[i] == 0) {
+            cached_key[i] = key;
+            cached_val[i] = n;
+            break;
+        }
+    *clusters = n;
+    return cudaSuccess;
+}
+
 template <int D>
 static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, DecodePlan* plan) {
     using C = DecodeCfg<D>;
     const int nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
-    const int G = std::max(1, Hq / std::max(Hkv, 1));
-    int cs, bpc;
+    const int Gfull = std::max(1, Hq / std::max(Hkv, 1));
+    const int G = std::min(Gfull, 8);            // query heads of one CTA
+    const int hchunks = (Gfull + 7) / 8;          // CTAs per (sequence, KV head) along the heads
+    int cs = 1, bpc = nblk;
     if (bpc_req > 0) {
         bpc = std::min(bpc_req, kMaxClusterBlocks);
         cs = std::max(1, std::min(kMaxCluster, (bpc + C::kWarps - 1) / C::kWarps));
     } else {
-        const int sms = sm_count();
-        if (sms <= 0) return cudaErrorNoDevice;
-        // one wave of KVC_DEC_PLAN_CTAS CTAs per SM for all (sequence, KV head) pairs, at least one block per
-        // warp; recomputed once if the chosen cluster's inbox lowers the occupancy below that
+        // One wave: for each cluster size, the clusters that can be resident (KVC_DEC_PLAN_CTAS of the CTAs an SM
+        // holds, the rest left for the next launch) are shared out over the (sequence, KV head) pairs, at most
+        // one cluster per cs x warps blocks.  The size that keeps the most CTAs busy wins; among equals, fewer
+        // clusters per context (less merging), then the larger cluster.  Where not even one CTA per pair fits in a
+        // wave, each pair gets one CTA (several waves).
+        const int smem_est = C::smem_bytes(kMaxCluster, G, std::min(nblk, kMaxClusterBlocks));
         int occ = 0;
-        cudaError_t e = decode_occupancy<D>(C::smem_bytes(1, G, std::min(nblk, kMaxClusterBlocks)), &occ);
+        cudaError_t e = decode_occupancy<D>(smem_est, &occ);
         if (e != cudaSuccess) return e;
-        const int64_t segs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv);
-        for (int pass = 0; pass < 2; ++pass) {
-            const int64_t slots = static_cast<int64_t>(sms) * std::min(occ, KVC_DEC_PLAN_CTAS);
-            const int64_t per_seg = std::max<int64_t>(1, slots / segs);
-            cs = static_cast<int>(std::max<int64_t>(
-                1, std::min<int64_t>({kMaxCluster, per_seg, (nblk + C::kWarps - 1) / C::kWarps})));
-            int64_t ncl = std::max<int64_t>(
-                1, std::min<int64_t>(per_seg / cs, (nblk + static_cast<int64_t>(cs) * C::kWarps - 1) /
-                                                       (static_cast<int64_t>(cs) * C::kWarps)));
-            ncl = std::max<int64_t>(ncl, (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks);
-            bpc = static_cast<int>((nblk + ncl - 1) / ncl);
-            int occ2 = 0;
-            e = decode_occupancy<D>(C::smem_bytes(cs, G, bpc), &occ2);
+        const int64_t segs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv * hchunks);
+        const int64_t min_ncl = (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks;
+        int64_t best_ctas = 0, best_ncl = 0, best_score = 0;
+        for (int c = 1; c <= kMaxCluster; ++c) {
+            if (c > 1 && (static_cast<int64_t>(c - 1) * C::kWarps >= nblk)) break;  // a CTA would have no block
+            int resident = 0;
+            e = decode_resident_clusters<D>(c, C::smem_bytes(c, G, std::min(nblk, kMaxClusterBlocks)), &resident);
             if (e != cudaSuccess) return e;
-            if (occ2 >= std::min(occ, KVC_DEC_PLAN_CTAS)) break;
-            occ = occ2;
+            const int64_t usable = static_cast<int64_t>(resident) * std::min(occ, KVC_DEC_PLAN_CTAS) / occ;
+            const int64_t per_seg = usable / segs;
+            if (per_seg < 1) continue;
+            const int64_t want = (nblk + static_cast<int64_t>(c) * C::kWarps - 1) / (static_cast<int64_t>(c) * C::kWarps);
+            const int64_t ncl = std::max(min_ncl, std::min(per_seg, want));
+            const int64_t ctas = segs * ncl * c;
+            // weight: busy CTAs, discounted per cluster along a context and for needing the combine launch
+            const int64_t score = ctas * 1000 * (1000 - (ncl > 1 ? KVC_DEC_COMBINE_PENALTY : 0)) /
+                                  (1000 + KVC_DEC_PART_PENALTY * ncl);
+            if (score > best_score || (score == best_score && ncl <= best_ncl)) {
+                best_score = score;
+                best_ctas = ctas;
+                best_ncl = ncl;
+                cs = c;
+            }
         }
+        const int64_t ncl = best_ctas > 0 ? best_ncl : min_ncl;
+        if (best_ctas == 0) cs = 1;
+        bpc = static_cast<int>((nblk + ncl - 1) / ncl);
     }
     const int nparts = (nblk + bpc - 1) / bpc;
     plan->blocks_per_split = bpc;
@@ -900,6 +962,7 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.G = a.Hq / a.Hkv;
+    p.hchunks = (p.G + 7) / 8;
     p.max_ctx = a.max_context_len;
     p.bpc = plan.blocks_per_split;
     p.csize = plan.cluster;
@@ -934,15 +997,15 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     float* part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
     const DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
-    dim3 grid(plan.num_splits, a.Hkv, a.B);
+    dim3 grid(plan.num_splits, a.Hkv * p.hchunks, a.B);
     if (fp8)
         e = launch(paged_decode_kernel<D, false, true>, grid, dim3(DecodeCfg<D, true>::kThreads),
-                   DecodeCfg<D, true>::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream, pdl,
+                   DecodeCfg<D, true>::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split), stream, pdl,
                    static_cast<unsigned>(plan.cluster),
                    tmK, tmV, p);
     else
         e = launch(paged_decode_kernel<D, false>, grid, dim3(C::kThreads),
-                   C::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream,
+                   C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split), stream,
                    pdl, static_cast<unsigned>(plan.cluster), tmK, tmV, p);
     if (e != cudaSuccess) return e;
     if (plan.num_parts > 1) {
@@ -1005,8 +1068,8 @@ static cudaError_t launch_suffix_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.part_base = part_base;
     p.part_stride = part_stride;
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
-    return launch(paged_decode_kernel<D, true>, dim3(plan.num_splits, a.Hkv, a.B), dim3(C::kThreads),
-                  C::smem_bytes(plan.cluster, p.G, plan.blocks_per_split), stream, pdl,
+    return launch(paged_decode_kernel<D, true>, dim3(plan.num_splits, a.Hkv * p.hchunks, a.B), dim3(C::kThreads),
+                  C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split), stream, pdl,
                   static_cast<unsigned>(plan.cluster), tmK, tmV, p);
 }
 
@@ -1082,7 +1145,6 @@ extern "C" kvc_status paged_decode_attention_static_workspace(
     if (B < 0 || Hq < 1 || Hkv < 1 || max_context_len < 1 || num_blocks < 1 || max_blocks < 1 || blocks_per_split < 0)
         return fail(KVC_ERR_INVALID, "bad sizes");
     if (Hq % Hkv) return fail(KVC_ERR_INVALID, "Hq must be a multiple of Hkv");
-    if (Hq / Hkv > 8) return fail(KVC_ERR_UNSUPPORTED, "group size > 8 not supported");
     if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (block_size != kvc::kBlockSize) return fail(KVC_ERR_UNSUPPORTED, "block_size must be 16");
     if (B > 65535 || Hkv > 65535) return fail(KVC_ERR_UNSUPPORTED, "B and Hkv must be <= 65535");

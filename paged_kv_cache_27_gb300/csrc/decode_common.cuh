@@ -57,6 +57,17 @@ namespace kvc {
 #ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
 #define KVC_DEC_PLAN_CTAS 2
 #endif
+// Split planner weights, per mille of a plan's busy CTAs: a discount per cluster along a context (each adds a
+// partial state to merge), and one for needing the separate combine launch at all (more than one cluster).
+// Measured on one call with L2 flushed: B = 1 x 131072 ran 26.9 us with 76 two-CTA clusters per context and
+// 23.6 us with 18 eight-CTA clusters; B = 16 x 16384 32.5 us with one eight-CTA cluster per context against
+// 33.6-34.0 us with 3 three-CTA or 9 one-CTA clusters and the combine kernel.
+#ifndef KVC_DEC_PART_PENALTY
+#define KVC_DEC_PART_PENALTY 10
+#endif
+#ifndef KVC_DEC_COMBINE_PENALTY
+#define KVC_DEC_COMBINE_PENALTY 150
+#endif
 // 1: the CTAs of a cluster hand their merged states to rank 0 with st.async, whose bytes complete on an mbarrier
 // in rank 0 (senders leave at once); 0: remote stores, then a cluster barrier (release / acquire)
 #ifndef KVC_DEC_ASYNC_PUSH

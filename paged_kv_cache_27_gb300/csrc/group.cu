@@ -46,14 +46,15 @@ namespace kvc {
 #ifndef KVC_MULTI_CTAS  // CTAs per SM the chunking aims for (one where a CTA needs the SM's registers)
 #define KVC_MULTI_CTAS 2
 #endif
-// A cascade call whose shared prefixes are shorter than this many blocks runs the plain decode instead: reading a
-// short prefix once per group saves less than the two extra launches cost (measured on the shared-prefix serving
-// mix and on longer shared prefixes)
-#ifndef KVC_CASCADE_MIN_SHARED_BLOCKS
-#define KVC_CASCADE_MIN_SHARED_BLOCKS 384
+// A cascade call runs the cascade kernels only when the block reads it saves per KV head, at most
+// (B - n_groups) x max_shared_blocks, reach this many; otherwise the plain decode (one launch) is faster.  Measured
+// on GB300 (one call, L2 flushed; groups x members x shared blocks, 1..200 private tokens each): 8 x 8 x 512
+// (28,672 saved) 0.94x, 25 x 8 x 128 (22,400) 0.89x, 8 x 8 x 768 (43,008) 1.11x, 25 x 8 x 256 (44,800) 1.13x.
+#ifndef KVC_CASCADE_MIN_SAVED_BLOCKS
+#define KVC_CASCADE_MIN_SAVED_BLOCKS 36000
 #endif
-static std::atomic<int> g_cascade_min_shared{KVC_CASCADE_MIN_SHARED_BLOCKS};
-void set_cascade_min_shared_blocks(int blocks) { g_cascade_min_shared.store(blocks); }
+static std::atomic<int> g_cascade_min_saved{KVC_CASCADE_MIN_SAVED_BLOCKS};
+void set_cascade_min_saved_blocks(int blocks) { g_cascade_min_saved.store(blocks); }
 #ifndef KVC_PREFIX_TC_MIN_ROWS  // cascade prefix, head dim 64: groups of this many query rows run on the tensor cores
 #define KVC_PREFIX_TC_MIN_ROWS 17
 #endif
@@ -334,28 +335,36 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
                 const float x2 = k0 + g + 8 <= lastk[nt][0] ? sc[nt][2] * sl2 : -INFINITY;
                 const float x3 = k0 + g + 8 <= lastk[nt][1] ? sc[nt][3] * sl2 : -INFINITY;
                 float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                // lazy running maxima (as in the decode kernel): they move only when a visible score exceeds them
+                // by more than 2^KVC_DEC_LAZY_MAX, so the weights stay <= 2^KVC_DEC_LAZY_MAX
+                if (KVC_DEC_LAZY_MAX == 0 || __any_sync(0xffffffffu, mx0 > m_run[nt][0] + KVC_DEC_LAZY_MAX ||
+                                                                      mx1 > m_run[nt][1] + KVC_DEC_LAZY_MAX)) {
 #pragma unroll
-                for (int sh = 4; sh < 32; sh <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+                    for (int sh = 4; sh < 32; sh <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+                    }
+                    const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+                    // a row with no visible key so far (m stays -inf) keeps a zero state
+                    const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[nt][0] - mn0);
+                    const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[nt][1] - mn1);
+                    m_run[nt][0] = mn0;
+                    m_run[nt][1] = mn1;
+                    l_run[nt][0] *= al0;
+                    l_run[nt][1] *= al1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[nt][mt][0] *= al0;
+                        o[nt][mt][1] *= al1;
+                        o[nt][mt][2] *= al0;
+                        o[nt][mt][3] *= al1;
+                    }
                 }
-                const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-                // a row with no visible key so far (m stays -inf) keeps a zero state
-                const float al0 = mn0 == -INFINITY ? 1.f : ex2(m_run[nt][0] - mn0);
-                const float al1 = mn1 == -INFINITY ? 1.f : ex2(m_run[nt][1] - mn1);
-                m_run[nt][0] = mn0;
-                m_run[nt][1] = mn1;
+                const float mn0 = m_run[nt][0], mn1 = m_run[nt][1];
                 const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0), p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
                 const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1), p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
-                l_run[nt][0] = l_run[nt][0] * al0 + p0 + p2;
-                l_run[nt][1] = l_run[nt][1] * al1 + p1 + p3;
-#pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    o[nt][mt][0] *= al0;
-                    o[nt][mt][1] *= al1;
-                    o[nt][mt][2] *= al0;
-                    o[nt][mt][3] *= al1;
-                }
+                l_run[nt][0] += p0 + p2;
+                l_run[nt][1] += p1 + p3;
                 // P^T as the B operand: fp16 high part and fp16 residual
                 const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
                 const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
@@ -609,7 +618,8 @@ static GroupKernelParams group_params(const DecodeArgs& a, float* part_ml, float
 }
 
 // the cascade prefix on the tensor cores (group_tc.cu): head dim 64, groups of up to `rows` query rows
-static bool use_tc_prefix(int D, int rows) { return D == gtc::D && rows >= KVC_PREFIX_TC_MIN_ROWS; }
+// the tensor-core prefix kernel takes at most 64 query rows (a group's sequences x its G heads)
+static bool use_tc_prefix(int D, int rows) { return D == gtc::D && rows >= KVC_PREFIX_TC_MIN_ROWS && rows <= 64; }
 
 // chunking for the tensor-core prefix pass: one CTA per SM over all (group, KV head) pairs, whole 128-key tiles
 static void tc_chunks(int64_t units, int64_t nblk, int sms, int* chunk, int* nchunks) {
@@ -740,7 +750,8 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_ctx, int n_group
     }
     if (max_shared_blocks <= 0) plan->nchunks = 0;
     plan->part_stride = plan->nchunks + plan->suffix.num_parts;
-    plan->plain = max_shared_blocks < g_cascade_min_shared.load(std::memory_order_relaxed);
+    const int64_t saved = static_cast<int64_t>(std::max(B - n_groups, 0)) * std::max(max_shared_blocks, 0);
+    plan->plain = saved < g_cascade_min_saved.load(std::memory_order_relaxed);
     // the plain decode over the full contexts is the suffix plan without block offsets: its workspace
     // (plan->suffix.workspace_bytes) never exceeds the cascade's, so one size serves both routes
     plan->workspace_bytes = plan->plain ? plan->suffix.workspace_bytes

@@ -9,6 +9,8 @@
 namespace kvc {
 
 constexpr int kBlockSize = 16;  // tokens per block (the page size used throughout the pages)
+// query heads per KV head the decode paths take (the decode kernel in chunks of 8 heads per CTA)
+constexpr int kMaxGroupHeads = 64;
 
 // Device address of the sticky error word of the current device.
 cudaError_t device_error_word(unsigned** ptr);
@@ -99,8 +101,8 @@ struct CascadePlan {
 };
 cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int n_groups, int max_shared_blocks,
                          CascadePlan* plan);
-// process-wide: cascade calls with max_shared_blocks below this run the plain decode
-void set_cascade_min_shared_blocks(int blocks);
+// process-wide: cascade calls saving fewer block reads per KV head than this run the plain decode
+void set_cascade_min_saved_blocks(int blocks);
 // group_start: device [n_groups + 1]; shared_blocks: device [B], the shared blocks of each sequence's group
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);

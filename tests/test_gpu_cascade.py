@@ -10,16 +10,16 @@ from parity import check_attention
 
 pytestmark = pytest.mark.gpu
 
-DEFAULT_MIN_SHARED = 384  # the library's default routing threshold (blocks)
+DEFAULT_MIN_SAVED = 36000  # the library's default routing threshold (saved block reads)
 
 
 @pytest.fixture(autouse=True)
 def always_cascade():
     """These tests exercise the cascade kernels themselves: route every call to them, whatever its prefix."""
     import paged_kv_cache_27_gb300 as kvc
-    kvc.kvc_set_cascade_min_shared_blocks(0)
+    kvc.kvc_set_cascade_min_saved_blocks(0)
     yield
-    kvc.kvc_set_cascade_min_shared_blocks(DEFAULT_MIN_SHARED)
+    kvc.kvc_set_cascade_min_saved_blocks(DEFAULT_MIN_SAVED)
 
 
 def run_cascade(wl, out_dtype=torch.float32, checked=False, group_start=None, shared=None, max_shared=None):
@@ -64,6 +64,7 @@ CASES = [
     ([4, 4], [10, 2], None, 8, 8, 128),
     ([8], [300], [1, 2, 3, 50, 100, 16, 17, 8], 14, 2, 64),
     ([5, 1, 7], [64, 12, 1], None, 16, 2, 128),
+    ([8, 3], [24, 9], None, 64, 4, 64),  # 16 query heads per KV head: 128 prefix rows, the mma.sync prefix
 ]
 
 
@@ -167,20 +168,25 @@ def test_cascade_full_group_rows_and_scale_sign(scale_sign):
     assert (out - pout).abs().max().item() < 1e-4
 
 
-def test_short_prefix_routes_to_plain_decode():
-    """With the default routing, a cascade call whose shared prefixes are short runs the plain decode kernel: its
-    output is bit-identical to paged_decode_attention's; forced onto the cascade kernels it agrees within the
-    tolerance.  Both are checked against the oracle."""
+def test_routing_by_saved_block_reads():
+    """A cascade call saves at most (B - n_groups) * max_shared_blocks block reads per KV head.  Below the routing
+    threshold it runs the plain decode kernel (output bit-identical to paged_decode_attention's); at the threshold
+    it runs the cascade kernels (agreeing within the tolerance, in another summation order).  Both are checked
+    against the oracle; the default threshold sends this small case to the plain decode."""
     import paged_kv_cache_27_gb300 as kvc
     wl = workloads.cascade_decode(71, [8, 8], [32, 20], list(np.random.default_rng(3).integers(1, 300, size=16)))
-    kvc.kvc_set_cascade_min_shared_blocks(DEFAULT_MIN_SHARED)
-    out, pout = run_cascade(wl)
-    assert torch.equal(out, pout)
-    kvc.kvc_set_cascade_min_shared_blocks(0)
-    out_c, _ = run_cascade(wl)
+    saved = (16 - 2) * 32
     ref = oracle_out(wl)
-    check_attention(out, ref, "routed to the plain decode")
-    check_attention(out_c, ref, "forced cascade")
-    assert not torch.equal(out_c, pout)  # a different summation order: the cascade kernels really ran
+    kvc.kvc_set_cascade_min_saved_blocks(DEFAULT_MIN_SAVED)
+    out_default, pout = run_cascade(wl)
+    assert torch.equal(out_default, pout)
+    kvc.kvc_set_cascade_min_saved_blocks(saved + 1)
+    out_plain, pout = run_cascade(wl)
+    assert torch.equal(out_plain, pout)
+    kvc.kvc_set_cascade_min_saved_blocks(saved)
+    out_c, pout = run_cascade(wl)
+    assert not torch.equal(out_c, pout)  # a different summation order: the cascade kernels ran
+    check_attention(out_plain, ref, "routed to the plain decode")
+    check_attention(out_c, ref, "cascade kernels")
     with pytest.raises(kvc.KvcError):
-        kvc.kvc_set_cascade_min_shared_blocks(-1)
+        kvc.kvc_set_cascade_min_saved_blocks(-1)

@@ -82,6 +82,27 @@ def test_small_sweep(kvc, B, Hq, Hkv, D, ctx, fused):
         check_workload(kvc, wl, dt, fused=fused)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,ctx", [
+    (3, 64, 4, 64, [1, 500, 3000]),       # 16 query heads per KV head: two chunks of 8
+    (2, 12, 1, 128, [17, 2049]),          # 12: a full chunk and a chunk of 4
+    (2, 32, 1, 64, [300, 40000]),         # 32: four chunks, a context over several clusters
+    (1, 64, 1, 64, [1024]),               # 64: the widest group the library takes
+])
+@pytest.mark.parametrize("fused", [False, True])
+def test_wide_query_groups(kvc, B, Hq, Hkv, D, ctx, fused):
+    """More than 8 query heads per KV head (the grouped-query paragraph of the neuralialabs.com page and the
+    xformers article's part 5 fix no bound): the heads go in chunks of 8 to consecutive CTAs."""
+    wl = workloads.small_decode(B * 1000 + Hq, B=B, Hq=Hq, Hkv=Hkv, D=D, ctx=ctx, L=1)
+    for dt in (torch.float32, torch.float16):
+        check_workload(kvc, wl, dt, fused=fused)
+
+
+def test_group_size_limit(kvc):
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.paged_decode_plan(1, 65, 1, 64, 16)
+    assert e.value.name == "KVC_ERR_UNSUPPORTED"
+
+
 @pytest.mark.parametrize("bps", [1, 2, 3, 4, 7, 8, 64, 128])
 @pytest.mark.parametrize("fused", [False, True])
 def test_forced_split_sizes(kvc, bps, fused):

@@ -87,11 +87,11 @@ def test_argument_errors(kvc):
         kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
                                    s.out[0], small_ws, s.max_ctx, blocks_per_split=1)
     assert e.value.name == "KVC_ERR_INVALID"
-    q9 = torch.zeros((2, 18, 64), dtype=torch.float16, device="cuda")
+    q65 = torch.zeros((2, 130, 64), dtype=torch.float16, device="cuda")
     with pytest.raises(kvc.KvcError) as e:
-        kvc.paged_decode_attention(q9, s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
-                                   torch.empty_like(q9, dtype=torch.float32), s.workspace, s.max_ctx)
-    assert e.value.name == "KVC_ERR_UNSUPPORTED"  # group of 9 query heads per KV head
+        kvc.paged_decode_attention(q65, s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
+                                   torch.empty_like(q65, dtype=torch.float32), s.workspace, s.max_ctx)
+    assert e.value.name == "KVC_ERR_UNSUPPORTED"  # group of 65 query heads per KV head: beyond the 64 taken
     with pytest.raises(kvc.KvcError) as e:
         kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, s.context_lens, wl.scale,
                                    s.out[0], s.workspace, 10 ** 6)

@@ -98,6 +98,7 @@ CASES = [
     (5, [300, 1025, 2048], 14, 2, 64, 3),
     (6, [40000, 5000, 1], 14, 2, 64, 0),
     (7, [129, 2000], 16, 2, 128, 2),
+    (8, [3, 900, 5000], 48, 2, 64, 0),  # 24 query heads per KV head: three chunks of 8
 ]
 
 

@@ -58,6 +58,9 @@ CASES = [
     (8, [8, 100, 2049], 8, 16, 2, 64),
     (9, [2, 31, 32, 33, 9000], 2, 16, 4, 128),
     (10, [6, 64, 65, 3000], 6, 12, 4, 128),
+    # wider query groups than 8 heads per KV head
+    (11, [3, 40, 5000], 3, 32, 2, 64),
+    (12, [1, 700], 1, 16, 1, 64),
 ]
 
 

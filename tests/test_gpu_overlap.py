@@ -63,9 +63,9 @@ def test_multi_token_chain_in_graph(T, ctx):
 @pytest.fixture
 def always_cascade():
     import paged_kv_cache_27_gb300 as kvc
-    kvc.kvc_set_cascade_min_shared_blocks(0)  # the cascade kernels, whatever the prefix length
+    kvc.kvc_set_cascade_min_saved_blocks(0)  # the cascade kernels, whatever the prefix length
     yield
-    kvc.kvc_set_cascade_min_shared_blocks(384)
+    kvc.kvc_set_cascade_min_saved_blocks(36000)
 
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(64, 14, 2), (128, 8, 8)])
