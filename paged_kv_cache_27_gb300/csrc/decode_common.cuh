@@ -73,6 +73,11 @@ namespace kvc {
 #ifndef KVC_DEC_ASYNC_PUSH
 #define KVC_DEC_ASYNC_PUSH 1
 #endif
+// 1: the decode kernel waits for its cluster's prologue phase right after its dependency wait; 0: just before
+// its first push into rank 0's inbox
+#ifndef KVC_DEC_EARLY_CLUSTER_WAIT
+#define KVC_DEC_EARLY_CLUSTER_WAIT 1
+#endif
 // Lazy running maximum in the decode kernel's online softmax: a block's scores are weighted against the running
 // maximum m as they are, 2^(x - m) <= 2^KVC_DEC_LAZY_MAX, unless one of them exceeds m by more than that; only
 // then is the block's maximum reduced across the lanes and the state rescaled.  0: every block moves the maximum.

@@ -231,6 +231,9 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
     if (cs > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     grid_dependency_wait();  // q and out may belong to the previous kernel
     if (n == 0) grid_dependents_launch();  // a CTA without blocks; the others release at their first refill
+    // every CTA of the cluster has passed its prologue (rank 0's inbox barrier is initialised): the pushes after
+    // the block loop need no further check (the decode kernel measured this wait at the end of a launch)
+    if (KVC_DEC_EARLY_CLUSTER_WAIT && cs > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
     // query fragments (B operand of S^T = K Q^T): column g of tile nt is row r0 + 8 nt + g (zero past R)
     uint32_t qa[NT][D / 16][2];
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
     // every CTA of the cluster has started (the arrive after the prologue), so rank 0's shared memory is live
     uint32_t slot = 0, remote_bar = 0;
     if (cs > 1) {
-        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        if (!KVC_DEC_EARLY_CLUSTER_WAIT) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
         slot = map_to_rank(s_inbox + rank * C::kSlotFloats, 0);
         remote_bar = map_to_rank(inbox_bar, 0);
     }
