@@ -597,14 +597,12 @@ def _fp8_vs_fp16_graph(device, stream, Lq=24, Bq=32, Cq=2048):
     gen = torch.Generator(device=device).manual_seed(99)
     k16 = [kp0] + [torch.randn(kp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
     v16 = [vp0] + [torch.randn(vp0.shape, generator=gen, device=device).half() for _ in range(Lq - 1)]
-    k8 = [torch.empty(kp0.shape, dtype=torch.uint8, device=device) for _ in range(Lq)]
-    v8 = [torch.empty(kp0.shape[:2] + (64, 16), dtype=torch.uint8, device=device) for _ in range(Lq)]  # V^T rows
-    ks8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
-    vs8 = [torch.empty(kp0.shape[:3], dtype=torch.float32, device=device) for _ in range(Lq)]
+    rec_bytes = kvc.kv_fp8_record_bytes(64)
+    r8 = [torch.empty((NBq, 2, rec_bytes), dtype=torch.uint8, device=device) for _ in range(Lq)]
     all_slots = torch.arange(NBq * 16, dtype=torch.int64, device=device)
     for l in range(Lq):  # every pool row quantized through the library's append
         rows = lambda t: t.permute(0, 2, 1, 3).reshape(NBq * 16, 2, 64).contiguous()
-        kvc.kv_append_fp8(rows(k16[l]), rows(v16[l]), all_slots, k8[l], v8[l], ks8[l], vs8[l])
+        kvc.kv_append_fp8(rows(k16[l]), rows(v16[l]), all_slots, r8[l])
     qs = [torch.randn((Bq, 14, 64), generator=gen, device=device).half() for _ in range(Lq)]
     outq = torch.empty((Bq, 14, 64), dtype=torch.float16, device=device)
     _, _, wq = kvc.paged_decode_plan(Bq, 14, 2, 64, Cq)
@@ -618,8 +616,7 @@ def _fp8_vs_fp16_graph(device, stream, Lq=24, Bq=32, Cq=2048):
                     if name == "fp16":
                         kvc.paged_decode_attention(qs[l], k16[l], v16[l], tbq, ctq, 0.125, outq, wsq, Cq)
                     else:
-                        kvc.paged_decode_attention_fp8(qs[l], k8[l], v8[l], ks8[l], vs8[l], tbq, ctq, 0.125, outq,
-                                                       wsq, Cq)
+                        kvc.paged_decode_attention_fp8(qs[l], r8[l], tbq, ctq, 0.125, outq, wsq, Cq)
             body()
             torch.cuda.synchronize()
             gq = torch.cuda.CUDAGraph()
@@ -639,7 +636,7 @@ def _fp8_vs_fp16_graph(device, stream, Lq=24, Bq=32, Cq=2048):
             res_q[name] = e0.elapsed_time(e1) * 1e3 / (100 * Lq)
     finally:
         kvc.kvc_set_launch_overlap(False)
-    del k16, v16, k8, v8
+    del k16, v16, r8
     toks = Bq * Cq
     b16 = toks * 2 * 2 * 64 * 2
     b8 = toks * 2 * 2 * 64 + toks * 2 * 2 * 4
@@ -763,26 +760,22 @@ def run_suite_decode(device, stream, flush, emit, peak):
     for (Bl, Cl) in ((16, 65536), (4, 131072)):
         kpl, vpl, tbl, ctl, ql, _, _ = _decode_state(Bl, Cl, 14, 2, 64, device, seed=Bl + Cl)
         NBl = kpl.shape[0]
-        k8l = torch.empty(kpl.shape, dtype=torch.uint8, device=device)
-        v8l = torch.empty(kpl.shape[:2] + (64, 16), dtype=torch.uint8, device=device)
-        ks8l = torch.empty(kpl.shape[:3], dtype=torch.float32, device=device)
-        vs8l = torch.empty(kpl.shape[:3], dtype=torch.float32, device=device)
+        r8l = torch.empty((NBl, 2, kvc.kv_fp8_record_bytes(64)), dtype=torch.uint8, device=device)
         rows = lambda t: t.permute(0, 2, 1, 3).reshape(NBl * 16, 2, 64).contiguous()
-        kvc.kv_append_fp8(rows(kpl), rows(vpl), torch.arange(NBl * 16, dtype=torch.int64, device=device), k8l, v8l,
-                          ks8l, vs8l)
+        kvc.kv_append_fp8(rows(kpl), rows(vpl), torch.arange(NBl * 16, dtype=torch.int64, device=device), r8l)
         ol = torch.empty((Bl, 14, 64), dtype=torch.float16, device=device)
         _, _, wl_ = kvc.paged_decode_plan(Bl, 14, 2, 64, Cl)
         wsl = torch.zeros(max(wl_, 16), dtype=torch.uint8, device=device)
         us16 = _timed_calls(lambda: kvc.paged_decode_attention(ql, kpl, vpl, tbl, ctl, 0.125, ol, wsl, Cl), 20, flush,
                             stream)
-        us8 = _timed_calls(lambda: kvc.paged_decode_attention_fp8(ql, k8l, v8l, ks8l, vs8l, tbl, ctl, 0.125, ol, wsl,
+        us8 = _timed_calls(lambda: kvc.paged_decode_attention_fp8(ql, r8l, tbl, ctl, 0.125, ol, wsl,
                                                                    Cl), 20, flush, stream)
         tl = Bl * Cl
         b16l, b8l = tl * 2 * 2 * 64 * 2, tl * 2 * 2 * 64 + tl * 2 * 2 * 4
         emit({"config": f"quantized cache: B={Bl} x ctx {Cl}, 14 q / 2 KV heads, D=64, one call, fp16 vs fp8 e4m3",
               "us_fp16": us16, "us_fp8": us8, "speedup": us16 / us8, "GBps_fp16": b16l / (us16 * 1e-6) / 1e9,
               "GBps_fp8": b8l / (us8 * 1e-6) / 1e9, "pct_hbm_peak_fp8": b8l / (us8 * 1e-6) / 1e9 / peak * 100})
-        del kpl, vpl, k8l, v8l
+        del kpl, vpl, r8l
 
     # head_dim 128 shapes: the 7B-class model (32 q / 8 KV heads) and the 32 x 32 x 128 MHA shape
     for Hq, Hkv in ((32, 8), (32, 32)):

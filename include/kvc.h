@@ -312,34 +312,42 @@ kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, cons
                                         size_t workspace_bytes, void* stream);
 
 /* Quantized (fp8) KV cache — an extension: the pages quantize weights, not
- * the KV cache, and fix no quantized format.  A layer's cache is e4m3 codes
- * (1 sign, 4 exponent bits with bias 7, 3 fraction bits; largest 448), one
- * byte each, and one float scale per (slot, KV head) row, k_scales / v_scales
- * [NB][Hkv][bs]; a cached value is code value * scale.  k_codes is
- * [NB][Hkv][bs][D] (a row of D codes per token, as the fp16 cache);
- * v_codes is [NB][Hkv][D][bs]: per block and KV head, one row of 16 token
- * codes per dim, token tau (0..15) at byte
- *   4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1)
- * of the row (tokens 2t, 2t+1, 2t+8, 2t+9 are bytes 4t..4t+3: the decode
- * kernel loads its matrix-multiply fragments with one 32-bit read per row).
- * Per-row scales mean that appending a token never re-quantizes the rest of
- * its block.  The bytes per token are 53 % of the fp16 cache's (D = 64).
- *
- * kv_append_fp8: quantize k_new / v_new (device fp16 [n][Hkv][D]) and write
- * them to their slots: scale = absmax / 448 of the row (IEEE division; 1 for
- * an all-zero row), code = e4m3(x / scale) rounded to nearest even.  Slots as
- * in kv_append (negative = skip, >= NB*bs sets KVC_DEVERR_SLOT).  All device
- * pointers 16-byte aligned. */
-kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n, void* k_codes,
-                         void* v_codes, float* k_scales, float* v_scales, int num_blocks, int Hkv, int head_dim,
-                         int block_size, void* stream);
-/* paged_decode_attention over an fp8 cache: the same result definition with
- * every cached value code value * scale; workspace as paged_decode_plan's.
- * Codes convert to fp16 exactly; the K scale multiplies the scores and the
- * V scale the probabilities in fp32, so the arithmetic matches the fp16
- * kernel's. */
-kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
-                                      const float* v_scales, int num_blocks, const int32_t* block_table,
+ * the KV cache, and fix no quantized format.  Values are e4m3 codes (1 sign,
+ * 4 exponent bits with bias 7, 3 fraction bits; largest 448), one byte each,
+ * with one float scale per (slot, KV head) row: a cached value is
+ * code value * scale.  Per-row scales mean that appending a token never
+ * re-quantizes the rest of its block.  A layer's fp8 cache is one record of
+ * kv_fp8_record_bytes(head_dim) = 32 * D + 128 bytes per (block, KV head),
+ * [NB][Hkv][record], so that the decode reads a block with one copy:
+ *   bytes [0, 16 D)          K codes: 16 token rows of D codes; code x of row
+ *                            r sits at r * D + (((x >> 4) ^ p(r)) << 4) +
+ *                            (x & 15), p(r) = (r >> 1) & 3 for D = 64, r & 7
+ *                            for D = 128 (the 16-byte chunks of a row are
+ *                            permuted so the kernel's fragment loads hit
+ *                            distinct shared-memory banks)
+ *   bytes [16 D, 16 D + 64)  the 16 K scales (float, token order)
+ *   then 16 D bytes          V codes: D dim rows of 16 token codes, token
+ *                            tau (0..15) at byte 4 * ((tau & 7) >> 1) +
+ *                            2 * (tau >> 3) + (tau & 1) of its row (tokens
+ *                            2t, 2t+1, 2t+8, 2t+9 are bytes 4t..4t+3: the
+ *                            kernel loads its matrix-multiply fragments with
+ *                            one 32-bit read per row)
+ *   last 64 bytes            the 16 V scales (float, token order).
+ * The bytes per token are 53 % of the fp16 cache's (D = 64). */
+kvc_status kv_fp8_record_bytes(int head_dim, size_t* bytes);
+/* kv_append_fp8: quantize k_new / v_new (device fp16 [n][Hkv][D]) and write
+ * them into the records of their slots: scale = absmax / 448 of the row (IEEE
+ * division; 1 for an all-zero row), code = e4m3(x / scale) rounded to nearest
+ * even.  Slots as in kv_append (negative = skip, >= NB*bs sets
+ * KVC_DEVERR_SLOT).  All device pointers 16-byte aligned. */
+kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n, void* kv_fp8,
+                         int num_blocks, int Hkv, int head_dim, int block_size, void* stream);
+/* paged_decode_attention over an fp8 cache (kv_fp8: the layer's records):
+ * the same result definition with every cached value code value * scale;
+ * workspace as paged_decode_plan's.  Codes convert to fp16 exactly; the K
+ * scale multiplies the scores and the V scale the probabilities in fp32, so
+ * the arithmetic matches the fp16 kernel's. */
+kvc_status paged_decode_attention_fp8(const void* q, const void* kv_fp8, int num_blocks, const int32_t* block_table,
                                       int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv,
                                       int head_dim, int block_size, int max_context_len, float scale, void* out,
                                       int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,

@@ -32,6 +32,7 @@ __all__ = [
     "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
+    "kv_fp8_record_bytes",
     "prefill_attention", "prefill_attention_ex", "fp8_v_position", "DEVERR",
 ]
 
@@ -118,9 +119,9 @@ def _load():
         "paged_decode_cascade_plan": (I, [I, I, I, I, I, I, I, I, PSZ]),
         "kv_cascade_groups": (I, [P, I, I, P, I, I, P, PI, P, PI]),
         "paged_decode_multi_plan": (I, [I, I, I, I, I, I, I, PSZ]),
-        "kv_append_fp8": (I, [P, P, P, I, P, P, P, P, I, I, I, I, P]),
-        "paged_decode_attention_fp8": (I, [P, P, P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ,
-                                           I, P]),
+        "kv_fp8_record_bytes": (I, [I, PSZ]),
+        "kv_append_fp8": (I, [P, P, P, I, P, I, I, I, I, P]),
+        "paged_decode_attention_fp8": (I, [P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ, I, P]),
         "paged_decode_multi_attention": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, I, ctypes.c_float, P, I, P, SZ,
                                              P]),
         "paged_decode_cascade_attention": (I, [P, P, P, I, P, I, P, P, P, I, I, I, I, I, I, I, I, ctypes.c_float, P,
@@ -548,38 +549,41 @@ def paged_decode_multi_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache
 
 
 def fp8_v_position(tau: int) -> int:
-    """Byte position of token tau (0..15) of a block within each 16-byte dim row of the fp8 V code pool."""
+    """Byte position of token tau (0..15) of a block within each 16-byte dim row of an fp8 record's V codes."""
     return 4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1)
 
 
-def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
-                  v_codes: torch.Tensor, k_scales: torch.Tensor, v_scales: torch.Tensor, stream=None) -> None:
-    """Quantize k_new / v_new (fp16 [n][Hkv][D]) into an fp8 cache layer: K codes uint8 [NB][Hkv][bs][D], V codes
-    uint8 [NB][Hkv][D][bs] (token tau of a block at position fp8_v_position(tau) of each dim row), scales float32
-    [NB][Hkv][bs] (one per (slot, KV head); value = e4m3 code value * scale); slot_mapping int64 [n]."""
+def kv_fp8_record_bytes(head_dim: int) -> int:
+    """Bytes of one fp8 cache record (one per (block, KV head)): 32 * head_dim + 128."""
+    n = ctypes.c_size_t()
+    _check(_lib.kv_fp8_record_bytes(int(head_dim), ctypes.byref(n)), "kv_fp8_record_bytes")
+    return n.value
+
+
+def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, kv_fp8: torch.Tensor,
+                  stream=None) -> None:
+    """Quantize k_new / v_new (fp16 [n][Hkv][D]) into an fp8 cache layer kv_fp8, uint8 [NB][Hkv][record] (one
+    record of kv_fp8_record_bytes(D) per (block, KV head): K codes, K scales, V codes, V scales; value = e4m3
+    code value * scale); slot_mapping int64 [n]."""
     n, Hkv, D = k_new.shape
-    NB, Hkv2, bs, D2 = k_codes.shape
-    if (Hkv2, D2) != (Hkv, D) or v_codes.shape != (NB, Hkv, D, bs) or k_scales.shape != (NB, Hkv, bs) or \
-            v_scales.shape != k_scales.shape or v_new.shape != k_new.shape or slot_mapping.numel() != n:
+    NB, Hkv2, rec = kv_fp8.shape
+    if Hkv2 != Hkv or rec != kv_fp8_record_bytes(D) or v_new.shape != k_new.shape or slot_mapping.numel() != n:
         raise ValueError("fp8 cache shapes do not match")
     _check(_lib.kv_append_fp8(
         _dptr(k_new, torch.float16, "k_new"), _dptr(v_new, torch.float16, "v_new"),
-        _dptr(slot_mapping, torch.int64, "slot_mapping"), n, _dptr(k_codes, torch.uint8, "k_codes"),
-        _dptr(v_codes, torch.uint8, "v_codes"), _dptr(k_scales, torch.float32, "k_scales"),
-        _dptr(v_scales, torch.float32, "v_scales"), NB, Hkv, D, bs, _stream(stream, k_new)), "kv_append_fp8")
+        _dptr(slot_mapping, torch.int64, "slot_mapping"), n, _dptr(kv_fp8, torch.uint8, "kv_fp8"), NB, Hkv, D, 16,
+        _stream(stream, k_new)), "kv_append_fp8")
 
 
-def paged_decode_attention_fp8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor,
-                               k_scales: torch.Tensor, v_scales: torch.Tensor, block_table: torch.Tensor,
+def paged_decode_attention_fp8(q: torch.Tensor, kv_fp8: torch.Tensor, block_table: torch.Tensor,
                                context_lens: torch.Tensor, scale: float, out: torch.Tensor,
                                workspace: Optional[torch.Tensor], max_context_len: int, blocks_per_split: int = 0,
                                stream=None) -> None:
-    """paged_decode_attention over an fp8 cache layer (K codes uint8 [NB][Hkv][bs][D], V codes uint8
-    [NB][Hkv][D][bs] as kv_append_fp8 writes them, scales float32 [NB][Hkv][bs])."""
+    """paged_decode_attention over an fp8 cache layer (kv_fp8 uint8 [NB][Hkv][record] as kv_append_fp8 writes it)."""
     B, Hq, D = q.shape
-    NB, Hkv, bs, Dk = k_codes.shape
-    if Dk != D or v_codes.shape != (NB, Hkv, D, bs) or k_scales.shape != (NB, Hkv, bs) or v_scales.shape != k_scales.shape:
-        raise ValueError("fp8 cache shapes do not match q")
+    NB, Hkv, rec = kv_fp8.shape
+    if rec != kv_fp8_record_bytes(D):
+        raise ValueError("fp8 cache records do not match q's head dim")
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
     if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.numel() != B:
@@ -590,10 +594,9 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: 
     ws_ptr = _dptr(workspace, None, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_lib.paged_decode_attention_fp8(
-        _dptr(q, torch.float16, "q"), _dptr(k_codes, torch.uint8, "k_codes"), _dptr(v_codes, torch.uint8, "v_codes"),
-        _dptr(k_scales, torch.float32, "k_scales"), _dptr(v_scales, torch.float32, "v_scales"), NB,
+        _dptr(q, torch.float16, "q"), _dptr(kv_fp8, torch.uint8, "kv_fp8"), NB,
         _dptr(block_table, torch.int32, "block_table"), block_table.shape[1],
-        _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, bs, int(max_context_len), float(scale),
+        _dptr(context_lens, torch.int32, "context_lens"), B, Hq, Hkv, D, 16, int(max_context_len), float(scale),
         _dptr(out, None, "out"), od, ws_ptr, ws_bytes, int(blocks_per_split), _stream(stream, q)),
         "paged_decode_attention_fp8")
 

@@ -649,17 +649,21 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
     return KVC_OK;
 }
 
-kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n, void* k_codes,
-                         void* v_codes, float* k_scales, float* v_scales, int num_blocks, int Hkv, int head_dim,
-                         int block_size, void* stream) {
+kvc_status kv_fp8_record_bytes(int head_dim, size_t* bytes) {
+    if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
+    if (!bytes) return fail(KVC_ERR_INVALID, "null pointer");
+    *bytes = static_cast<size_t>(kvc::fp8_record_bytes(head_dim));
+    return KVC_OK;
+}
+
+kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int n, void* kv_fp8,
+                         int num_blocks, int Hkv, int head_dim, int block_size, void* stream) {
     if (n < 0 || num_blocks < 1 || Hkv < 1) return fail(KVC_ERR_INVALID, "bad sizes");
     if (head_dim != 64 && head_dim != 128) return fail(KVC_ERR_UNSUPPORTED, "head_dim %d not supported", head_dim);
     if (block_size != kvc::kBlockSize) return fail(KVC_ERR_UNSUPPORTED, "block_size %d not supported", block_size);
     if (n == 0) return KVC_OK;
-    if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
-        return fail(KVC_ERR_INVALID, "null pointer");
-    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scales) ||
-        !aligned16(v_scales))
+    if (!k_new || !v_new || !slot_mapping || !kv_fp8) return fail(KVC_ERR_INVALID, "null pointer");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kv_fp8))
         return fail(KVC_ERR_INVALID, "device buffers must be 16-byte aligned");
     if (g_checked.load()) {
         std::vector<int64_t> sl;
@@ -673,32 +677,25 @@ kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* sl
     cudaError_t e = kvc::device_error_word(&err);
     if (e != cudaSuccess) return cuda_fail(e, "device error word");
     e = kvc::launch_append_fp8(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), slot_mapping, n,
-                               static_cast<uint8_t*>(k_codes), static_cast<uint8_t*>(v_codes), k_scales, v_scales,
-                               num_blocks, Hkv, head_dim, err, as_stream(stream));
+                               static_cast<uint8_t*>(kv_fp8), num_blocks, Hkv, head_dim, err, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kv_append_fp8 launch");
     return KVC_OK;
 }
 
-kvc_status paged_decode_attention_fp8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
-                                      const float* v_scales, int num_blocks, const int32_t* block_table,
+kvc_status paged_decode_attention_fp8(const void* q, const void* kv_fp8, int num_blocks, const int32_t* block_table,
                                       int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv,
                                       int head_dim, int block_size, int max_context_len, float scale, void* out,
                                       int out_dtype, void* workspace, size_t workspace_bytes, int blocks_per_split,
                                       void* stream) {
     std::vector<int32_t> ctx, table;
-    kvc_status s = decode_validate(q, k_codes, v_codes, num_blocks, block_table, max_blocks, context_lens, B, Hq, Hkv,
+    kvc_status s = decode_validate(q, kv_fp8, kv_fp8, num_blocks, block_table, max_blocks, context_lens, B, Hq, Hkv,
                                    head_dim, block_size, max_context_len, out, out_dtype, blocks_per_split, stream, ctx,
                                    table);
     if (s != KVC_OK || B == 0) return s;
-    if (!k_scales || !v_scales) return fail(KVC_ERR_INVALID, "null scales");
-    if (!aligned16(k_scales) || !aligned16(v_scales)) return fail(KVC_ERR_INVALID, "scales must be 16-byte aligned");
     kvc::DecodeArgs a = decode_args(q, nullptr, nullptr, nullptr, nullptr, num_blocks, block_table,
                                     max_blocks, context_lens, B, Hq, Hkv, head_dim, max_context_len, scale, out,
                                     out_dtype, workspace, workspace_bytes, blocks_per_split);
-    a.k_codes = static_cast<const uint8_t*>(k_codes);
-    a.v_codes = static_cast<const uint8_t*>(v_codes);
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
+    a.kv_fp8 = static_cast<const uint8_t*>(kv_fp8);
     kvc::DecodePlan plan;
     cudaError_t e = kvc::decode_plan(B, Hq, Hkv, head_dim, max_context_len, blocks_per_split, &plan);
     if (e != cudaSuccess) return cuda_fail(e, "decode plan");

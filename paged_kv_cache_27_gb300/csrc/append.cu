@@ -87,15 +87,15 @@ cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_
 // Quantized cache (an extension; the pages fix no quantized format): rows of D fp16 values become e4m3 codes
 // with one float scale per (token, KV head) row, so that appending a token never re-quantizes the rest of its
 // block. One warp per (token, KV head, K or V) row: scale = absmax / 448 with IEEE division (1 for an all-zero
-// row), code_i = e4m3(x_i / scale) rounded to nearest even, saturating at 448. Codes go to the slot's row of
-// k_codes / v_codes [NB][Hkv][16][D], the scale to k_scales / v_scales [NB][Hkv][16].
+// row), code_i = e4m3(x_i / scale) rounded to nearest even, saturating at 448. Codes and scale go into the
+// record of the slot's (block, KV head), [NB][Hkv][fp8_record_bytes(D)]: K codes at fp8_kswz(D, row, i), the
+// K scale after the K codes, V codes in the block's dim rows at the token's position vt_pos, the V scale last.
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __half* __restrict__ k_new,
                                                             const __half* __restrict__ v_new,
                                                             const int64_t* __restrict__ slots, int n,
-                                                            uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
-                                                            float* __restrict__ k_scales, float* __restrict__ v_scales,
-                                                            int num_blocks, int Hkv, unsigned* err) {
+                                                            uint8_t* __restrict__ kv_fp8, int num_blocks, int Hkv,
+                                                            unsigned* err) {
     constexpr int PER = D / 32;  // values per lane
     const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -130,36 +130,35 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __half* __rest
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-    const int64_t dst_row = ((slot / kBlockSize) * Hkv + h) * kBlockSize + slot % kBlockSize;
+    const int tok = static_cast<int>(slot % kBlockSize);
+    uint8_t* rec = kv_fp8 + ((slot / kBlockSize) * Hkv + h) * static_cast<int64_t>(fp8_record_bytes(D));
     uint32_t codes = float2_to_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc));
     if constexpr (PER == 4) codes |= static_cast<uint32_t>(float2_to_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc))) << 16;
-    if (kv == 0) {  // K: the token's row of D codes
-        uint8_t* dst = k_codes + dst_row * D + lane * PER;
+    if (kv == 0) {  // K: the token's row of D codes (its lane's PER codes stay inside one 16-byte chunk)
+        uint8_t* dst = rec + fp8_kswz(D, tok, lane * PER);
         if constexpr (PER == 2)
             *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
         else
             *reinterpret_cast<uint32_t*>(dst) = codes;
+        if (lane == 0) reinterpret_cast<float*>(rec + kBlockSize * D)[tok] = sc;
     } else {  // V: one byte in each of the block's D dim rows of 16 tokens, at the token's position
-        uint8_t* dst = v_codes + ((slot / kBlockSize) * Hkv + h) * static_cast<int64_t>(D) * kBlockSize +
-                       vt_pos(static_cast<int>(slot % kBlockSize));
+        uint8_t* vrec = rec + kBlockSize * D + kBlockSize * 4;
+        uint8_t* dst = vrec + vt_pos(tok);
 #pragma unroll
         for (int i = 0; i < PER; ++i) dst[(lane * PER + i) * kBlockSize] = static_cast<uint8_t>(codes >> (8 * i));
+        if (lane == 0) reinterpret_cast<float*>(vrec + kBlockSize * D)[tok] = sc;
     }
-    if (lane == 0) (kv ? v_scales : k_scales)[dst_row] = sc;
 }
 
 cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const int64_t* slots, int n,
-                              uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales, int num_blocks,
-                              int Hkv, int D, unsigned* err, cudaStream_t stream) {
+                              uint8_t* kv_fp8, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
     const int64_t warps = static_cast<int64_t>(n) * Hkv * 2;
     const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
     if (D == 64)
-        kv_append_fp8_kernel<64><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, k_codes, v_codes, k_scales,
-                                                             v_scales, num_blocks, Hkv, err);
+        kv_append_fp8_kernel<64><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, kv_fp8, num_blocks, Hkv, err);
     else if (D == 128)
-        kv_append_fp8_kernel<128><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, k_codes, v_codes, k_scales,
-                                                              v_scales, num_blocks, Hkv, err);
+        kv_append_fp8_kernel<128><<<blocks, 256, 0, stream>>>(k_new, v_new, slots, n, kv_fp8, num_blocks, Hkv, err);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

@@ -53,7 +53,7 @@ struct DecodeKernelParams {
     const __half* v_new;
     __half* k_cache;      // generic pointers to the same layer as the tensor maps (append target)
     __half* v_cache;
-    const uint8_t* v_codes;  // fp8: the layer's V code pool (a block's codes for one KV head are contiguous)
+    const uint8_t* kv_fp8;   // fp8: the layer's records, one per (block, KV head) (fp8_record_bytes each)
     const int32_t* block_table;
     const int32_t* context_lens;
     void* out;
@@ -68,8 +68,6 @@ struct DecodeKernelParams {
     // part_base + c of part_ml / part_acc
     int part_base, part_stride;
     const int32_t* blk_off;  // suffix pass: per sequence, the leading blocks of its table row attended elsewhere
-    const float* k_scales;   // fp8 cache: per (slot, KV head) row scales of the codes, [NB][Hkv][16]
-    const float* v_scales;
     int out_f32;
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
@@ -231,15 +229,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
             return;
         }
         uint8_t* st = wring + s * C::kStageBytes;
-        mbar_arrive_expect_tx(bar, C::kStageBytes + (kFp8 ? 2 * C::kScaleBytes : 0));
+        mbar_arrive_expect_tx(bar, C::kStageBytes);
         const int y = (phys * p.Hkv + kvh) * kBlockSize;
-        if constexpr (kFp8) {  // K codes (16 x D bytes), V codes (D x 16 bytes); the 16 K and 16 V scales
-            uint8_t* sc = wring + C::kScaleOff + s * 2 * C::kScaleBytes;
-            tma_load_2d(st, &tmK, bar, 0, y, policy);
-            bulk_load(st + C::kCodeTileBytes, p.v_codes + static_cast<int64_t>(phys * p.Hkv + kvh) * D * kBlockSize,
-                      C::kCodeTileBytes, bar);
-            bulk_load(sc, p.k_scales + y, C::kScaleBytes, bar);
-            bulk_load(sc + C::kScaleBytes, p.v_scales + y, C::kScaleBytes, bar);
+        if constexpr (kFp8) {  // the block's record: K codes and scales, V codes and scales, in one copy
+            bulk_load(st, p.kv_fp8 + static_cast<int64_t>(phys * p.Hkv + kvh) * C::kStageBytes, C::kStageBytes, bar);
         } else {
 #pragma unroll
             for (int x = 0; x < D; x += 64) {
@@ -257,7 +250,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
         blk[s] = j < cb1 ? j : -1;
     }
     if (lane == 0) {
-        if (warp == 0) {
+        if (!kFp8 && warp == 0) {  // the fp8 records come by bulk copies (the maps are unused)
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
         }
@@ -314,7 +307,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     // further: its swizzle term is the same)
     uint32_t koff[D / 16];
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) koff[ks] = code_swz<D>(g, 16 * ks + 4 * t4);
+    for (int ks = 0; ks < D / 16; ++ks) koff[ks] = fp8_kswz(D, g, 16 * ks + 4 * t4);
 
     // O^T accumulators: o[mt] = dims mt*16 + g (+8) x heads 2*t4, 2*t4+1; running max / sum per head pair
     float o[D / 16][4];
@@ -374,10 +367,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                 uint32_t vbase = 0;
                 const int mi = lane >> 3;
                 if constexpr (kFp8) {
-                    const uint8_t* kt = wring + s * C::kStageBytes;  // K codes, a (swizzled) row per token
-                    const uint8_t* vt = kt + C::kCodeTileBytes;       // V codes, a row of 16 tokens per dim
-                    const float* sk = reinterpret_cast<const float*>(wring + C::kScaleOff + s * 2 * C::kScaleBytes);
-                    const float* sv = sk + kBlockSize;
+                    // the record: K codes (a row per token, chunks permuted), K scales, V codes (a row of 16
+                    // tokens per dim), V scales
+                    const uint8_t* kt = wring + s * C::kStageBytes;
+                    const float* sk = reinterpret_cast<const float*>(kt + C::kCodeTileBytes);
+                    const uint8_t* vt = kt + C::kCodeTileBytes + C::kScaleBytes;
+                    const float* sv = reinterpret_cast<const float*>(vt + C::kCodeTileBytes);
                     sl2g = sl2 * sk[g];
                     sl2g8 = sl2 * sk[g + 8];
                     vsg = g < rem ? sv[g] : 0.f;
@@ -974,9 +969,7 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.part_base = 0;
     p.part_stride = plan.num_parts;
     p.blk_off = nullptr;
-    p.k_scales = a.k_scales;
-    p.v_scales = a.v_scales;
-    p.v_codes = static_cast<const uint8_t*>(a.v_codes);
+    p.kv_fp8 = a.kv_fp8;
     p.out_f32 = a.out_f32;
     p.scale_log2 = a.scale * kLog2e;
     static std::atomic<unsigned> launch_seq{0};
@@ -990,13 +983,16 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
     cudaError_t e = decode_setup<D>();
     if (e != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.Hkv * kBlockSize;
-    const bool fp8 = a.k_codes != nullptr;
-    CUtensorMap tmK, tmV;
-    e = fp8 ? make_code_map(&tmK, a.k_codes, D, rows) : make_tile_map(&tmK, a.k_cache, D, rows);
-    if (e != cudaSuccess) return e;
-    // fp8: V codes come by bulk copy (a block's V^T for one KV head is 16 * D contiguous bytes); tmV is unused
-    e = fp8 ? make_code_map(&tmV, a.k_codes, D, rows) : make_tile_map(&tmV, a.v_cache, D, rows);
-    if (e != cudaSuccess) return e;
+    const bool fp8 = a.kv_fp8 != nullptr;
+    CUtensorMap tmK, tmV;  // fp8: the records come by bulk copies and the maps are unused
+    if (fp8) {
+        memset(&tmK, 0, sizeof(tmK));
+        memset(&tmV, 0, sizeof(tmV));
+    } else {
+        e = make_tile_map(&tmK, a.k_cache, D, rows);
+        if (e == cudaSuccess) e = make_tile_map(&tmV, a.v_cache, D, rows);
+        if (e != cudaSuccess) return e;
+    }
 
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
     float* part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;

@@ -90,11 +90,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
 constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
 
-// Tile configuration per head dim. With kFp8 the cache holds e4m3 codes and a float scale per (token, KV
-// head) row: a stage is the block's K codes (16 token rows of D bytes, in the swizzle of a D-byte row, by TMA)
-// and V codes (D dim rows of 16 token bytes, one bulk copy), and the warp's ring ends with the stages' K and V
-// scales.  The codes
-// go from shared memory straight into the mma.sync fragments (one 32-bit load per fragment row).
+// Tile configuration per head dim. With kFp8 the cache holds one record per (block, KV head) (fp8_record_bytes):
+// the block's K codes (16 token rows of D bytes, each row's 16-byte chunks permuted by fp8_kswz), its 16 K
+// scales, its V codes (D dim rows of 16 token bytes in the order vt_pos gives) and its 16 V scales.  A stage is
+// one record, brought in by one bulk copy; the codes go from shared memory straight into the mma.sync fragments
+// (one 32-bit load per fragment row).
 template <int D, bool kFp8 = false>
 struct DecodeCfg {
     static constexpr int kWarps = D == 64 ? KVC_DEC_WARPS64 : KVC_DEC_WARPS128;
@@ -104,12 +104,10 @@ struct DecodeCfg {
     static constexpr int kTileBytes = kBlockSize * D * 2;    // one 16 x D fp16 tile
     static constexpr int kCodeTileBytes = kBlockSize * D;    // one 16 x D e4m3 tile
     static constexpr int kScaleBytes = kBlockSize * 4;       // 16 float scales
-    static constexpr int kStageBytes = kFp8 ? 2 * kCodeTileBytes  // K codes, V codes
+    static constexpr int kStageBytes = kFp8 ? fp8_record_bytes(D)  // one record: K codes, K scales, V codes, V scales
                                             : 2 * kTileBytes;     // K tile + V tile
-    static constexpr int kScaleOff = kStages * kStageBytes;       // fp8: per stage, 16 K then 16 V scales
-    // a warp's ring starts on a 1024-byte boundary (the swizzle patterns repeat every 1024 bytes)
-    static constexpr int kWarpRingBytes = kFp8 ? (kScaleOff + kStages * 2 * kScaleBytes + 1023) / 1024 * 1024
-                                               : kStages * kStageBytes;
+    // a warp's ring starts on a 1024-byte boundary (the fp16 tiles' TMA swizzle repeats every 1024 bytes)
+    static constexpr int kWarpRingBytes = (kStages * kStageBytes + 1023) / 1024 * 1024;
     static constexpr int kRingBytes = kWarps * kWarpRingBytes;
     // the warps' stage barriers, then rank 0's inbox barrier (padded to keep what follows 16-byte aligned)
     static constexpr int kBarBytes = kWarps * kStages * 8 + 16;
@@ -201,28 +199,6 @@ inline cudaError_t make_tile_map(CUtensorMap* map, const void* base, int D, int6
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// 2-D view of one layer's e4m3 K code pool: rows of D bytes (one per (block, KV head, token)), boxes of 16
-// rows, swizzled so that the 16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3) (64-byte rows) or
-// c ^ (r & 7) (128-byte rows): the fragment loads of 8 rows x 4 lanes then hit 32 different banks.
-inline cudaError_t make_code_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(D)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlockSize)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-// byte offset of byte x of row r in a K code tile as the map above writes it
-template <int D>
-__device__ __forceinline__ uint32_t code_swz(int r, int x) {
-    const int sw = D == 64 ? ((r >> 1) & 3) : (r & 7);
-    return static_cast<uint32_t>(r * D + ((((x >> 4) ^ sw) << 4) | (x & 15)));
 }
 
 

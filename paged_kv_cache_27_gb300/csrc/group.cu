@@ -38,7 +38,7 @@ namespace kvc {
 #define KVC_MULTI_STAGES128 2
 #endif
 #ifndef KVC_MULTI_MAX_TILES64  // n-tiles per warp at most, head_dim 64 (more rows make more row groups)
-#define KVC_MULTI_MAX_TILES64 4
+#define KVC_MULTI_MAX_TILES64 2
 #endif
 #ifndef KVC_MULTI_EARLY_REFILL  // 1: refill a stage once its V fragments are in registers, before the softmax
 #define KVC_MULTI_EARLY_REFILL 1

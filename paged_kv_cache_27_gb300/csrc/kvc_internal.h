@@ -22,9 +22,16 @@ cudaError_t launch_append(const __half* k_new, const __half* v_new, const int64_
 // fp8 V code pool: per (block, KV head), D rows (one per dim) of 16 token codes; token tau (0..15) sits at byte
 // vt_pos(tau) of its row, so that the mma.sync fragment of lane t (tokens 2t, 2t+1, 2t+8, 2t+9) is the 4 bytes at 4t
 __host__ __device__ constexpr int vt_pos(int tau) { return 4 * ((tau & 7) >> 1) + 2 * (tau >> 3) + (tau & 1); }
+// fp8 cache record of one (block, KV head): K codes (16 x D bytes), K scales (16 floats), V codes (D x 16
+// bytes), V scales (16 floats)
+__host__ __device__ constexpr int fp8_record_bytes(int D) { return 2 * (kBlockSize * D + kBlockSize * 4); }
+// byte offset of K code x of token row r inside a record: the row's 16-byte chunks are permuted (by (r >> 1) & 3
+// at D = 64, r & 7 at D = 128) so that the decode kernel's fragment loads of 8 rows x 4 lanes hit 32 banks
+__host__ __device__ constexpr int fp8_kswz(int D, int r, int x) {
+    return r * D + ((((x >> 4) ^ (D == 64 ? ((r >> 1) & 3) : (r & 7))) << 4) | (x & 15));
+}
 cudaError_t launch_append_fp8(const __half* k_new, const __half* v_new, const int64_t* slots, int n,
-                              uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales, int num_blocks,
-                              int Hkv, int D, unsigned* err, cudaStream_t stream);
+                              uint8_t* kv_fp8, int num_blocks, int Hkv, int D, unsigned* err, cudaStream_t stream);
 // copies whole blocks src[i] -> dst[i] for every layer (pools [L][NB][block_elems])
 cudaError_t launch_copy_blocks(const int32_t* src, const int32_t* dst, int n, __half* k_pool, __half* v_pool,
                                int L, int num_blocks, int64_t block_elems, cudaStream_t stream);
@@ -58,12 +65,8 @@ struct DecodeArgs {
     size_t workspace_bytes;
     int blocks_per_split;  // blocks per cluster, 0 = automatic
     unsigned* err;
-    // fp8 cache instead of k_cache / v_cache when k_codes is set: e4m3 codes [NB][Hkv][16][D] and per-row
-    // float scales [NB][Hkv][16]
-    const uint8_t* k_codes = nullptr;
-    const uint8_t* v_codes = nullptr;
-    const float* k_scales = nullptr;
-    const float* v_scales = nullptr;
+    // fp8 cache instead of k_cache / v_cache when set: one record per (block, KV head), [NB][Hkv][record]
+    const uint8_t* kv_fp8 = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -106,9 +106,9 @@ def test_cascade_chain_in_graph(D, Hq, Hkv, always_cascade):
 def test_fp8_decode_chain_in_graph():
     """The fp8-cache decode chained the same way (contexts over one cluster, so the combine kernel runs too)."""
     import paged_kv_cache_27_gb300 as kvc
-    from test_gpu_fp8 import quantized_cache, v_natural
+    from test_gpu_fp8 import oracle_fp8, quantized_cache
     wl = workloads.multi_token_decode(47, [3000, 17, 40000, 2048], 1)
-    kc, vc, ks, vs, _ = quantized_cache(wl)
+    rec, _ = quantized_cache(wl)
     dev = "cuda"
     B = len(wl.ctx)
     table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
@@ -121,7 +121,7 @@ def test_fp8_decode_chain_in_graph():
     def chain():
         src = q0
         for o in outs:
-            kvc.paged_decode_attention_fp8(src, kc, vc, ks, vs, table, ctx_d, wl.scale, o, ws, max_ctx)
+            kvc.paged_decode_attention_fp8(src, rec, table, ctx_d, wl.scale, o, ws, max_ctx)
             src = o
     g = _graph(chain)
     for o in outs:
@@ -131,9 +131,7 @@ def test_fp8_decode_chain_in_graph():
     assert kvc.kvc_device_error_flags(clear=True) == 0
     src = wl.q[:, 0]
     for i, o in enumerate(outs):
-        ref = oracle.decode_fp8(src, kc.cpu().numpy(), v_natural(vc), ks.cpu().numpy(), vs.cpu().numpy(),
-                                wl.block_table, wl.ctx, wl.scale)
-        check_attention(o, ref, f"fp8 chain call {i}")
+        check_attention(o, oracle_fp8(src, rec, wl), f"fp8 chain call {i}")
         src = o.cpu().numpy()
 
 
