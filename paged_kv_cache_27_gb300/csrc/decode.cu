@@ -908,6 +908,7 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
             const int64_t per_seg = usable / segs;
             if (per_seg < 1) continue;
             const int64_t want = (nblk + static_cast<int64_t>(c) * C::kWarps - 1) / (static_cast<int64_t>(c) * C::kWarps);
+            if (min_ncl > per_seg) continue;  // the table-slice bound would push clusters into a second wave
             const int64_t ncl = std::max(min_ncl, std::min(per_seg, want));
             const int64_t ctas = segs * ncl * c;
             // weight: busy CTAs, discounted per cluster along a context and for needing the combine launch

@@ -88,7 +88,9 @@ namespace kvc {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
-constexpr int kMaxClusterBlocks = 2048;  // blocks one cluster covers at most (its table slice is in shared memory)
+// blocks one cluster covers at most: its slice of the block table sits in shared memory (16 KiB at 4096 blocks,
+// which keeps two 8-warp CTAs per SM)
+constexpr int kMaxClusterBlocks = 4096;
 
 // Tile configuration per head dim. With kFp8 the cache holds one record per (block, KV head) (fp8_record_bytes):
 // the block's K codes (16 token rows of D bytes, each row's 16-byte chunks permuted by fp8_kswz), its 16 K

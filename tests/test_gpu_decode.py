@@ -111,11 +111,11 @@ def test_forced_split_sizes(kvc, bps, fused):
     check_workload(kvc, wl, torch.float32, bps=bps, fused=fused)
 
 
-@pytest.mark.parametrize("bps", [0, 256, 512, 1024, 2048])
+@pytest.mark.parametrize("bps", [0, 256, 512, 1024, 2048, 4096])
 def test_long_context_cluster_slices(kvc, bps):
-    """Clusters covering up to 2048 blocks each (the largest table slice a cluster stages): one part per
+    """Clusters covering up to 4096 blocks each (the largest table slice a cluster stages): one part per
     sequence, or a few parts merged by the combine kernel."""
-    wl = workloads.small_decode(91, B=3, Hq=14, Hkv=2, D=64, ctx=[40000, 5000, 1], peak_frac=0.01)
+    wl = workloads.small_decode(91, B=3, Hq=14, Hkv=2, D=64, ctx=[70000, 5000, 1], peak_frac=0.01)
     check_workload(kvc, wl, torch.float32, bps=bps, fused=True)
 
 
