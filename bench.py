@@ -63,8 +63,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "a0cd586161d6516ebf4d80e1dc9454c0642f8df9da0f7bf6f4420ddf1985d0aa",
-                      "bytes_per_launch": 33675008}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "e6ef086d83c001b8718f01eacbb3c335aac0aecd049c8b6fe5d0d23781c21f6a",
+                      "bytes_per_launch": 33676032}
 
 
 def decode_sources_sha256() -> str:
