@@ -551,6 +551,11 @@ def _cfg3_serving_mix(device, stream, flush):
     step = lambda: kvc.paged_decode_append_attention(q, kn, vn, res["k_cache"], res["v_cache"], table, ctx,
                                                       mix.scale, out, wsb, max_ctx)
     us_step = _timed_calls(step, 20, flush, stream)
+    pools = [(res["k_cache"], res["v_cache"])] + [(res["k_cache"].clone(), res["v_cache"].clone()) for _ in range(23)]
+    calls = [lambda k=k, v=v: kvc.paged_decode_append_attention(q, kn, vn, k, v, table, ctx, mix.scale, out, wsb,
+                                                                 max_ctx) for (k, v) in pools]
+    us_graph = _layers_graph_us(calls, device, stream, flush)
+    del pools, calls
     plain = lambda: kvc.paged_decode_attention(q, res["k_cache"], res["v_cache"], table, ctx, mix.scale, out, wsb,
                                                max_ctx)
     us_plain = _timed_calls(plain, 20, flush, stream)
@@ -567,7 +572,8 @@ def _cfg3_serving_mix(device, stream, flush):
     for b in range(mix.B):
         used.update(res["block_table"][b, :-(-int(mix.ctx[b]) // 16)].tolist())
     unique = len(used) * 16 * row
-    return {"us_step": us_step, "logical_bytes": logical, "unique_bytes": unique, "tokens": mix.B,
+    return {"us_step": us_step, "us_step_graph24": us_graph, "logical_bytes": logical, "unique_bytes": unique,
+            "tokens": mix.B,
             "us_decode_plain": us_plain, "us_decode_cascade": us_casc}
 
 
@@ -583,6 +589,45 @@ def _cfg4_cell_us(B, c, device, stream, flush):
     us = _timed_calls(fn, 20, flush, stream)
     del kp, vp
     return us, ns, bps
+
+
+def _layers_graph_us(calls, device, stream, flush, reps=10):
+    """Device time per call of `calls` (one per layer, each on its own pools) captured in one CUDA graph with
+    launch overlap between consecutive kernels, as a model's decode step runs its layers; L2 flushed before each
+    timed replay, so every layer reads its pools from HBM.  Returns us per layer."""
+    import torch
+    g = _graph_of(lambda: [c() for c in calls], device)
+    for _ in range(3):
+        g()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(reps):
+        _flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1) * 1e3
+    return total / (reps * len(calls))
+
+
+def _cfg4_cell_graph_us(B, c, device, stream, flush, layers=24):
+    """One long-context cell as the layers of a decode step: `layers` fused append + decode calls, each on its own
+    K/V pools (copies of one seeded pool, so no layer's reads hit another's lines in L2), in one CUDA graph with
+    launch overlap; L2 flushed before each replay.  Returns us per layer."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    kp, vp, tb, ct, q4, kn4, vn4 = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
+    pools = [(kp, vp)] + [(kp.clone(), vp.clone()) for _ in range(layers - 1)]
+    o4 = torch.empty((B, 14, 64), dtype=torch.float16, device=device)
+    _, _, ws = kvc.paged_decode_plan(B, 14, 2, 64, c)
+    w4 = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+    calls = [lambda k=k, v=v: kvc.paged_decode_append_attention(q4, kn4, vn4, k, v, tb, ct, 0.125, o4, w4, c)
+             for (k, v) in pools]
+    us = _layers_graph_us(calls, device, stream, flush)
+    del pools, kp, vp
+    return us
 
 
 def _prefill_us(seqlens, Hq, Hkv, D, causal, precise, device, stream, flush):
@@ -683,6 +728,11 @@ def config_summary(device, peak, tflops_peak):
         "logical_GBps": round(gbs(c3["logical_bytes"], c3["us_step"]), 1),
         "unique_GBps": round(gbs(c3["unique_bytes"], c3["us_step"]), 1),
         "pct_hbm_peak_unique": round(gbs(c3["unique_bytes"], c3["us_step"]) / peak * 100, 2),
+        "us_per_layer_graph24": round(c3["us_step_graph24"], 2),
+        "tokens_per_s_graph24": round(c3["tokens"] / (c3["us_step_graph24"] * 24e-6)),
+        "logical_GBps_graph24": round(gbs(c3["logical_bytes"], c3["us_step_graph24"]), 1),
+        "unique_GBps_graph24": round(gbs(c3["unique_bytes"], c3["us_step_graph24"]), 1),
+        "pct_hbm_peak_unique_graph24": round(gbs(c3["unique_bytes"], c3["us_step_graph24"]) / peak * 100, 2),
         "us_decode_plain": round(c3["us_decode_plain"], 2), "us_decode_cascade": round(c3["us_decode_cascade"], 2),
         "cascade_speedup": round(c3["us_decode_plain"] / c3["us_decode_cascade"], 3),
         "logical_bytes": c3["logical_bytes"], "unique_bytes": c3["unique_bytes"]}
@@ -690,10 +740,18 @@ def config_summary(device, peak, tflops_peak):
     for B in (1, 4, 16):
         for c in (4096, 16384, 65536, 131072):
             us, ns, bps = _cfg4_cell_us(B, c, device, stream, flush)
+            usg = _cfg4_cell_graph_us(B, c, device, stream, flush)
             nb = B * c * 2 * 2 * 64 * 2
             cells.append({"B": B, "ctx": c, "us_per_call": round(us, 2), "GBps": round(gbs(nb, us), 1),
-                          "pct_hbm_peak": round(gbs(nb, us) / peak * 100, 2), "splits": ns, "blocks_per_split": bps})
+                          "pct_hbm_peak": round(gbs(nb, us) / peak * 100, 2), "splits": ns, "blocks_per_split": bps,
+                          "us_per_layer_graph24": round(usg, 2), "GBps_graph24": round(gbs(nb, usg), 1),
+                          "pct_hbm_peak_graph24": round(gbs(nb, usg) / peak * 100, 2)})
     out["long_context"] = cells
+    out["long_context_timing"] = (
+        "us_per_call: one call between CUDA events, L2 flushed before it; includes the launch gaps around a lone "
+        "kernel (an event pair around a trivial kernel measures ~4 us on this GPU). *_graph24: the cell as the 24 "
+        "layers of a decode step (each layer its own K/V pools), one CUDA graph with launch overlap, L2 flushed "
+        "before each replay, device time per layer")
     for name, seqlens, hq, hkv in (("prefill_varlen_37_120_8_200_8x8_d64_causal", (37, 120, 8, 200), 8, 8),
                                    ("prefill_gqa_2x256_8x2_d64_causal", (256, 256), 8, 2)):
         us, us_g, fl = _prefill_us(seqlens, hq, hkv, 64, True, False, device, stream, flush)
@@ -815,9 +873,12 @@ def run_suite_decode(device, stream, flush, emit, peak):
     for B in (1, 4, 16):
         for c in (4096, 16384, 65536, 131072):
             us, ns, bps = _cfg4_cell_us(B, c, device, stream, flush)
+            usg = _cfg4_cell_graph_us(B, c, device, stream, flush)
             nbytes = B * c * 2 * 2 * 64 * 2
             emit({"config": f"long context: B={B}, ctx={c}, 14 q / 2 KV heads, D=64", "us_per_call": us,
                   "GBps": nbytes / (us * 1e-6) / 1e9, "pct_hbm_peak": nbytes / (us * 1e-6) / 1e9 / peak * 100,
+                  "us_per_layer_graph24": usg, "GBps_graph24": nbytes / (usg * 1e-6) / 1e9,
+                  "pct_hbm_peak_graph24": nbytes / (usg * 1e-6) / 1e9 / peak * 100,
                   "splits": ns, "blocks_per_split": bps, "kv_bytes": nbytes})
 
 

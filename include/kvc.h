@@ -206,7 +206,7 @@ kvc_status paged_decode_workspace_init(void* workspace, size_t bytes, void* stre
  * exp-sum per query head; the splits merge with the rescaling rule of the
  * FlashAttention article, on chip within a thread-block cluster and, for
  * contexts longer than one cluster covers, through the workspace.
- * Preconditions: Hq % Hkv == 0, Hq/Hkv <= 8, head_dim in {64, 128},
+ * Preconditions: Hq % Hkv == 0, Hq/Hkv <= 64, head_dim in {64, 128},
  * block_size == 16; 16-byte aligned pointers. */
 kvc_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
                                   const int32_t* block_table, int max_blocks, const int32_t* context_lens,

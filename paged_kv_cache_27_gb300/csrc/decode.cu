@@ -709,14 +709,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
 
 
 // Merge the partial states of every (sequence, query head): the clusters along a context longer than
-// one cluster covers, and in a cascade also the parts of the shared prefix. 8 groups of 32 lanes walk
-// the parts with a running (M, L, acc), then the groups merge.
+// one cluster covers, and in a cascade also the parts of the shared prefix.  The merge rule is the
+// FlashAttention article's ("Was ist der mathematische Aspekt von Softmax?"): with M the largest part
+// maximum, out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s over the parts that saw a token (l > 0).
+// Written for latency, since the parts sit in L2 and there are few of them: every thread loads the (m, l)
+// of its parts at once for M, then for L, then each thread accumulates one float4 of dims over a strided
+// subset of the parts (independent loads, no running-maximum chain), and the subsets are summed in shared
+// memory.  An earlier form walked the parts with a running (M, L, acc) per warp, one dependent L2 round
+// trip per part.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const CombineParams p) {
-    constexpr int V = D / 32;  // dims per lane
-    __shared__ float sM[8], sL[8], sO[8][D];
+    constexpr int NT = 256, Q = D / 4, NPG = NT / Q;  // float4 columns of a row; part subsets
+    __shared__ float s_red[NT / 32];
+    __shared__ float4 s_o[NPG][Q];
     const int h = blockIdx.x, y = blockIdx.y, b = y / p.q_len;  // y: the query row (a sequence's token)
-    const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // With early_release the next kernel (the next layer's decode) may launch and fetch its tables and first K/V
+    // tiles while this one waits; its own dependency wait still covers this grid, whose completion covers the
+    // decode before it.  The host asks for it only where a decode grid of this shape takes at most half the
+    // resident CTA slots, so the next one fits beside the current one: on grids that fill the GPU the early
+    // launch made the next grid's clusters land piecemeal in the slots the current one frees, and the layer of a
+    // 24-layer step slowed (B = 1 x 131072: 17.1 -> 20.2 us; B = 1 x 4096: 6.0 -> 4.9 us, where it fits).
+    if (KVC_COMBINE_EARLY_TRIGGER && p.early_release) grid_dependents_launch();
     // context lengths and prefix offsets are never written by the kernel before (the launch-overlap contract):
     // they are read before the dependency wait, the parts and the output only after it
     const int ctx_full = p.context_lens[b];
@@ -733,46 +747,66 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
     grid_dependency_wait();
     if (bad) {
         if (p.cascade) {  // the attention kernels left this row to us
-            if (h == 0 && threadIdx.x == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
-            if (threadIdx.x < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + threadIdx.x, 0.f);
+            if (h == 0 && tid == 0) atomicOr(p.err, KVC_DEVERR_CONTEXT);
+            if (tid < D) store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + tid, 0.f);
         }
         return;
     }
+    const int n = npre + nsuf;
     const int64_t row0 = (static_cast<int64_t>(y) * p.Hq + h) * p.part_stride;
-    float M = -INFINITY, L = 0.f, O[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) O[v] = 0.f;
-    for (int s = grp; s < npre + nsuf; s += 8) {
-        const int64_t row = row0 + (s < npre ? s : p.part_base + s - npre);
-        const float m = p.part_ml[row * 2], l = p.part_ml[row * 2 + 1];
-        if (!(l > 0.f)) continue;
-        const float Mn = fmaxf(M, m);
-        const float a = M == -INFINITY ? 0.f : ex2(M - Mn);
-        const float w = ex2(m - Mn);
-        L = L * a + l * w;
-#pragma unroll
-        for (int v = 0; v < V; ++v) O[v] = O[v] * a + p.part_acc[row * D + lane * V + v] * w;
-        M = Mn;
-    }
-    if (lane == 0) {
-        sM[grp] = M;
-        sL[grp] = L;
+    auto part_row = [&](int s) -> int64_t { return row0 + (s < npre ? s : p.part_base + s - npre); };
+    auto ml_of = [&](int s) { return *reinterpret_cast<const float2*>(p.part_ml + part_row(s) * 2); };
+
+    // M: the largest maximum among the parts that saw a token
+    float mx = -INFINITY;
+    for (int s = tid; s < n; s += NT) {
+        const float2 ml = ml_of(s);
+        if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
 #pragma unroll
-    for (int v = 0; v < V; ++v) sO[grp][lane * V + v] = O[v];
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_red[warp] = mx;
     __syncthreads();
-    if (threadIdx.x < D) {
-        const int d = threadIdx.x;
-        float Mx = -INFINITY;
-        for (int k = 0; k < 8; ++k) Mx = fmaxf(Mx, sM[k]);
-        float Lt = 0.f, Ot = 0.f;
-        for (int k = 0; k < 8; ++k) {
-            if (!(sL[k] > 0.f)) continue;  // groups that saw no part
-            const float w = ex2(sM[k] - Mx);
-            Lt += sL[k] * w;
-            Ot += sO[k][d] * w;
+    float M = s_red[0];
+#pragma unroll
+    for (int k = 1; k < NT / 32; ++k) M = fmaxf(M, s_red[k]);
+    __syncthreads();  // s_red is reused below
+    // L = sum_s 2^(m_s - M) l_s
+    float ls = 0.f;
+    for (int s = tid; s < n; s += NT) {
+        const float2 ml = ml_of(s);
+        if (ml.y > 0.f) ls += ml.y * ex2(ml.x - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (lane == 0) s_red[warp] = ls;
+    // acc: thread (pg, q) sums float4 column q over parts pg, pg + NPG, ...
+    const int q = tid % Q, pg = tid / Q;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = pg; s < n; s += NPG) {
+        const int64_t r = part_row(s);
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
+        const float4 a = *reinterpret_cast<const float4*>(p.part_acc + r * D + 4 * q);
+        O = fma4(ml.y > 0.f ? ex2(ml.x - M) : 0.f, a, O);
+    }
+    s_o[pg][q] = O;
+    __syncthreads();
+    if (tid < Q) {
+        float L = 0.f;
+#pragma unroll
+        for (int k = 0; k < NT / 32; ++k) L += s_red[k];
+        float4 t = s_o[0][tid];
+#pragma unroll
+        for (int k = 1; k < NPG; ++k) {
+            const float4 u = s_o[k][tid];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
         }
-        store_out(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + d, Lt > 0.f ? Ot / Lt : 0.f);
+        store_out4(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + 4 * tid,
+                   scale4(t, L > 0.f ? 1.f / L : 0.f));
     }
 }
 
@@ -887,42 +921,39 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
         bpc = std::min(bpc_req, kMaxClusterBlocks);
         cs = std::max(1, std::min(kMaxCluster, (bpc + C::kWarps - 1) / C::kWarps));
     } else {
-        // One wave: for each cluster size, the clusters that can be resident (KVC_DEC_PLAN_CTAS of the CTAs an SM
-        // holds, the rest left for the next launch) are shared out over the (sequence, KV head) pairs, at most
-        // one cluster per cs x warps blocks.  The size that keeps the most CTAs busy wins; among equals, fewer
-        // clusters per context (less merging), then the larger cluster.  Where not even one CTA per pair fits in a
-        // wave, each pair gets one CTA (several waves).
+        // One wave, few parts.  For cluster sizes from the largest down, the clusters that can be resident
+        // (KVC_DEC_PLAN_CTAS of the CTAs an SM holds, the rest left for the next launch) are shared out over the
+        // (sequence, KV head, head chunk) units; a unit takes one cluster per cs x warps x
+        // KVC_DEC_MIN_BLOCKS_PER_WARP blocks of its context, up to its share.  A plan with several clusters per
+        // unit needs the combine launch; below KVC_DEC_SMALL_BYTES of K/V such a plan keeps to half the resident
+        // clusters, so that the combine can let the next launch (the next layer) start beside it.  The largest
+        // cluster size that gives every unit its clusters wins; where none does, each unit gets one CTA (several
+        // waves).
         const int smem_est = C::smem_bytes(kMaxCluster, G, std::min(nblk, kMaxClusterBlocks));
         int occ = 0;
         cudaError_t e = decode_occupancy<D>(smem_est, &occ);
         if (e != cudaSuccess) return e;
         const int64_t segs = std::max<int64_t>(1, static_cast<int64_t>(B) * Hkv * hchunks);
         const int64_t min_ncl = (nblk + kMaxClusterBlocks - 1) / kMaxClusterBlocks;
-        int64_t best_ctas = 0, best_ncl = 0, best_score = 0;
-        for (int c = 1; c <= kMaxCluster; ++c) {
-            if (c > 1 && (static_cast<int64_t>(c - 1) * C::kWarps >= nblk)) break;  // a CTA would have no block
+        const int64_t kv_bytes = static_cast<int64_t>(B) * Hkv * nblk * (2 * kBlockSize * D * 2);
+        int64_t ncl = min_ncl;
+        cs = 1;
+        for (int c = kMaxCluster; c >= 1; --c) {
+            if (c > 1 && (static_cast<int64_t>(c - 1) * C::kWarps >= nblk)) continue;  // a CTA would have no block
             int resident = 0;
             e = decode_resident_clusters<D>(c, C::smem_bytes(c, G, std::min(nblk, kMaxClusterBlocks)), &resident);
             if (e != cudaSuccess) return e;
             const int64_t usable = static_cast<int64_t>(resident) * std::min(occ, KVC_DEC_PLAN_CTAS) / occ;
             const int64_t per_seg = usable / segs;
-            if (per_seg < 1) continue;
-            const int64_t want = (nblk + static_cast<int64_t>(c) * C::kWarps - 1) / (static_cast<int64_t>(c) * C::kWarps);
-            if (min_ncl > per_seg) continue;  // the table-slice bound would push clusters into a second wave
-            const int64_t ncl = std::max(min_ncl, std::min(per_seg, want));
-            const int64_t ctas = segs * ncl * c;
-            // weight: busy CTAs, discounted per cluster along a context and for needing the combine launch
-            const int64_t score = ctas * 1000 * (1000 - (ncl > 1 ? KVC_DEC_COMBINE_PENALTY : 0)) /
-                                  (1000 + KVC_DEC_PART_PENALTY * ncl);
-            if (score > best_score || (score == best_score && ncl <= best_ncl)) {
-                best_score = score;
-                best_ctas = ctas;
-                best_ncl = ncl;
-                cs = c;
-            }
+            if (per_seg < min_ncl) continue;  // (the table-slice bound) clusters would spill into a second wave
+            const int64_t span = static_cast<int64_t>(c) * C::kWarps * KVC_DEC_MIN_BLOCKS_PER_WARP;
+            const int64_t want = (nblk + span - 1) / span;
+            int64_t n = std::max(min_ncl, std::min(per_seg, want));
+            if (n > 1 && kv_bytes < KVC_DEC_SMALL_BYTES) n = std::max(min_ncl, std::min((usable / 2) / segs, want));
+            ncl = n;
+            cs = c;
+            break;
         }
-        const int64_t ncl = best_ctas > 0 ? best_ncl : min_ncl;
-        if (best_ctas == 0) cs = 1;
         bpc = static_cast<int>((nblk + ncl - 1) / ncl);
     }
     const int nparts = (nblk + bpc - 1) / bpc;
@@ -1028,6 +1059,12 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
         c.prefix_chunk = 0;
         c.cascade = 0;
         c.q_len = 1;
+        // release the next kernel at the combine's start when two decode grids of this shape fit at once
+        int occ = 0;
+        const int smem = C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split);
+        c.early_release = 0;
+        if (!fp8 && decode_occupancy<D>(smem, &occ) == cudaSuccess)
+            c.early_release = 2 * static_cast<int64_t>(grid.x) * grid.y * grid.z <= static_cast<int64_t>(occ) * sm_count();
         e = launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
     }
     return e;

@@ -45,6 +45,9 @@ namespace kvc {
 #ifndef KVC_DEC_TRIGGER
 #define KVC_DEC_TRIGGER 2
 #endif
+#ifndef KVC_COMBINE_EARLY_TRIGGER  // the split combine kernel lets the next kernel launch as soon as it starts
+#define KVC_COMBINE_EARLY_TRIGGER 1
+#endif
 #ifndef KVC_GROUP_EARLY_TRIGGER  // the group kernel lets the next kernel launch as soon as it starts
 #define KVC_GROUP_EARLY_TRIGGER 1
 #endif
@@ -57,16 +60,19 @@ namespace kvc {
 #ifndef KVC_DEC_PLAN_CTAS  // CTAs per SM one launch is sized for; the rest lets the next launch start early
 #define KVC_DEC_PLAN_CTAS 2
 #endif
-// Split planner weights, per mille of a plan's busy CTAs: a discount per cluster along a context (each adds a
-// partial state to merge), and one for needing the separate combine launch at all (more than one cluster).
-// Measured on one call with L2 flushed: B = 1 x 131072 ran 26.9 us with 76 two-CTA clusters per context and
-// 23.6 us with 18 eight-CTA clusters; B = 16 x 16384 32.5 us with one eight-CTA cluster per context against
-// 33.6-34.0 us with 3 three-CTA or 9 one-CTA clusters and the combine kernel.
-#ifndef KVC_DEC_PART_PENALTY
-#define KVC_DEC_PART_PENALTY 10
+// Fewest blocks per warp the split planner aims for: with two stages per warp, four blocks are two copy round
+// trips.  Below KVC_DEC_SMALL_BYTES of K/V per call a plan that needs the combine launch keeps to half the
+// resident clusters, so that the combine can release the next launch (the next layer) at its start and the two
+// run side by side; above it the halved copy rate costs more than the overlap gains.  Measured per layer of a
+// 24-layer graph (L2 flushed per replay), against plans that filled the GPU with one or two blocks per warp:
+// B = 1 x 4096 5.5 -> 4.7 us, B = 4 x 4096 8.3 -> 5.0, B = 1 x 16384 8.9 -> 7.0-7.2, B = 1 x 65536 12.3 -> 11.1,
+// B = 4 x 16384 11.8 -> 11.2; at 64 MiB and above the full wave stays ahead (B = 4 x 65536 26.5 us against 28.5
+// on half of it).  The 32 x 2048 step keeps its four blocks per warp in one cluster per (sequence, KV head).
+#ifndef KVC_DEC_MIN_BLOCKS_PER_WARP
+#define KVC_DEC_MIN_BLOCKS_PER_WARP 4
 #endif
-#ifndef KVC_DEC_COMBINE_PENALTY
-#define KVC_DEC_COMBINE_PENALTY 150
+#ifndef KVC_DEC_SMALL_BYTES
+#define KVC_DEC_SMALL_BYTES (int64_t(64) << 20)
 #endif
 // 1: the CTAs of a cluster hand their merged states to rank 0 with st.async, whose bytes complete on an mbarrier
 // in rank 0 (senders leave at once); 0: remote stores, then a cluster barrier (release / acquire)

@@ -717,6 +717,7 @@ static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPla
     c.prefix_chunk = 0;
     c.cascade = 1;  // every output row comes from the parts
     c.q_len = q_len;
+    c.early_release = 0;
     return launch_combine(c, D, a.B * q_len, stream);
 }
 
@@ -817,6 +818,7 @@ static cudaError_t launch_cascade_d(const DecodeArgs& a, const int32_t* group_st
     c.prefix_chunk = cp.cluster * cp.chunk;  // shared blocks per prefix part
     c.cascade = 1;
     c.q_len = 1;
+    c.early_release = 0;
     return launch_combine(c, D, a.B, stream);
 }
 

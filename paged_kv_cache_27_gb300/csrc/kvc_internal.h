@@ -82,6 +82,7 @@ struct CombineParams {
     int prefix_chunk;  // blocks per prefix part (cascade), 0 = no prefix parts
     int cascade;       // 1: only partials were written; this kernel writes every output row
     int q_len;         // query rows per sequence (multi-token decode; 1 otherwise): row y is sequence y / q_len
+    int early_release; // 1: the next kernel may launch as soon as this one starts (see the combine kernel)
 };
 // grid (Hq, rows): one CTA per (query head, query row)
 cudaError_t launch_combine(const CombineParams& c, int D, int rows, cudaStream_t stream);
