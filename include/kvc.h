@@ -305,6 +305,19 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
  * (partial states per cluster, then their merge). */
 kvc_status paged_decode_multi_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,
                                    int q_len, size_t* workspace_bytes);
+/* Process-wide: 1 runs multi-token calls with head_dim 64 and q_len x
+ * (Hq / Hkv) <= 64 query rows on a tensor-core (tcgen05) kernel instead of
+ * the default mma.sync kernel; 0 (the default) keeps the mma.sync kernel.
+ * Both give the same result within the decode tolerance.  The tensor-core
+ * kernel puts the 128 keys of a tile on the products' M side, one TMEM lane
+ * and softmax thread per key, and the query rows on N.  On GB300 it measured
+ * slower for 32 sequences x 2048 tokens, 14 / 2 heads (per layer of a
+ * 24-layer graph, q_len 2 / 4 / 8: 13.3 / 15.5 / 21.6 us against 8.4 / 12.1
+ * / 18.8 us): a tile's 12 MMA instructions and its softmax stage, handed from
+ * warp role to warp role, take longer than the tile's copy.  A plan made under
+ * one setting is valid under the other only if the two give the same
+ * workspace size: plan again after changing it. */
+kvc_status kvc_set_multi_tc(int on);
 kvc_status paged_decode_multi_attention(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
                                         const int32_t* block_table, int max_blocks, const int32_t* context_lens,
                                         int q_len, int B, int Hq, int Hkv, int head_dim, int block_size,

@@ -28,7 +28,7 @@ __all__ = [
     "kv_block_release", "kv_block_refcount", "kv_block_num_free", "kv_cache_utilisation",
     "kv_block_cow", "kv_copy_blocks", "kv_slot_mapping", "kv_step_prepare", "kv_append",
     "paged_decode_plan", "paged_decode_workspace_init", "paged_decode_attention",
-    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_set_cascade_min_saved_blocks", "kvc_copy_async", "KVC_COPY_AHEAD", "PreparedCall",
+    "paged_decode_append_attention", "kvc_set_launch_overlap", "kvc_set_cascade_min_saved_blocks", "kvc_set_multi_tc", "kvc_copy_async", "KVC_COPY_AHEAD", "PreparedCall",
     "kvc_trace_read",
     "paged_decode_attention_static_workspace", "paged_decode_cascade_plan", "paged_decode_cascade_attention", "kv_cascade_groups",
     "paged_decode_multi_plan", "paged_decode_multi_attention", "kv_append_fp8", "paged_decode_attention_fp8",
@@ -112,6 +112,7 @@ def _load():
                                               I, P, SZ, I, P]),
         "kvc_set_launch_overlap": (I, [I]),
         "kvc_set_cascade_min_saved_blocks": (I, [I]),
+        "kvc_set_multi_tc": (I, [I]),
         "kvc_copy_async": (I, [P, P, SZ, ctypes.c_uint, P]),
         "paged_decode_attention_static_workspace": (I, [P, P, P, I, P, I, P, I, I, I, I, I, I, ctypes.c_float, P, I,
                                                         I, P]),
@@ -224,6 +225,11 @@ def kvc_set_cascade_min_saved_blocks(blocks: int) -> None:
     """Cascade calls saving fewer than `blocks` block reads per KV head ((B - n_groups) * max_shared_blocks) run the
     plain decode (0: always the cascade kernels)."""
     _check(_lib.kvc_set_cascade_min_saved_blocks(int(blocks)), "kvc_set_cascade_min_saved_blocks")
+
+
+def kvc_set_multi_tc(on: bool) -> None:
+    """Multi-token calls at head dim 64 with up to 64 query rows on the tensor-core kernel (off: the mma.sync kernel)."""
+    _check(_lib.kvc_set_multi_tc(int(bool(on))), "kvc_set_multi_tc")
 
 
 def kvc_set_launch_overlap(on: bool) -> None:

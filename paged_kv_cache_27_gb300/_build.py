@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(OUT_DIR, "libkvc.so")
-SOURCES = ["api.cu", "append.cu", "decode.cu", "group.cu", "group_tc.cu", "prefill.cu", "prefill_1t.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "group.cu", "group_tc.cu", "multi_tc.cu", "prefill.cu",
+           "prefill_1t.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-cudart", "shared"]

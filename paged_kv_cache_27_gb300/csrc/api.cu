@@ -379,6 +379,11 @@ kvc_status kvc_set_launch_overlap(int on) {
     return KVC_OK;
 }
 
+kvc_status kvc_set_multi_tc(int on) {
+    kvc::set_multi_tc(on);
+    return KVC_OK;
+}
+
 kvc_status kvc_set_cascade_min_saved_blocks(int blocks) {
     if (blocks < 0) return fail(KVC_ERR_INVALID, "negative block count %d", blocks);
     kvc::set_cascade_min_saved_blocks(blocks);

@@ -455,21 +455,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
 #if KVC_DEC_EARLY_REFILL
                     // V^T fragments now; the stage is then free and its refill goes out before the softmax
 #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
+                    for (int mt = 0; mt < D / 16; ++mt)
                         ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), va[mt][0], va[mt][1],
                                   va[mt][2], va[mt][3]);
-                        va[mt][0] &= keep0;
-                        va[mt][1] &= keep0;
-                        va[mt][2] &= keep1;
-                        va[mt][3] &= keep1;
+                    if (rem < kBlockSize) {  // the context's last block (warp-uniform)
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            va[mt][0] &= keep0;
+                            va[mt][1] &= keep0;
+                            va[mt][2] &= keep1;
+                            va[mt][3] &= keep1;
+                        }
                     }
-                    // the copy may overwrite the stage only once the warp's reads of it have returned: fold
-                    // the loaded registers (the K fragments were consumed by the S products above)
+                    // the copy may overwrite the stage only once the warp's reads of it have returned: one register
+                    // of each ldmatrix folded (a warp issues in order, and an ldmatrix's four registers arrive
+                    // together), so the refill below cannot issue before every read is back (the K fragments were
+                    // consumed by the S products above)
                     uint32_t dep = 0;
 #pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][k]));
+                    for (int mt = 0; mt < D / 16; ++mt) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][0]));
                     refill(s);
                     refilled = true;
 #endif

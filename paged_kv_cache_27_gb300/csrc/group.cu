@@ -22,6 +22,7 @@
 // state and the combine kernel (decode.cu) merges them.
 #include "decode_common.cuh"
 #include "group_tc.h"
+#include "multi_tc.h"
 
 namespace kvc {
 
@@ -55,6 +56,10 @@ namespace kvc {
 #endif
 static std::atomic<int> g_cascade_min_saved{KVC_CASCADE_MIN_SAVED_BLOCKS};
 void set_cascade_min_saved_blocks(int blocks) { g_cascade_min_saved.store(blocks); }
+// multi-token decode at head dim 64 with up to 64 query rows on the tensor cores (multi_tc.cu) when set; off by
+// default (measured slower than the mma.sync kernel on the listed shapes)
+static std::atomic<int> g_multi_tc{0};
+void set_multi_tc(int on) { g_multi_tc.store(on ? 1 : 0); }
 #ifndef KVC_PREFIX_TC_MIN_ROWS  // cascade prefix, head dim 64: groups of this many query rows run on the tensor cores
 #define KVC_PREFIX_TC_MIN_ROWS 17
 #endif
@@ -312,31 +317,45 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
             // V^T fragments into registers, then the stage goes back to the copy engine before the softmax
             uint32_t va[D / 16][4];
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
+            for (int mt = 0; mt < D / 16; ++mt)
                 ldsm_x4_t(vbase + swz((mi >> 1) * 8 + (lane & 7), 2 * mt + (mi & 1)), va[mt][0], va[mt][1], va[mt][2],
                           va[mt][3]);
-                va[mt][0] &= keep0;
-                va[mt][1] &= keep0;
-                va[mt][2] &= keep1;
-                va[mt][3] &= keep1;
+            if (rem < kBlockSize) {  // the context's last block (warp-uniform)
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    va[mt][0] &= keep0;
+                    va[mt][1] &= keep0;
+                    va[mt][2] &= keep1;
+                    va[mt][3] &= keep1;
+                }
             }
-            // the copy may overwrite the stage only once the warp's reads of it have returned: fold the loaded
-            // registers (the K fragments were consumed by the S products above)
+            // the copy may overwrite the stage only once the warp's reads of it have returned: one register of each
+            // ldmatrix folded (a warp issues in order, and an ldmatrix's four registers arrive together), so the
+            // refill cannot issue before every read is back (the K fragments were consumed by the S products above)
             uint32_t dep = 0;
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][q]));
+            for (int mt = 0; mt < D / 16; ++mt) asm volatile("xor.b32 %0, %0, %1;" : "+r"(dep) : "r"(va[mt][0]));
             refill(k, s);
 #endif
             uint32_t bh[NT][2], bl[NT][2];
+            // every row sees every key of this block (warp-uniform): no mask, and every running maximum is finite
+            // once the first update below has run
+            const bool all_vis = k0 + kBlockSize - 1 <= (kPrefix ? ctx - 1 : ctx - T);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 // keys k0 + g and k0 + g + 8 against rows 2 t4 (+1): visible up to each row's last key
-                const float x0 = k0 + g <= lastk[nt][0] ? sc[nt][0] * sl2 : -INFINITY;
-                const float x1 = k0 + g <= lastk[nt][1] ? sc[nt][1] * sl2 : -INFINITY;
-                const float x2 = k0 + g + 8 <= lastk[nt][0] ? sc[nt][2] * sl2 : -INFINITY;
-                const float x3 = k0 + g + 8 <= lastk[nt][1] ? sc[nt][3] * sl2 : -INFINITY;
+                float x0, x1, x2, x3;
+                if (all_vis) {
+                    x0 = sc[nt][0] * sl2;
+                    x1 = sc[nt][1] * sl2;
+                    x2 = sc[nt][2] * sl2;
+                    x3 = sc[nt][3] * sl2;
+                } else {
+                    x0 = k0 + g <= lastk[nt][0] ? sc[nt][0] * sl2 : -INFINITY;
+                    x1 = k0 + g <= lastk[nt][1] ? sc[nt][1] * sl2 : -INFINITY;
+                    x2 = k0 + g + 8 <= lastk[nt][0] ? sc[nt][2] * sl2 : -INFINITY;
+                    x3 = k0 + g + 8 <= lastk[nt][1] ? sc[nt][3] * sl2 : -INFINITY;
+                }
                 float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
                 // lazy running maxima (as in the decode kernel): they move only when a visible score exceeds them
                 // by more than 2^KVC_DEC_LAZY_MAX, so the weights stay <= 2^KVC_DEC_LAZY_MAX
@@ -364,8 +383,18 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
                     }
                 }
                 const float mn0 = m_run[nt][0], mn1 = m_run[nt][1];
-                const float p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0), p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
-                const float p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1), p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
+                float p0, p1, p2, p3;
+                if (all_vis) {
+                    p0 = ex2(x0 - mn0);
+                    p2 = ex2(x2 - mn0);
+                    p1 = ex2(x1 - mn1);
+                    p3 = ex2(x3 - mn1);
+                } else {
+                    p0 = mn0 == -INFINITY ? 0.f : ex2(x0 - mn0);
+                    p2 = mn0 == -INFINITY ? 0.f : ex2(x2 - mn0);
+                    p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1);
+                    p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
+                }
                 l_run[nt][0] += p0 + p2;
                 l_run[nt][1] += p1 + p3;
                 // P^T as the B operand: fp16 high part and fp16 residual
@@ -656,10 +685,22 @@ static gtc::Params tc_params(const DecodeArgs& a, const int32_t* group_start, co
 }
 
 // ---- multi-token decode ------------------------------------------------------------------------------
+// q_len >= 2 tokens of q_len x G query rows on the tensor-core kernel (multi_tc.cu)
+static bool use_multi_tc(int D, int q_len, int G) {
+    return g_multi_tc.load(std::memory_order_relaxed) != 0 && q_len >= 2 && mtc::supported(D, q_len * G);
+}
+
 cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, MultiPlan* plan) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
     if (D != 64 && D != 128) return cudaErrorInvalidValue;
+    if (use_multi_tc(D, q_len, Hq / Hkv)) {
+        mtc::plan(B, Hkv, q_len * (Hq / Hkv), max_ctx, sms, &plan->chunk, &plan->cluster, &plan->nclus);
+        plan->stages = 3;
+        plan->workspace_bytes =
+            plan->nclus > 1 ? partials_bytes(static_cast<size_t>(B) * q_len * Hq * plan->nclus, D) : 0;
+        return cudaSuccess;
+    }
     int nt, nrg;
     group_tiles(D, q_len * (Hq / Hkv), &nt, &nrg);
     const int64_t nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
@@ -688,16 +729,43 @@ static cudaError_t launch_multi_d(const DecodeArgs& a, int q_len, const MultiPla
     float* part_ml = static_cast<float*>(a.workspace);
     const bool parts = mp.nclus > 1;  // partial states and the combine kernel
     float* part_acc = parts ? partials_acc(part_ml, nrow) : nullptr;
-    GroupKernelParams p = group_params(a, parts ? part_ml : nullptr, part_acc);
-    p.q_len = q_len;
-    p.chunk = mp.chunk;
-    p.cs = mp.cluster;
-    p.nclus = mp.nclus;
-    p.part_stride = mp.nclus;
-    int nt, nrg;
-    group_tiles(D, q_len * p.G, &nt, &nrg);
-    e = launch_group_nt<D, false>(nt, tmK, tmV, p, dim3(nrg * mp.nclus * mp.cluster, a.Hkv, a.B),
-                                  launch_overlap() != 0, stream);
+    const int G = a.Hq / a.Hkv;
+    if (use_multi_tc(D, q_len, G)) {
+        mtc::Params tp;
+        tp.q = a.q;
+        tp.block_table = a.block_table;
+        tp.context_lens = a.context_lens;
+        tp.out = a.out;
+        tp.part_ml = parts ? part_ml : nullptr;
+        tp.part_acc = part_acc;
+        tp.err = a.err;
+        tp.B = a.B;
+        tp.max_blocks = a.max_blocks;
+        tp.num_blocks = a.num_blocks;
+        tp.Hq = a.Hq;
+        tp.Hkv = a.Hkv;
+        tp.G = G;
+        tp.q_len = q_len;
+        tp.max_ctx = a.max_context_len;
+        tp.out_f32 = a.out_f32;
+        tp.chunk = mp.chunk;
+        tp.cs = mp.cluster;
+        tp.nclus = mp.nclus;
+        tp.part_stride = mp.nclus;
+        tp.scale_log2 = a.scale * kLog2e;
+        e = mtc::launch(tmK, tmV, tp, q_len * G, launch_overlap() != 0, stream);
+    } else {
+        GroupKernelParams p = group_params(a, parts ? part_ml : nullptr, part_acc);
+        p.q_len = q_len;
+        p.chunk = mp.chunk;
+        p.cs = mp.cluster;
+        p.nclus = mp.nclus;
+        p.part_stride = mp.nclus;
+        int nt, nrg;
+        group_tiles(D, q_len * p.G, &nt, &nrg);
+        e = launch_group_nt<D, false>(nt, tmK, tmV, p, dim3(nrg * mp.nclus * mp.cluster, a.Hkv, a.B),
+                                      launch_overlap() != 0, stream);
+    }
     if (e != cudaSuccess || !parts) return e;
     // several clusters per context: merge their partial states
     CombineParams c;

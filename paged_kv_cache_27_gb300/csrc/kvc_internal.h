@@ -107,6 +107,8 @@ cudaError_t cascade_plan(int B, int Hq, int Hkv, int D, int max_context_len, int
                          CascadePlan* plan);
 // process-wide: cascade calls saving fewer block reads per KV head than this run the plain decode
 void set_cascade_min_saved_blocks(int blocks);
+// process-wide: multi-token calls at head dim 64 on the tensor-core kernel (multi_tc.cu) instead of mma.sync
+void set_multi_tc(int on);
 // group_start: device [n_groups + 1]; shared_blocks: device [B], the shared blocks of each sequence's group
 cudaError_t launch_cascade(const DecodeArgs& a, const int32_t* group_start, const int32_t* shared_blocks,
                            int n_groups, int max_shared_blocks, cudaStream_t stream);

@@ -129,3 +129,50 @@ def test_multi_token_bad_inputs_flagged_without_faulting():
     assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["BLOCK_ID"]
     assert torch.isfinite(out2).all()
     check_attention(out2[1:].reshape(-1, wl.Hq, wl.D), ref[1:].reshape(-1, wl.Hq, wl.D), "multi-token, other rows")
+
+
+TC_CASES = [i for i, c in enumerate(CASES) if c[5] == 64 and c[2] >= 2 and c[2] * (c[3] // c[4]) <= 64]
+
+
+@pytest.mark.parametrize("case", TC_CASES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_multi_token_tensor_core_kernel_matches_oracle(case, out_dtype):
+    """The opt-in tensor-core multi-token kernel (keys as the products' M side, query rows as N) on the same cases:
+    several row counts (14 to 64), contexts at block and tile edges, several clusters per context, poisoned pools."""
+    import paged_kv_cache_27_gb300 as kvc
+    seed, ctx, T, Hq, Hkv, D = CASES[case]
+    wl = workloads.multi_token_decode(seed, ctx, T, Hq=Hq, Hkv=Hkv, D=D)
+    kvc.kvc_set_multi_tc(True)
+    try:
+        out = run_multi(wl, out_dtype, checked=(case % 2 == 1))[0]
+    finally:
+        kvc.kvc_set_multi_tc(False)
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref = oracle.decode_multi(wl.q, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+    check_attention(out.reshape(-1, Hq, D), ref.reshape(-1, Hq, D), f"multi-token (tensor cores) case {case}")
+
+
+def test_multi_token_tensor_core_kernel_bad_inputs():
+    """The tensor-core kernel with a short context (zero rows, flagged) and an out-of-range block id (skipped,
+    flagged, outputs finite) over several clusters per context."""
+    import paged_kv_cache_27_gb300 as kvc
+    kvc.kvc_device_error_flags(clear=True)
+    kvc.kvc_set_multi_tc(True)
+    try:
+        wl = workloads.multi_token_decode(13, [20000, 5000, 700], 3)
+        ctx = np.array(wl.ctx, np.int32)
+        ctx[1] = 2
+        out = run_multi(wl, ctx=ctx)[0]
+        assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["CONTEXT"]
+        assert torch.all(out[1] == 0)
+        ref = oracle.decode_multi(wl.q, wl.k_pool, wl.v_pool, wl.block_table, wl.ctx, wl.scale)
+        check_attention(out[0].reshape(-1, wl.Hq, wl.D), ref[0].reshape(-1, wl.Hq, wl.D), "tensor cores, long context")
+        check_attention(out[2].reshape(-1, wl.Hq, wl.D), ref[2].reshape(-1, wl.Hq, wl.D), "tensor cores, third")
+        bad_table = wl.block_table.copy()
+        bad_table[0, 3] = -5
+        out2 = run_multi(dataclasses.replace(wl, block_table=bad_table))[0]
+        assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["BLOCK_ID"]
+        assert torch.isfinite(out2).all()
+        check_attention(out2[1:].reshape(-1, wl.Hq, wl.D), ref[1:].reshape(-1, wl.Hq, wl.D), "tensor cores, others")
+    finally:
+        kvc.kvc_set_multi_tc(False)
