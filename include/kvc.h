@@ -300,7 +300,10 @@ kvc_status paged_decode_cascade_attention(const void* q, const void* k_cache, co
  *   workspace     device, 16-byte aligned, >= paged_decode_multi_plan's bytes
  * Other arguments as in paged_decode_attention; the new tokens' K/V must be
  * in the cache already (kv_append with their slots).  Each block is read
- * once for all q_len tokens.  One kernel launch where a thread-block cluster
+ * once for all q_len tokens.  The softmax weights multiply V in fp16 and the
+ * row sums add the same rounded weights, so every output row is an exact
+ * convex combination of V rows with weights off by at most 2^-11 relative
+ * (the prefill's default form); the single-token decode keeps ~fp32 weights.  One kernel launch where a thread-block cluster
  * covers the longest context (the plan's workspace is then 0 bytes), else two
  * (partial states per cluster, then their merge). */
 kvc_status paged_decode_multi_plan(int B, int Hq, int Hkv, int head_dim, int block_size, int max_context_len,

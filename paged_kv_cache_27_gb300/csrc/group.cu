@@ -44,6 +44,13 @@ namespace kvc {
 #ifndef KVC_MULTI_EARLY_REFILL  // 1: refill a stage once its V fragments are in registers, before the softmax
 #define KVC_MULTI_EARLY_REFILL 1
 #endif
+// Multi-token calls: 1 = the P V products take P as an fp16 high part plus an fp16 residual (~fp32 weights, twice
+// the products); 0 = P in fp16 with the sums over the rounded weights (the prefill's default form), measured on the
+// 24-layer graph at 32 x 2048: T = 2 / 4 / 8 8.43 / 12.0 / 18.7 -> 7.94 / 11.1 / 16.9 us per layer.  The cascade's
+// prefix pass always splits P: it re-associates the plain decode's sum, and stays within 1e-5 of it.
+#ifndef KVC_MULTI_P_SPLIT
+#define KVC_MULTI_P_SPLIT 0
+#endif
 #ifndef KVC_MULTI_CTAS  // CTAs per SM the chunking aims for (one where a CTA needs the SM's registers)
 #define KVC_MULTI_CTAS 2
 #endif
@@ -119,6 +126,7 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
                               const GroupKernelParams p) {
     using C = GroupCfg<D, NT>;
     constexpr int NW = C::kWarps, ST = C::kStages, RG = C::RG;
+    constexpr bool kSplitP = kPrefix || KVC_MULTI_P_SPLIT;  // P as high part + residual (see KVC_MULTI_P_SPLIT)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int cs = p.cs;
@@ -395,15 +403,22 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
                     p1 = mn1 == -INFINITY ? 0.f : ex2(x1 - mn1);
                     p3 = mn1 == -INFINITY ? 0.f : ex2(x3 - mn1);
                 }
-                l_run[nt][0] += p0 + p2;
-                l_run[nt][1] += p1 + p3;
-                // P^T as the B operand: fp16 high part and fp16 residual
+                // P^T as the B operand in fp16 (split: plus the fp16 residual as a second operand)
                 const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
                 const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
                 bh[nt][0] = movmatrix_trans(h01);
                 bh[nt][1] = movmatrix_trans(h23);
-                bl[nt][0] = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
-                bl[nt][1] = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+                if constexpr (kSplitP) {
+                    l_run[nt][0] += p0 + p2;
+                    l_run[nt][1] += p1 + p3;
+                    bl[nt][0] = movmatrix_trans(pack_half2(p0 - f01.x, p1 - f01.y));
+                    bl[nt][1] = movmatrix_trans(pack_half2(p2 - f23.x, p3 - f23.y));
+                } else {
+                    // the sums take the rounded weights that multiply V, so each output row stays an exact convex
+                    // combination of V rows (weights off by at most 2^-11 relative)
+                    l_run[nt][0] += f01.x + f23.x;
+                    l_run[nt][1] += f01.y + f23.y;
+                }
             }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
@@ -420,7 +435,7 @@ __global__ void __launch_bounds__(GroupCfg<D, NT>::kThreads, GroupCfg<D, NT>::kM
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     mma_f16_16816(o[nt][mt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                    mma_f16_16816(o[nt][mt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    if constexpr (kSplitP) mma_f16_16816(o[nt][mt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
                 }
             }
         }
