@@ -1068,7 +1068,8 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
         const int smem = C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split);
         c.early_release = 0;
         if (!fp8 && decode_occupancy<D>(smem, &occ) == cudaSuccess)
-            c.early_release = 2 * static_cast<int64_t>(grid.x) * grid.y * grid.z <= static_cast<int64_t>(occ) * sm_count();
+            c.early_release = KVC_COMBINE_EARLY_ALWAYS ||
+                              2 * static_cast<int64_t>(grid.x) * grid.y * grid.z <= static_cast<int64_t>(occ) * sm_count();
         e = launch(paged_decode_combine_kernel<D>, dim3(a.Hq, a.B), dim3(256), 0, stream, true, 1u, c);
     }
     return e;

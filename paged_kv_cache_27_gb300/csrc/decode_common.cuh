@@ -48,6 +48,9 @@ namespace kvc {
 #ifndef KVC_COMBINE_EARLY_TRIGGER  // the split combine kernel lets the next kernel launch as soon as it starts
 #define KVC_COMBINE_EARLY_TRIGGER 1
 #endif
+#ifndef KVC_COMBINE_EARLY_ALWAYS  // 1: the combine releases the next launch at its start whatever the grid's size
+#define KVC_COMBINE_EARLY_ALWAYS 0
+#endif
 #ifndef KVC_GROUP_EARLY_TRIGGER  // the group kernel lets the next kernel launch as soon as it starts
 #define KVC_GROUP_EARLY_TRIGGER 1
 #endif
