@@ -63,8 +63,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "c6d39e09772c6b34146d4bee946a05efad0575f355560fc7a3012b99f47d6c53",
-                      "bytes_per_launch": 33676416}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "0ee538cf43f70d165ae7649e039bbf45f1fb19c59da1d362eb1255936a19bf6a",
+                      "bytes_per_launch": 33681792}
 
 
 def decode_sources_sha256() -> str:

@@ -69,6 +69,7 @@ struct DecodeKernelParams {
     int part_base, part_stride;
     const int32_t* blk_off;  // suffix pass: per sequence, the leading blocks of its table row attended elsewhere
     int out_f32;
+    int len_order;  // 1: the CTAs at position z along the sequences take the z-th longest context
     float scale_log2;
     unsigned trace_seq;  // launch counter, used by the optional trace only
 };
@@ -144,7 +145,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
     const int g = lane >> 2, t4 = lane & 3;
     // a KV head's G query heads go in chunks of at most 8 (the mma tiles' 8 columns) to consecutive CTAs along y,
     // which read the same K/V blocks at about the same time (the second read is mostly an L2 hit)
-    const int kvh = blockIdx.y / p.hchunks, hc = blockIdx.y - kvh * p.hchunks, b = blockIdx.z;
+    __shared__ int s_len_hist[33];
+    __shared__ uint8_t s_len_cls[kLenOrderMaxB];
+    const int kvh = blockIdx.y / p.hchunks, hc = blockIdx.y - kvh * p.hchunks;
+    const int b = p.len_order ? seq_by_length(p.context_lens, p.B, p.max_ctx, static_cast<int>(blockIdx.z),
+                                              s_len_hist, s_len_cls, s_len_hist + 32)
+                              : static_cast<int>(blockIdx.z);
     const int Gc = min(8, p.G - hc * 8);  // query heads of this CTA
     const int h0 = kvh * p.G + hc * 8;    // its first query head
     // the cluster's slice of the block table (bpc entries), after the inbox's cluster - 1 slots
@@ -1007,10 +1013,22 @@ static DecodeKernelParams decode_params(const DecodeArgs& a, const DecodePlan& p
     p.blk_off = nullptr;
     p.kv_fp8 = a.kv_fp8;
     p.out_f32 = a.out_f32;
+    p.len_order = 0;
     p.scale_log2 = a.scale * kLog2e;
     static std::atomic<unsigned> launch_seq{0};
     p.trace_seq = launch_seq.fetch_add(1);
     return p;
+}
+
+// 1 where the grid has more CTAs than can be resident at once (several waves): the kernel then dispatches the
+// longest contexts first
+template <int D>
+static int len_order_for(const DecodeArgs& a, const DecodePlan& plan, int hchunks, int smem) {
+    if (!KVC_DEC_LEN_ORDER || a.B < 2 || a.B > kLenOrderMaxB) return 0;
+    int occ = 0;
+    if (decode_occupancy<D>(smem, &occ) != cudaSuccess) return 0;
+    const int64_t ctas = static_cast<int64_t>(plan.num_splits) * a.Hkv * hchunks * a.B;
+    return ctas > static_cast<int64_t>(occ) * sm_count() ? 1 : 0;
 }
 
 template <int D>
@@ -1032,9 +1050,13 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, const DecodePlan& plan, 
 
     const size_t nrow = static_cast<size_t>(a.B) * a.Hq * plan.num_parts;
     float* part_ml = plan.num_parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    const DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
+    DecodeKernelParams p = decode_params(a, plan, part_ml, part_ml ? partials_acc(part_ml, nrow) : nullptr);
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     dim3 grid(plan.num_splits, a.Hkv * p.hchunks, a.B);
+    p.len_order = len_order_for<D>(a, plan, p.hchunks,
+                                   fp8 ? DecodeCfg<D, true>::smem_bytes(plan.cluster, std::min(p.G, 8),
+                                                                        plan.blocks_per_split)
+                                       : C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split));
     if (fp8)
         e = launch(paged_decode_kernel<D, false, true>, grid, dim3(DecodeCfg<D, true>::kThreads),
                    DecodeCfg<D, true>::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split), stream, pdl,
@@ -1111,6 +1133,8 @@ static cudaError_t launch_suffix_d(const DecodeArgs& a, const DecodePlan& plan, 
     p.blk_off = blk_off;
     p.part_base = part_base;
     p.part_stride = part_stride;
+    p.len_order = len_order_for<D>(a, plan, p.hchunks, C::smem_bytes(plan.cluster, std::min(p.G, 8),
+                                                                     plan.blocks_per_split));
     const bool pdl = g_launch_overlap.load(std::memory_order_relaxed) != 0;
     return launch(paged_decode_kernel<D, true>, dim3(plan.num_splits, a.Hkv * p.hchunks, a.B), dim3(C::kThreads),
                   C::smem_bytes(plan.cluster, std::min(p.G, 8), plan.blocks_per_split), stream, pdl,

@@ -94,6 +94,16 @@ namespace kvc {
 #define KVC_DEC_LAZY_MAX 8
 #endif
 
+// Plans of several waves (more CTAs than can be resident): the CTAs at position z along the sequences take the
+// z-th longest context, so that the long contexts start in the first wave and the short ones fill the tail
+// (longest-processing-time-first list scheduling; CTAs are dispatched in the order of their linear index).
+// B = 200 sequences of 16..4096 tokens, 14 q / 2 KV heads: 41.5 -> 36.9 us per call with the batch itself
+// sorted.  0: sequence z.
+#ifndef KVC_DEC_LEN_ORDER
+#define KVC_DEC_LEN_ORDER 1
+#endif
+constexpr int kLenOrderMaxB = 1024;  // batches up to this size (the order costs two warp passes over B lengths)
+
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = KVC_DEC_MAX_CLUSTER;
@@ -160,6 +170,59 @@ __device__ __forceinline__ float4 fma4(float w, float4 a, float4 acc) {
     return make_float4(fmaf(w, a.x, acc.x), fmaf(w, a.y, acc.y), fmaf(w, a.z, acc.z), fmaf(w, a.w, acc.w));
 }
 __device__ __forceinline__ float4 scale4(float4 a, float s) { return make_float4(a.x * s, a.y * s, a.z * s, a.w * s); }
+
+// The sequence at position z (0 <= z < B <= kLenOrderMaxB) of the order "longer length class first, then lower
+// index", over 32 classes of about max_ctx / 32 tokens (longest: class 31).  Every thread of the CTA calls it
+// (it holds two CTA barriers); the answer depends on the lengths alone, so every CTA computes the same order and
+// z -> sequence is a permutation of [0, B) whatever the lengths hold (out-of-range lengths are clamped into a
+// class; the kernel reports them as before).  Shared scratch: hist 32 ints, cls B bytes, one int for the answer.
+__device__ inline int seq_by_length(const int32_t* __restrict__ lens, int B, int max_ctx, int z, int* hist,
+                                    uint8_t* cls, int* answer) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    // class = floor(len * 32 / (max_ctx + 1)) in float: monotone in len and the same in every CTA
+    const float per_token = 32.f / (static_cast<float>(max_ctx) + 1.f);
+    if (threadIdx.x < 32) hist[threadIdx.x] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < B; j += blockDim.x) {
+        const int len = min(max(lens[j], 0), max_ctx);
+        const int c = min(31, static_cast<int>(static_cast<float>(len) * per_token));
+        cls[j] = static_cast<uint8_t>(c);
+        atomicAdd(&hist[c], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        // lane i counts class 31 - i: the inclusive scan over the lanes ends at each class's last position + 1
+        const int c = hist[31 - lane];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const unsigned hit = __ballot_sync(full, z >= incl - c && z < incl);
+        int seq = min(max(z, 0), B - 1);  // z outside [0, B): not a launch this kernel makes
+        if (hit != 0) {
+            const int src = __ffs(hit) - 1;
+            const int want = 31 - src;
+            int r = z - __shfl_sync(full, incl - c, src);  // rank within the class, by index
+            for (int j0 = 0; j0 < B; j0 += 32) {
+                const int j = j0 + lane;
+                unsigned m = __ballot_sync(full, j < B && cls[j] == want);
+                const int n = __popc(m);
+                if (r < n) {
+                    for (int k = 0; k < r; ++k) m &= m - 1;
+                    seq = j0 + __ffs(m) - 1;
+                    break;
+                }
+                r -= n;
+            }
+        }
+        if (lane == 0) *answer = seq;
+    }
+    __syncthreads();
+    return *answer;
+}
 
 // ---- host helpers ------------------------------------------------------------------------------------
 inline int sm_count() {

@@ -159,6 +159,40 @@ def test_workspace_reuse_across_context_lengths(kvc):
     s.close()
 
 
+def _permuted(wl, perm):
+    """The same sequences in the order perm (history repacked, physical blocks unchanged)."""
+    import dataclasses
+    off = wl.hist_off
+    ctx = wl.ctx[perm]
+    hist_off = np.zeros(wl.B + 1, dtype=np.int64)
+    hist_off[1:] = np.cumsum(ctx.astype(np.int64) - 1)
+    k = np.concatenate([wl.k_hist[:, off[i]:off[i + 1]] for i in perm], axis=1)
+    v = np.concatenate([wl.v_hist[:, off[i]:off[i + 1]] for i in perm], axis=1)
+    return dataclasses.replace(wl, ctx=ctx, block_table=wl.block_table[perm], hist_off=hist_off, k_hist=k, v_hist=v,
+                               q=wl.q[:, perm], k_new=wl.k_new[:, perm], v_new=wl.v_new[:, perm])
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_several_waves_longest_first(kvc, fused):
+    """400 sequences x 2 KV heads: more CTAs than the GPU holds at once, so they take the sequences longest
+    first.  Ragged lengths with ties, single tokens and the longest; every output and cache row against the
+    oracle, and the same sequences in another order give the reordered outputs bit for bit."""
+    rng = np.random.default_rng(5)
+    ctx = rng.integers(1, 700, size=400)
+    ctx[::9] = 1
+    ctx[::7] = 350
+    ctx[5] = ctx[123] = 700
+    wl = workloads.small_decode(4040, B=400, Hq=14, Hkv=2, D=64, ctx=ctx.tolist())
+    check_workload(kvc, wl, torch.float16, fused=fused, graph=True, overlap=True)
+    s1 = run_session(kvc, wl, torch.float16, fused=fused)
+    perm = np.random.default_rng(6).permutation(wl.B)
+    s2 = run_session(kvc, _permuted(wl, perm), torch.float16, fused=fused)
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    assert torch.equal(s2.out[0], s1.out[0][torch.from_numpy(perm).to(s1.out.device)])
+    s1.close()
+    s2.close()
+
+
 def test_results_invariant_to_physical_placement(kvc):
     """Same logical data under two block permutations gives bit-identical outputs."""
     from paged_kv_cache_27_gb300.harness import DecodeSession
