@@ -793,7 +793,7 @@ def run_suite(args):
     if args.suite_part in ("all", "decode"):
         run_suite_decode(device, stream, flush, emit, peak)
     elif args.suite_part == "multi":
-        run_suite_multi(device, stream, flush, emit, peak)
+        run_suite_multi(device, stream, flush, emit, peak, args.suite_multi_t)
     elif args.suite_part == "cascade":
         run_suite_cascade(device, stream, flush, emit, peak)
     if args.suite_part in ("all", "prefill"):
@@ -953,7 +953,7 @@ def run_suite_cascade(device, stream, flush, emit, peak, mix=None, res=None):
     del ckp, cvp
 
 
-def run_suite_multi(device, stream, flush, emit, peak):
+def run_suite_multi(device, stream, flush, emit, peak, only_t=0):
     import torch
     import paged_kv_cache_27_gb300 as kvc
 
@@ -966,7 +966,7 @@ def run_suite_multi(device, stream, flush, emit, peak):
     kml = [kpm0] + [torch.randn(kpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
     vml = [vpm0] + [torch.randn(vpm0.shape, generator=genm, device=device).half() for _ in range(Lm - 1)]
     nbytes = 32 * 2048 * 2 * 2 * 64 * 2
-    for T in (1, 2, 3, 4, 8):
+    for T in ((only_t,) if only_t else (1, 2, 3, 4, 8)):
         qms = [torch.randn((32, T, 14, 64), generator=genm, device=device).half() for _ in range(Lm)]
         om = torch.empty((32, T, 14, 64), dtype=torch.float16, device=device)
         wsm = torch.zeros(max(kvc.paged_decode_multi_plan(32, 14, 2, 64, 2048, T), 16), dtype=torch.uint8,
@@ -1052,9 +1052,13 @@ def main():
     ap.add_argument("--suite-part", choices=["all", "decode", "prefill", "multi", "cascade"], default="all",
                     help="decode: every decode configuration (multi-token and cascade included); multi / cascade: "
                          "those lines only")
+    ap.add_argument("--suite-multi-t", type=int, default=0,
+                    help="with --suite-part multi: only this number of new tokens per sequence (1..8)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not 0 <= args.suite_multi_t <= 8:
+        ap.error("--suite-multi-t must be in 1..8 (0: every listed T)")
     if args.impl == "reference":
         return run_reference(args)
     if args.suite:

@@ -41,6 +41,9 @@ namespace kvc {
 #ifndef KVC_MULTI_MAX_TILES64  // n-tiles per warp at most, head_dim 64 (more rows make more row groups)
 #define KVC_MULTI_MAX_TILES64 2
 #endif
+#ifndef KVC_MULTI_TWO_CTA_TILES  // head_dim 64: n-tiles per warp up to which a CTA is sized for two CTAs per SM
+#define KVC_MULTI_TWO_CTA_TILES 2
+#endif
 #ifndef KVC_MULTI_EARLY_REFILL  // 1: refill a stage once its V fragments are in registers, before the softmax
 #define KVC_MULTI_EARLY_REFILL 1
 #endif
@@ -79,9 +82,12 @@ struct GroupCfg {
     static constexpr int kWarps = KVC_MULTI_WARPS;
     static constexpr int kThreads = kWarps * 32;
     // resident CTAs per SM the register allocation must allow
-    static constexpr int kMinCtas = D == 64 && NT <= 2 ? 2 : 1;
+    static constexpr int kMinCtas = D == 64 && NT <= KVC_MULTI_TWO_CTA_TILES ? 2 : 1;
+    // (two CTAs per SM with 4 n-tiles: 3 stages, so that the parked state fits a warp's ring)
     static constexpr int kStages =
-        D == 64 ? (kMinCtas == 2 ? KVC_MULTI_STAGES64 : KVC_MULTI_STAGES64_WIDE) : KVC_MULTI_STAGES128;
+        D == 64 ? (kMinCtas == 2 ? (NT == 4 && KVC_MULTI_STAGES64 < 3 ? 3 : KVC_MULTI_STAGES64)
+                                 : KVC_MULTI_STAGES64_WIDE)
+                : KVC_MULTI_STAGES128;
     static constexpr int RG = 8 * NT;  // query rows of a CTA
     static constexpr int kTileBytes = kBlockSize * D * 2;
     static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
@@ -598,7 +604,7 @@ static void group_tiles(int D, int R, int* nt, int* nrg) {
 // number of blocks; the chunks of a unit form one cluster where they fit one, else clusters of the largest size
 static void group_chunks(int D, int nt, int64_t units, int64_t nblk, int sms, int* chunk, int* cluster, int* nclus) {
     const int nw = KVC_MULTI_WARPS;
-    const int per_sm = D == 64 && nt <= 2 ? KVC_MULTI_CTAS : 1;
+    const int per_sm = D == 64 && nt <= KVC_MULTI_TWO_CTA_TILES ? KVC_MULTI_CTAS : 1;
     const int64_t per_unit = std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sms / std::max<int64_t>(1, units));
     int64_t c = (std::max<int64_t>(1, nblk) + per_unit - 1) / per_unit;
     c = (c + nw - 1) / nw * nw;
@@ -720,7 +726,9 @@ cudaError_t multi_plan(int B, int Hq, int Hkv, int D, int max_ctx, int q_len, Mu
     group_tiles(D, q_len * (Hq / Hkv), &nt, &nrg);
     const int64_t nblk = std::max((max_ctx + kBlockSize - 1) / kBlockSize, 1);
     group_chunks(D, nt, static_cast<int64_t>(B) * Hkv * nrg, nblk, sms, &plan->chunk, &plan->cluster, &plan->nclus);
-    plan->stages = D == 64 ? (nt <= 2 ? KVC_MULTI_STAGES64 : KVC_MULTI_STAGES64_WIDE) : KVC_MULTI_STAGES128;
+    plan->stages = D != 64 ? KVC_MULTI_STAGES128
+                   : nt > KVC_MULTI_TWO_CTA_TILES ? KVC_MULTI_STAGES64_WIDE
+                   : nt == 4 && KVC_MULTI_STAGES64 < 3 ? 3 : KVC_MULTI_STAGES64;
     plan->workspace_bytes =
         plan->nclus > 1 ? partials_bytes(static_cast<size_t>(B) * q_len * Hq * plan->nclus, D) : 0;
     if (q_len == 1) {  // a single new token is the plain decode
