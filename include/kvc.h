@@ -361,8 +361,11 @@ kvc_status kv_append_fp8(const void* k_new, const void* v_new, const int64_t* sl
 /* paged_decode_attention over an fp8 cache (kv_fp8: the layer's records):
  * the same result definition with every cached value code value * scale;
  * workspace as paged_decode_plan's.  Codes convert to fp16 exactly; the K
- * scale multiplies the scores and the V scale the probabilities in fp32, so
- * the arithmetic matches the fp16 kernel's. */
+ * scale multiplies the scores in fp32; each probability times its V scale
+ * multiplies V as one fp16 value, and the softmax sums add each rounded
+ * value times the reciprocal of its scale, so every output row is a convex
+ * combination of the dequantized V rows with weights within 2^-11 relative
+ * of the exact ones. */
 kvc_status paged_decode_attention_fp8(const void* q, const void* kv_fp8, int num_blocks, const int32_t* block_table,
                                       int max_blocks, const int32_t* context_lens, int B, int Hq, int Hkv,
                                       int head_dim, int block_size, int max_context_len, float scale, void* out,

@@ -516,16 +516,26 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                 }
                 const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]), p2 = ex2(x[2] - m_run[0]),
                             p3 = ex2(x[3] - m_run[1]);
-                l_run[0] += p0 + p2;
-                l_run[1] += p1 + p3;
                 // P^T as the B operand (k = tokens, n = heads): transpose the two 8x8 halves in registers;
                 // P = hi + lo, both fp16, so the P V product keeps ~fp32 accuracy
                 const float q0 = p0 * vsg, q1 = p1 * vsg, q2 = p2 * vsg8, q3 = p3 * vsg8;
                 const uint32_t h01 = pack_half2(q0, q1), h23 = pack_half2(q2, q3);
                 const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
                 const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-                const uint32_t bl0 = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
-                const uint32_t bl1 = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
+                constexpr bool kOneP = kFp8 && KVC_DEC_FP8_ONE_P;
+                uint32_t bl0 = 0, bl1 = 0;
+                if constexpr (kOneP) {
+                    // one fp16 operand q = p x scale: the sums take each rounded q back over its scale (a key with
+                    // a zero scale, an all-zero row, still counts its weight p)
+                    const float r = rcp_approx(vsg), r8 = rcp_approx(vsg8);
+                    l_run[0] += (vsg > 0.f ? f01.x * r : p0) + (vsg8 > 0.f ? f23.x * r8 : p2);
+                    l_run[1] += (vsg > 0.f ? f01.y * r : p1) + (vsg8 > 0.f ? f23.y * r8 : p3);
+                } else {
+                    l_run[0] += p0 + p2;
+                    l_run[1] += p1 + p3;
+                    bl0 = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
+                    bl1 = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
+                }
                 // ---- O^T += V^T P^T, one m-tile per 16 dims ----
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
@@ -540,7 +550,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
                     }
 #endif
                     mma_f16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+                    if constexpr (!kOneP) mma_f16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
                 }
             }
             if (!refilled) refill(s);

@@ -21,6 +21,14 @@ namespace kvc {
 #ifndef KVC_DEC_STAGES64
 #define KVC_DEC_STAGES64 2
 #endif
+// fp8 cache: 1 = the P V products take each weight times its V scale as one fp16 operand, and the row sums add
+// each rounded weight times the reciprocal of its scale (so every output row stays a convex combination of the
+// dequantized V rows, weights within 2^-11 relative); 0 = an fp16 high part plus residual, two products per tile.
+// Measured (two A/B pairs, one call with L2 flushed): B = 16 x 65536 67.6 -> 65.5 us, B = 4 x 131072 41.0 ->
+// 38.9-39.6 us; the 24-layer 32 x 2048 graph unchanged (6.61 -> 6.59 us per layer).
+#ifndef KVC_DEC_FP8_ONE_P
+#define KVC_DEC_FP8_ONE_P 1
+#endif
 #ifndef KVC_DEC_STAGES64_FP8  // stages per warp with an fp8 cache (a stage is half the bytes)
 #define KVC_DEC_STAGES64_FP8 2
 #endif

@@ -160,6 +160,12 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 1 / x to about 1 ulp (the hardware's approximate reciprocal)
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Two e4m3 codes (low byte first) -> f16x2 (low half first); exact, every e4m3 value is an fp16 value.
 __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
