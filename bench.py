@@ -63,8 +63,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "0ee538cf43f70d165ae7649e039bbf45f1fb19c59da1d362eb1255936a19bf6a",
-                      "bytes_per_launch": 33681792}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "8abceccdc0d12edb19457245e4dd113630961cdd00a639290d07ced854502608",
+                      "bytes_per_launch": 33681920}
 
 
 def decode_sources_sha256() -> str:
@@ -821,8 +821,13 @@ def run_suite_decode(device, stream, flush, emit, peak):
           "us_per_step": us, "tokens_per_s": c3["tokens"] / (us * 1e-6),
           "logical_GBps": logical / (us * 1e-6) / 1e9, "unique_GBps": unique / (us * 1e-6) / 1e9,
           "logical_bytes": logical, "unique_bytes": unique, "pct_hbm_peak_unique": unique / (us * 1e-6) / 1e9 / peak * 100,
+          "us_per_layer_graph24": c3["us_step_graph24"],
+          "unique_GBps_graph24": unique / (c3["us_step_graph24"] * 1e-6) / 1e9,
+          "pct_hbm_peak_unique_graph24": unique / (c3["us_step_graph24"] * 1e-6) / 1e9 / peak * 100,
+          "us_decode_plain": c3["us_decode_plain"],
           "note": "fused append + decode per step, L2 flushed before each step; shared prefix blocks are read "
-                  "once per sequence (logical) but may hit in L2 (unique = distinct blocks)"})
+                  "once per sequence (logical) but may hit in L2 (unique = distinct blocks); graph24: the step as "
+                  "the 24 layers of a CUDA graph, each on its own pools, L2 flushed per replay"})
 
     run_suite_cascade(device, stream, flush, emit, peak)
 

@@ -193,6 +193,15 @@ def test_several_waves_longest_first(kvc, fused):
     s2.close()
 
 
+def test_several_waves_wide_groups(kvc):
+    """160 sequences, 16 query heads per KV head (two head chunks per KV head): 640 CTAs, dispatched longest
+    context first, against the oracle."""
+    ctx = np.random.default_rng(8).integers(1, 500, size=160)
+    ctx[::5] = 250
+    wl = workloads.small_decode(4041, B=160, Hq=32, Hkv=2, D=64, ctx=ctx.tolist())
+    check_workload(kvc, wl, torch.float32, fused=True)
+
+
 def test_results_invariant_to_physical_placement(kvc):
     """Same logical data under two block permutations gives bit-identical outputs."""
     from paged_kv_cache_27_gb300.harness import DecodeSession

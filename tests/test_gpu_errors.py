@@ -77,6 +77,33 @@ def test_unchecked_bad_inputs_set_device_flags_without_faulting(kvc):
     s.close()
 
 
+def test_bad_contexts_in_a_several_wave_batch(kvc):
+    """400 ragged sequences (more CTAs than the GPU holds, dispatched longest first) with two bad context
+    lengths: those two rows come out zero with the context flag set, every other row matches the oracle."""
+    from oracle import paging as opaging
+    from parity import check_attention
+    ctx = np.random.default_rng(11).integers(1, 300, size=400)
+    wl = workloads.small_decode(12, B=400, Hq=14, Hkv=2, D=64, ctx=ctx.tolist())
+    s = session(wl)
+    s.step()
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    ref, _, _ = opaging.decode_step(wl, 0)
+    bad_ctx = s.context_lens.clone()
+    bad_ctx[7] = 0
+    bad_ctx[300] = s.max_ctx + 100
+    out = torch.full_like(s.out[0], 5.0)
+    kvc.paged_decode_attention(s.q[0], s.k_pool[0], s.v_pool[0], s.block_table, bad_ctx, wl.scale, out,
+                               s.workspace, s.max_ctx)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) & kvc.DEVERR["CONTEXT"]
+    assert (out[7] == 0).all() and (out[300] == 0).all()
+    keep = np.ones(400, dtype=bool)
+    keep[[7, 300]] = False
+    check_attention(out[torch.from_numpy(keep).cuda()], ref[keep], "several-wave batch, good rows")
+    s.close()
+
+
 def test_argument_errors(kvc):
     wl = workloads.small_decode(3, B=2, Hq=4, Hkv=2, D=64, ctx=[20, 300])
     s = session(wl)

@@ -119,6 +119,8 @@ CASES = [
     (6, [40000, 5000, 1], 14, 2, 64, 0),
     (7, [129, 2000], 16, 2, 128, 2),
     (8, [3, 900, 5000], 48, 2, 64, 0),  # 24 query heads per KV head: three chunks of 8
+    # 400 ragged contexts: more CTAs than the GPU holds at once, dispatched longest context first
+    (9, [int(c) for c in np.random.default_rng(9).integers(1, 600, size=400)], 14, 2, 64, 0),
 ]
 
 
