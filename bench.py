@@ -779,6 +779,106 @@ def load_tflops_peak():
         return 1900.0, "fallback"
 
 
+def run_profile_configs(args):
+    """Each listed configuration's hot-path call four times (a warm-up call, then three with L2 flushed before
+    each): a short command for a per-configuration ncu launch list.  One configuration's buffers at a time (at most
+    ~2.2 GB on the device); prints one JSON line per configuration with the mean CUDA-event time of the three
+    flushed calls and the number of library kernels one call launches."""
+    import torch
+    import paged_kv_cache_27_gb300 as kvc
+    import workloads
+    from paged_kv_cache_27_gb300 import harness
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+    flush()  # the flush's own kernels load before the first timed call
+    torch.cuda.synchronize()
+
+    def once(name, fn, launches, algorithmic_bytes=None, flops=None, launches_before=0):
+        fn()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1) * 1e3
+        rec = {"profile_config": name, "us_mean_of_3": total / 3, "calls": 4, "kernels_per_call": launches,
+               "library_launches_before": launches_before}
+        if algorithmic_bytes is not None:
+            rec["algorithmic_bytes"] = algorithmic_bytes
+        if flops is not None:
+            rec["flops"] = flops
+        print(json.dumps(rec), flush=True)
+
+    # 1: single sequence at context 256, fused append + decode
+    wl = workloads.single_sequence_256()
+    sess = harness.DecodeSession(wl, device=device, out_dtype=torch.float32).fill()
+    once("1: single sequence, B=1, 1/1 heads, D=64, ctx 256",
+         lambda: kvc.paged_decode_append_attention(sess.q[0], sess.k_new[0], sess.v_new[0], sess.k_pool[0],
+                                                   sess.v_pool[0], sess.block_table, sess.context_lens, wl.scale,
+                                                   sess.out[0], sess.workspace, sess.max_ctx), 1,
+         algorithmic_bytes=256 * 2 * 64 * 2)
+    sess.close()
+    # 2: one layer of the 24-layer step (32 x 2048, 14 / 2 heads), fused append + decode
+    kp, vp, tb, ct, q, kn, vn = _decode_state(32, 2048, 14, 2, 64, device, seed=5)
+    o = torch.empty((32, 14, 64), dtype=torch.float16, device=device)
+    _, _, ws = kvc.paged_decode_plan(32, 14, 2, 64, 2048)
+    w = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+    once("2: one layer of the decode step, B=32, 14/2 heads, D=64, ctx 2048",
+         lambda: kvc.paged_decode_append_attention(q, kn, vn, kp, vp, tb, ct, 0.125, o, w, 2048), 1,
+         algorithmic_bytes=32 * 2048 * 512)
+    del kp, vp
+    # 3: the shared-prefix serving mix after its step's block management, fused append + decode
+    mix = workloads.shared_prefix_mix()
+    res = harness.serving_mix(mix, device=device, poison=False)
+    table = torch.from_numpy(res["block_table"]).to(device)
+    ctx = torch.from_numpy(mix.ctx).to(device)
+    q3 = torch.from_numpy(mix.q).to(device)
+    kn3, vn3 = torch.from_numpy(mix.k_new).to(device), torch.from_numpy(mix.v_new).to(device)
+    o3 = torch.empty((mix.B, mix.Hq, mix.D), dtype=torch.float16, device=device)
+    mc = int(mix.ctx.max())
+    ns3, _, ws3 = kvc.paged_decode_plan(mix.B, mix.Hq, mix.Hkv, mix.D, mc)
+    w3 = torch.zeros(max(ws3, 16), dtype=torch.uint8, device=device)
+    once("3: shared-prefix serving mix, B=200, 14/2 heads, D=64, ctx U{16..4096}",
+         lambda: kvc.paged_decode_append_attention(q3, kn3, vn3, res["k_cache"], res["v_cache"], table, ctx,
+                                                   mix.scale, o3, w3, mc), 1,
+         algorithmic_bytes=int(mix.ctx.astype(np.int64).sum()) * 512, launches_before=1)  # the mix's own step
+    del res
+    # 4: the long-context cells, fused append + decode
+    for B in (1, 4, 16):
+        for c in (4096, 16384, 65536, 131072):
+            kp, vp, tb, ct, q, kn, vn = _decode_state(B, c, 14, 2, 64, device, seed=B * 1000003 + c)
+            o = torch.empty((B, 14, 64), dtype=torch.float16, device=device)
+            ns, bps, ws = kvc.paged_decode_plan(B, 14, 2, 64, c)
+            w = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
+            nblk = -(-c // 16)
+            parts = -(-nblk // bps)
+            once(f"4: B={B}, ctx={c}, 14/2 heads, D=64",
+                 lambda: kvc.paged_decode_append_attention(q, kn, vn, kp, vp, tb, ct, 0.125, o, w, c),
+                 2 if parts > 1 else 1, algorithmic_bytes=B * c * 512)
+            del kp, vp, tb, ct, q, kn, vn, o, w
+            torch.cuda.empty_cache()
+    # 5: the two small prefills (causal)
+    for name, seqlens, Hq, Hkv in (("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal",
+                                    (37, 120, 8, 200), 8, 8),
+                                   ("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2)):
+        T = sum(seqlens)
+        gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
+        qq = torch.randn((T, Hq, 64), generator=gen, device=device).half()
+        kk = torch.randn((T, Hkv, 64), generator=gen, device=device).half()
+        vv = torch.randn((T, Hkv, 64), generator=gen, device=device).half()
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
+        oo = torch.empty((T, Hq, 64), dtype=torch.float16, device=device)
+        once(name, lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 0.125, True, oo), 1,
+             algorithmic_bytes=T * (Hq + 2 * Hkv) * 64 * 2,  # q, k and v read once (out written)
+             flops=4 * 64 * Hq * sum(s * (s + 1) // 2 for s in seqlens))
+
+
 def run_suite(args):
     import torch
 
@@ -1057,6 +1157,8 @@ def main():
     ap.add_argument("--suite-part", choices=["all", "decode", "prefill", "multi", "cascade"], default="all",
                     help="decode: every decode configuration (multi-token and cascade included); multi / cascade: "
                          "those lines only")
+    ap.add_argument("--profile-configs", action="store_true",
+                    help="each listed configuration's call once after a warm-up (a short command for ncu)")
     ap.add_argument("--suite-multi-t", type=int, default=0,
                     help="with --suite-part multi: only this number of new tokens per sequence (1..8)")
     args = ap.parse_args()
@@ -1068,6 +1170,8 @@ def main():
         return run_reference(args)
     if args.suite:
         return run_suite(args)
+    if args.profile_configs:
+        return run_profile_configs(args)
     return run_ours(args)
 
 
