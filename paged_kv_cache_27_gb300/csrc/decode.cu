@@ -970,6 +970,7 @@ static cudaError_t plan_d(int B, int Hq, int Hkv, int max_ctx, int bpc_req, Deco
             const int64_t want = (nblk + span - 1) / span;
             int64_t n = std::max(min_ncl, std::min(per_seg, want));
             if (n > 1 && kv_bytes < KVC_DEC_SMALL_BYTES) n = std::max(min_ncl, std::min((usable / 2) / segs, want));
+            if (n > 1 && c > KVC_DEC_SPLIT_MAX_CLUSTER) continue;  // a plan with the combine: smaller clusters
             ncl = n;
             cs = c;
             break;

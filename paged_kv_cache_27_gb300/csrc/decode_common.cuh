@@ -85,6 +85,13 @@ namespace kvc {
 #ifndef KVC_DEC_SMALL_BYTES
 #define KVC_DEC_SMALL_BYTES (int64_t(64) << 20)
 #endif
+// Largest cluster of a plan with several clusters per (sequence, KV head) (the combine merges their parts).
+// Measured against 8 (two A/B pairs; one call with L2 flushed / per layer of a 24-layer graph): B = 1 x 16384
+// 13.4 -> 12.3 / 6.93 -> 6.64 us, B = 1 x 131072 22.0 -> 20.7 / 17.2 -> 16.7, B = 4 x 16384 18.4 -> 16.5 /
+// 10.8 -> 9.9, B = 4 x 131072 55.9 -> 53.3 / 46.0 -> 45.2; plans of one cluster per unit keep clusters of 8.
+#ifndef KVC_DEC_SPLIT_MAX_CLUSTER
+#define KVC_DEC_SPLIT_MAX_CLUSTER 4
+#endif
 // 1: the CTAs of a cluster hand their merged states to rank 0 with st.async, whose bytes complete on an mbarrier
 // in rank 0 (senders leave at once); 0: remote stores, then a cluster barrier (release / acquire)
 #ifndef KVC_DEC_ASYNC_PUSH
