@@ -63,8 +63,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "8abceccdc0d12edb19457245e4dd113630961cdd00a639290d07ced854502608",
-                      "bytes_per_launch": 33681920}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "c62bfae3cd01adef3abce9ed6c989f5e4ae8094a27c64b48869ccbdcd99364b3",
+                      "bytes_per_launch": 33682048}
 
 
 def decode_sources_sha256() -> str:
