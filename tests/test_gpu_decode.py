@@ -202,6 +202,30 @@ def test_several_waves_wide_groups(kvc):
     check_workload(kvc, wl, torch.float32, fused=True)
 
 
+def _random_case(i):
+    """Seeded random decode shape: batch, heads (GQA groups 1..16), head dim, ragged contexts with ties and
+    single tokens, an explicit split size or the planner's, the fused or separate append, eager or graph."""
+    rng = np.random.default_rng(700 + i)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 7, 8, 12, 16] if D == 64 else [1, 2, 4, 8]))
+    B = int(rng.choice([1, 3, 17, 64, 180]))
+    hi = int(rng.choice([40, 600, 3000]))
+    ctx = rng.integers(1, hi + 1, size=B)
+    ctx[rng.random(B) < 0.1] = 1
+    ctx[rng.random(B) < 0.2] = hi
+    bps = int(rng.choice([0, 0, 0, 1, 7, 64]))
+    return dict(B=B, Hq=G * Hkv, Hkv=Hkv, D=D, ctx=ctx.tolist(), bps=bps, fused=bool(rng.random() < 0.5),
+                graph=bool(rng.random() < 0.5))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_shapes_against_oracle(kvc, i):
+    c = _random_case(i)
+    wl = workloads.small_decode(5000 + i, B=c["B"], Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"], ctx=c["ctx"])
+    check_workload(kvc, wl, torch.float32, bps=c["bps"], fused=c["fused"], graph=c["graph"], overlap=c["graph"])
+
+
 def test_results_invariant_to_physical_placement(kvc):
     """Same logical data under two block permutations gives bit-identical outputs."""
     from paged_kv_cache_27_gb300.harness import DecodeSession
