@@ -145,6 +145,34 @@ def test_decode_fp8_matches_oracle(case, out_dtype):
     check_attention(out, oracle_fp8(wl.q[:, 0], rec, wl), f"fp8 decode case {case}")
 
 
+@pytest.mark.parametrize("i", range(8))
+def test_decode_fp8_random_shapes(i):
+    """Seeded random shapes on the fp8 cache: batch up to 180 (several waves), GQA groups up to 16, both head dims,
+    ragged contexts with single tokens, the planner's split or an explicit one."""
+    import paged_kv_cache_27_gb300 as kvc
+    rng = np.random.default_rng(900 + i)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([1, 4, 7, 16] if D == 64 else [1, 4, 8]))
+    B = int(rng.choice([2, 31, 180]))
+    ctx = rng.integers(1, int(rng.choice([50, 900, 2500])) + 1, size=B)
+    ctx[rng.random(B) < 0.1] = 1
+    bps = int(rng.choice([0, 0, 5]))
+    wl = workloads.multi_token_decode(300 + i, ctx.tolist(), 1, Hq=G * Hkv, Hkv=Hkv, D=D)
+    rec, _ = quantized_cache(wl)
+    dev = "cuda"
+    q = torch.from_numpy(np.ascontiguousarray(wl.q[:, 0])).to(dev)
+    table, ctx_d = torch.from_numpy(wl.block_table).to(dev), torch.from_numpy(wl.ctx).to(dev)
+    max_ctx = int(wl.ctx.max())
+    _, _, ws = kvc.paged_decode_plan(B, G * Hkv, Hkv, D, max_ctx, bps)
+    out = torch.empty((B, G * Hkv, D), dtype=torch.float32, device=dev)
+    kvc.paged_decode_attention_fp8(q, rec, table, ctx_d, wl.scale, out,
+                                   torch.full((max(ws, 16),), 0x7F, dtype=torch.uint8, device=dev), max_ctx, bps)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error_flags(clear=True) == 0
+    check_attention(out, oracle_fp8(wl.q[:, 0], rec, wl), f"fp8 random case {i}")
+
+
 def test_decode_fp8_model_step_shape():
     """One layer of the 24-layer benchmark shape (32 x 2048, 14 / 2 heads) on an fp8 cache."""
     import paged_kv_cache_27_gb300 as kvc
