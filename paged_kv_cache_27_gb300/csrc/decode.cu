@@ -740,10 +740,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, kFp8>::kThreads, KVC_DEC_MIN_CTAS
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const CombineParams p) {
     constexpr int NT = 256, Q = D / 4, NPG = NT / Q;  // float4 columns of a row; part subsets
-    __shared__ float s_red[NT / 32];
     __shared__ float4 s_o[NPG][Q];
     const int h = blockIdx.x, y = blockIdx.y, b = y / p.q_len;  // y: the query row (a sequence's token)
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     // With early_release the next kernel (the next layer's decode) may launch and fetch its tables and first K/V
     // tiles while this one waits; its own dependency wait still covers this grid, whose completion covers the
     // decode before it.  The host asks for it only where a decode grid of this shape takes at most half the
@@ -777,6 +776,51 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
     auto part_row = [&](int s) -> int64_t { return row0 + (s < npre ? s : p.part_base + s - npre); };
     auto ml_of = [&](int s) { return *reinterpret_cast<const float2*>(p.part_ml + part_row(s) * 2); };
 
+#if KVC_COMBINE_ONE_PASS
+    // One pass over the parts: thread (pg, q) keeps a running maximum, sum and float4 column q of the
+    // accumulator over parts pg, pg + NPG, ... (online rescaling, so every load can be in flight at once); the
+    // NPG part subsets are then merged in shared memory by the threads of the first subset.
+    __shared__ float s_mg[NPG], s_lg[NPG];
+    const int q = tid % Q, pg = tid / Q;
+    float mt = -INFINITY, lt = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = pg; s < n; s += NPG) {
+        const int64_t r = part_row(s);
+        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
+        const float4 a = *reinterpret_cast<const float4*>(p.part_acc + r * D + 4 * q);
+        if (ml.y > 0.f) {  // a part that saw no token adds nothing
+            const float mn = fmaxf(mt, ml.x);
+            const float c_old = mt == -INFINITY ? 0.f : ex2(mt - mn), c_new = ex2(ml.x - mn);
+            O = fma4(c_new, a, scale4(O, c_old));
+            lt = lt * c_old + ml.y * c_new;
+            mt = mn;
+        }
+    }
+    s_o[pg][q] = O;
+    if (q == 0) {  // every thread of a subset saw the same parts: one (m, l) per subset
+        s_mg[pg] = mt;
+        s_lg[pg] = lt;
+    }
+    __syncthreads();
+    if (tid < Q) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NPG; ++k) M = fmaxf(M, s_mg[k]);
+        float L = 0.f;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NPG; ++k) {
+            const float w = s_mg[k] == -INFINITY ? 0.f : ex2(s_mg[k] - M);
+            L += s_lg[k] * w;
+            t = fma4(w, s_o[k][tid], t);
+        }
+        store_out4(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + 4 * tid,
+                   scale4(t, L > 0.f ? 1.f / L : 0.f));
+    }
+#else
+    // two passes: the maximum over every part first, then the weighted sums
+    __shared__ float s_red[NT / 32];
     // M: the largest maximum among the parts that saw a token
     float mx = -INFINITY;
     for (int s = tid; s < n; s += NT) {
@@ -785,7 +829,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_red[warp] = mx;
+    if ((tid & 31) == 0) s_red[tid >> 5] = mx;
     __syncthreads();
     float M = s_red[0];
 #pragma unroll
@@ -799,7 +843,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    if (lane == 0) s_red[warp] = ls;
+    if ((tid & 31) == 0) s_red[tid >> 5] = ls;
     // acc: thread (pg, q) sums float4 column q over parts pg, pg + NPG, ...
     const int q = tid % Q, pg = tid / Q;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -828,6 +872,7 @@ __global__ void __launch_bounds__(256) paged_decode_combine_kernel(const Combine
         store_out4(p.out, p.out_f32, (static_cast<int64_t>(y) * p.Hq + h) * D + 4 * tid,
                    scale4(t, L > 0.f ? 1.f / L : 0.f));
     }
+#endif
 }
 
 // ---------------------------------------------------------------------------

@@ -56,6 +56,13 @@ namespace kvc {
 #ifndef KVC_COMBINE_EARLY_TRIGGER  // the split combine kernel lets the next kernel launch as soon as it starts
 #define KVC_COMBINE_EARLY_TRIGGER 1
 #endif
+// 1: the split combine merges the parts in one pass with online rescaling (one round trip to the partials);
+// 0: the maximum over every part first, then the weighted sums (two).  Per layer of a 24-layer graph, two A/B
+// pairs: B = 1 x 16384 6.50 -> 6.16 us, B = 4 x 16384 10.1 -> 9.6, B = 1 x 131072 16.6 -> 16.4, B = 4 x 65536
+// 26.2 -> 25.7.
+#ifndef KVC_COMBINE_ONE_PASS
+#define KVC_COMBINE_ONE_PASS 1
+#endif
 #ifndef KVC_COMBINE_EARLY_ALWAYS  // 1: the combine releases the next launch at its start whatever the grid's size
 #define KVC_COMBINE_EARLY_ALWAYS 0
 #endif
