@@ -63,8 +63,8 @@ def decode_call_bytes(ctx_total: int, nblocks_total: int) -> int:
 # `bench.py --profile-only`, valid only for the decode sources it was taken on (sha256 of the files below).
 DECODE_SOURCES = ("paged_kv_cache_27_gb300/csrc/decode.cu", "paged_kv_cache_27_gb300/csrc/decode_common.cuh",
                   "paged_kv_cache_27_gb300/csrc/ptx.cuh", "paged_kv_cache_27_gb300/csrc/kvc_internal.h")
-NCU_DECODE_TRAFFIC = {"sources_sha256": "c62bfae3cd01adef3abce9ed6c989f5e4ae8094a27c64b48869ccbdcd99364b3",
-                      "bytes_per_launch": 33682048}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "e85d0f413793837192b265257551d14610c53f4d97d6bd88e0fd9f7395eef05d",
+                      "bytes_per_launch": 33681920}
 
 
 def decode_sources_sha256() -> str:
