@@ -863,20 +863,42 @@ def run_profile_configs(args):
                  2 if parts > 1 else 1, algorithmic_bytes=B * c * 512)
             del kp, vp, tb, ct, q, kn, vn, o, w
             torch.cuda.empty_cache()
-    # 5: the two small prefills (causal)
-    for name, seqlens, Hq, Hkv in (("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal",
-                                    (37, 120, 8, 200), 8, 8),
-                                   ("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2)):
-        T = sum(seqlens)
-        gen = torch.Generator(device=device).manual_seed(T * 31 + Hq)
-        qq = torch.randn((T, Hq, 64), generator=gen, device=device).half()
-        kk = torch.randn((T, Hkv, 64), generator=gen, device=device).half()
-        vv = torch.randn((T, Hkv, 64), generator=gen, device=device).half()
-        cu = torch.tensor(np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32), device=device)
-        oo = torch.empty((T, Hq, 64), dtype=torch.float16, device=device)
-        once(name, lambda: kvc.prefill_attention(qq, kk, vv, cu, max(seqlens), 0.125, True, oo), 1,
-             algorithmic_bytes=T * (Hq + 2 * Hkv) * 64 * 2,  # q, k and v read once (out written)
-             flops=4 * 64 * Hq * sum(s * (s + 1) // 2 for s in seqlens))
+    # 5: the two small prefills as their step runs: causal prefill, every token's K/V appended into a paged
+    # cache, the next token's K/V appended, one decode step over the cache
+    for name, wl5 in (("5: varlen prefill, seqlens 37/120/8/200, 8/8 heads, D=64, causal, then a decode step",
+                       workloads.varlen_prefill()),
+                      ("5: GQA prefill, B=2 x 256, 8/2 heads, D=64, causal, then a decode step",
+                       workloads.gqa_prefill())):
+        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        q5, k5, v5, cu5 = dv(wl5.q), dv(wl5.k), dv(wl5.v), dv(wl5.cu_seqlens)
+        T = q5.shape[0]
+        n5 = len(wl5.seqlens)
+        o5 = torch.empty((T, wl5.Hq, wl5.D), dtype=torch.float16, device=device)
+        cfg5 = kvc.KvcConfig(num_layers=1, num_blocks=wl5.NB, num_kv_heads=wl5.Hkv, head_dim=wl5.D,
+                             block_size=wl5.bs)
+        kp5 = torch.zeros(cfg5.pool_shape, dtype=torch.float16, device=device)
+        vp5 = torch.zeros_like(kp5)
+        h5 = kvc.kv_cache_create(cfg5, kp5, vp5)
+        seqlens = np.array(wl5.seqlens, np.int32)
+        slots_all = dv(kvc.kv_slot_mapping(wl5.block_table, np.zeros(n5, np.int32), seqlens, wl5.bs))
+        slots_new = dv(kvc.kv_slot_mapping(wl5.block_table, seqlens, np.ones(n5, np.int32), wl5.bs))
+        qd, kd, vd = dv(wl5.q_dec), dv(wl5.k_dec), dv(wl5.v_dec)
+        ctx5 = seqlens + 1
+        tb5, ct5 = dv(wl5.block_table), dv(ctx5)
+        od = torch.empty((n5, wl5.Hq, wl5.D), dtype=torch.float16, device=device)
+        _, _, ws5 = kvc.paged_decode_plan(n5, wl5.Hq, wl5.Hkv, wl5.D, int(ctx5.max()))
+        w5 = torch.zeros(max(ws5, 16), dtype=torch.uint8, device=device)
+
+        def step5():
+            kvc.prefill_attention(q5, k5, v5, cu5, max(wl5.seqlens), wl5.scale, True, o5)
+            kvc.kv_append(h5, 0, k5, v5, slots_all)
+            kvc.kv_append(h5, 0, kd, vd, slots_new)
+            kvc.paged_decode_attention(qd, kp5[0], vp5[0], tb5, ct5, wl5.scale, od, w5, int(ctx5.max()))
+        row = wl5.Hkv * wl5.D * 2 * 2  # K and V bytes of one token
+        once(name, step5, 2,  # the prefill and the decode kernel (the appends are not in the list's filter)
+             algorithmic_bytes=T * (wl5.Hq + 2 * wl5.Hkv) * wl5.D * 2 + (T + n5) * row + int(ctx5.sum()) * row,
+             flops=4 * wl5.D * wl5.Hq * sum(s_ * (s_ + 1) // 2 for s_ in wl5.seqlens))
+        kvc.kv_cache_destroy(h5)
 
 
 def run_suite(args):
