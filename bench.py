@@ -1154,6 +1154,8 @@ def run_suite_prefill(device, stream, flush, emit, tflops_peak, tflops_kind):
     prefill_case("GQA prefill, B=2 x 256, 8/2 heads, D=64, causal", (256, 256), 8, 2, 64)
     prefill_case("supplementary (not a listed config): varlen x16, seqlens 592/1920/128/3200, 8/8, D=64, causal",
                  (592, 1920, 128, 3200), 8, 8, 64)
+    prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=64, causal",
+                 (4096,) * 4, 32, 8, 64)
     prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",
                  (4096,) * 4, 32, 8, 128)
     prefill_case("supplementary (not a listed config): 4 x 4096 tokens, 32/8 heads, D=128, causal",

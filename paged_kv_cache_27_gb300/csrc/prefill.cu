@@ -7,7 +7,8 @@
 // KV head h / (Hq / Hkv).  Per row: softmax(q K^T * scale) V, with the
 // running-max / exp-sum rule of the FlashAttention article over key tiles.
 //
-// Design (head dim 128; head dim 64 runs prefill_1t.cu): one CTA per (256 query rows of a segment, query
+// Design (head dim 128, and head dim 64 on batches of 65,536 (token, query head) pairs or more; smaller head
+// dim 64 batches run prefill_1t.cu): one CTA per (256 query rows of a segment, query
 // head) = two 128-row query tiles A and B that share every K/V tile; ten warps.  Warps 0-3 own tile A's rows
 // and warps 4-7 tile B's (thread = row = TMEM lane) and run the softmax; lane 0 of warp 8 issues every
 // tcgen05.mma, lane 0 of warp 9 every TMA copy.  Per 128-key tile j and query tile X:
@@ -609,9 +610,23 @@ static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Head dim 64: batches of at least this many (token, query head) pairs take this file's kernel (two query tiles
+// sharing each K/V tile); smaller ones the one-tile kernel (prefill_1t.cu), whose twice as many CTAs shorten the
+// critical path of a small or skewed batch.  Measured (causal unless noted, us per call, one-tile vs two-tile):
+// seqlens 37/120/8/200 x 8 heads (2,920 pairs) 12.1 vs 16.4; 592/1920/128/3200 x 8 (46,720) 49.2 vs 57.3,
+// non-causal 86.0 vs 87.6; 2 x 4096 x 8 (65,536) 81.9 vs 76.4; 4 x 4096 x 8 157.7 vs 141.9; 16 x 1024 x 16 135.4
+// vs 125.1; 4 x 4096 x 32 604.4 vs 536.5, non-causal 1018 vs 877.
+#ifndef KVC_PREFILL_D64_TWO_TILE_WORK
+#define KVC_PREFILL_D64_TWO_TILE_WORK 65536
+#endif
+
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (a.nseq <= 0 || a.total_tokens <= 0 || a.max_seqlen <= 0) return cudaSuccess;
-    if (a.D == 64) return launch_prefill_1t(a, stream);  // one query tile per CTA (prefill_1t.cu)
+    if (a.D == 64) {
+        if (static_cast<int64_t>(a.total_tokens) * a.Hq < KVC_PREFILL_D64_TWO_TILE_WORK)
+            return launch_prefill_1t(a, stream);  // one query tile per CTA (prefill_1t.cu)
+        return a.split_p ? launch_prefill_d<64, true>(a, stream) : launch_prefill_d<64, false>(a, stream);
+    }
     switch (a.D * 2 + (a.split_p ? 1 : 0)) {
         case 256: return launch_prefill_d<128, false>(a, stream);
         case 257: return launch_prefill_d<128, true>(a, stream);

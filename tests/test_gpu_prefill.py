@@ -50,6 +50,9 @@ def test_small_prefills(make, causal, out_dtype):
     ((333,), 14, 2, 64),
     ((255, 256, 257, 384, 129, 128, 1, 640), 4, 2, 64),  # around the 256-row blocks of two query tiles
     ((600, 250, 513, 64), 8, 2, 128),
+    # head dim 64 with at least 65,536 (token, query head) pairs: the two-query-tile kernel
+    ((255, 256, 257, 384, 129, 128, 1, 640), 32, 8, 64),
+    ((1500, 700), 32, 4, 64),
 ])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("precise", [False, True])
