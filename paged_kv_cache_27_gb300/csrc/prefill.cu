@@ -150,6 +150,14 @@ __device__ __forceinline__ int pf_key_tiles(int rx, int len, int causal) {
     return (kv_len + kPfKeys - 1) / kPfKeys;
 }
 
+// 1: the fp16 weights of a 64-key half go to TMEM in one 32-column store; 0: two 16-column stores.  Two A/B
+// pairs, 4 x 4096 tokens, 32 / 8 heads: head dim 128 causal 601.3 -> 598.5 us, non-causal 1005.7 -> 994.7, head
+// dim 64 causal 537.1 -> 534.7.  (Eight 8-column stores per half, interleaved with the weights: 1001 us; half of
+// the weights' 2^x on the FMA pipe by a cubic instead of the multi-function unit: 818 us.)
+#ifndef KVC_PREFILL_SOFTMAX_ST32
+#define KVC_PREFILL_SOFTMAX_ST32 1
+#endif
+
 template <int D, bool kSplitP>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                 const __grid_constant__ CUtensorMap tmK,
@@ -455,6 +463,39 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = ex2(fmaf(s[c], sl2, neg_m));
                 }
+#if KVC_PREFILL_SOFTMAX_ST32
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (kSplitP) {
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    uint32_t hv[16], lv[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const int c = qq * 32 + 2 * e2;
+                        hv[e2] = pack_half2(s[c], s[c + 1]);
+                        if constexpr (kSplitP) {
+                            const float2 f = unpack_half2(hv[e2]);
+                            lv[e2] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
+                            ls4[e2 & 3] += s[c] + s[c + 1];
+                        } else {
+                            ls4[e2 & 3] = add_f16x2_to_f32(hv[e2], ls4[e2 & 3]);
+                        }
+                    }
+                    tmem_st16(tS + hh * 64 + qq * 16, hv);
+                    if constexpr (kSplitP) tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
+                }
+                } else {
+                    // the half's 32 fp16 pairs in one store
+                    float hv[32];
+#pragma unroll
+                    for (int e2 = 0; e2 < 32; ++e2) {
+                        const uint32_t h2 = pack_half2(s[2 * e2], s[2 * e2 + 1]);
+                        hv[e2] = __uint_as_float(h2);
+                        ls4[e2 & 3] = add_f16x2_to_f32(h2, ls4[e2 & 3]);
+                    }
+                    tmem_st32(tS + hh * 64, hv);
+                }
+#else
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
@@ -474,6 +515,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     tmem_st16(tS + hh * 64 + qq * 16, hv);
                     if constexpr (kSplitP) tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
                 }
+#endif
                 lsum[hh] = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
             }
             l = l * alpha + (lsum[0] + lsum[1]);
