@@ -23,6 +23,10 @@ roofline    the decode call (append + decode + split merge, one kernel) alone:
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload
 
 --impl reference times the fp64 CPU oracle on the same workload instead.
+--suite prints one JSON line per further listed workload (--suite-part picks a
+part, --suite-multi-t one multi-token T); --profile-configs runs each listed
+configuration's call a few times, a short command for a per-configuration ncu
+launch list; --profile-only replays the headline step without printing.
 Multi-GPU (torchrun): every rank runs its own replica (weak scaling), no
 collective on the data path; the timing barrier and max-over-ranks use
 torch.distributed.
