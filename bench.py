@@ -1186,7 +1186,7 @@ def main():
                     help="decode: every decode configuration (multi-token and cascade included); multi / cascade: "
                          "those lines only")
     ap.add_argument("--profile-configs", action="store_true",
-                    help="each listed configuration's call once after a warm-up (a short command for ncu)")
+                    help="each listed configuration's call four times (a warm-up, three with L2 flushed): a short command for ncu")
     ap.add_argument("--suite-multi-t", type=int, default=0,
                     help="with --suite-part multi: only this number of new tokens per sequence (1..8)")
     args = ap.parse_args()
