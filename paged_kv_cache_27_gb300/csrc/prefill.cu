@@ -467,23 +467,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
                 if constexpr (kSplitP) {
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    uint32_t hv[16], lv[16];
+                    for (int qq = 0; qq < 2; ++qq) {
+                        uint32_t hv[16], lv[16];
 #pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) {
-                        const int c = qq * 32 + 2 * e2;
-                        hv[e2] = pack_half2(s[c], s[c + 1]);
-                        if constexpr (kSplitP) {
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const int c = qq * 32 + 2 * e2;
+                            hv[e2] = pack_half2(s[c], s[c + 1]);
                             const float2 f = unpack_half2(hv[e2]);
                             lv[e2] = pack_half2(s[c] - f.x, s[c + 1] - f.y);
                             ls4[e2 & 3] += s[c] + s[c + 1];
-                        } else {
-                            ls4[e2 & 3] = add_f16x2_to_f32(hv[e2], ls4[e2 & 3]);
                         }
+                        tmem_st16(tS + hh * 64 + qq * 16, hv);
+                        tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
                     }
-                    tmem_st16(tS + hh * 64 + qq * 16, hv);
-                    if constexpr (kSplitP) tmem_st16(tS + hh * 64 + 32 + qq * 16, lv);
-                }
                 } else {
                     // the half's 32 fp16 pairs in one store
                     float hv[32];
