@@ -106,6 +106,28 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
     return r;
 }
 
+// packed fp32 pairs: a x b + c lane by lane, each lane rounded as fmaf
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// 1: the softmax's scale-and-shift of unmasked scores in packed fp32x2 multiply-adds (half the instructions,
+// the same rounding per lane); 0: one fmaf per score.  The softmax is bound by its instruction stream: two A/B
+// pairs, 4 x 4096 tokens, 32 / 8 heads: head dim 128 causal 596.1 -> 583.8 us, non-causal 994 -> 968, head dim
+// 64 causal 534 -> 522.
+#ifndef KVC_PREFILL_FMA2
+#define KVC_PREFILL_FMA2 1
+#endif
+
 // acc + the two fp16 halves of h (each converted exactly), as two rounded fp32 additions
 __device__ __forceinline__ float add_f16x2_to_f32(uint32_t h, float acc) {
     asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %0;\n\t"
@@ -460,8 +482,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                         s[c] = valid ? ex2(fmaf(s[c], sl2, neg_m)) : 0.f;
                     }
                 } else {
+#if KVC_PREFILL_FMA2
+                    // two scores per packed fp32x2 multiply-add (each lane rounds as fmaf does), then 2^x each
+                    const uint64_t sc2 = pack_f32x2(sl2, sl2), nm2 = pack_f32x2(neg_m, neg_m);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        float x0, x1;
+                        unpack_f32x2(fma_f32x2(pack_f32x2(s[c], s[c + 1]), sc2, nm2), x0, x1);
+                        s[c] = ex2(x0);
+                        s[c + 1] = ex2(x1);
+                    }
+#else
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = ex2(fmaf(s[c], sl2, neg_m));
+#endif
                 }
 #if KVC_PREFILL_SOFTMAX_ST32
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
