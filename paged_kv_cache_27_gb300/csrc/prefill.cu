@@ -106,20 +106,6 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
     return r;
 }
 
-// packed fp32 pairs: a x b + c lane by lane, each lane rounded as fmaf
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
 // 1: the softmax's scale-and-shift of unmasked scores in packed fp32x2 multiply-adds (half the instructions,
 // the same rounding per lane); 0: one fmaf per score.  The softmax is bound by its instruction stream: two A/B
 // pairs, 4 x 4096 tokens, 32 / 8 heads: head dim 128 causal 596.1 -> 583.8 us, non-causal 994 -> 968, head dim

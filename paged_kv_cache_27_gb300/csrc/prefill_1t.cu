@@ -30,6 +30,13 @@
 namespace kvc {
 namespace pf1 {
 
+// 1: the softmax's scale-and-shift of unmasked scores in packed fp32x2 multiply-adds (the same rounding per
+// lane); 0: one fmaf per score.  Two A/B pairs: seqlens 592/1920/128/3200 x 8 heads causal 49.1 -> 47.2 us,
+// non-causal 86.0 -> 83.2; B = 2 x 256, 8 / 2 heads 12.0 -> 11.5.
+#ifndef KVC_PREFILL_1T_FMA2
+#define KVC_PREFILL_1T_FMA2 1
+#endif
+
 
 constexpr int kPfRows = 128;   // query rows per CTA: the MMA's M, one TMEM lane each
 constexpr int kPfCtaRows = kPfRows;
@@ -418,8 +425,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     s[c] = valid ? ex2(fmaf(s[c], sl2, neg_m)) : 0.f;
                 }
             } else {
+#if KVC_PREFILL_1T_FMA2
+                // two scores per packed fp32x2 multiply-add (each lane rounds as fmaf does), then 2^x each
+                const uint64_t sc2 = pack_f32x2(sl2, sl2), nm2 = pack_f32x2(neg_m, neg_m);
+#pragma unroll
+                for (int c = 0; c < kPfPartKeys; c += 2) {
+                    float x0, x1;
+                    unpack_f32x2(fma_f32x2(pack_f32x2(s[c], s[c + 1]), sc2, nm2), x0, x1);
+                    s[c] = ex2(x0);
+                    s[c + 1] = ex2(x1);
+                }
+#else
 #pragma unroll
                 for (int c = 0; c < kPfPartKeys; ++c) s[c] = ex2(fmaf(s[c], sl2, neg_m));
+#endif
             }
             float ls4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t hv[16], lv[16];
