@@ -5,6 +5,8 @@
 #pragma once
 #include "ptx.cuh"
 
+#include "f32x2.cuh"
+
 namespace kvc {
 
 // ---- 5th-generation tensor cores (tcgen05) and tensor memory -----------------
@@ -159,21 +161,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
-// packed fp32 pairs (the sm_100 family's fp32x2 arithmetic): a x b + c lane by lane, each lane rounded as fmaf
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // 32 lanes x 16 consecutive 32-bit columns (no wait: tmem_wait_st orders the stores)
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
